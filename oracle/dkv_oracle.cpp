@@ -1,0 +1,361 @@
+// dkv_oracle.cpp -- the slow, plain CPU oracle for single-token decode attention
+// over a paged KV cache.
+//
+// TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or call
+// this file: only the test suite, the smoke check and the benchmark's CPU
+// baseline leg use it.  It shares no source, header, table or helper with the
+// CUDA library; it is written from the pages' definitions alone:
+//
+//   [TS]  "TinyServe: Query-Aware Cache Selection for Efficient LLM Serving"
+//         - 结构化内存布局 (pages of S tokens, P = ceil(t/S))
+//         - 相关性函数实例化 (page metadata phi = (m_j, M_j), bound score r)
+//         - 问题公式化定义 (S_t = TopK_j r, |S_t| = K; SparseAttn over S_t)
+//         - 标准Transformer解码层的注意力计算 (Attn(q_t, K, V))
+//         - Algorithm 1 "Fused Query-Aware Sparse Attention Kernel", steps 1-4
+//   [HI]  "论文阅读：HeadInfer" - 核心 idea (A^(h) = Softmax(Q K^T / sqrt(d_k)) V,
+//         heads independent, head-by-head evaluation identical to all heads)
+//   [FG]  "FlexGen: High-Throughput Generative Inference of Large Language
+//         Models with a Single GPU" (解读) - 4-bit 近似方法 (groups of 64,
+//         per-group min/max, 4-bit integers, dequantised to FP16; KV grouped
+//         along the hidden dimension)
+//
+// Arithmetic: every accumulation is in double.  The 4-bit format is a storage
+// format, not an accumulation, so it is defined by the exact IEEE fp32/fp16
+// operations listed at oracle_quant4 / oracle_dequant4; this file must be
+// compiled with -ffp-contract=off so that no multiply-add is fused behind our
+// back.  Readings of points the pages leave open are stated where they apply.
+//
+// Layouts (row-major, innermost last):
+//   q      [B, Hq, d]            16-bit float bits (bf16 or fp16)
+//   K, V   [B, Hkv, N, d]        16-bit float bits
+//   meta   [B, Hkv, P, d]        16-bit float bits, P = ceil(N / S)
+//   codes  [rows, d/2]           u8, channel 2i in the low nibble of byte i
+//   gmin, gmax [rows, d/64]      fp16 bits
+//   scores [B, Hq, P]            double
+//   sel    [B, Hq, kk]           int32, kk = min(K, P), ascending page indices
+//   out    [B, Hq, d]            double
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <functional>
+#include <numeric>
+#include <thread>
+#include <vector>
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// 16-bit float formats, decoded from their IEEE / bfloat16 definitions.
+// ---------------------------------------------------------------------------
+
+// bfloat16: the upper 16 bits of an IEEE binary32.
+double bf16_value(uint16_t h) {
+  uint32_t w = static_cast<uint32_t>(h) << 16;
+  float f;
+  std::memcpy(&f, &w, sizeof f);
+  return static_cast<double>(f);
+}
+
+// IEEE binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
+double fp16_value(uint16_t h) {
+  const int sign = (h >> 15) & 1;
+  const int e = (h >> 10) & 0x1f;
+  const int f = h & 0x3ff;
+  double v;
+  if (e == 0) {
+    v = std::ldexp(static_cast<double>(f), -24);  // zero or subnormal
+  } else if (e == 31) {
+    v = f ? std::nan("") : INFINITY;
+  } else {
+    v = std::ldexp(static_cast<double>(1024 + f), e - 25);
+  }
+  return sign ? -v : v;
+}
+
+double value16(uint16_t h, int is_fp16) { return is_fp16 ? fp16_value(h) : bf16_value(h); }
+
+// Round a double to the nearest IEEE binary16, ties to even, overflow to inf.
+// The input is taken as an exact real number: this is the single rounding the
+// 4-bit format's dequantisation performs.
+uint16_t fp16_round(double x) {
+  if (std::isnan(x)) return 0x7e00;
+  const uint16_t sign = std::signbit(x) ? 0x8000 : 0;
+  const double a = std::fabs(x);
+  if (a == 0.0) return sign;
+  // Quantum of the binade containing a (subnormals share the 2^-24 quantum).
+  int e2;
+  std::frexp(a, &e2);           // a = m * 2^e2, m in [0.5, 1)
+  int exp_unbiased = e2 - 1;    // a in [2^exp, 2^(exp+1))
+  if (exp_unbiased < -14) exp_unbiased = -14;
+  const double quantum = std::ldexp(1.0, exp_unbiased - 10);
+  const double n = std::nearbyint(a / quantum);  // FE_TONEAREST: ties to even
+  const double r = n * quantum;                  // exact
+  if (r >= 65536.0) return sign | 0x7c00;        // rounds past the largest finite
+  // Encode the exactly representable r.
+  if (r < std::ldexp(1.0, -14)) {
+    return sign | static_cast<uint16_t>(r / std::ldexp(1.0, -24));
+  }
+  int e3;
+  std::frexp(r, &e3);
+  const int ex = e3 - 1;  // r in [2^ex, 2^(ex+1))
+  const uint16_t frac = static_cast<uint16_t>(r / std::ldexp(1.0, ex - 10) - 1024.0);
+  return sign | static_cast<uint16_t>((ex + 15) << 10) | frac;
+}
+
+// Total order on 16-bit float bit patterns: numeric order, with -0 below +0.
+// Min/max of stored values then always returns one of the stored bit patterns.
+// (NaN inputs are outside the supported domain.)
+bool less16(uint16_t a, uint16_t b, int is_fp16) {
+  const double va = value16(a, is_fp16), vb = value16(b, is_fp16);
+  if (va != vb) return va < vb;
+  return (a & 0x8000) && !(b & 0x8000);
+}
+
+// Run f(unit) for unit in [0, n) on `threads` std::threads (0 = all cores).
+int g_threads = 0;
+void parallel_for(int64_t n, const std::function<void(int64_t)>& f) {
+  int t = g_threads > 0 ? g_threads : static_cast<int>(std::thread::hardware_concurrency());
+  if (t < 1) t = 1;
+  if (n < t) t = static_cast<int>(std::max<int64_t>(n, 1));
+  if (t == 1) {
+    for (int64_t i = 0; i < n; ++i) f(i);
+    return;
+  }
+  std::atomic<int64_t> next{0};
+  std::vector<std::thread> pool;
+  for (int i = 0; i < t; ++i) {
+    pool.emplace_back([&] {
+      for (int64_t u = next.fetch_add(1); u < n; u = next.fetch_add(1)) f(u);
+    });
+  }
+  for (auto& th : pool) th.join();
+}
+
+}  // namespace
+
+extern "C" {
+
+// Threads used by every oracle routine (0 = std::thread::hardware_concurrency).
+void oracle_set_threads(int n) { g_threads = n; }
+int oracle_get_threads(void) {
+  return g_threads > 0 ? g_threads : static_cast<int>(std::thread::hardware_concurrency());
+}
+
+// Format helpers, exposed so the tests can pin them against independent
+// library conversions.
+double oracle_value16(uint16_t h, int is_fp16) { return value16(h, is_fp16); }
+uint16_t oracle_fp16_round(double x) { return fp16_round(x); }
+
+// ---------------------------------------------------------------------------
+// Page metadata  [TS 结构化内存布局, 相关性函数实例化]
+// The keys of one (batch, kv-head) are split into P = ceil(N/S) pages of S
+// consecutive tokens (the last page may be ragged).  phi(K_j) = (m_j, M_j):
+// the channel-wise minimum and maximum over the page's tokens.
+// ---------------------------------------------------------------------------
+void oracle_meta(int B, int Hkv, int N, int d, int S, int is_fp16, const uint16_t* K,
+                 uint16_t* meta_min, uint16_t* meta_max) {
+  const int P = (N + S - 1) / S;
+  parallel_for(static_cast<int64_t>(B) * Hkv, [&](int64_t bh) {
+    const uint16_t* Kbh = K + bh * static_cast<int64_t>(N) * d;
+    uint16_t* mn = meta_min + bh * static_cast<int64_t>(P) * d;
+    uint16_t* mx = meta_max + bh * static_cast<int64_t>(P) * d;
+    for (int j = 0; j < P; ++j) {
+      const int t0 = j * S, t1 = std::min(N, (j + 1) * S);
+      for (int i = 0; i < d; ++i) {
+        uint16_t lo = Kbh[static_cast<int64_t>(t0) * d + i], hi = lo;
+        for (int t = t0 + 1; t < t1; ++t) {
+          const uint16_t k = Kbh[static_cast<int64_t>(t) * d + i];
+          if (less16(k, lo, is_fp16)) lo = k;
+          if (less16(hi, k, is_fp16)) hi = k;
+        }
+        mn[static_cast<int64_t>(j) * d + i] = lo;
+        mx[static_cast<int64_t>(j) * d + i] = hi;
+      }
+    }
+  });
+}
+
+// ---------------------------------------------------------------------------
+// Bound score  [TS 相关性函数实例化; Algorithm 1 step 1]
+//   r(q, phi_j) = sum_i ( q_i >= 0 ? q_i * M_{j,i} : q_i * m_{j,i} )
+// for every (batch, q-head, page); q-head h reads kv-head h / (Hq/Hkv).
+// ---------------------------------------------------------------------------
+void oracle_scores(int B, int Hq, int Hkv, int P, int d, int is_fp16, const uint16_t* q,
+                   const uint16_t* meta_min, const uint16_t* meta_max, double* scores) {
+  const int G = Hq / Hkv;
+  parallel_for(static_cast<int64_t>(B) * Hq, [&](int64_t bh) {
+    const int64_t b = bh / Hq, h = bh % Hq, kvh = h / G;
+    const uint16_t* qv = q + bh * d;
+    const uint16_t* mn = meta_min + (b * Hkv + kvh) * static_cast<int64_t>(P) * d;
+    const uint16_t* mx = meta_max + (b * Hkv + kvh) * static_cast<int64_t>(P) * d;
+    for (int j = 0; j < P; ++j) {
+      double s = 0.0;
+      for (int i = 0; i < d; ++i) {
+        const double qi = value16(qv[i], is_fp16);
+        if (qi >= 0.0) {
+          s += qi * value16(mx[static_cast<int64_t>(j) * d + i], is_fp16);
+        } else {
+          s += qi * value16(mn[static_cast<int64_t>(j) * d + i], is_fp16);
+        }
+      }
+      scores[bh * P + j] = s;
+    }
+  });
+}
+
+// ---------------------------------------------------------------------------
+// Top-K page selection  [TS 问题公式化定义; Algorithm 1 step 2]
+// S_t = the K pages with the largest score (K clamped to P).  Ties, which the
+// pages leave open, go to the lower page index.  The result is returned in
+// ascending page order.
+// ---------------------------------------------------------------------------
+void oracle_topk(int BH, int P, int K, const double* scores, int32_t* sel) {
+  const int kk = std::min(K, P);
+  parallel_for(BH, [&](int64_t bh) {
+    const double* r = scores + bh * P;
+    std::vector<int32_t> idx(P);
+    std::iota(idx.begin(), idx.end(), 0);
+    std::stable_sort(idx.begin(), idx.end(), [&](int32_t a, int32_t b) {
+      if (r[a] != r[b]) return r[a] > r[b];
+      return a < b;
+    });
+    idx.resize(kk);
+    std::sort(idx.begin(), idx.end());
+    std::copy(idx.begin(), idx.end(), sel + bh * kk);
+  });
+}
+
+// ---------------------------------------------------------------------------
+// Decode attention  [HI 核心 idea; TS 标准Transformer解码层的注意力计算,
+//                    问题公式化定义 (SparseAttn), Algorithm 1 steps 3-4]
+// For q-head h of batch b (kv-head h / G):
+//   tokens T = all N context tokens (sel == NULL), or the tokens of the pages
+//              in sel[b, h, :] taken in the order given (ascending pages);
+//   s_t = scale * q . k_t;  w_t = exp(s_t - max_t s_t);
+//   out = sum_t w_t v_t / sum_t w_t.
+// The softmax normalises over T only.  The cache holds every context token
+// (the current token's K/V already appended), and all of them are attended.
+// ---------------------------------------------------------------------------
+void oracle_attention(int B, int Hq, int Hkv, int N, int d, int S, int is_fp16,
+                      const uint16_t* q, const uint16_t* K, const uint16_t* V, double scale,
+                      const int32_t* sel, int nsel, double* out) {
+  const int G = Hq / Hkv;
+  parallel_for(static_cast<int64_t>(B) * Hq, [&](int64_t bh) {
+    const int64_t b = bh / Hq, h = bh % Hq, kvh = h / G;
+    const uint16_t* qv = q + bh * d;
+    const uint16_t* Kbh = K + (b * Hkv + kvh) * static_cast<int64_t>(N) * d;
+    const uint16_t* Vbh = V + (b * Hkv + kvh) * static_cast<int64_t>(N) * d;
+    std::vector<int32_t> tokens;
+    if (sel == nullptr) {
+      tokens.resize(N);
+      std::iota(tokens.begin(), tokens.end(), 0);
+    } else {
+      for (int u = 0; u < nsel; ++u) {
+        const int j = sel[bh * nsel + u];
+        for (int t = j * S; t < std::min(N, (j + 1) * S); ++t) tokens.push_back(t);
+      }
+    }
+    std::vector<double> qd(d), s(tokens.size());
+    for (int i = 0; i < d; ++i) qd[i] = value16(qv[i], is_fp16);
+    double smax = -INFINITY;
+    for (size_t u = 0; u < tokens.size(); ++u) {
+      const uint16_t* k = Kbh + static_cast<int64_t>(tokens[u]) * d;
+      double dot = 0.0;
+      for (int i = 0; i < d; ++i) dot += qd[i] * value16(k[i], is_fp16);
+      s[u] = scale * dot;
+      smax = std::max(smax, s[u]);
+    }
+    std::vector<double> acc(d, 0.0);
+    double denom = 0.0;
+    for (size_t u = 0; u < tokens.size(); ++u) {
+      const double w = std::exp(s[u] - smax);
+      denom += w;
+      const uint16_t* v = Vbh + static_cast<int64_t>(tokens[u]) * d;
+      for (int i = 0; i < d; ++i) acc[i] += w * value16(v[i], is_fp16);
+    }
+    for (int i = 0; i < d; ++i) out[bh * d + i] = acc[i] / denom;
+  });
+}
+
+// ---------------------------------------------------------------------------
+// 4-bit KV format  [FG 4-bit 近似方法]
+// The page fixes: groups of 64 elements along the hidden dimension of each
+// (token, head) row, per-group min and max, 4-bit integer codes, values
+// dequantised back to FP16 before use.  It leaves the rounding open; the
+// reading adopted here, and shared by the GPU kernels through the format, is:
+//   mn, mx   = min / max of the group's fp16 values (total order, -0 < +0)
+//   step     = fp16_rn( fp32( fp32(mx - mn) / 15 ) )          (15 steps, 16 levels)
+//   code_i   = 0 if step == 0, else
+//              clamp( rint_even( fp32( fp32(x_i - mn) / step ) ), 0, 15 )
+//   x^_i     = fp16_rn( code_i * step + mn )     (exact, rounded once to fp16)
+// fp32(.) is one IEEE binary32 round-to-nearest-even operation.  Codes are
+// packed two per byte, channel 2i in the low nibble.
+// ---------------------------------------------------------------------------
+namespace {
+float group_step(uint16_t mn, uint16_t mx) {
+  const float fmn = static_cast<float>(fp16_value(mn));
+  const float fmx = static_cast<float>(fp16_value(mx));
+  const float range = fmx - fmn;       // one fp32 rounding
+  const float third = range / 15.0f;   // one fp32 rounding
+  return static_cast<float>(fp16_value(fp16_round(static_cast<double>(third))));
+}
+}  // namespace
+
+void oracle_quant4(int64_t rows, int d, const uint16_t* x, uint8_t* codes, uint16_t* gmin,
+                   uint16_t* gmax) {
+  const int ng = d / 64;
+  parallel_for(rows, [&](int64_t r) {
+    const uint16_t* xr = x + r * d;
+    uint8_t* cr = codes + r * (d / 2);
+    for (int g = 0; g < ng; ++g) {
+      uint16_t lo = xr[g * 64], hi = lo;
+      for (int i = 1; i < 64; ++i) {
+        const uint16_t v = xr[g * 64 + i];
+        if (less16(v, lo, 1)) lo = v;
+        if (less16(hi, v, 1)) hi = v;
+      }
+      gmin[r * ng + g] = lo;
+      gmax[r * ng + g] = hi;
+      const float step = group_step(lo, hi);
+      const float fmn = static_cast<float>(fp16_value(lo));
+      for (int i = 0; i < 64; i += 2) {
+        int c[2] = {0, 0};
+        for (int e = 0; e < 2; ++e) {
+          if (step != 0.0f) {
+            const float xv = static_cast<float>(fp16_value(xr[g * 64 + i + e]));
+            const float diff = xv - fmn;   // one fp32 rounding
+            const float u = diff / step;   // one fp32 rounding
+            float rc = std::nearbyint(u);  // ties to even
+            rc = std::min(15.0f, std::max(0.0f, rc));
+            c[e] = static_cast<int>(rc);
+          }
+        }
+        cr[(g * 64 + i) / 2] = static_cast<uint8_t>(c[0] | (c[1] << 4));
+      }
+    }
+  });
+}
+
+void oracle_dequant4(int64_t rows, int d, const uint8_t* codes, const uint16_t* gmin,
+                     const uint16_t* gmax, uint16_t* x) {
+  const int ng = d / 64;
+  parallel_for(rows, [&](int64_t r) {
+    for (int g = 0; g < ng; ++g) {
+      const uint16_t lo = gmin[r * ng + g], hi = gmax[r * ng + g];
+      const double step = static_cast<double>(group_step(lo, hi));
+      const double mn = fp16_value(lo);
+      for (int i = 0; i < 64; ++i) {
+        const int ch = g * 64 + i;
+        const uint8_t byte = codes[r * (d / 2) + ch / 2];
+        const int c = (ch & 1) ? (byte >> 4) : (byte & 0xf);
+        // c * step + mn is exact in double (fp16-scale operands); round once.
+        x[r * d + ch] = fp16_round(static_cast<double>(c) * step + mn);
+      }
+    }
+  });
+}
+
+}  // extern "C"

@@ -1,0 +1,77 @@
+"""Write the golden fixtures in this folder.  Calls only the oracle.
+
+The pages print no worked numeric example of the kernel, so these fixtures are
+regression pins of the oracle itself: small inputs (stored verbatim as bit
+patterns, drawn from numpy's PCG64 so they are platform independent) together
+with the oracle's outputs.  ``tests/test_golden.py`` recomputes them on
+whatever machine runs the suite (x86 here, Arm on the GPU host) and requires the
+same answers.  Regenerate only when the oracle's arithmetic changes for a
+reason named in the commit message:
+
+    python tests/golden/make_golden.py
+"""
+
+import json
+import math
+import os
+import sys
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, os.path.dirname(os.path.dirname(HERE)))
+
+import oracle  # noqa: E402
+
+
+def _bf16_bits(x):
+    """Round float64 -> bf16 (nearest even) and return the bit patterns."""
+    f = np.asarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    rounded = (f + 0x7FFF + ((f >> 16) & 1)) >> 16
+    return rounded.astype(np.uint16)
+
+
+def case_sparse_small():
+    rng = np.random.default_rng(2024)
+    B, Hq, Hkv, d, N, S, K = 1, 4, 2, 64, 83, 16, 3   # P = 6, last page ragged
+    q = _bf16_bits(rng.standard_normal((B, Hq, d)))
+    Kc = _bf16_bits(rng.standard_normal((B, Hkv, N, d)))
+    Vc = _bf16_bits(rng.standard_normal((B, Hkv, N, d)))
+    mn, mx = oracle.meta(Kc, S, 0)
+    r = oracle.scores(q, mn, mx, 0)
+    sel = oracle.topk(r, K)
+    scale = 1.0 / math.sqrt(d)
+    full = oracle.attention(q, Kc, Vc, S, scale, 0)
+    sparse = oracle.attention(q, Kc, Vc, S, scale, 0, sel=sel)
+    return {
+        "shape": dict(B=B, Hq=Hq, Hkv=Hkv, d=d, N=N, S=S, K=K, scale=scale, dtype="bf16"),
+        "q": q.ravel().tolist(), "K": Kc.ravel().tolist(), "V": Vc.ravel().tolist(),
+        "meta_min": mn.ravel().tolist(), "meta_max": mx.ravel().tolist(),
+        "scores": [float.hex(float(v)) for v in r.ravel()],
+        "selected": sel.ravel().tolist(),
+        "out_full": [float.hex(float(v)) for v in full.ravel()],
+        "out_sparse": [float.hex(float(v)) for v in sparse.ravel()],
+    }
+
+
+def case_quant4():
+    rng = np.random.default_rng(99)
+    x = rng.standard_normal((6, 128)) * np.array([[0.01], [1], [3], [100], [1e-5], [1]])
+    x[5] = 7.0
+    xb = np.asarray(x, np.float64).astype(np.float16).view(np.uint16)
+    codes, gmin, gmax = oracle.quant4(xb)
+    xh = oracle.dequant4(codes, gmin, gmax)
+    return {"x": xb.ravel().tolist(), "rows": 6, "d": 128,
+            "codes": codes.ravel().tolist(), "gmin": gmin.ravel().tolist(),
+            "gmax": gmax.ravel().tolist(), "xhat": xh.ravel().tolist()}
+
+
+def main():
+    for name, fn in [("sparse_small", case_sparse_small), ("quant4", case_quant4)]:
+        with open(os.path.join(HERE, f"{name}.json"), "w") as f:
+            json.dump(fn(), f, separators=(",", ":"))
+            f.write("\n")
+
+
+if __name__ == "__main__":
+    main()
