@@ -1,0 +1,479 @@
+#!/usr/bin/env python
+"""Benchmark: decode attention over a paged KV cache on GB300.
+
+One step = one pass of the whole decode path over one batch (Llama-3-8B GQA
+shape by default: B=16 sequences, 32 q / 8 kv heads, d=128, 32K context,
+16-token pages, 128 pages kept per q-head):
+    kv_meta_build   page min/max metadata        (reads K, writes meta)
+    decode_attn_full   exact attention            (reads q, K, V)
+    decode_attn_select bound scores, top-K, sparse attention over the pages
+The metric is queries/s (a query = one sequence's one-token decode over all
+heads of one layer) and the effective GB/s of algorithmic bytes.  Inputs are
+seeded synthetic tensors already resident in HBM; K+V (2 GiB) exceed L2, and
+the step orders the calls so the exact path's 2 GiB stream sits between the
+metadata build and the sparse read of that metadata.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl dkv|reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank decodes its own batch
+(weak scaling, no collective on the data path); the time is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from workloads import WORKLOADS, Workload, bits, by_name  # noqa: E402
+
+METRIC = "decode-attn queries/s and effective KV GB/s (% of GB300 8 TB/s HBM roofline)"
+DEFAULT_WORKLOAD = "llama3-8b-gqa-b16-n32k"
+NOMINAL_HBM_GBS = 8000.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["dkv", "reference"], default="dkv")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the 1M-token head-wise and e2e / CPU-baseline legs")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "decode_attention_paged_kv_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        e = t["kernels"][kernel_key]
+        if e.get("source_sha") != source_sha():
+            return None
+        return e["dram_bytes_per_launch_full_size"]
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+        except Exception:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except Exception:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        busy = [s for s in sm if smax and s > 0.3 * max(smax)] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def union_tokens(sel: torch.Tensor, w: Workload) -> int:
+    """Valid tokens of the unique pages gathered per (batch, kv head)."""
+    B, Hq, kk = sel.shape
+    mask = torch.zeros(B, w.Hkv, w.P, dtype=torch.bool, device=sel.device)
+    grp = sel.view(B, w.Hkv, w.G * kk).long()
+    mask.scatter_(2, grp, True)
+    toks = torch.full((w.P,), w.S, dtype=torch.int64, device=sel.device)
+    toks[-1] = w.N - (w.P - 1) * w.S
+    return int((mask.long() * toks).sum().item())
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_dkv(args, rank, world, local):
+    import decode_attention_paged_kv_gb300 as dkv
+    from decode_attention_paged_kv_gb300 import accounting as acc
+    from workloads import make_inputs
+
+    dkv.lib()  # fails loudly if the CUDA library is missing
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = by_name(args.workload)
+    widx = [x.name for x in WORKLOADS].index(w.name)
+    if w.q4:
+        raise SystemExit("the 4-bit workload is a parity case; the bench times the dense path")
+    q, K, V = make_inputs(w, seed=42 + widx + 1000 * rank, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    ws_full = torch.zeros(dkv.workspace_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, 0), dtype=torch.uint8,
+                          device=dev)
+    ws_sel = torch.zeros(dkv.workspace_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, w.top_k),
+                         dtype=torch.uint8, device=dev)
+    kk = min(w.top_k, w.P)
+    out_full = torch.empty(w.B, w.Hq, w.d, dtype=torch.float32, device=dev)
+    out_sel = torch.empty_like(out_full)
+    sel = torch.empty(w.B, w.Hq, kk, dtype=torch.int32, device=dev)
+    calls = ["kv_meta_build", "decode_attn_full", "decode_attn_select"]
+    ev = {c: [] for c in calls}
+
+    def step(record=False):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)] if record else None
+        if record:
+            e[0].record(stream)
+        meta = dkv.kv_meta_build(K)
+        if record:
+            e[1].record(stream)
+        dkv.decode_attn_full(q, K, V, out=out_full, workspace=ws_full)
+        if record:
+            e[2].record(stream)
+        dkv.decode_attn_select(q, K, V, meta, w.top_k, out=out_sel, selected=sel,
+                               workspace=ws_sel)
+        if record:
+            e[3].record(stream)
+            for i, c in enumerate(calls):
+                ev[c].append((e[i], e[i + 1]))
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    gathered = union_tokens(sel, w)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        t0.record(stream)
+        for _ in range(args.steps):
+            step(record=True)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms_total = t0.elapsed_time(t1)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    per_call = {c: statistics.mean(a.elapsed_time(b) for a, b in ev[c]) for c in calls}
+
+    status = max(dkv.read_device_status(ws_full), dkv.read_device_status(ws_sel))
+    if status != 0:
+        raise SystemExit(f"device status {status} during the timed region")
+
+    bytes_call = {
+        "kv_meta_build": acc.meta_bytes(w.B, w.Hkv, w.d, w.N, w.S),
+        "decode_attn_full": acc.full_bytes(w.B, w.Hq, w.Hkv, w.d, w.N),
+        "decode_attn_select": acc.select_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, gathered, w.S),
+    }
+    step_bytes = sum(bytes_call.values())
+    peak, peak_kind = peaks()
+    kernels = {}
+    for c in calls:
+        gbs = bytes_call[c] / (per_call[c] * 1e-3) / 1e9
+        kernels[c] = {"ms": round(per_call[c], 5), "alg_bytes": bytes_call[c],
+                      "GB/s": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak, 4),
+                      "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4)}
+    kernels["decode_attn_select"]["gathered_pages"] = gathered // w.S
+    kernels["decode_attn_full"]["queries_per_s"] = round(w.B / (per_call["decode_attn_full"] * 1e-3), 1)
+    kernels["decode_attn_select"]["queries_per_s"] = round(
+        w.B / (per_call["decode_attn_select"] * 1e-3), 1)
+    dom = max(calls, key=lambda c: per_call[c])
+    dom_gbs = bytes_call[dom] / (per_call[dom] * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(dom_gbs, 1),
+                "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                "frac": round(dom_gbs / peak, 4),
+                "frac_of_8tbs": round(dom_gbs / NOMINAL_HBM_GBS, 4),
+                "traffic": ncu_traffic(dom)}
+    value = world * w.B / (ms_step * 1e-3)
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": "queries/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded torch Philox on device; K pages 2% hot, aligned to the group query)",
+        "config": {"workload": w.name, "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv,
+                   "head_dim": w.d, "context": w.N, "page_size": w.S, "top_k_pages": w.top_k,
+                   "step": "kv_meta_build + decode_attn_full + decode_attn_select",
+                   "l2": "inputs larger than L2 (2 GiB K+V streamed every step)",
+                   "parallelism": f"replicas x{world} (each rank its own batch)"},
+        "effective_GB_per_s": round(step_bytes / (ms_step * 1e-3) / 1e9, 1),
+        "kernels": kernels, "roofline": roofline,
+        "gpu_launches": args.steps * (1 + 2 + 4),
+        "clocks": clk.summary(),
+    }
+    return res, (q, K, V, w, widx, dev, stream)
+
+
+def headwise_leg(dev, stream):
+    """1M-token context, 8 kv heads: exact attention all heads at once and one
+    kv head at a time (HeadInfer), bitwise-equal outputs."""
+    import decode_attention_paged_kv_gb300 as dkv
+    from decode_attention_paged_kv_gb300 import accounting as acc
+    from workloads import make_inputs
+
+    w = WORKLOADS[3]
+    q, K, V = make_inputs(w, seed=45, device=dev)
+    ws = torch.zeros(dkv.workspace_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, 0), dtype=torch.uint8,
+                     device=dev)
+    ws1 = torch.zeros(dkv.workspace_bytes(w.B, w.G, 1, w.d, w.N, 0), dtype=torch.uint8,
+                      device=dev)
+    out = torch.empty(w.B, w.Hq, w.d, device=dev)
+    out_hw = torch.empty_like(out)
+
+    def all_heads():
+        dkv.decode_attn_full(q, K, V, out=out, workspace=ws)
+
+    def head_wise():
+        for h in range(w.Hkv):
+            dkv.decode_attn_full(q[:, h * w.G:(h + 1) * w.G], K[:, h:h + 1], V[:, h:h + 1],
+                                 out=out_hw[:, h * w.G:(h + 1) * w.G], workspace=ws1)
+
+    res = {}
+    nbytes = acc.full_bytes(w.B, w.Hq, w.Hkv, w.d, w.N)
+    peak, _ = peaks()
+    for name, fn in [("all_heads", all_heads), ("head_wise_8_calls", head_wise)]:
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 5
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[name] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
+                     "frac_of_measured_hbm": round(gbs / peak, 4),
+                     "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4)}
+    res["bitwise_equal"] = bool(torch.equal(out, out_hw))
+    res["workload"] = w.name
+    del q, K, V
+    torch.cuda.empty_cache()
+    return res
+
+
+def e2e_leg(q, K, V, w, dev, stream, steps):
+    """The same step through the public API with host inputs: every step copies
+    q, K, V from pinned host memory and reads the outputs back."""
+    import decode_attention_paged_kv_gb300 as dkv
+
+    hq = q.cpu().pin_memory()
+    hK = K.cpu().pin_memory()
+    hV = V.cpu().pin_memory()
+    kk = min(w.top_k, w.P)
+    ho = torch.empty(w.B, w.Hq, w.d, dtype=torch.float32).pin_memory()
+    hs = torch.empty_like(ho).pin_memory()
+    hsel = torch.empty(w.B, w.Hq, kk, dtype=torch.int32).pin_memory()
+    dq, dK, dV = torch.empty_like(q), torch.empty_like(K), torch.empty_like(V)
+    ws_full = torch.zeros(dkv.workspace_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, 0), dtype=torch.uint8,
+                          device=dev)
+    ws_sel = torch.zeros(dkv.workspace_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, w.top_k),
+                         dtype=torch.uint8, device=dev)
+    of, osl = torch.empty(w.B, w.Hq, w.d, device=dev), torch.empty(w.B, w.Hq, w.d, device=dev)
+    sel = torch.empty(w.B, w.Hq, kk, dtype=torch.int32, device=dev)
+
+    def step():
+        dq.copy_(hq, non_blocking=True)
+        dK.copy_(hK, non_blocking=True)
+        dV.copy_(hV, non_blocking=True)
+        meta = dkv.kv_meta_build(dK)
+        dkv.decode_attn_full(dq, dK, dV, out=of, workspace=ws_full)
+        dkv.decode_attn_select(dq, dK, dV, meta, w.top_k, out=osl, selected=sel,
+                               workspace=ws_sel)
+        ho.copy_(of, non_blocking=True)
+        hs.copy_(osl, non_blocking=True)
+        hsel.copy_(sel, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    n = max(3, min(steps, 10))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    h2d = (hq.numel() * 2 + hK.numel() * 2 + hV.numel() * 2)
+    d2h = ho.numel() * 4 + hs.numel() * 4 + hsel.numel() * 4
+    return {"value": round(w.B / (ms * 1e-3), 1), "unit": "queries/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_sample_step(q, K, V, w, heads=None):
+    """The oracle's step (meta + exact + sparse) on sequence 0 (all kv heads, or
+    the first `heads` of them).  Returns (seconds, fraction of one query)."""
+    import oracle
+
+    hk = w.Hkv if heads is None else heads
+    qs = bits(q[:1, :hk * w.G].cpu())
+    Ks = bits(K[:1, :hk].cpu())
+    Vs = bits(V[:1, :hk].cpu())
+    is16 = int(w.dtype == "fp16")
+    scale = 1.0 / math.sqrt(w.d)
+    t = time.perf_counter()
+    mn, mx = oracle.meta(Ks, w.S, is16)
+    oracle.attention(qs, Ks, Vs, w.S, scale, is16)
+    r = oracle.scores(qs, mn, mx, is16)
+    sel = oracle.topk(r, w.top_k)
+    oracle.attention(qs, Ks, Vs, w.S, scale, is16, sel=sel)
+    return time.perf_counter() - t, hk / w.Hkv
+
+
+def cpu_baseline_leg(q, K, V, w):
+    import oracle
+    oracle.build()
+    secs, frac = oracle_sample_step(q, K, V, w)
+    return {"value": round(frac / secs, 4), "unit": "queries/s", "cores": oracle.threads(),
+            "kind": "oracle",
+            "sample": f"sequence 0 of {w.B} (all {w.Hkv} kv heads): meta + exact + sparse, "
+                      f"{secs:.2f} s"}
+
+
+def run_reference(args, rank, world, local):
+    """The oracle as the reference arm, on the same workload and metric."""
+    import oracle
+    from workloads import make_inputs
+
+    oracle.build()
+    w = by_name(args.workload)
+    widx = [x.name for x in WORKLOADS].index(w.name)
+    # one sequence of the workload, drawn on the CPU (the oracle's own inputs)
+    small = w.replace(B=1)
+    q, K, V = make_inputs(small, seed=42 + widx)
+    heads = 1  # one kv head (G query heads) per step keeps a step to seconds
+    for _ in range(max(1, min(args.warmup, 1))):
+        oracle_sample_step(q, K, V, small, heads)
+    tot, frac = 0.0, 0.0
+    for _ in range(args.steps):
+        s, f = oracle_sample_step(q, K, V, small, heads)
+        tot += s
+        frac += f
+    value = frac / tot
+    sample = (f"per step: kv head 0 of sequence 0 ({small.G} q heads, {w.N} tokens): "
+              "meta + exact + sparse")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "queries/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * tot / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name},
+            "cpu_baseline": {"value": round(value, 4), "unit": "queries/s",
+                             "cores": oracle.threads(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "queries/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_info()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, world, local)), flush=True)
+        return
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    res, (q, K, V, w, widx, dev, stream) = run_dkv(args, rank, world, local)
+    if not args.no_extra and rank == 0:
+        res["e2e"] = e2e_leg(q, K, V, w, dev, stream, args.steps)
+        res["cpu_baseline"] = cpu_baseline_leg(q, K, V, w)
+        del q, K, V
+        torch.cuda.empty_cache()
+        res["headwise_1m"] = headwise_leg(dev, stream)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

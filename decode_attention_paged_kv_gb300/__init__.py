@@ -1,0 +1,296 @@
+"""Python binding of libdkv: GB300 decode attention over a paged KV cache.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in ``include/dkv.h``.  PyTorch provides the
+device memory (outputs and workspace are allocated with torch) and the current
+stream.  There is no fallback: if ``libdkv.so`` has not been built, or a call
+returns an error status, the call raises.
+
+Public calls (same names as the C ABI, without the ``dkv_`` prefix):
+  kv_meta_build(K)                      -> (meta_min, meta_max)
+  decode_attn_full(q, K, V)             -> out
+  decode_attn_select(q, K, V, meta, k)  -> out (, selected)
+  kv_quant4(x) / kv_dequant4(q4)
+  workspace_bytes(...), read_device_status(workspace)
+K and V are dense tensors [B, Hkv, N, d] (bf16 / fp16; any batch / head
+strides, token stride d) or ``Q4Cache`` tuples in the 4-bit format.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import NamedTuple, Optional
+
+import torch
+
+from . import build as _build_mod
+
+__all__ = [
+    "Q4Cache", "DkvError", "lib", "kv_meta_build", "decode_attn_full", "decode_attn_select",
+    "kv_quant4", "kv_dequant4", "workspace_bytes", "read_device_status", "status_string",
+    "PAGE_SIZE",
+]
+
+PAGE_SIZE = 16
+
+# enums of include/dkv.h
+DKV_OK = 0
+DKV_ERR_DEVICE_TIMEOUT = 8
+DKV_BF16, DKV_FP16, DKV_FP32 = 0, 1, 2
+DKV_KV_DENSE, DKV_KV_Q4G64 = 0, 1
+DKV_FLAG_FORCE_TIMEOUT = 0x1
+
+
+class DkvError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: dkv status {status} ({status_string(status)})")
+
+
+class Q4Cache(NamedTuple):
+    """A K or V cache in the 4-bit group-of-64 format.
+
+    codes [B, Hkv, N, d/2] uint8 (channel 2i in the low nibble of byte i);
+    gmin, gmax [B, Hkv, N, d/64] fp16 (per-group min / max).
+    """
+    codes: torch.Tensor
+    gmin: torch.Tensor
+    gmax: torch.Tensor
+
+
+class _Params(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("seq_len", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("q_stride_b", ctypes.c_int64), ("q_stride_h", ctypes.c_int64),
+                ("o_stride_b", ctypes.c_int64), ("o_stride_h", ctypes.c_int64),
+                ("scale", ctypes.c_float), ("flags", ctypes.c_uint32)]
+
+
+class _KV(ctypes.Structure):
+    _fields_ = [("format", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("data", ctypes.c_void_p), ("gmin", ctypes.c_void_p), ("gmax", ctypes.c_void_p),
+                ("stride_b", ctypes.c_int64), ("stride_h", ctypes.c_int64),
+                ("gstride_b", ctypes.c_int64), ("gstride_h", ctypes.c_int64)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libdkv.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build_mod.LIB
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"libdkv.so not found at {path}; build it with "
+                    "`python -m decode_attention_paged_kv_gb300.build`")
+            L = ctypes.CDLL(path)
+            vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+            P, KVp = ctypes.POINTER(_Params), ctypes.POINTER(_KV)
+            L.dkv_workspace_bytes.argtypes = [P, i32]
+            L.dkv_workspace_bytes.restype = sz
+            L.dkv_kv_meta_build.argtypes = [P, KVp, vp, vp, vp]
+            L.dkv_decode_attn_full.argtypes = [P, vp, KVp, KVp, vp, i32, vp, sz, vp]
+            L.dkv_decode_attn_select.argtypes = [P, vp, KVp, KVp, vp, vp, i32, vp, i32, vp, vp,
+                                                 sz, vp]
+            L.dkv_kv_quant4.argtypes = [i64, i32, vp, vp, vp, vp, vp]
+            L.dkv_kv_dequant4.argtypes = [i64, i32, vp, vp, vp, vp, vp]
+            L.dkv_read_device_status.argtypes = [vp, vp]
+            L.dkv_status_string.argtypes = [i32]
+            L.dkv_status_string.restype = ctypes.c_char_p
+            for name in ("dkv_kv_meta_build", "dkv_decode_attn_full", "dkv_decode_attn_select",
+                         "dkv_kv_quant4", "dkv_kv_dequant4", "dkv_read_device_status"):
+                getattr(L, name).restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().dkv_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != DKV_OK:
+        raise DkvError(status, where)
+
+
+def _stream(t: torch.Tensor) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.bfloat16:
+        return DKV_BF16
+    if dt == torch.float16:
+        return DKV_FP16
+    if dt == torch.float32:
+        return DKV_FP32
+    raise TypeError(f"unsupported dtype {dt}")
+
+
+def _kv_struct(kv) -> tuple[_KV, int, int, int, int]:
+    """(struct, B, Hkv, N, d) for a dense tensor or a Q4Cache."""
+    s = _KV()
+    if isinstance(kv, Q4Cache):
+        c, gmn, gmx = kv
+        B, H, N, half = c.shape
+        d = half * 2
+        if c.dtype != torch.uint8 or gmn.dtype != torch.float16 or gmx.dtype != torch.float16:
+            raise TypeError("Q4Cache wants uint8 codes and fp16 gmin/gmax")
+        if c.stride(3) != 1 or c.stride(2) != half:
+            raise ValueError("codes must have token stride d/2 and channel stride 1")
+        if gmn.stride() != gmx.stride() or gmn.stride(3) != 1 or gmn.stride(2) != d // 64:
+            raise ValueError("gmin / gmax must share strides with token stride d/64")
+        s.format, s.dtype = DKV_KV_Q4G64, DKV_FP16
+        s.data, s.gmin, s.gmax = c.data_ptr(), gmn.data_ptr(), gmx.data_ptr()
+        s.stride_b, s.stride_h = c.stride(0), c.stride(1)
+        s.gstride_b, s.gstride_h = gmn.stride(0), gmn.stride(1)
+        return s, B, H, N, d
+    B, H, N, d = kv.shape
+    if kv.stride(3) != 1 or kv.stride(2) != d:
+        raise ValueError("K/V must have token stride d and channel stride 1")
+    s.format, s.dtype = DKV_KV_DENSE, _dtype_code(kv.dtype)
+    s.data = kv.data_ptr()
+    s.stride_b, s.stride_h = kv.stride(0), kv.stride(1)
+    return s, B, H, N, d
+
+
+def _device_of(kv) -> torch.device:
+    return kv.codes.device if isinstance(kv, Q4Cache) else kv.device
+
+
+def _params(q: Optional[torch.Tensor], B, Hkv, N, d, out: Optional[torch.Tensor],
+            scale: Optional[float], flags: int = 0) -> _Params:
+    p = _Params()
+    p.batch, p.num_kv_heads, p.head_dim, p.seq_len, p.page_size = B, Hkv, d, N, PAGE_SIZE
+    p.num_q_heads = q.shape[1] if q is not None else Hkv
+    if q is not None:
+        if q.shape[0] != B or q.shape[2] != d or q.stride(2) != 1:
+            raise ValueError(f"q shape {tuple(q.shape)} does not match the cache")
+        p.q_stride_b, p.q_stride_h = q.stride(0), q.stride(1)
+    if out is not None:
+        p.o_stride_b, p.o_stride_h = out.stride(0), out.stride(1)
+    p.scale = float(scale) if scale is not None else 1.0 / math.sqrt(d)
+    p.flags = flags
+    return p
+
+
+def workspace_bytes(B: int, Hq: int, Hkv: int, d: int, N: int, top_k: int = 0) -> int:
+    """Workspace bytes dkv_decode_attn_full (top_k = 0) or _select needs."""
+    p = _Params()
+    p.batch, p.num_q_heads, p.num_kv_heads, p.head_dim, p.seq_len = B, Hq, Hkv, d, N
+    p.page_size, p.scale = PAGE_SIZE, 1.0
+    n = lib().dkv_workspace_bytes(ctypes.byref(p), int(top_k))
+    if n == 0:
+        raise DkvError(2, "dkv_workspace_bytes")
+    return int(n)
+
+
+def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]) -> torch.Tensor:
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError("workspace too small")
+        return workspace
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device)
+
+
+def kv_meta_build(K, page_size: int = PAGE_SIZE):
+    """Page metadata (meta_min, meta_max), each [B, Hkv, P, d]."""
+    ks, B, H, N, d = _kv_struct(K)
+    dev = _device_of(K)
+    dt = torch.float16 if isinstance(K, Q4Cache) else K.dtype
+    P = (N + page_size - 1) // page_size
+    mn = torch.empty(B, H, P, d, dtype=dt, device=dev)
+    mx = torch.empty(B, H, P, d, dtype=dt, device=dev)
+    p = _params(None, B, H, N, d, None, None)
+    p.page_size = page_size
+    _check(lib().dkv_kv_meta_build(ctypes.byref(p), ctypes.byref(ks), mn.data_ptr(),
+                                   mx.data_ptr(), _stream(mn)), "dkv_kv_meta_build")
+    return mn, mx
+
+
+def decode_attn_full(q, K, V, scale: Optional[float] = None,
+                     out_dtype: torch.dtype = torch.float32,
+                     out: Optional[torch.Tensor] = None,
+                     workspace: Optional[torch.Tensor] = None, flags: int = 0):
+    """Exact decode attention; returns out [B, Hq, d]."""
+    ks, B, H, N, d = _kv_struct(K)
+    vs, B2, H2, N2, d2 = _kv_struct(V)
+    if (B, H, N, d) != (B2, H2, N2, d2):
+        raise ValueError("K and V shapes differ")
+    if out is None:
+        out = torch.empty(B, q.shape[1], d, dtype=out_dtype, device=q.device)
+    p = _params(q, B, H, N, d, out, scale, flags)
+    nbytes = lib().dkv_workspace_bytes(ctypes.byref(p), 0)
+    ws = _workspace(nbytes, q.device, workspace)
+    _check(lib().dkv_decode_attn_full(ctypes.byref(p), q.data_ptr(), ctypes.byref(ks),
+                                      ctypes.byref(vs), out.data_ptr(), _dtype_code(out.dtype),
+                                      ws.data_ptr(), nbytes, _stream(q)), "dkv_decode_attn_full")
+    return out
+
+
+def decode_attn_select(q, K, V, meta, top_k: int, scale: Optional[float] = None,
+                       out_dtype: torch.dtype = torch.float32,
+                       out: Optional[torch.Tensor] = None, return_selected: bool = False,
+                       selected: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None, flags: int = 0):
+    """Query-aware page-sparse decode attention over the top_k pages per q-head."""
+    ks, B, H, N, d = _kv_struct(K)
+    vs, B2, H2, N2, d2 = _kv_struct(V)
+    if (B, H, N, d) != (B2, H2, N2, d2):
+        raise ValueError("K and V shapes differ")
+    mn, mx = meta
+    P = (N + PAGE_SIZE - 1) // PAGE_SIZE
+    if tuple(mn.shape) != (B, H, P, d) or not mn.is_contiguous() or not mx.is_contiguous():
+        raise ValueError("meta must be contiguous [B, Hkv, P, d]")
+    if out is None:
+        out = torch.empty(B, q.shape[1], d, dtype=out_dtype, device=q.device)
+    kk = min(int(top_k), P)
+    if return_selected and selected is None:
+        selected = torch.empty(B, q.shape[1], kk, dtype=torch.int32, device=q.device)
+    p = _params(q, B, H, N, d, out, scale, flags)
+    nbytes = lib().dkv_workspace_bytes(ctypes.byref(p), int(top_k))
+    ws = _workspace(nbytes, q.device, workspace)
+    sel_ptr = selected.data_ptr() if selected is not None else None
+    _check(lib().dkv_decode_attn_select(ctypes.byref(p), q.data_ptr(), ctypes.byref(ks),
+                                        ctypes.byref(vs), mn.data_ptr(), mx.data_ptr(),
+                                        int(top_k), out.data_ptr(), _dtype_code(out.dtype),
+                                        sel_ptr, ws.data_ptr(), nbytes, _stream(q)),
+           "dkv_decode_attn_select")
+    return (out, selected) if return_selected else out
+
+
+def kv_quant4(x: torch.Tensor) -> Q4Cache:
+    """4-bit group-of-64 quantisation of an fp16 tensor [..., d] (contiguous)."""
+    if x.dtype != torch.float16 or not x.is_contiguous():
+        raise ValueError("kv_quant4 wants a contiguous fp16 tensor")
+    d = x.shape[-1]
+    rows = x.numel() // d
+    codes = torch.empty(*x.shape[:-1], d // 2, dtype=torch.uint8, device=x.device)
+    gmin = torch.empty(*x.shape[:-1], d // 64, dtype=torch.float16, device=x.device)
+    gmax = torch.empty_like(gmin)
+    _check(lib().dkv_kv_quant4(rows, d, x.data_ptr(), codes.data_ptr(), gmin.data_ptr(),
+                               gmax.data_ptr(), _stream(x)), "dkv_kv_quant4")
+    return Q4Cache(codes, gmin, gmax)
+
+
+def kv_dequant4(q4: Q4Cache) -> torch.Tensor:
+    codes, gmin, gmax = q4
+    d = codes.shape[-1] * 2
+    rows = codes.numel() // (d // 2)
+    x = torch.empty(*codes.shape[:-1], d, dtype=torch.float16, device=codes.device)
+    _check(lib().dkv_kv_dequant4(rows, d, codes.data_ptr(), gmin.data_ptr(), gmax.data_ptr(),
+                                 x.data_ptr(), _stream(x)), "dkv_kv_dequant4")
+    return x
+
+
+def read_device_status(workspace: torch.Tensor) -> int:
+    """Synchronise and return (then clear) the device status word of a workspace."""
+    return int(lib().dkv_read_device_status(workspace.data_ptr(), _stream(workspace)))

@@ -1,0 +1,397 @@
+// api.cu -- the extern "C" boundary of libdkv (declared in include/dkv.h):
+// argument validation, workspace layout, TMA tensor-map encoding and kernel
+// launches.  Every argument error is returned before anything is launched.
+
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/dkv.h"
+#include "dkv_kernels.h"
+
+namespace {
+
+using dkv::ceil_div;
+
+constexpr uint64_t kWaitLimitNs = 200000000ull;  // 200 ms per bounded device wait
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Byte offsets of the regions inside a caller-provided workspace.
+struct WsLayout {
+  size_t status = 0;     // u32 device status word (first 256 bytes)
+  size_t part_ml = 0;    // [B, Hq, n_chunks, 2] fp32
+  size_t part_o = 0;     // [B, Hq, n_chunks, d] fp32
+  size_t scores = 0;     // sparse: [B, Hq, P] fp32
+  size_t selected = 0;   // sparse: [B, Hq, kk] int32 (used when the caller passes none)
+  size_t bitmaps = 0;    // sparse: [B, Hq, W32] u32
+  size_t total = 0;
+  int n_chunks = 0, kk = 0, W32 = 0;
+};
+
+WsLayout layout_for(const dkv_params& p, int top_k) {
+  WsLayout L;
+  const int d = p.head_dim;
+  const int64_t P = ceil_div(p.seq_len, p.page_size);
+  const int64_t rows = static_cast<int64_t>(p.batch) * p.num_q_heads;
+  size_t off = kAlign;  // status word
+  if (top_k <= 0) {
+    L.n_chunks = static_cast<int>(ceil_div(P, dkv::full_pages_per_chunk(d)));
+  } else {
+    const int G = p.num_q_heads / p.num_kv_heads;
+    L.kk = static_cast<int>(top_k < P ? top_k : P);
+    L.W32 = static_cast<int>(ceil_div(P, 32));
+    const int64_t union_max = (static_cast<int64_t>(G) * L.kk < P) ? G * L.kk : P;
+    L.n_chunks = static_cast<int>(ceil_div(union_max, dkv::select_pages_per_chunk(d)));
+    L.scores = off;
+    off = align_up(off + sizeof(float) * rows * P);
+    L.selected = off;
+    off = align_up(off + sizeof(int32_t) * rows * L.kk);
+    L.bitmaps = off;
+    off = align_up(off + sizeof(uint32_t) * rows * L.W32);
+  }
+  L.part_ml = off;
+  off = align_up(off + sizeof(float) * 2 * rows * L.n_chunks);
+  L.part_o = off;
+  off = align_up(off + sizeof(float) * static_cast<size_t>(d) * rows * L.n_chunks);
+  L.total = off;
+  return L;
+}
+
+dkv_status check_params(const dkv_params* p) {
+  if (p == nullptr) return DKV_ERR_NULL;
+  if (p->batch < 1 || p->num_q_heads < 1 || p->num_kv_heads < 1 || p->seq_len < 1 ||
+      p->page_size < 1 || p->head_dim < 1)
+    return DKV_ERR_SHAPE;
+  if (p->num_q_heads % p->num_kv_heads != 0) return DKV_ERR_SHAPE;
+  if (p->head_dim != 64 && p->head_dim != 128) return DKV_ERR_UNSUPPORTED;
+  if (p->page_size != dkv::kPage) return DKV_ERR_UNSUPPORTED;
+  if (p->num_q_heads / p->num_kv_heads > 8) return DKV_ERR_UNSUPPORTED;
+  if (p->batch > 65535 || p->num_kv_heads > 65535) return DKV_ERR_SHAPE;  // grid limits
+  return DKV_OK;
+}
+
+dkv_status check_query_out(const dkv_params* p, const void* q, const void* out) {
+  if (q == nullptr || out == nullptr) return DKV_ERR_NULL;
+  if (!aligned16(q) || !aligned16(out)) return DKV_ERR_ALIGN;
+  if (p->q_stride_b % 8 || p->q_stride_h % 8 || p->o_stride_b % 8 || p->o_stride_h % 8)
+    return DKV_ERR_ALIGN;
+  if (p->q_stride_b < 0 || p->q_stride_h < 0 || p->o_stride_b < 0 || p->o_stride_h < 0)
+    return DKV_ERR_SHAPE;
+  if (!(p->scale > 0.f) || !isfinite(p->scale)) return DKV_ERR_SHAPE;
+  return DKV_OK;
+}
+
+dkv_status check_kv(const dkv_params* p, const dkv_kv* kv) {
+  if (kv == nullptr || kv->data == nullptr) return DKV_ERR_NULL;
+  if (!aligned16(kv->data)) return DKV_ERR_ALIGN;
+  if (kv->stride_b < 0 || kv->stride_h < 0) return DKV_ERR_SHAPE;
+  if (kv->format == DKV_KV_DENSE) {
+    if (kv->dtype != DKV_BF16 && kv->dtype != DKV_FP16) return DKV_ERR_DTYPE;
+    if (kv->stride_b % 8 || kv->stride_h % 8) return DKV_ERR_ALIGN;
+    return DKV_OK;
+  }
+  if (kv->format == DKV_KV_Q4G64) {
+    if (kv->dtype != DKV_FP16) return DKV_ERR_DTYPE;
+    if (kv->gmin == nullptr || kv->gmax == nullptr) return DKV_ERR_NULL;
+    if (!aligned16(kv->gmin) || !aligned16(kv->gmax)) return DKV_ERR_ALIGN;
+    if (kv->stride_b % 16 || kv->stride_h % 16) return DKV_ERR_ALIGN;
+    if (kv->gstride_b < 0 || kv->gstride_h < 0) return DKV_ERR_SHAPE;
+    if (kv->gstride_b % 8 || kv->gstride_h % 8) return DKV_ERR_ALIGN;
+    return DKV_OK;
+  }
+  return DKV_ERR_DTYPE;
+}
+
+// ------------------------------------------------------------- tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// Map over one dense K or V cache [B, Hkv, N, d] viewed as 5-D
+// {64 channels, N tokens, d/64 halves, Hkv, B} with a box of one page
+// {64, 16, d/64, 1, 1} and 128-byte swizzle.
+bool encode_page_map(CUtensorMap* map, const dkv_params* p, const dkv_kv* kv) {
+  if (!get_encode()) return false;
+  const int d = p->head_dim;
+  const cuuint64_t dims[5] = {64, static_cast<cuuint64_t>(p->seq_len),
+                              static_cast<cuuint64_t>(d / 64),
+                              static_cast<cuuint64_t>(p->num_kv_heads),
+                              static_cast<cuuint64_t>(p->batch)};
+  const cuuint64_t strides[4] = {static_cast<cuuint64_t>(d) * 2, 128,
+                                 static_cast<cuuint64_t>(kv->stride_h) * 2,
+                                 static_cast<cuuint64_t>(kv->stride_b) * 2};
+  const cuuint32_t box[5] = {64, static_cast<cuuint32_t>(dkv::kPage),
+                             static_cast<cuuint32_t>(d / 64), 1, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUtensorMapDataType dt = kv->dtype == DKV_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                        : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  // A size-1 dimension's stride still has to be a valid (16-byte multiple) value.
+  cuuint64_t st[4] = {strides[0], strides[1], strides[2], strides[3]};
+  if (p->num_kv_heads == 1 && st[2] == 0) st[2] = 16;
+  if (p->batch == 1 && st[3] == 0) st[3] = 16;
+  const CUresult r = g_encode(map, dt, 5, const_cast<void*>(kv->data), dims, st, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int out_code(int32_t out_dtype) {
+  return out_dtype == DKV_FP32 ? 2 : (out_dtype == DKV_FP16 ? 1 : 0);
+}
+
+dkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DKV_OK : DKV_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+size_t dkv_workspace_bytes(const dkv_params* p, int32_t top_k) {
+  if (check_params(p) != DKV_OK || top_k < 0) return 0;
+  return layout_for(*p, top_k).total;
+}
+
+dkv_status dkv_kv_meta_build(const dkv_params* p, const dkv_kv* K, void* meta_min,
+                             void* meta_max, void* stream) {
+  dkv_status st = check_params(p);
+  if (st != DKV_OK) return st;
+  if ((st = check_kv(p, K)) != DKV_OK) return st;
+  if (meta_min == nullptr || meta_max == nullptr) return DKV_ERR_NULL;
+  if (!aligned16(meta_min) || !aligned16(meta_max)) return DKV_ERR_ALIGN;
+  dkv::MetaArgs a{};
+  a.data = K->data;
+  a.gmin = K->gmin;
+  a.gmax = K->gmax;
+  a.sb = K->stride_b;
+  a.sh = K->stride_h;
+  a.gsb = K->gstride_b;
+  a.gsh = K->gstride_h;
+  a.B = p->batch;
+  a.Hkv = p->num_kv_heads;
+  a.N = p->seq_len;
+  a.P = static_cast<int>(ceil_div(p->seq_len, p->page_size));
+  a.d = p->head_dim;
+  a.meta_min = meta_min;
+  a.meta_max = meta_max;
+  return cuda_status(dkv::launch_meta(K->format == DKV_KV_Q4G64, K->dtype == DKV_FP16, a,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+static dkv_status attn_common(const dkv_params* p, const void* q, const dkv_kv* K,
+                              const dkv_kv* V, void* out, int32_t out_dtype, void* workspace,
+                              size_t workspace_bytes, int top_k, const WsLayout& L) {
+  dkv_status st = check_params(p);
+  if (st != DKV_OK) return st;
+  if ((st = check_query_out(p, q, out)) != DKV_OK) return st;
+  if ((st = check_kv(p, K)) != DKV_OK) return st;
+  if ((st = check_kv(p, V)) != DKV_OK) return st;
+  if (K->format != V->format || K->dtype != V->dtype) return DKV_ERR_DTYPE;
+  if (out_dtype != DKV_FP32 && out_dtype != DKV_BF16 && out_dtype != DKV_FP16)
+    return DKV_ERR_DTYPE;
+  if (K->format == DKV_KV_Q4G64) return DKV_ERR_UNSUPPORTED;  // dense caches only for now
+  if (workspace == nullptr) return DKV_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return DKV_ERR_ALIGN;
+  if (workspace_bytes < L.total) return DKV_ERR_WORKSPACE;
+  (void)top_k;
+  return DKV_OK;
+}
+
+dkv_status dkv_decode_attn_full(const dkv_params* p, const void* q, const dkv_kv* K,
+                                const dkv_kv* V, void* out, int32_t out_dtype,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  dkv_status st = check_params(p);
+  if (st != DKV_OK) return st;
+  const WsLayout L = layout_for(*p, 0);
+  if ((st = attn_common(p, q, K, V, out, out_dtype, workspace, workspace_bytes, 0, L)) != DKV_OK)
+    return st;
+  CUtensorMap mk, mv;
+  if (!encode_page_map(&mk, p, K) || !encode_page_map(&mv, p, V)) return DKV_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  dkv::AttnArgs a{};
+  a.q = q;
+  a.q_sb = p->q_stride_b;
+  a.q_sh = p->q_stride_h;
+  a.B = p->batch;
+  a.Hq = p->num_q_heads;
+  a.Hkv = p->num_kv_heads;
+  a.G = p->num_q_heads / p->num_kv_heads;
+  a.N = p->seq_len;
+  a.P = static_cast<int>(ceil_div(p->seq_len, p->page_size));
+  a.scale_log2 = p->scale * 1.4426950408889634f;
+  a.pages_per_chunk = dkv::full_pages_per_chunk(p->head_dim);
+  a.n_chunks = L.n_chunks;
+  a.part_ml = reinterpret_cast<float*>(ws + L.part_ml);
+  a.part_o = reinterpret_cast<float*>(ws + L.part_o);
+  a.status = reinterpret_cast<uint32_t*>(ws + L.status);
+  a.wait_limit_ns = (p->flags & DKV_FLAG_FORCE_TIMEOUT) ? 0 : kWaitLimitNs;
+  const bool f16 = K->dtype == DKV_FP16;
+  dim3 grid(L.n_chunks, p->num_kv_heads, p->batch);
+  if ((st = cuda_status(dkv::launch_attn(p->head_dim, f16, false, a, mk, mv, grid, s))) != DKV_OK)
+    return st;
+  dkv::CombineArgs c{};
+  c.part_ml = a.part_ml;
+  c.part_o = a.part_o;
+  c.n_chunks = L.n_chunks;
+  c.Hq = p->num_q_heads;
+  c.out = out;
+  c.out_dtype = out_code(out_dtype);
+  c.o_sb = p->o_stride_b;
+  c.o_sh = p->o_stride_h;
+  return cuda_status(dkv::launch_combine(p->head_dim, c, p->batch * p->num_q_heads, s));
+}
+
+dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_kv* K,
+                                  const dkv_kv* V, const void* meta_min,
+                                  const void* meta_max, int32_t top_k, void* out,
+                                  int32_t out_dtype, int32_t* selected, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  dkv_status st = check_params(p);
+  if (st != DKV_OK) return st;
+  if (top_k < 1) return DKV_ERR_SHAPE;
+  const WsLayout L = layout_for(*p, top_k);
+  if ((st = attn_common(p, q, K, V, out, out_dtype, workspace, workspace_bytes, top_k, L)) !=
+      DKV_OK)
+    return st;
+  if (meta_min == nullptr || meta_max == nullptr) return DKV_ERR_NULL;
+  if (!aligned16(meta_min) || !aligned16(meta_max)) return DKV_ERR_ALIGN;
+  if (selected != nullptr && (reinterpret_cast<uintptr_t>(selected) & 3u)) return DKV_ERR_ALIGN;
+  CUtensorMap mk, mv;
+  if (!encode_page_map(&mk, p, K) || !encode_page_map(&mv, p, V)) return DKV_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int P = static_cast<int>(ceil_div(p->seq_len, p->page_size));
+  const int G = p->num_q_heads / p->num_kv_heads;
+  const bool f16 = K->dtype == DKV_FP16;
+
+  dkv::ScoreArgs sa{};
+  sa.q = q;
+  sa.q_sb = p->q_stride_b;
+  sa.q_sh = p->q_stride_h;
+  sa.meta_min = meta_min;
+  sa.meta_max = meta_max;
+  sa.B = p->batch;
+  sa.Hq = p->num_q_heads;
+  sa.Hkv = p->num_kv_heads;
+  sa.G = G;
+  sa.P = P;
+  sa.scores = reinterpret_cast<float*>(ws + L.scores);
+  if ((st = cuda_status(dkv::launch_score(p->head_dim, f16, sa, s))) != DKV_OK) return st;
+
+  dkv::TopkArgs ta{};
+  ta.scores = sa.scores;
+  ta.rows = p->batch * p->num_q_heads;
+  ta.P = P;
+  ta.kk = L.kk;
+  ta.selected = selected != nullptr ? selected : reinterpret_cast<int32_t*>(ws + L.selected);
+  ta.bitmaps = reinterpret_cast<uint32_t*>(ws + L.bitmaps);
+  ta.W32 = L.W32;
+  if ((st = cuda_status(dkv::launch_topk(ta, s))) != DKV_OK) return st;
+
+  dkv::AttnArgs a{};
+  a.q = q;
+  a.q_sb = p->q_stride_b;
+  a.q_sh = p->q_stride_h;
+  a.B = p->batch;
+  a.Hq = p->num_q_heads;
+  a.Hkv = p->num_kv_heads;
+  a.G = G;
+  a.N = p->seq_len;
+  a.P = P;
+  a.scale_log2 = p->scale * 1.4426950408889634f;
+  a.pages_per_chunk = dkv::select_pages_per_chunk(p->head_dim);
+  a.n_chunks = L.n_chunks;
+  a.part_ml = reinterpret_cast<float*>(ws + L.part_ml);
+  a.part_o = reinterpret_cast<float*>(ws + L.part_o);
+  a.bitmaps = ta.bitmaps;
+  a.W32 = L.W32;
+  a.status = reinterpret_cast<uint32_t*>(ws + L.status);
+  a.wait_limit_ns = (p->flags & DKV_FLAG_FORCE_TIMEOUT) ? 0 : kWaitLimitNs;
+  dim3 grid(L.n_chunks, p->num_kv_heads, p->batch);
+  if ((st = cuda_status(dkv::launch_attn(p->head_dim, f16, true, a, mk, mv, grid, s))) != DKV_OK)
+    return st;
+  dkv::CombineArgs c{};
+  c.part_ml = a.part_ml;
+  c.part_o = a.part_o;
+  c.n_chunks = L.n_chunks;
+  c.Hq = p->num_q_heads;
+  c.out = out;
+  c.out_dtype = out_code(out_dtype);
+  c.o_sb = p->o_stride_b;
+  c.o_sh = p->o_stride_h;
+  return cuda_status(dkv::launch_combine(p->head_dim, c, p->batch * p->num_q_heads, s));
+}
+
+dkv_status dkv_kv_quant4(int64_t rows, int32_t d, const void* x, void* codes, void* gmin,
+                         void* gmax, void* stream) {
+  if (x == nullptr || codes == nullptr || gmin == nullptr || gmax == nullptr) return DKV_ERR_NULL;
+  if (rows < 0 || d < 64 || d % 64 != 0) return DKV_ERR_SHAPE;
+  if (rows * (d / 64) * 8 > (static_cast<int64_t>(1) << 40)) return DKV_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(codes) || (reinterpret_cast<uintptr_t>(gmin) & 1u) ||
+      (reinterpret_cast<uintptr_t>(gmax) & 1u))
+    return DKV_ERR_ALIGN;
+  if (rows == 0) return DKV_OK;
+  return cuda_status(
+      dkv::launch_quant4(rows, d, x, codes, gmin, gmax, static_cast<cudaStream_t>(stream)));
+}
+
+dkv_status dkv_kv_dequant4(int64_t rows, int32_t d, const void* codes, const void* gmin,
+                           const void* gmax, void* x, void* stream) {
+  if (x == nullptr || codes == nullptr || gmin == nullptr || gmax == nullptr) return DKV_ERR_NULL;
+  if (rows < 0 || d < 64 || d % 64 != 0) return DKV_ERR_SHAPE;
+  if (rows * (d / 64) * 8 > (static_cast<int64_t>(1) << 40)) return DKV_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(codes) || (reinterpret_cast<uintptr_t>(gmin) & 1u) ||
+      (reinterpret_cast<uintptr_t>(gmax) & 1u))
+    return DKV_ERR_ALIGN;
+  if (rows == 0) return DKV_OK;
+  return cuda_status(
+      dkv::launch_dequant4(rows, d, codes, gmin, gmax, x, static_cast<cudaStream_t>(stream)));
+}
+
+dkv_status dkv_read_device_status(void* workspace, void* stream) {
+  if (workspace == nullptr) return DKV_ERR_NULL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return DKV_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DKV_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, sizeof v, s) != cudaSuccess) return DKV_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DKV_ERR_CUDA;
+  return static_cast<dkv_status>(v);
+}
+
+const char* dkv_status_string(int32_t status) {
+  switch (status) {
+    case DKV_OK: return "ok";
+    case DKV_ERR_NULL: return "a required pointer is NULL";
+    case DKV_ERR_SHAPE: return "a size or stride is out of range";
+    case DKV_ERR_ALIGN: return "a pointer or stride is not 16-byte aligned";
+    case DKV_ERR_DTYPE: return "unsupported dtype or format combination";
+    case DKV_ERR_UNSUPPORTED: return "head_dim, page_size or query group outside the kernels";
+    case DKV_ERR_WORKSPACE: return "workspace missing or too small";
+    case DKV_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    case DKV_ERR_DEVICE_TIMEOUT: return "device: a bounded wait expired";
+    case DKV_ERR_DEVICE_CHECK: return "device: an in-kernel check failed";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,238 @@
+// dkv_device.cuh -- device helpers for the sm_103a kernels of libdkv:
+// mbarrier / TMA / ldmatrix / mma.sync wrappers in inline PTX, bounded waits
+// that report through the status word, 16-bit float key transforms and the
+// in-register 4-bit dequantisation.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace dkv {
+
+// Device status codes (mirror dkv_status in include/dkv.h).
+constexpr uint32_t kStatusTimeout = 8;
+constexpr uint32_t kStatusCheck = 9;
+
+__device__ __forceinline__ void set_status(uint32_t* status, uint32_t code) {
+  if (status != nullptr) atomicCAS(status, 0u, code);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait until the phase with `parity` of `bar` has completed.  Gives up (returns
+// false) after `limit_ns` of wall time, or at once when limit_ns == 0 (the
+// forced-timeout test hook), or when *abort becomes non-zero.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t limit_ns,
+                                                  const volatile int* abort_flag) {
+  if (limit_ns == 0) return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (abort_flag != nullptr && *abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// ---------------------------------------------------------------- TMA
+// Tiled tensor copy global -> shared, 5-D coordinates, completion counted in
+// bytes on `bar`.
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(c4)
+      : "memory");
+}
+
+// Same, with an L2 eviction-priority hint (streamed-once data).
+__device__ __forceinline__ void tma_load_5d_hint(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar, int c0, int c1, int c2, int c3,
+                                                 int c4, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(c4), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// Untiled bulk copy global -> shared (both 16-byte aligned, bytes % 16 == 0).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---------------------------------------------------------------- ldmatrix / mma
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                              uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D[16x8] += A[16x16] * B[16x8], fp32 accumulate.  F16 selects fp16 operands
+// (otherwise bf16).
+template <bool F16>
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  if constexpr (F16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+
+// Round two floats to a packed pair of 16-bit floats (round to nearest even);
+// `lo` lands in the low half.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (F16) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+// Value of the low / high 16-bit float of a packed pair.
+template <bool F16>
+__device__ __forceinline__ float lo16(uint32_t w) {
+  if constexpr (F16) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
+  } else {
+    return __uint_as_float(w << 16);
+  }
+}
+template <bool F16>
+__device__ __forceinline__ float hi16(uint32_t w) {
+  if constexpr (F16) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+  } else {
+    return __uint_as_float(w & 0xffff0000u);
+  }
+}
+
+// Split p into hi + lo, each a 16-bit float pair, so that the tensor-core PV
+// product keeps ~16 significant bits of the softmax weights.
+template <bool F16>
+__device__ __forceinline__ void split_pair(float p0, float p1, uint32_t& hi, uint32_t& lo) {
+  hi = pack2<F16>(p0, p1);
+  lo = pack2<F16>(p0 - lo16<F16>(hi), p1 - hi16<F16>(hi));
+}
+
+// ---------------------------------------------------------------- 16-bit keys
+// Order-preserving map of two packed 16-bit floats to unsigned 16-bit keys
+// (numeric order, -0 below +0), and its inverse.
+__device__ __forceinline__ uint32_t to_key2(uint32_t x) {
+  const uint32_t s = (x >> 15) & 0x00010001u;
+  return x ^ ((s * 0xffffu) | 0x80008000u);
+}
+__device__ __forceinline__ uint32_t from_key2(uint32_t k) {
+  const uint32_t t = (~k >> 15) & 0x00010001u;
+  return k ^ ((t * 0x7fffu) | 0x80008000u);
+}
+
+// ---------------------------------------------------------------- 4-bit format
+// step = fp16(fp32(fp32(mx - mn) / 15)), from the group's stored min / max.
+__device__ __forceinline__ __half q4_step(__half mn, __half mx) {
+  const float range = __fsub_rn(__half2float(mx), __half2float(mn));
+  return __float2half_rn(__fdiv_rn(range, 15.0f));
+}
+
+// Dequantise the 8 codes of one 32-bit word (byte i: channel 2i low nibble,
+// 2i+1 high nibble): x = fp16(code * step + mn), one rounding (fp16 FMA),
+// replaced by mx where it exceeds mx.  Output: 4 packed half pairs, channels in
+// order.
+__device__ __forceinline__ void q4_dequant8(uint32_t c4, __half2 mn2, __half2 step2,
+                                            __half2 mx2, uint32_t (&out)[4]) {
+  const __half2 k1024 = __half2half2(__ushort_as_half(0x6400));  // 1024.0
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t byte = (c4 >> (8 * i)) & 0xffu;
+    // 1024 + code as an exact fp16 in each half, then subtract 1024 exactly.
+    const uint32_t bits = (byte & 0x0fu) | ((byte & 0xf0u) << 12) | 0x64006400u;
+    const __half2 biased = *reinterpret_cast<const __half2*>(&bits);
+    const __half2 code = __hsub2(biased, k1024);
+    const __half2 x = __hfma2(code, step2, mn2);
+    const uint32_t over = __hgt2_mask(x, mx2);  // 0xffff per half where x > mx
+    out[i] = (over & *reinterpret_cast<const uint32_t*>(&mx2)) |
+             (~over & *reinterpret_cast<const uint32_t*>(&x));
+  }
+}
+
+}  // namespace dkv

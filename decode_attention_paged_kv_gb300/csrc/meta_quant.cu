@@ -1,0 +1,207 @@
+// meta_quant.cu -- page metadata build and the 4-bit KV format.
+//
+// Page metadata ("TinyServe: Query-Aware Cache Selection for Efficient LLM
+// Serving", 结构化内存布局 / 相关性函数实例化): for every page of S = 16 tokens,
+// m_j and M_j are the channel-wise min / max of the page's keys.  One thread
+// owns 8 channels of one page: it streams the page's (up to) 16 rows as 16-byte
+// vectors -- a warp covers whole contiguous 256-byte key rows -- and reduces on
+// order-preserving 16-bit keys with per-halfword integer min / max, so the
+// result is exactly one of the stored values (-0 below +0).  A 4-bit cache is
+// dequantised in registers first; its metadata describes the fp16 keys that
+// attention actually uses.
+//
+// 4-bit format ("FlexGen: High-Throughput Generative Inference of Large
+// Language Models with a Single GPU" 解读, 4-bit 近似方法): groups of 64
+// channels of one (token, head) row; per-group min / max in fp16; 15 equal
+// steps between them; codes rounded to nearest even in fp32 IEEE operations;
+// values dequantised back to fp16 with one fused fp16 multiply-add, saturated
+// at the group max.
+
+#include "dkv_device.cuh"
+#include "dkv_kernels.h"
+
+namespace dkv {
+namespace {
+
+constexpr int kMetaThreads = 256;
+
+template <bool Q4>
+__global__ void __launch_bounds__(kMetaThreads) meta_kernel(const MetaArgs a) {
+  const int vpr = a.d / 8;  // 16-byte vectors per row
+  const int64_t total = static_cast<int64_t>(a.B) * a.Hkv * a.P * vpr;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int v = static_cast<int>(idx % vpr);
+    const int64_t pg = idx / vpr;  // (b * Hkv + h) * P + page
+    const int page = static_cast<int>(pg % a.P);
+    const int64_t bh = pg / a.P;
+    const int h = static_cast<int>(bh % a.Hkv);
+    const int b = static_cast<int>(bh / a.Hkv);
+    const int t0 = page * kPage;
+    const int nt = min(kPage, a.N - t0);
+    uint32_t kmin[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+    uint32_t kmax[4] = {0u, 0u, 0u, 0u};
+    if constexpr (!Q4) {
+      const uint16_t* src = static_cast<const uint16_t*>(a.data) + b * a.sb + h * a.sh +
+                            static_cast<int64_t>(t0) * a.d + 8 * v;
+      uint4 x[kPage];
+#pragma unroll
+      for (int t = 0; t < kPage; ++t)
+        if (t < nt) x[t] = __ldcs(reinterpret_cast<const uint4*>(src + static_cast<int64_t>(t) * a.d));
+#pragma unroll
+      for (int t = 0; t < kPage; ++t) {
+        if (t < nt) {
+          const uint32_t w[4] = {x[t].x, x[t].y, x[t].z, x[t].w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t k = to_key2(w[u]);
+            kmin[u] = __vminu2(kmin[u], k);
+            kmax[u] = __vmaxu2(kmax[u], k);
+          }
+        }
+      }
+    } else {
+      const uint8_t* src = static_cast<const uint8_t*>(a.data) + b * a.sb + h * a.sh +
+                           static_cast<int64_t>(t0) * (a.d / 2) + 4 * v;
+      const int grp = v / 8;
+      const int ng = a.d / 64;
+      const __half* gmn = static_cast<const __half*>(a.gmin) + b * a.gsb + h * a.gsh +
+                          static_cast<int64_t>(t0) * ng + grp;
+      const __half* gmx = static_cast<const __half*>(a.gmax) + b * a.gsb + h * a.gsh +
+                          static_cast<int64_t>(t0) * ng + grp;
+#pragma unroll 4
+      for (int t = 0; t < nt; ++t) {
+        const uint32_t c4 = __ldcs(reinterpret_cast<const uint32_t*>(src + static_cast<int64_t>(t) * (a.d / 2)));
+        const __half mn = gmn[static_cast<int64_t>(t) * ng];
+        const __half mx = gmx[static_cast<int64_t>(t) * ng];
+        uint32_t w[4];
+        q4_dequant8(c4, __half2half2(mn), __half2half2(q4_step(mn, mx)), __half2half2(mx), w);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t k = to_key2(w[u]);
+          kmin[u] = __vminu2(kmin[u], k);
+          kmax[u] = __vmaxu2(kmax[u], k);
+        }
+      }
+    }
+    uint4 omin, omax;
+    omin.x = from_key2(kmin[0]);
+    omin.y = from_key2(kmin[1]);
+    omin.z = from_key2(kmin[2]);
+    omin.w = from_key2(kmin[3]);
+    omax.x = from_key2(kmax[0]);
+    omax.y = from_key2(kmax[1]);
+    omax.z = from_key2(kmax[2]);
+    omax.w = from_key2(kmax[3]);
+    const int64_t o = pg * a.d + 8 * v;
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.meta_min) + o) = omin;
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.meta_max) + o) = omax;
+  }
+}
+
+// 8 threads per group of 64 channels, 8 channels (16 bytes) per thread.  The
+// loop advances whole blocks, so the 8 lanes of a group always shuffle together.
+__global__ void __launch_bounds__(256) quant4_kernel(int64_t groups, const __half* x,
+                                                     uint8_t* codes, __half* gmin, __half* gmax) {
+  const int64_t total = groups * 8;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.x; t0 < total; t0 += stride) {
+    const int64_t t = t0 + threadIdx.x;
+    const int64_t grp = t >> 3;
+    const int sub = static_cast<int>(t & 7);
+    const bool valid = grp < groups;
+    uint4 xv = make_uint4(0, 0, 0, 0);
+    if (valid) xv = __ldcs(reinterpret_cast<const uint4*>(x + grp * 64 + sub * 8));
+    const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t k = to_key2(w[u]);
+      kmin = __vminu2(kmin, k);
+      kmax = __vmaxu2(kmax, k);
+    }
+    // fold the two halfwords, then the 8 lanes of the group
+    kmin = min(kmin & 0xffffu, kmin >> 16);
+    kmax = max(kmax & 0xffffu, kmax >> 16);
+#pragma unroll
+    for (int off = 1; off < 8; off <<= 1) {
+      kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, off));
+      kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, off));
+    }
+    if (!valid) continue;
+    const __half mn = __ushort_as_half(static_cast<unsigned short>(from_key2(kmin) & 0xffffu));
+    const __half mx = __ushort_as_half(static_cast<unsigned short>(from_key2(kmax) & 0xffffu));
+    const __half step = q4_step(mn, mx);
+    const float fstep = __half2float(step);
+    const float fmn = __half2float(mn);
+    uint32_t packed = 0;
+    if (fstep != 0.f) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t hv = (w[e >> 1] >> (16 * (e & 1))) & 0xffffu;
+        const float xf = __half2float(__ushort_as_half(static_cast<unsigned short>(hv)));
+        float c = rintf(__fdiv_rn(__fsub_rn(xf, fmn), fstep));
+        c = fminf(15.f, fmaxf(0.f, c));
+        packed |= static_cast<uint32_t>(c) << (4 * e);
+      }
+    }
+    *reinterpret_cast<uint32_t*>(codes + grp * 32 + sub * 4) = packed;
+    if (sub == 0) {
+      gmin[grp] = mn;
+      gmax[grp] = mx;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) dequant4_kernel(int64_t groups, const uint8_t* codes,
+                                                       const __half* gmin, const __half* gmax,
+                                                       __half* x) {
+  const int64_t total = groups * 8;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
+       t += stride) {
+    const int64_t grp = t >> 3;
+    const int sub = static_cast<int>(t & 7);
+    const __half mn = gmin[grp], mx = gmax[grp];
+    const uint32_t c4 = __ldcs(reinterpret_cast<const uint32_t*>(codes + grp * 32 + sub * 4));
+    uint32_t w[4];
+    q4_dequant8(c4, __half2half2(mn), __half2half2(q4_step(mn, mx)), __half2half2(mx), w);
+    *reinterpret_cast<uint4*>(x + grp * 64 + sub * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+int grid_for(int64_t threads, int block) {
+  const int64_t blocks = ceil_div(threads, block);
+  return static_cast<int>(blocks < 152 * 64 ? blocks : 152 * 64);
+}
+
+}  // namespace
+
+cudaError_t launch_meta(bool q4, bool f16, const MetaArgs& a, cudaStream_t s) {
+  (void)f16;  // min / max on order-preserving keys: identical code for bf16 and fp16
+  const int64_t work = static_cast<int64_t>(a.B) * a.Hkv * a.P * (a.d / 8);
+  const int grid = grid_for(work, kMetaThreads);
+  if (q4) meta_kernel<true><<<grid, kMetaThreads, 0, s>>>(a);
+  else meta_kernel<false><<<grid, kMetaThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant4(int64_t rows, int d, const void* x, void* codes, void* gmin,
+                          void* gmax, cudaStream_t s) {
+  const int64_t groups = rows * (d / 64);
+  quant4_kernel<<<grid_for(groups * 8, 256), 256, 0, s>>>(
+      groups, static_cast<const __half*>(x), static_cast<uint8_t*>(codes),
+      static_cast<__half*>(gmin), static_cast<__half*>(gmax));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant4(int64_t rows, int d, const void* codes, const void* gmin,
+                            const void* gmax, void* x, cudaStream_t s) {
+  const int64_t groups = rows * (d / 64);
+  dequant4_kernel<<<grid_for(groups * 8, 256), 256, 0, s>>>(
+      groups, static_cast<const uint8_t*>(codes), static_cast<const __half*>(gmin),
+      static_cast<const __half*>(gmax), static_cast<__half*>(x));
+  return cudaGetLastError();
+}
+
+}  // namespace dkv

@@ -1,0 +1,170 @@
+/*
+ * dkv.h -- C ABI of libdkv: single-token decode attention over a paged KV cache
+ * on NVIDIA GB300 (sm_103a).
+ *
+ * The operations and where they are defined:
+ *
+ *   dkv_kv_meta_build       page metadata phi(K_j) = (m_j, M_j), the channel-wise
+ *                           min / max of each page of S keys.
+ *                           "TinyServe: Query-Aware Cache Selection for Efficient
+ *                           LLM Serving", 方法细节: 结构化内存布局 and
+ *                           相关性函数实例化.
+ *   dkv_decode_attn_full    exact decode attention Softmax(q K^T * scale) V per
+ *                           query head, with grouped kv heads (GQA).
+ *                           "论文阅读：HeadInfer", 核心 idea (the A^(h) equation);
+ *                           TinyServe, 标准Transformer解码层的注意力计算.
+ *   dkv_decode_attn_select  query-aware page-sparse attention: bound score
+ *                           r(q, phi_j) = sum_i (q_i >= 0 ? q_i M_ji : q_i m_ji),
+ *                           top-K pages, attention over the selected pages only.
+ *                           TinyServe, 相关性函数实例化, 问题公式化定义 and
+ *                           Algorithm 1 (Fused Query-Aware Sparse Attention
+ *                           Kernel), steps 1-4.
+ *   dkv_kv_quant4 /         4-bit KV format: groups of 64 channels along the head
+ *   dkv_kv_dequant4         dimension, per-group min / max, 4-bit codes,
+ *                           dequantised to fp16 before use.
+ *                           "FlexGen: High-Throughput Generative Inference of
+ *                           Large Language Models with a Single GPU" (解读),
+ *                           4-bit 近似方法.
+ *
+ * Conventions shared by every entry point:
+ *   - Every data pointer is a DEVICE pointer owned by the caller, 16-byte
+ *     aligned.  The library allocates no device memory and keeps no per-call
+ *     state.  Scratch space is a caller-owned `workspace` of
+ *     dkv_workspace_bytes() bytes.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Every call is asynchronous on that stream; only
+ *     dkv_read_device_status synchronises.
+ *   - Layouts are row-major with the innermost (channel) stride 1:
+ *       q        [B, Hq, d]        strides q_stride_b, q_stride_h (elements)
+ *       out      [B, Hq, d]        strides o_stride_b, o_stride_h (elements)
+ *       K, V     [B, Hkv, N, d]    token stride d; batch / head strides in dkv_kv
+ *       meta     [B, Hkv, P, d]    contiguous, P = ceil(N / S)
+ *       selected [B, Hq, kk]       contiguous int32, kk = min(top_k, P)
+ *     Query head h reads kv head h / (Hq / Hkv).
+ *   - Argument errors are returned before anything is launched.  Launch
+ *     failures return DKV_ERR_CUDA.  Errors found on the device (a bounded
+ *     wait that expired, an in-kernel check) are written to a status word at
+ *     the start of the workspace and read back with dkv_read_device_status.
+ *     No call aborts the process.
+ *   - Supported: d in {64, 128}; S == 16; Hq % Hkv == 0 and Hq / Hkv <= 8;
+ *     1 <= N < 2^31; bf16 or fp16 dense caches (q in the same dtype), or the
+ *     4-bit format with fp16 q.  A ragged last page is masked.
+ */
+#ifndef DKV_H_
+#define DKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dkv_status {
+  DKV_OK = 0,
+  DKV_ERR_NULL = 1,           /* a required pointer is NULL */
+  DKV_ERR_SHAPE = 2,          /* a size or stride is out of range */
+  DKV_ERR_ALIGN = 3,          /* a pointer or stride is not 16-byte aligned */
+  DKV_ERR_DTYPE = 4,          /* unsupported dtype / format combination */
+  DKV_ERR_UNSUPPORTED = 5,    /* d, S or Hq/Hkv outside what the kernels cover */
+  DKV_ERR_WORKSPACE = 6,      /* workspace NULL or smaller than required */
+  DKV_ERR_CUDA = 7,           /* a CUDA runtime call or kernel launch failed */
+  DKV_ERR_DEVICE_TIMEOUT = 8, /* device status: a bounded wait expired */
+  DKV_ERR_DEVICE_CHECK = 9    /* device status: an in-kernel check failed */
+} dkv_status;
+
+typedef enum dkv_dtype { DKV_BF16 = 0, DKV_FP16 = 1, DKV_FP32 = 2 } dkv_dtype;
+
+typedef enum dkv_kv_format {
+  DKV_KV_DENSE = 0, /* data: [B, Hkv, N, d] elements of `dtype` (bf16 or fp16) */
+  DKV_KV_Q4G64 = 1  /* data: codes [B, Hkv, N, d/2] bytes, channel 2i in the low
+                       nibble of byte i; gmin / gmax: [B, Hkv, N, d/64] fp16 */
+} dkv_kv_format;
+
+/* One K or V cache. */
+typedef struct dkv_kv {
+  int32_t format;           /* dkv_kv_format */
+  int32_t dtype;            /* DENSE: DKV_BF16 | DKV_FP16.  Q4G64: DKV_FP16 */
+  const void* data;         /* device pointer, see dkv_kv_format */
+  const void* gmin;         /* Q4G64 only (else NULL) */
+  const void* gmax;         /* Q4G64 only (else NULL) */
+  int64_t stride_b;         /* of data: elements (DENSE) or bytes (Q4G64 codes) */
+  int64_t stride_h;         /*   token stride is d (DENSE) or d/2 (codes) */
+  int64_t gstride_b;        /* of gmin / gmax, in fp16 elements; Q4G64 only */
+  int64_t gstride_h;        /*   token stride is d/64 */
+} dkv_kv;
+
+/* Problem description shared by the attention and metadata calls. */
+typedef struct dkv_params {
+  int32_t batch;            /* B  >= 1 */
+  int32_t num_q_heads;      /* Hq >= 1 */
+  int32_t num_kv_heads;     /* Hkv >= 1, Hq % Hkv == 0, Hq / Hkv <= 8 */
+  int32_t head_dim;         /* d in {64, 128} */
+  int32_t seq_len;          /* N >= 1 context tokens, all attended */
+  int32_t page_size;        /* S == 16 */
+  int64_t q_stride_b, q_stride_h;   /* q, in elements */
+  int64_t o_stride_b, o_stride_h;   /* out, in elements */
+  float scale;              /* softmax scale, usually 1/sqrt(d) */
+  uint32_t flags;           /* DKV_FLAG_* ; 0 for normal use */
+} dkv_params;
+
+/* Test hook: every bounded device wait gives up at once, so the timeout path
+   (status word set, in-flight copies drained, clean exit) runs without a hang. */
+#define DKV_FLAG_FORCE_TIMEOUT 0x1u
+
+/* Bytes of workspace the attention calls need for `p` (top_k = 0: the exact
+   path; top_k >= 1: the sparse path).  0 if `p` is invalid.  Host only. */
+size_t dkv_workspace_bytes(const dkv_params* p, int32_t top_k);
+
+/* Page metadata.  meta_min / meta_max: [B, Hkv, P, d] contiguous, in K's dtype
+   (fp16 for a Q4G64 cache, built from the dequantised fp16 keys).  m_j / M_j
+   are exact: minimum and maximum of the stored values (total order, -0 < +0).
+   Uses p->batch, num_kv_heads, head_dim, seq_len, page_size. */
+dkv_status dkv_kv_meta_build(const dkv_params* p, const dkv_kv* K, void* meta_min,
+                             void* meta_max, void* stream);
+
+/* Exact decode attention.  out [B, Hq, d] in out_dtype (DKV_FP32 | DKV_BF16 |
+   DKV_FP16).  Splits the sequence into fixed chunks whose length depends only
+   on d, so evaluating one kv head at a time (a view with Hkv = 1) gives results
+   bitwise identical to the all-heads call. */
+dkv_status dkv_decode_attn_full(const dkv_params* p, const void* q, const dkv_kv* K,
+                                const dkv_kv* V, void* out, int32_t out_dtype,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/* Query-aware page-sparse decode attention.  For each (b, q-head): bound
+   scores of all P pages from meta_min / meta_max, the top_k best pages (ties
+   to the lower page index; top_k clamped to P), attention over those pages'
+   tokens only (softmax normalised over them).  `selected` (nullable) receives
+   the chosen pages [B, Hq, min(top_k, P)] in ascending order. */
+dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_kv* K,
+                                  const dkv_kv* V, const void* meta_min,
+                                  const void* meta_max, int32_t top_k, void* out,
+                                  int32_t out_dtype, int32_t* selected, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/* 4-bit group-of-64 quantisation of `rows` fp16 rows of d channels (d % 64 == 0):
+     mn, mx = group min / max;  step = fp16(fp32(fp32(mx - mn) / 15))
+     code   = step == 0 ? 0 : clamp(rint(fp32(fp32(x - mn) / step)), 0, 15)
+   codes [rows, d/2] (channel 2i in the low nibble), gmin / gmax [rows, d/64]. */
+dkv_status dkv_kv_quant4(int64_t rows, int32_t d, const void* x, void* codes, void* gmin,
+                         void* gmax, void* stream);
+
+/* Inverse: x = fp16(code * step + mn), rounded once (a fused fp16 multiply-add),
+   replaced by mx where it exceeds mx, so x always lies in [mn, mx].  Inputs are
+   finite fp16 values. */
+dkv_status dkv_kv_dequant4(int64_t rows, int32_t d, const void* codes, const void* gmin,
+                           const void* gmax, void* x, void* stream);
+
+/* Synchronises `stream`, returns the device status word held at the start of
+   `workspace` (DKV_OK, DKV_ERR_DEVICE_TIMEOUT or DKV_ERR_DEVICE_CHECK) and
+   resets it to DKV_OK.  Returns DKV_ERR_CUDA if the copy itself fails. */
+dkv_status dkv_read_device_status(void* workspace, void* stream);
+
+/* Static description of a status code. */
+const char* dkv_status_string(int32_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DKV_H_ */

@@ -290,7 +290,10 @@ void oracle_attention(int B, int Hq, int Hkv, int N, int d, int S, int is_fp16,
 //   step     = fp16_rn( fp32( fp32(mx - mn) / 15 ) )          (15 steps, 16 levels)
 //   code_i   = 0 if step == 0, else
 //              clamp( rint_even( fp32( fp32(x_i - mn) / step ) ), 0, 15 )
-//   x^_i     = fp16_rn( code_i * step + mn )     (exact, rounded once to fp16)
+//   x^_i     = fp16_rn( code_i * step + mn )     (exact, rounded once to fp16),
+//              replaced by mx where it exceeds mx (the rounded step can carry
+//              the top codes past the group max, near the fp16 limit even to
+//              infinity; the reconstruction stays inside [mn, mx])
 // fp32(.) is one IEEE binary32 round-to-nearest-even operation.  Codes are
 // packed two per byte, channel 2i in the low nibble.
 // ---------------------------------------------------------------------------
@@ -347,12 +350,14 @@ void oracle_dequant4(int64_t rows, int d, const uint8_t* codes, const uint16_t* 
       const uint16_t lo = gmin[r * ng + g], hi = gmax[r * ng + g];
       const double step = static_cast<double>(group_step(lo, hi));
       const double mn = fp16_value(lo);
+      const double mx = fp16_value(hi);
       for (int i = 0; i < 64; ++i) {
         const int ch = g * 64 + i;
         const uint8_t byte = codes[r * (d / 2) + ch / 2];
         const int c = (ch & 1) ? (byte >> 4) : (byte & 0xf);
         // c * step + mn is exact in double (fp16-scale operands); round once.
-        x[r * d + ch] = fp16_round(static_cast<double>(c) * step + mn);
+        const uint16_t v = fp16_round(static_cast<double>(c) * step + mn);
+        x[r * d + ch] = (fp16_value(v) > mx) ? hi : v;
       }
     }
   });

@@ -1,0 +1,104 @@
+"""The C-ABI library loads, exports every symbol include/dkv.h declares, and
+rejects bad arguments on the host -- before any CUDA call, so this runs
+without a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from decode_attention_paged_kv_gb300 import build as b
+    b.build()
+    import decode_attention_paged_kv_gb300 as dkv
+    return dkv.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "dkv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dkv_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = _declared()
+    assert "dkv_decode_attn_select" in names and len(names) >= 8
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    assert L.dkv_status_string(0) == b"ok"
+    assert b"timeout" not in L.dkv_status_string(1)
+    assert L.dkv_status_string(8).startswith(b"device")
+    assert L.dkv_status_string(12345) == b"unknown status"
+
+
+def _params(**kw):
+    import decode_attention_paged_kv_gb300 as dkv
+    p = dkv._Params()
+    p.batch, p.num_q_heads, p.num_kv_heads, p.head_dim, p.seq_len, p.page_size = 2, 8, 2, 128, 1000, 16
+    p.q_stride_b, p.q_stride_h, p.o_stride_b, p.o_stride_h = 8 * 128, 128, 8 * 128, 128
+    p.scale = 0.088
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+def test_workspace_bytes_layout(L):
+    p = _params()
+    full = L.dkv_workspace_bytes(ctypes.byref(p), 0)
+    sel = L.dkv_workspace_bytes(ctypes.byref(p), 8)
+    # status + ml + o for ceil(63/64) = 1 chunk per row (16 rows, d=128)
+    assert full == 256 + 256 + ((16 * 128 * 4 + 255) // 256) * 256
+    assert sel > full
+    assert L.dkv_workspace_bytes(ctypes.byref(_params(head_dim=96)), 0) == 0
+    assert L.dkv_workspace_bytes(ctypes.byref(_params(num_q_heads=7)), 0) == 0
+    assert L.dkv_workspace_bytes(ctypes.byref(_params(page_size=32)), 0) == 0
+    assert L.dkv_workspace_bytes(None, 0) == 0
+
+
+def test_host_validation_before_launch(L):
+    import decode_attention_paged_kv_gb300 as dkv
+    kv = dkv._KV()
+    kv.format, kv.dtype, kv.data = 0, 0, 4096
+    kv.stride_b, kv.stride_h = 2 * 1000 * 128, 1000 * 128
+    p = _params()
+    ws = ctypes.c_void_p(1 << 20)
+    q = out = ctypes.c_void_p(1 << 16)
+    f = L.dkv_decode_attn_full
+    assert f(None, q, ctypes.byref(kv), ctypes.byref(kv), out, 2, ws, 1 << 20, None) == 1
+    assert f(ctypes.byref(p), None, ctypes.byref(kv), ctypes.byref(kv), out, 2, ws, 1 << 20, None) == 1
+    assert f(ctypes.byref(_params(head_dim=80)), q, ctypes.byref(kv), ctypes.byref(kv), out, 2,
+             ws, 1 << 20, None) == 5
+    assert f(ctypes.byref(_params(num_kv_heads=3)), q, ctypes.byref(kv), ctypes.byref(kv), out,
+             2, ws, 1 << 20, None) == 2
+    assert f(ctypes.byref(_params(num_q_heads=32, num_kv_heads=2)), q, ctypes.byref(kv),
+             ctypes.byref(kv), out, 2, ws, 1 << 20, None) == 5
+    assert f(ctypes.byref(p), ctypes.c_void_p((1 << 16) + 2), ctypes.byref(kv), ctypes.byref(kv),
+             out, 2, ws, 1 << 20, None) == 3
+    assert f(ctypes.byref(_params(q_stride_h=100)), q, ctypes.byref(kv), ctypes.byref(kv), out,
+             2, ws, 1 << 20, None) == 3
+    assert f(ctypes.byref(p), q, ctypes.byref(kv), ctypes.byref(kv), out, 2, ws, 16, None) == 6
+    assert f(ctypes.byref(p), q, ctypes.byref(kv), ctypes.byref(kv), out, 2, None, 1 << 20, None) == 6
+    assert f(ctypes.byref(p), q, ctypes.byref(kv), ctypes.byref(kv), out, 7, ws, 1 << 20, None) == 4
+    bad = dkv._KV()
+    bad.format, bad.dtype, bad.data = 0, 2, 4096  # fp32 cache
+    assert f(ctypes.byref(p), q, ctypes.byref(bad), ctypes.byref(kv), out, 2, ws, 1 << 20, None) == 4
+    assert f(ctypes.byref(_params(scale=0.0)), q, ctypes.byref(kv), ctypes.byref(kv), out, 2, ws,
+             1 << 20, None) == 2
+    s = L.dkv_decode_attn_select
+    assert s(ctypes.byref(p), q, ctypes.byref(kv), ctypes.byref(kv), None, None, 0, out, 2, None,
+             ws, 1 << 24, None) == 2
+    assert s(ctypes.byref(p), q, ctypes.byref(kv), ctypes.byref(kv), None, None, 4, out, 2, None,
+             ws, 1 << 24, None) == 1
+    assert L.dkv_kv_quant4(10, 100, q, q, q, q, None) == 2
+    assert L.dkv_kv_quant4(10, 128, None, q, q, q, None) == 1
+    assert L.dkv_kv_dequant4(10, 128, ctypes.c_void_p(3), q, q, q, None) == 3
+    assert L.dkv_kv_meta_build(ctypes.byref(p), ctypes.byref(kv), None, q, None) == 1
+    assert L.dkv_read_device_status(None, None) == 1

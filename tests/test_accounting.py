@@ -1,0 +1,35 @@
+"""The bench's byte accounting reproduces TinyServe's memory-fraction model
+("TinyServe: ...", 与全缓存注意力的归一化对比: 1/S + rho K S / L, rho = 1)."""
+
+import pytest
+
+from decode_attention_paged_kv_gb300 import accounting as acc
+
+
+@pytest.mark.parametrize("N,K,S,d", [(8192, 128, 16, 64), (32768, 128, 16, 128),
+                                     (32768, 614, 16, 128), (2048, 32, 16, 128)])
+def test_select_over_full_is_memory_fraction(N, K, S, d):
+    B, H = 3, 5  # MHA: each head gathers exactly its own K pages
+    gathered = B * H * K * S
+    q_out = B * H * d * 2 + B * H * d * 4
+    sel = acc.select_bytes(B, H, H, d, N, gathered, S=S) - q_out
+    full = acc.full_bytes(B, H, H, d, N) - q_out
+    assert sel / full == pytest.approx(acc.memory_fraction(S, K, N), rel=1e-12)
+
+
+def test_fraction_values():
+    # K = 0.3 P at L = 32K, S = 16: 1/16 + 0.3 = 0.3625 (about 2.8x less traffic)
+    P = 32768 // 16
+    assert acc.memory_fraction(16, int(0.3 * P), 32768) == pytest.approx(1 / 16 + 614 * 16 / 32768)
+    assert acc.memory_fraction(16, 128, 8192) == pytest.approx(0.3125)
+
+
+def test_full_bytes_workloads():
+    # Llama-3-8B GQA, B=16, N=32K: 2 GiB of K+V
+    kv = acc.full_bytes(16, 32, 8, 128, 32768) - 16 * 32 * 128 * 6
+    assert kv == 2 * 2 ** 30
+    # 1M tokens x 8 kv heads x d=128: 4 GiB
+    assert acc.full_bytes(1, 32, 8, 128, 1 << 20) - 32 * 128 * 6 == 4 * 2 ** 30
+    # 4-bit OPT-30B shape: codes + group min/max
+    b = acc.full_bytes(64, 56, 56, 128, 2048, q4=True) - 64 * 56 * 128 * 6
+    assert b == 2 * 64 * 56 * 2048 * (64 + 8)

@@ -1,0 +1,172 @@
+"""GPU parity at sizes the oracle finishes in seconds: several tiles per call,
+ragged tails, GQA and MHA, bf16 and fp16, strided views.
+
+Bars: metadata and 4-bit codes / group min / max / dequantised values
+bit-exact; attention outputs within 2e-3 max-abs (fp32 output); selections
+identical to the oracle's top-K except inside the 1e-5 relative band around
+the K-th score, and the sparse output compared with the oracle's attention
+over the pages the GPU selected.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import ATOL, check_selection, max_abs, require_cuda
+from workloads import Workload, bits, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return require_cuda()
+
+
+@pytest.fixture(scope="module")
+def dkv():
+    import decode_attention_paged_kv_gb300 as m
+    return m
+
+
+CASES = [
+    Workload("c0", B=1, Hq=16, Hkv=16, d=64, N=1024, top_k=16),
+    Workload("mha-ragged", B=2, Hq=4, Hkv=4, d=64, N=3001, top_k=40, kind="offset"),
+    Workload("gqa-hot", B=2, Hq=8, Hkv=2, d=128, N=5000, top_k=24, kind="hot"),
+    Workload("gqa8", B=1, Hq=16, Hkv=2, d=128, N=2100, top_k=10),
+    Workload("gqa2-fp16", B=3, Hq=4, Hkv=2, d=64, N=777, top_k=7, dtype="fp16"),
+    Workload("fp16-d128", B=1, Hq=8, Hkv=8, d=128, N=4096, top_k=33, dtype="fp16", kind="offset"),
+    Workload("one-token", B=2, Hq=4, Hkv=1, d=128, N=1, top_k=3),
+    Workload("one-page", B=1, Hq=2, Hkv=1, d=64, N=16, top_k=1),
+    Workload("page+1", B=1, Hq=2, Hkv=2, d=128, N=17, top_k=1),
+    Workload("long-chunks", B=1, Hq=4, Hkv=1, d=128, N=70000, top_k=64),
+]
+
+
+def _is16(w):
+    return int(w.dtype == "fp16")
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+def test_meta_bit_exact(w, dev, dkv):
+    _, K, _ = make_inputs(w, seed=11)
+    mn, mx = dkv.kv_meta_build(K.to(dev))
+    omn, omx = oracle.meta(bits(K), w.S, _is16(w))
+    assert np.array_equal(bits(mn.cpu()), omn)
+    assert np.array_equal(bits(mx.cpu()), omx)
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+def test_full_matches_oracle(w, dev, dkv):
+    q, K, V = make_inputs(w, seed=21)
+    scale = 1.0 / math.sqrt(w.d)
+    out = dkv.decode_attn_full(q.to(dev), K.to(dev), V.to(dev))
+    ref = oracle.attention(bits(q), bits(K), bits(V), w.S, scale, _is16(w))
+    assert max_abs(out, ref) <= ATOL
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+def test_select_matches_oracle(w, dev, dkv):
+    q, K, V = make_inputs(w, seed=31)
+    scale = 1.0 / math.sqrt(w.d)
+    qd, Kd, Vd = q.to(dev), K.to(dev), V.to(dev)
+    meta = dkv.kv_meta_build(Kd)
+    out, sel = dkv.decode_attn_select(qd, Kd, Vd, meta, w.top_k, return_selected=True)
+    sel = sel.cpu().numpy()
+    omn, omx = oracle.meta(bits(K), w.S, _is16(w))
+    r = oracle.scores(bits(q), omn, omx, _is16(w))
+    check_selection(sel.reshape(-1, sel.shape[-1]), r.reshape(-1, r.shape[-1]), w.top_k)
+    ref = oracle.attention(bits(q), bits(K), bits(V), w.S, scale, _is16(w), sel=sel)
+    assert max_abs(out, ref) <= ATOL
+
+
+@pytest.mark.parametrize("w", CASES[:4], ids=lambda w: w.name)
+def test_select_all_pages_equals_full(w, dev, dkv):
+    q, K, V = make_inputs(w, seed=41)
+    qd, Kd, Vd = q.to(dev), K.to(dev), V.to(dev)
+    meta = dkv.kv_meta_build(Kd)
+    out, sel = dkv.decode_attn_select(qd, Kd, Vd, meta, w.P + 5, return_selected=True)
+    assert sel.shape[-1] == w.P
+    assert torch.equal(sel.cpu(), torch.arange(w.P, dtype=torch.int32).expand_as(sel.cpu()))
+    full = dkv.decode_attn_full(qd, Kd, Vd)
+    assert max_abs(out, full) <= ATOL
+    ref = oracle.attention(bits(q), bits(K), bits(V), w.S, 1 / math.sqrt(w.d), _is16(w))
+    assert max_abs(out, ref) <= ATOL
+
+
+def test_headwise_equals_all_heads_bitwise(dev, dkv):
+    # One kv head at a time (HeadInfer) through strided views == the all-heads call.
+    w = Workload("hw", B=2, Hq=8, Hkv=4, d=128, N=9000)
+    q, K, V = (t.to(dev) for t in make_inputs(w, seed=51))
+    full = dkv.decode_attn_full(q, K, V)
+    for h in range(w.Hkv):
+        part = dkv.decode_attn_full(q[:, 2 * h:2 * h + 2], K[:, h:h + 1], V[:, h:h + 1])
+        assert torch.equal(part, full[:, 2 * h:2 * h + 2])
+
+
+def test_strided_query_and_output(dev, dkv):
+    w = Workload("st", B=2, Hq=4, Hkv=2, d=64, N=600)
+    q, K, V = make_inputs(w, seed=61)
+    big_q = torch.zeros(2, 6, 64, dtype=q.dtype)
+    big_q[:, 1:5] = q
+    qd = big_q.to(dev)[:, 1:5]
+    out_big = torch.full((2, 7, 64), float("nan"), device=dev)
+    dkv.decode_attn_full(qd, K.to(dev), V.to(dev), out=out_big[:, 2:6])
+    ref = oracle.attention(bits(q), bits(K), bits(V), w.S, 1 / 8, 0)
+    assert max_abs(out_big[:, 2:6], ref) <= ATOL
+    assert torch.isnan(out_big[:, :2]).all() and torch.isnan(out_big[:, 6:]).all()
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float16])
+def test_half_outputs(out_dtype, dev, dkv):
+    w = Workload("ho", B=2, Hq=8, Hkv=2, d=128, N=2000)
+    q, K, V = make_inputs(w, seed=71)
+    out = dkv.decode_attn_full(q.to(dev), K.to(dev), V.to(dev), out_dtype=out_dtype)
+    ref = oracle.attention(bits(q), bits(K), bits(V), w.S, 1 / math.sqrt(128), 0)
+    got = out.float().cpu().double().numpy()
+    eps = 2.0 ** -9 if out_dtype == torch.bfloat16 else 2.0 ** -12
+    assert np.all(np.abs(got - ref) <= ATOL + eps * np.abs(ref))
+
+
+def test_custom_scale(dev, dkv):
+    w = Workload("sc", B=1, Hq=4, Hkv=4, d=64, N=500)
+    q, K, V = make_inputs(w, seed=81)
+    out = dkv.decode_attn_full(q.to(dev), K.to(dev), V.to(dev), scale=0.02)
+    ref = oracle.attention(bits(q), bits(K), bits(V), w.S, 0.02, 0)
+    assert max_abs(out, ref) <= ATOL
+
+
+def test_quant4_dequant4_bit_exact(dev, dkv):
+    rng = np.random.default_rng(5)
+    rows, d = 3000, 128
+    x = rng.standard_normal((rows, d)) * np.exp2(rng.integers(-20, 12, (rows, 1)))
+    x[0] = 0.0
+    x[1] = -0.0
+    x[1, 7] = 0.0
+    x[2] = 1.5
+    x[3, :64] = np.arange(64)
+    x[4] = np.clip(rng.standard_normal(d) * 4e4, -65504, 65504)  # finite, near the fp16 max
+    xb = np.asarray(x, np.float64).astype(np.float16).view(np.uint16)
+    xt = torch.from_numpy(xb.view(np.int16)).view(torch.float16)
+    q4 = dkv.kv_quant4(xt.to(dev))
+    codes, gmin, gmax = oracle.quant4(xb)
+    assert np.array_equal(q4.codes.cpu().numpy(), codes)
+    assert np.array_equal(bits(q4.gmin.cpu()), gmin)
+    assert np.array_equal(bits(q4.gmax.cpu()), gmax)
+    xh = dkv.kv_dequant4(q4)
+    assert np.array_equal(bits(xh.cpu()), oracle.dequant4(codes, gmin, gmax))
+
+
+def test_q4_meta_bit_exact(dev, dkv):
+    w = Workload("q4m", B=2, Hq=3, Hkv=3, d=128, N=1000, dtype="fp16")
+    _, K, _ = make_inputs(w, seed=91)
+    q4 = dkv.kv_quant4(K.to(dev).contiguous())
+    mn, mx = dkv.kv_meta_build(q4)
+    codes, gmin, gmax = oracle.quant4(bits(K))
+    kh = oracle.dequant4(codes, gmin, gmax)
+    omn, omx = oracle.meta(kh, w.S, 1)
+    assert np.array_equal(bits(mn.cpu()), omn)
+    assert np.array_equal(bits(mx.cpu()), omx)

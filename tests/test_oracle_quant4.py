@@ -96,3 +96,18 @@ def test_signed_zero_group():
     assert np.all(codes == 0)
     xh = oracle.dequant4(codes, gmin, gmax)
     assert np.all(_v(xh) == 0.0)
+
+
+def test_reconstruction_saturates_at_group_max():
+    # (65504 - 0) / 15 = 4366.93 rounds to the fp16 step 4368, and 15 * 4368 =
+    # 65520 would round to infinity: the reconstruction is held at the max.
+    x = np.zeros((1, 64))
+    x[0, 1] = 65504.0
+    x[0, 2:] = np.linspace(0, 65504, 62)
+    xb = _f16(x)
+    codes, gmin, gmax = oracle.quant4(xb)
+    xh = _v(oracle.dequant4(codes, gmin, gmax))
+    assert np.all(np.isfinite(xh))
+    assert xh[0, 1] == 65504.0
+    assert np.all((xh >= 0) & (xh <= 65504.0))
+    assert np.all(np.abs(xh - _v(xb)) <= 65504.0 / 30 * (1 + 2.0 ** -9) + 16)

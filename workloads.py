@@ -5,7 +5,9 @@ input generators only -- none of the method's arithmetic (no metadata, scores,
 selection, attention or quantisation) -- so that the CUDA path and the CPU
 oracle can be fed identical inputs without sharing any code that computes.
 
-Every tensor is drawn on the CPU from ``torch.Generator().manual_seed(seed)``
+Every tensor is drawn from ``torch.Generator(device).manual_seed(seed)`` -- on
+the CPU for the small parity cases, on the GPU (torch's Philox generator) for
+the full-size workloads, where a CPU draw of 2^31 normals would take minutes --
 and rounded to its storage dtype with round-to-nearest-even.  The workloads
 stand in for the pages' LongBench / 32K-prompt serving runs (TinyServe) and
 the 1M-token Llama-3-8B runs (HeadInfer) with synthetic data of the same
@@ -77,15 +79,15 @@ def by_name(name: str) -> Workload:
 def _randn(gen: torch.Generator, shape, chunk_elems: int = 1 << 26) -> torch.Tensor:
     """Standard normals in fp32, drawn in fixed-size chunks (bounded memory)."""
     n = math.prod(shape)
-    out = torch.empty(n, dtype=torch.float32)
+    out = torch.empty(n, dtype=torch.float32, device=gen.device)
     for s in range(0, n, chunk_elems):
         e = min(n, s + chunk_elems)
-        out[s:e] = torch.randn(e - s, generator=gen, dtype=torch.float32)
+        out[s:e] = torch.randn(e - s, generator=gen, dtype=torch.float32, device=gen.device)
     return out.view(*shape)
 
 
-def make_inputs(w: Workload, seed: int):
-    """Return (q [B,Hq,d], K [B,Hkv,N,d], V [B,Hkv,N,d]) CPU tensors in w's dtype.
+def make_inputs(w: Workload, seed: int, device="cpu"):
+    """Return (q [B,Hq,d], K [B,Hkv,N,d], V [B,Hkv,N,d]) in w's dtype on `device`.
 
     kinds:
       normal  q, K, V ~ N(0, 1).
@@ -96,11 +98,13 @@ def make_inputs(w: Workload, seed: int):
               shifted by 2 * qhat, qhat = the unit-length mean of that group's
               query heads (pages that the group's queries should find).
     """
-    gen = torch.Generator().manual_seed(int(seed))
+    gen = torch.Generator(device=device).manual_seed(int(seed))
     dt = w.torch_dtype
     q = _randn(gen, (w.B, w.Hq, w.d))
-    K = _randn(gen, (w.B, w.Hkv, w.N, w.d))
-    V = _randn(gen, (w.B, w.Hkv, w.N, w.d))
+    K = _randn(gen, (w.B, w.Hkv, w.N, w.d)).to(dt) if w.kind == "normal" else \
+        _randn(gen, (w.B, w.Hkv, w.N, w.d))
+    V = _randn(gen, (w.B, w.Hkv, w.N, w.d)).to(dt) if w.kind == "normal" else \
+        _randn(gen, (w.B, w.Hkv, w.N, w.d))
     if w.kind == "offset":
         K += 0.5 * _randn(gen, (w.B, w.Hkv, 1, w.d))
         V += 0.5 * _randn(gen, (w.B, w.Hkv, 1, w.d))
@@ -108,11 +112,14 @@ def make_inputs(w: Workload, seed: int):
         n_hot = int(round(0.02 * w.P))
         qg = q.view(w.B, w.Hkv, w.G, w.d).mean(dim=2)
         qhat = qg / qg.norm(dim=-1, keepdim=True).clamp_min(1e-30)
+        # page-level mask of the hot pages, then one broadcast add per token
+        hot = torch.zeros(w.B, w.Hkv, w.P, dtype=torch.float32, device=K.device)
         for b in range(w.B):
             for h in range(w.Hkv):
-                pages = torch.randperm(w.P, generator=gen)[:n_hot]
-                for j in pages.tolist():
-                    K[b, h, j * w.S:(j + 1) * w.S, :] += 2.0 * qhat[b, h]
+                pages = torch.randperm(w.P, generator=gen, device=gen.device)[:n_hot]
+                hot[b, h, pages] = 1.0
+        tok_hot = hot.repeat_interleave(w.S, dim=2)[:, :, :w.N]
+        K += 2.0 * tok_hot.unsqueeze(-1) * qhat.unsqueeze(2)
     elif w.kind != "normal":
         raise ValueError(w.kind)
     return q.to(dt), K.to(dt), V.to(dt)
