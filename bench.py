@@ -51,6 +51,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["dkv", "reference"], default="dkv")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch (small cases for ncu captures)")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the 1M-token head-wise and e2e / CPU-baseline legs")
     return ap.parse_args()
@@ -117,7 +119,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -181,6 +183,8 @@ def run_dkv(args, rank, world, local):
     torch.cuda.set_device(dev)
     w = by_name(args.workload)
     widx = [x.name for x in WORKLOADS].index(w.name)
+    if args.batch:
+        w = w.replace(B=args.batch)
     if w.q4:
         raise SystemExit("the 4-bit workload is a parity case; the bench times the dense path")
     q, K, V = make_inputs(w, seed=42 + widx + 1000 * rank, device=dev)

@@ -26,13 +26,17 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // Byte offsets of the regions inside a caller-provided workspace.
 struct WsLayout {
   size_t status = 0;     // u32 device status word (first 256 bytes)
+  size_t tickets = 0;    // u32 [B * Hkv * (n_groups + 1)], zero between calls
   size_t part_ml = 0;    // [B, Hq, n_chunks, 2] fp32
   size_t part_o = 0;     // [B, Hq, n_chunks, d] fp32
+  size_t part2_ml = 0;   // [B, Hq, n_groups, 2] fp32
+  size_t part2_o = 0;    // [B, Hq, n_groups, d] fp32
   size_t scores = 0;     // sparse: [B, Hq, P] fp32
   size_t selected = 0;   // sparse: [B, Hq, kk] int32 (used when the caller passes none)
   size_t bitmaps = 0;    // sparse: [B, Hq, W32] u32
   size_t total = 0;
-  int n_chunks = 0, kk = 0, W32 = 0;
+  int n_chunks = 0, n_groups = 0, pages_per_chunk = 0, kk = 0, W32 = 0;
+  bool ok = true;        // false: the sizes exceed what the kernels cover
 };
 
 WsLayout layout_for(const dkv_params& p, int top_k) {
@@ -40,15 +44,25 @@ WsLayout layout_for(const dkv_params& p, int top_k) {
   const int d = p.head_dim;
   const int64_t P = ceil_div(p.seq_len, p.page_size);
   const int64_t rows = static_cast<int64_t>(p.batch) * p.num_q_heads;
+  const int64_t units = static_cast<int64_t>(p.batch) * p.num_kv_heads;
   size_t off = kAlign;  // status word
   if (top_k <= 0) {
-    L.n_chunks = static_cast<int>(ceil_div(P, dkv::full_pages_per_chunk(d)));
+    L.pages_per_chunk = dkv::full_pages_per_chunk(P, d);
+    L.n_chunks = static_cast<int>(ceil_div(P, L.pages_per_chunk));
   } else {
     const int G = p.num_q_heads / p.num_kv_heads;
     L.kk = static_cast<int>(top_k < P ? top_k : P);
     L.W32 = static_cast<int>(ceil_div(P, 32));
     const int64_t union_max = (static_cast<int64_t>(G) * L.kk < P) ? G * L.kk : P;
-    L.n_chunks = static_cast<int>(ceil_div(union_max, dkv::select_pages_per_chunk(d)));
+    L.pages_per_chunk = dkv::select_pages_per_chunk(union_max, d);
+    if (L.pages_per_chunk > dkv::kMaxSelectList) L.ok = false;
+    L.n_chunks = static_cast<int>(ceil_div(union_max, L.pages_per_chunk));
+  }
+  if (L.n_chunks > dkv::kMaxChunks) L.ok = false;
+  L.n_groups = static_cast<int>(ceil_div(L.n_chunks, dkv::kGroup));
+  L.tickets = off;
+  off = align_up(off + sizeof(uint32_t) * units * (L.n_groups + 1));
+  if (top_k > 0) {
     L.scores = off;
     off = align_up(off + sizeof(float) * rows * P);
     L.selected = off;
@@ -60,6 +74,10 @@ WsLayout layout_for(const dkv_params& p, int top_k) {
   off = align_up(off + sizeof(float) * 2 * rows * L.n_chunks);
   L.part_o = off;
   off = align_up(off + sizeof(float) * static_cast<size_t>(d) * rows * L.n_chunks);
+  L.part2_ml = off;
+  off = align_up(off + sizeof(float) * 2 * rows * L.n_groups);
+  L.part2_o = off;
+  off = align_up(off + sizeof(float) * static_cast<size_t>(d) * rows * L.n_groups);
   L.total = off;
   return L;
 }
@@ -166,7 +184,8 @@ extern "C" {
 
 size_t dkv_workspace_bytes(const dkv_params* p, int32_t top_k) {
   if (check_params(p) != DKV_OK || top_k < 0) return 0;
-  return layout_for(*p, top_k).total;
+  const WsLayout L = layout_for(*p, top_k);
+  return L.ok ? L.total : 0;
 }
 
 dkv_status dkv_kv_meta_build(const dkv_params* p, const dkv_kv* K, void* meta_min,
@@ -207,11 +226,42 @@ static dkv_status attn_common(const dkv_params* p, const void* q, const dkv_kv* 
   if (out_dtype != DKV_FP32 && out_dtype != DKV_BF16 && out_dtype != DKV_FP16)
     return DKV_ERR_DTYPE;
   if (K->format == DKV_KV_Q4G64) return DKV_ERR_UNSUPPORTED;  // dense caches only for now
+  if (!L.ok) return DKV_ERR_UNSUPPORTED;
   if (workspace == nullptr) return DKV_ERR_WORKSPACE;
   if (!aligned16(workspace)) return DKV_ERR_ALIGN;
   if (workspace_bytes < L.total) return DKV_ERR_WORKSPACE;
   (void)top_k;
   return DKV_OK;
+}
+
+static dkv::AttnArgs attn_args(const dkv_params* p, const void* q, const WsLayout& L,
+                               uint8_t* ws, void* out, int32_t out_dtype) {
+  dkv::AttnArgs a{};
+  a.q = q;
+  a.q_sb = p->q_stride_b;
+  a.q_sh = p->q_stride_h;
+  a.B = p->batch;
+  a.Hq = p->num_q_heads;
+  a.Hkv = p->num_kv_heads;
+  a.G = p->num_q_heads / p->num_kv_heads;
+  a.N = p->seq_len;
+  a.P = static_cast<int>(ceil_div(p->seq_len, p->page_size));
+  a.scale_log2 = p->scale * 1.4426950408889634f;
+  a.pages_per_chunk = L.pages_per_chunk;
+  a.n_chunks = L.n_chunks;
+  a.n_groups = L.n_groups;
+  a.part_ml = reinterpret_cast<float*>(ws + L.part_ml);
+  a.part_o = reinterpret_cast<float*>(ws + L.part_o);
+  a.part2_ml = reinterpret_cast<float*>(ws + L.part2_ml);
+  a.part2_o = reinterpret_cast<float*>(ws + L.part2_o);
+  a.tickets = reinterpret_cast<uint32_t*>(ws + L.tickets);
+  a.out = out;
+  a.out_dtype = out_code(out_dtype);
+  a.o_sb = p->o_stride_b;
+  a.o_sh = p->o_stride_h;
+  a.status = reinterpret_cast<uint32_t*>(ws + L.status);
+  a.wait_limit_ns = (p->flags & DKV_FLAG_FORCE_TIMEOUT) ? 0 : kWaitLimitNs;
+  return a;
 }
 
 dkv_status dkv_decode_attn_full(const dkv_params* p, const void* q, const dkv_kv* K,
@@ -226,37 +276,10 @@ dkv_status dkv_decode_attn_full(const dkv_params* p, const void* q, const dkv_kv
   if (!encode_page_map(&mk, p, K) || !encode_page_map(&mv, p, V)) return DKV_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  dkv::AttnArgs a{};
-  a.q = q;
-  a.q_sb = p->q_stride_b;
-  a.q_sh = p->q_stride_h;
-  a.B = p->batch;
-  a.Hq = p->num_q_heads;
-  a.Hkv = p->num_kv_heads;
-  a.G = p->num_q_heads / p->num_kv_heads;
-  a.N = p->seq_len;
-  a.P = static_cast<int>(ceil_div(p->seq_len, p->page_size));
-  a.scale_log2 = p->scale * 1.4426950408889634f;
-  a.pages_per_chunk = dkv::full_pages_per_chunk(p->head_dim);
-  a.n_chunks = L.n_chunks;
-  a.part_ml = reinterpret_cast<float*>(ws + L.part_ml);
-  a.part_o = reinterpret_cast<float*>(ws + L.part_o);
-  a.status = reinterpret_cast<uint32_t*>(ws + L.status);
-  a.wait_limit_ns = (p->flags & DKV_FLAG_FORCE_TIMEOUT) ? 0 : kWaitLimitNs;
+  const dkv::AttnArgs a = attn_args(p, q, L, ws, out, out_dtype);
   const bool f16 = K->dtype == DKV_FP16;
   dim3 grid(L.n_chunks, p->num_kv_heads, p->batch);
-  if ((st = cuda_status(dkv::launch_attn(p->head_dim, f16, false, a, mk, mv, grid, s))) != DKV_OK)
-    return st;
-  dkv::CombineArgs c{};
-  c.part_ml = a.part_ml;
-  c.part_o = a.part_o;
-  c.n_chunks = L.n_chunks;
-  c.Hq = p->num_q_heads;
-  c.out = out;
-  c.out_dtype = out_code(out_dtype);
-  c.o_sb = p->o_stride_b;
-  c.o_sh = p->o_stride_h;
-  return cuda_status(dkv::launch_combine(p->head_dim, c, p->batch * p->num_q_heads, s));
+  return cuda_status(dkv::launch_attn(p->head_dim, f16, false, a, mk, mv, grid, s));
 }
 
 dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_kv* K,
@@ -306,38 +329,11 @@ dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_
   ta.W32 = L.W32;
   if ((st = cuda_status(dkv::launch_topk(ta, s))) != DKV_OK) return st;
 
-  dkv::AttnArgs a{};
-  a.q = q;
-  a.q_sb = p->q_stride_b;
-  a.q_sh = p->q_stride_h;
-  a.B = p->batch;
-  a.Hq = p->num_q_heads;
-  a.Hkv = p->num_kv_heads;
-  a.G = G;
-  a.N = p->seq_len;
-  a.P = P;
-  a.scale_log2 = p->scale * 1.4426950408889634f;
-  a.pages_per_chunk = dkv::select_pages_per_chunk(p->head_dim);
-  a.n_chunks = L.n_chunks;
-  a.part_ml = reinterpret_cast<float*>(ws + L.part_ml);
-  a.part_o = reinterpret_cast<float*>(ws + L.part_o);
+  dkv::AttnArgs a = attn_args(p, q, L, ws, out, out_dtype);
   a.bitmaps = ta.bitmaps;
   a.W32 = L.W32;
-  a.status = reinterpret_cast<uint32_t*>(ws + L.status);
-  a.wait_limit_ns = (p->flags & DKV_FLAG_FORCE_TIMEOUT) ? 0 : kWaitLimitNs;
   dim3 grid(L.n_chunks, p->num_kv_heads, p->batch);
-  if ((st = cuda_status(dkv::launch_attn(p->head_dim, f16, true, a, mk, mv, grid, s))) != DKV_OK)
-    return st;
-  dkv::CombineArgs c{};
-  c.part_ml = a.part_ml;
-  c.part_o = a.part_o;
-  c.n_chunks = L.n_chunks;
-  c.Hq = p->num_q_heads;
-  c.out = out;
-  c.out_dtype = out_code(out_dtype);
-  c.o_sb = p->o_stride_b;
-  c.o_sh = p->o_stride_h;
-  return cuda_status(dkv::launch_combine(p->head_dim, c, p->batch * p->num_q_heads, s));
+  return cuda_status(dkv::launch_attn(p->head_dim, f16, true, a, mk, mv, grid, s));
 }
 
 dkv_status dkv_kv_quant4(int64_t rows, int32_t d, const void* x, void* codes, void* gmin,

@@ -6,22 +6,39 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace dkv {
 
 constexpr int kPage = 16;             // tokens per page (S)
 constexpr int kConsumerWarps = 4;     // attention: warps that compute
 constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
 
-// Pages one attention CTA streams in the exact path.  Depends only on d, so the
-// sequence chunking (and hence every result bit) is the same whether the call
-// covers all kv heads or one.  512 KiB of K+V per CTA.
-constexpr int full_pages_per_chunk(int d) { return d == 128 ? 64 : 128; }
-// Selected pages one attention CTA gathers in the sparse path (128 KiB K+V).
-constexpr int select_pages_per_chunk(int d) { return d == 128 ? 16 : 32; }
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Split-K partials are merged in groups of kGroup chunks, then the groups.
+constexpr int kGroup = 16;
+constexpr int kMaxChunks = kGroup * kGroup;  // per (batch, kv head)
+
+// Pages one attention CTA streams in the exact path: 512 KiB of K+V at least,
+// more for long contexts so a (batch, kv head) never has more than kMaxChunks
+// chunks.  Depends only on (P, d) -- not on the batch or the number of kv heads
+// in the call -- so one kv head at a time gives bitwise the all-heads result.
+inline int full_pages_per_chunk(int64_t P, int d) {
+  const int64_t base = d == 128 ? 64 : 128;
+  const int64_t need = ceil_div(P, kMaxChunks);
+  return static_cast<int>(need > base ? ceil_div(need, 16) * 16 : base);
+}
+// Selected pages one attention CTA gathers in the sparse path (256 KiB K+V at
+// least), from a union of at most `union_max` pages per (batch, kv head).
+constexpr int kMaxSelectList = 256;  // shared-memory page list capacity
+inline int select_pages_per_chunk(int64_t union_max, int d) {
+  const int64_t base = d == 128 ? 32 : 64;
+  const int64_t need = ceil_div(union_max, kMaxChunks);
+  return static_cast<int>(need > base ? need : base);
+}
 // Pipeline depth: pages of K+V in flight per CTA (96 KiB of shared memory).
 constexpr int attn_stages(int d) { return d == 128 ? 12 : 24; }
-
-inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 struct AttnArgs {
   const void* q;
@@ -29,23 +46,20 @@ struct AttnArgs {
   int B, Hq, Hkv, G, N, P;
   float scale_log2;            // softmax scale * log2(e)
   int pages_per_chunk;
-  int n_chunks;
-  float* part_ml;              // [B, Hq, n_chunks, 2]  (running max in log2 units, sum)
+  int n_chunks;                // per (batch, kv head), <= kMaxChunks
+  int n_groups;                // ceil(n_chunks / kGroup)
+  float* part_ml;              // [B, Hq, n_chunks, 2]  (max in log2 units, sum)
   float* part_o;               // [B, Hq, n_chunks, d]  unnormalised
+  float* part2_ml;             // [B, Hq, n_groups, 2]
+  float* part2_o;              // [B, Hq, n_groups, d]
+  uint32_t* tickets;           // [B * Hkv * n_groups] then [B * Hkv]; zero between calls
   const uint32_t* bitmaps;     // sparse path: [B, Hq, W32] selected-page bits
   int W32;
-  uint32_t* status;
-  uint64_t wait_limit_ns;
-};
-
-struct CombineArgs {
-  const float* part_ml;
-  const float* part_o;
-  int n_chunks;
-  int Hq;
   void* out;
   int out_dtype;               // 0 bf16, 1 fp16, 2 fp32
   int64_t o_sb, o_sh;
+  uint32_t* status;
+  uint64_t wait_limit_ns;
 };
 
 struct ScoreArgs {
@@ -75,10 +89,28 @@ struct MetaArgs {
   void* meta_max;
 };
 
+// Launch `kern` with programmatic stream serialisation, so it may begin while
+// the previous kernel in the stream drains (every kernel here calls
+// griddep_wait() before touching data a predecessor could have written).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 // Launchers: return the launch's cudaError_t.
 cudaError_t launch_attn(int d, bool f16, bool sparse, const AttnArgs& a, const CUtensorMap& mk,
                         const CUtensorMap& mv, dim3 grid, cudaStream_t s);
-cudaError_t launch_combine(int d, const CombineArgs& a, int rows, cudaStream_t s);
 cudaError_t launch_score(int d, bool f16, const ScoreArgs& a, cudaStream_t s);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
 cudaError_t launch_meta(bool q4, bool f16, const MetaArgs& a, cudaStream_t s);

@@ -27,6 +27,8 @@ constexpr int kMetaThreads = 256;
 
 template <bool Q4>
 __global__ void __launch_bounds__(kMetaThreads) meta_kernel(const MetaArgs a) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int vpr = a.d / 8;  // 16-byte vectors per row
   const int64_t total = static_cast<int64_t>(a.B) * a.Hkv * a.P * vpr;
   for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
@@ -103,6 +105,8 @@ __global__ void __launch_bounds__(kMetaThreads) meta_kernel(const MetaArgs a) {
 // loop advances whole blocks, so the 8 lanes of a group always shuffle together.
 __global__ void __launch_bounds__(256) quant4_kernel(int64_t groups, const __half* x,
                                                      uint8_t* codes, __half* gmin, __half* gmax) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int64_t total = groups * 8;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.x; t0 < total; t0 += stride) {
@@ -156,6 +160,8 @@ __global__ void __launch_bounds__(256) quant4_kernel(int64_t groups, const __hal
 __global__ void __launch_bounds__(256) dequant4_kernel(int64_t groups, const uint8_t* codes,
                                                        const __half* gmin, const __half* gmax,
                                                        __half* x) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int64_t total = groups * 8;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
@@ -180,28 +186,25 @@ int grid_for(int64_t threads, int block) {
 cudaError_t launch_meta(bool q4, bool f16, const MetaArgs& a, cudaStream_t s) {
   (void)f16;  // min / max on order-preserving keys: identical code for bf16 and fp16
   const int64_t work = static_cast<int64_t>(a.B) * a.Hkv * a.P * (a.d / 8);
-  const int grid = grid_for(work, kMetaThreads);
-  if (q4) meta_kernel<true><<<grid, kMetaThreads, 0, s>>>(a);
-  else meta_kernel<false><<<grid, kMetaThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  const dim3 grid(grid_for(work, kMetaThreads)), block(kMetaThreads);
+  return q4 ? launch_pdl(meta_kernel<true>, grid, block, 0, s, a)
+            : launch_pdl(meta_kernel<false>, grid, block, 0, s, a);
 }
 
 cudaError_t launch_quant4(int64_t rows, int d, const void* x, void* codes, void* gmin,
                           void* gmax, cudaStream_t s) {
   const int64_t groups = rows * (d / 64);
-  quant4_kernel<<<grid_for(groups * 8, 256), 256, 0, s>>>(
-      groups, static_cast<const __half*>(x), static_cast<uint8_t*>(codes),
-      static_cast<__half*>(gmin), static_cast<__half*>(gmax));
-  return cudaGetLastError();
+  return launch_pdl(quant4_kernel, dim3(grid_for(groups * 8, 256)), dim3(256), 0, s, groups,
+                    static_cast<const __half*>(x), static_cast<uint8_t*>(codes),
+                    static_cast<__half*>(gmin), static_cast<__half*>(gmax));
 }
 
 cudaError_t launch_dequant4(int64_t rows, int d, const void* codes, const void* gmin,
                             const void* gmax, void* x, cudaStream_t s) {
   const int64_t groups = rows * (d / 64);
-  dequant4_kernel<<<grid_for(groups * 8, 256), 256, 0, s>>>(
-      groups, static_cast<const uint8_t*>(codes), static_cast<const __half*>(gmin),
-      static_cast<const __half*>(gmax), static_cast<__half*>(x));
-  return cudaGetLastError();
+  return launch_pdl(dequant4_kernel, dim3(grid_for(groups * 8, 256)), dim3(256), 0, s, groups,
+                    static_cast<const uint8_t*>(codes), static_cast<const __half*>(gmin),
+                    static_cast<const __half*>(gmax), static_cast<__half*>(x));
 }
 
 }  // namespace dkv

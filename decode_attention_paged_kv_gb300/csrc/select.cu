@@ -47,6 +47,8 @@ __global__ void __launch_bounds__(kScoreWarps * 32) score_kernel(const ScoreArgs
   const int g = lane >> 2, t4 = lane & 3;
   const int b = blockIdx.z, kvh = blockIdx.y;
   const int page0 = blockIdx.x * kScorePagesPerCta + warp * 16;
+  griddep_launch_dependents();
+  griddep_wait();
   if (page0 >= a.P) return;
 
   // Contraction index k (0..2d) runs over the concatenation [M | m]; thread
@@ -111,6 +113,7 @@ __device__ __forceinline__ uint32_t score_key(float f) {
 }
 
 constexpr int kTopkThreads = 256;
+constexpr size_t kTopkSmemKeyBytes = 192 * 1024;  // rows of up to 49152 pages
 
 // Block-wide exclusive prefix count of `flag`; *total gets the block total.
 __device__ __forceinline__ int block_excl_count(bool flag, int* warp_tot, int* total) {
@@ -131,13 +134,34 @@ __device__ __forceinline__ int block_excl_count(bool flag, int* warp_tot, int* t
   return before + in_warp;
 }
 
+// Keys of one row: staged in shared memory once when they fit, else re-read
+// (order-preserving transform applied on the fly) from global memory.
+template <bool SMEM>
+struct RowKeys {
+  const float* r;
+  const uint32_t* s;
+  __device__ __forceinline__ uint32_t operator()(int j) const {
+    if constexpr (SMEM) return s[j];
+    return score_key(r[j]);
+  }
+};
+
+template <bool SMEM>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
+  extern __shared__ uint32_t s_keys[];
   __shared__ uint32_t hist[256];
   __shared__ int warp_tot[kTopkThreads / 32];
   __shared__ uint32_t s_digit, s_above;
   const int row = blockIdx.x;
-  const float* r = a.scores + static_cast<int64_t>(row) * a.P;
   const int tid = threadIdx.x;
+  griddep_launch_dependents();
+  griddep_wait();  // the scores come from the previous kernel
+  const float* r = a.scores + static_cast<int64_t>(row) * a.P;
+  if constexpr (SMEM) {
+#pragma unroll 8
+    for (int j = tid; j < a.P; j += kTopkThreads) s_keys[j] = score_key(__ldcg(r + j));
+  }
+  const RowKeys<SMEM> key{r, s_keys};
 
   uint32_t prefix = 0, mask = 0;
   int need = a.kk;  // still to choose among keys matching `prefix` under `mask`
@@ -146,7 +170,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
     hist[tid] = 0;
     __syncthreads();
     for (int j = tid; j < a.P; j += kTopkThreads) {
-      const uint32_t k = score_key(r[j]);
+      const uint32_t k = key(j);
       if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 0xffu], 1u);
     }
     __syncthreads();
@@ -189,7 +213,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
   int eq_before = 0, sel_before = 0;
   for (int base = 0; base < a.P; base += kTopkThreads) {
     const int j = base + tid;
-    const uint32_t k = (j < a.P) ? (score_key(r[j]) & mask) : 0u;
+    const uint32_t k = (j < a.P) ? (key(j) & mask) : 0u;
     const bool gt = (j < a.P) && k > prefix;
     const bool eq = (j < a.P) && k == prefix;
     int eq_tot, sel_tot;
@@ -209,19 +233,25 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
 
 cudaError_t launch_score(int d, bool f16, const ScoreArgs& a, cudaStream_t s) {
   dim3 grid(static_cast<unsigned>(ceil_div(a.P, kScorePagesPerCta)), a.Hkv, a.B);
+  dim3 block(kScoreWarps * 32);
   if (d == 128) {
-    if (f16) score_kernel<128, true><<<grid, kScoreWarps * 32, 0, s>>>(a);
-    else score_kernel<128, false><<<grid, kScoreWarps * 32, 0, s>>>(a);
-  } else {
-    if (f16) score_kernel<64, true><<<grid, kScoreWarps * 32, 0, s>>>(a);
-    else score_kernel<64, false><<<grid, kScoreWarps * 32, 0, s>>>(a);
+    return f16 ? launch_pdl(score_kernel<128, true>, grid, block, 0, s, a)
+               : launch_pdl(score_kernel<128, false>, grid, block, 0, s, a);
   }
-  return cudaGetLastError();
+  return f16 ? launch_pdl(score_kernel<64, true>, grid, block, 0, s, a)
+             : launch_pdl(score_kernel<64, false>, grid, block, 0, s, a);
 }
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
-  topk_kernel<<<a.rows, kTopkThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  const size_t key_bytes = sizeof(uint32_t) * static_cast<size_t>(a.P);
+  if (key_bytes <= kTopkSmemKeyBytes) {
+    cudaError_t e = cudaFuncSetAttribute(topk_kernel<true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kTopkSmemKeyBytes));
+    if (e != cudaSuccess) return e;
+    return launch_pdl(topk_kernel<true>, dim3(a.rows), dim3(kTopkThreads), key_bytes, s, a);
+  }
+  return launch_pdl(topk_kernel<false>, dim3(a.rows), dim3(kTopkThreads), 0, s, a);
 }
 
 }  // namespace dkv

@@ -107,6 +107,27 @@ def test_headwise_equals_all_heads_bitwise(dev, dkv):
         assert torch.equal(part, full[:, 2 * h:2 * h + 2])
 
 
+def test_workspace_reuse_across_calls(dev, dkv):
+    # One zero-filled workspace serves calls of different shapes in a row: the
+    # merge counters return to zero after every call.
+    wa = Workload("wa", B=2, Hq=8, Hkv=2, d=128, N=40000, top_k=20, kind="hot")
+    wb = Workload("wb", B=3, Hq=4, Hkv=4, d=64, N=3000, top_k=9)
+    qa, Ka, Va = (t.to(dev) for t in make_inputs(wa, seed=3))
+    qb, Kb, Vb = (t.to(dev) for t in make_inputs(wb, seed=4))
+    n = max(dkv.workspace_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, k)
+            for w in (wa, wb) for k in (0, w.top_k))
+    ws = torch.zeros(n, dtype=torch.uint8, device=dev)
+    ref_a = dkv.decode_attn_full(qa, Ka, Va)
+    ma, mb = dkv.kv_meta_build(Ka), dkv.kv_meta_build(Kb)
+    ref_sa = dkv.decode_attn_select(qa, Ka, Va, ma, wa.top_k)
+    ref_sb = dkv.decode_attn_select(qb, Kb, Vb, mb, wb.top_k)
+    for _ in range(2):
+        assert torch.equal(dkv.decode_attn_full(qa, Ka, Va, workspace=ws), ref_a)
+        assert torch.equal(dkv.decode_attn_select(qb, Kb, Vb, mb, wb.top_k, workspace=ws), ref_sb)
+        assert torch.equal(dkv.decode_attn_select(qa, Ka, Va, ma, wa.top_k, workspace=ws), ref_sa)
+    assert int(ws[256:352].sum().item()) == 0  # merge counters (first 96 bytes after the status) back at zero
+
+
 def test_strided_query_and_output(dev, dkv):
     w = Workload("st", B=2, Hq=4, Hkv=2, d=64, N=600)
     q, K, V = make_inputs(w, seed=61)
