@@ -26,16 +26,15 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // Byte offsets of the regions inside a caller-provided workspace.
 struct WsLayout {
   size_t status = 0;     // u32 device status word (first 256 bytes)
-  size_t tickets = 0;    // u32 [B * Hkv * (n_groups + 1)], zero between calls
+  size_t counter = 0;    // u32 attention work counter, zero between calls
   size_t part_ml = 0;    // [B, Hq, n_chunks, 2] fp32
   size_t part_o = 0;     // [B, Hq, n_chunks, d] fp32
-  size_t part2_ml = 0;   // [B, Hq, n_groups, 2] fp32
-  size_t part2_o = 0;    // [B, Hq, n_groups, d] fp32
   size_t scores = 0;     // sparse: [B, Hq, P] fp32
   size_t selected = 0;   // sparse: [B, Hq, kk] int32 (used when the caller passes none)
   size_t bitmaps = 0;    // sparse: [B, Hq, W32] u32
   size_t total = 0;
-  int n_chunks = 0, n_groups = 0, pages_per_chunk = 0, kk = 0, W32 = 0;
+  int n_chunks = 0, pages_per_chunk = 0, kk = 0, W32 = 0;
+  int64_t n_items = 0;
   bool ok = true;        // false: the sizes exceed what the kernels cover
 };
 
@@ -45,7 +44,6 @@ WsLayout layout_for(const dkv_params& p, int top_k) {
   const int64_t P = ceil_div(p.seq_len, p.page_size);
   const int64_t rows = static_cast<int64_t>(p.batch) * p.num_q_heads;
   const int64_t units = static_cast<int64_t>(p.batch) * p.num_kv_heads;
-  size_t off = kAlign;  // status word
   if (top_k <= 0) {
     L.pages_per_chunk = dkv::full_pages_per_chunk(P, d);
     L.n_chunks = static_cast<int>(ceil_div(P, L.pages_per_chunk));
@@ -59,9 +57,12 @@ WsLayout layout_for(const dkv_params& p, int top_k) {
     L.n_chunks = static_cast<int>(ceil_div(union_max, L.pages_per_chunk));
   }
   if (L.n_chunks > dkv::kMaxChunks) L.ok = false;
-  L.n_groups = static_cast<int>(ceil_div(L.n_chunks, dkv::kGroup));
-  L.tickets = off;
-  off = align_up(off + sizeof(uint32_t) * units * (L.n_groups + 1));
+  L.n_items = units * L.n_chunks;
+  if (L.n_items >= (static_cast<int64_t>(1) << 31)) L.ok = false;
+  size_t off = 0;
+  L.status = off;
+  L.counter = off + 4;
+  off = kAlign;
   if (top_k > 0) {
     L.scores = off;
     off = align_up(off + sizeof(float) * rows * P);
@@ -74,12 +75,20 @@ WsLayout layout_for(const dkv_params& p, int top_k) {
   off = align_up(off + sizeof(float) * 2 * rows * L.n_chunks);
   L.part_o = off;
   off = align_up(off + sizeof(float) * static_cast<size_t>(d) * rows * L.n_chunks);
-  L.part2_ml = off;
-  off = align_up(off + sizeof(float) * 2 * rows * L.n_groups);
-  L.part2_o = off;
-  off = align_up(off + sizeof(float) * static_cast<size_t>(d) * rows * L.n_groups);
   L.total = off;
   return L;
+}
+
+// Multiprocessor count of the current device (the persistent attention grid).
+int current_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
 }
 
 dkv_status check_params(const dkv_params* p) {
@@ -235,7 +244,7 @@ static dkv_status attn_common(const dkv_params* p, const void* q, const dkv_kv* 
 }
 
 static dkv::AttnArgs attn_args(const dkv_params* p, const void* q, const WsLayout& L,
-                               uint8_t* ws, void* out, int32_t out_dtype) {
+                               uint8_t* ws) {
   dkv::AttnArgs a{};
   a.q = q;
   a.q_sb = p->q_stride_b;
@@ -249,19 +258,35 @@ static dkv::AttnArgs attn_args(const dkv_params* p, const void* q, const WsLayou
   a.scale_log2 = p->scale * 1.4426950408889634f;
   a.pages_per_chunk = L.pages_per_chunk;
   a.n_chunks = L.n_chunks;
-  a.n_groups = L.n_groups;
+  a.n_items = static_cast<int>(L.n_items);
   a.part_ml = reinterpret_cast<float*>(ws + L.part_ml);
   a.part_o = reinterpret_cast<float*>(ws + L.part_o);
-  a.part2_ml = reinterpret_cast<float*>(ws + L.part2_ml);
-  a.part2_o = reinterpret_cast<float*>(ws + L.part2_o);
-  a.tickets = reinterpret_cast<uint32_t*>(ws + L.tickets);
-  a.out = out;
-  a.out_dtype = out_code(out_dtype);
-  a.o_sb = p->o_stride_b;
-  a.o_sh = p->o_stride_h;
+  a.work_counter = reinterpret_cast<uint32_t*>(ws + L.counter);
   a.status = reinterpret_cast<uint32_t*>(ws + L.status);
   a.wait_limit_ns = (p->flags & DKV_FLAG_FORCE_TIMEOUT) ? 0 : kWaitLimitNs;
   return a;
+}
+
+// Persistent attention over all work items, then the split-K merge into out.
+static dkv_status run_attention(const dkv_params* p, const dkv::AttnArgs& a, bool sparse,
+                                bool f16, const CUtensorMap& mk, const CUtensorMap& mv,
+                                void* out, int32_t out_dtype, cudaStream_t s) {
+  const int sms = current_sm_count();
+  if (sms <= 0) return DKV_ERR_CUDA;
+  dkv_status st =
+      cuda_status(dkv::launch_attn(p->head_dim, f16, sparse, a, mk, mv, sms, s));
+  if (st != DKV_OK) return st;
+  dkv::MergeArgs m{};
+  m.part_ml = a.part_ml;
+  m.part_o = a.part_o;
+  m.n_chunks = a.n_chunks;
+  m.Hq = p->num_q_heads;
+  m.out = out;
+  m.out_dtype = out_code(out_dtype);
+  m.o_sb = p->o_stride_b;
+  m.o_sh = p->o_stride_h;
+  m.work_counter = a.work_counter;
+  return cuda_status(dkv::launch_merge(p->head_dim, m, p->batch * p->num_q_heads, s));
 }
 
 dkv_status dkv_decode_attn_full(const dkv_params* p, const void* q, const dkv_kv* K,
@@ -276,10 +301,8 @@ dkv_status dkv_decode_attn_full(const dkv_params* p, const void* q, const dkv_kv
   if (!encode_page_map(&mk, p, K) || !encode_page_map(&mv, p, V)) return DKV_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const dkv::AttnArgs a = attn_args(p, q, L, ws, out, out_dtype);
-  const bool f16 = K->dtype == DKV_FP16;
-  dim3 grid(L.n_chunks, p->num_kv_heads, p->batch);
-  return cuda_status(dkv::launch_attn(p->head_dim, f16, false, a, mk, mv, grid, s));
+  const dkv::AttnArgs a = attn_args(p, q, L, ws);
+  return run_attention(p, a, false, K->dtype == DKV_FP16, mk, mv, out, out_dtype, s);
 }
 
 dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_kv* K,
@@ -329,11 +352,10 @@ dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_
   ta.W32 = L.W32;
   if ((st = cuda_status(dkv::launch_topk(ta, s))) != DKV_OK) return st;
 
-  dkv::AttnArgs a = attn_args(p, q, L, ws, out, out_dtype);
+  dkv::AttnArgs a = attn_args(p, q, L, ws);
   a.bitmaps = ta.bitmaps;
   a.W32 = L.W32;
-  dim3 grid(L.n_chunks, p->num_kv_heads, p->batch);
-  return cuda_status(dkv::launch_attn(p->head_dim, f16, true, a, mk, mv, grid, s));
+  return run_attention(p, a, true, f16, mk, mv, out, out_dtype, s);
 }
 
 dkv_status dkv_kv_quant4(int64_t rows, int32_t d, const void* x, void* codes, void* gmin,

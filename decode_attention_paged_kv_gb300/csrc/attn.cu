@@ -1,5 +1,5 @@
-// attn.cu -- decode attention over pages of a KV cache (exact and page-sparse),
-// with the split-K merge done inside the same kernel.
+// attn.cu -- decode attention over pages of a KV cache (exact and page-sparse)
+// and the merge of its split-K partials.
 //
 // What it computes (per query head h of batch b, kv head h / G):
 //   out = sum_t softmax_t(scale * q . k_t) v_t
@@ -8,28 +8,34 @@
 // or over the tokens of the pages selected for h (TinyServe, 问题公式化定义,
 // Algorithm 1 steps 3-4: gather the selected pages, then softmax-weighted sum).
 //
-// Structure (one CTA = one chunk of pages of one (batch, kv head)):
-//   * warp 4 (producer): one lane streams whole pages of K and V into a ring of
+// attn_kernel is persistent: kAttnCtasPerSm CTAs per SM pull work items --
+// (batch, kv head, chunk of pages) -- from an atomic counter until none are
+// left.  Inside a CTA:
+//   * warp 4 (producer) takes the next item, turns it into a page list (in the
+//     sparse path: the union of the group's selections, from the per-head
+//     bitmaps, with a bit per query head that chose each page), publishes it
+//     through a two-slot descriptor ring and streams the pages' K and V into
 //     shared-memory stages with TMA tensor copies (cp.async.bulk.tensor, 128B
-//     swizzle), each stage guarded by a full / empty mbarrier pair.  In the
-//     sparse path the warp first turns the per-head selection bitmaps into the
-//     CTA's page list (union over the G query heads of the group).
-//   * warps 0-3 (consumers): page i goes to warp i % 4.  A warp computes the
-//     16-token page for all G <= 8 query heads of the group at once on tensor
+//     swizzle), one full / empty mbarrier pair per stage.  It runs ahead
+//     across item boundaries, so the copy engine never drains between items.
+//   * warps 0-3 (consumers): page j of an item goes to warp j % 4, through that
+//     warp's own sub-ring of stages.  Each stage is therefore filled and drained
+//     by one fixed pair (producer, warp) in strict order, so no waiter is ever
+//     more than one phase behind a barrier (parity waits cannot alias).  A warp
+//     computes a 16-token page for all G <= 8 query heads at once on tensor
 //     cores: S[8 heads x 16 tokens] = Q K^T with mma.sync m16n8k16 (heads on the
-//     M side, rows 8-15 unused), an online softmax in fp32 (log2 domain), then
-//     O += P V with P split into a high and a low 16-bit half (rows 0-7 / 8-15
-//     of the A operand) so the weights keep ~16 significant bits.
-//   * the four warps' (max, sum, o) states are merged in shared memory into the
-//     chunk's partial.  The last CTA to finish among a group of kGroup chunks
-//     (an atomic ticket) merges the group; the last group merges the groups
-//     and writes out.  Merges run in ascending order, so results are
-//     deterministic, and chunking depends only on (P, d), so one kv head at a
-//     time gives bitwise the all-heads result.  Tickets return to zero at the
-//     end of every call.
+//     M side), an online softmax in fp32 (log2 domain), then O += P V with P
+//     split into a high and a low 16-bit half (A rows 0-7 / 8-15) so the
+//     weights keep ~16 significant bits.  At the end of an item warps 1-3 hand
+//     their (max, sum, o) to warp 0 through shared memory, which merges them
+//     with its own and writes the item's partial.
+// merge_kernel then combines the chunks of every (b, h) in a fixed tree over
+// ascending chunk indices, writes out, and resets the work counter.  Partials
+// do not depend on which CTA computed them and chunking depends only on
+// (P, d), so results are deterministic and one kv head at a time gives
+// bitwise the all-heads result.
 // Every mbarrier wait is bounded; on expiry the kernel records a timeout in
-// the status word, stops issuing, drains the copies it issued and still takes
-// its tickets (so the counters stay consistent), leaving garbage output.
+// the status word, stops issuing, drains the copies it issued and exits.
 
 #include <math.h>
 
@@ -41,21 +47,31 @@ namespace {
 
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // 200 ms for the whole drain
 
+struct ItemDesc {
+  int item;     // work item, -1: no more work
+  int n_pages;  // pages in the item (0 for an empty sparse chunk)
+  int seq0;     // producer sequence number of the item's first page
+  int pad;
+};
+
 template <int D>
 struct AttnCfg {
   static constexpr int kPageBytes = kPage * D * 2;  // one tensor's page
   static constexpr int kStageBytes = 2 * kPageBytes;
   static constexpr int kStages = attn_stages(D);
-  static constexpr int kBarOffset = kStages * kStageBytes;
-  static constexpr int kMiscOffset = kBarOffset + 2 * kStages * 8;
-  // misc: abort, n_pages, last-flag | list[256] | mask[256] | merge scratch
-  static constexpr int kListOffset = kMiscOffset + 16;
-  static constexpr int kMaskOffset = kListOffset + 4 * kMaxSelectList;
-  static constexpr int kScratchOffset = kMaskOffset + 4 * kMaxSelectList;
-  static constexpr int kScratchBytes = 4 * (2 * 8 * kGroup + 2 * 8);
-  static constexpr int kSmemBytes = 1024 + kScratchOffset + kScratchBytes;
+  static constexpr int kSub = kStages / kConsumerWarps;             // stages per consumer warp
+  static constexpr int kBarOffset = kStages * kStageBytes;          // full, empty, dfull, dempty
+  static constexpr int kStageMetaOffset = kBarOffset + (2 * kStages + 4) * 8;
+  static constexpr int kDescOffset = kStageMetaOffset + kStages * 8;
+  static constexpr int kMergeOffset = kDescOffset + 2 * 16;
+  static constexpr int kMergeRow = D + 2;                           // o[D], max, sum
+  static constexpr int kMergeBytes = (kConsumerWarps - 1) * 8 * kMergeRow * 4;
+  static constexpr int kListOffset = kMergeOffset + kMergeBytes;
+  static constexpr int kMiscOffset = kListOffset + 8 * kMaxSelectList;
+  static constexpr int kSmemBytes = 1024 + kMiscOffset + 16;
   static_assert(kPageBytes % 1024 == 0, "stages must stay 1024-byte aligned");
-  static_assert(kConsumerWarps * 8 * (D + 2) * 4 <= kBarOffset, "merge area fits");
+  static_assert(kStages % kConsumerWarps == 0, "one sub-ring per consumer warp");
+  static_assert((kSmemBytes + 1024) * kAttnCtasPerSm <= 228 * 1024, "two CTAs per SM");
 };
 
 // Shared address of channels [c, c+8) of token t in a page tile written by the
@@ -68,6 +84,12 @@ __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int t, int c) {
   return base + static_cast<uint32_t>(row * 128 + chunk * 16);
 }
 
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+}
+
+// Barrier over the consumer warps that also ORs `flag` across them, so every
+// consumer takes the same branch afterwards.
 __device__ __forceinline__ bool consumers_any(bool flag) {
   uint32_t res;
   asm volatile(
@@ -81,15 +103,12 @@ __device__ __forceinline__ bool consumers_any(bool flag) {
   return res != 0;
 }
 
-__device__ __forceinline__ void consumers_sync() {
-  asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
-}
-
 // Sparse path: the pages of the union of the group's selections whose rank (in
 // ascending page order) falls in [chunk * ppc, (chunk + 1) * ppc), with a
-// bit per query head that selected each page.  Run by one full warp.
-__device__ void build_sparse_list(const AttnArgs& a, int b, int kvh, int chunk, int* s_list,
-                                  uint32_t* s_mask, int* s_npages, int lane) {
+// bit per query head that selected each page.  Run by one full warp; returns
+// the page count (to every lane).
+__device__ int build_sparse_list(const AttnArgs& a, int b, int kvh, int chunk, int2* list,
+                                 int lane) {
   const int lo = chunk * a.pages_per_chunk, hi = lo + a.pages_per_chunk;
   const uint32_t* bm = a.bitmaps + (static_cast<int64_t>(b) * a.Hq + kvh * a.G) * a.W32;
   int count = 0;
@@ -119,93 +138,21 @@ __device__ void build_sparse_list(const AttnArgs& a, int b, int kvh, int chunk, 
           uint32_t m = 0;
 #pragma unroll
           for (int g = 0; g < 8; ++g) m |= ((words[g] >> j) & 1u) << g;
-          s_list[r - lo] = wi * 32 + j;
-          s_mask[r - lo] = m;
+          list[r - lo] = make_int2(wi * 32 + j, static_cast<int>(m));
         }
         ++r;
       }
     }
     count += __shfl_sync(0xffffffffu, incl, 31);
   }
-  if (lane == 0) *s_npages = max(0, min(count, hi) - lo);
-}
-
-__device__ __forceinline__ void store_out(const AttnArgs& a, int b, int h, int c, float v) {
-  const int64_t off = b * a.o_sb + h * a.o_sh + c;
-  if (a.out_dtype == 2) {
-    static_cast<float*>(a.out)[off] = v;
-  } else if (a.out_dtype == 1) {
-    static_cast<__half*>(a.out)[off] = __float2half_rn(v);
-  } else {
-    static_cast<__nv_bfloat16*>(a.out)[off] = __float2bfloat16_rn(v);
-  }
-}
-
-// Merge `count` (<= kGroup) consecutive partials [first, first + count) of the
-// G rows (b, kvh*G + h): weights w_i = 2^(m_i - max m), in ascending order.
-// Writes one merged partial (item `out_item` of rows with `n_out` items) or,
-// when final, out = sum w_i o_i / sum w_i l_i.  All threads of the CTA call it.
-template <int D>
-__device__ void merge_partials(const AttnArgs& a, int b, int kvh, const float* ml_in,
-                               const float* o_in, int n_in, int first, int count, bool final,
-                               float* ml_out, float* o_out, int n_out, int out_item,
-                               float* scratch) {
-  float* s_w = scratch;                 // [8][kGroup] m_i, then weights
-  float* s_l = scratch + 8 * kGroup;    // [8][kGroup]
-  float* s_M = scratch + 16 * kGroup;   // [8]
-  float* s_L = s_M + 8;                 // [8]
-  const int64_t row0 = static_cast<int64_t>(b) * a.Hq + kvh * a.G;
-  for (int t = threadIdx.x; t < a.G * count; t += blockDim.x) {
-    const int h = t / count, i = t % count;
-    const int64_t item = (row0 + h) * n_in + first + i;
-    s_w[h * kGroup + i] = __ldcg(ml_in + 2 * item);
-    s_l[h * kGroup + i] = __ldcg(ml_in + 2 * item + 1);
-  }
-  __syncthreads();
-  if (threadIdx.x < a.G) {
-    const int h = threadIdx.x;
-    float M = -INFINITY;
-    for (int i = 0; i < count; ++i) M = fmaxf(M, s_w[h * kGroup + i]);
-    float L = 0.f;
-    for (int i = 0; i < count; ++i) {
-      const float m = s_w[h * kGroup + i];
-      const float w = (m == -INFINITY) ? 0.f : exp2f(m - M);
-      L += w * s_l[h * kGroup + i];
-      s_w[h * kGroup + i] = w;
-    }
-    s_M[h] = M;
-    s_L[h] = L;
-  }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < a.G * D; idx += blockDim.x) {
-    const int h = idx / D, c = idx % D;
-    const float* src = o_in + ((row0 + h) * n_in + first) * D + c;
-    float x[kGroup];
-#pragma unroll
-    for (int i = 0; i < kGroup; ++i) x[i] = (i < count) ? __ldcg(src + i * D) : 0.f;
-    float O = 0.f;
-#pragma unroll
-    for (int i = 0; i < kGroup; ++i) {
-      const float w = (i < count) ? s_w[h * kGroup + i] : 0.f;
-      O += (w != 0.f) ? w * x[i] : 0.f;  // empty partials hold no o values
-    }
-    if (final) {
-      store_out(a, b, kvh * a.G + h, c, O / s_L[h]);
-    } else {
-      const int64_t item = (row0 + h) * n_out + out_item;
-      o_out[item * D + c] = O;
-      if (c == 0) {
-        ml_out[2 * item] = s_M[h];
-        ml_out[2 * item + 1] = s_L[h];
-      }
-    }
-  }
+  __syncwarp();
+  return max(0, min(count, hi) - lo);
 }
 
 template <int D, bool F16, bool SPARSE>
 __global__ void __launch_bounds__(kAttnThreads)
-    attn_pages_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mk,
-                      const __grid_constant__ CUtensorMap mv) {
+    attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mk,
+                const __grid_constant__ CUtensorMap mv) {
   using C = AttnCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -213,20 +160,23 @@ __global__ void __launch_bounds__(kAttnThreads)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t full0 = sbase + C::kBarOffset;
   const uint32_t empty0 = full0 + 8 * C::kStages;
+  const uint32_t dfull0 = empty0 + 8 * C::kStages;
+  const uint32_t dempty0 = dfull0 + 16;
+  int2* stage_meta = reinterpret_cast<int2*>(smem + C::kStageMetaOffset);
+  volatile ItemDesc* desc = reinterpret_cast<volatile ItemDesc*>(smem + C::kDescOffset);
+  float* mrg = reinterpret_cast<float*>(smem + C::kMergeOffset);
+  int2* list = reinterpret_cast<int2*>(smem + C::kListOffset);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOffset);
-  int* s_npages = reinterpret_cast<int*>(smem + C::kMiscOffset + 4);
-  volatile int* s_last = reinterpret_cast<volatile int*>(smem + C::kMiscOffset + 8);
-  int* s_list = reinterpret_cast<int*>(smem + C::kListOffset);
-  uint32_t* s_mask = reinterpret_cast<uint32_t*>(smem + C::kMaskOffset);
-  float* scratch = reinterpret_cast<float*>(smem + C::kScratchOffset);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int chunk = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(dfull0 + 8 * s, 1);
+      mbar_init(dempty0 + 8 * s, 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -236,63 +186,125 @@ __global__ void __launch_bounds__(kAttnThreads)
     prefetch_tensormap(&mv);
   }
   griddep_launch_dependents();
-  griddep_wait();  // q, K, V, bitmaps and the workspace may come from earlier kernels
-  int first_page = 0, n_pages = 0;
-  if constexpr (SPARSE) {
-    if (warp == kConsumerWarps) build_sparse_list(a, b, kvh, chunk, s_list, s_mask, s_npages, lane);
-  } else {
-    first_page = chunk * a.pages_per_chunk;
-    n_pages = max(0, min(a.P - first_page, a.pages_per_chunk));
-  }
+  griddep_wait();  // q, K, V, bitmaps and the work counter come from earlier kernels
   __syncthreads();
-  if constexpr (SPARSE) n_pages = *s_npages;
 
-  const int64_t row0 = static_cast<int64_t>(b) * a.Hq + kvh * a.G;
-  if (n_pages <= 0) {
-    // Nothing to attend in this chunk: an empty partial (no o values).
-    if (threadIdx.x < a.G) {
-      const int64_t item = (row0 + threadIdx.x) * a.n_chunks + chunk;
-      a.part_ml[2 * item] = -INFINITY;
-      a.part_ml[2 * item + 1] = 0.f;
-    }
-  } else if (warp == kConsumerWarps) {
+  if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const uint64_t pol = l2_evict_first_policy();
-      int issued = 0;
-      for (int i = 0; i < n_pages; ++i) {
-        const int s = i % C::kStages, k = i / C::kStages;
-        if (i >= C::kStages &&
-            !mbar_wait_bounded(empty0 + 8 * s, (k - 1) & 1, a.wait_limit_ns, abort_flag)) {
-          if (!*abort_flag) {
-            set_status(a.status, kStatusTimeout);
-            *abort_flag = 1;
-          }
-          break;
+    const uint64_t pol = l2_evict_first_policy();
+    int seq = 0, issued = 0;
+    // Pages issued so far to consumer warps 0-3 (each item starts at warp 0).
+    int wc0 = 0, wc1 = 0, wc2 = 0, wc3 = 0;
+    for (int k = 0;; ++k) {
+      int item = 0;
+      if (lane == 0) item = static_cast<int>(atomicAdd(a.work_counter, 1u));
+      item = __shfl_sync(0xffffffffu, item, 0);
+      if (item >= a.n_items) item = -1;
+      const int slot = k & 1;
+      int ok = 1;
+      if (lane == 0 && k >= 2) {
+        ok = mbar_wait_bounded(dempty0 + 8 * slot, ((k >> 1) - 1) & 1, a.wait_limit_ns,
+                               abort_flag);
+        if (!ok && *abort_flag == 0) {
+          set_status(a.status, kStatusTimeout);
+          *abort_flag = 1;
         }
-        if (*abort_flag) break;
-        const int page = SPARSE ? s_list[i] : first_page + i;
-        const uint32_t dst = sbase + s * C::kStageBytes;
-        mbar_arrive_expect_tx(full0 + 8 * s, C::kStageBytes);
-        tma_load_5d_hint(dst, &mk, full0 + 8 * s, 0, page * kPage, 0, kvh, b, pol);
-        tma_load_5d_hint(dst + C::kPageBytes, &mv, full0 + 8 * s, 0, page * kPage, 0, kvh, b,
-                         pol);
-        ++issued;
       }
-      if (*abort_flag) {  // let every copy this CTA issued land before it exits
-        const uint64_t deadline = globaltimer_ns() + kDrainLimitNs;
-        for (int i = max(0, issued - C::kStages); i < issued; ++i) {
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      int n = 0, b = 0, kvh = 0, first = 0;
+      if (item >= 0) {
+        const int chunk = item % a.n_chunks;
+        const int unit = item / a.n_chunks;
+        kvh = unit % a.Hkv;
+        b = unit / a.Hkv;
+        if constexpr (SPARSE) {
+          n = build_sparse_list(a, b, kvh, chunk, list, lane);
+        } else {
+          first = chunk * a.pages_per_chunk;
+          n = max(0, min(a.P - first, a.pages_per_chunk));
+        }
+      }
+      if (lane == 0) {
+        desc[slot].item = item;
+        desc[slot].n_pages = n;
+        desc[slot].seq0 = seq;
+        mbar_arrive(dfull0 + 8 * slot);  // release: consumers see the descriptor
+        static_assert(kConsumerWarps == 4, "four consumer sub-rings");
+        int jd = 0;  // pages of this item issued
+        for (int j = 0; j < n && item >= 0; ++j) {
+          const int w = j & 3;
+          const int c = (j >> 2) + (w == 0 ? wc0 : w == 1 ? wc1 : w == 2 ? wc2 : wc3);
+          const int s = w * C::kSub + c % C::kSub;  // warp w's sub-ring, in order
+          if (c >= C::kSub &&
+              !mbar_wait_bounded(empty0 + 8 * s, ((c / C::kSub) - 1) & 1, a.wait_limit_ns,
+                                 abort_flag)) {
+            ok = 0;
+            break;
+          }
+          const int page = SPARSE ? list[j].x : first + j;
+          stage_meta[s] = make_int2(page, SPARSE ? list[j].y : 0xff);
+          const uint32_t dst = sbase + s * C::kStageBytes;
+          mbar_arrive_expect_tx(full0 + 8 * s, C::kStageBytes);
+          tma_load_5d_hint(dst, &mk, full0 + 8 * s, 0, page * kPage, 0, kvh, b, pol);
+          tma_load_5d_hint(dst + C::kPageBytes, &mv, full0 + 8 * s, 0, page * kPage, 0, kvh, b,
+                           pol);
+          ++issued;
+          jd = j + 1;
+        }
+        wc0 += (jd + 3) >> 2;
+        wc1 += (jd + 2) >> 2;
+        wc2 += (jd + 1) >> 2;
+        wc3 += jd >> 2;
+      }
+      seq += n;
+      if (!__shfl_sync(0xffffffffu, ok, 0) || item < 0) break;
+    }
+    if (lane == 0 && *abort_flag == 0 && issued < seq) {
+      set_status(a.status, kStatusTimeout);
+      *abort_flag = 1;
+    }
+    if (lane == 0 && *abort_flag) {  // let every copy this CTA issued land before it exits
+      const uint64_t deadline = globaltimer_ns() + kDrainLimitNs;
+      // A sub-ring holds at most kSub copies in flight: waiting for the last
+      // kSub issued to every sub-ring covers all of them.
+      const int wcs[4] = {wc0, wc1, wc2, wc3};
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        for (int c = max(0, wcs[w] - C::kSub); c < wcs[w]; ++c) {
           const uint64_t now = globaltimer_ns();
           if (now >= deadline) break;
-          mbar_wait_bounded(full0 + 8 * (i % C::kStages), (i / C::kStages) & 1, deadline - now,
-                            nullptr);
+          mbar_wait_bounded(full0 + 8 * (w * C::kSub + c % C::kSub), (c / C::kSub) & 1,
+                            deadline - now, nullptr);
         }
       }
     }
-  } else {
-    // ------------------------------------------------------------ consumers
-    const int g = lane >> 2, t4 = lane & 3;
-    const bool head_ok = g < a.G;
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int g = lane >> 2, t4 = lane & 3;
+  const bool head_ok = g < a.G;
+  const int mtx = lane >> 3, mrow = lane & 7;
+  int mycnt = 0;  // pages this warp has taken from its sub-ring
+  // Exits are taken by all four consumer warps together (consumers_any), so no
+  // warp is ever left waiting at a consumer barrier.
+  for (int k = 0;; ++k) {
+    const int slot = k & 1;
+    const bool dok = mbar_wait_bounded(dfull0 + 8 * slot, (k >> 1) & 1, a.wait_limit_ns,
+                                       abort_flag);
+    if (consumers_any(!dok)) {
+      if (threadIdx.x == 0) {
+        set_status(a.status, kStatusTimeout);
+        *abort_flag = 1;
+      }
+      return;
+    }
+    const int item = desc[slot].item, n_pages = desc[slot].n_pages;
+    if (item < 0) return;  // the same descriptor for every consumer warp
+    const int chunk = item % a.n_chunks;
+    const int unit = item / a.n_chunks;
+    const int kvh = unit % a.Hkv, b = unit / a.Hkv;
+
     uint32_t qa[D / 16][2];
     {
       const uint16_t* qrow = static_cast<const uint16_t*>(a.q) + b * a.q_sb +
@@ -310,10 +322,11 @@ __global__ void __launch_bounds__(kAttnThreads)
     for (int cn = 0; cn < D / 8; ++cn) acc[cn][0] = acc[cn][1] = acc[cn][2] = acc[cn][3] = 0.f;
 
     bool aborted = false;
-    const int mtx = lane >> 3, mrow = lane & 7;
-    for (int i = warp; i < n_pages; i += kConsumerWarps) {
-      const int s = i % C::kStages, k = i / C::kStages;
-      const bool ok = mbar_wait_bounded(full0 + 8 * s, k & 1, a.wait_limit_ns, abort_flag);
+    for (int j = warp; j < n_pages; j += kConsumerWarps) {
+      const int s = warp * C::kSub + mycnt % C::kSub;
+      const bool ok = mbar_wait_bounded(full0 + 8 * s, (mycnt / C::kSub) & 1, a.wait_limit_ns,
+                                        abort_flag);
+      ++mycnt;
       if (!__all_sync(0xffffffffu, ok)) {
         if (lane == 0) {
           set_status(a.status, kStatusTimeout);
@@ -323,8 +336,9 @@ __global__ void __launch_bounds__(kAttnThreads)
         break;
       }
       const uint32_t kb = sbase + s * C::kStageBytes, vb = kb + C::kPageBytes;
-      const int page = SPARSE ? s_list[i] : first_page + i;
-      const uint32_t hmask = SPARSE ? s_mask[i] : 0xffu;
+      const int2 meta = stage_meta[s];
+      const int page = meta.x;
+      const uint32_t hmask = static_cast<uint32_t>(meta.y);
 
       // S = Q K^T for the page: sc[nt][e] = score of head g, token 8 nt + 2 t4 + e.
       float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -341,10 +355,10 @@ __global__ void __launch_bounds__(kAttnThreads)
       float sv[4];
       float pmax = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int tok = page * kPage + 8 * (j >> 1) + 2 * t4 + (j & 1);
-        sv[j] = (head_on && tok < a.N) ? sc[j >> 1][j & 1] * a.scale_log2 : -INFINITY;
-        pmax = fmaxf(pmax, sv[j]);
+      for (int e = 0; e < 4; ++e) {
+        const int tok = page * kPage + 8 * (e >> 1) + 2 * t4 + (e & 1);
+        sv[e] = (head_on && tok < a.N) ? sc[e >> 1][e & 1] * a.scale_log2 : -INFINITY;
+        pmax = fmaxf(pmax, sv[e]);
       }
       pmax = fmaxf(pmax, __shfl_xor_sync(0xffffffffu, pmax, 1));
       pmax = fmaxf(pmax, __shfl_xor_sync(0xffffffffu, pmax, 2));
@@ -354,9 +368,9 @@ __global__ void __launch_bounds__(kAttnThreads)
       float p[4];
       float psum = 0.f;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        p[j] = exp2f(sv[j] - m_use);
-        psum += p[j];
+      for (int e = 0; e < 4; ++e) {
+        p[e] = exp2f(sv[e] - m_use);
+        psum += p[e];
       }
       l_run = l_run * alpha + psum;
       if (__any_sync(0xffffffffu, m_new != m_run)) {
@@ -389,110 +403,161 @@ __global__ void __launch_bounds__(kAttnThreads)
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
 
-    // Merge the consumer warps' states into the chunk's partial (the stage ring
-    // is free once every warp is past its loop: all issued copies were consumed).
-    if (!consumers_any(aborted)) {
-      float* mrg = reinterpret_cast<float*>(smem);
-      {
-        float* r = mrg + (warp * 8 + g) * (D + 2);
-        if (t4 == 0) {
-          r[D] = m_run;
-          r[D + 1] = l_run;
-        }
-#pragma unroll
-        for (int cn = 0; cn < D / 8; ++cn) {
-          r[8 * cn + 2 * t4] = acc[cn][0] + acc[cn][2];
-          r[8 * cn + 2 * t4 + 1] = acc[cn][1] + acc[cn][3];
-        }
+    // Warps 1-3 hand their states to warp 0, which merges them with its own
+    // (ascending warp order) and writes the item's partial.
+    if (consumers_any(aborted)) return;
+    if (warp > 0) {
+      float* r = mrg + ((warp - 1) * 8 + g) * C::kMergeRow;
+      if (t4 == 0) {
+        r[D] = m_run;
+        r[D + 1] = l_run;
       }
-      consumers_sync();
-      for (int idx = threadIdx.x; idx < a.G * D; idx += kConsumerWarps * 32) {
-        const int h = idx / D, c = idx % D;
-        float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mrg[(w * 8 + h) * (D + 2) + D]);
-        float L = 0.f, O = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) {
-            const float* r = mrg + (w * 8 + h) * (D + 2);
-            if (r[D] == -INFINITY) continue;
-            const float f = exp2f(r[D] - M);
-            L += f * r[D + 1];
-            O += f * r[c];
-          }
-        }
-        const int64_t item = (row0 + h) * a.n_chunks + chunk;
-        a.part_o[item * D + c] = O;
-        if (c == 0) {
-          a.part_ml[2 * item] = M;
-          a.part_ml[2 * item + 1] = L;
-        }
+      for (int cn = 0; cn < D / 8; ++cn) {
+        r[8 * cn + 2 * t4] = acc[cn][0] + acc[cn][2];
+        r[8 * cn + 2 * t4 + 1] = acc[cn][1] + acc[cn][3];
       }
     }
+    consumers_sync();
+    if (warp == 0 && head_ok) {
+      float M = m_run;
+#pragma unroll
+      for (int w = 1; w < kConsumerWarps; ++w)
+        M = fmaxf(M, mrg[((w - 1) * 8 + g) * C::kMergeRow + D]);
+      float f[kConsumerWarps];
+      f[0] = (m_run == -INFINITY) ? 0.f : exp2f(m_run - M);
+      float L = f[0] * l_run;
+#pragma unroll
+      for (int w = 1; w < kConsumerWarps; ++w) {
+        const float* r = mrg + ((w - 1) * 8 + g) * C::kMergeRow;
+        f[w] = (r[D] == -INFINITY) ? 0.f : exp2f(r[D] - M);
+        L += f[w] * r[D + 1];
+      }
+      const int64_t pi = (static_cast<int64_t>(b) * a.Hq + kvh * a.G + g) * a.n_chunks + chunk;
+      float* po = a.part_o + pi * D;
+#pragma unroll
+      for (int cn = 0; cn < D / 8; ++cn) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int c = 8 * cn + 2 * t4 + e;
+          float O = f[0] * (acc[cn][e] + acc[cn][2 + e]);
+#pragma unroll
+          for (int w = 1; w < kConsumerWarps; ++w)
+            O += f[w] * mrg[((w - 1) * 8 + g) * C::kMergeRow + c];
+          po[c] = O;
+        }
+      }
+      if (t4 == 0) {
+        a.part_ml[2 * pi] = M;
+        a.part_ml[2 * pi + 1] = L;
+      }
+    }
+    consumers_sync();  // merge area free again; the descriptor slot was read by all
+    if (threadIdx.x == 0) mbar_arrive(dempty0 + 8 * slot);
   }
+}
 
-  // ---------------------------------------------------------- split-K merge
-  __syncthreads();
-  const int64_t unit = static_cast<int64_t>(b) * a.Hkv + kvh;
-  const int grp = chunk / kGroup;
-  const int gsize = min(kGroup, a.n_chunks - grp * kGroup);
-  if (threadIdx.x == 0) {
-    __threadfence();
-    uint32_t* t = a.tickets + unit * a.n_groups + grp;
-    const bool last = atomicAdd(t, 1u) == static_cast<uint32_t>(gsize - 1);
-    if (last) atomicExch(t, 0u);  // every CTA of the group has arrived: reset
-    *s_last = last;
+// One CTA per (b, h) row and 32 output channels.  Thread (cg, cq) folds the
+// chunks k = cg, cg + 32, ... (ascending) for 4 channels with an online max;
+// the 32 chunk groups are then folded in ascending order.  out = sum w o /
+// sum w l with w = 2^(m - max m).  Also resets the attention work counter.
+template <int D>
+__global__ void __launch_bounds__(256) merge_kernel(const MergeArgs m) {
+  __shared__ float sM[32], sL[32], sO[32][33];
+  griddep_launch_dependents();
+  griddep_wait();  // the attention grid has finished writing its partials
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *m.work_counter = 0u;
+  const int row = blockIdx.x, cb = blockIdx.y;
+  const int cg = threadIdx.x >> 3, cq = threadIdx.x & 7;
+  const float* ml = m.part_ml + static_cast<int64_t>(row) * m.n_chunks * 2;
+  const float* po = m.part_o + static_cast<int64_t>(row) * m.n_chunks * D + 32 * cb + 4 * cq;
+  float M = -INFINITY, L = 0.f, O[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+  for (int k = cg; k < m.n_chunks; k += 32) {
+    const float mk = __ldcg(ml + 2 * k);
+    const float lk = __ldcg(ml + 2 * k + 1);
+    const float4 ok = __ldcg(reinterpret_cast<const float4*>(po + static_cast<int64_t>(k) * D));
+    if (mk == -INFINITY) continue;  // empty chunk: no o values
+    if (mk > M) {
+      const float f = exp2f(M - mk);
+      L *= f;
+      O[0] *= f;
+      O[1] *= f;
+      O[2] *= f;
+      O[3] *= f;
+      M = mk;
+    }
+    const float w = exp2f(mk - M);
+    L += w * lk;
+    O[0] += w * ok.x;
+    O[1] += w * ok.y;
+    O[2] += w * ok.z;
+    O[3] += w * ok.w;
   }
-  __syncthreads();
-  if (!*s_last) return;
-  __threadfence();
-  const bool skip = *abort_flag != 0;  // this CTA's copies may still be landing
-  if (!skip)
-    merge_partials<D>(a, b, kvh, a.part_ml, a.part_o, a.n_chunks, grp * kGroup, gsize,
-                      a.n_groups == 1, a.part2_ml, a.part2_o, a.n_groups, grp, scratch);
-  if (a.n_groups == 1) return;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    uint32_t* t = a.tickets + static_cast<int64_t>(a.B) * a.Hkv * a.n_groups + unit;
-    const bool last = atomicAdd(t, 1u) == static_cast<uint32_t>(a.n_groups - 1);
-    if (last) atomicExch(t, 0u);
-    *s_last = last;
+  if (cq == 0) {
+    sM[cg] = M;
+    sL[cg] = L;
   }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) sO[cg][4 * cq + e] = O[e];
   __syncthreads();
-  if (!*s_last) return;
-  __threadfence();
-  if (!skip)
-    merge_partials<D>(a, b, kvh, a.part2_ml, a.part2_o, a.n_groups, 0, a.n_groups, true,
-                      nullptr, nullptr, 0, 0, scratch);
+  if (threadIdx.x < 32) {
+    const int c = threadIdx.x;
+    float Mx = -INFINITY;
+    for (int i = 0; i < 32; ++i) Mx = fmaxf(Mx, sM[i]);
+    float num = 0.f, den = 0.f;
+    for (int i = 0; i < 32; ++i) {
+      if (sM[i] == -INFINITY) continue;
+      const float w = exp2f(sM[i] - Mx);
+      num += w * sO[i][c];
+      den += w * sL[i];
+    }
+    const float v = num / den;
+    const int b = row / m.Hq, h = row % m.Hq;
+    const int64_t off = b * m.o_sb + h * m.o_sh + 32 * cb + c;
+    if (m.out_dtype == 2) {
+      static_cast<float*>(m.out)[off] = v;
+    } else if (m.out_dtype == 1) {
+      static_cast<__half*>(m.out)[off] = __float2half_rn(v);
+    } else {
+      static_cast<__nv_bfloat16*>(m.out)[off] = __float2bfloat16_rn(v);
+    }
+  }
 }
 
 template <int D, bool F16, bool SPARSE>
 cudaError_t launch_attn_t(const AttnArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
-                          dim3 grid, cudaStream_t s) {
+                          int num_sms, cudaStream_t s) {
   using C = AttnCfg<D>;
-  auto kern = attn_pages_kernel<D, F16, SPARSE>;
+  auto kern = attn_kernel<D, F16, SPARSE>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, grid, dim3(kAttnThreads), C::kSmemBytes, s, a, mk, mv);
+  const int64_t want = static_cast<int64_t>(num_sms) * kAttnCtasPerSm;
+  const int grid = static_cast<int>(a.n_items < want ? a.n_items : want);
+  return launch_pdl(kern, dim3(grid), dim3(kAttnThreads), C::kSmemBytes, s, a, mk, mv);
 }
 
 }  // namespace
 
 cudaError_t launch_attn(int d, bool f16, bool sparse, const AttnArgs& a, const CUtensorMap& mk,
-                        const CUtensorMap& mv, dim3 grid, cudaStream_t s) {
+                        const CUtensorMap& mv, int num_sms, cudaStream_t s) {
   if (d == 128) {
-    if (f16) return sparse ? launch_attn_t<128, true, true>(a, mk, mv, grid, s)
-                           : launch_attn_t<128, true, false>(a, mk, mv, grid, s);
-    return sparse ? launch_attn_t<128, false, true>(a, mk, mv, grid, s)
-                  : launch_attn_t<128, false, false>(a, mk, mv, grid, s);
+    if (f16) return sparse ? launch_attn_t<128, true, true>(a, mk, mv, num_sms, s)
+                           : launch_attn_t<128, true, false>(a, mk, mv, num_sms, s);
+    return sparse ? launch_attn_t<128, false, true>(a, mk, mv, num_sms, s)
+                  : launch_attn_t<128, false, false>(a, mk, mv, num_sms, s);
   }
-  if (f16) return sparse ? launch_attn_t<64, true, true>(a, mk, mv, grid, s)
-                         : launch_attn_t<64, true, false>(a, mk, mv, grid, s);
-  return sparse ? launch_attn_t<64, false, true>(a, mk, mv, grid, s)
-                : launch_attn_t<64, false, false>(a, mk, mv, grid, s);
+  if (f16) return sparse ? launch_attn_t<64, true, true>(a, mk, mv, num_sms, s)
+                         : launch_attn_t<64, true, false>(a, mk, mv, num_sms, s);
+  return sparse ? launch_attn_t<64, false, true>(a, mk, mv, num_sms, s)
+                : launch_attn_t<64, false, false>(a, mk, mv, num_sms, s);
+}
+
+cudaError_t launch_merge(int d, const MergeArgs& m, int rows, cudaStream_t s) {
+  const dim3 grid(rows, d / 32), block(256);
+  return d == 128 ? launch_pdl(merge_kernel<128>, grid, block, 0, s, m)
+                  : launch_pdl(merge_kernel<64>, grid, block, 0, s, m);
 }
 
 }  // namespace dkv

@@ -16,29 +16,33 @@ constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Split-K partials are merged in groups of kGroup chunks, then the groups.
-constexpr int kGroup = 16;
-constexpr int kMaxChunks = kGroup * kGroup;  // per (batch, kv head)
+// Split-K: a (batch, kv head) is cut into at most kMaxChunks chunks of pages;
+// each chunk's partial (max, sum, o) is merged by merge_kernel.
+constexpr int kMaxChunks = 256;
 
-// Pages one attention CTA streams in the exact path: 512 KiB of K+V at least,
-// more for long contexts so a (batch, kv head) never has more than kMaxChunks
-// chunks.  Depends only on (P, d) -- not on the batch or the number of kv heads
-// in the call -- so one kv head at a time gives bitwise the all-heads result.
+// Pages one attention work item streams in the exact path: 512 KiB of K+V at
+// least, more for long contexts so a (batch, kv head) never has more than
+// kMaxChunks chunks.  Depends only on (P, d) -- not on the batch or the number
+// of kv heads in the call -- so one kv head at a time gives bitwise the
+// all-heads result.
 inline int full_pages_per_chunk(int64_t P, int d) {
   const int64_t base = d == 128 ? 64 : 128;
   const int64_t need = ceil_div(P, kMaxChunks);
   return static_cast<int>(need > base ? ceil_div(need, 16) * 16 : base);
 }
-// Selected pages one attention CTA gathers in the sparse path (256 KiB K+V at
-// least), from a union of at most `union_max` pages per (batch, kv head).
+// Selected pages one sparse work item gathers (256 KiB of K+V at least), from a
+// union of at most `union_max` pages per (batch, kv head).
 constexpr int kMaxSelectList = 256;  // shared-memory page list capacity
 inline int select_pages_per_chunk(int64_t union_max, int d) {
   const int64_t base = d == 128 ? 32 : 64;
   const int64_t need = ceil_div(union_max, kMaxChunks);
   return static_cast<int>(need > base ? need : base);
 }
-// Pipeline depth: pages of K+V in flight per CTA (96 KiB of shared memory).
+// Pipeline depth: pages of K+V in flight per CTA (96 KiB of shared memory), as
+// one sub-ring per consumer warp (a multiple of kConsumerWarps).
 constexpr int attn_stages(int d) { return d == 128 ? 12 : 24; }
+// Resident attention CTAs per SM (the persistent grid is this times the SMs).
+constexpr int kAttnCtasPerSm = 2;
 
 struct AttnArgs {
   const void* q;
@@ -47,19 +51,25 @@ struct AttnArgs {
   float scale_log2;            // softmax scale * log2(e)
   int pages_per_chunk;
   int n_chunks;                // per (batch, kv head), <= kMaxChunks
-  int n_groups;                // ceil(n_chunks / kGroup)
+  int n_items;                 // B * Hkv * n_chunks work items
   float* part_ml;              // [B, Hq, n_chunks, 2]  (max in log2 units, sum)
   float* part_o;               // [B, Hq, n_chunks, d]  unnormalised
-  float* part2_ml;             // [B, Hq, n_groups, 2]
-  float* part2_o;              // [B, Hq, n_groups, d]
-  uint32_t* tickets;           // [B * Hkv * n_groups] then [B * Hkv]; zero between calls
+  uint32_t* work_counter;      // next work item; zero between calls
   const uint32_t* bitmaps;     // sparse path: [B, Hq, W32] selected-page bits
   int W32;
+  uint32_t* status;
+  uint64_t wait_limit_ns;
+};
+
+struct MergeArgs {
+  const float* part_ml;
+  const float* part_o;
+  int n_chunks;
+  int Hq;
   void* out;
   int out_dtype;               // 0 bf16, 1 fp16, 2 fp32
   int64_t o_sb, o_sh;
-  uint32_t* status;
-  uint64_t wait_limit_ns;
+  uint32_t* work_counter;      // reset to zero once the attention grid is done
 };
 
 struct ScoreArgs {
@@ -110,7 +120,8 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 // Launchers: return the launch's cudaError_t.
 cudaError_t launch_attn(int d, bool f16, bool sparse, const AttnArgs& a, const CUtensorMap& mk,
-                        const CUtensorMap& mv, dim3 grid, cudaStream_t s);
+                        const CUtensorMap& mv, int num_sms, cudaStream_t s);
+cudaError_t launch_merge(int d, const MergeArgs& m, int rows, cudaStream_t s);
 cudaError_t launch_score(int d, bool f16, const ScoreArgs& a, cudaStream_t s);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
 cudaError_t launch_meta(bool q4, bool f16, const MetaArgs& a, cudaStream_t s);

@@ -43,6 +43,10 @@ CASES = [
     Workload("one-page", B=1, Hq=2, Hkv=1, d=64, N=16, top_k=1),
     Workload("page+1", B=1, Hq=2, Hkv=2, d=128, N=17, top_k=1),
     Workload("long-chunks", B=1, Hq=4, Hkv=1, d=128, N=70000, top_k=64),
+    # more work items than persistent CTAs (2 per SM): every CTA streams
+    # several items back to back, exact and sparse
+    Workload("multi-item-gqa", B=16, Hq=16, Hkv=8, d=128, N=8192, top_k=48, kind="hot"),
+    Workload("multi-item-mha", B=16, Hq=32, Hkv=32, d=64, N=4100, top_k=64, kind="offset"),
 ]
 
 
@@ -109,7 +113,7 @@ def test_headwise_equals_all_heads_bitwise(dev, dkv):
 
 def test_workspace_reuse_across_calls(dev, dkv):
     # One zero-filled workspace serves calls of different shapes in a row: the
-    # merge counters return to zero after every call.
+    # work counter returns to zero after every call.
     wa = Workload("wa", B=2, Hq=8, Hkv=2, d=128, N=40000, top_k=20, kind="hot")
     wb = Workload("wb", B=3, Hq=4, Hkv=4, d=64, N=3000, top_k=9)
     qa, Ka, Va = (t.to(dev) for t in make_inputs(wa, seed=3))
@@ -125,7 +129,7 @@ def test_workspace_reuse_across_calls(dev, dkv):
         assert torch.equal(dkv.decode_attn_full(qa, Ka, Va, workspace=ws), ref_a)
         assert torch.equal(dkv.decode_attn_select(qb, Kb, Vb, mb, wb.top_k, workspace=ws), ref_sb)
         assert torch.equal(dkv.decode_attn_select(qa, Ka, Va, ma, wa.top_k, workspace=ws), ref_sa)
-    assert int(ws[256:352].sum().item()) == 0  # merge counters (first 96 bytes after the status) back at zero
+    assert int(ws[4:8].sum().item()) == 0  # the work counter is back at zero
 
 
 def test_strided_query_and_output(dev, dkv):
