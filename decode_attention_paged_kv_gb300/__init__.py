@@ -292,5 +292,12 @@ def kv_dequant4(q4: Q4Cache) -> torch.Tensor:
 
 
 def read_device_status(workspace: torch.Tensor) -> int:
-    """Synchronise and return (then clear) the device status word of a workspace."""
-    return int(lib().dkv_read_device_status(workspace.data_ptr(), _stream(workspace)))
+    """Synchronise and return (then clear) the device status word of a workspace.
+
+    After a device error the workspace's merge counters may be left mid-count,
+    so the whole workspace is zero-filled again, ready for the next call.
+    """
+    st = int(lib().dkv_read_device_status(workspace.data_ptr(), _stream(workspace)))
+    if st != DKV_OK:
+        workspace.zero_()
+    return st

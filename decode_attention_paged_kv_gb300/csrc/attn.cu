@@ -29,11 +29,13 @@
 //     weights keep ~16 significant bits.  At the end of an item warps 1-3 hand
 //     their (max, sum, o) to warp 0 through shared memory, which merges them
 //     with its own and writes the item's partial.
-// merge_kernel then combines the chunks of every (b, h) in a fixed tree over
-// ascending chunk indices, writes out, and resets the work counter.  Partials
-// do not depend on which CTA computed them and chunking depends only on
-// (P, d), so results are deterministic and one kv head at a time gives
-// bitwise the all-heads result.
+// The chunks of every (b, h) are merged in ascending chunk order: for up to
+// kInKernelMergeChunks chunks per (batch, kv head) by the CTA that finishes a
+// unit's last chunk (a per-unit atomic ticket), else by merge_kernel.  The
+// choice, like the chunking, depends only on (P, d); partials do not depend on
+// which CTA computed them.  So results are deterministic and one kv head at a
+// time gives bitwise the all-heads result.  The last CTA to stop fetching
+// work resets the work counter; tickets reset themselves.
 // Every mbarrier wait is bounded; on expiry the kernel records a timeout in
 // the status word, stops issuing, drains the copies it issued and exits.
 
@@ -149,6 +151,66 @@ __device__ int build_sparse_list(const AttnArgs& a, int b, int kvh, int chunk, i
   return max(0, min(count, hi) - lo);
 }
 
+__device__ __forceinline__ void store_out(void* out, int out_dtype, int64_t off, float v) {
+  if (out_dtype == 2) {
+    static_cast<float*>(out)[off] = v;
+  } else if (out_dtype == 1) {
+    static_cast<__half*>(out)[off] = __float2half_rn(v);
+  } else {
+    static_cast<__nv_bfloat16*>(out)[off] = __float2bfloat16_rn(v);
+  }
+}
+
+// Merge the n_chunks (<= kInKernelMergeChunks) partials of the G query heads
+// of one unit, in ascending chunk order, and write out.  Run by the consumer
+// warps of the CTA that finished the unit's last chunk; `scratch` holds
+// (8 x 32) weights, (8 x 32) sums and 8 totals.
+template <int D>
+__device__ void merge_unit(const AttnArgs& a, int b, int kvh, float* scratch) {
+  constexpr int kT = kConsumerWarps * 32;
+  constexpr int kC = kInKernelMergeChunks;
+  float* s_w = scratch;           // [8][kC] max, then weights
+  float* s_l = scratch + 8 * kC;  // [8][kC]
+  float* s_L = scratch + 16 * kC; // [8]
+  const int nc = a.n_chunks;
+  const int64_t row0 = static_cast<int64_t>(b) * a.Hq + kvh * a.G;
+  for (int t = threadIdx.x; t < a.G * nc; t += kT) {
+    const int h = t / nc, k = t % nc;
+    const int64_t pi = (row0 + h) * nc + k;
+    s_w[h * kC + k] = __ldcg(a.part_ml + 2 * pi);
+    s_l[h * kC + k] = __ldcg(a.part_ml + 2 * pi + 1);
+  }
+  consumers_sync();
+  if (threadIdx.x < a.G) {
+    const int h = threadIdx.x;
+    float M = -INFINITY;
+    for (int k = 0; k < nc; ++k) M = fmaxf(M, s_w[h * kC + k]);
+    float L = 0.f;
+    for (int k = 0; k < nc; ++k) {
+      const float m = s_w[h * kC + k];
+      const float w = (m == -INFINITY) ? 0.f : exp2f(m - M);
+      L += w * s_l[h * kC + k];
+      s_w[h * kC + k] = w;
+    }
+    s_L[h] = L;
+  }
+  consumers_sync();
+  for (int idx = threadIdx.x; idx < a.G * D; idx += kT) {
+    const int h = idx / D, c = idx % D;
+    const float* src = a.part_o + (row0 + h) * nc * D + c;
+    float x[kC];
+#pragma unroll
+    for (int k = 0; k < kC; ++k) x[k] = (k < nc) ? __ldcg(src + static_cast<int64_t>(k) * D) : 0.f;
+    float O = 0.f;
+#pragma unroll
+    for (int k = 0; k < kC; ++k) {
+      const float w = (k < nc) ? s_w[h * kC + k] : 0.f;
+      O += (w != 0.f) ? w * x[k] : 0.f;  // empty partials hold no o values
+    }
+    store_out(a.out, a.out_dtype, b * a.o_sb + (kvh * a.G + h) * a.o_sh + c, O / s_L[h]);
+  }
+}
+
 template <int D, bool F16, bool SPARSE>
 __global__ void __launch_bounds__(kAttnThreads)
     attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mk,
@@ -167,6 +229,7 @@ __global__ void __launch_bounds__(kAttnThreads)
   float* mrg = reinterpret_cast<float*>(smem + C::kMergeOffset);
   int2* list = reinterpret_cast<int2*>(smem + C::kListOffset);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOffset);
+  volatile int* s_last = reinterpret_cast<volatile int*>(smem + C::kMiscOffset + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -276,6 +339,16 @@ __global__ void __launch_bounds__(kAttnThreads)
           mbar_wait_bounded(full0 + 8 * (w * C::kSub + c % C::kSub), (c / C::kSub) & 1,
                             deadline - now, nullptr);
         }
+      }
+    }
+    if (lane == 0) {
+      // This CTA fetches no more work.  The last CTA to get here resets the
+      // counters for the next call (every earlier fetch is ordered before its
+      // exit ticket by the fence).
+      __threadfence();
+      if (atomicAdd(a.exit_counter, 1u) == gridDim.x - 1) {
+        atomicExch(a.work_counter, 0u);
+        atomicExch(a.exit_counter, 0u);
       }
     }
     return;
@@ -451,8 +524,23 @@ __global__ void __launch_bounds__(kAttnThreads)
         a.part_ml[2 * pi] = M;
         a.part_ml[2 * pi + 1] = L;
       }
+      if (a.merge_here) __threadfence();  // this lane's partial, before the ticket
+    }
+    if (warp == 0 && a.merge_here) {
+      __syncwarp();
+      if (lane == 0) {
+        uint32_t* t = a.unit_tickets + unit;
+        const bool last = atomicAdd(t, 1u) == static_cast<uint32_t>(a.n_chunks - 1);
+        if (last) atomicExch(t, 0u);  // all chunks of the unit are in: reset
+        *s_last = last;
+      }
     }
     consumers_sync();  // merge area free again; the descriptor slot was read by all
+    if (a.merge_here && *s_last) {
+      __threadfence();
+      merge_unit<D>(a, b, kvh, mrg);
+      consumers_sync();
+    }
     if (threadIdx.x == 0) mbar_arrive(dempty0 + 8 * slot);
   }
 }
@@ -460,13 +548,12 @@ __global__ void __launch_bounds__(kAttnThreads)
 // One CTA per (b, h) row and 32 output channels.  Thread (cg, cq) folds the
 // chunks k = cg, cg + 32, ... (ascending) for 4 channels with an online max;
 // the 32 chunk groups are then folded in ascending order.  out = sum w o /
-// sum w l with w = 2^(m - max m).  Also resets the attention work counter.
+// sum w l with w = 2^(m - max m).
 template <int D>
 __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs m) {
   __shared__ float sM[32], sL[32], sO[32][33];
   griddep_launch_dependents();
   griddep_wait();  // the attention grid has finished writing its partials
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *m.work_counter = 0u;
   const int row = blockIdx.x, cb = blockIdx.y;
   const int cg = threadIdx.x >> 3, cq = threadIdx.x & 7;
   const float* ml = m.part_ml + static_cast<int64_t>(row) * m.n_chunks * 2;
@@ -514,14 +601,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs m) {
     }
     const float v = num / den;
     const int b = row / m.Hq, h = row % m.Hq;
-    const int64_t off = b * m.o_sb + h * m.o_sh + 32 * cb + c;
-    if (m.out_dtype == 2) {
-      static_cast<float*>(m.out)[off] = v;
-    } else if (m.out_dtype == 1) {
-      static_cast<__half*>(m.out)[off] = __float2half_rn(v);
-    } else {
-      static_cast<__nv_bfloat16*>(m.out)[off] = __float2bfloat16_rn(v);
-    }
+    store_out(m.out, m.out_dtype, b * m.o_sb + h * m.o_sh + 32 * cb + c, v);
   }
 }
 

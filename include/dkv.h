@@ -31,9 +31,10 @@
  *     aligned.  The library allocates no device memory and keeps no per-call
  *     state.  Scratch space is a caller-owned `workspace` of
  *     dkv_workspace_bytes() bytes, zero-filled once before its first use; each
- *     call returns the workspace's work counter to zero, so it can be reused
- *     by any later call (of any shape that fits).  One workspace serves one
- *     call at a time: calls that may overlap on the GPU need separate ones.
+ *     call that completes returns the workspace's counters to zero, so it can
+ *     be reused by any later call (of any shape that fits).  After a device
+ *     error (dkv_read_device_status) zero-fill it again.  One workspace serves
+ *     one call at a time: calls that may overlap on the GPU need separate ones.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *     stream).  Every call is asynchronous on that stream; only
  *     dkv_read_device_status synchronises.
