@@ -28,7 +28,6 @@ struct WsLayout {
   size_t status = 0;     // u32 device status word (first 256 bytes)
   size_t counter = 0;    // u32 attention work counter, zero between calls
   size_t exit_counter = 0;  // u32 CTAs done fetching, zero between calls
-  size_t tickets = 0;    // u32 [B * Hkv] chunks merged per unit, zero between calls
   size_t part_ml = 0;    // [B, Hq, n_chunks, 2] fp32
   size_t part_o = 0;     // [B, Hq, n_chunks, d] fp32
   size_t scores = 0;     // sparse: [B, Hq, P] fp32
@@ -65,8 +64,6 @@ WsLayout layout_for(const dkv_params& p, int top_k) {
   L.counter = 4;
   L.exit_counter = 8;
   size_t off = kAlign;
-  L.tickets = off;
-  off = align_up(off + sizeof(uint32_t) * units);
   if (top_k > 0) {
     L.scores = off;
     off = align_up(off + sizeof(float) * rows * P);
@@ -267,34 +264,27 @@ static dkv::AttnArgs attn_args(const dkv_params* p, const void* q, const WsLayou
   a.part_o = reinterpret_cast<float*>(ws + L.part_o);
   a.work_counter = reinterpret_cast<uint32_t*>(ws + L.counter);
   a.exit_counter = reinterpret_cast<uint32_t*>(ws + L.exit_counter);
-  a.unit_tickets = reinterpret_cast<uint32_t*>(ws + L.tickets);
-  a.merge_here = L.n_chunks <= dkv::kInKernelMergeChunks;
   a.status = reinterpret_cast<uint32_t*>(ws + L.status);
   a.wait_limit_ns = (p->flags & DKV_FLAG_FORCE_TIMEOUT) ? 0 : kWaitLimitNs;
   return a;
 }
 
-// Persistent attention over all work items; the split-K merge into out runs in
-// the same kernel for short chunk lists, else in merge_kernel.
-static dkv_status run_attention(const dkv_params* p, dkv::AttnArgs a, bool sparse, bool f16,
-                                const CUtensorMap& mk, const CUtensorMap& mv, void* out,
-                                int32_t out_dtype, cudaStream_t s) {
+// Persistent attention over all work items, then the split-K merge into out.
+static dkv_status run_attention(const dkv_params* p, const dkv::AttnArgs& a, bool sparse,
+                                bool f16, const CUtensorMap& mk, const CUtensorMap& mv,
+                                void* out, int32_t out_dtype, cudaStream_t s) {
   const int sms = current_sm_count();
   if (sms <= 0) return DKV_ERR_CUDA;
-  a.out = out;
-  a.out_dtype = out_code(out_dtype);
-  a.o_sb = p->o_stride_b;
-  a.o_sh = p->o_stride_h;
   dkv_status st =
       cuda_status(dkv::launch_attn(p->head_dim, f16, sparse, a, mk, mv, sms, s));
-  if (st != DKV_OK || a.merge_here) return st;
+  if (st != DKV_OK) return st;
   dkv::MergeArgs m{};
   m.part_ml = a.part_ml;
   m.part_o = a.part_o;
   m.n_chunks = a.n_chunks;
   m.Hq = p->num_q_heads;
   m.out = out;
-  m.out_dtype = a.out_dtype;
+  m.out_dtype = out_code(out_dtype);
   m.o_sb = p->o_stride_b;
   m.o_sh = p->o_stride_h;
   return cuda_status(dkv::launch_merge(p->head_dim, m, p->batch * p->num_q_heads, s));

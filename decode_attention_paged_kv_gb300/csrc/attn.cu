@@ -29,13 +29,11 @@
 //     weights keep ~16 significant bits.  At the end of an item warps 1-3 hand
 //     their (max, sum, o) to warp 0 through shared memory, which merges them
 //     with its own and writes the item's partial.
-// The chunks of every (b, h) are merged in ascending chunk order: for up to
-// kInKernelMergeChunks chunks per (batch, kv head) by the CTA that finishes a
-// unit's last chunk (a per-unit atomic ticket), else by merge_kernel.  The
-// choice, like the chunking, depends only on (P, d); partials do not depend on
-// which CTA computed them.  So results are deterministic and one kv head at a
-// time gives bitwise the all-heads result.  The last CTA to stop fetching
-// work resets the work counter; tickets reset themselves.
+// merge_kernel then combines the chunks of every (b, h) in a fixed order and
+// writes out.  Its structure, like the chunking, depends only on (P, d), and
+// partials do not depend on which CTA computed them, so results are
+// deterministic and one kv head at a time gives bitwise the all-heads result.
+// The last CTA to stop fetching work resets the work counter.
 // Every mbarrier wait is bounded; on expiry the kernel records a timeout in
 // the status word, stops issuing, drains the copies it issued and exits.
 
@@ -161,56 +159,6 @@ __device__ __forceinline__ void store_out(void* out, int out_dtype, int64_t off,
   }
 }
 
-// Merge the n_chunks (<= kInKernelMergeChunks) partials of the G query heads
-// of one unit, in ascending chunk order, and write out.  Run by the consumer
-// warps of the CTA that finished the unit's last chunk; `scratch` holds
-// (8 x 32) weights, (8 x 32) sums and 8 totals.
-template <int D>
-__device__ void merge_unit(const AttnArgs& a, int b, int kvh, float* scratch) {
-  constexpr int kT = kConsumerWarps * 32;
-  constexpr int kC = kInKernelMergeChunks;
-  float* s_w = scratch;           // [8][kC] max, then weights
-  float* s_l = scratch + 8 * kC;  // [8][kC]
-  float* s_L = scratch + 16 * kC; // [8]
-  const int nc = a.n_chunks;
-  const int64_t row0 = static_cast<int64_t>(b) * a.Hq + kvh * a.G;
-  for (int t = threadIdx.x; t < a.G * nc; t += kT) {
-    const int h = t / nc, k = t % nc;
-    const int64_t pi = (row0 + h) * nc + k;
-    s_w[h * kC + k] = __ldcg(a.part_ml + 2 * pi);
-    s_l[h * kC + k] = __ldcg(a.part_ml + 2 * pi + 1);
-  }
-  consumers_sync();
-  if (threadIdx.x < a.G) {
-    const int h = threadIdx.x;
-    float M = -INFINITY;
-    for (int k = 0; k < nc; ++k) M = fmaxf(M, s_w[h * kC + k]);
-    float L = 0.f;
-    for (int k = 0; k < nc; ++k) {
-      const float m = s_w[h * kC + k];
-      const float w = (m == -INFINITY) ? 0.f : exp2f(m - M);
-      L += w * s_l[h * kC + k];
-      s_w[h * kC + k] = w;
-    }
-    s_L[h] = L;
-  }
-  consumers_sync();
-  for (int idx = threadIdx.x; idx < a.G * D; idx += kT) {
-    const int h = idx / D, c = idx % D;
-    const float* src = a.part_o + (row0 + h) * nc * D + c;
-    float x[kC];
-#pragma unroll
-    for (int k = 0; k < kC; ++k) x[k] = (k < nc) ? __ldcg(src + static_cast<int64_t>(k) * D) : 0.f;
-    float O = 0.f;
-#pragma unroll
-    for (int k = 0; k < kC; ++k) {
-      const float w = (k < nc) ? s_w[h * kC + k] : 0.f;
-      O += (w != 0.f) ? w * x[k] : 0.f;  // empty partials hold no o values
-    }
-    store_out(a.out, a.out_dtype, b * a.o_sb + (kvh * a.G + h) * a.o_sh + c, O / s_L[h]);
-  }
-}
-
 template <int D, bool F16, bool SPARSE>
 __global__ void __launch_bounds__(kAttnThreads)
     attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mk,
@@ -229,7 +177,6 @@ __global__ void __launch_bounds__(kAttnThreads)
   float* mrg = reinterpret_cast<float*>(smem + C::kMergeOffset);
   int2* list = reinterpret_cast<int2*>(smem + C::kListOffset);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOffset);
-  volatile int* s_last = reinterpret_cast<volatile int*>(smem + C::kMiscOffset + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -524,84 +471,68 @@ __global__ void __launch_bounds__(kAttnThreads)
         a.part_ml[2 * pi] = M;
         a.part_ml[2 * pi + 1] = L;
       }
-      if (a.merge_here) __threadfence();  // this lane's partial, before the ticket
-    }
-    if (warp == 0 && a.merge_here) {
-      __syncwarp();
-      if (lane == 0) {
-        uint32_t* t = a.unit_tickets + unit;
-        const bool last = atomicAdd(t, 1u) == static_cast<uint32_t>(a.n_chunks - 1);
-        if (last) atomicExch(t, 0u);  // all chunks of the unit are in: reset
-        *s_last = last;
-      }
     }
     consumers_sync();  // merge area free again; the descriptor slot was read by all
-    if (a.merge_here && *s_last) {
-      __threadfence();
-      merge_unit<D>(a, b, kvh, mrg);
-      consumers_sync();
-    }
     if (threadIdx.x == 0) mbar_arrive(dempty0 + 8 * slot);
   }
 }
 
-// One CTA per (b, h) row and 32 output channels.  Thread (cg, cq) folds the
-// chunks k = cg, cg + 32, ... (ascending) for 4 channels with an online max;
-// the 32 chunk groups are then folded in ascending order.  out = sum w o /
-// sum w l with w = 2^(m - max m).
+// One CTA per (b, h) row; D * S threads, S = ceil(n_chunks / 32) slices.
+//   1. (m_k, l_k) of all chunks into shared memory; warp 0 takes the max M and
+//      the weights w_k = 2^(m_k - M) (0 for empty chunks) and L = sum w_k l_k,
+//      each lane over chunks lane, lane + 32, ... then a fixed shuffle tree.
+//   2. thread (slice s, channel c) sums w_k o_k[c] over its <= 32 chunks with
+//      every load in flight; the S slice sums are added in order.
+// out = sum / L.  A fixed order throughout: deterministic.
 template <int D>
-__global__ void __launch_bounds__(256) merge_kernel(const MergeArgs m) {
-  __shared__ float sM[32], sL[32], sO[32][33];
+__global__ void __launch_bounds__(1024) merge_kernel(const MergeArgs m) {
+  __shared__ float s_w[kMaxChunks], s_l[kMaxChunks], s_o[kMaxChunks / 32][D];
+  __shared__ float s_L;
   griddep_launch_dependents();
   griddep_wait();  // the attention grid has finished writing its partials
-  const int row = blockIdx.x, cb = blockIdx.y;
-  const int cg = threadIdx.x >> 3, cq = threadIdx.x & 7;
-  const float* ml = m.part_ml + static_cast<int64_t>(row) * m.n_chunks * 2;
-  const float* po = m.part_o + static_cast<int64_t>(row) * m.n_chunks * D + 32 * cb + 4 * cq;
-  float M = -INFINITY, L = 0.f, O[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-  for (int k = cg; k < m.n_chunks; k += 32) {
-    const float mk = __ldcg(ml + 2 * k);
-    const float lk = __ldcg(ml + 2 * k + 1);
-    const float4 ok = __ldcg(reinterpret_cast<const float4*>(po + static_cast<int64_t>(k) * D));
-    if (mk == -INFINITY) continue;  // empty chunk: no o values
-    if (mk > M) {
-      const float f = exp2f(M - mk);
-      L *= f;
-      O[0] *= f;
-      O[1] *= f;
-      O[2] *= f;
-      O[3] *= f;
-      M = mk;
-    }
-    const float w = exp2f(mk - M);
-    L += w * lk;
-    O[0] += w * ok.x;
-    O[1] += w * ok.y;
-    O[2] += w * ok.z;
-    O[3] += w * ok.w;
+  const int row = blockIdx.x, nc = m.n_chunks;
+  const float* ml = m.part_ml + static_cast<int64_t>(row) * nc * 2;
+  for (int k = threadIdx.x; k < nc; k += blockDim.x) {
+    s_w[k] = __ldcg(ml + 2 * k);
+    s_l[k] = __ldcg(ml + 2 * k + 1);
   }
-  if (cq == 0) {
-    sM[cg] = M;
-    sL[cg] = L;
-  }
-#pragma unroll
-  for (int e = 0; e < 4; ++e) sO[cg][4 * cq + e] = O[e];
   __syncthreads();
   if (threadIdx.x < 32) {
-    const int c = threadIdx.x;
-    float Mx = -INFINITY;
-    for (int i = 0; i < 32; ++i) Mx = fmaxf(Mx, sM[i]);
-    float num = 0.f, den = 0.f;
-    for (int i = 0; i < 32; ++i) {
-      if (sM[i] == -INFINITY) continue;
-      const float w = exp2f(sM[i] - Mx);
-      num += w * sO[i][c];
-      den += w * sL[i];
+    const int lane = threadIdx.x;
+    float M = -INFINITY;
+    for (int k = lane; k < nc; k += 32) M = fmaxf(M, s_w[k]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float L = 0.f;
+    for (int k = lane; k < nc; k += 32) {
+      const float w = (s_w[k] == -INFINITY) ? 0.f : exp2f(s_w[k] - M);
+      L += w * s_l[k];
+      s_w[k] = w;
     }
-    const float v = num / den;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    if (lane == 0) s_L = L;
+  }
+  __syncthreads();
+  const int c = threadIdx.x % D, sl = threadIdx.x / D;
+  const int k0 = sl * 32, k1 = min(nc, k0 + 32);
+  const float* po = m.part_o + (static_cast<int64_t>(row) * nc + k0) * D + c;
+  float x[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) x[i] = (k0 + i < k1) ? __ldcg(po + static_cast<int64_t>(i) * D) : 0.f;
+  float O = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float w = (k0 + i < k1) ? s_w[k0 + i] : 0.f;
+    O += (w != 0.f) ? w * x[i] : 0.f;  // empty chunks hold no o values
+  }
+  s_o[sl][c] = O;
+  __syncthreads();
+  if (threadIdx.x < D) {
+    float sum = 0.f;
+    for (int i = 0; i < blockDim.x / D; ++i) sum += s_o[i][c];
     const int b = row / m.Hq, h = row % m.Hq;
-    store_out(m.out, m.out_dtype, b * m.o_sb + h * m.o_sh + 32 * cb + c, v);
+    store_out(m.out, m.out_dtype, b * m.o_sb + h * m.o_sh + c, sum / s_L);
   }
 }
 
@@ -635,7 +566,8 @@ cudaError_t launch_attn(int d, bool f16, bool sparse, const AttnArgs& a, const C
 }
 
 cudaError_t launch_merge(int d, const MergeArgs& m, int rows, cudaStream_t s) {
-  const dim3 grid(rows, d / 32), block(256);
+  const int slices = static_cast<int>(ceil_div(m.n_chunks, 32));
+  const dim3 grid(rows), block(d * slices);
   return d == 128 ? launch_pdl(merge_kernel<128>, grid, block, 0, s, m)
                   : launch_pdl(merge_kernel<64>, grid, block, 0, s, m);
 }

@@ -19,10 +19,6 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // Split-K: a (batch, kv head) is cut into at most kMaxChunks chunks of pages;
 // each chunk's partial (max, sum, o) is merged by merge_kernel.
 constexpr int kMaxChunks = 256;
-// Up to this many chunks per (batch, kv head) the attention kernel merges the
-// partials itself (the CTA that finishes a unit's last chunk); beyond it,
-// merge_kernel does, with more parallelism.
-constexpr int kInKernelMergeChunks = 32;
 
 // Pages one attention work item streams in the exact path: 512 KiB of K+V at
 // least, more for long contexts so a (batch, kv head) never has more than
@@ -60,11 +56,6 @@ struct AttnArgs {
   float* part_o;               // [B, Hq, n_chunks, d]  unnormalised
   uint32_t* work_counter;      // next work item; zero between calls
   uint32_t* exit_counter;      // CTAs done fetching; zero between calls
-  uint32_t* unit_tickets;      // [B * Hkv] chunks finished per unit; zero between calls
-  bool merge_here;             // n_chunks <= kInKernelMergeChunks: merge in this kernel
-  void* out;
-  int out_dtype;               // 0 bf16, 1 fp16, 2 fp32
-  int64_t o_sb, o_sh;
   const uint32_t* bitmaps;     // sparse path: [B, Hq, W32] selected-page bits
   int W32;
   uint32_t* status;

@@ -113,25 +113,24 @@ __device__ __forceinline__ uint32_t score_key(float f) {
 }
 
 constexpr int kTopkThreads = 256;
-constexpr size_t kTopkSmemKeyBytes = 192 * 1024;  // rows of up to 49152 pages
+constexpr size_t kTopkSmemKeyBytes = 160 * 1024;  // rows of up to 40960 pages
+constexpr int kTopkMaxWordsSmem = 2048;           // bitmap words built in shared memory
 
-// Block-wide exclusive prefix count of `flag`; *total gets the block total.
-__device__ __forceinline__ int block_excl_count(bool flag, int* warp_tot, int* total) {
+// Block-wide exclusive prefix sum of v.
+__device__ __forceinline__ long long block_excl_sum(long long v, long long* warp_tot) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t bal = __ballot_sync(0xffffffffu, flag);
-  const int in_warp = __popc(bal & ((1u << lane) - 1u));
-  if (lane == 0) warp_tot[warp] = __popc(bal);
-  __syncthreads();
-  int before = 0, tot = 0;
+  long long incl = v;
 #pragma unroll
-  for (int w = 0; w < kTopkThreads / 32; ++w) {
-    const int v = warp_tot[w];
-    before += (w < warp) ? v : 0;
-    tot += v;
+  for (int off = 1; off < 32; off <<= 1) {
+    const long long t = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += t;
   }
+  if (lane == 31) warp_tot[warp] = incl;
   __syncthreads();
-  *total = tot;
-  return before + in_warp;
+  long long before = 0;
+#pragma unroll
+  for (int w = 0; w < kTopkThreads / 32; ++w) before += (w < warp) ? warp_tot[w] : 0;
+  return before + incl - v;
 }
 
 // Keys of one row: staged in shared memory once when they fit, else re-read
@@ -142,18 +141,26 @@ struct RowKeys {
   const uint32_t* s;
   __device__ __forceinline__ uint32_t operator()(int j) const {
     if constexpr (SMEM) return s[j];
-    return score_key(r[j]);
+    return score_key(__ldcg(r + j));
   }
 };
 
+// One CTA per (b, h) row.  Radix select on 8-bit digits, most significant
+// first: each pass histograms the digit of the keys that still match the
+// prefix (one shared atomic per distinct digit per warp), and warp 0 finds the
+// digit that holds the K-th largest key.  Then every thread takes a contiguous
+// range of pages: keys above the threshold are in, keys equal to it are in for
+// the first `need` of them in page order; one block scan gives every thread
+// its output position, so pages come out ascending.
 template <bool SMEM>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
   extern __shared__ uint32_t s_keys[];
   __shared__ uint32_t hist[256];
-  __shared__ int warp_tot[kTopkThreads / 32];
+  __shared__ long long warp_tot[kTopkThreads / 32];
   __shared__ uint32_t s_digit, s_above;
+  __shared__ uint32_t s_bits[kTopkMaxWordsSmem];
   const int row = blockIdx.x;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
   griddep_launch_dependents();
   griddep_wait();  // the scores come from the previous kernel
   const float* r = a.scores + static_cast<int64_t>(row) * a.P;
@@ -162,6 +169,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
     for (int j = tid; j < a.P; j += kTopkThreads) s_keys[j] = score_key(__ldcg(r + j));
   }
   const RowKeys<SMEM> key{r, s_keys};
+  const int P_round = (a.P + kTopkThreads - 1) / kTopkThreads * kTopkThreads;
 
   uint32_t prefix = 0, mask = 0;
   int need = a.kk;  // still to choose among keys matching `prefix` under `mask`
@@ -169,9 +177,15 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
     const int shift = 24 - 8 * pass;
     hist[tid] = 0;
     __syncthreads();
-    for (int j = tid; j < a.P; j += kTopkThreads) {
-      const uint32_t k = key(j);
-      if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 0xffu], 1u);
+    for (int j = tid; j < P_round; j += kTopkThreads) {
+      const uint32_t k = (j < a.P) ? key(j) : 0u;
+      const bool in = (j < a.P) && (k & mask) == prefix;
+      const uint32_t digit = (k >> shift) & 0xffu;
+      const uint32_t act = __ballot_sync(0xffffffffu, in);
+      if (in) {
+        const uint32_t peers = __match_any_sync(act, digit);
+        if (lane == __ffs(peers) - 1) atomicAdd(&hist[digit], static_cast<uint32_t>(__popc(peers)));
+      }
     }
     __syncthreads();
     if (tid < 32) {
@@ -208,24 +222,44 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
     if (all_taken) break;
   }
 
-  // Keys above the threshold prefix are in; of those equal to it, the first
-  // `need` in ascending page order.  Emit ascending.
-  int eq_before = 0, sel_before = 0;
-  for (int base = 0; base < a.P; base += kTopkThreads) {
-    const int j = base + tid;
-    const uint32_t k = (j < a.P) ? (key(j) & mask) : 0u;
-    const bool gt = (j < a.P) && k > prefix;
-    const bool eq = (j < a.P) && k == prefix;
-    int eq_tot, sel_tot;
-    const int eq_rank = eq_before + block_excl_count(eq, warp_tot, &eq_tot);
-    const bool sel = gt || (eq && eq_rank < need);
-    const int pos = sel_before + block_excl_count(sel, warp_tot, &sel_tot);
-    if (sel && pos < a.kk) a.selected[static_cast<int64_t>(row) * a.kk + pos] = j;
-    const uint32_t bal = __ballot_sync(0xffffffffu, sel);
-    const int word = (base >> 5) + (tid >> 5);
-    if ((tid & 31) == 0 && word < a.W32) a.bitmaps[static_cast<int64_t>(row) * a.W32 + word] = bal;
-    eq_before += eq_tot;
-    sel_before += sel_tot;
+  // Contiguous page range of this thread; counts of keys above / equal.
+  const int per = (a.P + kTopkThreads - 1) / kTopkThreads;
+  const int j0 = min(a.P, tid * per), j1 = min(a.P, j0 + per);
+  int gt = 0, eq = 0;
+  for (int j = j0; j < j1; ++j) {
+    const uint32_t k = key(j) & mask;
+    gt += k > prefix;
+    eq += k == prefix;
+  }
+  const bool bits_in_smem = a.W32 <= kTopkMaxWordsSmem;
+  if (bits_in_smem)
+    for (int w = tid; w < a.W32; w += kTopkThreads) s_bits[w] = 0u;
+  // One scan of (gt << 32 | eq): both sums stay below 2^31.
+  const long long before =
+      block_excl_sum((static_cast<long long>(gt) << 32) | static_cast<long long>(eq), warp_tot);
+  int gt_before = static_cast<int>(before >> 32);
+  int eq_before = static_cast<int>(before & 0xffffffffll);
+  for (int j = j0; j < j1; ++j) {
+    const uint32_t k = key(j) & mask;
+    bool sel = false;
+    if (k > prefix) {
+      sel = true;
+    } else if (k == prefix) {
+      sel = eq_before < need;
+      ++eq_before;
+    }
+    if (sel) {
+      const int pos = gt_before + min(eq_before - (k == prefix ? 1 : 0), need);
+      a.selected[static_cast<int64_t>(row) * a.kk + pos] = j;
+      if (bits_in_smem) atomicOr(&s_bits[j >> 5], 1u << (j & 31));
+      else atomicOr(&a.bitmaps[static_cast<int64_t>(row) * a.W32 + (j >> 5)], 1u << (j & 31));
+      if (k > prefix) ++gt_before;
+    }
+  }
+  if (bits_in_smem) {
+    __syncthreads();
+    for (int w = tid; w < a.W32; w += kTopkThreads)
+      a.bitmaps[static_cast<int64_t>(row) * a.W32 + w] = s_bits[w];
   }
 }
 
@@ -250,6 +284,12 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
                                          static_cast<int>(kTopkSmemKeyBytes));
     if (e != cudaSuccess) return e;
     return launch_pdl(topk_kernel<true>, dim3(a.rows), dim3(kTopkThreads), key_bytes, s, a);
+  }
+  // Large rows set their bitmap bits straight in global memory: clear it first.
+  if (a.W32 > kTopkMaxWordsSmem) {
+    cudaError_t e = cudaMemsetAsync(a.bitmaps, 0,
+                                    sizeof(uint32_t) * static_cast<size_t>(a.rows) * a.W32, s);
+    if (e != cudaSuccess) return e;
   }
   return launch_pdl(topk_kernel<false>, dim3(a.rows), dim3(kTopkThreads), 0, s, a);
 }
