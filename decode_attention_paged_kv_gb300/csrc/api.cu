@@ -7,6 +7,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/dkv.h"
@@ -30,11 +31,13 @@ struct WsLayout {
   size_t exit_counter = 0;  // u32 CTAs done fetching, zero between calls
   size_t part_ml = 0;    // [B, Hq, n_chunks, 2] fp32
   size_t part_o = 0;     // [B, Hq, n_chunks, d] fp32
-  size_t scores = 0;     // sparse: [B, Hq, P] fp32
+  size_t scores = 0;     // sparse: [B, Hq, P] fp32 (fallback selection only)
   size_t selected = 0;   // sparse: [B, Hq, kk] int32 (used when the caller passes none)
-  size_t bitmaps = 0;    // sparse: [B, Hq, W32] u32
+  size_t bitmaps = 0;    // sparse: [B, Hq, W32] u32 (fallback selection only)
+  size_t union_list = 0; // sparse: [B * Hkv, union_stride] (page, head mask)
+  size_t union_count = 0;  // sparse: [B * Hkv] int32
   size_t total = 0;
-  int n_chunks = 0, pages_per_chunk = 0, kk = 0, W32 = 0;
+  int n_chunks = 0, pages_per_chunk = 0, kk = 0, W32 = 0, union_stride = 0;
   int64_t n_items = 0;
   bool ok = true;        // false: the sizes exceed what the kernels cover
 };
@@ -53,6 +56,7 @@ WsLayout layout_for(const dkv_params& p, int top_k) {
     L.kk = static_cast<int>(top_k < P ? top_k : P);
     L.W32 = static_cast<int>(ceil_div(P, 32));
     const int64_t union_max = (static_cast<int64_t>(G) * L.kk < P) ? G * L.kk : P;
+    L.union_stride = static_cast<int>(union_max);
     L.pages_per_chunk = dkv::select_pages_per_chunk(union_max, d);
     if (L.pages_per_chunk > dkv::kMaxSelectList) L.ok = false;
     L.n_chunks = static_cast<int>(ceil_div(union_max, L.pages_per_chunk));
@@ -71,6 +75,10 @@ WsLayout layout_for(const dkv_params& p, int top_k) {
     off = align_up(off + sizeof(int32_t) * rows * L.kk);
     L.bitmaps = off;
     off = align_up(off + sizeof(uint32_t) * rows * L.W32);
+    L.union_list = off;
+    off = align_up(off + 8 * static_cast<size_t>(units) * L.union_stride);
+    L.union_count = off;
+    off = align_up(off + sizeof(int32_t) * units);
   }
   L.part_ml = off;
   off = align_up(off + sizeof(float) * 2 * rows * L.n_chunks);
@@ -273,6 +281,7 @@ static dkv::AttnArgs attn_args(const dkv_params* p, const void* q, const WsLayou
 static dkv_status run_attention(const dkv_params* p, const dkv::AttnArgs& a, bool sparse,
                                 bool f16, const CUtensorMap& mk, const CUtensorMap& mv,
                                 void* out, int32_t out_dtype, cudaStream_t s) {
+  // (sparse: a.union_count tells the merge how many chunks of a unit hold pages)
   const int sms = current_sm_count();
   if (sms <= 0) return DKV_ERR_CUDA;
   dkv_status st =
@@ -287,6 +296,10 @@ static dkv_status run_attention(const dkv_params* p, const dkv::AttnArgs& a, boo
   m.out_dtype = out_code(out_dtype);
   m.o_sb = p->o_stride_b;
   m.o_sh = p->o_stride_h;
+  m.union_count = sparse ? a.union_count : nullptr;
+  m.pages_per_chunk = a.pages_per_chunk;
+  m.G = a.G;
+  m.Hkv = a.Hkv;
   return cuda_status(dkv::launch_merge(p->head_dim, m, p->batch * p->num_q_heads, s));
 }
 
@@ -329,33 +342,76 @@ dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_
   const int G = p->num_q_heads / p->num_kv_heads;
   const bool f16 = K->dtype == DKV_FP16;
 
-  dkv::ScoreArgs sa{};
-  sa.q = q;
-  sa.q_sb = p->q_stride_b;
-  sa.q_sh = p->q_stride_h;
-  sa.meta_min = meta_min;
-  sa.meta_max = meta_max;
-  sa.B = p->batch;
-  sa.Hq = p->num_q_heads;
-  sa.Hkv = p->num_kv_heads;
-  sa.G = G;
-  sa.P = P;
-  sa.scores = reinterpret_cast<float*>(ws + L.scores);
-  if ((st = cuda_status(dkv::launch_score(p->head_dim, f16, sa, s))) != DKV_OK) return st;
+  int32_t* sel = selected != nullptr ? selected : reinterpret_cast<int32_t*>(ws + L.selected);
+  int2* ulist = reinterpret_cast<int2*>(ws + L.union_list);
+  int* ucount = reinterpret_cast<int*>(ws + L.union_count);
 
-  dkv::TopkArgs ta{};
-  ta.scores = sa.scores;
-  ta.rows = p->batch * p->num_q_heads;
-  ta.P = P;
-  ta.kk = L.kk;
-  ta.selected = selected != nullptr ? selected : reinterpret_cast<int32_t*>(ws + L.selected);
-  ta.bitmaps = reinterpret_cast<uint32_t*>(ws + L.bitmaps);
-  ta.W32 = L.W32;
-  if ((st = cuda_status(dkv::launch_topk(ta, s))) != DKV_OK) return st;
+  // Bound scores, per-head top-K and the group's page union: one cluster per
+  // (batch, kv head) when its scores fit in shared memory.
+  dkv::SelectArgs fa{};
+  fa.q = q;
+  fa.q_sb = p->q_stride_b;
+  fa.q_sh = p->q_stride_h;
+  fa.meta_min = meta_min;
+  fa.meta_max = meta_max;
+  fa.B = p->batch;
+  fa.Hq = p->num_q_heads;
+  fa.Hkv = p->num_kv_heads;
+  fa.G = G;
+  fa.P = P;
+  fa.kk = L.kk;
+  fa.W32 = L.W32;
+  fa.cluster = static_cast<int>(std::min<int64_t>(8, std::max<int64_t>(1, ceil_div(P, 256))));
+  fa.ppr = static_cast<int>(ceil_div(ceil_div(P, fa.cluster), 16) * 16);
+  fa.stage_keys = P <= 16384;
+  fa.selected = sel;
+  fa.union_list = ulist;
+  fa.union_count = ucount;
+  fa.union_stride = L.union_stride;
+  if (dkv::select_fused_smem(fa) > 0) {
+    if ((st = cuda_status(dkv::launch_select_fused(p->head_dim, f16, fa, s))) != DKV_OK)
+      return st;
+  } else {
+    dkv::ScoreArgs sa{};
+    sa.q = q;
+    sa.q_sb = p->q_stride_b;
+    sa.q_sh = p->q_stride_h;
+    sa.meta_min = meta_min;
+    sa.meta_max = meta_max;
+    sa.B = p->batch;
+    sa.Hq = p->num_q_heads;
+    sa.Hkv = p->num_kv_heads;
+    sa.G = G;
+    sa.P = P;
+    sa.scores = reinterpret_cast<float*>(ws + L.scores);
+    if ((st = cuda_status(dkv::launch_score(p->head_dim, f16, sa, s))) != DKV_OK) return st;
+    dkv::TopkArgs ta{};
+    ta.scores = sa.scores;
+    ta.rows = p->batch * p->num_q_heads;
+    ta.P = P;
+    ta.kk = L.kk;
+    ta.selected = sel;
+    ta.bitmaps = reinterpret_cast<uint32_t*>(ws + L.bitmaps);
+    ta.W32 = L.W32;
+    if ((st = cuda_status(dkv::launch_topk(ta, s))) != DKV_OK) return st;
+    dkv::UnionArgs ua{};
+    ua.bitmaps = ta.bitmaps;
+    ua.Hq = p->num_q_heads;
+    ua.Hkv = p->num_kv_heads;
+    ua.G = G;
+    ua.P = P;
+    ua.W32 = L.W32;
+    ua.union_list = ulist;
+    ua.union_count = ucount;
+    ua.union_stride = L.union_stride;
+    if ((st = cuda_status(dkv::launch_union(ua, p->batch * p->num_kv_heads, s))) != DKV_OK)
+      return st;
+  }
 
   dkv::AttnArgs a = attn_args(p, q, L, ws);
-  a.bitmaps = ta.bitmaps;
-  a.W32 = L.W32;
+  a.union_list = ulist;
+  a.union_count = ucount;
+  a.union_stride = L.union_stride;
   return run_attention(p, a, true, f16, mk, mv, out, out_dtype, s);
 }
 

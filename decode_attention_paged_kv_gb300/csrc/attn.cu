@@ -12,8 +12,9 @@
 // (batch, kv head, chunk of pages) -- from an atomic counter until none are
 // left.  Inside a CTA:
 //   * warp 4 (producer) takes the next item, turns it into a page list (in the
-//     sparse path: the union of the group's selections, from the per-head
-//     bitmaps, with a bit per query head that chose each page), publishes it
+//     sparse path: its slice of the group's union of selected pages, each with
+//     a bit per query head that chose it; slices past the union are skipped
+//     unpublished), publishes it
 //     through a two-slot descriptor ring and streams the pages' K and V into
 //     shared-memory stages with TMA tensor copies (cp.async.bulk.tensor, 128B
 //     swizzle), one full / empty mbarrier pair per stage.  It runs ahead
@@ -103,52 +104,6 @@ __device__ __forceinline__ bool consumers_any(bool flag) {
   return res != 0;
 }
 
-// Sparse path: the pages of the union of the group's selections whose rank (in
-// ascending page order) falls in [chunk * ppc, (chunk + 1) * ppc), with a
-// bit per query head that selected each page.  Run by one full warp; returns
-// the page count (to every lane).
-__device__ int build_sparse_list(const AttnArgs& a, int b, int kvh, int chunk, int2* list,
-                                 int lane) {
-  const int lo = chunk * a.pages_per_chunk, hi = lo + a.pages_per_chunk;
-  const uint32_t* bm = a.bitmaps + (static_cast<int64_t>(b) * a.Hq + kvh * a.G) * a.W32;
-  int count = 0;
-  for (int w0 = 0; w0 < a.W32 && count < hi; w0 += 32) {
-    const int wi = w0 + lane;
-    uint32_t words[8];
-    uint32_t uni = 0;
-#pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      words[g] = (g < a.G && wi < a.W32) ? bm[static_cast<int64_t>(g) * a.W32 + wi] : 0u;
-      uni |= words[g];
-    }
-    const int c = __popc(uni);
-    int incl = c;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += t;
-    }
-    int r = count + incl - c;
-    if (r < hi && r + c > lo) {
-      uint32_t bits = uni;
-      while (bits) {
-        const int j = __ffs(bits) - 1;
-        bits &= bits - 1;
-        if (r >= lo && r < hi) {
-          uint32_t m = 0;
-#pragma unroll
-          for (int g = 0; g < 8; ++g) m |= ((words[g] >> j) & 1u) << g;
-          list[r - lo] = make_int2(wi * 32 + j, static_cast<int>(m));
-        }
-        ++r;
-      }
-    }
-    count += __shfl_sync(0xffffffffu, incl, 31);
-  }
-  __syncwarp();
-  return max(0, min(count, hi) - lo);
-}
-
 __device__ __forceinline__ void store_out(void* out, int out_dtype, int64_t off, float v) {
   if (out_dtype == 2) {
     static_cast<float*>(out)[off] = v;
@@ -206,10 +161,33 @@ __global__ void __launch_bounds__(kAttnThreads)
     // Pages issued so far to consumer warps 0-3 (each item starts at warp 0).
     int wc0 = 0, wc1 = 0, wc2 = 0, wc3 = 0;
     for (int k = 0;; ++k) {
-      int item = 0;
-      if (lane == 0) item = static_cast<int>(atomicAdd(a.work_counter, 1u));
-      item = __shfl_sync(0xffffffffu, item, 0);
-      if (item >= a.n_items) item = -1;
+      // Next work item with pages (sparse chunks past a unit's union are
+      // skipped here and never published).
+      int item = 0, n = 0, b = 0, kvh = 0, first = 0;
+      while (true) {
+        if (lane == 0) item = static_cast<int>(atomicAdd(a.work_counter, 1u));
+        item = __shfl_sync(0xffffffffu, item, 0);
+        if (item >= a.n_items) {
+          item = -1;
+          break;
+        }
+        const int chunk = item % a.n_chunks;
+        const int unit = item / a.n_chunks;
+        kvh = unit % a.Hkv;
+        b = unit / a.Hkv;
+        first = chunk * a.pages_per_chunk;
+        if constexpr (SPARSE) {
+          const int count = a.union_count[unit];
+          n = max(0, min(count - first, a.pages_per_chunk));
+          if (n == 0) continue;
+          const int2* src = a.union_list + static_cast<int64_t>(unit) * a.union_stride + first;
+          for (int j = lane; j < n; j += 32) list[j] = src[j];
+          __syncwarp();
+        } else {
+          n = max(0, min(a.P - first, a.pages_per_chunk));
+        }
+        break;
+      }
       const int slot = k & 1;
       int ok = 1;
       if (lane == 0 && k >= 2) {
@@ -221,19 +199,6 @@ __global__ void __launch_bounds__(kAttnThreads)
         }
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      int n = 0, b = 0, kvh = 0, first = 0;
-      if (item >= 0) {
-        const int chunk = item % a.n_chunks;
-        const int unit = item / a.n_chunks;
-        kvh = unit % a.Hkv;
-        b = unit / a.Hkv;
-        if constexpr (SPARSE) {
-          n = build_sparse_list(a, b, kvh, chunk, list, lane);
-        } else {
-          first = chunk * a.pages_per_chunk;
-          n = max(0, min(a.P - first, a.pages_per_chunk));
-        }
-      }
       if (lane == 0) {
         desc[slot].item = item;
         desc[slot].n_pages = n;
@@ -490,8 +455,14 @@ __global__ void __launch_bounds__(1024) merge_kernel(const MergeArgs m) {
   __shared__ float s_L;
   griddep_launch_dependents();
   griddep_wait();  // the attention grid has finished writing its partials
-  const int row = blockIdx.x, nc = m.n_chunks;
-  const float* ml = m.part_ml + static_cast<int64_t>(row) * nc * 2;
+  const int row = blockIdx.x, stride = m.n_chunks;
+  int nc = stride;  // chunks holding pages
+  if (m.union_count != nullptr) {
+    const int b = row / m.Hq, h = row % m.Hq;
+    const int count = m.union_count[b * m.Hkv + h / m.G];
+    nc = static_cast<int>(ceil_div(count, m.pages_per_chunk));
+  }
+  const float* ml = m.part_ml + static_cast<int64_t>(row) * stride * 2;
   for (int k = threadIdx.x; k < nc; k += blockDim.x) {
     s_w[k] = __ldcg(ml + 2 * k);
     s_l[k] = __ldcg(ml + 2 * k + 1);
@@ -516,7 +487,7 @@ __global__ void __launch_bounds__(1024) merge_kernel(const MergeArgs m) {
   __syncthreads();
   const int c = threadIdx.x % D, sl = threadIdx.x / D;
   const int k0 = sl * 32, k1 = min(nc, k0 + 32);
-  const float* po = m.part_o + (static_cast<int64_t>(row) * nc + k0) * D + c;
+  const float* po = m.part_o + (static_cast<int64_t>(row) * stride + k0) * D + c;
   float x[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) x[i] = (k0 + i < k1) ? __ldcg(po + static_cast<int64_t>(i) * D) : 0.f;

@@ -14,7 +14,7 @@ constexpr int kPage = 16;             // tokens per page (S)
 constexpr int kConsumerWarps = 4;     // attention: warps that compute
 constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
 
-inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+__host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Split-K: a (batch, kv head) is cut into at most kMaxChunks chunks of pages;
 // each chunk's partial (max, sum, o) is merged by merge_kernel.
@@ -56,8 +56,11 @@ struct AttnArgs {
   float* part_o;               // [B, Hq, n_chunks, d]  unnormalised
   uint32_t* work_counter;      // next work item; zero between calls
   uint32_t* exit_counter;      // CTAs done fetching; zero between calls
-  const uint32_t* bitmaps;     // sparse path: [B, Hq, W32] selected-page bits
-  int W32;
+  // sparse path: per (batch, kv head) the ascending union of the group's
+  // selected pages, as (page, bit per query head that chose it)
+  const int2* union_list;      // [B * Hkv, union_stride]
+  const int* union_count;      // [B * Hkv]
+  int union_stride;
   uint32_t* status;
   uint64_t wait_limit_ns;
 };
@@ -67,6 +70,9 @@ struct MergeArgs {
   const float* part_o;
   int n_chunks;
   int Hq;
+  // sparse path: only the chunks that hold pages, ceil(count / ppc) per unit
+  const int* union_count;      // [B * Hkv] or nullptr (every chunk is valid)
+  int pages_per_chunk, G, Hkv;
   void* out;
   int out_dtype;               // 0 bf16, 1 fp16, 2 fp32
   int64_t o_sb, o_sh;
@@ -87,6 +93,31 @@ struct TopkArgs {
   int32_t* selected;           // [rows, kk]
   uint32_t* bitmaps;           // [rows, W32]
   int W32;
+};
+
+// Fused selection: bound scores, per-head top-K and the group's page union
+// for one (batch, kv head) per thread-block cluster.
+struct SelectArgs {
+  const void* q;
+  int64_t q_sb, q_sh;
+  const void* meta_min;
+  const void* meta_max;
+  int B, Hq, Hkv, G, P, kk, W32;
+  int cluster;                 // CTAs per (batch, kv head)
+  int ppr;                     // pages scored per CTA (multiple of 16)
+  bool stage_keys;             // top-K keys fit in the CTA's shared memory
+  int32_t* selected;           // [B, Hq, kk]
+  int2* union_list;            // [B * Hkv, union_stride]
+  int* union_count;            // [B * Hkv]
+  int union_stride;
+};
+
+struct UnionArgs {
+  const uint32_t* bitmaps;     // [B, Hq, W32]
+  int Hq, Hkv, G, P, W32;
+  int2* union_list;
+  int* union_count;
+  int union_stride;
 };
 
 struct MetaArgs {
@@ -124,6 +155,10 @@ cudaError_t launch_attn(int d, bool f16, bool sparse, const AttnArgs& a, const C
 cudaError_t launch_merge(int d, const MergeArgs& m, int rows, cudaStream_t s);
 cudaError_t launch_score(int d, bool f16, const ScoreArgs& a, cudaStream_t s);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
+cudaError_t launch_union(const UnionArgs& a, int units, cudaStream_t s);
+// Shared memory the fused selection needs per CTA (0 if it does not fit).
+size_t select_fused_smem(const SelectArgs& a);
+cudaError_t launch_select_fused(int d, bool f16, const SelectArgs& a, cudaStream_t s);
 cudaError_t launch_meta(bool q4, bool f16, const MetaArgs& a, cudaStream_t s);
 cudaError_t launch_quant4(int64_t rows, int d, const void* x, void* codes, void* gmin,
                           void* gmax, cudaStream_t s);

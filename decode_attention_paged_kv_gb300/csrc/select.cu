@@ -1,33 +1,52 @@
-// select.cu -- query-aware page selection: bound scores and top-K.
+// select.cu -- query-aware page selection: bound scores, per-head top-K and
+// the union of a query group's selected pages.
 //
 // Bound score ("TinyServe: Query-Aware Cache Selection for Efficient LLM
 // Serving", 相关性函数实例化; Algorithm 1 step 1):
 //   r(q, phi_j) = sum_i (q_i >= 0 ? q_i M_ji : q_i m_ji)
 // Because the two cases are exclusive it equals  q+ . M_j + q- . m_j  with
 // q+ = max(q, 0), q- = min(q, 0): one dot product of length 2d between the
-// page's concatenated metadata [M_j | m_j] and [q+ | q-].  score_kernel runs it
+// page's concatenated metadata [M_j | m_j] and [q+ | q-].  score_tile runs it
 // for 16 pages x (up to 8) query heads per mma.sync m16n8k16 step: pages on the
 // M side straight from global memory (16-byte loads, coalesced rows), the G
 // query heads of the group on the N side.  bf16 x bf16 products are exact in
 // the fp32 accumulator.
 //
 // Top-K (问题公式化定义: S_t = TopK_j r, |S_t| = K; Algorithm 1 step 2, "radix
-// select"): topk_kernel radix-selects the K largest scores of one (b, h) row on
+// select"): radix selection of the K largest scores of one (b, h) on
 // order-preserving 32-bit keys (8-bit digits, most significant first), then
-// writes the selected pages in ascending order; among equal scores the lower
-// page index is taken first.  It also writes a bitmap of the selection, which
-// the sparse attention kernel merges across the heads of a group.
+// the selected pages in ascending order; among equal scores the lower page
+// index is taken first.
+//
+// Union: the pages any query head of a group selected, ascending, each with a
+// bit per head that chose it -- the list the sparse attention gathers (each
+// page once for the whole group).
+//
+// select_fused_kernel does all three for one (batch, kv head) per thread-block
+// cluster: every CTA scores a range of pages into its shared memory; after a
+// cluster barrier CTA r selects for query heads r, r + C, ... reading the
+// peers' scores over distributed shared memory and keeps each head's
+// selection bitmap; after another barrier CTA 0 ORs the bitmaps into the union
+// list.  When a row's scores do not fit in shared memory, score_kernel,
+// topk_kernel and union_kernel do the same through global memory.
 
+#include <cooperative_groups.h>
 #include <math.h>
 
 #include "dkv_device.cuh"
 #include "dkv_kernels.h"
+
+namespace cg = cooperative_groups;
 
 namespace dkv {
 namespace {
 
 constexpr int kScoreWarps = 4;
 constexpr int kScorePagesPerCta = 16 * kScoreWarps;
+constexpr int kSelThreads = 256;  // top-K, union and fused selection CTAs
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr size_t kTopkSmemKeyBytes = 160 * 1024;  // stage rows of up to 40960 pages
+constexpr size_t kFusedSmemBytes = 200 * 1024;
 
 // Split 8 packed 16-bit q values (one 16-byte chunk) into q+ or q-.
 __device__ __forceinline__ uint32_t keep_sign(uint32_t w, bool negative_part) {
@@ -41,67 +60,64 @@ __device__ __forceinline__ uint32_t keep_sign(uint32_t w, bool negative_part) {
   return out;
 }
 
-template <int D, bool F16>
-__global__ void __launch_bounds__(kScoreWarps * 32) score_kernel(const ScoreArgs a) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// B operand of the score MMA for lane (g, t4): [q+ | q-] of query head g of the
+// group (zero for g >= G).  The contraction index runs over the concatenation
+// [M | m]; the lane owns 16-byte chunks c = t4 + 4 s of it, two k-steps each.
+template <int D>
+__device__ __forceinline__ void load_q_pm(const void* q, int64_t q_sb, int64_t q_sh, int b,
+                                          int kvh, int G, int lane,
+                                          uint32_t (&bq)[D / 16][4]) {
   const int g = lane >> 2, t4 = lane & 3;
-  const int b = blockIdx.z, kvh = blockIdx.y;
-  const int page0 = blockIdx.x * kScorePagesPerCta + warp * 16;
-  griddep_launch_dependents();
-  griddep_wait();
-  if (page0 >= a.P) return;
-
-  // Contraction index k (0..2d) runs over the concatenation [M | m]; thread
-  // (g, t4) owns 16-byte chunks c = t4 + 4 s of it, each giving two k-steps.
-  constexpr int kChunks = D / 16;  // per thread per row
-  // B operand: [q+ | q-] of head g (zero for g >= G).
-  uint32_t bq[kChunks][4];
-  {
-    const bool hv = g < a.G;
-    const uint16_t* qrow = static_cast<const uint16_t*>(a.q) + b * a.q_sb +
-                           static_cast<int64_t>(kvh * a.G + (hv ? g : 0)) * a.q_sh;
+  const bool hv = g < G;
+  const uint16_t* qrow = static_cast<const uint16_t*>(q) + b * q_sb +
+                         static_cast<int64_t>(kvh * G + (hv ? g : 0)) * q_sh;
 #pragma unroll
-    for (int s = 0; s < kChunks; ++s) {
-      const int c = t4 + 4 * s;
-      const bool neg_part = c >= D / 8;
-      const int ch = 8 * (neg_part ? c - D / 8 : c);
-      uint4 w = hv ? *reinterpret_cast<const uint4*>(qrow + ch) : make_uint4(0, 0, 0, 0);
-      bq[s][0] = keep_sign(w.x, neg_part);
-      bq[s][1] = keep_sign(w.y, neg_part);
-      bq[s][2] = keep_sign(w.z, neg_part);
-      bq[s][3] = keep_sign(w.w, neg_part);
-    }
+  for (int s = 0; s < D / 16; ++s) {
+    const int c = t4 + 4 * s;
+    const bool neg_part = c >= D / 8;
+    const int ch = 8 * (neg_part ? c - D / 8 : c);
+    const uint4 w = hv ? *reinterpret_cast<const uint4*>(qrow + ch) : make_uint4(0, 0, 0, 0);
+    bq[s][0] = keep_sign(w.x, neg_part);
+    bq[s][1] = keep_sign(w.y, neg_part);
+    bq[s][2] = keep_sign(w.z, neg_part);
+    bq[s][3] = keep_sign(w.w, neg_part);
   }
-  // A operand: rows g and g + 8 are pages page0 + g and page0 + g + 8.
-  const int64_t mbase = (static_cast<int64_t>(b) * a.Hkv + kvh) * a.P;
-  const uint16_t* mmax = static_cast<const uint16_t*>(a.meta_max);
-  const uint16_t* mmin = static_cast<const uint16_t*>(a.meta_min);
-  uint4 ra[2][kChunks];
+}
+
+// Bound scores of pages page0 .. page0+15 (< P) of one (batch, kv head) for the
+// group's query heads: acc = [page g][head 2t4], [g][2t4+1], [g+8][2t4],
+// [g+8][2t4+1].  mmax / mmin point at the unit's [P, d] metadata.
+template <int D, bool F16>
+__device__ __forceinline__ void score_tile(const uint32_t (&bq)[D / 16][4], const uint16_t* mmax,
+                                           const uint16_t* mmin, int page0, int P, int lane,
+                                           float (&acc)[4]) {
+  const int g = lane >> 2, t4 = lane & 3;
+  // Every load is issued before the first MMA (rows past P read a valid page
+  // and are zeroed afterwards), so a lane has 2 d / 8 16-byte loads in flight.
+  uint4 ra[2][D / 16];
 #pragma unroll
   for (int hr = 0; hr < 2; ++hr) {
-    const int page = page0 + g + 8 * hr;
-    const bool pv = page < a.P;
+    const int page = min(page0 + g + 8 * hr, P - 1);
 #pragma unroll
-    for (int s = 0; s < kChunks; ++s) {
+    for (int s = 0; s < D / 16; ++s) {
       const int c = t4 + 4 * s;
-      const uint16_t* src = (c < D / 8) ? mmax + (mbase + page) * D + 8 * c
-                                        : mmin + (mbase + page) * D + 8 * (c - D / 8);
-      ra[hr][s] = pv ? __ldg(reinterpret_cast<const uint4*>(src)) : make_uint4(0, 0, 0, 0);
+      const uint16_t* src = (c < D / 8) ? mmax + static_cast<int64_t>(page) * D + 8 * c
+                                        : mmin + static_cast<int64_t>(page) * D + 8 * (c - D / 8);
+      ra[hr][s] = __ldg(reinterpret_cast<const uint4*>(src));
     }
   }
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int s = 0; s < kChunks; ++s) {
+  for (int hr = 0; hr < 2; ++hr) {
+    if (page0 + g + 8 * hr >= P) {
+#pragma unroll
+      for (int s = 0; s < D / 16; ++s) ra[hr][s] = make_uint4(0, 0, 0, 0);
+    }
+  }
+  acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+#pragma unroll
+  for (int s = 0; s < D / 16; ++s) {
     mma16816<F16>(acc, ra[0][s].x, ra[1][s].x, ra[0][s].y, ra[1][s].y, bq[s][0], bq[s][1]);
     mma16816<F16>(acc, ra[0][s].z, ra[1][s].z, ra[0][s].w, ra[1][s].w, bq[s][2], bq[s][3]);
-  }
-  // acc: [page g][head 2t4], [g][2t4+1], [g+8][2t4], [g+8][2t4+1]
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int head = 2 * t4 + (e & 1);
-    const int page = page0 + g + 8 * (e >> 1);
-    if (head < a.G && page < a.P)
-      a.scores[(static_cast<int64_t>(b) * a.Hq + kvh * a.G + head) * a.P + page] = acc[e];
   }
 }
 
@@ -112,79 +128,36 @@ __device__ __forceinline__ uint32_t score_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-constexpr int kTopkThreads = 256;
-constexpr size_t kTopkSmemKeyBytes = 160 * 1024;  // rows of up to 40960 pages
-constexpr int kTopkMaxWordsSmem = 2048;           // bitmap words built in shared memory
-
-// Block-wide exclusive prefix sum of v.
-__device__ __forceinline__ long long block_excl_sum(long long v, long long* warp_tot) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  long long incl = v;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const long long t = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += t;
-  }
-  if (lane == 31) warp_tot[warp] = incl;
-  __syncthreads();
-  long long before = 0;
-#pragma unroll
-  for (int w = 0; w < kTopkThreads / 32; ++w) before += (w < warp) ? warp_tot[w] : 0;
-  return before + incl - v;
-}
-
-// Keys of one row: staged in shared memory once when they fit, else re-read
-// (order-preserving transform applied on the fly) from global memory.
-template <bool SMEM>
-struct RowKeys {
-  const float* r;
-  const uint32_t* s;
-  __device__ __forceinline__ uint32_t operator()(int j) const {
-    if constexpr (SMEM) return s[j];
-    return score_key(__ldcg(r + j));
-  }
+struct SelScratch {
+  uint32_t hist[256];
+  long long warp_tot[kSelWarps];
+  uint32_t digit, above;
 };
 
-// One CTA per (b, h) row.  Radix select on 8-bit digits, most significant
-// first: each pass histograms the digit of the keys that still match the
-// prefix (one shared atomic per distinct digit per warp), and warp 0 finds the
-// digit that holds the K-th largest key.  Then every thread takes a contiguous
-// range of pages: keys above the threshold are in, keys equal to it are in for
-// the first `need` of them in page order; one block scan gives every thread
-// its output position, so pages come out ascending.
-template <bool SMEM>
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
-  extern __shared__ uint32_t s_keys[];
-  __shared__ uint32_t hist[256];
-  __shared__ long long warp_tot[kTopkThreads / 32];
-  __shared__ uint32_t s_digit, s_above;
-  __shared__ uint32_t s_bits[kTopkMaxWordsSmem];
-  const int row = blockIdx.x;
+// Radix selection (block of kSelThreads) of the kk largest of P keys.  On
+// return: keys with (key & mask) > prefix are selected, and of the keys with
+// (key & mask) == prefix the first `need` in index order.
+template <typename KeyFn>
+__device__ void block_radix_select(const KeyFn& key, int P, int kk, SelScratch& sc,
+                                   uint32_t& prefix, uint32_t& mask, int& need) {
   const int tid = threadIdx.x, lane = tid & 31;
-  griddep_launch_dependents();
-  griddep_wait();  // the scores come from the previous kernel
-  const float* r = a.scores + static_cast<int64_t>(row) * a.P;
-  if constexpr (SMEM) {
-#pragma unroll 8
-    for (int j = tid; j < a.P; j += kTopkThreads) s_keys[j] = score_key(__ldcg(r + j));
-  }
-  const RowKeys<SMEM> key{r, s_keys};
-  const int P_round = (a.P + kTopkThreads - 1) / kTopkThreads * kTopkThreads;
-
-  uint32_t prefix = 0, mask = 0;
-  int need = a.kk;  // still to choose among keys matching `prefix` under `mask`
+  const int P_round = (P + kSelThreads - 1) / kSelThreads * kSelThreads;
+  prefix = 0;
+  mask = 0;
+  need = kk;
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
-    hist[tid] = 0;
+    sc.hist[tid] = 0;
     __syncthreads();
-    for (int j = tid; j < P_round; j += kTopkThreads) {
-      const uint32_t k = (j < a.P) ? key(j) : 0u;
-      const bool in = (j < a.P) && (k & mask) == prefix;
+    for (int j = tid; j < P_round; j += kSelThreads) {
+      const uint32_t k = (j < P) ? key(j) : 0u;
+      const bool in = (j < P) && (k & mask) == prefix;
       const uint32_t digit = (k >> shift) & 0xffu;
       const uint32_t act = __ballot_sync(0xffffffffu, in);
-      if (in) {
+      if (in) {  // one shared atomic per distinct digit per warp
         const uint32_t peers = __match_any_sync(act, digit);
-        if (lane == __ffs(peers) - 1) atomicAdd(&hist[digit], static_cast<uint32_t>(__popc(peers)));
+        if (lane == __ffs(peers) - 1)
+          atomicAdd(&sc.hist[digit], static_cast<uint32_t>(__popc(peers)));
       }
     }
     __syncthreads();
@@ -193,7 +166,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
       uint32_t c[8], sum = 0;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        c[u] = hist[255 - 8 * tid - u];
+        c[u] = sc.hist[255 - 8 * tid - u];
         sum += c[u];
       }
       uint32_t incl = sum;
@@ -206,64 +179,294 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         if (above < static_cast<uint32_t>(need) && above + c[u] >= static_cast<uint32_t>(need)) {
-          s_digit = 255 - 8 * tid - u;
-          s_above = above;
+          sc.digit = 255 - 8 * tid - u;
+          sc.above = above;
         }
         above += c[u];
       }
     }
     __syncthreads();
-    const uint32_t digit = s_digit;
-    need -= static_cast<int>(s_above);
+    const uint32_t digit = sc.digit;
+    need -= static_cast<int>(sc.above);
     prefix |= digit << shift;
     mask |= 0xffu << shift;
-    const bool all_taken = hist[digit] == static_cast<uint32_t>(need);
+    const bool all_taken = sc.hist[digit] == static_cast<uint32_t>(need);
     __syncthreads();
     if (all_taken) break;
   }
+}
 
-  // Contiguous page range of this thread; counts of keys above / equal.
-  const int per = (a.P + kTopkThreads - 1) / kTopkThreads;
-  const int j0 = min(a.P, tid * per), j1 = min(a.P, j0 + per);
+// Writes the selection in ascending page order to sel_row[0 .. kk) and its
+// bitmap word by word (word_out(w, bits)).  Warp w walks a contiguous range of
+// pages 32 at a time; one block scan of the per-warp counts places it.
+template <typename KeyFn, typename WordOut>
+__device__ void block_emit(const KeyFn& key, int P, uint32_t prefix, uint32_t mask, int need,
+                           int32_t* sel_row, const WordOut& word_out, SelScratch& sc) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int span = (P + 32 * kSelWarps - 1) / (32 * kSelWarps) * 32;
+  const int j0 = warp * span, j1 = min(P, j0 + span);
   int gt = 0, eq = 0;
-  for (int j = j0; j < j1; ++j) {
-    const uint32_t k = key(j) & mask;
-    gt += k > prefix;
-    eq += k == prefix;
+  for (int base = j0; base < j1; base += 32) {
+    const int j = base + lane;
+    const uint32_t k = (j < j1) ? (key(j) & mask) : 0u;
+    gt += __popc(__ballot_sync(0xffffffffu, j < j1 && k > prefix));
+    eq += __popc(__ballot_sync(0xffffffffu, j < j1 && k == prefix));
   }
-  const bool bits_in_smem = a.W32 <= kTopkMaxWordsSmem;
-  if (bits_in_smem)
-    for (int w = tid; w < a.W32; w += kTopkThreads) s_bits[w] = 0u;
-  // One scan of (gt << 32 | eq): both sums stay below 2^31.
-  const long long before =
-      block_excl_sum((static_cast<long long>(gt) << 32) | static_cast<long long>(eq), warp_tot);
+  if (lane == 0) sc.warp_tot[warp] = (static_cast<long long>(gt) << 32) | eq;
+  __syncthreads();
+  long long before = 0;
+  for (int w = 0; w < warp; ++w) before += sc.warp_tot[w];
   int gt_before = static_cast<int>(before >> 32);
   int eq_before = static_cast<int>(before & 0xffffffffll);
-  for (int j = j0; j < j1; ++j) {
-    const uint32_t k = key(j) & mask;
-    bool sel = false;
-    if (k > prefix) {
-      sel = true;
-    } else if (k == prefix) {
-      sel = eq_before < need;
-      ++eq_before;
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int base = j0; base < j1; base += 32) {
+    const int j = base + lane;
+    const uint32_t k = (j < j1) ? (key(j) & mask) : 0u;
+    const bool is_gt = j < j1 && k > prefix, is_eq = j < j1 && k == prefix;
+    const uint32_t gtm = __ballot_sync(0xffffffffu, is_gt);
+    const uint32_t eqm = __ballot_sync(0xffffffffu, is_eq);
+    const int eq_rank = eq_before + __popc(eqm & lt);
+    const bool sel = is_gt || (is_eq && eq_rank < need);
+    const uint32_t selm = __ballot_sync(0xffffffffu, sel);
+    if (sel) sel_row[gt_before + __popc(gtm & lt) + min(eq_rank, need)] = j;
+    if (lane == 0) word_out(base >> 5, selm);
+    gt_before += __popc(gtm);
+    eq_before += __popc(eqm);
+  }
+  __syncthreads();  // the scratch may be reused
+}
+
+// The union of G heads' selection bitmaps (word(h, w)), ascending, with a bit
+// per head: out[0 .. count) = (page, mask); *count_out = count.
+template <typename WordFn>
+__device__ void block_union(const WordFn& word, int G, int W32, int2* out, int* count_out,
+                            SelScratch& sc) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int span = (W32 + 32 * kSelWarps - 1) / (32 * kSelWarps) * 32;  // words per warp
+  const int w0 = warp * span, w1 = min(W32, w0 + span);
+  int cnt = 0;
+  for (int wi = w0 + lane; wi < w1; wi += 32) {
+    uint32_t u = 0;
+    for (int h = 0; h < G; ++h) u |= word(h, wi);
+    cnt += __popc(u);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
+  if (lane == 0) sc.warp_tot[warp] = cnt;
+  __syncthreads();
+  int before = 0, total = 0;
+  for (int w = 0; w < kSelWarps; ++w) {
+    before += (w < warp) ? static_cast<int>(sc.warp_tot[w]) : 0;
+    total += static_cast<int>(sc.warp_tot[w]);
+  }
+  for (int base = w0; base < w1; base += 32) {
+    const int wi = base + lane;
+    uint32_t hw[8];
+    uint32_t u = 0;
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+      hw[h] = (h < G && wi < w1) ? word(h, wi) : 0u;
+      u |= hw[h];
     }
-    if (sel) {
-      const int pos = gt_before + min(eq_before - (k == prefix ? 1 : 0), need);
-      a.selected[static_cast<int64_t>(row) * a.kk + pos] = j;
-      if (bits_in_smem) atomicOr(&s_bits[j >> 5], 1u << (j & 31));
-      else atomicOr(&a.bitmaps[static_cast<int64_t>(row) * a.W32 + (j >> 5)], 1u << (j & 31));
-      if (k > prefix) ++gt_before;
+    const int c = __popc(u);
+    int incl = c;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += t;
+    }
+    int pos = before + incl - c;
+    while (u) {
+      const int bit = __ffs(u) - 1;
+      u &= u - 1;
+      uint32_t m = 0;
+#pragma unroll
+      for (int h = 0; h < 8; ++h) m |= ((hw[h] >> bit) & 1u) << h;
+      out[pos++] = make_int2(wi * 32 + bit, static_cast<int>(m));
+    }
+    before += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (threadIdx.x == 0) *count_out = total;
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------- fused
+template <int D, bool F16>
+__global__ void __launch_bounds__(kSelThreads) select_fused_kernel(const SelectArgs a) {
+  extern __shared__ __align__(16) uint8_t dsm[];
+  __shared__ SelScratch sc;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nloc = (a.G + a.cluster - 1) / a.cluster;  // heads this CTA selects for
+  float* scores = reinterpret_cast<float*>(dsm);                      // [G][ppr]
+  uint32_t* hbits = reinterpret_cast<uint32_t*>(scores + a.G * a.ppr);  // [nloc][W32]
+  uint32_t* keys = hbits + nloc * a.W32;                               // [P] if staged
+  griddep_launch_dependents();
+  griddep_wait();
+
+  // 1. bound scores of this CTA's pages [p0, p1)
+  const int p0 = rank * a.ppr, p1 = min(a.P, p0 + a.ppr);
+  {
+    uint32_t bq[D / 16][4];
+    load_q_pm<D>(a.q, a.q_sb, a.q_sh, b, kvh, a.G, lane, bq);
+    const int64_t mbase = (static_cast<int64_t>(b) * a.Hkv + kvh) * a.P * D;
+    const uint16_t* mmax = static_cast<const uint16_t*>(a.meta_max) + mbase;
+    const uint16_t* mmin = static_cast<const uint16_t*>(a.meta_min) + mbase;
+    const int g = lane >> 2, t4 = lane & 3;
+    for (int page0 = p0 + 16 * warp; page0 < p1; page0 += 16 * kSelWarps) {
+      float acc[4];
+      score_tile<D, F16>(bq, mmax, mmin, page0, p1, lane, acc);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int head = 2 * t4 + (e & 1), page = page0 + g + 8 * (e >> 1);
+        if (head < a.G && page < p1) scores[head * a.ppr + (page - p0)] = acc[e];
+      }
     }
   }
-  if (bits_in_smem) {
-    __syncthreads();
-    for (int w = tid; w < a.W32; w += kTopkThreads)
-      a.bitmaps[static_cast<int64_t>(row) * a.W32 + w] = s_bits[w];
+  cluster.sync();
+
+  // 2. top-K of query heads rank, rank + C, ... over all P pages of the unit
+  for (int h = rank, slot = 0; h < a.G; h += a.cluster, ++slot) {
+    auto peer_key = [&](int j) {
+      const int r = j / a.ppr;
+      const float* src = cluster.map_shared_rank(scores + h * a.ppr + (j - r * a.ppr), r);
+      return score_key(*src);
+    };
+    auto staged_key = [&](int j) { return keys[j]; };
+    int32_t* sel_row = a.selected + (static_cast<int64_t>(b) * a.Hq + kvh * a.G + h) * a.kk;
+    uint32_t* bits = hbits + slot * a.W32;
+    auto word_out = [&](int w, uint32_t v) { bits[w] = v; };
+    uint32_t prefix, mask;
+    int need;
+    if (a.stage_keys) {
+      for (int j = threadIdx.x; j < a.P; j += kSelThreads) keys[j] = peer_key(j);
+      __syncthreads();
+      block_radix_select(staged_key, a.P, a.kk, sc, prefix, mask, need);
+      block_emit(staged_key, a.P, prefix, mask, need, sel_row, word_out, sc);
+    } else {
+      block_radix_select(peer_key, a.P, a.kk, sc, prefix, mask, need);
+      block_emit(peer_key, a.P, prefix, mask, need, sel_row, word_out, sc);
+    }
+  }
+  cluster.sync();
+
+  // 3. the group's union, ascending, by CTA 0
+  if (rank == 0) {
+    auto word = [&](int h, int w) {
+      const uint32_t* src =
+          cluster.map_shared_rank(hbits + (h / a.cluster) * a.W32 + w, h % a.cluster);
+      return *src;
+    };
+    const int64_t unit = static_cast<int64_t>(b) * a.Hkv + kvh;
+    block_union(word, a.G, a.W32, a.union_list + unit * a.union_stride, a.union_count + unit, sc);
+  }
+  cluster.sync();  // peers keep their shared memory until CTA 0 has read it
+}
+
+// ---------------------------------------------------------------- fallback
+template <int D, bool F16>
+__global__ void __launch_bounds__(kScoreWarps * 32) score_kernel(const ScoreArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int b = blockIdx.z, kvh = blockIdx.y;
+  const int page0 = blockIdx.x * kScorePagesPerCta + warp * 16;
+  griddep_launch_dependents();
+  griddep_wait();
+  if (page0 >= a.P) return;
+  uint32_t bq[D / 16][4];
+  load_q_pm<D>(a.q, a.q_sb, a.q_sh, b, kvh, a.G, lane, bq);
+  const int64_t mbase = (static_cast<int64_t>(b) * a.Hkv + kvh) * a.P * D;
+  float acc[4];
+  score_tile<D, F16>(bq, static_cast<const uint16_t*>(a.meta_max) + mbase,
+                     static_cast<const uint16_t*>(a.meta_min) + mbase, page0, a.P, lane, acc);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int head = 2 * t4 + (e & 1);
+    const int page = page0 + g + 8 * (e >> 1);
+    if (head < a.G && page < a.P)
+      a.scores[(static_cast<int64_t>(b) * a.Hq + kvh * a.G + head) * a.P + page] = acc[e];
   }
 }
 
+template <bool SMEM>
+__global__ void __launch_bounds__(kSelThreads) topk_kernel(const TopkArgs a) {
+  extern __shared__ uint32_t s_keys[];
+  __shared__ SelScratch sc;
+  const int row = blockIdx.x;
+  griddep_launch_dependents();
+  griddep_wait();  // the scores come from the previous kernel
+  const float* r = a.scores + static_cast<int64_t>(row) * a.P;
+  if constexpr (SMEM) {
+    for (int j = threadIdx.x; j < a.P; j += kSelThreads) s_keys[j] = score_key(__ldcg(r + j));
+    __syncthreads();
+  }
+  auto key = [&](int j) {
+    if constexpr (SMEM) return s_keys[j];
+    return score_key(__ldcg(r + j));
+  };
+  uint32_t* bits = a.bitmaps + static_cast<int64_t>(row) * a.W32;
+  auto word_out = [&](int w, uint32_t v) { bits[w] = v; };
+  uint32_t prefix, mask;
+  int need;
+  block_radix_select(key, a.P, a.kk, sc, prefix, mask, need);
+  block_emit(key, a.P, prefix, mask, need, a.selected + static_cast<int64_t>(row) * a.kk,
+             word_out, sc);
+}
+
+__global__ void __launch_bounds__(kSelThreads) union_kernel(const UnionArgs a) {
+  __shared__ SelScratch sc;
+  griddep_launch_dependents();
+  griddep_wait();  // the bitmaps come from the previous kernel
+  const int unit = blockIdx.x;
+  const int b = unit / a.Hkv, kvh = unit % a.Hkv;
+  const uint32_t* bm = a.bitmaps + (static_cast<int64_t>(b) * a.Hq + kvh * a.G) * a.W32;
+  auto word = [&](int h, int w) { return __ldcg(bm + static_cast<int64_t>(h) * a.W32 + w); };
+  block_union(word, a.G, a.W32, a.union_list + static_cast<int64_t>(unit) * a.union_stride,
+              a.union_count + unit, sc);
+}
+
+template <int D, bool F16>
+cudaError_t launch_fused_t(const SelectArgs& a, size_t smem, cudaStream_t s) {
+  auto kern = select_fused_kernel<D, F16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.cluster, a.Hkv, a.B);
+  cfg.blockDim = dim3(kSelThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = a.cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
 }  // namespace
+
+size_t select_fused_smem(const SelectArgs& a) {
+  const int nloc = (a.G + a.cluster - 1) / a.cluster;
+  size_t bytes = sizeof(float) * static_cast<size_t>(a.G) * a.ppr +
+                 sizeof(uint32_t) * static_cast<size_t>(nloc) * a.W32;
+  if (a.stage_keys) bytes += sizeof(uint32_t) * static_cast<size_t>(a.P);
+  return bytes <= kFusedSmemBytes ? bytes : 0;
+}
+
+cudaError_t launch_select_fused(int d, bool f16, const SelectArgs& a, cudaStream_t s) {
+  const size_t smem = select_fused_smem(a);
+  if (smem == 0) return cudaErrorInvalidValue;
+  if (d == 128)
+    return f16 ? launch_fused_t<128, true>(a, smem, s) : launch_fused_t<128, false>(a, smem, s);
+  return f16 ? launch_fused_t<64, true>(a, smem, s) : launch_fused_t<64, false>(a, smem, s);
+}
 
 cudaError_t launch_score(int d, bool f16, const ScoreArgs& a, cudaStream_t s) {
   dim3 grid(static_cast<unsigned>(ceil_div(a.P, kScorePagesPerCta)), a.Hkv, a.B);
@@ -283,15 +486,13 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kTopkSmemKeyBytes));
     if (e != cudaSuccess) return e;
-    return launch_pdl(topk_kernel<true>, dim3(a.rows), dim3(kTopkThreads), key_bytes, s, a);
+    return launch_pdl(topk_kernel<true>, dim3(a.rows), dim3(kSelThreads), key_bytes, s, a);
   }
-  // Large rows set their bitmap bits straight in global memory: clear it first.
-  if (a.W32 > kTopkMaxWordsSmem) {
-    cudaError_t e = cudaMemsetAsync(a.bitmaps, 0,
-                                    sizeof(uint32_t) * static_cast<size_t>(a.rows) * a.W32, s);
-    if (e != cudaSuccess) return e;
-  }
-  return launch_pdl(topk_kernel<false>, dim3(a.rows), dim3(kTopkThreads), 0, s, a);
+  return launch_pdl(topk_kernel<false>, dim3(a.rows), dim3(kSelThreads), 0, s, a);
+}
+
+cudaError_t launch_union(const UnionArgs& a, int units, cudaStream_t s) {
+  return launch_pdl(union_kernel, dim3(units), dim3(kSelThreads), 0, s, a);
 }
 
 }  // namespace dkv
