@@ -346,32 +346,8 @@ dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_
   int2* ulist = reinterpret_cast<int2*>(ws + L.union_list);
   int* ucount = reinterpret_cast<int*>(ws + L.union_count);
 
-  // Bound scores, per-head top-K and the group's page union: one cluster per
-  // (batch, kv head) when its scores fit in shared memory.
-  dkv::SelectArgs fa{};
-  fa.q = q;
-  fa.q_sb = p->q_stride_b;
-  fa.q_sh = p->q_stride_h;
-  fa.meta_min = meta_min;
-  fa.meta_max = meta_max;
-  fa.B = p->batch;
-  fa.Hq = p->num_q_heads;
-  fa.Hkv = p->num_kv_heads;
-  fa.G = G;
-  fa.P = P;
-  fa.kk = L.kk;
-  fa.W32 = L.W32;
-  fa.cluster = static_cast<int>(std::min<int64_t>(8, std::max<int64_t>(1, ceil_div(P, 256))));
-  fa.ppr = static_cast<int>(ceil_div(ceil_div(P, fa.cluster), 16) * 16);
-  fa.stage_keys = P <= 16384;
-  fa.selected = sel;
-  fa.union_list = ulist;
-  fa.union_count = ucount;
-  fa.union_stride = L.union_stride;
-  if (dkv::select_fused_smem(fa) > 0) {
-    if ((st = cuda_status(dkv::launch_select_fused(p->head_dim, f16, fa, s))) != DKV_OK)
-      return st;
-  } else {
+  // Bound scores, per-head top-K and the group's page union.
+  {
     dkv::ScoreArgs sa{};
     sa.q = q;
     sa.q_sb = p->q_stride_b;

@@ -95,23 +95,6 @@ struct TopkArgs {
   int W32;
 };
 
-// Fused selection: bound scores, per-head top-K and the group's page union
-// for one (batch, kv head) per thread-block cluster.
-struct SelectArgs {
-  const void* q;
-  int64_t q_sb, q_sh;
-  const void* meta_min;
-  const void* meta_max;
-  int B, Hq, Hkv, G, P, kk, W32;
-  int cluster;                 // CTAs per (batch, kv head)
-  int ppr;                     // pages scored per CTA (multiple of 16)
-  bool stage_keys;             // top-K keys fit in the CTA's shared memory
-  int32_t* selected;           // [B, Hq, kk]
-  int2* union_list;            // [B * Hkv, union_stride]
-  int* union_count;            // [B * Hkv]
-  int union_stride;
-};
-
 struct UnionArgs {
   const uint32_t* bitmaps;     // [B, Hq, W32]
   int Hq, Hkv, G, P, W32;
@@ -156,9 +139,7 @@ cudaError_t launch_merge(int d, const MergeArgs& m, int rows, cudaStream_t s);
 cudaError_t launch_score(int d, bool f16, const ScoreArgs& a, cudaStream_t s);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
 cudaError_t launch_union(const UnionArgs& a, int units, cudaStream_t s);
-// Shared memory the fused selection needs per CTA (0 if it does not fit).
-size_t select_fused_smem(const SelectArgs& a);
-cudaError_t launch_select_fused(int d, bool f16, const SelectArgs& a, cudaStream_t s);
+
 cudaError_t launch_meta(bool q4, bool f16, const MetaArgs& a, cudaStream_t s);
 cudaError_t launch_quant4(int64_t rows, int d, const void* x, void* codes, void* gmin,
                           void* gmax, cudaStream_t s);

@@ -22,31 +22,23 @@
 // bit per head that chose it -- the list the sparse attention gathers (each
 // page once for the whole group).
 //
-// select_fused_kernel does all three for one (batch, kv head) per thread-block
-// cluster: every CTA scores a range of pages into its shared memory; after a
-// cluster barrier CTA r selects for query heads r, r + C, ... reading the
-// peers' scores over distributed shared memory and keeps each head's
-// selection bitmap; after another barrier CTA 0 ORs the bitmaps into the union
-// list.  When a row's scores do not fit in shared memory, score_kernel,
-// topk_kernel and union_kernel do the same through global memory.
+// Three kernels, chained with programmatic dependent launch: score_kernel
+// (scores to global memory), topk_kernel (one CTA per (b, h): selection and
+// its bitmap) and union_kernel (one CTA per (batch, kv head)).
 
-#include <cooperative_groups.h>
 #include <math.h>
 
 #include "dkv_device.cuh"
 #include "dkv_kernels.h"
-
-namespace cg = cooperative_groups;
 
 namespace dkv {
 namespace {
 
 constexpr int kScoreWarps = 4;
 constexpr int kScorePagesPerCta = 16 * kScoreWarps;
-constexpr int kSelThreads = 256;  // top-K, union and fused selection CTAs
+constexpr int kSelThreads = 256;  // top-K and union CTAs
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr size_t kTopkSmemKeyBytes = 160 * 1024;  // stage rows of up to 40960 pages
-constexpr size_t kFusedSmemBytes = 200 * 1024;
 
 // Split 8 packed 16-bit q values (one 16-byte chunk) into q+ or q-.
 __device__ __forceinline__ uint32_t keep_sign(uint32_t w, bool negative_part) {
@@ -290,82 +282,7 @@ __device__ void block_union(const WordFn& word, int G, int W32, int2* out, int* 
   __syncthreads();
 }
 
-// ---------------------------------------------------------------- fused
-template <int D, bool F16>
-__global__ void __launch_bounds__(kSelThreads) select_fused_kernel(const SelectArgs a) {
-  extern __shared__ __align__(16) uint8_t dsm[];
-  __shared__ SelScratch sc;
-  cg::cluster_group cluster = cg::this_cluster();
-  const int rank = static_cast<int>(cluster.block_rank());
-  const int kvh = blockIdx.y, b = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nloc = (a.G + a.cluster - 1) / a.cluster;  // heads this CTA selects for
-  float* scores = reinterpret_cast<float*>(dsm);                      // [G][ppr]
-  uint32_t* hbits = reinterpret_cast<uint32_t*>(scores + a.G * a.ppr);  // [nloc][W32]
-  uint32_t* keys = hbits + nloc * a.W32;                               // [P] if staged
-  griddep_launch_dependents();
-  griddep_wait();
-
-  // 1. bound scores of this CTA's pages [p0, p1)
-  const int p0 = rank * a.ppr, p1 = min(a.P, p0 + a.ppr);
-  {
-    uint32_t bq[D / 16][4];
-    load_q_pm<D>(a.q, a.q_sb, a.q_sh, b, kvh, a.G, lane, bq);
-    const int64_t mbase = (static_cast<int64_t>(b) * a.Hkv + kvh) * a.P * D;
-    const uint16_t* mmax = static_cast<const uint16_t*>(a.meta_max) + mbase;
-    const uint16_t* mmin = static_cast<const uint16_t*>(a.meta_min) + mbase;
-    const int g = lane >> 2, t4 = lane & 3;
-    for (int page0 = p0 + 16 * warp; page0 < p1; page0 += 16 * kSelWarps) {
-      float acc[4];
-      score_tile<D, F16>(bq, mmax, mmin, page0, p1, lane, acc);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int head = 2 * t4 + (e & 1), page = page0 + g + 8 * (e >> 1);
-        if (head < a.G && page < p1) scores[head * a.ppr + (page - p0)] = acc[e];
-      }
-    }
-  }
-  cluster.sync();
-
-  // 2. top-K of query heads rank, rank + C, ... over all P pages of the unit
-  for (int h = rank, slot = 0; h < a.G; h += a.cluster, ++slot) {
-    auto peer_key = [&](int j) {
-      const int r = j / a.ppr;
-      const float* src = cluster.map_shared_rank(scores + h * a.ppr + (j - r * a.ppr), r);
-      return score_key(*src);
-    };
-    auto staged_key = [&](int j) { return keys[j]; };
-    int32_t* sel_row = a.selected + (static_cast<int64_t>(b) * a.Hq + kvh * a.G + h) * a.kk;
-    uint32_t* bits = hbits + slot * a.W32;
-    auto word_out = [&](int w, uint32_t v) { bits[w] = v; };
-    uint32_t prefix, mask;
-    int need;
-    if (a.stage_keys) {
-      for (int j = threadIdx.x; j < a.P; j += kSelThreads) keys[j] = peer_key(j);
-      __syncthreads();
-      block_radix_select(staged_key, a.P, a.kk, sc, prefix, mask, need);
-      block_emit(staged_key, a.P, prefix, mask, need, sel_row, word_out, sc);
-    } else {
-      block_radix_select(peer_key, a.P, a.kk, sc, prefix, mask, need);
-      block_emit(peer_key, a.P, prefix, mask, need, sel_row, word_out, sc);
-    }
-  }
-  cluster.sync();
-
-  // 3. the group's union, ascending, by CTA 0
-  if (rank == 0) {
-    auto word = [&](int h, int w) {
-      const uint32_t* src =
-          cluster.map_shared_rank(hbits + (h / a.cluster) * a.W32 + w, h % a.cluster);
-      return *src;
-    };
-    const int64_t unit = static_cast<int64_t>(b) * a.Hkv + kvh;
-    block_union(word, a.G, a.W32, a.union_list + unit * a.union_stride, a.union_count + unit, sc);
-  }
-  cluster.sync();  // peers keep their shared memory until CTA 0 has read it
-}
-
-// ---------------------------------------------------------------- fallback
+// ---------------------------------------------------------------- kernels
 template <int D, bool F16>
 __global__ void __launch_bounds__(kScoreWarps * 32) score_kernel(const ScoreArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -427,46 +344,7 @@ __global__ void __launch_bounds__(kSelThreads) union_kernel(const UnionArgs a) {
               a.union_count + unit, sc);
 }
 
-template <int D, bool F16>
-cudaError_t launch_fused_t(const SelectArgs& a, size_t smem, cudaStream_t s) {
-  auto kern = select_fused_kernel<D, F16>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.cluster, a.Hkv, a.B);
-  cfg.blockDim = dim3(kSelThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = a.cluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, a);
-}
-
 }  // namespace
-
-size_t select_fused_smem(const SelectArgs& a) {
-  const int nloc = (a.G + a.cluster - 1) / a.cluster;
-  size_t bytes = sizeof(float) * static_cast<size_t>(a.G) * a.ppr +
-                 sizeof(uint32_t) * static_cast<size_t>(nloc) * a.W32;
-  if (a.stage_keys) bytes += sizeof(uint32_t) * static_cast<size_t>(a.P);
-  return bytes <= kFusedSmemBytes ? bytes : 0;
-}
-
-cudaError_t launch_select_fused(int d, bool f16, const SelectArgs& a, cudaStream_t s) {
-  const size_t smem = select_fused_smem(a);
-  if (smem == 0) return cudaErrorInvalidValue;
-  if (d == 128)
-    return f16 ? launch_fused_t<128, true>(a, smem, s) : launch_fused_t<128, false>(a, smem, s);
-  return f16 ? launch_fused_t<64, true>(a, smem, s) : launch_fused_t<64, false>(a, smem, s);
-}
 
 cudaError_t launch_score(int d, bool f16, const ScoreArgs& a, cudaStream_t s) {
   dim3 grid(static_cast<unsigned>(ceil_div(a.P, kScorePagesPerCta)), a.Hkv, a.B);
