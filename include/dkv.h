@@ -159,6 +159,26 @@ dkv_status dkv_kv_quant4(int64_t rows, int32_t d, const void* x, void* codes, vo
 dkv_status dkv_kv_dequant4(int64_t rows, int32_t d, const void* codes, const void* gmin,
                            const void* gmax, void* x, void* stream);
 
+/* Exact decode attention with no workspace argument and no allocation.  The
+   pages have no counterpart: this serves callers that cannot allocate device
+   memory for the library (a host whose allocator owns the device budget, or a
+   loop that must never call cudaMalloc).  Same arguments, layouts and results
+   as dkv_decode_attn_full, whose kernels it runs; the scratch is a fixed
+   array of DKV_NOALLOC_SCRATCH_BYTES inside the library, held by every GPU that
+   loads it until exit.
+   - Returns DKV_ERR_WORKSPACE when the problem needs more scratch than that
+     (dkv_workspace_bytes(p, 0) > DKV_NOALLOC_SCRATCH_BYTES).
+   - The first call on a device looks up the array's address (with that device
+     current); make that first call before any stream capture.
+   - Every call shares the array: calls that may overlap on the GPU race and
+     must be serialised by the caller.
+   - Device-side errors (an expired bounded wait) are cleared by the next call
+     and cannot be read back. */
+#define DKV_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+dkv_status dkv_decode_attn_full_noalloc(const dkv_params* p, const void* q, const dkv_kv* K,
+                                        const dkv_kv* V, void* out, int32_t out_dtype,
+                                        void* stream);
+
 /* Synchronises `stream`, returns the device status word held at the start of
    `workspace` (DKV_OK, DKV_ERR_DEVICE_TIMEOUT or DKV_ERR_DEVICE_CHECK) and
    resets it to DKV_OK.  Returns DKV_ERR_CUDA if the copy itself fails. */
