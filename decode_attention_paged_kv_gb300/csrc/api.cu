@@ -243,13 +243,37 @@ static dkv_status attn_common(const dkv_params* p, const void* q, const dkv_kv* 
   if (K->format != V->format || K->dtype != V->dtype) return DKV_ERR_DTYPE;
   if (out_dtype != DKV_FP32 && out_dtype != DKV_BF16 && out_dtype != DKV_FP16)
     return DKV_ERR_DTYPE;
-  if (K->format == DKV_KV_Q4G64) return DKV_ERR_UNSUPPORTED;  // dense caches only for now
   if (!L.ok) return DKV_ERR_UNSUPPORTED;
   if (workspace == nullptr) return DKV_ERR_WORKSPACE;
   if (!aligned16(workspace)) return DKV_ERR_ALIGN;
   if (workspace_bytes < L.total) return DKV_ERR_WORKSPACE;
   (void)top_k;
   return DKV_OK;
+}
+
+static dkv::Q4View q4_view(const dkv_kv* kv) {
+  dkv::Q4View v{};
+  v.codes = static_cast<const uint8_t*>(kv->data);
+  v.gmin = static_cast<const __half*>(kv->gmin);
+  v.gmax = static_cast<const __half*>(kv->gmax);
+  v.sb = kv->stride_b;
+  v.sh = kv->stride_h;
+  v.gsb = kv->gstride_b;
+  v.gsh = kv->gstride_h;
+  return v;
+}
+
+// Tensor maps for a dense cache; a 4-bit cache is described by Q4 views instead.
+static bool cache_views(const dkv_params* p, const dkv_kv* K, const dkv_kv* V, CUtensorMap* mk,
+                        CUtensorMap* mv, dkv::AttnArgs* a) {
+  if (K->format == DKV_KV_Q4G64) {
+    memset(mk, 0, sizeof *mk);
+    memset(mv, 0, sizeof *mv);
+    a->k4 = q4_view(K);
+    a->v4 = q4_view(V);
+    return true;
+  }
+  return encode_page_map(mk, p, K) && encode_page_map(mv, p, V);
 }
 
 static dkv::AttnArgs attn_args(const dkv_params* p, const void* q, const WsLayout& L,
@@ -284,8 +308,10 @@ static dkv_status run_attention(const dkv_params* p, const dkv::AttnArgs& a, boo
   // (sparse: a.union_count tells the merge how many chunks of a unit hold pages)
   const int sms = current_sm_count();
   if (sms <= 0) return DKV_ERR_CUDA;
-  dkv_status st =
-      cuda_status(dkv::launch_attn(p->head_dim, f16, sparse, a, mk, mv, sms, s));
+  const bool q4 = a.k4.codes != nullptr;
+  dkv_status st = cuda_status(
+      q4 ? dkv::launch_attn_q4(p->head_dim, sparse, a, sms, s)
+         : dkv::launch_attn(p->head_dim, f16, sparse, a, mk, mv, sms, s));
   if (st != DKV_OK) return st;
   dkv::MergeArgs m{};
   m.part_ml = a.part_ml;
@@ -312,10 +338,10 @@ dkv_status dkv_decode_attn_full(const dkv_params* p, const void* q, const dkv_kv
   if ((st = attn_common(p, q, K, V, out, out_dtype, workspace, workspace_bytes, 0, L)) != DKV_OK)
     return st;
   CUtensorMap mk, mv;
-  if (!encode_page_map(&mk, p, K) || !encode_page_map(&mv, p, V)) return DKV_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const dkv::AttnArgs a = attn_args(p, q, L, ws);
+  dkv::AttnArgs a = attn_args(p, q, L, ws);
+  if (!cache_views(p, K, V, &mk, &mv, &a)) return DKV_ERR_CUDA;
   return run_attention(p, a, false, K->dtype == DKV_FP16, mk, mv, out, out_dtype, s);
 }
 
@@ -335,7 +361,6 @@ dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_
   if (!aligned16(meta_min) || !aligned16(meta_max)) return DKV_ERR_ALIGN;
   if (selected != nullptr && (reinterpret_cast<uintptr_t>(selected) & 3u)) return DKV_ERR_ALIGN;
   CUtensorMap mk, mv;
-  if (!encode_page_map(&mk, p, K) || !encode_page_map(&mv, p, V)) return DKV_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const int P = static_cast<int>(ceil_div(p->seq_len, p->page_size));
@@ -385,6 +410,7 @@ dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_
   }
 
   dkv::AttnArgs a = attn_args(p, q, L, ws);
+  if (!cache_views(p, K, V, &mk, &mv, &a)) return DKV_ERR_CUDA;
   a.union_list = ulist;
   a.union_count = ucount;
   a.union_stride = L.union_stride;

@@ -39,6 +39,7 @@
 // the status word, stops issuing, drains the copies it issued and exits.
 
 #include <math.h>
+#include <string.h>
 
 #include "dkv_device.cuh"
 #include "dkv_kernels.h"
@@ -55,13 +56,24 @@ struct ItemDesc {
   int pad;
 };
 
-template <int D>
+template <int D, bool Q4>
 struct AttnCfg {
-  static constexpr int kPageBytes = kPage * D * 2;  // one tensor's page
-  static constexpr int kStageBytes = 2 * kPageBytes;
+  static constexpr int kPageBytes = kPage * D * 2;          // one 16-bit page tile
+  static constexpr int kCodeBytes = kPage * D / 2;          // 4-bit: one tensor's page of codes
+  static constexpr int kGroupBytes = kPage * (D / 64) * 2;  // 4-bit: one page of gmin (or gmax)
+  // 4-bit stage: K codes | V codes | K min | K max | V min | V max
+  static constexpr int kQ4StageBytes = 2 * kCodeBytes + 4 * kGroupBytes;
+  static constexpr int kStageBytes = Q4 ? (kQ4StageBytes + 127) / 128 * 128 : 2 * kPageBytes;
   static constexpr int kStages = attn_stages(D);
   static constexpr int kSub = kStages / kConsumerWarps;             // stages per consumer warp
-  static constexpr int kBarOffset = kStages * kStageBytes;          // full, empty, dfull, dempty
+  // 4-bit: per consumer warp, the dequantised K and V tiles of its page and
+  // the (min, max, step) of every (tensor, token, group) of that page.
+  static constexpr int kTileOffset = (kStages * kStageBytes + 1023) / 1024 * 1024;
+  static constexpr int kTileBytes = Q4 ? kConsumerWarps * 2 * kPageBytes : 0;
+  static constexpr int kStepsPerWarp = 2 * kPage * (D / 64);
+  static constexpr int kStepOffset = kTileOffset + kTileBytes;
+  static constexpr int kStepBytes = Q4 ? kConsumerWarps * 3 * kStepsPerWarp * 2 : 0;
+  static constexpr int kBarOffset = (kStepOffset + kStepBytes + 15) / 16 * 16;
   static constexpr int kStageMetaOffset = kBarOffset + (2 * kStages + 4) * 8;
   static constexpr int kDescOffset = kStageMetaOffset + kStages * 8;
   static constexpr int kMergeOffset = kDescOffset + 2 * 16;
@@ -70,7 +82,7 @@ struct AttnCfg {
   static constexpr int kListOffset = kMergeOffset + kMergeBytes;
   static constexpr int kMiscOffset = kListOffset + 8 * kMaxSelectList;
   static constexpr int kSmemBytes = 1024 + kMiscOffset + 16;
-  static_assert(kPageBytes % 1024 == 0, "stages must stay 1024-byte aligned");
+  static_assert(Q4 || kPageBytes % 1024 == 0, "TMA stages must stay 1024-byte aligned");
   static_assert(kStages % kConsumerWarps == 0, "one sub-ring per consumer warp");
   static_assert((kSmemBytes + 1024) * kAttnCtasPerSm <= 228 * 1024, "two CTAs per SM");
 };
@@ -104,6 +116,88 @@ __device__ __forceinline__ bool consumers_any(bool flag) {
   return res != 0;
 }
 
+// 4-bit path, producer: move one page of K and V codes and group bounds into
+// a stage.  Whole pages go by five-plus-one 1-D bulk copies; a ragged last page
+// copies only its valid tokens' codes and loads their group bounds with plain
+// loads, so nothing is read past the cache.
+template <typename C>
+__device__ __forceinline__ void issue_q4_page(const AttnArgs& a, int b, int kvh, int page,
+                                              uint32_t dst, uint8_t* dst_ptr, uint32_t bar) {
+  constexpr int D = C::kPageBytes / (kPage * 2);
+  constexpr int ng = D / 64;
+  const int t0 = page * kPage;
+  const int nt = min(kPage, a.N - t0);
+  const uint8_t* kc = a.k4.codes + b * a.k4.sb + kvh * a.k4.sh + static_cast<int64_t>(t0) * (D / 2);
+  const uint8_t* vc = a.v4.codes + b * a.v4.sb + kvh * a.v4.sh + static_cast<int64_t>(t0) * (D / 2);
+  const int64_t kg = b * a.k4.gsb + kvh * a.k4.gsh + static_cast<int64_t>(t0) * ng;
+  const int64_t vg = b * a.v4.gsb + kvh * a.v4.gsh + static_cast<int64_t>(t0) * ng;
+  const __half* src[4] = {a.k4.gmin + kg, a.k4.gmax + kg, a.v4.gmin + vg, a.v4.gmax + vg};
+  if (nt == kPage) {
+    mbar_arrive_expect_tx(bar, C::kQ4StageBytes);
+    bulk_load(dst, kc, C::kCodeBytes, bar);
+    bulk_load(dst + C::kCodeBytes, vc, C::kCodeBytes, bar);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      bulk_load(dst + 2 * C::kCodeBytes + i * C::kGroupBytes, src[i], C::kGroupBytes, bar);
+  } else {
+    __half* gb = reinterpret_cast<__half*>(dst_ptr + 2 * C::kCodeBytes);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      for (int e = 0; e < nt * ng; ++e) gb[i * kPage * ng + e] = src[i][e];
+    const uint32_t cb = static_cast<uint32_t>(nt * (D / 2));
+    mbar_arrive_expect_tx(bar, 2 * cb);  // also releases the plain stores above
+    bulk_load(dst, kc, cb, bar);
+    bulk_load(dst + C::kCodeBytes, vc, cb, bar);
+  }
+}
+
+// 4-bit path, consumer warp: dequantise one stage (nt valid tokens) into the
+// warp's K and V tiles, laid out like the TMA page tiles (tile_addr), so the
+// attention code is shared.  x = fp16(code * step + mn) capped at mx, exactly
+// as dkv_kv_dequant4 computes it; tokens past nt become zeros.
+template <typename C, int D>
+__device__ __forceinline__ void dequant_q4_page(const uint8_t* stage, uint8_t* ktile,
+                                                uint8_t* vtile, __half* steps, int nt, int lane) {
+  constexpr int ng = D / 64;
+  constexpr int kPer = kPage * ng;  // (token, group) pairs per tensor
+  const __half* gb = reinterpret_cast<const __half*>(stage + 2 * C::kCodeBytes);
+  __half* s_mn = steps;
+  __half* s_mx = steps + C::kStepsPerWarp;
+  __half* s_st = steps + 2 * C::kStepsPerWarp;
+  for (int e = lane; e < 2 * kPer; e += 32) {
+    const int tensor = e / kPer, r = e % kPer;
+    __half mn = __ushort_as_half(0), mx = __ushort_as_half(0), st = __ushort_as_half(0);
+    if (r / ng < nt) {
+      mn = gb[(2 * tensor) * kPer + r];
+      mx = gb[(2 * tensor + 1) * kPer + r];
+      st = q4_step(mn, mx);
+    }
+    s_mn[e] = mn;
+    s_mx[e] = mx;
+    s_st[e] = st;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int tensor = 0; tensor < 2; ++tensor) {
+    uint8_t* tile = tensor == 0 ? ktile : vtile;
+    const uint8_t* codes = stage + tensor * C::kCodeBytes;
+#pragma unroll 4
+    for (int i = lane; i < kPage * (D / 8); i += 32) {
+      const int t = i / (D / 8), c8 = i % (D / 8);
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
+      if (t < nt) {
+        const uint32_t c4 = *reinterpret_cast<const uint32_t*>(codes + t * (D / 2) + 4 * c8);
+        const int e = tensor * kPer + t * ng + c8 / 8;
+        q4_dequant8(c4, __half2half2(s_mn[e]), __half2half2(s_st[e]), __half2half2(s_mx[e]), w);
+      }
+      const int row = (c8 >> 3) * 16 + t;
+      const int chunk = (c8 & 7) ^ (row & 7);
+      *reinterpret_cast<uint4*>(tile + row * 128 + chunk * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+  __syncwarp();
+}
+
 __device__ __forceinline__ void store_out(void* out, int out_dtype, int64_t off, float v) {
   if (out_dtype == 2) {
     static_cast<float*>(out)[off] = v;
@@ -114,11 +208,12 @@ __device__ __forceinline__ void store_out(void* out, int out_dtype, int64_t off,
   }
 }
 
-template <int D, bool F16, bool SPARSE>
-__global__ void __launch_bounds__(kAttnThreads)
+template <int D, bool F16, bool SPARSE, bool Q4>
+__global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 1)
     attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mk,
                 const __grid_constant__ CUtensorMap mv) {
-  using C = AttnCfg<D>;
+  using C = AttnCfg<D, Q4>;
+  static_assert(!Q4 || F16, "a 4-bit cache is dequantised to fp16");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -146,7 +241,7 @@ __global__ void __launch_bounds__(kAttnThreads)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == kConsumerWarps && lane == 0) {
+  if (!Q4 && warp == kConsumerWarps && lane == 0) {
     prefetch_tensormap(&mk);
     prefetch_tensormap(&mv);
   }
@@ -219,10 +314,14 @@ __global__ void __launch_bounds__(kAttnThreads)
           const int page = SPARSE ? list[j].x : first + j;
           stage_meta[s] = make_int2(page, SPARSE ? list[j].y : 0xff);
           const uint32_t dst = sbase + s * C::kStageBytes;
-          mbar_arrive_expect_tx(full0 + 8 * s, C::kStageBytes);
-          tma_load_5d_hint(dst, &mk, full0 + 8 * s, 0, page * kPage, 0, kvh, b, pol);
-          tma_load_5d_hint(dst + C::kPageBytes, &mv, full0 + 8 * s, 0, page * kPage, 0, kvh, b,
-                           pol);
+          if constexpr (Q4) {
+            issue_q4_page<C>(a, b, kvh, page, dst, smem + s * C::kStageBytes, full0 + 8 * s);
+          } else {
+            mbar_arrive_expect_tx(full0 + 8 * s, C::kStageBytes);
+            tma_load_5d_hint(dst, &mk, full0 + 8 * s, 0, page * kPage, 0, kvh, b, pol);
+            tma_load_5d_hint(dst + C::kPageBytes, &mv, full0 + 8 * s, 0, page * kPage, 0, kvh,
+                             b, pol);
+          }
           ++issued;
           jd = j + 1;
         }
@@ -320,10 +419,21 @@ __global__ void __launch_bounds__(kAttnThreads)
         aborted = true;
         break;
       }
-      const uint32_t kb = sbase + s * C::kStageBytes, vb = kb + C::kPageBytes;
       const int2 meta = stage_meta[s];
       const int page = meta.x;
       const uint32_t hmask = static_cast<uint32_t>(meta.y);
+      uint32_t kb = sbase + s * C::kStageBytes, vb = kb + C::kPageBytes;
+      if constexpr (Q4) {
+        // Dequantise the page into this warp's tiles, then free the stage.
+        kb = sbase + C::kTileOffset + warp * 2 * C::kPageBytes;
+        vb = kb + C::kPageBytes;
+        dequant_q4_page<C, D>(smem + s * C::kStageBytes, smem + (kb - sbase),
+                              smem + (vb - sbase),
+                              reinterpret_cast<__half*>(smem + C::kStepOffset) +
+                                  warp * 3 * C::kStepsPerWarp,
+                              min(kPage, a.N - page * kPage), lane);
+        if (lane == 0) mbar_arrive(empty0 + 8 * s);
+      }
 
       // S = Q K^T for the page: sc[nt][e] = score of head g, token 8 nt + 2 t4 + e.
       float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -382,7 +492,7 @@ __global__ void __launch_bounds__(kAttnThreads)
         mma16816<F16>(acc[2 * jn + 1], a0, a1, a2, a3, r2, r3);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * s);
+      if (!Q4 && lane == 0) mbar_arrive(empty0 + 8 * s);
     }
 
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
@@ -507,11 +617,11 @@ __global__ void __launch_bounds__(1024) merge_kernel(const MergeArgs m) {
   }
 }
 
-template <int D, bool F16, bool SPARSE>
+template <int D, bool F16, bool SPARSE, bool Q4>
 cudaError_t launch_attn_t(const AttnArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
                           int num_sms, cudaStream_t s) {
-  using C = AttnCfg<D>;
-  auto kern = attn_kernel<D, F16, SPARSE>;
+  using C = AttnCfg<D, Q4>;
+  auto kern = attn_kernel<D, F16, SPARSE, Q4>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -525,15 +635,25 @@ cudaError_t launch_attn_t(const AttnArgs& a, const CUtensorMap& mk, const CUtens
 cudaError_t launch_attn(int d, bool f16, bool sparse, const AttnArgs& a, const CUtensorMap& mk,
                         const CUtensorMap& mv, int num_sms, cudaStream_t s) {
   if (d == 128) {
-    if (f16) return sparse ? launch_attn_t<128, true, true>(a, mk, mv, num_sms, s)
-                           : launch_attn_t<128, true, false>(a, mk, mv, num_sms, s);
-    return sparse ? launch_attn_t<128, false, true>(a, mk, mv, num_sms, s)
-                  : launch_attn_t<128, false, false>(a, mk, mv, num_sms, s);
+    if (f16) return sparse ? launch_attn_t<128, true, true, false>(a, mk, mv, num_sms, s)
+                           : launch_attn_t<128, true, false, false>(a, mk, mv, num_sms, s);
+    return sparse ? launch_attn_t<128, false, true, false>(a, mk, mv, num_sms, s)
+                  : launch_attn_t<128, false, false, false>(a, mk, mv, num_sms, s);
   }
-  if (f16) return sparse ? launch_attn_t<64, true, true>(a, mk, mv, num_sms, s)
-                         : launch_attn_t<64, true, false>(a, mk, mv, num_sms, s);
-  return sparse ? launch_attn_t<64, false, true>(a, mk, mv, num_sms, s)
-                : launch_attn_t<64, false, false>(a, mk, mv, num_sms, s);
+  if (f16) return sparse ? launch_attn_t<64, true, true, false>(a, mk, mv, num_sms, s)
+                         : launch_attn_t<64, true, false, false>(a, mk, mv, num_sms, s);
+  return sparse ? launch_attn_t<64, false, true, false>(a, mk, mv, num_sms, s)
+                : launch_attn_t<64, false, false, false>(a, mk, mv, num_sms, s);
+}
+
+cudaError_t launch_attn_q4(int d, bool sparse, const AttnArgs& a, int num_sms, cudaStream_t s) {
+  CUtensorMap unused;  // the 4-bit path moves pages with 1-D bulk copies
+  memset(&unused, 0, sizeof unused);
+  if (d == 128)
+    return sparse ? launch_attn_t<128, true, true, true>(a, unused, unused, num_sms, s)
+                  : launch_attn_t<128, true, false, true>(a, unused, unused, num_sms, s);
+  return sparse ? launch_attn_t<64, true, true, true>(a, unused, unused, num_sms, s)
+                : launch_attn_t<64, true, false, true>(a, unused, unused, num_sms, s);
 }
 
 cudaError_t launch_merge(int d, const MergeArgs& m, int rows, cudaStream_t s) {

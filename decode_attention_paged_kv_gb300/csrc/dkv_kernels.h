@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -44,6 +45,15 @@ constexpr int attn_stages(int d) { return d == 128 ? 12 : 24; }
 // Resident attention CTAs per SM (the persistent grid is this times the SMs).
 constexpr int kAttnCtasPerSm = 2;
 
+// One K or V cache in the 4-bit group-of-64 format (device pointers).
+struct Q4View {
+  const uint8_t* codes;        // [B, Hkv, N, d/2]
+  const __half* gmin;          // [B, Hkv, N, d/64]
+  const __half* gmax;
+  int64_t sb, sh;              // codes strides, bytes
+  int64_t gsb, gsh;            // gmin / gmax strides, elements
+};
+
 struct AttnArgs {
   const void* q;
   int64_t q_sb, q_sh;          // elements
@@ -61,6 +71,7 @@ struct AttnArgs {
   const int2* union_list;      // [B * Hkv, union_stride]
   const int* union_count;      // [B * Hkv]
   int union_stride;
+  Q4View k4, v4;               // 4-bit caches (the dense path uses the tensor maps)
   uint32_t* status;
   uint64_t wait_limit_ns;
 };
@@ -135,6 +146,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 // Launchers: return the launch's cudaError_t.
 cudaError_t launch_attn(int d, bool f16, bool sparse, const AttnArgs& a, const CUtensorMap& mk,
                         const CUtensorMap& mv, int num_sms, cudaStream_t s);
+cudaError_t launch_attn_q4(int d, bool sparse, const AttnArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_merge(int d, const MergeArgs& m, int rows, cudaStream_t s);
 cudaError_t launch_score(int d, bool f16, const ScoreArgs& a, cudaStream_t s);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);

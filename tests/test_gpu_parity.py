@@ -195,3 +195,35 @@ def test_q4_meta_bit_exact(dev, dkv):
     omn, omx = oracle.meta(kh, w.S, 1)
     assert np.array_equal(bits(mn.cpu()), omn)
     assert np.array_equal(bits(mx.cpu()), omx)
+
+
+Q4_CASES = [
+    Workload("q4-mha", B=3, Hq=8, Hkv=8, d=128, N=2000, top_k=20, dtype="fp16"),
+    Workload("q4-gqa-d64", B=2, Hq=8, Hkv=2, d=64, N=1001, top_k=9, dtype="fp16", kind="offset"),
+    Workload("q4-ragged", B=1, Hq=4, Hkv=1, d=128, N=37, top_k=2, dtype="fp16"),
+    Workload("q4-multi-item", B=16, Hq=16, Hkv=16, d=128, N=2055, top_k=32, dtype="fp16"),
+]
+
+
+@pytest.mark.parametrize("w", Q4_CASES, ids=lambda w: w.name)
+def test_q4_attention_matches_oracle(w, dev, dkv):
+    # Attention over 4-bit caches: the kernels dequantise in registers to the
+    # same fp16 values as kv_dequant4; the oracle attends over its own
+    # dequantised cache.
+    q, K, V = make_inputs(w, seed=201)
+    scale = 1.0 / math.sqrt(w.d)
+    K4, V4 = dkv.kv_quant4(K.to(dev)), dkv.kv_quant4(V.to(dev))
+    kh = oracle.dequant4(*oracle.quant4(bits(K)))
+    vh = oracle.dequant4(*oracle.quant4(bits(V)))
+    qd = q.to(dev)
+    out = dkv.decode_attn_full(qd, K4, V4)
+    ref = oracle.attention(bits(q), kh, vh, w.S, scale, 1)
+    assert max_abs(out, ref) <= ATOL
+    meta = dkv.kv_meta_build(K4)
+    out_s, sel = dkv.decode_attn_select(qd, K4, V4, meta, w.top_k, return_selected=True)
+    sel = sel.cpu().numpy()
+    omn, omx = oracle.meta(kh, w.S, 1)
+    r = oracle.scores(bits(q), omn, omx, 1)
+    check_selection(sel.reshape(-1, sel.shape[-1]), r.reshape(-1, r.shape[-1]), w.top_k)
+    ref_s = oracle.attention(bits(q), kh, vh, w.S, scale, 1, sel=sel)
+    assert max_abs(out_s, ref_s) <= ATOL
