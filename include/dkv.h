@@ -94,8 +94,9 @@ typedef struct dkv_kv {
   const void* gmax;         /* Q4G64 only (else NULL) */
   int64_t stride_b;         /* of data: elements (DENSE) or bytes (Q4G64 codes) */
   int64_t stride_h;         /*   token stride is d (DENSE) or d/2 (codes) */
-  int64_t gstride_b;        /* of gmin / gmax, in fp16 elements; Q4G64 only */
-  int64_t gstride_h;        /*   token stride is d/64 */
+  int64_t gstride_b;        /* of gmin / gmax, in fp16 elements; Q4G64 only, */
+  int64_t gstride_h;        /*   multiples of 8 (16 bytes: contiguous bounds need
+                               N * d / 64 % 8 == 0); token stride is d/64 */
 } dkv_kv;
 
 /* Problem description shared by the attention and metadata calls. */

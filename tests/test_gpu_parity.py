@@ -197,11 +197,13 @@ def test_q4_meta_bit_exact(dev, dkv):
     assert np.array_equal(bits(mx.cpu()), omx)
 
 
+# 4-bit caches: contiguous group bounds need N * d / 64 to be a multiple of 8
+# (16-byte head strides); every case still ends in a ragged page.
 Q4_CASES = [
     Workload("q4-mha", B=3, Hq=8, Hkv=8, d=128, N=2000, top_k=20, dtype="fp16"),
-    Workload("q4-gqa-d64", B=2, Hq=8, Hkv=2, d=64, N=1001, top_k=9, dtype="fp16", kind="offset"),
-    Workload("q4-ragged", B=1, Hq=4, Hkv=1, d=128, N=37, top_k=2, dtype="fp16"),
-    Workload("q4-multi-item", B=16, Hq=16, Hkv=16, d=128, N=2055, top_k=32, dtype="fp16"),
+    Workload("q4-gqa-d64", B=2, Hq=8, Hkv=2, d=64, N=1000, top_k=9, dtype="fp16", kind="offset"),
+    Workload("q4-ragged", B=1, Hq=4, Hkv=1, d=128, N=36, top_k=2, dtype="fp16"),
+    Workload("q4-multi-item", B=16, Hq=16, Hkv=16, d=128, N=2052, top_k=32, dtype="fp16"),
 ]
 
 
