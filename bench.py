@@ -54,7 +54,7 @@ def parse_args():
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (small cases for ncu captures)")
     ap.add_argument("--no-extra", action="store_true",
-                    help="skip the 1M-token head-wise and e2e / CPU-baseline legs")
+                    help="skip the e2e, CPU-baseline, 1M-token head-wise and other-workload legs")
     return ap.parse_args()
 
 
@@ -343,6 +343,80 @@ def headwise_leg(dev, stream):
     return res
 
 
+def workload_leg(name, dev, stream, reps=10):
+    """Per-call device times and GB/s on another workload: the 1.3B-MHA shape
+    (dense bf16) or the OPT-30B shape in the 4-bit format (quantise K and V,
+    then metadata, exact and page-sparse attention over the 4-bit cache)."""
+    import decode_attention_paged_kv_gb300 as dkv
+    from decode_attention_paged_kv_gb300 import accounting as acc
+    from workloads import make_inputs
+
+    w = by_name(name)
+    widx = [x.name for x in WORKLOADS].index(w.name)
+    q, K, V = make_inputs(w, seed=42 + widx, device=dev)
+    kk = min(w.top_k, w.P)
+    ws_full = torch.zeros(dkv.workspace_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, 0), dtype=torch.uint8,
+                          device=dev)
+    ws_sel = torch.zeros(dkv.workspace_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, w.top_k),
+                         dtype=torch.uint8, device=dev)
+    out_full = torch.empty(w.B, w.Hq, w.d, device=dev)
+    out_sel = torch.empty_like(out_full)
+    sel = torch.empty(w.B, w.Hq, kk, dtype=torch.int32, device=dev)
+    state = {}
+    calls = []
+    if w.q4:
+        def quant():
+            state["K"], state["V"] = dkv.kv_quant4(K), dkv.kv_quant4(V)
+        calls.append(("kv_quant4 (K and V)", quant,
+                      2 * acc.quant4_bytes(w.B * w.Hkv * w.N, w.d)))
+    else:
+        state["K"], state["V"] = K, V
+
+    def meta():
+        state["meta"] = dkv.kv_meta_build(state["K"])
+
+    def full():
+        dkv.decode_attn_full(q, state["K"], state["V"], out=out_full, workspace=ws_full)
+
+    def select():
+        dkv.decode_attn_select(q, state["K"], state["V"], state["meta"], w.top_k, out=out_sel,
+                               selected=sel, workspace=ws_sel)
+
+    calls += [("kv_meta_build", meta, acc.meta_bytes(w.B, w.Hkv, w.d, w.N, w.S, q4=w.q4)),
+              ("decode_attn_full", full, acc.full_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, q4=w.q4)),
+              ("decode_attn_select", select, None)]
+    for _ in range(3):
+        for _, fn, _ in calls:
+            fn()
+    torch.cuda.synchronize()
+    gathered = union_tokens(sel, w)
+    times = {c: 0.0 for c, _, _ in calls}
+    for _ in range(reps):
+        for c, fn, _ in calls:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times[c] += e0.elapsed_time(e1) / reps
+    if max(dkv.read_device_status(ws_full), dkv.read_device_status(ws_sel)) != 0:
+        raise SystemExit(f"device status error on {w.name}")
+    peak, _ = peaks()
+    res = {"workload": w.name, "dtype": w.dtype, "kv_format": "q4g64" if w.q4 else "dense",
+           "top_k_pages": w.top_k, "gathered_pages": gathered // w.S}
+    for c, _, nbytes in calls:
+        if nbytes is None:
+            nbytes = acc.select_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, gathered, w.S, q4=w.q4)
+        gbs = nbytes / (times[c] * 1e-3) / 1e9
+        res[c] = {"ms": round(times[c], 5), "alg_bytes": nbytes, "GB/s": round(gbs, 1),
+                  "frac_of_measured_hbm": round(gbs / peak, 4),
+                  "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4)}
+    res["decode_attn_full"]["queries_per_s"] = round(w.B / (times["decode_attn_full"] * 1e-3), 1)
+    del q, K, V, state
+    torch.cuda.empty_cache()
+    return res
+
+
 def e2e_leg(q, K, V, w, dev, stream, steps):
     """The same step through the public API with host inputs: every step copies
     q, K, V from pinned host memory and reads the outputs back."""
@@ -472,6 +546,8 @@ def main():
         del q, K, V
         torch.cuda.empty_cache()
         res["headwise_1m"] = headwise_leg(dev, stream)
+        res["other_workloads"] = [workload_leg(n, dev, stream)
+                                  for n in (WORKLOADS[1].name, WORKLOADS[4].name)]
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

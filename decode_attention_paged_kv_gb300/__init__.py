@@ -103,10 +103,12 @@ def lib() -> ctypes.CDLL:
             L.dkv_kv_quant4.argtypes = [i64, i32, vp, vp, vp, vp, vp]
             L.dkv_kv_dequant4.argtypes = [i64, i32, vp, vp, vp, vp, vp]
             L.dkv_read_device_status.argtypes = [vp, vp]
+            L.dkv_attn_ctas_per_sm.argtypes = [i32, i32, i32, i32, ctypes.POINTER(i32)]
             L.dkv_status_string.argtypes = [i32]
             L.dkv_status_string.restype = ctypes.c_char_p
             for name in ("dkv_kv_meta_build", "dkv_decode_attn_full", "dkv_decode_attn_select",
-                         "dkv_kv_quant4", "dkv_kv_dequant4", "dkv_read_device_status"):
+                         "dkv_kv_quant4", "dkv_kv_dequant4", "dkv_read_device_status",
+                         "dkv_attn_ctas_per_sm"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -289,6 +291,16 @@ def kv_dequant4(q4: Q4Cache) -> torch.Tensor:
     _check(lib().dkv_kv_dequant4(rows, d, codes.data_ptr(), gmin.data_ptr(), gmax.data_ptr(),
                                  x.data_ptr(), _stream(x)), "dkv_kv_dequant4")
     return x
+
+
+def attn_ctas_per_sm(head_dim: int, dtype: torch.dtype = torch.bfloat16, q4: bool = False,
+                     sparse: bool = False) -> int:
+    """Resident CTAs per SM of the persistent attention kernel (a diagnostic)."""
+    n = ctypes.c_int32(0)
+    _check(lib().dkv_attn_ctas_per_sm(int(head_dim), _dtype_code(dtype),
+                                      DKV_KV_Q4G64 if q4 else DKV_KV_DENSE, int(sparse),
+                                      ctypes.byref(n)), "dkv_attn_ctas_per_sm")
+    return int(n.value)
 
 
 def read_device_status(workspace: torch.Tensor) -> int:

@@ -51,6 +51,11 @@ def select_bytes(B, Hq, Hkv, d, N, gathered_tokens, S=16, elt=2, out_elt=4, q4=F
     return q + meta + 2 * gathered_tokens * per_tok + out
 
 
+def quant4_bytes(rows, d) -> int:
+    """fp16 rows read + 4-bit codes and group min / max written."""
+    return rows * d * 2 + rows * (d // 2 + 2 * (d // 64) * 2)
+
+
 def memory_fraction(S: int, K: int, L: int, rho: float = 1.0) -> float:
     """TinyServe's sparse-over-full memory fraction 1/S + rho K S / L."""
     return 1.0 / S + rho * K * S / L

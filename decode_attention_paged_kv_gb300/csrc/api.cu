@@ -455,6 +455,21 @@ dkv_status dkv_read_device_status(void* workspace, void* stream) {
   return static_cast<dkv_status>(v);
 }
 
+dkv_status dkv_attn_ctas_per_sm(int32_t head_dim, int32_t dtype, int32_t format, int32_t sparse,
+                                int32_t* ctas_per_sm) {
+  if (ctas_per_sm == nullptr) return DKV_ERR_NULL;
+  if (head_dim != 64 && head_dim != 128) return DKV_ERR_UNSUPPORTED;
+  if (format == DKV_KV_DENSE ? (dtype != DKV_BF16 && dtype != DKV_FP16)
+                             : (format != DKV_KV_Q4G64 || dtype != DKV_FP16))
+    return DKV_ERR_UNSUPPORTED;
+  int n = 0;
+  const cudaError_t e = dkv::attn_ctas_per_sm(head_dim, dtype == DKV_FP16, sparse != 0,
+                                              format == DKV_KV_Q4G64, &n);
+  if (e != cudaSuccess) return DKV_ERR_CUDA;
+  *ctas_per_sm = n;
+  return DKV_OK;
+}
+
 const char* dkv_status_string(int32_t status) {
   switch (status) {
     case DKV_OK: return "ok";

@@ -209,7 +209,7 @@ __device__ __forceinline__ void store_out(void* out, int out_dtype, int64_t off,
 }
 
 template <int D, bool F16, bool SPARSE, bool Q4>
-__global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 1)
+__global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
     attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mk,
                 const __grid_constant__ CUtensorMap mv) {
   using C = AttnCfg<D, Q4>;
@@ -617,17 +617,40 @@ __global__ void __launch_bounds__(1024) merge_kernel(const MergeArgs m) {
   }
 }
 
+// Resident CTAs per SM of one attention instantiation (its registers and shared
+// memory as compiled), at most kAttnCtasPerSm; computed once.
 template <int D, bool F16, bool SPARSE, bool Q4>
-cudaError_t launch_attn_t(const AttnArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
-                          int num_sms, cudaStream_t s) {
+cudaError_t attn_ctas_per_sm_t(int* out) {
   using C = AttnCfg<D, Q4>;
+  static int cached = 0;  // benign race: every thread computes the same value
+  if (cached > 0) {
+    *out = cached;
+    return cudaSuccess;
+  }
   auto kern = attn_kernel<D, F16, SPARSE, Q4>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int64_t want = static_cast<int64_t>(num_sms) * kAttnCtasPerSm;
+  int n = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kAttnThreads, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  if (n < 1) return cudaErrorInvalidConfiguration;
+  cached = n < kAttnCtasPerSm ? n : kAttnCtasPerSm;
+  *out = cached;
+  return cudaSuccess;
+}
+
+template <int D, bool F16, bool SPARSE, bool Q4>
+cudaError_t launch_attn_t(const AttnArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
+                          int num_sms, cudaStream_t s) {
+  using C = AttnCfg<D, Q4>;
+  int per_sm = 0;
+  cudaError_t e = attn_ctas_per_sm_t<D, F16, SPARSE, Q4>(&per_sm);
+  if (e != cudaSuccess) return e;
+  const int64_t want = static_cast<int64_t>(num_sms) * per_sm;
   const int grid = static_cast<int>(a.n_items < want ? a.n_items : want);
-  return launch_pdl(kern, dim3(grid), dim3(kAttnThreads), C::kSmemBytes, s, a, mk, mv);
+  return launch_pdl(attn_kernel<D, F16, SPARSE, Q4>, dim3(grid), dim3(kAttnThreads),
+                    C::kSmemBytes, s, a, mk, mv);
 }
 
 }  // namespace
@@ -654,6 +677,25 @@ cudaError_t launch_attn_q4(int d, bool sparse, const AttnArgs& a, int num_sms, c
                   : launch_attn_t<128, true, false, true>(a, unused, unused, num_sms, s);
   return sparse ? launch_attn_t<64, true, true, true>(a, unused, unused, num_sms, s)
                 : launch_attn_t<64, true, false, true>(a, unused, unused, num_sms, s);
+}
+
+cudaError_t attn_ctas_per_sm(int d, bool f16, bool sparse, bool q4, int* out) {
+  if (q4) {
+    if (d == 128) return sparse ? attn_ctas_per_sm_t<128, true, true, true>(out)
+                                : attn_ctas_per_sm_t<128, true, false, true>(out);
+    return sparse ? attn_ctas_per_sm_t<64, true, true, true>(out)
+                  : attn_ctas_per_sm_t<64, true, false, true>(out);
+  }
+  if (d == 128) {
+    if (f16) return sparse ? attn_ctas_per_sm_t<128, true, true, false>(out)
+                           : attn_ctas_per_sm_t<128, true, false, false>(out);
+    return sparse ? attn_ctas_per_sm_t<128, false, true, false>(out)
+                  : attn_ctas_per_sm_t<128, false, false, false>(out);
+  }
+  if (f16) return sparse ? attn_ctas_per_sm_t<64, true, true, false>(out)
+                         : attn_ctas_per_sm_t<64, true, false, false>(out);
+  return sparse ? attn_ctas_per_sm_t<64, false, true, false>(out)
+                : attn_ctas_per_sm_t<64, false, false, false>(out);
 }
 
 cudaError_t launch_merge(int d, const MergeArgs& m, int rows, cudaStream_t s) {

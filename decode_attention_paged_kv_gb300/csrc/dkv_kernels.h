@@ -44,6 +44,11 @@ inline int select_pages_per_chunk(int64_t union_max, int d) {
 constexpr int attn_stages(int d) { return d == 128 ? 12 : 24; }
 // Resident attention CTAs per SM (the persistent grid is this times the SMs).
 constexpr int kAttnCtasPerSm = 2;
+// Two resident CTAs need at most 168 registers a thread: an SM's registers are
+// split over its four sub-partitions (16384 each) and warps are placed on them
+// by index, so two CTAs of five warps put three warps on one sub-partition
+// (3 x 32 x 168 <= 16384).  The launch sizes the persistent grid from the
+// occupancy the compiled kernel actually gets.
 
 // One K or V cache in the 4-bit group-of-64 format (device pointers).
 struct Q4View {
@@ -147,6 +152,8 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 cudaError_t launch_attn(int d, bool f16, bool sparse, const AttnArgs& a, const CUtensorMap& mk,
                         const CUtensorMap& mv, int num_sms, cudaStream_t s);
 cudaError_t launch_attn_q4(int d, bool sparse, const AttnArgs& a, int num_sms, cudaStream_t s);
+// Resident attention CTAs per SM for one instantiation (1 .. kAttnCtasPerSm).
+cudaError_t attn_ctas_per_sm(int d, bool f16, bool sparse, bool q4, int* out);
 cudaError_t launch_merge(int d, const MergeArgs& m, int rows, cudaStream_t s);
 cudaError_t launch_score(int d, bool f16, const ScoreArgs& a, cudaStream_t s);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);

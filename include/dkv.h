@@ -185,6 +185,15 @@ dkv_status dkv_decode_attn_full_noalloc(const dkv_params* p, const void* q, cons
    resets it to DKV_OK.  Returns DKV_ERR_CUDA if the copy itself fails. */
 dkv_status dkv_read_device_status(void* workspace, void* stream);
 
+/* Diagnostic with no counterpart in the pages: how many CTAs of the persistent
+   attention kernel for (head_dim, dtype, format, sparse != 0) stay resident on
+   one multiprocessor of the current device (the grid is this times the SM
+   count; the kernels are built for two).  Writes it to *ctas_per_sm.  Returns
+   DKV_ERR_UNSUPPORTED for a head_dim / dtype / format the kernels do not
+   cover, DKV_ERR_CUDA if the query fails. */
+dkv_status dkv_attn_ctas_per_sm(int32_t head_dim, int32_t dtype, int32_t format, int32_t sparse,
+                                int32_t* ctas_per_sm);
+
 /* Static description of a status code. */
 const char* dkv_status_string(int32_t status);
 

@@ -103,3 +103,8 @@ def test_host_validation_before_launch(L):
     assert L.dkv_kv_dequant4(10, 128, ctypes.c_void_p(3), q, q, q, None) == 3
     assert L.dkv_kv_meta_build(ctypes.byref(p), ctypes.byref(kv), None, q, None) == 1
     assert L.dkv_read_device_status(None, None) == 1
+    n = ctypes.c_int32(0)
+    assert L.dkv_attn_ctas_per_sm(128, 0, 0, 0, None) == 1
+    assert L.dkv_attn_ctas_per_sm(96, 0, 0, 0, ctypes.byref(n)) == 5
+    assert L.dkv_attn_ctas_per_sm(128, 2, 0, 0, ctypes.byref(n)) == 5   # fp32 cache
+    assert L.dkv_attn_ctas_per_sm(128, 0, 1, 0, ctypes.byref(n)) == 5   # bf16 4-bit cache

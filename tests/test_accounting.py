@@ -33,3 +33,8 @@ def test_full_bytes_workloads():
     # 4-bit OPT-30B shape: codes + group min/max
     b = acc.full_bytes(64, 56, 56, 128, 2048, q4=True) - 64 * 56 * 128 * 6
     assert b == 2 * 64 * 56 * 2048 * (64 + 8)
+
+
+def test_quant4_bytes():
+    # 2 bytes in per value; 4 bits + 4 bytes of bounds per 64 values out
+    assert acc.quant4_bytes(10, 128) == 10 * 256 + 10 * (64 + 8)

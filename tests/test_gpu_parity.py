@@ -229,3 +229,15 @@ def test_q4_attention_matches_oracle(w, dev, dkv):
     check_selection(sel.reshape(-1, sel.shape[-1]), r.reshape(-1, r.shape[-1]), w.top_k)
     ref_s = oracle.attention(bits(q), kh, vh, w.S, scale, 1, sel=sel)
     assert max_abs(out_s, ref_s) <= ATOL
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("kind", ["bf16", "fp16", "q4"])
+@pytest.mark.parametrize("sparse", [False, True])
+def test_attention_kernels_keep_two_ctas_per_sm(d, kind, sparse):
+    """The persistent attention grid is built for two resident CTAs per SM;
+    a register count above 168 silently halves the bytes in flight."""
+    require_cuda()
+    import decode_attention_paged_kv_gb300 as dkv
+    dt = torch.float16 if kind != "bf16" else torch.bfloat16
+    assert dkv.attn_ctas_per_sm(d, dt, q4=kind == "q4", sparse=sparse) == 2
