@@ -251,10 +251,19 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
+    // Lane 0 fetches items and publishes their descriptors; lanes 0-7 issue
+    // the copies, one page each per round.  Page j of an item goes to consumer
+    // warp j % 4, so lane l always feeds warp l % 4 (lanes l and l + 4 fill
+    // consecutive slots of that warp's sub-ring).  One issuing thread would cap
+    // a CTA at a few copies per microsecond, far below HBM bandwidth for pages
+    // of 2-8 KiB; eight lanes issue in parallel.
+    static_assert(kConsumerWarps == 4, "four consumer sub-rings");
+    constexpr int kIssueLanes = 8;
     const uint64_t pol = l2_evict_first_policy();
-    int seq = 0, issued = 0;
-    // Pages issued so far to consumer warps 0-3 (each item starts at warp 0).
-    int wc0 = 0, wc1 = 0, wc2 = 0, wc3 = 0;
+    const int my_w = lane & 3;      // consumer warp this lane feeds
+    int wc = 0;                     // pages issued so far to warp my_w
+    int seq = 0;
+    bool failed = false;            // a lane gave up waiting for a free slot
     for (int k = 0;; ++k) {
       // Next work item with pages (sparse chunks past a unit's union are
       // skipped here and never published).
@@ -299,59 +308,59 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
         desc[slot].n_pages = n;
         desc[slot].seq0 = seq;
         mbar_arrive(dfull0 + 8 * slot);  // release: consumers see the descriptor
-        static_assert(kConsumerWarps == 4, "four consumer sub-rings");
-        int jd = 0;  // pages of this item issued
-        for (int j = 0; j < n && item >= 0; ++j) {
-          const int w = j & 3;
-          const int c = (j >> 2) + (w == 0 ? wc0 : w == 1 ? wc1 : w == 2 ? wc2 : wc3);
-          const int s = w * C::kSub + c % C::kSub;  // warp w's sub-ring, in order
+      }
+      if (item < 0) break;
+      bool lok = true;
+      for (int j0 = 0; j0 < n; j0 += kIssueLanes) {
+        const int j = j0 + lane;
+        if (lane < kIssueLanes && j < n) {
+          const int c = wc + (j >> 2);
+          const int s = my_w * C::kSub + c % C::kSub;  // warp my_w's sub-ring, in order
           if (c >= C::kSub &&
               !mbar_wait_bounded(empty0 + 8 * s, ((c / C::kSub) - 1) & 1, a.wait_limit_ns,
                                  abort_flag)) {
-            ok = 0;
-            break;
-          }
-          const int page = SPARSE ? list[j].x : first + j;
-          stage_meta[s] = make_int2(page, SPARSE ? list[j].y : 0xff);
-          const uint32_t dst = sbase + s * C::kStageBytes;
-          if constexpr (Q4) {
-            issue_q4_page<C>(a, b, kvh, page, dst, smem + s * C::kStageBytes, full0 + 8 * s);
+            lok = false;
           } else {
-            mbar_arrive_expect_tx(full0 + 8 * s, C::kStageBytes);
-            tma_load_5d_hint(dst, &mk, full0 + 8 * s, 0, page * kPage, 0, kvh, b, pol);
-            tma_load_5d_hint(dst + C::kPageBytes, &mv, full0 + 8 * s, 0, page * kPage, 0, kvh,
-                             b, pol);
+            const int page = SPARSE ? list[j].x : first + j;
+            stage_meta[s] = make_int2(page, SPARSE ? list[j].y : 0xff);
+            const uint32_t dst = sbase + s * C::kStageBytes;
+            if constexpr (Q4) {
+              issue_q4_page<C>(a, b, kvh, page, dst, smem + s * C::kStageBytes, full0 + 8 * s);
+            } else {
+              mbar_arrive_expect_tx(full0 + 8 * s, C::kStageBytes);
+              tma_load_5d_hint(dst, &mk, full0 + 8 * s, 0, page * kPage, 0, kvh, b, pol);
+              tma_load_5d_hint(dst + C::kPageBytes, &mv, full0 + 8 * s, 0, page * kPage, 0,
+                               kvh, b, pol);
+            }
           }
-          ++issued;
-          jd = j + 1;
         }
-        wc0 += (jd + 3) >> 2;
-        wc1 += (jd + 2) >> 2;
-        wc2 += (jd + 1) >> 2;
-        wc3 += jd >> 2;
+        if (!__all_sync(0xffffffffu, lok)) break;
       }
+      wc += n > my_w ? (n - my_w + 3) >> 2 : 0;
       seq += n;
-      if (!__shfl_sync(0xffffffffu, ok, 0) || item < 0) break;
+      if (!__all_sync(0xffffffffu, lok)) {
+        failed = true;
+        break;
+      }
     }
-    if (lane == 0 && *abort_flag == 0 && issued < seq) {
+    if (lane == 0 && failed && *abort_flag == 0) {
       set_status(a.status, kStatusTimeout);
       *abort_flag = 1;
     }
-    if (lane == 0 && *abort_flag) {  // let every copy this CTA issued land before it exits
+    __syncwarp();
+    if (lane < kConsumerWarps && *abort_flag) {
+      // Let every copy this CTA issued land before it exits.  A sub-ring holds
+      // at most kSub copies in flight, so lane w waits for the last kSub slots
+      // of warp w's sub-ring (slots never issued just run into the deadline).
       const uint64_t deadline = globaltimer_ns() + kDrainLimitNs;
-      // A sub-ring holds at most kSub copies in flight: waiting for the last
-      // kSub issued to every sub-ring covers all of them.
-      const int wcs[4] = {wc0, wc1, wc2, wc3};
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        for (int c = max(0, wcs[w] - C::kSub); c < wcs[w]; ++c) {
-          const uint64_t now = globaltimer_ns();
-          if (now >= deadline) break;
-          mbar_wait_bounded(full0 + 8 * (w * C::kSub + c % C::kSub), (c / C::kSub) & 1,
-                            deadline - now, nullptr);
-        }
+      for (int c = max(0, wc - C::kSub); c < wc; ++c) {
+        const uint64_t now = globaltimer_ns();
+        if (now >= deadline) break;
+        mbar_wait_bounded(full0 + 8 * (my_w * C::kSub + c % C::kSub), (c / C::kSub) & 1,
+                          deadline - now, nullptr);
       }
     }
+    __syncwarp();
     if (lane == 0) {
       // This CTA fetches no more work.  The last CTA to get here resets the
       // counters for the next call (every earlier fetch is ordered before its
