@@ -19,6 +19,11 @@ using dkv::ceil_div;
 
 constexpr uint64_t kWaitLimitNs = 200000000ull;  // 200 ms per bounded device wait
 constexpr size_t kAlign = 256;
+static_assert(DKV_WORKSPACE_HEADER_BYTES == kAlign, "status word and counters");
+// Shared memory the per-unit selection kernel may take (one CTA per SM), and
+// the shortest context (pages) it is used for.
+constexpr size_t kUnitSelectSmemLimit = 200 * 1024;
+constexpr int kUnitSelectMinP = 1024;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -67,7 +72,7 @@ WsLayout layout_for(const dkv_params& p, int top_k) {
   L.status = 0;
   L.counter = 4;
   L.exit_counter = 8;
-  size_t off = kAlign;
+  size_t off = DKV_WORKSPACE_HEADER_BYTES;
   if (top_k > 0) {
     L.scores = off;
     off = align_up(off + sizeof(float) * rows * P);
@@ -371,7 +376,40 @@ dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_
   int2* ulist = reinterpret_cast<int2*>(ws + L.union_list);
   int* ucount = reinterpret_cast<int*>(ws + L.union_count);
 
-  // Bound scores, per-head top-K and the group's page union.
+  dkv::AttnArgs a = attn_args(p, q, L, ws);
+  if (!cache_views(p, K, V, &mk, &mv, &a)) return DKV_ERR_CUDA;
+  a.union_list = ulist;
+  a.union_count = ucount;
+  a.union_stride = L.union_stride;
+
+  if (P >= kUnitSelectMinP && P <= dkv::kUnitMaxP &&
+      dkv::unit_select_smem(G, P) <= static_cast<size_t>(kUnitSelectSmemLimit)) {
+    // Long contexts: one CTA per (batch, kv head) scores its pages, selects
+    // each head's top-K and builds the union list.  (Shorter ones have too
+    // little metadata per CTA to hide the selection's latency; the three
+    // kernels below spread the same work wider.)
+    dkv::UnitSelectArgs ua{};
+    ua.q = q;
+    ua.q_sb = p->q_stride_b;
+    ua.q_sh = p->q_stride_h;
+    ua.meta_min = meta_min;
+    ua.meta_max = meta_max;
+    ua.B = p->batch;
+    ua.Hq = p->num_q_heads;
+    ua.Hkv = p->num_kv_heads;
+    ua.G = G;
+    ua.P = P;
+    ua.kk = L.kk;
+    ua.selected = sel;
+    ua.union_list = ulist;
+    ua.union_count = ucount;
+    ua.union_stride = L.union_stride;
+    if ((st = cuda_status(dkv::launch_unit_select(p->head_dim, f16, ua, s))) != DKV_OK) return st;
+    return run_attention(p, a, true, f16, mk, mv, out, out_dtype, s);
+  }
+
+  // Otherwise: bound scores, per-head top-K and the group's page union as
+  // three kernels.
   {
     dkv::ScoreArgs sa{};
     sa.q = q;
@@ -409,11 +447,6 @@ dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_
       return st;
   }
 
-  dkv::AttnArgs a = attn_args(p, q, L, ws);
-  if (!cache_views(p, K, V, &mk, &mv, &a)) return DKV_ERR_CUDA;
-  a.union_list = ulist;
-  a.union_count = ucount;
-  a.union_stride = L.union_stride;
   return run_attention(p, a, true, f16, mk, mv, out, out_dtype, s);
 }
 

@@ -579,7 +579,7 @@ __global__ void __launch_bounds__(1024) merge_kernel(const MergeArgs m) {
   if (m.union_count != nullptr) {
     const int b = row / m.Hq, h = row % m.Hq;
     const int count = m.union_count[b * m.Hkv + h / m.G];
-    nc = static_cast<int>(ceil_div(count, m.pages_per_chunk));
+    nc = min(stride, static_cast<int>(ceil_div(count, m.pages_per_chunk)));
   }
   const float* ml = m.part_ml + static_cast<int64_t>(row) * stride * 2;
   for (int k = threadIdx.x; k < nc; k += blockDim.x) {

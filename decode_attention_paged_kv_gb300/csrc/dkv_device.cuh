@@ -249,4 +249,25 @@ __device__ __forceinline__ void q4_dequant8(uint32_t c4, __half2 mn2, __half2 st
   }
 }
 
+// ---------------------------------------------------------------- selection
+// Keep the halves of two packed 16-bit floats that belong to q+ (negative_part
+// false: +0, -0 and positive values) or to q- (negative values); zero the rest.
+__device__ __forceinline__ uint32_t keep_sign(uint32_t w, bool negative_part) {
+  uint32_t out = 0;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t v = (w >> (16 * h)) & 0xffffu;
+    const bool neg = (v & 0x8000u) && (v & 0x7fffu);
+    if (neg == negative_part) out |= v << (16 * h);
+  }
+  return out;
+}
+
+// Order-preserving key of an fp32 score (-0 taken as +0).
+__device__ __forceinline__ uint32_t score_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 }  // namespace dkv

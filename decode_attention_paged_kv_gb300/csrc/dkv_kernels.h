@@ -39,6 +39,10 @@ inline int select_pages_per_chunk(int64_t union_max, int d) {
   const int64_t need = ceil_div(union_max, kMaxChunks);
   return static_cast<int>(need > base ? need : base);
 }
+// The per-(batch, kv head) selection kernel holds a head's P scores in a
+// warp's registers, 64 a lane at most; longer contexts take the separate
+// score / top-K / union kernels.
+constexpr int kUnitMaxP = 64 * 32;  // 2048 pages (32K tokens)
 // Pipeline depth: pages of K+V in flight per CTA (96 KiB of shared memory), as
 // one sub-ring per consumer warp (a multiple of kConsumerWarps).
 constexpr int attn_stages(int d) { return d == 128 ? 12 : 24; }
@@ -119,6 +123,19 @@ struct UnionArgs {
   int union_stride;
 };
 
+// One CTA per (batch, kv head): bound scores, per-head top-K and union.
+struct UnitSelectArgs {
+  const void* q;
+  int64_t q_sb, q_sh;
+  const void* meta_min;        // [B, Hkv, P, d]
+  const void* meta_max;
+  int B, Hq, Hkv, G, P, kk;
+  int32_t* selected;           // [B, Hq, kk]
+  int2* union_list;            // [B * Hkv, union_stride]
+  int* union_count;            // [B * Hkv]
+  int union_stride;
+};
+
 struct MetaArgs {
   const void* data;            // dense K or Q4 codes
   const void* gmin;
@@ -158,6 +175,9 @@ cudaError_t launch_merge(int d, const MergeArgs& m, int rows, cudaStream_t s);
 cudaError_t launch_score(int d, bool f16, const ScoreArgs& a, cudaStream_t s);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
 cudaError_t launch_union(const UnionArgs& a, int units, cudaStream_t s);
+// Shared memory of unit_select_kernel for G heads of P pages (P <= kUnitMaxP).
+size_t unit_select_smem(int G, int P);
+cudaError_t launch_unit_select(int d, bool f16, const UnitSelectArgs& a, cudaStream_t s);
 
 cudaError_t launch_meta(bool q4, bool f16, const MetaArgs& a, cudaStream_t s);
 cudaError_t launch_quant4(int64_t rows, int d, const void* x, void* codes, void* gmin,

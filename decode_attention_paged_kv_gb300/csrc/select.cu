@@ -28,6 +28,7 @@
 
 #include <math.h>
 
+#include "select_warp.cuh"
 #include "dkv_device.cuh"
 #include "dkv_kernels.h"
 
@@ -39,18 +40,6 @@ constexpr int kScorePagesPerCta = 16 * kScoreWarps;
 constexpr int kSelThreads = 256;  // top-K and union CTAs
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr size_t kTopkSmemKeyBytes = 160 * 1024;  // stage rows of up to 40960 pages
-
-// Split 8 packed 16-bit q values (one 16-byte chunk) into q+ or q-.
-__device__ __forceinline__ uint32_t keep_sign(uint32_t w, bool negative_part) {
-  uint32_t out = 0;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const uint32_t v = (w >> (16 * h)) & 0xffffu;
-    const bool neg = (v & 0x8000u) && (v & 0x7fffu);
-    if (neg == negative_part) out |= v << (16 * h);
-  }
-  return out;
-}
 
 // B operand of the score MMA for lane (g, t4): [q+ | q-] of query head g of the
 // group (zero for g >= G).  The contraction index runs over the concatenation
@@ -113,11 +102,41 @@ __device__ __forceinline__ void score_tile(const uint32_t (&bq)[D / 16][4], cons
   }
 }
 
-// Order-preserving key of an fp32 score (-0 taken as +0).
-__device__ __forceinline__ uint32_t score_key(float f) {
-  uint32_t u = __float_as_uint(f);
-  if (u == 0x80000000u) u = 0;
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+// Two tiles (pages page0.. and page1.. , both < P rows clamped) with every
+// load of both issued before the first MMA.
+template <int D, bool F16>
+__device__ __forceinline__ void score_tile2(const uint32_t (&bq)[D / 16][4], const uint16_t* mmax,
+                                            const uint16_t* mmin, int page0, int page1, int P,
+                                            int lane, float (&acc0)[4], float (&acc1)[4]) {
+  const int g = lane >> 2, t4 = lane & 3;
+  uint4 ra[2][2][D / 16];
+#pragma unroll
+  for (int tt = 0; tt < 2; ++tt) {
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int page = min((tt ? page1 : page0) + g + 8 * hr, P - 1);
+#pragma unroll
+      for (int s = 0; s < D / 16; ++s) {
+        const int c = t4 + 4 * s;
+        const uint16_t* src = (c < D / 8) ? mmax + static_cast<int64_t>(page) * D + 8 * c
+                                          : mmin + static_cast<int64_t>(page) * D + 8 * (c - D / 8);
+        ra[tt][hr][s] = __ldg(reinterpret_cast<const uint4*>(src));
+      }
+    }
+  }
+  acc0[0] = acc0[1] = acc0[2] = acc0[3] = 0.f;
+  acc1[0] = acc1[1] = acc1[2] = acc1[3] = 0.f;
+#pragma unroll
+  for (int s = 0; s < D / 16; ++s) {
+    mma16816<F16>(acc0, ra[0][0][s].x, ra[0][1][s].x, ra[0][0][s].y, ra[0][1][s].y, bq[s][0],
+                  bq[s][1]);
+    mma16816<F16>(acc0, ra[0][0][s].z, ra[0][1][s].z, ra[0][0][s].w, ra[0][1][s].w, bq[s][2],
+                  bq[s][3]);
+    mma16816<F16>(acc1, ra[1][0][s].x, ra[1][1][s].x, ra[1][0][s].y, ra[1][1][s].y, bq[s][0],
+                  bq[s][1]);
+    mma16816<F16>(acc1, ra[1][0][s].z, ra[1][1][s].z, ra[1][0][s].w, ra[1][1][s].w, bq[s][2],
+                  bq[s][3]);
+  }
 }
 
 struct SelScratch {
@@ -344,6 +363,68 @@ __global__ void __launch_bounds__(kSelThreads) union_kernel(const UnionArgs a) {
               a.union_count + unit, sc);
 }
 
+// ------------------------------------------------------- one CTA per unit
+// unit_select_kernel: the bound scores, per-head top-K and union of one
+// (batch, kv head) in one CTA of kUnitWarps warps.  The scores stay in shared
+// memory as order-preserving keys [G][P]; warp h selects head h (and h + 8)
+// from them (select_warp.cuh); warp 0 then builds
+// the union from the heads' bitmaps.  Scoring streams the unit's metadata with
+// two 16-page tiles in flight per warp.
+constexpr int kUnitWarps = 8;
+
+template <int D, bool F16>
+__global__ void __launch_bounds__(kUnitWarps * 32, 1) unit_select_kernel(const UnitSelectArgs a) {
+  extern __shared__ __align__(16) uint8_t usm[];
+  uint32_t* s_keys = reinterpret_cast<uint32_t*>(usm);                     // [G][P]
+  uint32_t* s_bm = s_keys + static_cast<size_t>(a.G) * a.P;                // [G][kSelBitmapWords]
+  uint8_t* s_cand = reinterpret_cast<uint8_t*>(s_bm + a.G * kSelBitmapWords);  // per warp
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int unit = blockIdx.x;
+  const int b = unit / a.Hkv, kvh = unit % a.Hkv;
+  griddep_launch_dependents();
+  griddep_wait();
+  uint32_t bq[D / 16][4];
+  load_q_pm<D>(a.q, a.q_sb, a.q_sh, b, kvh, a.G, lane, bq);
+  const int64_t mbase = static_cast<int64_t>(unit) * a.P * D;
+  const uint16_t* mmax = static_cast<const uint16_t*>(a.meta_max) + mbase;
+  const uint16_t* mmin = static_cast<const uint16_t*>(a.meta_min) + mbase;
+  const int tiles = static_cast<int>(ceil_div(a.P, 16));
+  for (int t = warp; t < tiles; t += 2 * kUnitWarps) {
+    float acc0[4], acc1[4];
+    const int t1 = t + kUnitWarps;
+    score_tile2<D, F16>(bq, mmax, mmin, 16 * t, 16 * min(t1, tiles - 1), a.P, lane, acc0, acc1);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int head = 2 * t4 + (e & 1);
+      const int p0 = 16 * t + g + 8 * (e >> 1), p1 = 16 * t1 + g + 8 * (e >> 1);
+      if (head < a.G && p0 < a.P) s_keys[head * a.P + p0] = score_key(acc0[e]);
+      if (head < a.G && t1 < tiles && p1 < a.P) s_keys[head * a.P + p1] = score_key(acc1[e]);
+    }
+  }
+  __syncthreads();
+  uint32_t* cand_key = reinterpret_cast<uint32_t*>(s_cand + warp * kCandCap * 6);
+  uint16_t* cand_page = reinterpret_cast<uint16_t*>(s_cand + warp * kCandCap * 6 + kCandCap * 4);
+  const int W = static_cast<int>(ceil_div(a.P, 32));
+  for (int h = warp; h < a.G; h += kUnitWarps) {
+    uint32_t* bm = s_bm + h * kSelBitmapWords;
+    for (int w = lane; w < kSelBitmapWords; w += 32) bm[w] = 0u;
+    __syncwarp();
+    const uint32_t* keys = s_keys + h * a.P;
+    warp_topk_head([keys](int j) { return keys[j]; }, a.P, a.kk, bm, cand_key, cand_page);
+    __syncwarp();
+    const int64_t row = static_cast<int64_t>(b) * a.Hq + kvh * a.G + h;
+    warp_emit_row(bm, W, a.selected + row * a.kk, nullptr);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int count = warp_union(s_bm, kSelBitmapWords, a.G, W,
+                                 a.union_list + static_cast<int64_t>(unit) * a.union_stride,
+                                 false);
+    if (lane == 0) a.union_count[unit] = count;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_score(int d, bool f16, const ScoreArgs& a, cudaStream_t s) {
@@ -367,6 +448,22 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
     return launch_pdl(topk_kernel<true>, dim3(a.rows), dim3(kSelThreads), key_bytes, s, a);
   }
   return launch_pdl(topk_kernel<false>, dim3(a.rows), dim3(kSelThreads), 0, s, a);
+}
+
+size_t unit_select_smem(int G, int P) {
+  return static_cast<size_t>(G) * P * 4 + static_cast<size_t>(G) * kSelBitmapWords * 4 +
+         static_cast<size_t>(kUnitWarps) * kCandCap * 6;
+}
+
+cudaError_t launch_unit_select(int d, bool f16, const UnitSelectArgs& a, cudaStream_t s) {
+  const size_t smem = unit_select_smem(a.G, a.P);
+  const dim3 grid(a.B * a.Hkv), block(kUnitWarps * 32);
+  auto kern = d == 128 ? (f16 ? unit_select_kernel<128, true> : unit_select_kernel<128, false>)
+                       : (f16 ? unit_select_kernel<64, true> : unit_select_kernel<64, false>);
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  return launch_pdl(kern, grid, block, smem, s, a);
 }
 
 cudaError_t launch_union(const UnionArgs& a, int units, cudaStream_t s) {

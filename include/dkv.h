@@ -32,9 +32,12 @@
  *     state.  Scratch space is a caller-owned `workspace` of
  *     dkv_workspace_bytes() bytes, zero-filled once before its first use; each
  *     call that completes returns the workspace's counters to zero, so it can
- *     be reused by any later call (of any shape that fits).  After a device
- *     error (dkv_read_device_status) zero-fill it again.  One workspace serves
- *     one call at a time: calls that may overlap on the GPU need separate ones.
+ *     be reused by any later call (of any shape that fits).  The counters
+ *     live in the first DKV_WORKSPACE_HEADER_BYTES bytes, which no call uses
+ *     for anything else; the rest is scratch whose contents never matter.
+ *     After a device error (dkv_read_device_status) zero-fill the header (or
+ *     the whole workspace) again.  One workspace serves one call at a time:
+ *     calls that may overlap on the GPU need separate ones.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *     stream).  Every call is asynchronous on that stream; only
  *     dkv_read_device_status synchronises.
@@ -59,6 +62,9 @@
 
 #include <stddef.h>
 #include <stdint.h>
+
+/* Workspace header: the status word and the work counters. */
+#define DKV_WORKSPACE_HEADER_BYTES ((size_t)256)
 
 #ifdef __cplusplus
 extern "C" {

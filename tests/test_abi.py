@@ -54,9 +54,11 @@ def test_workspace_bytes_layout(L):
     p = _params()
     full = L.dkv_workspace_bytes(ctypes.byref(p), 0)
     sel = L.dkv_workspace_bytes(ctypes.byref(p), 8)
-    # status word and work counters, then (m, l) and o for one chunk per row
-    # (ceil(63 / 64) = 1 chunk; 16 rows, d = 128), each region 256-aligned
-    assert full == 256 + 256 + 16 * 128 * 4
+    # the header (status word, work counters), then
+    # (m, l) and o for one chunk per row (ceil(63 / 64) = 1 chunk; 16 rows,
+    # d = 128), each region 256-aligned
+    header = 256
+    assert full == header + 256 + 16 * 128 * 4
     assert sel > full
     assert L.dkv_workspace_bytes(ctypes.byref(_params(head_dim=96)), 0) == 0
     assert L.dkv_workspace_bytes(ctypes.byref(_params(num_q_heads=7)), 0) == 0

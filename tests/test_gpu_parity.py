@@ -43,6 +43,15 @@ CASES = [
     Workload("one-page", B=1, Hq=2, Hkv=1, d=64, N=16, top_k=1),
     Workload("page+1", B=1, Hq=2, Hkv=2, d=128, N=17, top_k=1),
     Workload("long-chunks", B=1, Hq=4, Hkv=1, d=128, N=70000, top_k=64),
+    # the largest context the per-unit selection kernel takes (2048 pages), and
+    # one page more, where the separate selection kernels run
+    Workload("unit-select-max-pages", B=1, Hq=4, Hkv=1, d=64, N=32768, top_k=100, kind="hot"),
+    Workload("unit-select-max-pages+1", B=1, Hq=8, Hkv=2, d=128, N=32769, top_k=100, kind="hot"),
+    # the per-unit selection kernel: 8 heads per group with a ragged last page;
+    # one head per group in fp16; exact score ties at the threshold
+    Workload("unit-select-gqa8", B=2, Hq=16, Hkv=2, d=128, N=20000, top_k=50, kind="hot"),
+    Workload("unit-select-mha-fp16", B=3, Hq=3, Hkv=3, d=64, N=16400, top_k=200, dtype="fp16"),
+    Workload("unit-select-ties", B=2, Hq=8, Hkv=2, d=64, N=16384, top_k=77, kind="coarse"),
     # more work items than persistent CTAs (2 per SM): every CTA streams
     # several items back to back, exact and sparse
     Workload("multi-item-gqa", B=16, Hq=16, Hkv=8, d=128, N=8192, top_k=48, kind="hot"),
@@ -129,7 +138,8 @@ def test_workspace_reuse_across_calls(dev, dkv):
         assert torch.equal(dkv.decode_attn_full(qa, Ka, Va, workspace=ws), ref_a)
         assert torch.equal(dkv.decode_attn_select(qb, Kb, Vb, mb, wb.top_k, workspace=ws), ref_sb)
         assert torch.equal(dkv.decode_attn_select(qa, Ka, Va, ma, wa.top_k, workspace=ws), ref_sa)
-    assert int(ws[4:12].sum().item()) == 0  # the work and exit counters are back at zero
+    # the status word and the work and exit counters are back at zero
+    assert int(ws[:256].sum().item()) == 0
 
 
 def test_strided_query_and_output(dev, dkv):
@@ -204,6 +214,7 @@ Q4_CASES = [
     Workload("q4-gqa-d64", B=2, Hq=8, Hkv=2, d=64, N=1000, top_k=9, dtype="fp16", kind="offset"),
     Workload("q4-ragged", B=1, Hq=4, Hkv=1, d=128, N=36, top_k=2, dtype="fp16"),
     Workload("q4-multi-item", B=16, Hq=16, Hkv=16, d=128, N=2052, top_k=32, dtype="fp16"),
+    Workload("q4-long-gqa", B=2, Hq=8, Hkv=2, d=128, N=16400, top_k=64, dtype="fp16"),
 ]
 
 

@@ -93,6 +93,8 @@ def make_inputs(w: Workload, seed: int, device="cpu"):
       normal  q, K, V ~ N(0, 1).
       offset  K, V = N(0, 1) + a per-(batch, head, channel) offset ~ N(0, 0.5^2),
               drawn separately for K and V; q ~ N(0, 1).
+      coarse  q, V ~ N(0, 1); K = N(0, 1) rounded to integers (many pages share
+              their channel min / max, so bound scores tie exactly).
       hot     q, V ~ N(0, 1); K ~ N(0, 1), and in every (batch, kv-head)
               round(0.02 * P) pages drawn without replacement get every key
               shifted by 2 * qhat, qhat = the unit-length mean of that group's
@@ -120,6 +122,8 @@ def make_inputs(w: Workload, seed: int, device="cpu"):
                 hot[b, h, pages] = 1.0
         tok_hot = hot.repeat_interleave(w.S, dim=2)[:, :, :w.N]
         K += 2.0 * tok_hot.unsqueeze(-1) * qhat.unsqueeze(2)
+    elif w.kind == "coarse":
+        K = torch.round(K)
     elif w.kind != "normal":
         raise ValueError(w.kind)
     return q.to(dt), K.to(dt), V.to(dt)
