@@ -22,7 +22,7 @@ constexpr size_t kAlign = 256;
 static_assert(DKV_WORKSPACE_HEADER_BYTES == kAlign, "status word and counters");
 // Shared memory the per-unit selection kernel may take (one CTA per SM), and
 // the shortest context (pages) it is used for.
-constexpr size_t kUnitSelectSmemLimit = 200 * 1024;
+constexpr size_t kUnitSelectSmemLimit = 227 * 1024;
 constexpr int kUnitSelectMinP = 1024;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -189,6 +189,31 @@ bool encode_page_map(CUtensorMap* map, const dkv_params* p, const dkv_kv* kv) {
   if (p->num_kv_heads == 1 && st[2] == 0) st[2] = 16;
   if (p->batch == 1 && st[3] == 0) st[3] = 16;
   const CUresult r = g_encode(map, dt, 5, const_cast<void*>(kv->data), dims, st, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Map over page metadata [B, Hkv, P, d] (contiguous) viewed like a cache:
+// {64 channels, P pages, d/64 halves, Hkv, B}, box {64, box_pages, d/64, 1, 1},
+// 128-byte swizzle.
+bool encode_meta_map(CUtensorMap* map, const dkv_params* p, const void* meta, bool f16,
+                     int box_pages) {
+  if (!get_encode()) return false;
+  const int d = p->head_dim;
+  const uint64_t P = static_cast<uint64_t>(ceil_div(p->seq_len, p->page_size));
+  const cuuint64_t dims[5] = {64, P, static_cast<cuuint64_t>(d / 64),
+                              static_cast<cuuint64_t>(p->num_kv_heads),
+                              static_cast<cuuint64_t>(p->batch)};
+  const cuuint64_t st[4] = {static_cast<cuuint64_t>(d) * 2, 128, P * d * 2,
+                            P * d * 2 * static_cast<cuuint64_t>(p->num_kv_heads)};
+  const cuuint32_t box[5] = {64, static_cast<cuuint32_t>(box_pages),
+                             static_cast<cuuint32_t>(d / 64), 1, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUresult r = g_encode(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                              5, const_cast<void*>(meta), dims, st, box, estr,
                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -383,7 +408,7 @@ dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_
   a.union_stride = L.union_stride;
 
   if (P >= kUnitSelectMinP && P <= dkv::kUnitMaxP &&
-      dkv::unit_select_smem(G, P) <= static_cast<size_t>(kUnitSelectSmemLimit)) {
+      dkv::unit_select_smem(p->head_dim, G, P) <= static_cast<size_t>(kUnitSelectSmemLimit)) {
     // Long contexts: one CTA per (batch, kv head) scores its pages, selects
     // each head's top-K and builds the union list.  (Shorter ones have too
     // little metadata per CTA to hide the selection's latency; the three
@@ -404,7 +429,13 @@ dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_
     ua.union_list = ulist;
     ua.union_count = ucount;
     ua.union_stride = L.union_stride;
-    if ((st = cuda_status(dkv::launch_unit_select(p->head_dim, f16, ua, s))) != DKV_OK) return st;
+    ua.status = a.status;
+    ua.wait_limit_ns = a.wait_limit_ns;
+    CUtensorMap mmx, mmn;
+    if (!encode_meta_map(&mmx, p, meta_max, f16, 64) || !encode_meta_map(&mmn, p, meta_min, f16, 64))
+      return DKV_ERR_CUDA;
+    if ((st = cuda_status(dkv::launch_unit_select(p->head_dim, f16, ua, mmx, mmn, s))) != DKV_OK)
+      return st;
     return run_attention(p, a, true, f16, mk, mv, out, out_dtype, s);
   }
 

@@ -134,6 +134,8 @@ struct UnitSelectArgs {
   int2* union_list;            // [B * Hkv, union_stride]
   int* union_count;            // [B * Hkv]
   int union_stride;
+  uint32_t* status;
+  uint64_t wait_limit_ns;
 };
 
 struct MetaArgs {
@@ -176,8 +178,10 @@ cudaError_t launch_score(int d, bool f16, const ScoreArgs& a, cudaStream_t s);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
 cudaError_t launch_union(const UnionArgs& a, int units, cudaStream_t s);
 // Shared memory of unit_select_kernel for G heads of P pages (P <= kUnitMaxP).
-size_t unit_select_smem(int G, int P);
-cudaError_t launch_unit_select(int d, bool f16, const UnitSelectArgs& a, cudaStream_t s);
+size_t unit_select_smem(int d, int G, int P);
+// mmx / mmn: maps over meta_max / meta_min, box {64, 64 pages, d/64, 1, 1}.
+cudaError_t launch_unit_select(int d, bool f16, const UnitSelectArgs& a, const CUtensorMap& mmx,
+                               const CUtensorMap& mmn, cudaStream_t s);
 
 cudaError_t launch_meta(bool q4, bool f16, const MetaArgs& a, cudaStream_t s);
 cudaError_t launch_quant4(int64_t rows, int d, const void* x, void* codes, void* gmin,

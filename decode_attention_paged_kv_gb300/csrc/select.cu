@@ -102,43 +102,6 @@ __device__ __forceinline__ void score_tile(const uint32_t (&bq)[D / 16][4], cons
   }
 }
 
-// Two tiles (pages page0.. and page1.. , both < P rows clamped) with every
-// load of both issued before the first MMA.
-template <int D, bool F16>
-__device__ __forceinline__ void score_tile2(const uint32_t (&bq)[D / 16][4], const uint16_t* mmax,
-                                            const uint16_t* mmin, int page0, int page1, int P,
-                                            int lane, float (&acc0)[4], float (&acc1)[4]) {
-  const int g = lane >> 2, t4 = lane & 3;
-  uint4 ra[2][2][D / 16];
-#pragma unroll
-  for (int tt = 0; tt < 2; ++tt) {
-#pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-      const int page = min((tt ? page1 : page0) + g + 8 * hr, P - 1);
-#pragma unroll
-      for (int s = 0; s < D / 16; ++s) {
-        const int c = t4 + 4 * s;
-        const uint16_t* src = (c < D / 8) ? mmax + static_cast<int64_t>(page) * D + 8 * c
-                                          : mmin + static_cast<int64_t>(page) * D + 8 * (c - D / 8);
-        ra[tt][hr][s] = __ldg(reinterpret_cast<const uint4*>(src));
-      }
-    }
-  }
-  acc0[0] = acc0[1] = acc0[2] = acc0[3] = 0.f;
-  acc1[0] = acc1[1] = acc1[2] = acc1[3] = 0.f;
-#pragma unroll
-  for (int s = 0; s < D / 16; ++s) {
-    mma16816<F16>(acc0, ra[0][0][s].x, ra[0][1][s].x, ra[0][0][s].y, ra[0][1][s].y, bq[s][0],
-                  bq[s][1]);
-    mma16816<F16>(acc0, ra[0][0][s].z, ra[0][1][s].z, ra[0][0][s].w, ra[0][1][s].w, bq[s][2],
-                  bq[s][3]);
-    mma16816<F16>(acc1, ra[1][0][s].x, ra[1][1][s].x, ra[1][0][s].y, ra[1][1][s].y, bq[s][0],
-                  bq[s][1]);
-    mma16816<F16>(acc1, ra[1][0][s].z, ra[1][1][s].z, ra[1][0][s].w, ra[1][1][s].w, bq[s][2],
-                  bq[s][3]);
-  }
-}
-
 struct SelScratch {
   uint32_t hist[256];
   long long warp_tot[kSelWarps];
@@ -365,48 +328,177 @@ __global__ void __launch_bounds__(kSelThreads) union_kernel(const UnionArgs a) {
 
 // ------------------------------------------------------- one CTA per unit
 // unit_select_kernel: the bound scores, per-head top-K and union of one
-// (batch, kv head) in one CTA of kUnitWarps warps.  The scores stay in shared
-// memory as order-preserving keys [G][P]; warp h selects head h (and h + 8)
-// from them (select_warp.cuh); warp 0 then builds
-// the union from the heads' bitmaps.  Scoring streams the unit's metadata with
-// two 16-page tiles in flight per warp.
-constexpr int kUnitWarps = 8;
+// (batch, kv head) in one CTA.  Warp 8 streams the unit's metadata with TMA
+// tensor copies, 64 pages of [M] and [m] per stage (128-byte swizzle); a stage
+// goes to consumer warps 0-3 or 4-7 (alternately), each of which scores one
+// 16-page tile of it on tensor cores: S[head][page] = q+ . M + q- . m, as in
+// the score kernel but with the pages' metadata read by ldmatrix.  The scores
+// stay in shared memory as order-preserving keys [G][P]; then warp h selects
+// head h (select_warp.cuh) and warp 0 builds the union from the heads'
+// bitmaps.  Every wait is bounded.
+constexpr int kUnitConsumers = 8;
+constexpr int kUnitThreads = (kUnitConsumers + 1) * 32;
+constexpr int kUnitBoxPages = 64;
+
+template <int D>
+struct UnitCfg {
+  static constexpr int kBoxBytes = kUnitBoxPages * D * 2;  // one of [M] / [m]
+  static constexpr int kStageBytes = 2 * kBoxBytes;
+  static constexpr int kStages = (128 * 1024) / kStageBytes;  // 128 KiB in flight
+  static constexpr int kBarOffset = kStages * kStageBytes;
+  static constexpr int kKeysOffset = kBarOffset + 2 * kStages * 8 + 16;  // + abort flag
+};
+
+// Shared address of channels [c, c+8) of page row t of a metadata box
+// {64 channels, 64 pages, D/64 halves} written with 128-byte swizzle.
+__device__ __forceinline__ uint32_t box_addr(uint32_t base, int t, int c) {
+  const int row = (c >> 6) * kUnitBoxPages + t;
+  const int chunk = ((c & 63) >> 3) ^ (row & 7);
+  return base + static_cast<uint32_t>(row * 128 + chunk * 16);
+}
+
+__device__ __forceinline__ void unit_consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"r"(kUnitConsumers * 32) : "memory");
+}
 
 template <int D, bool F16>
-__global__ void __launch_bounds__(kUnitWarps * 32, 1) unit_select_kernel(const UnitSelectArgs a) {
-  extern __shared__ __align__(16) uint8_t usm[];
-  uint32_t* s_keys = reinterpret_cast<uint32_t*>(usm);                     // [G][P]
-  uint32_t* s_bm = s_keys + static_cast<size_t>(a.G) * a.P;                // [G][kSelBitmapWords]
+__global__ void __launch_bounds__(kUnitThreads, 1)
+    unit_select_kernel(const UnitSelectArgs a, const __grid_constant__ CUtensorMap mmx,
+                       const __grid_constant__ CUtensorMap mmn) {
+  using C = UnitCfg<D>;
+  extern __shared__ uint8_t usm_raw[];
+  uint8_t* usm = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(usm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(usm);
+  const uint32_t full0 = sbase + C::kBarOffset, empty0 = full0 + 8 * C::kStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(usm + C::kBarOffset + 16 * C::kStages);
+  uint32_t* s_keys = reinterpret_cast<uint32_t*>(usm + C::kKeysOffset);      // [G][P]
+  uint32_t* s_bm = s_keys + static_cast<size_t>(a.G) * a.P;                  // [G][kSelBitmapWords]
   uint8_t* s_cand = reinterpret_cast<uint8_t*>(s_bm + a.G * kSelBitmapWords);  // per warp
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t4 = lane & 3;
   const int unit = blockIdx.x;
   const int b = unit / a.Hkv, kvh = unit % a.Hkv;
+  const int n_boxes = static_cast<int>(ceil_div(a.P, kUnitBoxPages));
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 4);  // the four warps that score the stage
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kUnitConsumers && lane == 0) {
+    prefetch_tensormap(&mmx);
+    prefetch_tensormap(&mmn);
+  }
   griddep_launch_dependents();
   griddep_wait();
-  uint32_t bq[D / 16][4];
-  load_q_pm<D>(a.q, a.q_sb, a.q_sh, b, kvh, a.G, lane, bq);
-  const int64_t mbase = static_cast<int64_t>(unit) * a.P * D;
-  const uint16_t* mmax = static_cast<const uint16_t*>(a.meta_max) + mbase;
-  const uint16_t* mmin = static_cast<const uint16_t*>(a.meta_min) + mbase;
-  const int tiles = static_cast<int>(ceil_div(a.P, 16));
-  for (int t = warp; t < tiles; t += 2 * kUnitWarps) {
-    float acc0[4], acc1[4];
-    const int t1 = t + kUnitWarps;
-    score_tile2<D, F16>(bq, mmax, mmin, 16 * t, 16 * min(t1, tiles - 1), a.P, lane, acc0, acc1);
+  __syncthreads();
+
+  if (warp == kUnitConsumers) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();
+      int issued = 0;
+      for (int i = 0; i < n_boxes; ++i) {
+        const int s = i % C::kStages;
+        if (i >= C::kStages &&
+            !mbar_wait_bounded(empty0 + 8 * s, ((i / C::kStages) - 1) & 1, a.wait_limit_ns,
+                               abort_flag)) {
+          if (*abort_flag == 0) {
+            set_status(a.status, kStatusTimeout);
+            *abort_flag = 1;
+          }
+          break;
+        }
+        const uint32_t dst = sbase + s * C::kStageBytes;
+        mbar_arrive_expect_tx(full0 + 8 * s, C::kStageBytes);
+        tma_load_5d_hint(dst, &mmx, full0 + 8 * s, 0, i * kUnitBoxPages, 0, kvh, b, pol);
+        tma_load_5d_hint(dst + C::kBoxBytes, &mmn, full0 + 8 * s, 0, i * kUnitBoxPages, 0, kvh, b,
+                         pol);
+        issued = i + 1;
+      }
+      // The last copies issued have landed before this warp leaves (so no copy
+      // is still writing when the consumers stop early); each wait is bounded.
+      const uint64_t deadline = globaltimer_ns() + 200000000ull;
+      for (int j = max(0, issued - C::kStages); j < issued; ++j) {
+        const uint64_t now = globaltimer_ns();
+        if (now >= deadline) break;
+        mbar_wait_bounded(full0 + 8 * (j % C::kStages), (j / C::kStages) & 1, deadline - now,
+                          nullptr);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- scoring
+  const int g = lane >> 2, t4 = lane & 3;
+  const bool head_ok = g < a.G;
+  const int mtx = lane >> 3, mrow = lane & 7;
+  uint32_t qp[D / 16][2], qm[D / 16][2];  // A fragments of q+ and q- (rows = heads)
+  {
+    const uint16_t* qrow = static_cast<const uint16_t*>(a.q) + b * a.q_sb +
+                           static_cast<int64_t>(kvh * a.G + (head_ok ? g : 0)) * a.q_sh;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int head = 2 * t4 + (e & 1);
-      const int p0 = 16 * t + g + 8 * (e >> 1), p1 = 16 * t1 + g + 8 * (e >> 1);
-      if (head < a.G && p0 < a.P) s_keys[head * a.P + p0] = score_key(acc0[e]);
-      if (head < a.G && t1 < tiles && p1 < a.P) s_keys[head * a.P + p1] = score_key(acc1[e]);
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const uint32_t w0 =
+          head_ok ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * t4) : 0u;
+      const uint32_t w1 =
+          head_ok ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * t4 + 8) : 0u;
+      qp[ks][0] = keep_sign(w0, false);
+      qm[ks][0] = keep_sign(w0, true);
+      qp[ks][1] = keep_sign(w1, false);
+      qm[ks][1] = keep_sign(w1, true);
     }
   }
-  __syncthreads();
+  const int half = warp >> 2, tile = warp & 3;  // boxes of parity `half`, tile `tile` of each
+  bool ok = true;
+  for (int i = half; i < n_boxes; i += 2) {
+    const int s = i % C::kStages;
+    ok = mbar_wait_bounded(full0 + 8 * s, (i / C::kStages) & 1, a.wait_limit_ns, abort_flag);
+    if (!__all_sync(0xffffffffu, ok)) {
+      ok = false;
+      break;
+    }
+    const uint32_t mb = sbase + s * C::kStageBytes, nb = mb + C::kBoxBytes;
+    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      uint32_t r0, r1, r2, r3;
+      const int row = 16 * tile + 8 * (mtx >> 1) + mrow, ch = 16 * ks + 8 * (mtx & 1);
+      ldsm_x4(box_addr(mb, row, ch), r0, r1, r2, r3);
+      mma16816<F16>(sc[0], qp[ks][0], 0u, qp[ks][1], 0u, r0, r1);
+      mma16816<F16>(sc[1], qp[ks][0], 0u, qp[ks][1], 0u, r2, r3);
+      ldsm_x4(box_addr(nb, row, ch), r0, r1, r2, r3);
+      mma16816<F16>(sc[0], qm[ks][0], 0u, qm[ks][1], 0u, r0, r1);
+      mma16816<F16>(sc[1], qm[ks][0], 0u, qm[ks][1], 0u, r2, r3);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    if (head_ok) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int p = i * kUnitBoxPages + 16 * tile + 8 * (e >> 1) + 2 * t4 + (e & 1);
+        if (p < a.P) s_keys[g * a.P + p] = score_key(sc[e >> 1][e & 1]);
+      }
+    }
+  }
+  // (a warp that timed out tells the others through the abort flag)
+  if (!ok && lane == 0 && *abort_flag == 0) {
+    set_status(a.status, kStatusTimeout);
+    *abort_flag = 1;
+  }
+  unit_consumers_sync();
+  if (*abort_flag) {
+    if (threadIdx.x == 0) a.union_count[unit] = 0;  // gather nothing for this unit
+    return;
+  }
+
+  // ------------------------------------------------------------ selection
   uint32_t* cand_key = reinterpret_cast<uint32_t*>(s_cand + warp * kCandCap * 6);
   uint16_t* cand_page = reinterpret_cast<uint16_t*>(s_cand + warp * kCandCap * 6 + kCandCap * 4);
   const int W = static_cast<int>(ceil_div(a.P, 32));
-  for (int h = warp; h < a.G; h += kUnitWarps) {
+  for (int h = warp; h < a.G; h += kUnitConsumers) {
     uint32_t* bm = s_bm + h * kSelBitmapWords;
     for (int w = lane; w < kSelBitmapWords; w += 32) bm[w] = 0u;
     __syncwarp();
@@ -416,7 +508,7 @@ __global__ void __launch_bounds__(kUnitWarps * 32, 1) unit_select_kernel(const U
     const int64_t row = static_cast<int64_t>(b) * a.Hq + kvh * a.G + h;
     warp_emit_row(bm, W, a.selected + row * a.kk, nullptr);
   }
-  __syncthreads();
+  unit_consumers_sync();
   if (warp == 0) {
     const int count = warp_union(s_bm, kSelBitmapWords, a.G, W,
                                  a.union_list + static_cast<int64_t>(unit) * a.union_stride,
@@ -450,20 +542,22 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
   return launch_pdl(topk_kernel<false>, dim3(a.rows), dim3(kSelThreads), 0, s, a);
 }
 
-size_t unit_select_smem(int G, int P) {
-  return static_cast<size_t>(G) * P * 4 + static_cast<size_t>(G) * kSelBitmapWords * 4 +
-         static_cast<size_t>(kUnitWarps) * kCandCap * 6;
+size_t unit_select_smem(int d, int G, int P) {
+  const size_t keys_off = d == 128 ? UnitCfg<128>::kKeysOffset : UnitCfg<64>::kKeysOffset;
+  return 1024 + keys_off + static_cast<size_t>(G) * P * 4 +
+         static_cast<size_t>(G) * kSelBitmapWords * 4 + static_cast<size_t>(kUnitConsumers) * kCandCap * 6;
 }
 
-cudaError_t launch_unit_select(int d, bool f16, const UnitSelectArgs& a, cudaStream_t s) {
-  const size_t smem = unit_select_smem(a.G, a.P);
-  const dim3 grid(a.B * a.Hkv), block(kUnitWarps * 32);
+cudaError_t launch_unit_select(int d, bool f16, const UnitSelectArgs& a, const CUtensorMap& mmx,
+                               const CUtensorMap& mmn, cudaStream_t s) {
+  const size_t smem = unit_select_smem(d, a.G, a.P);
+  const dim3 grid(a.B * a.Hkv), block(kUnitThreads);
   auto kern = d == 128 ? (f16 ? unit_select_kernel<128, true> : unit_select_kernel<128, false>)
                        : (f16 ? unit_select_kernel<64, true> : unit_select_kernel<64, false>);
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, grid, block, smem, s, a);
+  return launch_pdl(kern, grid, block, smem, s, a, mmx, mmn);
 }
 
 cudaError_t launch_union(const UnionArgs& a, int units, cudaStream_t s) {

@@ -47,6 +47,24 @@ def test_forced_timeout_reports_and_recovers(dev):
     assert dkv.read_device_status(ws) == dkv.DKV_OK
 
 
+@pytest.mark.parametrize("N", [20000, 2000])
+def test_forced_timeout_select_paths(N, dev):
+    # 1250 pages: the per-(batch, kv head) selection kernel; 125 pages: the
+    # score / top-K / union kernels.  Both report the timeout and recover.
+    import decode_attention_paged_kv_gb300 as dkv
+    w = Workload("to2", B=2, Hq=8, Hkv=2, d=128, N=N, top_k=16, kind="hot")
+    q, K, V = (t.to(dev) for t in make_inputs(w, seed=8))
+    meta = dkv.kv_meta_build(K)
+    n = dkv.workspace_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, w.top_k)
+    ws = torch.zeros(n, dtype=torch.uint8, device=dev)
+    dkv.decode_attn_select(q, K, V, meta, w.top_k, workspace=ws, flags=dkv.DKV_FLAG_FORCE_TIMEOUT)
+    assert dkv.read_device_status(ws) == dkv.DKV_ERR_DEVICE_TIMEOUT
+    good = dkv.decode_attn_select(q, K, V, meta, w.top_k, workspace=ws)
+    assert dkv.read_device_status(ws) == dkv.DKV_OK
+    ref = dkv.decode_attn_select(q, K, V, meta, w.top_k)
+    assert torch.equal(good, ref)
+
+
 def test_argument_errors_raise(dev):
     import decode_attention_paged_kv_gb300 as dkv
     q = torch.zeros(1, 4, 96, dtype=torch.bfloat16, device=dev)
