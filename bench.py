@@ -76,13 +76,14 @@ def peaks():
         return 6800.0, "fallback"
 
 
-def source_sha() -> str:
+def source_sha(files=None) -> str:
+    """Hash of the kernel sources (all of csrc/, or the listed files in it)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "decode_attention_paged_kv_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + fh.read())
+    names = files if files else [f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h"))]
+    for f in sorted(names):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
@@ -94,7 +95,7 @@ def ncu_traffic(kernel_key: str):
         with open(path) as f:
             t = json.load(f)
         e = t["kernels"][kernel_key]
-        if e.get("source_sha") != source_sha():
+        if e.get("source_sha") != source_sha(e.get("sources")):
             return None
         return e["dram_bytes_per_launch_full_size"]
     except Exception:

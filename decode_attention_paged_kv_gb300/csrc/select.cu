@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(kSelThreads) union_kernel(const UnionArgs a) {
 // 16-page tile of it on tensor cores: S[head][page] = q+ . M + q- . m, as in
 // the score kernel but with the pages' metadata read by ldmatrix.  The scores
 // stay in shared memory as order-preserving keys [G][P]; then warp h selects
-// head h (select_warp.cuh) and warp 0 builds the union from the heads'
+// head h (select_warp.cuh) and all eight warps build the union from the heads'
 // bitmaps.  Every wait is bounded.
 constexpr int kUnitConsumers = 8;
 constexpr int kUnitThreads = (kUnitConsumers + 1) * 32;
@@ -374,7 +374,6 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(usm + C::kBarOffset + 16 * C::kStages);
   uint32_t* s_keys = reinterpret_cast<uint32_t*>(usm + C::kKeysOffset);      // [G][P]
   uint32_t* s_bm = s_keys + static_cast<size_t>(a.G) * a.P;                  // [G][kSelBitmapWords]
-  uint8_t* s_cand = reinterpret_cast<uint8_t*>(s_bm + a.G * kSelBitmapWords);  // per warp
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int unit = blockIdx.x;
   const int b = unit / a.Hkv, kvh = unit % a.Hkv;
@@ -495,25 +494,56 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
   }
 
   // ------------------------------------------------------------ selection
-  uint32_t* cand_key = reinterpret_cast<uint32_t*>(s_cand + warp * kCandCap * 6);
-  uint16_t* cand_page = reinterpret_cast<uint16_t*>(s_cand + warp * kCandCap * 6 + kCandCap * 4);
   const int W = static_cast<int>(ceil_div(a.P, 32));
   for (int h = warp; h < a.G; h += kUnitConsumers) {
     uint32_t* bm = s_bm + h * kSelBitmapWords;
-    for (int w = lane; w < kSelBitmapWords; w += 32) bm[w] = 0u;
-    __syncwarp();
     const uint32_t* keys = s_keys + h * a.P;
-    warp_topk_head([keys](int j) { return keys[j]; }, a.P, a.kk, bm, cand_key, cand_page);
+    warp_topk_head([keys](int j) { return keys[j]; }, a.P, a.kk, bm);
     __syncwarp();
     const int64_t row = static_cast<int64_t>(b) * a.Hq + kvh * a.G + h;
     warp_emit_row(bm, W, a.selected + row * a.kk, nullptr);
   }
   unit_consumers_sync();
-  if (warp == 0) {
-    const int count = warp_union(s_bm, kSelBitmapWords, a.G, W,
-                                 a.union_list + static_cast<int64_t>(unit) * a.union_stride,
-                                 false);
-    if (lane == 0) a.union_count[unit] = count;
+  // Union of the heads' bitmaps, ascending, with a bit per head: warp w ORs
+  // words w * wpw .. (one per lane), the per-warp counts place them.
+  {
+    const int wpw = static_cast<int>(ceil_div(W, kUnitConsumers));
+    const int wi = warp * wpw + lane;
+    const bool own = lane < wpw && wi < W;
+    uint32_t hw[8];
+    uint32_t u = 0;
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+      hw[h] = (own && h < a.G) ? s_bm[h * kSelBitmapWords + wi] : 0u;
+      u |= hw[h];
+    }
+    const int c = __popc(u);
+    int incl = c;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += t;
+    }
+    int* wtot = reinterpret_cast<int*>(s_keys);  // (the keys are no longer needed)
+    if (lane == 31) wtot[warp] = incl;
+    unit_consumers_sync();
+    int before = 0, count = 0;
+#pragma unroll
+    for (int v = 0; v < kUnitConsumers; ++v) {
+      before += v < warp ? wtot[v] : 0;
+      count += wtot[v];
+    }
+    int2* out = a.union_list + static_cast<int64_t>(unit) * a.union_stride;
+    int at = before + incl - c;
+    while (u) {
+      const int bit = __ffs(u) - 1;
+      u &= u - 1;
+      uint32_t m = 0;
+#pragma unroll
+      for (int h = 0; h < 8; ++h) m |= ((hw[h] >> bit) & 1u) << h;
+      out[at++] = make_int2(wi * 32 + bit, static_cast<int>(m));
+    }
+    if (threadIdx.x == 0) a.union_count[unit] = count;
   }
 }
 
@@ -545,7 +575,7 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
 size_t unit_select_smem(int d, int G, int P) {
   const size_t keys_off = d == 128 ? UnitCfg<128>::kKeysOffset : UnitCfg<64>::kKeysOffset;
   return 1024 + keys_off + static_cast<size_t>(G) * P * 4 +
-         static_cast<size_t>(G) * kSelBitmapWords * 4 + static_cast<size_t>(kUnitConsumers) * kCandCap * 6;
+         static_cast<size_t>(G) * kSelBitmapWords * 4;
 }
 
 cudaError_t launch_unit_select(int d, bool f16, const UnitSelectArgs& a, const CUtensorMap& mmx,
