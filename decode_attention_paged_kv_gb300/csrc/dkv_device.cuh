@@ -225,7 +225,14 @@ __device__ __forceinline__ uint32_t from_key2(uint32_t k) {
 // step = fp16(fp32(fp32(mx - mn) / 15)), from the group's stored min / max.
 __device__ __forceinline__ __half q4_step(__half mn, __half mx) {
   const float range = __fsub_rn(__half2float(mx), __half2float(mn));
-  return __float2half_rn(__fdiv_rn(range, 15.0f));
+  // fl(range / 15) by the FMA method for division by a constant: q = fl(range
+  // * fl(1/15)), corrected once with the exact remainder.  Equal to the IEEE
+  // quotient for every binary32 in [0, 2^18), which holds every fp16 range
+  // (checked exhaustively on the host).
+  constexpr float kInv15 = 1.0f / 15.0f;
+  const float q = __fmul_rn(range, kInv15);
+  const float r = __fmaf_rn(-q, 15.0f, range);
+  return __float2half_rn(__fmaf_rn(r, kInv15, q));
 }
 
 // Dequantise the 8 codes of one 32-bit word (byte i: channel 2i low nibble,

@@ -140,11 +140,21 @@ __global__ void __launch_bounds__(256) quant4_kernel(int64_t groups, const __hal
     const float fmn = __half2float(mn);
     uint32_t packed = 0;
     if (fstep != 0.f) {
+      // code = min(15, rint(fl(d / step))), d = fl(x - mn) >= 0.  The
+      // product q = fl(d * fl(1 / step)) is within 2^-22 relative of
+      // fl(d / step) (three roundings of 2^-24 each), i.e. within 2^-18 while
+      // q < 16; from 16 up both clamp to 15.  So rint(q) is the code unless q
+      // lies within 2^-16 of a half-integer, and only then is the IEEE
+      // quotient computed.
+      const float inv = __frcp_rn(fstep);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const uint32_t hv = (w[e >> 1] >> (16 * (e & 1))) & 0xffffu;
         const float xf = __half2float(__ushort_as_half(static_cast<unsigned short>(hv)));
-        float c = rintf(__fdiv_rn(__fsub_rn(xf, fmn), fstep));
+        const float dq = __fsub_rn(xf, fmn);
+        const float q = __fmul_rn(dq, inv);
+        float c = rintf(q);
+        if (fabsf(fabsf(q - c) - 0.5f) < 0x1p-16f) c = rintf(__fdiv_rn(dq, fstep));
         c = fminf(15.f, fmaxf(0.f, c));
         packed |= static_cast<uint32_t>(c) << (4 * e);
       }

@@ -184,6 +184,12 @@ def test_quant4_dequant4_bit_exact(dev, dkv):
     x[2] = 1.5
     x[3, :64] = np.arange(64)
     x[4] = np.clip(rng.standard_normal(d) * 4e4, -65504, 65504)  # finite, near the fp16 max
+    # exact half-way quotients: step = 1 (min 0, max 15), values k + 1/2 round
+    # to even; and steps that are fp16 subnormals
+    x[5, :64] = np.concatenate([[0.0, 15.0], np.arange(31) * 0.5, np.arange(31) * 0.5 + 0.25])
+    x[5, 64:] = np.concatenate([[-3.0, 12.0], np.arange(62) * 0.5 - 3.0])
+    x[6] = rng.integers(0, 16, d) * 2.0 ** -24  # a subnormal grid
+    x[7] = rng.standard_normal(d) * 2.0 ** -20
     xb = np.asarray(x, np.float64).astype(np.float16).view(np.uint16)
     xt = torch.from_numpy(xb.view(np.int16)).view(torch.float16)
     q4 = dkv.kv_quant4(xt.to(dev))
