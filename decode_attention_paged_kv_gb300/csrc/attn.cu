@@ -64,16 +64,10 @@ struct AttnCfg {
   // 4-bit stage: K codes | V codes | K min | K max | V min | V max
   static constexpr int kQ4StageBytes = 2 * kCodeBytes + 4 * kGroupBytes;
   static constexpr int kStageBytes = Q4 ? (kQ4StageBytes + 127) / 128 * 128 : 2 * kPageBytes;
-  static constexpr int kStages = attn_stages(D);
+  // 4-bit pages are a quarter the size: more of them in flight.
+  static constexpr int kStages = Q4 ? (D == 128 ? 32 : 48) : attn_stages(D);
   static constexpr int kSub = kStages / kConsumerWarps;             // stages per consumer warp
-  // 4-bit: per consumer warp, the dequantised K and V tiles of its page and
-  // the (min, max, step) of every (tensor, token, group) of that page.
-  static constexpr int kTileOffset = (kStages * kStageBytes + 1023) / 1024 * 1024;
-  static constexpr int kTileBytes = Q4 ? kConsumerWarps * 2 * kPageBytes : 0;
-  static constexpr int kStepsPerWarp = 2 * kPage * (D / 64);
-  static constexpr int kStepOffset = kTileOffset + kTileBytes;
-  static constexpr int kStepBytes = Q4 ? kConsumerWarps * 3 * kStepsPerWarp * 2 : 0;
-  static constexpr int kBarOffset = (kStepOffset + kStepBytes + 15) / 16 * 16;
+  static constexpr int kBarOffset = (kStages * kStageBytes + 15) / 16 * 16;
   static constexpr int kStageMetaOffset = kBarOffset + (2 * kStages + 4) * 8;
   static constexpr int kDescOffset = kStageMetaOffset + kStages * 8;
   static constexpr int kMergeOffset = kDescOffset + 2 * 16;
@@ -116,86 +110,214 @@ __device__ __forceinline__ bool consumers_any(bool flag) {
   return res != 0;
 }
 
-// 4-bit path, producer: move one page of K and V codes and group bounds into
-// a stage.  Whole pages go by five-plus-one 1-D bulk copies; a ragged last page
-// copies only its valid tokens' codes and loads their group bounds with plain
-// loads, so nothing is read past the cache.
-template <typename C>
-__device__ __forceinline__ void issue_q4_page(const AttnArgs& a, int b, int kvh, int page,
-                                              uint32_t dst, uint8_t* dst_ptr, uint32_t bar) {
-  constexpr int D = C::kPageBytes / (kPage * 2);
+// 4-bit path, producer.  A whole page moves by six 1-D bulk copies, one per
+// issuing lane: part 0 K codes, 1 V codes, 2-5 K min, K max, V min, V max.
+template <typename C, int D>
+__device__ __forceinline__ void q4_copy(const AttnArgs& a, int b, int kvh, int page, int part,
+                                        uint32_t dst, uint32_t bar) {
   constexpr int ng = D / 64;
-  const int t0 = page * kPage;
-  const int nt = min(kPage, a.N - t0);
-  const uint8_t* kc = a.k4.codes + b * a.k4.sb + kvh * a.k4.sh + static_cast<int64_t>(t0) * (D / 2);
-  const uint8_t* vc = a.v4.codes + b * a.v4.sb + kvh * a.v4.sh + static_cast<int64_t>(t0) * (D / 2);
-  const int64_t kg = b * a.k4.gsb + kvh * a.k4.gsh + static_cast<int64_t>(t0) * ng;
-  const int64_t vg = b * a.v4.gsb + kvh * a.v4.gsh + static_cast<int64_t>(t0) * ng;
-  const __half* src[4] = {a.k4.gmin + kg, a.k4.gmax + kg, a.v4.gmin + vg, a.v4.gmax + vg};
-  if (nt == kPage) {
-    mbar_arrive_expect_tx(bar, C::kQ4StageBytes);
-    bulk_load(dst, kc, C::kCodeBytes, bar);
-    bulk_load(dst + C::kCodeBytes, vc, C::kCodeBytes, bar);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      bulk_load(dst + 2 * C::kCodeBytes + i * C::kGroupBytes, src[i], C::kGroupBytes, bar);
+  const int64_t t0 = static_cast<int64_t>(page) * kPage;
+  if (part < 2) {
+    const Q4View& v = part == 0 ? a.k4 : a.v4;
+    bulk_load(dst + part * C::kCodeBytes, v.codes + b * v.sb + kvh * v.sh + t0 * (D / 2),
+              C::kCodeBytes, bar);
   } else {
-    __half* gb = reinterpret_cast<__half*>(dst_ptr + 2 * C::kCodeBytes);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      for (int e = 0; e < nt * ng; ++e) gb[i * kPage * ng + e] = src[i][e];
-    const uint32_t cb = static_cast<uint32_t>(nt * (D / 2));
-    mbar_arrive_expect_tx(bar, 2 * cb);  // also releases the plain stores above
-    bulk_load(dst, kc, cb, bar);
-    bulk_load(dst + C::kCodeBytes, vc, cb, bar);
+    const int i = part - 2;
+    const Q4View& v = i < 2 ? a.k4 : a.v4;
+    const __half* src = ((i & 1) ? v.gmax : v.gmin) + b * v.gsb + kvh * v.gsh + t0 * ng;
+    bulk_load(dst + 2 * C::kCodeBytes + i * C::kGroupBytes, src, C::kGroupBytes, bar);
   }
 }
 
-// 4-bit path, consumer warp: dequantise one stage (nt valid tokens) into the
-// warp's K and V tiles, laid out like the TMA page tiles (tile_addr), so the
-// attention code is shared.  x = fp16(code * step + mn) capped at mx, exactly
-// as dkv_kv_dequant4 computes it; tokens past nt become zeros.
+// 4-bit path, producer: the ragged last page (nt < 16 tokens), by one lane.
+// Only the valid tokens' codes are copied and their group bounds loaded with
+// plain loads, so nothing is read past the cache; the bounds of the missing
+// tokens are zeroed, so whatever codes their rows hold dequantise to 0.
 template <typename C, int D>
-__device__ __forceinline__ void dequant_q4_page(const uint8_t* stage, uint8_t* ktile,
-                                                uint8_t* vtile, __half* steps, int nt, int lane) {
+__device__ __forceinline__ void q4_ragged(const AttnArgs& a, int b, int kvh, int page, int nt,
+                                          uint32_t dst, uint8_t* dst_ptr, uint32_t bar) {
   constexpr int ng = D / 64;
-  constexpr int kPer = kPage * ng;  // (token, group) pairs per tensor
-  const __half* gb = reinterpret_cast<const __half*>(stage + 2 * C::kCodeBytes);
-  __half* s_mn = steps;
-  __half* s_mx = steps + C::kStepsPerWarp;
-  __half* s_st = steps + 2 * C::kStepsPerWarp;
-  for (int e = lane; e < 2 * kPer; e += 32) {
-    const int tensor = e / kPer, r = e % kPer;
-    __half mn = __ushort_as_half(0), mx = __ushort_as_half(0), st = __ushort_as_half(0);
-    if (r / ng < nt) {
-      mn = gb[(2 * tensor) * kPer + r];
-      mx = gb[(2 * tensor + 1) * kPer + r];
-      st = q4_step(mn, mx);
-    }
-    s_mn[e] = mn;
-    s_mx[e] = mx;
-    s_st[e] = st;
-  }
-  __syncwarp();
+  const int64_t t0 = static_cast<int64_t>(page) * kPage;
+  __half* gb = reinterpret_cast<__half*>(dst_ptr + 2 * C::kCodeBytes);
 #pragma unroll
-  for (int tensor = 0; tensor < 2; ++tensor) {
-    uint8_t* tile = tensor == 0 ? ktile : vtile;
-    const uint8_t* codes = stage + tensor * C::kCodeBytes;
-#pragma unroll 4
-    for (int i = lane; i < kPage * (D / 8); i += 32) {
-      const int t = i / (D / 8), c8 = i % (D / 8);
-      uint32_t w[4] = {0u, 0u, 0u, 0u};
-      if (t < nt) {
-        const uint32_t c4 = *reinterpret_cast<const uint32_t*>(codes + t * (D / 2) + 4 * c8);
-        const int e = tensor * kPer + t * ng + c8 / 8;
-        q4_dequant8(c4, __half2half2(s_mn[e]), __half2half2(s_st[e]), __half2half2(s_mx[e]), w);
-      }
-      const int row = (c8 >> 3) * 16 + t;
-      const int chunk = (c8 & 7) ^ (row & 7);
-      *reinterpret_cast<uint4*>(tile + row * 128 + chunk * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+  for (int i = 0; i < 4; ++i) {
+    const Q4View& v = i < 2 ? a.k4 : a.v4;
+    const __half* src = ((i & 1) ? v.gmax : v.gmin) + b * v.gsb + kvh * v.gsh + t0 * ng;
+    for (int e = 0; e < kPage * ng; ++e)
+      gb[i * kPage * ng + e] = e < nt * ng ? src[e] : __ushort_as_half(0);
+  }
+  const uint32_t cb = static_cast<uint32_t>(nt * (D / 2));
+  mbar_arrive_expect_tx(bar, 2 * cb);  // also releases the plain stores above
+  bulk_load(dst, a.k4.codes + b * a.k4.sb + kvh * a.k4.sh + t0 * (D / 2), cb, bar);
+  bulk_load(dst + C::kCodeBytes, a.v4.codes + b * a.v4.sb + kvh * a.v4.sh + t0 * (D / 2), cb,
+            bar);
+}
+
+// 4-bit path, consumer warp.  The codes go straight from the stage into MMA
+// fragments in registers; no dequantised tile is written.  Channel orders are
+// chosen so that every lane's codes are contiguous:
+//   * S = Q K^T: lane (g, t4) holds tokens g and g + 8 of channels
+//     [D/4 t4, D/4 (t4 + 1)).  Code word j of that block (channels
+//     D/4 t4 + 8 j + n, nibble n) feeds k-steps 2 j (nibble pairs (0, 4) and
+//     (1, 5)) and 2 j + 1 ((2, 6) and (3, 7)); the query's A fragments take the
+//     same channel order.
+//   * O += P V: lane (g, t4) holds tokens 2 t4, 2 t4 + 1, 2 t4 + 8, 2 t4 + 9 of
+//     channels [D/8 g, D/8 (g + 1)); output tile cn, column n is channel
+//     D/8 n + cn.
+// A nibble masked into the mantissa of 1024 (bits 0-3) or 64 (bits 4-7) gives
+// bias + code exactly; subtracting the bias leaves the code, then
+// x = fp16(code * step + mn) by one fp16 FMA, replaced by mx where it exceeds
+// mx -- the dequantisation of the 4-bit format, bit for bit.
+template <int D>
+struct Q4Page {
+  uint32_t kc[2][D / 32];  // K codes, tokens g and g + 8
+  uint32_t vc[4][D / 64];  // V codes, tokens 2 t4, 2 t4 + 1, 2 t4 + 8, 2 t4 + 9
+  __half kmn[2], kmx[2];   // K group bounds, tokens g and g + 8
+  uint32_t vmn[2], vmx[2]; // V group bounds, half pairs for tokens (2 t4, 2 t4 + 1) and + 8
+};
+
+template <typename C, int D>
+__device__ __forceinline__ void q4_load(const uint8_t* st, int g, int t4, Q4Page<D>& r) {
+  constexpr int ng = D / 64;
+  const __half* gb = reinterpret_cast<const __half*>(st + 2 * C::kCodeBytes);
+  const int gk = (D / 4) * t4 / 64;  // group of the lane's K channels
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int t = g + 8 * h;
+    const uint8_t* src = st + t * (D / 2) + (D / 8) * t4;
+    if constexpr (D == 128) {
+      const uint4 w = *reinterpret_cast<const uint4*>(src);
+      r.kc[h][0] = w.x;
+      r.kc[h][1] = w.y;
+      r.kc[h][2] = w.z;
+      r.kc[h][3] = w.w;
+    } else {
+      const uint2 w = *reinterpret_cast<const uint2*>(src);
+      r.kc[h][0] = w.x;
+      r.kc[h][1] = w.y;
+    }
+    r.kmn[h] = gb[t * ng + gk];
+    r.kmx[h] = gb[kPage * ng + t * ng + gk];
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = 2 * t4 + (i & 1) + 8 * (i >> 1);
+    const uint8_t* src = st + C::kCodeBytes + t * (D / 2) + (D / 16) * g;
+    if constexpr (D == 128) {
+      const uint2 w = *reinterpret_cast<const uint2*>(src);
+      r.vc[i][0] = w.x;
+      r.vc[i][1] = w.y;
+    } else {
+      r.vc[i][0] = *reinterpret_cast<const uint32_t*>(src);
     }
   }
-  __syncwarp();
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int t = 2 * t4 + 8 * h;  // the pair (t, t + 1)
+    const __half* vmn = gb + 2 * kPage * ng + t * ng;
+    const __half* vmx = gb + 3 * kPage * ng + t * ng;
+    if constexpr (D == 128) {
+      const int gv = (D / 8) * g / 64;  // group of the lane's V channels
+      const uint2 lo = *reinterpret_cast<const uint2*>(vmn);
+      const uint2 hi = *reinterpret_cast<const uint2*>(vmx);
+      r.vmn[h] = __byte_perm(lo.x, lo.y, gv ? 0x7632 : 0x5410);
+      r.vmx[h] = __byte_perm(hi.x, hi.y, gv ? 0x7632 : 0x5410);
+    } else {
+      r.vmn[h] = *reinterpret_cast<const uint32_t*>(vmn);
+      r.vmx[h] = *reinterpret_cast<const uint32_t*>(vmx);
+    }
+  }
+}
+
+// (bits & mask) | bias, minus the bias: the masked nibbles as exact fp16 codes.
+__device__ __forceinline__ __half2 q4_codes(uint32_t w, uint32_t mask, uint32_t bias) {
+  const uint32_t x = (w & mask) | bias;
+  return __hsub2(*reinterpret_cast<const __half2*>(&x), *reinterpret_cast<const __half2*>(&bias));
+}
+
+__device__ __forceinline__ uint32_t q4_value(__half2 code, __half2 step, __half2 mn, __half2 mx) {
+  const __half2 x = __hfma2(code, step, mn);
+  const uint32_t over = __hgt2_mask(x, mx);
+  return (over & *reinterpret_cast<const uint32_t*>(&mx)) |
+         (~over & *reinterpret_cast<const uint32_t*>(&x));
+}
+
+constexpr uint32_t kNib0 = 0x000f000fu, kNib1 = 0x00f000f0u;
+constexpr uint32_t kBias1024 = 0x64006400u, kBias64 = 0x54005400u;
+
+// Query A fragments in the 4-bit path's channel order (see Q4Page).
+template <int D>
+__device__ __forceinline__ void q4_query(const uint16_t* qrow, bool head_ok, int t4,
+                                         uint32_t (&qa)[D / 16][2]) {
+#pragma unroll
+  for (int j = 0; j < D / 32; ++j) {
+    uint32_t w[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      w[u] = head_ok ? *reinterpret_cast<const uint32_t*>(qrow + (D / 4) * t4 + 8 * j + 2 * u)
+                     : 0u;
+    qa[2 * j][0] = __byte_perm(w[0], w[2], 0x5410);      // channels 0, 4
+    qa[2 * j][1] = __byte_perm(w[0], w[2], 0x7632);      // 1, 5
+    qa[2 * j + 1][0] = __byte_perm(w[1], w[3], 0x5410);  // 2, 6
+    qa[2 * j + 1][1] = __byte_perm(w[1], w[3], 0x7632);  // 3, 7
+  }
+}
+
+// S = Q K^T for a 4-bit page (sc[h]: tokens 8 h + 2 t4 + e, as the 16-bit path).
+template <int D>
+__device__ __forceinline__ void q4_scores(const Q4Page<D>& r, const uint32_t (&qa)[D / 16][2],
+                                          float (&sc)[2][4]) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const __half step = q4_step(r.kmn[h], r.kmx[h]);
+    const __half2 st2 = __half2half2(step), mn2 = __half2half2(r.kmn[h]),
+                  mx2 = __half2half2(r.kmx[h]);
+#pragma unroll
+    for (int j = 0; j < D / 32; ++j) {
+      const uint32_t w = r.kc[h][j], w8 = w >> 8;
+      const uint32_t b0 = q4_value(q4_codes(w, kNib0, kBias1024), st2, mn2, mx2);
+      const uint32_t b1 = q4_value(q4_codes(w, kNib1, kBias64), st2, mn2, mx2);
+      const uint32_t b2 = q4_value(q4_codes(w8, kNib0, kBias1024), st2, mn2, mx2);
+      const uint32_t b3 = q4_value(q4_codes(w8, kNib1, kBias64), st2, mn2, mx2);
+      mma16816<true>(sc[h], qa[2 * j][0], 0u, qa[2 * j][1], 0u, b0, b1);
+      mma16816<true>(sc[h], qa[2 * j + 1][0], 0u, qa[2 * j + 1][1], 0u, b2, b3);
+    }
+  }
+}
+
+// O += P V for a 4-bit page (a0-a3: the P fragments).
+template <int D>
+__device__ __forceinline__ void q4_pv(const Q4Page<D>& r, uint32_t a0, uint32_t a1, uint32_t a2,
+                                      uint32_t a3, float (&acc)[D / 8][4]) {
+  __half2 st2[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const __half2 mn = *reinterpret_cast<const __half2*>(&r.vmn[h]);
+    const __half2 mx = *reinterpret_cast<const __half2*>(&r.vmx[h]);
+    st2[h] = __halves2half2(q4_step(__low2half(mn), __low2half(mx)),
+                            q4_step(__high2half(mn), __high2half(mx)));
+  }
+#pragma unroll
+  for (int j = 0; j < D / 64; ++j) {
+    uint32_t bv[2][8];  // [token pair][nibble]: B fragments of tiles 8 j + nibble
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const __half2 mn = *reinterpret_cast<const __half2*>(&r.vmn[h]);
+      const __half2 mx = *reinterpret_cast<const __half2*>(&r.vmx[h]);
+      const uint32_t wa = r.vc[2 * h][j], wb = r.vc[2 * h + 1][j];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        // Nibbles 4 hh .. 4 hh + 3 of both tokens, token 2 t4 (+ 8 h) in the low half.
+        const uint32_t u = __byte_perm(wa, wb, hh ? 0x7632 : 0x5410), u8 = u >> 8;
+        bv[h][4 * hh + 0] = q4_value(q4_codes(u, kNib0, kBias1024), st2[h], mn, mx);
+        bv[h][4 * hh + 1] = q4_value(q4_codes(u, kNib1, kBias64), st2[h], mn, mx);
+        bv[h][4 * hh + 2] = q4_value(q4_codes(u8, kNib0, kBias1024), st2[h], mn, mx);
+        bv[h][4 * hh + 3] = q4_value(q4_codes(u8, kNib1, kBias64), st2[h], mn, mx);
+      }
+    }
+#pragma unroll
+    for (int n = 0; n < 8; ++n) mma16816<true>(acc[8 * j + n], a0, a1, a2, a3, bv[0][n], bv[1][n]);
+  }
 }
 
 __device__ __forceinline__ void store_out(void* out, int out_dtype, int64_t off, float v) {
@@ -251,16 +373,23 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    // Lane 0 fetches items and publishes their descriptors; lanes 0-7 issue
-    // the copies, one page each per round.  Page j of an item goes to consumer
-    // warp j % 4, so lane l always feeds warp l % 4 (lanes l and l + 4 fill
-    // consecutive slots of that warp's sub-ring).  One issuing thread would cap
-    // a CTA at a few copies per microsecond, far below HBM bandwidth for pages
-    // of 2-8 KiB; eight lanes issue in parallel.
+    // Lane 0 fetches items and publishes their descriptors; the other lanes
+    // help issue the copies.  Page j of an item goes to consumer warp j % 4.
+    // 16-bit pages: lanes 0-7 issue one page (two tensor copies) each per
+    // round, so lane l always feeds warp l % 4 (lanes l and l + 4 fill
+    // consecutive slots of that warp's sub-ring).  4-bit pages: lanes
+    // 6 w .. 6 w + 5 move the page of warp w, one bulk copy each, four pages per
+    // round; lane 6 w waits for the free slot and arms its barrier first.  One
+    // issuing thread would cap a CTA at a few copies per microsecond, far below
+    // HBM bandwidth for pages of 1-8 KiB.
     static_assert(kConsumerWarps == 4, "four consumer sub-rings");
     constexpr int kIssueLanes = 8;
+    constexpr int kQ4Parts = 6, kQ4IssueLanes = kQ4Parts * kConsumerWarps;
     const uint64_t pol = l2_evict_first_policy();
-    const int my_w = lane & 3;      // consumer warp this lane feeds
+    // consumer warp this lane feeds
+    const int my_w = Q4 ? (lane < kQ4IssueLanes ? lane / kQ4Parts : 0) : (lane & 3);
+    const int part = lane % kQ4Parts;  // 4-bit: which of the page's copies
+    const bool drainer = Q4 ? (lane < kQ4IssueLanes && part == 0) : (lane < kConsumerWarps);
     int wc = 0;                     // pages issued so far to warp my_w
     int seq = 0;
     bool failed = false;            // a lane gave up waiting for a free slot
@@ -311,30 +440,65 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
       }
       if (item < 0) break;
       bool lok = true;
-      for (int j0 = 0; j0 < n; j0 += kIssueLanes) {
-        const int j = j0 + lane;
-        if (lane < kIssueLanes && j < n) {
+      if constexpr (Q4) {
+        for (int j0 = 0; j0 < n; j0 += kConsumerWarps) {
+          const int j = j0 + my_w;
+          const bool mine = lane < kQ4IssueLanes && j < n;
           const int c = wc + (j >> 2);
           const int s = my_w * C::kSub + c % C::kSub;  // warp my_w's sub-ring, in order
-          if (c >= C::kSub &&
-              !mbar_wait_bounded(empty0 + 8 * s, ((c / C::kSub) - 1) & 1, a.wait_limit_ns,
-                                 abort_flag)) {
-            lok = false;
-          } else {
-            const int page = SPARSE ? list[j].x : first + j;
-            stage_meta[s] = make_int2(page, SPARSE ? list[j].y : 0xff);
-            const uint32_t dst = sbase + s * C::kStageBytes;
-            if constexpr (Q4) {
-              issue_q4_page<C>(a, b, kvh, page, dst, smem + s * C::kStageBytes, full0 + 8 * s);
+          const int page = mine ? (SPARSE ? list[j].x : first + j) : 0;
+          const int nt = min(kPage, a.N - page * kPage);
+          const uint32_t dst = sbase + s * C::kStageBytes;
+          int ok = 1;
+          if (mine && part == 0) {
+            if (c >= C::kSub &&
+                !mbar_wait_bounded(empty0 + 8 * s, ((c / C::kSub) - 1) & 1, a.wait_limit_ns,
+                                   abort_flag)) {
+              ok = 0;
             } else {
+              stage_meta[s] = make_int2(page, SPARSE ? list[j].y : 0xff);
+              if (nt == kPage) {
+                mbar_arrive_expect_tx(full0 + 8 * s, C::kQ4StageBytes);
+                q4_copy<C, D>(a, b, kvh, page, 0, dst, full0 + 8 * s);
+              } else {
+                q4_ragged<C, D>(a, b, kvh, page, nt, dst, smem + s * C::kStageBytes,
+                                full0 + 8 * s);
+              }
+            }
+          }
+          // The slot is free (and its barrier armed) before the page's other
+          // lanes copy into it.
+          ok = __shfl_sync(0xffffffffu, ok, lane < kQ4IssueLanes ? my_w * kQ4Parts : lane);
+          __syncwarp();
+          if (mine && part > 0 && ok && nt == kPage)
+            q4_copy<C, D>(a, b, kvh, page, part, dst, full0 + 8 * s);
+          if (!__all_sync(0xffffffffu, !mine || ok)) {
+            lok = false;
+            break;
+          }
+        }
+      } else {
+        for (int j0 = 0; j0 < n; j0 += kIssueLanes) {
+          const int j = j0 + lane;
+          if (lane < kIssueLanes && j < n) {
+            const int c = wc + (j >> 2);
+            const int s = my_w * C::kSub + c % C::kSub;  // warp my_w's sub-ring, in order
+            if (c >= C::kSub &&
+                !mbar_wait_bounded(empty0 + 8 * s, ((c / C::kSub) - 1) & 1, a.wait_limit_ns,
+                                   abort_flag)) {
+              lok = false;
+            } else {
+              const int page = SPARSE ? list[j].x : first + j;
+              stage_meta[s] = make_int2(page, SPARSE ? list[j].y : 0xff);
+              const uint32_t dst = sbase + s * C::kStageBytes;
               mbar_arrive_expect_tx(full0 + 8 * s, C::kStageBytes);
               tma_load_5d_hint(dst, &mk, full0 + 8 * s, 0, page * kPage, 0, kvh, b, pol);
               tma_load_5d_hint(dst + C::kPageBytes, &mv, full0 + 8 * s, 0, page * kPage, 0,
                                kvh, b, pol);
             }
           }
+          if (!__all_sync(0xffffffffu, lok)) break;
         }
-        if (!__all_sync(0xffffffffu, lok)) break;
       }
       wc += n > my_w ? (n - my_w + 3) >> 2 : 0;
       seq += n;
@@ -348,7 +512,7 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
       *abort_flag = 1;
     }
     __syncwarp();
-    if (lane < kConsumerWarps && *abort_flag) {
+    if (drainer && *abort_flag) {
       // Let every copy this CTA issued land before it exits.  A sub-ring holds
       // at most kSub copies in flight, so lane w waits for the last kSub slots
       // of warp w's sub-ring (slots never issued just run into the deadline).
@@ -377,6 +541,10 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
   // -------------------------------------------------------------- consumers
   const int g = lane >> 2, t4 = lane & 3;
   const bool head_ok = g < a.G;
+  // Channel of output tile cn, column 2 t4 + e (the 4-bit path permutes them).
+  auto out_channel = [](int cn, int t4_, int e) {
+    return Q4 ? (D / 8) * (2 * t4_ + e) + cn : 8 * cn + 2 * t4_ + e;
+  };
   const int mtx = lane >> 3, mrow = lane & 7;
   int mycnt = 0;  // pages this warp has taken from its sub-ring
   // Exits are taken by all four consumer warps together (consumers_any), so no
@@ -402,11 +570,15 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
     {
       const uint16_t* qrow = static_cast<const uint16_t*>(a.q) + b * a.q_sb +
                              static_cast<int64_t>(kvh * a.G + (head_ok ? g : 0)) * a.q_sh;
+      if constexpr (Q4) {
+        q4_query<D>(qrow, head_ok, t4, qa);
+      } else {
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        qa[ks][0] = head_ok ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * t4) : 0u;
-        qa[ks][1] =
-            head_ok ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * t4 + 8) : 0u;
+        for (int ks = 0; ks < D / 16; ++ks) {
+          qa[ks][0] = head_ok ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * t4) : 0u;
+          qa[ks][1] =
+              head_ok ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * t4 + 8) : 0u;
+        }
       }
     }
     float m_run = -INFINITY, l_run = 0.f;
@@ -431,27 +603,26 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
       const int2 meta = stage_meta[s];
       const int page = meta.x;
       const uint32_t hmask = static_cast<uint32_t>(meta.y);
-      uint32_t kb = sbase + s * C::kStageBytes, vb = kb + C::kPageBytes;
-      if constexpr (Q4) {
-        // Dequantise the page into this warp's tiles, then free the stage.
-        kb = sbase + C::kTileOffset + warp * 2 * C::kPageBytes;
-        vb = kb + C::kPageBytes;
-        dequant_q4_page<C, D>(smem + s * C::kStageBytes, smem + (kb - sbase),
-                              smem + (vb - sbase),
-                              reinterpret_cast<__half*>(smem + C::kStepOffset) +
-                                  warp * 3 * C::kStepsPerWarp,
-                              min(kPage, a.N - page * kPage), lane);
-        if (lane == 0) mbar_arrive(empty0 + 8 * s);
-      }
+      const uint32_t kb = sbase + s * C::kStageBytes, vb = kb + C::kPageBytes;
 
       // S = Q K^T for the page: sc[nt][e] = score of head g, token 8 nt + 2 t4 + e.
       float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      Q4Page<D> q4;  // 4-bit: the lane's codes and bounds of the page
+      if constexpr (Q4) {
+        // Everything the warp needs from the stage goes to registers; then the
+        // stage is free.
+        q4_load<C, D>(smem + s * C::kStageBytes, g, t4, q4);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * s);
+        q4_scores<D>(q4, qa, sc);
+      } else {
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        uint32_t r0, r1, r2, r3;
-        ldsm_x4(tile_addr(kb, 8 * (mtx >> 1) + mrow, 16 * ks + 8 * (mtx & 1)), r0, r1, r2, r3);
-        mma16816<F16>(sc[0], qa[ks][0], 0u, qa[ks][1], 0u, r0, r1);
-        mma16816<F16>(sc[1], qa[ks][0], 0u, qa[ks][1], 0u, r2, r3);
+        for (int ks = 0; ks < D / 16; ++ks) {
+          uint32_t r0, r1, r2, r3;
+          ldsm_x4(tile_addr(kb, 8 * (mtx >> 1) + mrow, 16 * ks + 8 * (mtx & 1)), r0, r1, r2, r3);
+          mma16816<F16>(sc[0], qa[ks][0], 0u, qa[ks][1], 0u, r0, r1);
+          mma16816<F16>(sc[1], qa[ks][0], 0u, qa[ks][1], 0u, r2, r3);
+        }
       }
 
       // Online softmax (log2 domain) for head g over its 4 tokens of this page.
@@ -492,16 +663,20 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
       uint32_t a0, a1, a2, a3;
       split_pair<F16>(p[0], p[1], a0, a1);
       split_pair<F16>(p[2], p[3], a2, a3);
+      if constexpr (Q4) {
+        q4_pv<D>(q4, a0, a1, a2, a3, acc);
+      } else {
 #pragma unroll
-      for (int jn = 0; jn < D / 16; ++jn) {
-        uint32_t r0, r1, r2, r3;
-        ldsm_x4_trans(tile_addr(vb, 8 * (mtx & 1) + mrow, 8 * (2 * jn + (mtx >> 1))), r0, r1,
-                      r2, r3);
-        mma16816<F16>(acc[2 * jn], a0, a1, a2, a3, r0, r1);
-        mma16816<F16>(acc[2 * jn + 1], a0, a1, a2, a3, r2, r3);
+        for (int jn = 0; jn < D / 16; ++jn) {
+          uint32_t r0, r1, r2, r3;
+          ldsm_x4_trans(tile_addr(vb, 8 * (mtx & 1) + mrow, 8 * (2 * jn + (mtx >> 1))), r0, r1,
+                        r2, r3);
+          mma16816<F16>(acc[2 * jn], a0, a1, a2, a3, r0, r1);
+          mma16816<F16>(acc[2 * jn + 1], a0, a1, a2, a3, r2, r3);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * s);
       }
-      __syncwarp();
-      if (!Q4 && lane == 0) mbar_arrive(empty0 + 8 * s);
     }
 
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
@@ -518,8 +693,8 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
       }
 #pragma unroll
       for (int cn = 0; cn < D / 8; ++cn) {
-        r[8 * cn + 2 * t4] = acc[cn][0] + acc[cn][2];
-        r[8 * cn + 2 * t4 + 1] = acc[cn][1] + acc[cn][3];
+        r[out_channel(cn, t4, 0)] = acc[cn][0] + acc[cn][2];
+        r[out_channel(cn, t4, 1)] = acc[cn][1] + acc[cn][3];
       }
     }
     consumers_sync();
@@ -543,7 +718,7 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
       for (int cn = 0; cn < D / 8; ++cn) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int c = 8 * cn + 2 * t4 + e;
+          const int c = out_channel(cn, t4, e);
           float O = f[0] * (acc[cn][e] + acc[cn][2 + e]);
 #pragma unroll
           for (int w = 1; w < kConsumerWarps; ++w)
