@@ -30,8 +30,8 @@
 //     weights keep ~16 significant bits.  At the end of an item warps 1-3 hand
 //     their (max, sum, o) to warp 0 through shared memory, which merges them
 //     with its own and writes the item's partial.
-// merge_kernel then combines the chunks of every (b, h) in a fixed order and
-// writes out.  Its structure, like the chunking, depends only on (P, d), and
+// merge_small_kernel (units of up to 32 chunks) or merge_kernel then combines
+// the chunks of every (b, h) in a fixed order and writes out.  Its structure, like the chunking, depends only on (P, d), and
 // partials do not depend on which CTA computed them, so results are
 // deterministic and one kv head at a time gives bitwise the all-heads result.
 // The last CTA to stop fetching work resets the work counter.
@@ -801,6 +801,54 @@ __global__ void __launch_bounds__(1024) merge_kernel(const MergeArgs m) {
   }
 }
 
+// Units of at most kSmallMergeChunks chunks (the usual case): one thread per
+// (row, channel), 256 / D rows per CTA.  Every load a thread needs -- the
+// union count, all (m_k, l_k) and its channel of all o_k -- is issued at once,
+// so the merge costs one memory round trip; then, in chunk order,
+// M = max m_k, w_k = 2^(m_k - M) (0 for empty chunks), L = sum w_k l_k,
+// out = (sum w_k o_k) / L.  Deterministic like merge_kernel.
+constexpr int kSmallMergeChunks = 32;
+constexpr int kSmallMergeThreads = 256;
+
+template <int D>
+__global__ void __launch_bounds__(kSmallMergeThreads) merge_small_kernel(const MergeArgs m,
+                                                                         int rows) {
+  griddep_launch_dependents();
+  griddep_wait();  // the attention grid has finished writing its partials
+  const int row = blockIdx.x * (kSmallMergeThreads / D) + threadIdx.x / D;
+  const int c = threadIdx.x % D;
+  if (row >= rows) return;
+  const int stride = m.n_chunks;
+  const int b = row / m.Hq, h = row % m.Hq;
+  const int count = m.union_count != nullptr ? __ldcg(m.union_count + b * m.Hkv + h / m.G) : 0;
+  const float2* ml = reinterpret_cast<const float2*>(m.part_ml) + static_cast<int64_t>(row) * stride;
+  const float* po = m.part_o + static_cast<int64_t>(row) * stride * D + c;
+  float2 mlv[kSmallMergeChunks];
+  float x[kSmallMergeChunks];
+#pragma unroll
+  for (int k = 0; k < kSmallMergeChunks; ++k) {
+    mlv[k] = k < stride ? __ldcg(ml + k) : make_float2(-INFINITY, 0.f);
+    x[k] = k < stride ? __ldcg(po + static_cast<int64_t>(k) * D) : 0.f;
+  }
+  const int nc = m.union_count != nullptr
+                     ? min(stride, static_cast<int>(ceil_div(count, m.pages_per_chunk)))
+                     : stride;
+  float M = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < kSmallMergeChunks; ++k)
+    if (k < nc) M = fmaxf(M, mlv[k].x);
+  float L = 0.f, O = 0.f;
+#pragma unroll
+  for (int k = 0; k < kSmallMergeChunks; ++k) {
+    if (k < nc) {
+      const float w = (mlv[k].x == -INFINITY) ? 0.f : exp2f(mlv[k].x - M);
+      L += w * mlv[k].y;
+      O += (w != 0.f) ? w * x[k] : 0.f;  // empty chunks hold no o values
+    }
+  }
+  store_out(m.out, m.out_dtype, b * m.o_sb + h * m.o_sh + c, O / L);
+}
+
 // Resident CTAs per SM of one attention instantiation (its registers and shared
 // memory as compiled), at most kAttnCtasPerSm; computed once.
 template <int D, bool F16, bool SPARSE, bool Q4>
@@ -883,6 +931,13 @@ cudaError_t attn_ctas_per_sm(int d, bool f16, bool sparse, bool q4, int* out) {
 }
 
 cudaError_t launch_merge(int d, const MergeArgs& m, int rows, cudaStream_t s) {
+  if (m.n_chunks <= kSmallMergeChunks) {
+    const dim3 grid(static_cast<unsigned>(ceil_div(rows, kSmallMergeThreads / d)));
+    return d == 128 ? launch_pdl(merge_small_kernel<128>, grid, dim3(kSmallMergeThreads), 0, s, m,
+                                 rows)
+                    : launch_pdl(merge_small_kernel<64>, grid, dim3(kSmallMergeThreads), 0, s, m,
+                                 rows);
+  }
   const int slices = static_cast<int>(ceil_div(m.n_chunks, 32));
   const dim3 grid(rows), block(d * slices);
   return d == 128 ? launch_pdl(merge_kernel<128>, grid, block, 0, s, m)

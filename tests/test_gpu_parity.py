@@ -56,6 +56,9 @@ CASES = [
     # several items back to back, exact and sparse
     Workload("multi-item-gqa", B=16, Hq=16, Hkv=8, d=128, N=8192, top_k=48, kind="hot"),
     Workload("multi-item-mha", B=16, Hq=32, Hkv=32, d=64, N=4100, top_k=64, kind="offset"),
+    # a union of 2400 pages (75 chunks per unit) chosen by the separate
+    # selection kernels
+    Workload("select-merge-kernel", B=1, Hq=4, Hkv=1, d=128, N=40000, top_k=600, kind="hot"),
 ]
 
 
