@@ -38,23 +38,17 @@ __device__ __forceinline__ int minus_borrow(uint32_t a, uint32_t b) {
   return static_cast<int>(d);
 }
 
-// Keys >= x among the warp's k[0 .. 8 ceil(used / 8)) (unused slots must hold
-// 0 and x >= 1).  Eight partial sums keep the compares from forming one
-// dependent chain.
+// Keys >= x among the warp's keys k (slots past the head's P hold 0, and
+// x >= 1, so they never count).  Every slot is counted: a per-group bound
+// check costs more than the compares it saves.  Eight partial sums keep the
+// compares from forming one dependent chain.
 template <int NK>
-__device__ __forceinline__ int warp_count_ge(const uint32_t (&k)[NK], int used, uint32_t x) {
+__device__ __forceinline__ int warp_count_ge(const uint32_t (&k)[NK], uint32_t x) {
   int c[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  int slots = 0;
 #pragma unroll
-  for (int g = 0; g < (NK + 7) / 8; ++g) {
-    if (8 * g < used) {
-#pragma unroll
-      for (int u = 0; u < 8 && 8 * g + u < NK; ++u) c[u] += minus_borrow(k[8 * g + u], x);
-      slots += (8 * g + 8 <= NK) ? 8 : NK - 8 * g;
-    }
-  }
+  for (int i = 0; i < NK; ++i) c[i & 7] += minus_borrow(k[i], x);
   const int below = -(((c[0] + c[1]) + (c[2] + c[3])) + ((c[4] + c[5]) + (c[6] + c[7])));
-  return 32 * slots - __reduce_add_sync(0xffffffffu, below);
+  return 32 * NK - __reduce_add_sync(0xffffffffu, below);
 }
 
 // The largest T such that at least lo of the warp's keys are >= T, found bit by
@@ -62,13 +56,13 @@ __device__ __forceinline__ int warp_count_ge(const uint32_t (&k)[NK], int used, 
 // agrees with it above bit `top`); stops early (with a smaller T) once the
 // count of keys >= T lies in [lo, hi].  ge = keys >= T.  lo >= 1.
 template <int NK>
-__device__ uint32_t warp_threshold(const uint32_t (&k)[NK], int used, int lo, int hi, int& ge,
+__device__ uint32_t warp_threshold(const uint32_t (&k)[NK], int lo, int hi, int& ge,
                                    uint32_t T0 = 0u, int top = 31) {
   uint32_t T = T0;
   ge = -1;  // not counted: every key at hand is >= T0
   for (int bit = top; bit >= 0; --bit) {
     const uint32_t cand = T | (1u << bit);
-    const int c = warp_count_ge(k, used, cand);
+    const int c = warp_count_ge(k, cand);
     if (c >= lo) {
       T = cand;
       ge = c;
@@ -110,7 +104,7 @@ __device__ void warp_topk_head(const KeyAt& key_at, int P, int kk, uint32_t* bm)
   } else {
     const int top = 31 - __clz(kmax ^ kmin);
     const uint32_t prefix = top == 31 ? 0u : (kmax >> (top + 1)) << (top + 1);
-    T = warp_threshold(key, nr, kk, kk, ge, prefix, top);
+    T = warp_threshold(key, kk, kk, ge, prefix, top);
   }
   if (ge == kk) {
     // No tie at T: the selection is every key >= T (eight ballots at a time).
@@ -132,7 +126,7 @@ __device__ void warp_topk_head(const KeyAt& key_at, int P, int kk, uint32_t* bm)
   }
   // Ties at T (or keys past P that compare as 0 with a zero prefix): T exactly,
   // then keys > T and the first kk - #(> T) keys equal to T in page order.
-  T = warp_threshold(key, nr, kk, kk, ge);
+  T = warp_threshold(key, kk, kk, ge);
   int gt = 0;
 #pragma unroll
   for (int i = 0; i < kSelKeys; ++i)
