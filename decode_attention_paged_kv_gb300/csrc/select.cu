@@ -334,8 +334,8 @@ __global__ void __launch_bounds__(kSelThreads) union_kernel(const UnionArgs a) {
 // 16-page tile of it on tensor cores: S[head][page] = q+ . M + q- . m, as in
 // the score kernel but with the pages' metadata read by ldmatrix.  The scores
 // stay in shared memory as order-preserving keys [G][P]; then warp h selects
-// head h (select_warp.cuh) and all eight warps build the union from the heads'
-// bitmaps.  Every wait is bounded.
+// head h (select_warp.cuh); warps 0-3 build the union from the heads' bitmaps
+// while warps 4-7 write the per-head rows.  Every wait is bounded.
 constexpr int kUnitConsumers = 8;
 constexpr int kUnitThreads = (kUnitConsumers + 1) * 32;
 constexpr int kUnitBoxPages = 64;
@@ -359,6 +359,12 @@ __device__ __forceinline__ uint32_t box_addr(uint32_t base, int t, int c) {
 
 __device__ __forceinline__ void unit_consumers_sync() {
   asm volatile("bar.sync 1, %0;" ::"r"(kUnitConsumers * 32) : "memory");
+}
+
+// The union is built by warps 0-3 (warps 4-7 write the per-head rows meanwhile).
+constexpr int kUnionWarps = 4;
+__device__ __forceinline__ void union_sync() {
+  asm volatile("bar.sync 2, %0;" ::"r"(kUnionWarps * 32) : "memory");
 }
 
 template <int D, bool F16>
@@ -499,15 +505,20 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
     uint32_t* bm = s_bm + h * kSelBitmapWords;
     const uint32_t* keys = s_keys + h * a.P;
     warp_topk_head([keys](int j) { return keys[j]; }, a.P, a.kk, bm);
-    __syncwarp();
-    const int64_t row = static_cast<int64_t>(b) * a.Hq + kvh * a.G + h;
-    warp_emit_row(bm, W, a.selected + row * a.kk, nullptr);
   }
   unit_consumers_sync();
+  if (warp >= kUnionWarps) {
+    // Warps 4-7 write each head's ascending row while warps 0-3 build the union.
+    for (int h = warp - kUnionWarps; h < a.G; h += kUnitConsumers - kUnionWarps) {
+      const int64_t row = static_cast<int64_t>(b) * a.Hq + kvh * a.G + h;
+      warp_emit_row(s_bm + h * kSelBitmapWords, W, a.selected + row * a.kk, nullptr);
+    }
+    return;
+  }
   // Union of the heads' bitmaps, ascending, with a bit per head: warp w ORs
   // words w * wpw .. (one per lane), the per-warp counts place them.
   {
-    const int wpw = static_cast<int>(ceil_div(W, kUnitConsumers));
+    const int wpw = static_cast<int>(ceil_div(W, kUnionWarps));
     const int wi = warp * wpw + lane;
     const bool own = lane < wpw && wi < W;
     uint32_t hw[8];
@@ -526,10 +537,10 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
     }
     int* wtot = reinterpret_cast<int*>(s_keys);  // (the keys are no longer needed)
     if (lane == 31) wtot[warp] = incl;
-    unit_consumers_sync();
+    union_sync();
     int before = 0, count = 0;
 #pragma unroll
-    for (int v = 0; v < kUnitConsumers; ++v) {
+    for (int v = 0; v < kUnionWarps; ++v) {
       before += v < warp ? wtot[v] : 0;
       count += wtot[v];
     }
