@@ -380,6 +380,7 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(usm + C::kBarOffset + 16 * C::kStages);
   uint32_t* s_keys = reinterpret_cast<uint32_t*>(usm + C::kKeysOffset);      // [G][P]
   uint32_t* s_bm = s_keys + static_cast<size_t>(a.G) * a.P;                  // [G][kSelBitmapWords]
+  uint32_t* s_kext = s_bm + static_cast<size_t>(a.G) * kSelBitmapWords;      // [2][8]: max, min key
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int unit = blockIdx.x;
   const int b = unit / a.Hkv, kvh = unit % a.Hkv;
@@ -392,6 +393,7 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
+  if (threadIdx.x < 16) s_kext[threadIdx.x] = threadIdx.x < 8 ? 0u : ~0u;
   if (warp == kUnitConsumers && lane == 0) {
     prefetch_tensormap(&mmx);
     prefetch_tensormap(&mmn);
@@ -458,6 +460,7 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
   }
   const int half = warp >> 2, tile = warp & 3;  // boxes of parity `half`, tile `tile` of each
   bool ok = true;
+  uint32_t kmx = 0u, kmn = ~0u;  // extremes of head g's keys this lane wrote
   for (int i = half; i < n_boxes; i += 2) {
     const int s = i % C::kStages;
     ok = mbar_wait_bounded(full0 + 8 * s, (i / C::kStages) & 1, a.wait_limit_ns, abort_flag);
@@ -484,9 +487,23 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int p = i * kUnitBoxPages + 16 * tile + 8 * (e >> 1) + 2 * t4 + (e & 1);
-        if (p < a.P) s_keys[g * a.P + p] = score_key(sc[e >> 1][e & 1]);
+        if (p < a.P) {
+          const uint32_t key = score_key(sc[e >> 1][e & 1]);
+          s_keys[g * a.P + p] = key;
+          kmx = max(kmx, key);
+          kmn = min(kmn, key);
+        }
       }
     }
+  }
+  // each head's largest and smallest key, for the selection's common prefix
+  kmx = max(kmx, __shfl_xor_sync(0xffffffffu, kmx, 1));
+  kmx = max(kmx, __shfl_xor_sync(0xffffffffu, kmx, 2));
+  kmn = min(kmn, __shfl_xor_sync(0xffffffffu, kmn, 1));
+  kmn = min(kmn, __shfl_xor_sync(0xffffffffu, kmn, 2));
+  if (head_ok && t4 == 0) {
+    atomicMax(s_kext + g, kmx);
+    atomicMin(s_kext + 8 + g, kmn);
   }
   // (a warp that timed out tells the others through the abort flag)
   if (!ok && lane == 0 && *abort_flag == 0) {
@@ -504,7 +521,7 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
   for (int h = warp; h < a.G; h += kUnitConsumers) {
     uint32_t* bm = s_bm + h * kSelBitmapWords;
     const uint32_t* keys = s_keys + h * a.P;
-    warp_topk_head([keys](int j) { return keys[j]; }, a.P, a.kk, bm);
+    warp_topk_head([keys](int j) { return keys[j]; }, a.P, a.kk, bm, s_kext[h], s_kext[8 + h]);
   }
   unit_consumers_sync();
   if (warp >= kUnionWarps) {
@@ -546,13 +563,24 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
     }
     int2* out = a.union_list + static_cast<int64_t>(unit) * a.union_stride;
     int at = before + incl - c;
-    while (u) {
-      const int bit = __ffs(u) - 1;
-      u &= u - 1;
-      uint32_t m = 0;
+    if (a.G <= 4) {
+      while (u) {
+        const int bit = __ffs(u) - 1;
+        u &= u - 1;
+        uint32_t m = 0;
 #pragma unroll
-      for (int h = 0; h < 8; ++h) m |= ((hw[h] >> bit) & 1u) << h;
-      out[at++] = make_int2(wi * 32 + bit, static_cast<int>(m));
+        for (int h = 0; h < 4; ++h) m |= ((hw[h] >> bit) & 1u) << h;
+        out[at++] = make_int2(wi * 32 + bit, static_cast<int>(m));
+      }
+    } else {
+      while (u) {
+        const int bit = __ffs(u) - 1;
+        u &= u - 1;
+        uint32_t m = 0;
+#pragma unroll
+        for (int h = 0; h < 8; ++h) m |= ((hw[h] >> bit) & 1u) << h;
+        out[at++] = make_int2(wi * 32 + bit, static_cast<int>(m));
+      }
     }
     if (threadIdx.x == 0) a.union_count[unit] = count;
   }
@@ -586,7 +614,7 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
 size_t unit_select_smem(int d, int G, int P) {
   const size_t keys_off = d == 128 ? UnitCfg<128>::kKeysOffset : UnitCfg<64>::kKeysOffset;
   return 1024 + keys_off + static_cast<size_t>(G) * P * 4 +
-         static_cast<size_t>(G) * kSelBitmapWords * 4;
+         static_cast<size_t>(G) * kSelBitmapWords * 4 + 16 * 4;
 }
 
 cudaError_t launch_unit_select(int d, bool f16, const UnitSelectArgs& a, const CUtensorMap& mmx,

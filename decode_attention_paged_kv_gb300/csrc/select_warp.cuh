@@ -74,9 +74,10 @@ __device__ uint32_t warp_threshold(const uint32_t (&k)[NK], int lo, int hi, int&
 
 // Top-kk of one head's P keys (key_at(j): the order-preserving key of page j;
 // 1 <= kk <= P <= kUnitMaxP) by one warp: writes the selection bitmap words
-// bm[0 .. ceil(P / 32)).
+// bm[0 .. ceil(P / 32)).  kmax / kmin: the largest and smallest of the keys.
 template <class KeyAt>
-__device__ void warp_topk_head(const KeyAt& key_at, int P, int kk, uint32_t* bm) {
+__device__ void warp_topk_head(const KeyAt& key_at, int P, int kk, uint32_t* bm, uint32_t kmax,
+                               uint32_t kmin) {
   const int lane = threadIdx.x & 31;
   const uint32_t lt = (1u << lane) - 1u;
   const int nr = static_cast<int>(ceil_div(P, 32));         // key rows
@@ -84,17 +85,6 @@ __device__ void warp_topk_head(const KeyAt& key_at, int P, int kk, uint32_t* bm)
   uint32_t key[kSelKeys];
 #pragma unroll
   for (int i = 0; i < kSelKeys; ++i) key[i] = i < nv ? key_at(32 * i + lane) : 0u;
-  // The keys' common leading bits (four independent max / min chains).
-  uint32_t mx[4] = {0u, 0u, 0u, 0u}, mn[4] = {~0u, ~0u, ~0u, ~0u};
-#pragma unroll
-  for (int i = 0; i < kSelKeys; ++i) {
-    if (i < nv) {
-      mx[i & 3] = max(mx[i & 3], key[i]);
-      mn[i & 3] = min(mn[i & 3], key[i]);
-    }
-  }
-  const uint32_t kmax = __reduce_max_sync(0xffffffffu, max(max(mx[0], mx[1]), max(mx[2], mx[3])));
-  const uint32_t kmin = __reduce_min_sync(0xffffffffu, min(min(mn[0], mn[1]), min(mn[2], mn[3])));
   // The kk-th largest key T, bit by bit below the common prefix (keys past P
   // read as 0 and stay below every candidate when the prefix is not 0).
   int ge = -1;
