@@ -56,20 +56,28 @@ struct ItemDesc {
   int pad;
 };
 
-template <int D, bool Q4>
+// QUAD: four pages a stage (the dense 4-bit path, whose pages are consecutive).
+template <int D, bool Q4, bool QUAD>
 struct AttnCfg {
   static constexpr int kPageBytes = kPage * D * 2;          // one 16-bit page tile
   static constexpr int kCodeBytes = kPage * D / 2;          // 4-bit: one tensor's page of codes
   static constexpr int kGroupBytes = kPage * (D / 64) * 2;  // 4-bit: one page of gmin (or gmax)
-  // 4-bit stage: K codes | V codes | K min | K max | V min | V max
-  static constexpr int kQ4StageBytes = 2 * kCodeBytes + 4 * kGroupBytes;
-  static constexpr int kStageBytes = Q4 ? (kQ4StageBytes + 127) / 128 * 128 : 2 * kPageBytes;
+  // A 4-bit stage holds one page, or four pages of one consumer warp in the
+  // dense path (consecutive pages of the cache move with one copy per part):
+  //   K codes [q][page] | V codes [q][page] | K min | K max | V min | V max,
+  // each bound array [q][page], q = kPagesPerStage.
+  static constexpr int kPagesPerStage = QUAD ? 4 : 1;
+  static constexpr int kQ4PageBytes = 2 * kCodeBytes + 4 * kGroupBytes;
+  static constexpr int kQ4VCodeOffset = kPagesPerStage * kCodeBytes;
+  static constexpr int kQ4BoundsOffset = 2 * kPagesPerStage * kCodeBytes;
+  static constexpr int kStageBytes =
+      Q4 ? (kPagesPerStage * kQ4PageBytes + 127) / 128 * 128 : 2 * kPageBytes;
   // 4-bit pages are a quarter the size: more of them in flight.
-  static constexpr int kStages = Q4 ? (D == 128 ? 32 : 48) : attn_stages(D);
+  static constexpr int kStages = Q4 ? (D == 128 ? 32 : 48) / kPagesPerStage : attn_stages(D);
   static constexpr int kSub = kStages / kConsumerWarps;             // stages per consumer warp
   static constexpr int kBarOffset = (kStages * kStageBytes + 15) / 16 * 16;
   static constexpr int kStageMetaOffset = kBarOffset + (2 * kStages + 4) * 8;
-  static constexpr int kDescOffset = kStageMetaOffset + kStages * 8;
+  static constexpr int kDescOffset = kStageMetaOffset + kStages * kPagesPerStage * 8;
   static constexpr int kMergeOffset = kDescOffset + 2 * 16;
   static constexpr int kMergeRow = D + 2;                           // o[D], max, sum
   static constexpr int kMergeBytes = (kConsumerWarps - 1) * 8 * kMergeRow * 4;
@@ -110,47 +118,57 @@ __device__ __forceinline__ bool consumers_any(bool flag) {
   return res != 0;
 }
 
-// 4-bit path, producer.  A whole page moves by six 1-D bulk copies, one per
-// issuing lane: part 0 K codes, 1 V codes, 2-5 K min, K max, V min, V max.
+// 4-bit path, producer.  A run of r consecutive whole pages of the cache,
+// going to stage slots slot0 .. slot0 + r - 1, moves by six 1-D bulk copies,
+// one per issuing lane: part 0 K codes, 1 V codes, 2-5 K min, K max, V min,
+// V max.
 template <typename C, int D>
-__device__ __forceinline__ void q4_copy(const AttnArgs& a, int b, int kvh, int page, int part,
-                                        uint32_t dst, uint32_t bar) {
+__device__ __forceinline__ void q4_copy_run(const AttnArgs& a, int b, int kvh, int page0, int r,
+                                            int slot0, int part, uint32_t dst, uint32_t bar) {
   constexpr int ng = D / 64;
-  const int64_t t0 = static_cast<int64_t>(page) * kPage;
+  const int64_t t0 = static_cast<int64_t>(page0) * kPage;
   if (part < 2) {
     const Q4View& v = part == 0 ? a.k4 : a.v4;
-    bulk_load(dst + part * C::kCodeBytes, v.codes + b * v.sb + kvh * v.sh + t0 * (D / 2),
-              C::kCodeBytes, bar);
+    bulk_load(dst + part * C::kQ4VCodeOffset + slot0 * C::kCodeBytes,
+              v.codes + b * v.sb + kvh * v.sh + t0 * (D / 2), r * C::kCodeBytes, bar);
   } else {
     const int i = part - 2;
     const Q4View& v = i < 2 ? a.k4 : a.v4;
     const __half* src = ((i & 1) ? v.gmax : v.gmin) + b * v.gsb + kvh * v.gsh + t0 * ng;
-    bulk_load(dst + 2 * C::kCodeBytes + i * C::kGroupBytes, src, C::kGroupBytes, bar);
+    bulk_load(dst + C::kQ4BoundsOffset + (i * C::kPagesPerStage + slot0) * C::kGroupBytes, src,
+              r * C::kGroupBytes, bar);
   }
 }
 
-// 4-bit path, producer: the ragged last page (nt < 16 tokens), by one lane.
-// Only the valid tokens' codes are copied and their group bounds loaded with
-// plain loads, so nothing is read past the cache; the bounds of the missing
-// tokens are zeroed, so whatever codes their rows hold dequantise to 0.
+// 4-bit path, producer: the ragged last page (nt < 16 tokens), by one lane,
+// into stage slot `slot`.  The valid tokens' group bounds are loaded with plain
+// loads (released by the caller's barrier arrival, which counts the codes'
+// 2 * nt * d/2 bytes) and the missing tokens' bounds zeroed, so whatever codes
+// their rows hold dequantise to 0; then only the valid tokens' codes are
+// copied, so nothing is read past the cache.
 template <typename C, int D>
-__device__ __forceinline__ void q4_ragged(const AttnArgs& a, int b, int kvh, int page, int nt,
-                                          uint32_t dst, uint8_t* dst_ptr, uint32_t bar) {
+__device__ __forceinline__ void q4_ragged_bounds(const AttnArgs& a, int b, int kvh, int page,
+                                                 int nt, int slot, uint8_t* stage) {
   constexpr int ng = D / 64;
   const int64_t t0 = static_cast<int64_t>(page) * kPage;
-  __half* gb = reinterpret_cast<__half*>(dst_ptr + 2 * C::kCodeBytes);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const Q4View& v = i < 2 ? a.k4 : a.v4;
     const __half* src = ((i & 1) ? v.gmax : v.gmin) + b * v.gsb + kvh * v.gsh + t0 * ng;
-    for (int e = 0; e < kPage * ng; ++e)
-      gb[i * kPage * ng + e] = e < nt * ng ? src[e] : __ushort_as_half(0);
+    __half* gb = reinterpret_cast<__half*>(stage + C::kQ4BoundsOffset +
+                                           (i * C::kPagesPerStage + slot) * C::kGroupBytes);
+    for (int e = 0; e < kPage * ng; ++e) gb[e] = e < nt * ng ? src[e] : __ushort_as_half(0);
   }
+}
+template <typename C, int D>
+__device__ __forceinline__ void q4_ragged_codes(const AttnArgs& a, int b, int kvh, int page,
+                                                int nt, int slot, uint32_t dst, uint32_t bar) {
+  const int64_t t0 = static_cast<int64_t>(page) * kPage;
   const uint32_t cb = static_cast<uint32_t>(nt * (D / 2));
-  mbar_arrive_expect_tx(bar, 2 * cb);  // also releases the plain stores above
-  bulk_load(dst, a.k4.codes + b * a.k4.sb + kvh * a.k4.sh + t0 * (D / 2), cb, bar);
-  bulk_load(dst + C::kCodeBytes, a.v4.codes + b * a.v4.sb + kvh * a.v4.sh + t0 * (D / 2), cb,
-            bar);
+  bulk_load(dst + slot * C::kCodeBytes, a.k4.codes + b * a.k4.sb + kvh * a.k4.sh + t0 * (D / 2),
+            cb, bar);
+  bulk_load(dst + C::kQ4VCodeOffset + slot * C::kCodeBytes,
+            a.v4.codes + b * a.v4.sb + kvh * a.v4.sh + t0 * (D / 2), cb, bar);
 }
 
 // 4-bit path, consumer warp.  The codes go straight from the stage into MMA
@@ -177,14 +195,16 @@ struct Q4Page {
 };
 
 template <typename C, int D>
-__device__ __forceinline__ void q4_load(const uint8_t* st, int g, int t4, Q4Page<D>& r) {
+__device__ __forceinline__ void q4_load(const uint8_t* st, int slot, int g, int t4, Q4Page<D>& r) {
   constexpr int ng = D / 64;
-  const __half* gb = reinterpret_cast<const __half*>(st + 2 * C::kCodeBytes);
+  constexpr int kBound = C::kPagesPerStage * kPage * ng;  // halves from one bound array to the next
+  const __half* gb =
+      reinterpret_cast<const __half*>(st + C::kQ4BoundsOffset + slot * C::kGroupBytes);
   const int gk = (D / 4) * t4 / 64;  // group of the lane's K channels
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int t = g + 8 * h;
-    const uint8_t* src = st + t * (D / 2) + (D / 8) * t4;
+    const uint8_t* src = st + slot * C::kCodeBytes + t * (D / 2) + (D / 8) * t4;
     if constexpr (D == 128) {
       const uint4 w = *reinterpret_cast<const uint4*>(src);
       r.kc[h][0] = w.x;
@@ -197,12 +217,12 @@ __device__ __forceinline__ void q4_load(const uint8_t* st, int g, int t4, Q4Page
       r.kc[h][1] = w.y;
     }
     r.kmn[h] = gb[t * ng + gk];
-    r.kmx[h] = gb[kPage * ng + t * ng + gk];
+    r.kmx[h] = gb[kBound + t * ng + gk];
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int t = 2 * t4 + (i & 1) + 8 * (i >> 1);
-    const uint8_t* src = st + C::kCodeBytes + t * (D / 2) + (D / 16) * g;
+    const uint8_t* src = st + C::kQ4VCodeOffset + slot * C::kCodeBytes + t * (D / 2) + (D / 16) * g;
     if constexpr (D == 128) {
       const uint2 w = *reinterpret_cast<const uint2*>(src);
       r.vc[i][0] = w.x;
@@ -214,8 +234,8 @@ __device__ __forceinline__ void q4_load(const uint8_t* st, int g, int t4, Q4Page
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int t = 2 * t4 + 8 * h;  // the pair (t, t + 1)
-    const __half* vmn = gb + 2 * kPage * ng + t * ng;
-    const __half* vmx = gb + 3 * kPage * ng + t * ng;
+    const __half* vmn = gb + 2 * kBound + t * ng;
+    const __half* vmx = gb + 3 * kBound + t * ng;
     if constexpr (D == 128) {
       const int gv = (D / 8) * g / 64;  // group of the lane's V channels
       const uint2 lo = *reinterpret_cast<const uint2*>(vmn);
@@ -334,7 +354,7 @@ template <int D, bool F16, bool SPARSE, bool Q4>
 __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
     attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mk,
                 const __grid_constant__ CUtensorMap mv) {
-  using C = AttnCfg<D, Q4>;
+  using C = AttnCfg<D, Q4, Q4 && !SPARSE>;
   static_assert(!Q4 || F16, "a 4-bit cache is dequantised to fp16");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -441,13 +461,19 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
       if (item < 0) break;
       bool lok = true;
       if constexpr (Q4) {
-        for (int j0 = 0; j0 < n; j0 += kConsumerWarps) {
-          const int j = j0 + my_w;
-          const bool mine = lane < kQ4IssueLanes && j < n;
-          const int c = wc + (j >> 2);
-          const int s = my_w * C::kSub + c % C::kSub;  // warp my_w's sub-ring, in order
-          const int page = mine ? (SPARSE ? list[j].x : first + j) : 0;
-          const int nt = min(kPage, a.N - page * kPage);
+        // Round: quads m0 .. m0 + 3 (quad m = pages 4 m .. 4 m + 3 of the
+        // item) go to warps 0-3; lanes 6 w .. 6 w + 5 fill warp w's.
+        constexpr int kQ = C::kPagesPerStage;
+        for (int j0 = 0; j0 < n; j0 += kConsumerWarps * kQ) {
+          const int m = j0 / kQ + my_w;  // this lane group's quad
+          const int cnt = lane < kQ4IssueLanes ? max(0, min(kQ, n - m * kQ)) : 0;
+          const bool mine = cnt > 0;
+          const int c = wc + (m >> 2);   // stages issued to warp my_w so far
+          const int s = my_w * C::kSub + c % C::kSub;
+          int pg[kQ];
+#pragma unroll
+          for (int t = 0; t < kQ; ++t)
+            pg[t] = t < cnt ? (SPARSE ? list[m * kQ + t].x : first + m * kQ + t) : 0;
           const uint32_t dst = sbase + s * C::kStageBytes;
           int ok = 1;
           if (mine && part == 0) {
@@ -456,22 +482,39 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
                                    abort_flag)) {
               ok = 0;
             } else {
-              stage_meta[s] = make_int2(page, SPARSE ? list[j].y : 0xff);
-              if (nt == kPage) {
-                mbar_arrive_expect_tx(full0 + 8 * s, C::kQ4StageBytes);
-                q4_copy<C, D>(a, b, kvh, page, 0, dst, full0 + 8 * s);
-              } else {
-                q4_ragged<C, D>(a, b, kvh, page, nt, dst, smem + s * C::kStageBytes,
-                                full0 + 8 * s);
+              uint32_t bytes = 0;
+              for (int t = 0; t < cnt; ++t) {
+                stage_meta[s * kQ + t] = make_int2(pg[t], SPARSE ? list[m * kQ + t].y : 0xff);
+                const int nt = min(kPage, a.N - pg[t] * kPage);
+                if (nt == kPage) {
+                  bytes += C::kQ4PageBytes;
+                } else {
+                  q4_ragged_bounds<C, D>(a, b, kvh, pg[t], nt, t, smem + s * C::kStageBytes);
+                  bytes += 2 * nt * (D / 2);
+                }
               }
+              mbar_arrive_expect_tx(full0 + 8 * s, bytes);  // (releases the plain stores)
             }
           }
-          // The slot is free (and its barrier armed) before the page's other
+          // The slot is free (and its barrier armed) before the quad's other
           // lanes copy into it.
           ok = __shfl_sync(0xffffffffu, ok, lane < kQ4IssueLanes ? my_w * kQ4Parts : lane);
           __syncwarp();
-          if (mine && part > 0 && ok && nt == kPage)
-            q4_copy<C, D>(a, b, kvh, page, part, dst, full0 + 8 * s);
+          if (mine && ok) {
+            // runs of consecutive whole pages: one copy per part each
+            for (int t = 0; t < cnt;) {
+              const int nt = min(kPage, a.N - pg[t] * kPage);
+              if (nt < kPage) {
+                if (part == 0) q4_ragged_codes<C, D>(a, b, kvh, pg[t], nt, t, dst, full0 + 8 * s);
+                ++t;
+                continue;
+              }
+              int r = 1;
+              while (t + r < cnt && pg[t + r] == pg[t] + r && (pg[t + r] + 1) * kPage <= a.N) ++r;
+              q4_copy_run<C, D>(a, b, kvh, pg[t], r, t, part, dst, full0 + 8 * s);
+              t += r;
+            }
+          }
           if (!__all_sync(0xffffffffu, !mine || ok)) {
             lok = false;
             break;
@@ -500,7 +543,12 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
           if (!__all_sync(0xffffffffu, lok)) break;
         }
       }
-      wc += n > my_w ? (n - my_w + 3) >> 2 : 0;
+      if constexpr (Q4) {
+        const int nq = static_cast<int>(ceil_div(n, C::kPagesPerStage));  // the item's quads
+        wc += nq > my_w ? (nq - my_w + 3) >> 2 : 0;
+      } else {
+        wc += n > my_w ? (n - my_w + 3) >> 2 : 0;
+      }
       seq += n;
       if (!__all_sync(0xffffffffu, lok)) {
         failed = true;
@@ -587,7 +635,9 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
     for (int cn = 0; cn < D / 8; ++cn) acc[cn][0] = acc[cn][1] = acc[cn][2] = acc[cn][3] = 0.f;
 
     bool aborted = false;
-    for (int j = warp; j < n_pages; j += kConsumerWarps) {
+    // Stage q of the item goes to warp q % 4; it holds pages kQ q .. of the item.
+    constexpr int kQ = C::kPagesPerStage;
+    for (int sq = warp; sq * kQ < n_pages; sq += kConsumerWarps) {
       const int s = warp * C::kSub + mycnt % C::kSub;
       const bool ok = mbar_wait_bounded(full0 + 8 * s, (mycnt / C::kSub) & 1, a.wait_limit_ns,
                                         abort_flag);
@@ -600,7 +650,9 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
         aborted = true;
         break;
       }
-      const int2 meta = stage_meta[s];
+      const int cnt = min(kQ, n_pages - sq * kQ);
+      for (int t = 0; t < cnt; ++t) {
+      const int2 meta = stage_meta[s * kQ + t];
       const int page = meta.x;
       const uint32_t hmask = static_cast<uint32_t>(meta.y);
       const uint32_t kb = sbase + s * C::kStageBytes, vb = kb + C::kPageBytes;
@@ -609,11 +661,13 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
       float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       Q4Page<D> q4;  // 4-bit: the lane's codes and bounds of the page
       if constexpr (Q4) {
-        // Everything the warp needs from the stage goes to registers; then the
-        // stage is free.
-        q4_load<C, D>(smem + s * C::kStageBytes, g, t4, q4);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty0 + 8 * s);
+        // Everything the warp needs from the page goes to registers; after
+        // the stage's last page, the stage is free.
+        q4_load<C, D>(smem + s * C::kStageBytes, t, g, t4, q4);
+        if (t == cnt - 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty0 + 8 * s);
+        }
         q4_scores<D>(q4, qa, sc);
       } else {
 #pragma unroll
@@ -676,6 +730,7 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * s);
+      }
       }
     }
 
@@ -853,7 +908,7 @@ __global__ void __launch_bounds__(kSmallMergeThreads) merge_small_kernel(const M
 // memory as compiled), at most kAttnCtasPerSm; computed once.
 template <int D, bool F16, bool SPARSE, bool Q4>
 cudaError_t attn_ctas_per_sm_t(int* out) {
-  using C = AttnCfg<D, Q4>;
+  using C = AttnCfg<D, Q4, Q4 && !SPARSE>;
   static int cached = 0;  // benign race: every thread computes the same value
   if (cached > 0) {
     *out = cached;
@@ -875,7 +930,7 @@ cudaError_t attn_ctas_per_sm_t(int* out) {
 template <int D, bool F16, bool SPARSE, bool Q4>
 cudaError_t launch_attn_t(const AttnArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
                           int num_sms, cudaStream_t s) {
-  using C = AttnCfg<D, Q4>;
+  using C = AttnCfg<D, Q4, Q4 && !SPARSE>;
   int per_sm = 0;
   cudaError_t e = attn_ctas_per_sm_t<D, F16, SPARSE, Q4>(&per_sm);
   if (e != cudaSuccess) return e;
