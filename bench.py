@@ -294,6 +294,45 @@ def run_dkv(args, rank, world, local):
     return res, (q, K, V, w, widx, dev, stream)
 
 
+def group_select_leg(q, K, V, w, dev, stream, reps=10):
+    """decode_attn_select with one selection per kv head group (summed bound
+    scores) on the bench workload; the same byte count rule (metadata plus the
+    unique pages gathered per (batch, kv head))."""
+    import decode_attention_paged_kv_gb300 as dkv
+    from decode_attention_paged_kv_gb300 import accounting as acc
+
+    meta = dkv.kv_meta_build(K)
+    kk = min(w.top_k, w.P)
+    ws = torch.zeros(dkv.workspace_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, w.top_k),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty(w.B, w.Hq, w.d, dtype=torch.float32, device=dev)
+    sel = torch.empty(w.B, w.Hq, kk, dtype=torch.int32, device=dev)
+
+    def call():
+        dkv.decode_attn_select(q, K, V, meta, w.top_k, out=out, selected=sel, workspace=ws,
+                               group_select=True)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    gathered = union_tokens(sel, w)
+    nbytes = acc.select_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, gathered, w.S)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak, _ = peaks()
+    return {"workload": w.name, "ms": round(ms, 5), "alg_bytes": nbytes, "GB/s": round(gbs, 1),
+            "frac_of_measured_hbm": round(gbs / peak, 4),
+            "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4), "gathered_pages": gathered // w.S,
+            "queries_per_s": round(w.B / (ms * 1e-3), 1),
+            "timing": f"{reps} back-to-back calls"}
+
+
 def headwise_leg(dev, stream):
     """1M-token context, 8 kv heads: exact attention all heads at once and one
     kv head at a time (HeadInfer), bitwise-equal outputs."""
@@ -545,6 +584,7 @@ def main():
     res, (q, K, V, w, widx, dev, stream) = run_dkv(args, rank, world, local)
     if not args.no_extra and rank == 0:
         res["e2e"] = e2e_leg(q, K, V, w, dev, stream, args.steps)
+        res["group_select"] = group_select_leg(q, K, V, w, dev, stream)
         res["cpu_baseline"] = cpu_baseline_leg(q, K, V, w)
         del q, K, V
         torch.cuda.empty_cache()

@@ -42,6 +42,7 @@ DKV_ERR_DEVICE_TIMEOUT = 8
 DKV_BF16, DKV_FP16, DKV_FP32 = 0, 1, 2
 DKV_KV_DENSE, DKV_KV_Q4G64 = 0, 1
 DKV_FLAG_FORCE_TIMEOUT = 0x1
+DKV_FLAG_GROUP_SELECT = 0x2
 
 
 class DkvError(RuntimeError):
@@ -242,8 +243,12 @@ def decode_attn_select(q, K, V, meta, top_k: int, scale: Optional[float] = None,
                        out_dtype: torch.dtype = torch.float32,
                        out: Optional[torch.Tensor] = None, return_selected: bool = False,
                        selected: Optional[torch.Tensor] = None,
-                       workspace: Optional[torch.Tensor] = None, flags: int = 0):
-    """Query-aware page-sparse decode attention over the top_k pages per q-head."""
+                       workspace: Optional[torch.Tensor] = None, flags: int = 0,
+                       group_select: bool = False):
+    """Query-aware page-sparse decode attention over the top_k pages per q-head
+    (group_select: one selection per kv head group, by the summed bound scores)."""
+    if group_select:
+        flags |= DKV_FLAG_GROUP_SELECT
     ks, B, H, N, d = _kv_struct(K)
     vs, B2, H2, N2, d2 = _kv_struct(V)
     if (B, H, N, d) != (B2, H2, N2, d2):

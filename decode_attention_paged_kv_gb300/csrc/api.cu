@@ -396,6 +396,7 @@ dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_
   const int P = static_cast<int>(ceil_div(p->seq_len, p->page_size));
   const int G = p->num_q_heads / p->num_kv_heads;
   const bool f16 = K->dtype == DKV_FP16;
+  const bool group = (p->flags & DKV_FLAG_GROUP_SELECT) != 0;
 
   int32_t* sel = selected != nullptr ? selected : reinterpret_cast<int32_t*>(ws + L.selected);
   int2* ulist = reinterpret_cast<int2*>(ws + L.union_list);
@@ -429,6 +430,7 @@ dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_
     ua.union_list = ulist;
     ua.union_count = ucount;
     ua.union_stride = L.union_stride;
+    ua.group = group ? 1 : 0;
     ua.status = a.status;
     ua.wait_limit_ns = a.wait_limit_ns;
     CUtensorMap mmx, mmn;
@@ -463,6 +465,8 @@ dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_
     ta.selected = sel;
     ta.bitmaps = reinterpret_cast<uint32_t*>(ws + L.bitmaps);
     ta.W32 = L.W32;
+    ta.Hq = p->num_q_heads;
+    ta.group = group ? G : 1;
     if ((st = cuda_status(dkv::launch_topk(ta, s))) != DKV_OK) return st;
     dkv::UnionArgs ua{};
     ua.bitmaps = ta.bitmaps;

@@ -110,6 +110,8 @@ struct ScoreArgs {
 struct TopkArgs {
   const float* scores;         // [rows, P]
   int rows, P, kk;
+  int Hq;                      // rows are (b, h): b * Hq + h
+  int group;                   // heads whose scores a row sums (1, or G for one selection per group)
   int32_t* selected;           // [rows, kk]
   uint32_t* bitmaps;           // [rows, W32]
   int W32;
@@ -134,6 +136,7 @@ struct UnitSelectArgs {
   int2* union_list;            // [B * Hkv, union_stride]
   int* union_count;            // [B * Hkv]
   int union_stride;
+  int group;                   // 1: one selection per kv head group (summed scores)
   uint32_t* status;
   uint64_t wait_limit_ns;
 };

@@ -296,14 +296,22 @@ __global__ void __launch_bounds__(kSelThreads) topk_kernel(const TopkArgs a) {
   const int row = blockIdx.x;
   griddep_launch_dependents();
   griddep_wait();  // the scores come from the previous kernel
-  const float* r = a.scores + static_cast<int64_t>(row) * a.P;
+  // One selection per kv head group: every row of the group sums the group's
+  // scores, head by head in order, so the group's rows select identically.
+  const int r0 = row - (row % a.Hq) % a.group;
+  const float* r = a.scores + static_cast<int64_t>(r0) * a.P;
+  auto score = [&](int j) {
+    float s = __ldcg(r + j);
+    for (int h = 1; h < a.group; ++h) s = __fadd_rn(s, __ldcg(r + static_cast<int64_t>(h) * a.P + j));
+    return s;
+  };
   if constexpr (SMEM) {
-    for (int j = threadIdx.x; j < a.P; j += kSelThreads) s_keys[j] = score_key(__ldcg(r + j));
+    for (int j = threadIdx.x; j < a.P; j += kSelThreads) s_keys[j] = score_key(score(j));
     __syncthreads();
   }
   auto key = [&](int j) {
     if constexpr (SMEM) return s_keys[j];
-    return score_key(__ldcg(r + j));
+    return score_key(score(j));
   };
   uint32_t* bits = a.bitmaps + static_cast<int64_t>(row) * a.W32;
   auto word_out = [&](int w, uint32_t v) { bits[w] = v; };
@@ -380,7 +388,9 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(usm + C::kBarOffset + 16 * C::kStages);
   uint32_t* s_keys = reinterpret_cast<uint32_t*>(usm + C::kKeysOffset);      // [G][P]
   uint32_t* s_bm = s_keys + static_cast<size_t>(a.G) * a.P;                  // [G][kSelBitmapWords]
-  uint32_t* s_kext = s_bm + static_cast<size_t>(a.G) * kSelBitmapWords;      // [2][8]: max, min key
+  // [0..7] / [8..15]: each head's largest / smallest key; [16] / [17]: the
+  // group score's (one selection per group)
+  uint32_t* s_kext = s_bm + static_cast<size_t>(a.G) * kSelBitmapWords;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int unit = blockIdx.x;
   const int b = unit / a.Hkv, kvh = unit % a.Hkv;
@@ -393,7 +403,7 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (threadIdx.x < 16) s_kext[threadIdx.x] = threadIdx.x < 8 ? 0u : ~0u;
+  if (threadIdx.x < 18) s_kext[threadIdx.x] = (threadIdx.x < 8 || threadIdx.x == 16) ? 0u : ~0u;
   if (warp == kUnitConsumers && lane == 0) {
     prefetch_tensormap(&mmx);
     prefetch_tensormap(&mmn);
@@ -518,17 +528,41 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
 
   // ------------------------------------------------------------ selection
   const int W = static_cast<int>(ceil_div(a.P, 32));
-  for (int h = warp; h < a.G; h += kUnitConsumers) {
+  if (a.group) {
+    // One selection per group: page j's key becomes that of the heads' scores
+    // summed in head order (row 0 of the keys; only this thread reads or
+    // writes page j).
+    uint32_t gmx = 0u, gmn = ~0u;
+    for (int j = threadIdx.x; j < a.P; j += kUnitConsumers * 32) {
+      float sum = key_score(s_keys[j]);
+      for (int h = 1; h < a.G; ++h) sum = __fadd_rn(sum, key_score(s_keys[h * a.P + j]));
+      const uint32_t k = score_key(sum);
+      s_keys[j] = k;
+      gmx = max(gmx, k);
+      gmn = min(gmn, k);
+    }
+    gmx = __reduce_max_sync(0xffffffffu, gmx);
+    gmn = __reduce_min_sync(0xffffffffu, gmn);
+    if (lane == 0) {
+      atomicMax(s_kext + 16, gmx);
+      atomicMin(s_kext + 17, gmn);
+    }
+    unit_consumers_sync();
+  }
+  const int n_sel = a.group ? 1 : a.G;  // selections: one per head, or one per group
+  for (int h = warp; h < n_sel; h += kUnitConsumers) {
     uint32_t* bm = s_bm + h * kSelBitmapWords;
     const uint32_t* keys = s_keys + h * a.P;
-    warp_topk_head([keys](int j) { return keys[j]; }, a.P, a.kk, bm, s_kext[h], s_kext[8 + h]);
+    warp_topk_head([keys](int j) { return keys[j]; }, a.P, a.kk, bm,
+                   s_kext[a.group ? 16 : h], s_kext[a.group ? 17 : 8 + h]);
   }
   unit_consumers_sync();
   if (warp >= kUnionWarps) {
     // Warps 4-7 write each head's ascending row while warps 0-3 build the union.
     for (int h = warp - kUnionWarps; h < a.G; h += kUnitConsumers - kUnionWarps) {
       const int64_t row = static_cast<int64_t>(b) * a.Hq + kvh * a.G + h;
-      warp_emit_row(s_bm + h * kSelBitmapWords, W, a.selected + row * a.kk, nullptr);
+      warp_emit_row(s_bm + (a.group ? 0 : h) * kSelBitmapWords, W, a.selected + row * a.kk,
+                    nullptr);
     }
     return;
   }
@@ -542,7 +576,7 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
     uint32_t u = 0;
 #pragma unroll
     for (int h = 0; h < 8; ++h) {
-      hw[h] = (own && h < a.G) ? s_bm[h * kSelBitmapWords + wi] : 0u;
+      hw[h] = (own && h < a.G) ? s_bm[(a.group ? 0 : h) * kSelBitmapWords + wi] : 0u;
       u |= hw[h];
     }
     const int c = __popc(u);
@@ -614,7 +648,7 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
 size_t unit_select_smem(int d, int G, int P) {
   const size_t keys_off = d == 128 ? UnitCfg<128>::kKeysOffset : UnitCfg<64>::kKeysOffset;
   return 1024 + keys_off + static_cast<size_t>(G) * P * 4 +
-         static_cast<size_t>(G) * kSelBitmapWords * 4 + 16 * 4;
+         static_cast<size_t>(G) * kSelBitmapWords * 4 + 32 * 4;
 }
 
 cudaError_t launch_unit_select(int d, bool f16, const UnitSelectArgs& a, const CUtensorMap& mmx,

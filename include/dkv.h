@@ -122,6 +122,16 @@ typedef struct dkv_params {
 /* Test hook: every bounded device wait gives up at once, so the timeout path
    (status word set, in-flight copies drained, clean exit) runs without a hang. */
 #define DKV_FLAG_FORCE_TIMEOUT 0x1u
+/* dkv_decode_attn_select only: one selection per kv head group (GQA).  Page
+   j's score is the sum of the group's bound scores, sum_h r(q_h, phi_j) (the
+   sum over heads h = 0 .. G-1 in that order, in fp32); the group keeps its
+   top_k pages and every head of the group attends them, so the `selected`
+   rows of a group are identical.  The sum stays an upper bound:
+   sum_h r(q_h, phi_j) >= max over the page's keys k of sum_h q_h . k.
+   ("TinyServe: Query-Aware Cache Selection for Efficient LLM Serving",
+   相关性函数实例化, defines r for one query vector; summing over a group is a
+   reading for grouped heads.) */
+#define DKV_FLAG_GROUP_SELECT 0x2u
 
 /* Bytes of workspace the attention calls need for `p` (top_k = 0: the exact
    path; top_k >= 1: the sparse path).  0 if `p` is invalid.  Host only. */

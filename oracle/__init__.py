@@ -138,6 +138,21 @@ def scores(q: np.ndarray, meta_min: np.ndarray, meta_max: np.ndarray, is_fp16: i
     return out
 
 
+def group_scores(q: np.ndarray, meta_min: np.ndarray, meta_max: np.ndarray, is_fp16: int):
+    """One selection per kv head group (GQA), float64 [B, Hkv, P].
+
+    Page j's group score is the sum over the group's query heads h of the
+    bound score r(q_h, phi_j) ("TinyServe", 相关性函数实例化).  The pages define
+    r for one query vector and are silent on grouped heads; the sum is the
+    reading used for one shared selection, and it stays an upper bound:
+    sum_h r(q_h, phi_j) >= max over the page's keys k of sum_h q_h . k.
+    """
+    r = scores(q, meta_min, meta_max, is_fp16)  # [B, Hq, P]
+    B, Hq, P = r.shape
+    Hkv = meta_min.shape[1]
+    return r.reshape(B, Hkv, Hq // Hkv, P).sum(axis=2)
+
+
 def topk(r: np.ndarray, K: int) -> np.ndarray:
     """Top-K page indices per row of r [..., P], ascending; ties -> lower index."""
     r = _c(r, np.float64)

@@ -99,6 +99,48 @@ def test_select_matches_oracle(w, dev, dkv):
     assert max_abs(out, ref) <= ATOL
 
 
+# One selection per kv head group (summed bound scores): the per-unit selection
+# kernel (1024-2048 pages) and the separate selection kernels (shorter and
+# longer contexts), GQA 4 and 8, bf16 and fp16, ragged last pages.
+GROUP_CASES = [
+    Workload("group-unit-gqa4", B=2, Hq=8, Hkv=2, d=128, N=20000, top_k=50, kind="hot"),
+    Workload("group-unit-gqa8-d64", B=1, Hq=16, Hkv=2, d=64, N=32768, top_k=100, kind="hot"),
+    Workload("group-kernels-short", B=2, Hq=8, Hkv=2, d=128, N=5000, top_k=24, kind="hot"),
+    Workload("group-kernels-long", B=1, Hq=4, Hkv=1, d=128, N=40000, top_k=300, kind="hot"),
+    Workload("group-unit-fp16", B=3, Hq=4, Hkv=2, d=64, N=16400, top_k=40, dtype="fp16"),
+]
+
+
+@pytest.mark.parametrize("w", GROUP_CASES, ids=lambda w: w.name)
+def test_group_select_matches_oracle(w, dev, dkv):
+    q, K, V = make_inputs(w, seed=41)
+    scale = 1.0 / math.sqrt(w.d)
+    qd, Kd, Vd = q.to(dev), K.to(dev), V.to(dev)
+    meta = dkv.kv_meta_build(Kd)
+    out, sel = dkv.decode_attn_select(qd, Kd, Vd, meta, w.top_k, return_selected=True,
+                                      group_select=True)
+    sel = sel.cpu().numpy()
+    kk = sel.shape[-1]
+    per_group = sel.reshape(w.B, w.Hkv, w.G, kk)
+    assert np.array_equal(per_group, np.broadcast_to(per_group[:, :, :1], per_group.shape))
+    omn, omx = oracle.meta(bits(K), w.S, _is16(w))
+    rg = oracle.group_scores(bits(q), omn, omx, _is16(w))
+    check_selection(per_group[:, :, 0].reshape(-1, kk), rg.reshape(-1, rg.shape[-1]), w.top_k)
+    ref = oracle.attention(bits(q), bits(K), bits(V), w.S, scale, _is16(w), sel=sel)
+    assert max_abs(out, ref) <= ATOL
+
+
+def test_group_select_with_one_head_per_group_is_per_head_select(dev, dkv):
+    w = Workload("mha", B=2, Hq=4, Hkv=4, d=128, N=20000, top_k=64, kind="offset")
+    q, K, V = (x.to(dev) for x in make_inputs(w, seed=43))
+    meta = dkv.kv_meta_build(K)
+    o1, s1 = dkv.decode_attn_select(q, K, V, meta, w.top_k, return_selected=True)
+    o2, s2 = dkv.decode_attn_select(q, K, V, meta, w.top_k, return_selected=True,
+                                    group_select=True)
+    assert torch.equal(s1, s2)
+    assert torch.equal(o1, o2)
+
+
 @pytest.mark.parametrize("w", CASES[:4], ids=lambda w: w.name)
 def test_select_all_pages_equals_full(w, dev, dkv):
     q, K, V = make_inputs(w, seed=41)

@@ -135,6 +135,64 @@ def test_score_gqa_head_mapping():
         assert np.all(r[0, h] == d * (h // 2 + 1))
 
 
+def test_group_score_bounds_the_group_dot_products():
+    # One selection per kv head group: sum_h r(q_h, phi_j) must bound the best
+    # summed dot product over the page's keys (brute force over every key).
+    w = Workload("t", B=2, Hq=8, Hkv=2, d=64, N=517, kind="hot")
+    q, K, _ = make_inputs(w, seed=21)
+    qb, Kb = bits(q), bits(K)
+    mn, mx = oracle.meta(Kb, 16, 0)
+    rg = oracle.group_scores(qb, mn, mx, 0)
+    assert rg.shape == (2, 2, w.P)
+    qv, Kv = _vals(qb, 0), _vals(Kb, 0)
+    for g in range(w.Hkv):
+        qsum = qv[:, g * w.G:(g + 1) * w.G].sum(axis=1)  # [B, d]
+        dots = np.einsum("bd,btd->bt", qsum, Kv[:, g])
+        for j in range(w.P):
+            best = dots[:, j * 16:min(w.N, (j + 1) * 16)].max(axis=1)
+            slack = 1e-12 * np.abs(qv[:, g * w.G:(g + 1) * w.G]).sum(axis=(1, 2)) * 8
+            assert np.all(rg[:, g, j] >= best - slack)
+
+
+def test_group_score_closed_forms():
+    # All q >= 0: the group score is (sum_h q_h) . M; all q <= 0: (sum_h q_h) . m.
+    # Computed here from the summed query, not from per-head scores.
+    w = Workload("t", B=1, Hq=6, Hkv=2, d=128, N=80)
+    q, K, _ = make_inputs(w, seed=23)
+    qv, Kb = _vals(bits(q), 0), bits(K)
+    mn, mx = oracle.meta(Kb, 16, 0)
+    qa = np.abs(qv)
+    rp = oracle.group_scores(bits(torch.tensor(qa).to(torch.bfloat16)), mn, mx, 0)
+    rn = oracle.group_scores(bits(torch.tensor(-qa).to(torch.bfloat16)), mn, mx, 0)
+    mxv, mnv = _vals(mx, 0), _vals(mn, 0)
+    for g in range(2):
+        qs = qa[0, 3 * g:3 * g + 3].sum(axis=0)
+        np.testing.assert_allclose(rp[0, g], mxv[0, g] @ qs, rtol=1e-13, atol=1e-12)
+        np.testing.assert_allclose(rn[0, g], mnv[0, g] @ -qs, rtol=1e-13, atol=1e-12)
+
+
+def test_group_score_head_mapping():
+    # Only q-head h is non-zero: its group (h // G) scores r(q_h), the others 0;
+    # with one head per group the group score is the head's own score.
+    w = Workload("t", B=1, Hq=8, Hkv=2, d=64, N=64)
+    q, K, _ = make_inputs(w, seed=25)
+    qv, Kb = _vals(bits(q), 0), bits(K)
+    mn, mx = oracle.meta(Kb, 16, 0)
+    for h in (0, 3, 5, 7):
+        qo = np.zeros_like(qv)
+        qo[0, h] = qv[0, h]
+        qob = bits(torch.tensor(qo).to(torch.bfloat16))
+        rg = oracle.group_scores(qob, mn, mx, 0)
+        r = oracle.scores(qob, mn, mx, 0)
+        assert np.array_equal(rg[0, h // 4], r[0, h])
+        assert np.all(rg[0, 1 - h // 4] == 0)
+    w1 = Workload("t", B=1, Hq=2, Hkv=2, d=64, N=64)
+    q1, K1, _ = make_inputs(w1, seed=27)
+    mn1, mx1 = oracle.meta(bits(K1), 16, 0)
+    assert np.array_equal(oracle.group_scores(bits(q1), mn1, mx1, 0),
+                          oracle.scores(bits(q1), mn1, mx1, 0))
+
+
 def _brute_topk(r, K):
     order = sorted(range(len(r)), key=lambda j: (-r[j], j))
     return sorted(order[:min(K, len(r))])
