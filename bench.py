@@ -333,6 +333,69 @@ def group_select_leg(q, K, V, w, dev, stream, reps=10):
             "timing": f"{reps} back-to-back calls"}
 
 
+def paged_leg(q, K, V, w, dev, stream, reps=10):
+    """The bench workload held as a pool of 16-token blocks in shuffled order
+    with a block table: exact and sparse attention timed like the contiguous
+    cache (10 back-to-back calls each), outputs compared bit for bit."""
+    import decode_attention_paged_kv_gb300 as dkv
+    from decode_attention_paged_kv_gb300 import accounting as acc
+
+    nb = w.B * w.P
+    g = torch.Generator(device=dev).manual_seed(11)
+    order = torch.randperm(nb, generator=g, device=dev)
+    bt = order.view(w.B, w.P).to(torch.int32).contiguous()
+
+    def pool_of(X):
+        pool = torch.empty(nb, w.Hkv, w.S, w.d, dtype=X.dtype, device=dev)
+        pool[order] = X.view(w.B, w.Hkv, w.P, w.S, w.d).permute(0, 2, 1, 3, 4).reshape(
+            nb, w.Hkv, w.S, w.d)
+        return pool
+
+    PK, PV = dkv.PagedCache(pool_of(K), bt, w.N), dkv.PagedCache(pool_of(V), bt, w.N)
+    meta = dkv.kv_meta_build(K)
+    ws = torch.zeros(dkv.workspace_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, w.top_k),
+                     dtype=torch.uint8, device=dev)
+    kk = min(w.top_k, w.P)
+    outs = {k: torch.empty(w.B, w.Hq, w.d, dtype=torch.float32, device=dev)
+            for k in ("full", "full_paged", "select", "select_paged")}
+    sel = torch.empty(w.B, w.Hq, kk, dtype=torch.int32, device=dev)
+    calls = {
+        "full": lambda: dkv.decode_attn_full(q, K, V, out=outs["full"], workspace=ws),
+        "full_paged": lambda: dkv.decode_attn_full(q, PK, PV, out=outs["full_paged"], workspace=ws),
+        "select": lambda: dkv.decode_attn_select(q, K, V, meta, w.top_k, out=outs["select"],
+                                                 selected=sel, workspace=ws),
+        "select_paged": lambda: dkv.decode_attn_select(q, PK, PV, meta, w.top_k,
+                                                       out=outs["select_paged"], selected=sel,
+                                                       workspace=ws),
+    }
+    peak, _ = peaks()
+    res = {"workload": w.name, "pool_blocks": nb, "timing": f"{reps} back-to-back calls"}
+    for name, fn in calls.items():
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        if name.startswith("full"):
+            nbytes = acc.full_bytes(w.B, w.Hq, w.Hkv, w.d, w.N)
+        else:
+            nbytes = acc.select_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, union_tokens(sel, w), w.S)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[name] = {"ms": round(ms, 5), "GB/s": round(gbs, 1),
+                     "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+                     "frac_of_measured_hbm": round(gbs / peak, 4)}
+    res["bitwise_equal_to_contiguous"] = bool(
+        torch.equal(outs["full"], outs["full_paged"]) and
+        torch.equal(outs["select"], outs["select_paged"]))
+    del PK, PV
+    return res
+
+
 def headwise_leg(dev, stream):
     """1M-token context, 8 kv heads: exact attention all heads at once and one
     kv head at a time (HeadInfer), bitwise-equal outputs."""
@@ -585,6 +648,7 @@ def main():
     if not args.no_extra and rank == 0:
         res["e2e"] = e2e_leg(q, K, V, w, dev, stream, args.steps)
         res["group_select"] = group_select_leg(q, K, V, w, dev, stream)
+        res["paged"] = paged_leg(q, K, V, w, dev, stream)
         res["cpu_baseline"] = cpu_baseline_leg(q, K, V, w)
         del q, K, V
         torch.cuda.empty_cache()

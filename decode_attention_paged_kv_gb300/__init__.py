@@ -40,7 +40,7 @@ PAGE_SIZE = 16
 DKV_OK = 0
 DKV_ERR_DEVICE_TIMEOUT = 8
 DKV_BF16, DKV_FP16, DKV_FP32 = 0, 1, 2
-DKV_KV_DENSE, DKV_KV_Q4G64 = 0, 1
+DKV_KV_DENSE, DKV_KV_Q4G64, DKV_KV_PAGED = 0, 1, 2
 DKV_FLAG_FORCE_TIMEOUT = 0x1
 DKV_FLAG_GROUP_SELECT = 0x2
 
@@ -62,6 +62,19 @@ class Q4Cache(NamedTuple):
     gmax: torch.Tensor
 
 
+class PagedCache(NamedTuple):
+    """A K or V cache held as a pool of 16-token pages (blocks).
+
+    pool [num_blocks, Hkv, 16, d] bf16 / fp16 (token and channel strides d, 1);
+    block_table [B, P] int32: page j of batch entry b is pool block
+    block_table[b, j]; seq_len: the N tokens every sequence attends.
+    K and V passed to one call must share the block table.
+    """
+    pool: torch.Tensor
+    block_table: torch.Tensor
+    seq_len: int
+
+
 class _Params(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
@@ -75,7 +88,9 @@ class _KV(ctypes.Structure):
     _fields_ = [("format", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("data", ctypes.c_void_p), ("gmin", ctypes.c_void_p), ("gmax", ctypes.c_void_p),
                 ("stride_b", ctypes.c_int64), ("stride_h", ctypes.c_int64),
-                ("gstride_b", ctypes.c_int64), ("gstride_h", ctypes.c_int64)]
+                ("gstride_b", ctypes.c_int64), ("gstride_h", ctypes.c_int64),
+                ("block_table", ctypes.c_void_p), ("block_table_stride", ctypes.c_int64),
+                ("num_blocks", ctypes.c_int32)]
 
 
 _lib = None
@@ -139,8 +154,23 @@ def _dtype_code(dt: torch.dtype) -> int:
 
 
 def _kv_struct(kv) -> tuple[_KV, int, int, int, int]:
-    """(struct, B, Hkv, N, d) for a dense tensor or a Q4Cache."""
+    """(struct, B, Hkv, N, d) for a dense tensor, a Q4Cache or a PagedCache."""
     s = _KV()
+    if isinstance(kv, PagedCache):
+        pool, bt, N = kv
+        nb, H, S, d = pool.shape
+        if S != PAGE_SIZE or pool.stride(3) != 1 or pool.stride(2) != d:
+            raise ValueError("pool must be [num_blocks, Hkv, 16, d] with token stride d")
+        if bt.dtype != torch.int32 or bt.dim() != 2 or bt.stride(1) != 1:
+            raise ValueError("block_table must be int32 [B, P] with unit column stride")
+        P = (int(N) + PAGE_SIZE - 1) // PAGE_SIZE
+        if bt.shape[1] < P:
+            raise ValueError("block_table has fewer than ceil(seq_len / 16) columns")
+        s.format, s.dtype = DKV_KV_PAGED, _dtype_code(pool.dtype)
+        s.data = pool.data_ptr()
+        s.stride_b, s.stride_h = pool.stride(0), pool.stride(1)
+        s.block_table, s.block_table_stride, s.num_blocks = bt.data_ptr(), bt.stride(0), nb
+        return s, bt.shape[0], H, int(N), d
     if isinstance(kv, Q4Cache):
         c, gmn, gmx = kv
         B, H, N, half = c.shape
@@ -166,7 +196,9 @@ def _kv_struct(kv) -> tuple[_KV, int, int, int, int]:
 
 
 def _device_of(kv) -> torch.device:
-    return kv.codes.device if isinstance(kv, Q4Cache) else kv.device
+    if isinstance(kv, Q4Cache):
+        return kv.codes.device
+    return kv.pool.device if isinstance(kv, PagedCache) else kv.device
 
 
 def _params(q: Optional[torch.Tensor], B, Hkv, N, d, out: Optional[torch.Tensor],
@@ -208,7 +240,8 @@ def kv_meta_build(K, page_size: int = PAGE_SIZE):
     """Page metadata (meta_min, meta_max), each [B, Hkv, P, d]."""
     ks, B, H, N, d = _kv_struct(K)
     dev = _device_of(K)
-    dt = torch.float16 if isinstance(K, Q4Cache) else K.dtype
+    dt = (torch.float16 if isinstance(K, Q4Cache)
+          else K.pool.dtype if isinstance(K, PagedCache) else K.dtype)
     P = (N + page_size - 1) // page_size
     mn = torch.empty(B, H, P, d, dtype=dt, device=dev)
     mx = torch.empty(B, H, P, d, dtype=dt, device=dev)

@@ -138,6 +138,14 @@ dkv_status check_kv(const dkv_params* p, const dkv_kv* kv) {
     if (kv->stride_b % 8 || kv->stride_h % 8) return DKV_ERR_ALIGN;
     return DKV_OK;
   }
+  if (kv->format == DKV_KV_PAGED) {
+    if (kv->dtype != DKV_BF16 && kv->dtype != DKV_FP16) return DKV_ERR_DTYPE;
+    if (kv->stride_b % 8 || kv->stride_h % 8) return DKV_ERR_ALIGN;
+    if (kv->block_table == nullptr) return DKV_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(kv->block_table) & 3u) return DKV_ERR_ALIGN;
+    if (kv->num_blocks < 1 || kv->block_table_stride < 0) return DKV_ERR_SHAPE;
+    return DKV_OK;
+  }
   if (kv->format == DKV_KV_Q4G64) {
     if (kv->dtype != DKV_FP16) return DKV_ERR_DTYPE;
     if (kv->gmin == nullptr || kv->gmax == nullptr) return DKV_ERR_NULL;
@@ -169,13 +177,18 @@ bool get_encode() {
 // Map over one dense K or V cache [B, Hkv, N, d] viewed as 5-D
 // {64 channels, N tokens, d/64 halves, Hkv, B} with a box of one page
 // {64, 16, d/64, 1, 1} and 128-byte swizzle.
+// Map over a cache [B, Hkv, N, d] viewed as {64 channels, N, d/64 halves, Hkv,
+// B}, or over a pool of blocks as {64 channels, 16 tokens, d/64 halves, Hkv,
+// blocks}; box {64, 16, d/64, 1, 1} (one page of one kv head), 128-byte swizzle.
 bool encode_page_map(CUtensorMap* map, const dkv_params* p, const dkv_kv* kv) {
   if (!get_encode()) return false;
   const int d = p->head_dim;
-  const cuuint64_t dims[5] = {64, static_cast<cuuint64_t>(p->seq_len),
+  const bool paged = kv->format == DKV_KV_PAGED;
+  const cuuint64_t dims[5] = {64,
+                              static_cast<cuuint64_t>(paged ? dkv::kPage : p->seq_len),
                               static_cast<cuuint64_t>(d / 64),
                               static_cast<cuuint64_t>(p->num_kv_heads),
-                              static_cast<cuuint64_t>(p->batch)};
+                              static_cast<cuuint64_t>(paged ? kv->num_blocks : p->batch)};
   const cuuint64_t strides[4] = {static_cast<cuuint64_t>(d) * 2, 128,
                                  static_cast<cuuint64_t>(kv->stride_h) * 2,
                                  static_cast<cuuint64_t>(kv->stride_b) * 2};
@@ -187,7 +200,7 @@ bool encode_page_map(CUtensorMap* map, const dkv_params* p, const dkv_kv* kv) {
   // A size-1 dimension's stride still has to be a valid (16-byte multiple) value.
   cuuint64_t st[4] = {strides[0], strides[1], strides[2], strides[3]};
   if (p->num_kv_heads == 1 && st[2] == 0) st[2] = 16;
-  if (p->batch == 1 && st[3] == 0) st[3] = 16;
+  if (dims[4] == 1 && st[3] == 0) st[3] = 16;
   const CUresult r = g_encode(map, dt, 5, const_cast<void*>(kv->data), dims, st, box, estr,
                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -258,6 +271,11 @@ dkv_status dkv_kv_meta_build(const dkv_params* p, const dkv_kv* K, void* meta_mi
   a.d = p->head_dim;
   a.meta_min = meta_min;
   a.meta_max = meta_max;
+  if (K->format == DKV_KV_PAGED) {
+    a.bt = K->block_table;
+    a.bts = K->block_table_stride;
+    a.nblocks = K->num_blocks;
+  }
   return cuda_status(dkv::launch_meta(K->format == DKV_KV_Q4G64, K->dtype == DKV_FP16, a,
                                       static_cast<cudaStream_t>(stream)));
 }
@@ -271,6 +289,13 @@ static dkv_status attn_common(const dkv_params* p, const void* q, const dkv_kv* 
   if ((st = check_kv(p, K)) != DKV_OK) return st;
   if ((st = check_kv(p, V)) != DKV_OK) return st;
   if (K->format != V->format || K->dtype != V->dtype) return DKV_ERR_DTYPE;
+  if (K->format == DKV_KV_PAGED) {
+    // K and V share one block table; an item's blocks fit the page list
+    if (K->block_table != V->block_table || K->block_table_stride != V->block_table_stride ||
+        K->num_blocks != V->num_blocks)
+      return DKV_ERR_SHAPE;
+    if (L.pages_per_chunk > dkv::kMaxSelectList) return DKV_ERR_UNSUPPORTED;
+  }
   if (out_dtype != DKV_FP32 && out_dtype != DKV_BF16 && out_dtype != DKV_FP16)
     return DKV_ERR_DTYPE;
   if (!L.ok) return DKV_ERR_UNSUPPORTED;
@@ -302,6 +327,11 @@ static bool cache_views(const dkv_params* p, const dkv_kv* K, const dkv_kv* V, C
     a->k4 = q4_view(K);
     a->v4 = q4_view(V);
     return true;
+  }
+  if (K->format == DKV_KV_PAGED) {
+    a->bt = K->block_table;
+    a->bts = K->block_table_stride;
+    a->nblocks = K->num_blocks;
   }
   return encode_page_map(mk, p, K) && encode_page_map(mv, p, V);
 }

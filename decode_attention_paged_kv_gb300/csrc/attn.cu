@@ -82,7 +82,8 @@ struct AttnCfg {
   static constexpr int kMergeRow = D + 2;                           // o[D], max, sum
   static constexpr int kMergeBytes = (kConsumerWarps - 1) * 8 * kMergeRow * 4;
   static constexpr int kListOffset = kMergeOffset + kMergeBytes;
-  static constexpr int kMiscOffset = kListOffset + 8 * kMaxSelectList;
+  static constexpr int kBlockOffset = kListOffset + 8 * kMaxSelectList;  // paged: pool blocks
+  static constexpr int kMiscOffset = kBlockOffset + 4 * kMaxSelectList;
   static constexpr int kSmemBytes = 1024 + kMiscOffset + 16;
   static_assert(Q4 || kPageBytes % 1024 == 0, "TMA stages must stay 1024-byte aligned");
   static_assert(kStages % kConsumerWarps == 0, "one sub-ring per consumer warp");
@@ -368,6 +369,7 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
   volatile ItemDesc* desc = reinterpret_cast<volatile ItemDesc*>(smem + C::kDescOffset);
   float* mrg = reinterpret_cast<float*>(smem + C::kMergeOffset);
   int2* list = reinterpret_cast<int2*>(smem + C::kListOffset);
+  int* blocks = reinterpret_cast<int*>(smem + C::kBlockOffset);  // paged: the item's pool blocks
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOffset);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -438,6 +440,14 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
           __syncwarp();
         } else {
           n = max(0, min(a.P - first, a.pages_per_chunk));
+        }
+        if (a.bt != nullptr) {
+          // paged cache: the pool block of each of the item's pages (clamped)
+          for (int j = lane; j < n; j += 32) {
+            const int page = SPARSE ? list[j].x : first + j;
+            blocks[j] = min(max(a.bt[b * a.bts + page], 0), a.nblocks - 1);
+          }
+          __syncwarp();
         }
         break;
       }
@@ -535,9 +545,12 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
               stage_meta[s] = make_int2(page, SPARSE ? list[j].y : 0xff);
               const uint32_t dst = sbase + s * C::kStageBytes;
               mbar_arrive_expect_tx(full0 + 8 * s, C::kStageBytes);
-              tma_load_5d_hint(dst, &mk, full0 + 8 * s, 0, page * kPage, 0, kvh, b, pol);
-              tma_load_5d_hint(dst + C::kPageBytes, &mv, full0 + 8 * s, 0, page * kPage, 0,
-                               kvh, b, pol);
+              // {channel, token, half, kv head, batch} of the cache, or
+              // {channel, token in block, half, kv head, block} of a pool
+              const int y = a.bt != nullptr ? 0 : page * kPage;
+              const int z = a.bt != nullptr ? blocks[j] : b;
+              tma_load_5d_hint(dst, &mk, full0 + 8 * s, 0, y, 0, kvh, z, pol);
+              tma_load_5d_hint(dst + C::kPageBytes, &mv, full0 + 8 * s, 0, y, 0, kvh, z, pol);
             }
           }
           if (!__all_sync(0xffffffffu, lok)) break;
@@ -720,6 +733,19 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
       if constexpr (Q4) {
         q4_pv<D>(q4, a0, a1, a2, a3, acc);
       } else {
+        if (a.bt != nullptr && (page + 1) * kPage > a.N) {
+          // A pool block's slots past N hold anything: zero those V rows (their
+          // weights are 0, but 0 * NaN is not).  The K rows' scores are masked.
+          const int nt = a.N - page * kPage;
+          uint8_t* vt = smem + s * C::kStageBytes + C::kPageBytes;
+          const int per_half = (kPage - nt) * 8;  // 16-byte chunks
+          for (int i = lane; i < (D / 64) * per_half; i += 32) {
+            const int h = i / per_half, r = i % per_half;
+            *reinterpret_cast<uint4*>(vt + (h * kPage + nt + r / 8) * 128 + (r % 8) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          __syncwarp();
+        }
 #pragma unroll
         for (int jn = 0; jn < D / 16; ++jn) {
           uint32_t r0, r1, r2, r3;

@@ -81,6 +81,11 @@ struct AttnArgs {
   const int* union_count;      // [B * Hkv]
   int union_stride;
   Q4View k4, v4;               // 4-bit caches (the dense path uses the tensor maps)
+  // paged caches: page j of batch entry b is pool block bt[b * bts + j] (the
+  // tensor maps then view the pool); nullptr for a [B, Hkv, N, d] cache
+  const int32_t* bt;
+  int64_t bts;
+  int nblocks;
   uint32_t* status;
   uint64_t wait_limit_ns;
 };
@@ -149,6 +154,9 @@ struct MetaArgs {
   int B, Hkv, N, P, d;
   void* meta_min;
   void* meta_max;
+  const int32_t* bt;           // paged cache: block table [B, P] (row stride bts), else nullptr
+  int64_t bts;
+  int nblocks;
 };
 
 // Launch `kern` with programmatic stream serialisation, so it may begin while

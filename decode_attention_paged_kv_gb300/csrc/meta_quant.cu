@@ -44,8 +44,12 @@ __global__ void __launch_bounds__(kMetaThreads) meta_kernel(const MetaArgs a) {
     uint32_t kmin[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
     uint32_t kmax[4] = {0u, 0u, 0u, 0u};
     if constexpr (!Q4) {
-      const uint16_t* src = static_cast<const uint16_t*>(a.data) + b * a.sb + h * a.sh +
-                            static_cast<int64_t>(t0) * a.d + 8 * v;
+      // a paged cache: the page's pool block (clamped), token 0 of the block
+      const int64_t base = a.bt != nullptr
+                               ? static_cast<int64_t>(min(max(a.bt[b * a.bts + page], 0),
+                                                          a.nblocks - 1)) * a.sb
+                               : b * a.sb + static_cast<int64_t>(t0) * a.d;
+      const uint16_t* src = static_cast<const uint16_t*>(a.data) + base + h * a.sh + 8 * v;
       uint4 x[kPage];
 #pragma unroll
       for (int t = 0; t < kPage; ++t)

@@ -87,8 +87,17 @@ typedef enum dkv_dtype { DKV_BF16 = 0, DKV_FP16 = 1, DKV_FP32 = 2 } dkv_dtype;
 
 typedef enum dkv_kv_format {
   DKV_KV_DENSE = 0, /* data: [B, Hkv, N, d] elements of `dtype` (bf16 or fp16) */
-  DKV_KV_Q4G64 = 1  /* data: codes [B, Hkv, N, d/2] bytes, channel 2i in the low
+  DKV_KV_Q4G64 = 1, /* data: codes [B, Hkv, N, d/2] bytes, channel 2i in the low
                        nibble of byte i; gmin / gmax: [B, Hkv, N, d/64] fp16 */
+  DKV_KV_PAGED = 2  /* a pool of pages (blocks) of S = 16 tokens, `dtype` bf16 or
+                       fp16: block n of kv head h starts at data + n * stride_b +
+                       h * stride_h (elements), token stride d.  block_table
+                       [B, P] int32 (row stride block_table_stride) maps page j
+                       of batch entry b to its block; entries outside
+                       [0, num_blocks) are clamped into it.  A sequence's ragged
+                       last page may hold anything past N: it is never used.
+                       K and V of one call share the table.  ("TinyServe"
+                       结构化内存布局: the cache as pages of S tokens.) */
 } dkv_kv_format;
 
 /* One K or V cache. */
@@ -103,6 +112,9 @@ typedef struct dkv_kv {
   int64_t gstride_b;        /* of gmin / gmax, in fp16 elements; Q4G64 only, */
   int64_t gstride_h;        /*   multiples of 8 (16 bytes: contiguous bounds need
                                N * d / 64 % 8 == 0); token stride is d/64 */
+  const int32_t* block_table;   /* PAGED only (else NULL): [B, P] block indices */
+  int64_t block_table_stride;   /* PAGED only: elements from one batch row to the next */
+  int32_t num_blocks;           /* PAGED only: blocks in the pool */
 } dkv_kv;
 
 /* Problem description shared by the attention and metadata calls. */

@@ -110,3 +110,65 @@ def test_host_validation_before_launch(L):
     assert L.dkv_attn_ctas_per_sm(96, 0, 0, 0, ctypes.byref(n)) == 5
     assert L.dkv_attn_ctas_per_sm(128, 2, 0, 0, ctypes.byref(n)) == 5   # fp32 cache
     assert L.dkv_attn_ctas_per_sm(128, 0, 1, 0, ctypes.byref(n)) == 5   # bf16 4-bit cache
+
+
+def test_struct_layout_matches_header(tmp_path):
+    # The ctypes structs the binding marshals must have the header's offsets.
+    import subprocess
+    import decode_attention_paged_kv_gb300 as dkv
+    fields = {"dkv_kv": [f for f, _ in dkv._KV._fields_],
+              "dkv_params": [f for f, _ in dkv._Params._fields_]}
+    lines = ['#include <stddef.h>', '#include <stdio.h>', '#include "dkv.h"', "int main(void) {"]
+    for st, fs in fields.items():
+        lines.append(f'  printf("{st} %zu\\n", sizeof({st}));')
+        for f in fs:
+            lines.append(f'  printf("{st}.{f} %zu\\n", offsetof({st}, {f}));')
+    lines.append("  return 0;\n}")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o",
+                    str(exe)], check=True)
+    out = dict(l.split() for l in subprocess.run([str(exe)], check=True, capture_output=True,
+                                                 text=True).stdout.splitlines())
+    for st, cls in (("dkv_kv", dkv._KV), ("dkv_params", dkv._Params)):
+        assert int(out[st]) == ctypes.sizeof(cls), st
+        for f in fields[st]:
+            assert int(out[f"{st}.{f}"]) == getattr(cls, f).offset, f"{st}.{f}"
+
+
+def test_paged_cache_validation(L):
+    import decode_attention_paged_kv_gb300 as dkv
+    bt = (ctypes.c_int32 * 256)()
+
+    def paged(**kw):
+        kv = dkv._KV()
+        kv.format, kv.dtype, kv.data = dkv.DKV_KV_PAGED, 0, 4096
+        kv.stride_b, kv.stride_h = 2 * 16 * 128, 16 * 128
+        kv.block_table, kv.block_table_stride, kv.num_blocks = ctypes.addressof(bt), 63, 200
+        for k, v in kw.items():
+            setattr(kv, k, v)
+        return kv
+
+    p = _params()
+    ws = ctypes.c_void_p(1 << 20)
+    q = out = ctypes.c_void_p(1 << 16)
+    f = L.dkv_decode_attn_full
+    mb = L.dkv_kv_meta_build
+    k, v = paged(), paged()
+    assert mb(ctypes.byref(p), ctypes.byref(paged(block_table=None)), q, q, None) == 1
+    assert mb(ctypes.byref(p), ctypes.byref(paged(block_table=ctypes.addressof(bt) + 2)), q, q,
+              None) == 3
+    assert mb(ctypes.byref(p), ctypes.byref(paged(num_blocks=0)), q, q, None) == 2
+    assert mb(ctypes.byref(p), ctypes.byref(paged(stride_h=16 * 128 + 4)), q, q, None) == 3
+    assert mb(ctypes.byref(p), ctypes.byref(paged(dtype=2)), q, q, None) == 4
+    # K and V must share one block table
+    assert f(ctypes.byref(p), q, ctypes.byref(k), ctypes.byref(paged(block_table_stride=64)), out,
+             2, ws, 1 << 20, None) == 2
+    assert f(ctypes.byref(p), q, ctypes.byref(k), ctypes.byref(paged(num_blocks=199)), out, 2, ws,
+             1 << 20, None) == 2
+    dense = dkv._KV()
+    dense.format, dense.dtype, dense.data = 0, 0, 4096
+    dense.stride_b, dense.stride_h = 2 * 1000 * 128, 1000 * 128
+    assert f(ctypes.byref(p), q, ctypes.byref(k), ctypes.byref(dense), out, 2, ws, 1 << 20,
+             None) == 4
