@@ -81,7 +81,8 @@ class _Params(ctypes.Structure):
                 ("seq_len", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("q_stride_b", ctypes.c_int64), ("q_stride_h", ctypes.c_int64),
                 ("o_stride_b", ctypes.c_int64), ("o_stride_h", ctypes.c_int64),
-                ("scale", ctypes.c_float), ("flags", ctypes.c_uint32)]
+                ("scale", ctypes.c_float), ("flags", ctypes.c_uint32),
+                ("seq_lens", ctypes.c_void_p)]
 
 
 class _KV(ctypes.Structure):
@@ -202,8 +203,14 @@ def _device_of(kv) -> torch.device:
 
 
 def _params(q: Optional[torch.Tensor], B, Hkv, N, d, out: Optional[torch.Tensor],
-            scale: Optional[float], flags: int = 0) -> _Params:
+            scale: Optional[float], flags: int = 0,
+            seq_lens: Optional[torch.Tensor] = None) -> _Params:
     p = _Params()
+    if seq_lens is not None:
+        if (seq_lens.dtype != torch.int32 or tuple(seq_lens.shape) != (B,) or not seq_lens.is_cuda
+                or not seq_lens.is_contiguous()):
+            raise ValueError("seq_lens must be a contiguous int32 CUDA tensor [B]")
+        p.seq_lens = seq_lens.data_ptr()
     p.batch, p.num_kv_heads, p.head_dim, p.seq_len, p.page_size = B, Hkv, d, N, PAGE_SIZE
     p.num_q_heads = q.shape[1] if q is not None else Hkv
     if q is not None:
@@ -236,7 +243,7 @@ def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]) -> torch.
     return torch.zeros(nbytes, dtype=torch.uint8, device=device)
 
 
-def kv_meta_build(K, page_size: int = PAGE_SIZE):
+def kv_meta_build(K, page_size: int = PAGE_SIZE, seq_lens: Optional[torch.Tensor] = None):
     """Page metadata (meta_min, meta_max), each [B, Hkv, P, d]."""
     ks, B, H, N, d = _kv_struct(K)
     dev = _device_of(K)
@@ -245,7 +252,7 @@ def kv_meta_build(K, page_size: int = PAGE_SIZE):
     P = (N + page_size - 1) // page_size
     mn = torch.empty(B, H, P, d, dtype=dt, device=dev)
     mx = torch.empty(B, H, P, d, dtype=dt, device=dev)
-    p = _params(None, B, H, N, d, None, None)
+    p = _params(None, B, H, N, d, None, None, seq_lens=seq_lens)
     p.page_size = page_size
     _check(lib().dkv_kv_meta_build(ctypes.byref(p), ctypes.byref(ks), mn.data_ptr(),
                                    mx.data_ptr(), _stream(mn)), "dkv_kv_meta_build")
@@ -255,15 +262,17 @@ def kv_meta_build(K, page_size: int = PAGE_SIZE):
 def decode_attn_full(q, K, V, scale: Optional[float] = None,
                      out_dtype: torch.dtype = torch.float32,
                      out: Optional[torch.Tensor] = None,
-                     workspace: Optional[torch.Tensor] = None, flags: int = 0):
-    """Exact decode attention; returns out [B, Hq, d]."""
+                     workspace: Optional[torch.Tensor] = None, flags: int = 0,
+                     seq_lens: Optional[torch.Tensor] = None):
+    """Exact decode attention; returns out [B, Hq, d] (seq_lens: int32 [B] on the
+    device, tokens each sequence attends; None: all N)."""
     ks, B, H, N, d = _kv_struct(K)
     vs, B2, H2, N2, d2 = _kv_struct(V)
     if (B, H, N, d) != (B2, H2, N2, d2):
         raise ValueError("K and V shapes differ")
     if out is None:
         out = torch.empty(B, q.shape[1], d, dtype=out_dtype, device=q.device)
-    p = _params(q, B, H, N, d, out, scale, flags)
+    p = _params(q, B, H, N, d, out, scale, flags, seq_lens)
     nbytes = lib().dkv_workspace_bytes(ctypes.byref(p), 0)
     ws = _workspace(nbytes, q.device, workspace)
     _check(lib().dkv_decode_attn_full(ctypes.byref(p), q.data_ptr(), ctypes.byref(ks),
@@ -277,7 +286,7 @@ def decode_attn_select(q, K, V, meta, top_k: int, scale: Optional[float] = None,
                        out: Optional[torch.Tensor] = None, return_selected: bool = False,
                        selected: Optional[torch.Tensor] = None,
                        workspace: Optional[torch.Tensor] = None, flags: int = 0,
-                       group_select: bool = False):
+                       group_select: bool = False, seq_lens: Optional[torch.Tensor] = None):
     """Query-aware page-sparse decode attention over the top_k pages per q-head
     (group_select: one selection per kv head group, by the summed bound scores)."""
     if group_select:
@@ -295,7 +304,7 @@ def decode_attn_select(q, K, V, meta, top_k: int, scale: Optional[float] = None,
     kk = min(int(top_k), P)
     if return_selected and selected is None:
         selected = torch.empty(B, q.shape[1], kk, dtype=torch.int32, device=q.device)
-    p = _params(q, B, H, N, d, out, scale, flags)
+    p = _params(q, B, H, N, d, out, scale, flags, seq_lens)
     nbytes = lib().dkv_workspace_bytes(ctypes.byref(p), int(top_k))
     ws = _workspace(nbytes, q.device, workspace)
     sel_ptr = selected.data_ptr() if selected is not None else None

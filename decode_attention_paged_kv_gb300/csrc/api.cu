@@ -115,6 +115,7 @@ dkv_status check_params(const dkv_params* p) {
   if (p->page_size != dkv::kPage) return DKV_ERR_UNSUPPORTED;
   if (p->num_q_heads / p->num_kv_heads > 8) return DKV_ERR_UNSUPPORTED;
   if (p->batch > 65535 || p->num_kv_heads > 65535) return DKV_ERR_SHAPE;  // grid limits
+  if (reinterpret_cast<uintptr_t>(p->seq_lens) & 3u) return DKV_ERR_ALIGN;
   return DKV_OK;
 }
 
@@ -271,6 +272,7 @@ dkv_status dkv_kv_meta_build(const dkv_params* p, const dkv_kv* K, void* meta_mi
   a.d = p->head_dim;
   a.meta_min = meta_min;
   a.meta_max = meta_max;
+  a.lens = p->seq_lens;
   if (K->format == DKV_KV_PAGED) {
     a.bt = K->block_table;
     a.bts = K->block_table_stride;
@@ -289,6 +291,7 @@ static dkv_status attn_common(const dkv_params* p, const void* q, const dkv_kv* 
   if ((st = check_kv(p, K)) != DKV_OK) return st;
   if ((st = check_kv(p, V)) != DKV_OK) return st;
   if (K->format != V->format || K->dtype != V->dtype) return DKV_ERR_DTYPE;
+  if (p->seq_lens != nullptr && K->format == DKV_KV_Q4G64) return DKV_ERR_UNSUPPORTED;
   if (K->format == DKV_KV_PAGED) {
     // K and V share one block table; an item's blocks fit the page list
     if (K->block_table != V->block_table || K->block_table_stride != V->block_table_stride ||
@@ -358,6 +361,7 @@ static dkv::AttnArgs attn_args(const dkv_params* p, const void* q, const WsLayou
   a.exit_counter = reinterpret_cast<uint32_t*>(ws + L.exit_counter);
   a.status = reinterpret_cast<uint32_t*>(ws + L.status);
   a.wait_limit_ns = (p->flags & DKV_FLAG_FORCE_TIMEOUT) ? 0 : kWaitLimitNs;
+  a.lens = p->seq_lens;
   return a;
 }
 
@@ -386,6 +390,8 @@ static dkv_status run_attention(const dkv_params* p, const dkv::AttnArgs& a, boo
   m.pages_per_chunk = a.pages_per_chunk;
   m.G = a.G;
   m.Hkv = a.Hkv;
+  m.lens = a.lens;
+  m.N = a.N;
   return cuda_status(dkv::launch_merge(p->head_dim, m, p->batch * p->num_q_heads, s));
 }
 
@@ -461,6 +467,8 @@ dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_
     ua.union_count = ucount;
     ua.union_stride = L.union_stride;
     ua.group = group ? 1 : 0;
+    ua.lens = p->seq_lens;
+    ua.N = p->seq_len;
     ua.status = a.status;
     ua.wait_limit_ns = a.wait_limit_ns;
     CUtensorMap mmx, mmn;
@@ -497,6 +505,8 @@ dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_
     ta.W32 = L.W32;
     ta.Hq = p->num_q_heads;
     ta.group = group ? G : 1;
+    ta.lens = p->seq_lens;
+    ta.N = p->seq_len;
     if ((st = cuda_status(dkv::launch_topk(ta, s))) != DKV_OK) return st;
     dkv::UnionArgs ua{};
     ua.bitmaps = ta.bitmaps;

@@ -439,7 +439,10 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
           for (int j = lane; j < n; j += 32) list[j] = src[j];
           __syncwarp();
         } else {
-          n = max(0, min(a.P - first, a.pages_per_chunk));
+          // (with per-sequence lengths, chunks past the sequence are skipped)
+          const int Pb = static_cast<int>(ceil_div(seq_len_of(a.lens, b, a.N), kPage));
+          n = max(0, min(Pb - first, a.pages_per_chunk));
+          if (n == 0) continue;
         }
         if (a.bt != nullptr) {
           // paged cache: the pool block of each of the item's pages (clamped)
@@ -626,6 +629,7 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
     const int chunk = item % a.n_chunks;
     const int unit = item / a.n_chunks;
     const int kvh = unit % a.Hkv, b = unit / a.Hkv;
+    const int Nb = seq_len_of(a.lens, b, a.N);  // tokens this sequence attends
 
     uint32_t qa[D / 16][2];
     {
@@ -699,7 +703,7 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int tok = page * kPage + 8 * (e >> 1) + 2 * t4 + (e & 1);
-        sv[e] = (head_on && tok < a.N) ? sc[e >> 1][e & 1] * a.scale_log2 : -INFINITY;
+        sv[e] = (head_on && tok < Nb) ? sc[e >> 1][e & 1] * a.scale_log2 : -INFINITY;
         pmax = fmaxf(pmax, sv[e]);
       }
       pmax = fmaxf(pmax, __shfl_xor_sync(0xffffffffu, pmax, 1));
@@ -733,10 +737,11 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
       if constexpr (Q4) {
         q4_pv<D>(q4, a0, a1, a2, a3, acc);
       } else {
-        if (a.bt != nullptr && (page + 1) * kPage > a.N) {
-          // A pool block's slots past N hold anything: zero those V rows (their
-          // weights are 0, but 0 * NaN is not).  The K rows' scores are masked.
-          const int nt = a.N - page * kPage;
+        if ((a.bt != nullptr || a.lens != nullptr) && (page + 1) * kPage > Nb) {
+          // A pool block's slots past N, or a cache's tokens past a shorter
+          // sequence's end, hold anything: zero those V rows (their weights
+          // are 0, but 0 * NaN is not).  The K rows' scores are masked.
+          const int nt = Nb - page * kPage;
           uint8_t* vt = smem + s * C::kStageBytes + C::kPageBytes;
           const int per_half = (kPage - nt) * 8;  // 16-byte chunks
           for (int i = lane; i < (D / 64) * per_half; i += 32) {
@@ -836,6 +841,9 @@ __global__ void __launch_bounds__(1024) merge_kernel(const MergeArgs m) {
     const int b = row / m.Hq, h = row % m.Hq;
     const int count = m.union_count[b * m.Hkv + h / m.G];
     nc = min(stride, static_cast<int>(ceil_div(count, m.pages_per_chunk)));
+  } else if (m.lens != nullptr) {
+    const int Pb = static_cast<int>(ceil_div(seq_len_of(m.lens, row / m.Hq, m.N), kPage));
+    nc = min(stride, static_cast<int>(ceil_div(Pb, m.pages_per_chunk)));
   }
   const float* ml = m.part_ml + static_cast<int64_t>(row) * stride * 2;
   for (int k = threadIdx.x; k < nc; k += blockDim.x) {
@@ -901,7 +909,11 @@ __global__ void __launch_bounds__(kSmallMergeThreads) merge_small_kernel(const M
   if (row >= rows) return;
   const int stride = m.n_chunks;
   const int b = row / m.Hq, h = row % m.Hq;
-  const int count = m.union_count != nullptr ? __ldcg(m.union_count + b * m.Hkv + h / m.G) : 0;
+  const int count = m.union_count != nullptr
+                        ? __ldcg(m.union_count + b * m.Hkv + h / m.G)
+                        : (m.lens != nullptr
+                               ? static_cast<int>(ceil_div(seq_len_of(m.lens, b, m.N), kPage))
+                               : 0);
   const float2* ml = reinterpret_cast<const float2*>(m.part_ml) + static_cast<int64_t>(row) * stride;
   const float* po = m.part_o + static_cast<int64_t>(row) * stride * D + c;
   float2 mlv[kSmallMergeChunks];
@@ -911,7 +923,7 @@ __global__ void __launch_bounds__(kSmallMergeThreads) merge_small_kernel(const M
     mlv[k] = k < stride ? __ldcg(ml + k) : make_float2(-INFINITY, 0.f);
     x[k] = k < stride ? __ldcg(po + static_cast<int64_t>(k) * D) : 0.f;
   }
-  const int nc = m.union_count != nullptr
+  const int nc = (m.union_count != nullptr || m.lens != nullptr)
                      ? min(stride, static_cast<int>(ceil_div(count, m.pages_per_chunk)))
                      : stride;
   float M = -INFINITY;

@@ -17,6 +17,11 @@ constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
 
 __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Tokens batch entry b attends: lens[b] clamped into [1, N], or N without lens.
+__device__ __forceinline__ int seq_len_of(const int32_t* lens, int b, int N) {
+  return lens != nullptr ? min(max(lens[b], 1), N) : N;
+}
+
 // Split-K: a (batch, kv head) is cut into at most kMaxChunks chunks of pages;
 // each chunk's partial (max, sum, o) is merged by merge_kernel.
 constexpr int kMaxChunks = 256;
@@ -86,6 +91,7 @@ struct AttnArgs {
   const int32_t* bt;
   int64_t bts;
   int nblocks;
+  const int32_t* lens;         // per-sequence lengths [B] or nullptr (all N)
   uint32_t* status;
   uint64_t wait_limit_ns;
 };
@@ -101,6 +107,9 @@ struct MergeArgs {
   void* out;
   int out_dtype;               // 0 bf16, 1 fp16, 2 fp32
   int64_t o_sb, o_sh;
+  // exact path with per-sequence lengths: ceil(ceil(N_b / 16) / ppc) chunks per row
+  const int32_t* lens;
+  int N;
 };
 
 struct ScoreArgs {
@@ -117,6 +126,8 @@ struct TopkArgs {
   int rows, P, kk;
   int Hq;                      // rows are (b, h): b * Hq + h
   int group;                   // heads whose scores a row sums (1, or G for one selection per group)
+  const int32_t* lens;         // per-sequence lengths [B] or nullptr; N = the longest
+  int N;
   int32_t* selected;           // [rows, kk]
   uint32_t* bitmaps;           // [rows, W32]
   int W32;
@@ -142,6 +153,8 @@ struct UnitSelectArgs {
   int* union_count;            // [B * Hkv]
   int union_stride;
   int group;                   // 1: one selection per kv head group (summed scores)
+  const int32_t* lens;         // per-sequence lengths [B] or nullptr; N = the longest
+  int N;
   uint32_t* status;
   uint64_t wait_limit_ns;
 };
@@ -157,6 +170,7 @@ struct MetaArgs {
   const int32_t* bt;           // paged cache: block table [B, P] (row stride bts), else nullptr
   int64_t bts;
   int nblocks;
+  const int32_t* lens;         // per-sequence lengths [B] or nullptr (all N)
 };
 
 // Launch `kern` with programmatic stream serialisation, so it may begin while

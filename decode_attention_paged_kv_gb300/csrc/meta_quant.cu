@@ -40,7 +40,9 @@ __global__ void __launch_bounds__(kMetaThreads) meta_kernel(const MetaArgs a) {
     const int h = static_cast<int>(bh % a.Hkv);
     const int b = static_cast<int>(bh / a.Hkv);
     const int t0 = page * kPage;
-    const int nt = min(kPage, a.N - t0);
+    const int Nb = seq_len_of(a.lens, b, a.N);
+    if (t0 >= Nb) continue;  // past a shorter sequence: not written
+    const int nt = min(kPage, Nb - t0);
     uint32_t kmin[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
     uint32_t kmax[4] = {0u, 0u, 0u, 0u};
     if constexpr (!Q4) {

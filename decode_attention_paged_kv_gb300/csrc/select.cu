@@ -315,11 +315,17 @@ __global__ void __launch_bounds__(kSelThreads) topk_kernel(const TopkArgs a) {
   };
   uint32_t* bits = a.bitmaps + static_cast<int64_t>(row) * a.W32;
   auto word_out = [&](int w, uint32_t v) { bits[w] = v; };
+  // a shorter sequence: its own pages only, and possibly fewer than kk kept
+  const int Pb = static_cast<int>(ceil_div(seq_len_of(a.lens, row / a.Hq, a.N), kPage));
+  const int kkb = min(a.kk, Pb);
   uint32_t prefix, mask;
   int need;
-  block_radix_select(key, a.P, a.kk, sc, prefix, mask, need);
-  block_emit(key, a.P, prefix, mask, need, a.selected + static_cast<int64_t>(row) * a.kk,
-             word_out, sc);
+  block_radix_select(key, Pb, kkb, sc, prefix, mask, need);
+  int32_t* sel_row = a.selected + static_cast<int64_t>(row) * a.kk;
+  block_emit(key, Pb, prefix, mask, need, sel_row, word_out, sc);
+  for (int w = static_cast<int>(ceil_div(Pb, 32)) + threadIdx.x; w < a.W32; w += kSelThreads)
+    bits[w] = 0u;
+  for (int i = kkb + threadIdx.x; i < a.kk; i += kSelThreads) sel_row[i] = -1;
 }
 
 __global__ void __launch_bounds__(kSelThreads) union_kernel(const UnionArgs a) {
@@ -394,7 +400,9 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int unit = blockIdx.x;
   const int b = unit / a.Hkv, kvh = unit % a.Hkv;
-  const int n_boxes = static_cast<int>(ceil_div(a.P, kUnitBoxPages));
+  // pages of this sequence (all P without per-sequence lengths)
+  const int Pb = static_cast<int>(ceil_div(seq_len_of(a.lens, b, a.N), kPage));
+  const int n_boxes = static_cast<int>(ceil_div(Pb, kUnitBoxPages));
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(full0 + 8 * s, 1);
@@ -497,7 +505,7 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int p = i * kUnitBoxPages + 16 * tile + 8 * (e >> 1) + 2 * t4 + (e & 1);
-        if (p < a.P) {
+        if (p < Pb) {
           const uint32_t key = score_key(sc[e >> 1][e & 1]);
           s_keys[g * a.P + p] = key;
           kmx = max(kmx, key);
@@ -527,13 +535,14 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
   }
 
   // ------------------------------------------------------------ selection
-  const int W = static_cast<int>(ceil_div(a.P, 32));
+  const int W = static_cast<int>(ceil_div(Pb, 32));
+  const int kkb = min(a.kk, Pb);  // pages kept (a shorter sequence may have fewer than kk)
   if (a.group) {
     // One selection per group: page j's key becomes that of the heads' scores
     // summed in head order (row 0 of the keys; only this thread reads or
     // writes page j).
     uint32_t gmx = 0u, gmn = ~0u;
-    for (int j = threadIdx.x; j < a.P; j += kUnitConsumers * 32) {
+    for (int j = threadIdx.x; j < Pb; j += kUnitConsumers * 32) {
       float sum = key_score(s_keys[j]);
       for (int h = 1; h < a.G; ++h) sum = __fadd_rn(sum, key_score(s_keys[h * a.P + j]));
       const uint32_t k = score_key(sum);
@@ -553,7 +562,7 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
   for (int h = warp; h < n_sel; h += kUnitConsumers) {
     uint32_t* bm = s_bm + h * kSelBitmapWords;
     const uint32_t* keys = s_keys + h * a.P;
-    warp_topk_head([keys](int j) { return keys[j]; }, a.P, a.kk, bm,
+    warp_topk_head([keys](int j) { return keys[j]; }, Pb, kkb, bm,
                    s_kext[a.group ? 16 : h], s_kext[a.group ? 17 : 8 + h]);
   }
   unit_consumers_sync();
@@ -563,6 +572,7 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
       const int64_t row = static_cast<int64_t>(b) * a.Hq + kvh * a.G + h;
       warp_emit_row(s_bm + (a.group ? 0 : h) * kSelBitmapWords, W, a.selected + row * a.kk,
                     nullptr);
+      for (int i = kkb + lane; i < a.kk; i += 32) a.selected[row * a.kk + i] = -1;
     }
     return;
   }

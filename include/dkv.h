@@ -129,6 +129,15 @@ typedef struct dkv_params {
   int64_t o_stride_b, o_stride_h;   /* out, in elements */
   float scale;              /* softmax scale, usually 1/sqrt(d) */
   uint32_t flags;           /* DKV_FLAG_* ; 0 for normal use */
+  const int32_t* seq_lens;  /* NULL, or a DEVICE array [B]: batch entry b attends
+                               its first N_b tokens (clamped into [1, seq_len]);
+                               seq_len is then the longest and sizes P, the
+                               workspace and the block table.  Tokens past N_b
+                               in the cache may hold anything.  Metadata rows
+                               of pages past ceil(N_b / S) are not written;
+                               selection keeps min(top_k, ceil(N_b / S)) pages
+                               and pads `selected` rows with -1.  Dense and
+                               paged caches only (not Q4G64). */
 } dkv_params;
 
 /* Test hook: every bounded device wait gives up at once, so the timeout path
