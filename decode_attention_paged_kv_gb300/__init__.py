@@ -224,11 +224,12 @@ def _params(q: Optional[torch.Tensor], B, Hkv, N, d, out: Optional[torch.Tensor]
     return p
 
 
-def workspace_bytes(B: int, Hq: int, Hkv: int, d: int, N: int, top_k: int = 0) -> int:
+def workspace_bytes(B: int, Hq: int, Hkv: int, d: int, N: int, top_k: int = 0,
+                    page_size: int = PAGE_SIZE) -> int:
     """Workspace bytes dkv_decode_attn_full (top_k = 0) or _select needs."""
     p = _Params()
     p.batch, p.num_q_heads, p.num_kv_heads, p.head_dim, p.seq_len = B, Hq, Hkv, d, N
-    p.page_size, p.scale = PAGE_SIZE, 1.0
+    p.page_size, p.scale = page_size, 1.0
     n = lib().dkv_workspace_bytes(ctypes.byref(p), int(top_k))
     if n == 0:
         raise DkvError(2, "dkv_workspace_bytes")
@@ -286,9 +287,11 @@ def decode_attn_select(q, K, V, meta, top_k: int, scale: Optional[float] = None,
                        out: Optional[torch.Tensor] = None, return_selected: bool = False,
                        selected: Optional[torch.Tensor] = None,
                        workspace: Optional[torch.Tensor] = None, flags: int = 0,
-                       group_select: bool = False, seq_lens: Optional[torch.Tensor] = None):
+                       group_select: bool = False, seq_lens: Optional[torch.Tensor] = None,
+                       page_size: int = PAGE_SIZE):
     """Query-aware page-sparse decode attention over the top_k pages per q-head
-    (group_select: one selection per kv head group, by the summed bound scores)."""
+    (group_select: one selection per kv head group, by the summed bound scores;
+    page_size: tokens per metadata / selection page, as meta was built with)."""
     if group_select:
         flags |= DKV_FLAG_GROUP_SELECT
     ks, B, H, N, d = _kv_struct(K)
@@ -296,7 +299,7 @@ def decode_attn_select(q, K, V, meta, top_k: int, scale: Optional[float] = None,
     if (B, H, N, d) != (B2, H2, N2, d2):
         raise ValueError("K and V shapes differ")
     mn, mx = meta
-    P = (N + PAGE_SIZE - 1) // PAGE_SIZE
+    P = (N + page_size - 1) // page_size
     if tuple(mn.shape) != (B, H, P, d) or not mn.is_contiguous() or not mx.is_contiguous():
         raise ValueError("meta must be contiguous [B, Hkv, P, d]")
     if out is None:
@@ -305,6 +308,7 @@ def decode_attn_select(q, K, V, meta, top_k: int, scale: Optional[float] = None,
     if return_selected and selected is None:
         selected = torch.empty(B, q.shape[1], kk, dtype=torch.int32, device=q.device)
     p = _params(q, B, H, N, d, out, scale, flags, seq_lens)
+    p.page_size = page_size
     nbytes = lib().dkv_workspace_bytes(ctypes.byref(p), int(top_k))
     ws = _workspace(nbytes, q.device, workspace)
     sel_ptr = selected.data_ptr() if selected is not None else None

@@ -50,17 +50,20 @@ struct WsLayout {
 WsLayout layout_for(const dkv_params& p, int top_k) {
   WsLayout L;
   const int d = p.head_dim;
-  const int64_t P = ceil_div(p.seq_len, p.page_size);
+  const int64_t P = ceil_div(p.seq_len, p.page_size);   // selection (metadata) pages
+  const int64_t P16 = ceil_div(p.seq_len, dkv::kPage);  // cache pages
   const int64_t rows = static_cast<int64_t>(p.batch) * p.num_q_heads;
   const int64_t units = static_cast<int64_t>(p.batch) * p.num_kv_heads;
   if (top_k <= 0) {
-    L.pages_per_chunk = dkv::full_pages_per_chunk(P, d);
-    L.n_chunks = static_cast<int>(ceil_div(P, L.pages_per_chunk));
+    L.pages_per_chunk = dkv::full_pages_per_chunk(P16, d);
+    L.n_chunks = static_cast<int>(ceil_div(P16, L.pages_per_chunk));
   } else {
     const int G = p.num_q_heads / p.num_kv_heads;
     L.kk = static_cast<int>(top_k < P ? top_k : P);
     L.W32 = static_cast<int>(ceil_div(P, 32));
-    const int64_t union_max = (static_cast<int64_t>(G) * L.kk < P) ? G * L.kk : P;
+    // the union list holds cache pages: a selection page is S / 16 of them
+    const int64_t union_sel = (static_cast<int64_t>(G) * L.kk < P) ? G * L.kk : P;
+    const int64_t union_max = std::min(union_sel * (p.page_size / dkv::kPage), P16);
     L.union_stride = static_cast<int>(union_max);
     L.pages_per_chunk = dkv::select_pages_per_chunk(union_max, d);
     if (L.pages_per_chunk > dkv::kMaxSelectList) L.ok = false;
@@ -112,7 +115,10 @@ dkv_status check_params(const dkv_params* p) {
     return DKV_ERR_SHAPE;
   if (p->num_q_heads % p->num_kv_heads != 0) return DKV_ERR_SHAPE;
   if (p->head_dim != 64 && p->head_dim != 128) return DKV_ERR_UNSUPPORTED;
-  if (p->page_size != dkv::kPage) return DKV_ERR_UNSUPPORTED;
+  // metadata / selection pages of 16, 32 or 64 tokens (the cache's pages are 16)
+  if (p->page_size != dkv::kPage && p->page_size != 2 * dkv::kPage &&
+      p->page_size != 4 * dkv::kPage)
+    return DKV_ERR_UNSUPPORTED;
   if (p->num_q_heads / p->num_kv_heads > 8) return DKV_ERR_UNSUPPORTED;
   if (p->batch > 65535 || p->num_kv_heads > 65535) return DKV_ERR_SHAPE;  // grid limits
   if (reinterpret_cast<uintptr_t>(p->seq_lens) & 3u) return DKV_ERR_ALIGN;
@@ -269,6 +275,7 @@ dkv_status dkv_kv_meta_build(const dkv_params* p, const dkv_kv* K, void* meta_mi
   a.Hkv = p->num_kv_heads;
   a.N = p->seq_len;
   a.P = static_cast<int>(ceil_div(p->seq_len, p->page_size));
+  a.S = p->page_size;
   a.d = p->head_dim;
   a.meta_min = meta_min;
   a.meta_max = meta_max;
@@ -350,7 +357,7 @@ static dkv::AttnArgs attn_args(const dkv_params* p, const void* q, const WsLayou
   a.Hkv = p->num_kv_heads;
   a.G = p->num_q_heads / p->num_kv_heads;
   a.N = p->seq_len;
-  a.P = static_cast<int>(ceil_div(p->seq_len, p->page_size));
+  a.P = static_cast<int>(ceil_div(p->seq_len, dkv::kPage));  // cache pages
   a.scale_log2 = p->scale * 1.4426950408889634f;
   a.pages_per_chunk = L.pages_per_chunk;
   a.n_chunks = L.n_chunks;
@@ -469,6 +476,7 @@ dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_
     ua.group = group ? 1 : 0;
     ua.lens = p->seq_lens;
     ua.N = p->seq_len;
+    ua.S = p->page_size;
     ua.status = a.status;
     ua.wait_limit_ns = a.wait_limit_ns;
     CUtensorMap mmx, mmn;
@@ -507,6 +515,7 @@ dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_
     ta.group = group ? G : 1;
     ta.lens = p->seq_lens;
     ta.N = p->seq_len;
+    ta.S = p->page_size;
     if ((st = cuda_status(dkv::launch_topk(ta, s))) != DKV_OK) return st;
     dkv::UnionArgs ua{};
     ua.bitmaps = ta.bitmaps;
@@ -518,6 +527,9 @@ dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_
     ua.union_list = ulist;
     ua.union_count = ucount;
     ua.union_stride = L.union_stride;
+    ua.lens = p->seq_lens;
+    ua.N = p->seq_len;
+    ua.S = p->page_size;
     if ((st = cuda_status(dkv::launch_union(ua, p->batch * p->num_kv_heads, s))) != DKV_OK)
       return st;
   }

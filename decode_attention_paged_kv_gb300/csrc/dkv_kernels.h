@@ -22,6 +22,13 @@ __device__ __forceinline__ int seq_len_of(const int32_t* lens, int b, int N) {
   return lens != nullptr ? min(max(lens[b], 1), N) : N;
 }
 
+// Selection pages of S tokens (S a multiple of the cache's 16-token pages):
+// the cache pages inside selection page j of a sequence of n tokens.  Every
+// page but the sequence's last holds S / 16 of them.
+__device__ __forceinline__ int cache_pages_in(int j, int S, int n) {
+  return min(S / kPage, static_cast<int>(ceil_div(n, kPage)) - j * (S / kPage));
+}
+
 // Split-K: a (batch, kv head) is cut into at most kMaxChunks chunks of pages;
 // each chunk's partial (max, sum, o) is merged by merge_kernel.
 constexpr int kMaxChunks = 256;
@@ -128,17 +135,21 @@ struct TopkArgs {
   int group;                   // heads whose scores a row sums (1, or G for one selection per group)
   const int32_t* lens;         // per-sequence lengths [B] or nullptr; N = the longest
   int N;
+  int S;                       // tokens per selection page
   int32_t* selected;           // [rows, kk]
   uint32_t* bitmaps;           // [rows, W32]
   int W32;
 };
 
 struct UnionArgs {
-  const uint32_t* bitmaps;     // [B, Hq, W32]
+  const uint32_t* bitmaps;     // [B, Hq, W32] over selection pages
   int Hq, Hkv, G, P, W32;
-  int2* union_list;
+  int2* union_list;            // cache pages (16 tokens), each selection page expanded
   int* union_count;
   int union_stride;
+  const int32_t* lens;         // per-sequence lengths [B] or nullptr; N = the longest
+  int N;
+  int S;                       // tokens per selection page (16, 32 or 64)
 };
 
 // One CTA per (batch, kv head): bound scores, per-head top-K and union.
@@ -155,6 +166,8 @@ struct UnitSelectArgs {
   int group;                   // 1: one selection per kv head group (summed scores)
   const int32_t* lens;         // per-sequence lengths [B] or nullptr; N = the longest
   int N;
+  int S;                       // tokens per selection page (16, 32 or 64); the union
+                               // list holds 16-token cache pages
   uint32_t* status;
   uint64_t wait_limit_ns;
 };
@@ -171,6 +184,7 @@ struct MetaArgs {
   int64_t bts;
   int nblocks;
   const int32_t* lens;         // per-sequence lengths [B] or nullptr (all N)
+  int S;                       // tokens per metadata page (16, 32 or 64); P = ceil(N / S)
 };
 
 // Launch `kern` with programmatic stream serialisation, so it may begin while

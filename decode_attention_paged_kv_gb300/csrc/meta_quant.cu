@@ -39,32 +39,38 @@ __global__ void __launch_bounds__(kMetaThreads) meta_kernel(const MetaArgs a) {
     const int64_t bh = pg / a.P;
     const int h = static_cast<int>(bh % a.Hkv);
     const int b = static_cast<int>(bh / a.Hkv);
-    const int t0 = page * kPage;
+    const int t0 = page * a.S;  // a metadata page of S tokens
     const int Nb = seq_len_of(a.lens, b, a.N);
     if (t0 >= Nb) continue;  // past a shorter sequence: not written
-    const int nt = min(kPage, Nb - t0);
+    const int nt = min(a.S, Nb - t0);
     uint32_t kmin[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
     uint32_t kmax[4] = {0u, 0u, 0u, 0u};
     if constexpr (!Q4) {
-      // a paged cache: the page's pool block (clamped), token 0 of the block
-      const int64_t base = a.bt != nullptr
-                               ? static_cast<int64_t>(min(max(a.bt[b * a.bts + page], 0),
-                                                          a.nblocks - 1)) * a.sb
-                               : b * a.sb + static_cast<int64_t>(t0) * a.d;
-      const uint16_t* src = static_cast<const uint16_t*>(a.data) + base + h * a.sh + 8 * v;
-      uint4 x[kPage];
+      // the metadata page's 16-token cache pages, one at a time
+      for (int c0 = 0; c0 < nt; c0 += kPage) {
+        const int cp = (t0 + c0) / kPage;  // cache page
+        const int ntc = min(kPage, nt - c0);
+        // a paged cache: the cache page's pool block (clamped), token 0 of it
+        const int64_t base = a.bt != nullptr
+                                 ? static_cast<int64_t>(min(max(a.bt[b * a.bts + cp], 0),
+                                                            a.nblocks - 1)) * a.sb
+                                 : b * a.sb + static_cast<int64_t>(t0 + c0) * a.d;
+        const uint16_t* src = static_cast<const uint16_t*>(a.data) + base + h * a.sh + 8 * v;
+        uint4 x[kPage];
 #pragma unroll
-      for (int t = 0; t < kPage; ++t)
-        if (t < nt) x[t] = __ldcs(reinterpret_cast<const uint4*>(src + static_cast<int64_t>(t) * a.d));
+        for (int t = 0; t < kPage; ++t)
+          if (t < ntc)
+            x[t] = __ldcs(reinterpret_cast<const uint4*>(src + static_cast<int64_t>(t) * a.d));
 #pragma unroll
-      for (int t = 0; t < kPage; ++t) {
-        if (t < nt) {
-          const uint32_t w[4] = {x[t].x, x[t].y, x[t].z, x[t].w};
+        for (int t = 0; t < kPage; ++t) {
+          if (t < ntc) {
+            const uint32_t w[4] = {x[t].x, x[t].y, x[t].z, x[t].w};
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint32_t k = to_key2(w[u]);
-            kmin[u] = __vminu2(kmin[u], k);
-            kmax[u] = __vmaxu2(kmax[u], k);
+            for (int u = 0; u < 4; ++u) {
+              const uint32_t k = to_key2(w[u]);
+              kmin[u] = __vminu2(kmin[u], k);
+              kmax[u] = __vmaxu2(kmax[u], k);
+            }
           }
         }
       }

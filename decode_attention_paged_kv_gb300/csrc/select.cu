@@ -210,19 +210,27 @@ __device__ void block_emit(const KeyFn& key, int P, uint32_t prefix, uint32_t ma
   __syncthreads();  // the scratch may be reused
 }
 
-// The union of G heads' selection bitmaps (word(h, w)), ascending, with a bit
-// per head: out[0 .. count) = (page, mask); *count_out = count.
+// The union of G heads' selection bitmaps (word(h, w)) over selection pages of
+// S tokens, ascending, with a bit per head, each selection page written as its
+// cache pages (S / 16 of them, fewer for the last page of a sequence of n
+// tokens): out[0 .. count) = (cache page, mask); *count_out = count.
 template <typename WordFn>
-__device__ void block_union(const WordFn& word, int G, int W32, int2* out, int* count_out,
-                            SelScratch& sc) {
+__device__ void block_union(const WordFn& word, int G, int W32, int S, int n, int2* out,
+                            int* count_out, SelScratch& sc) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int span = (W32 + 32 * kSelWarps - 1) / (32 * kSelWarps) * 32;  // words per warp
   const int w0 = warp * span, w1 = min(W32, w0 + span);
+  const int msub = S / kPage, last = static_cast<int>(ceil_div(n, S)) - 1;
+  auto pages_of = [&](uint32_t u, int wi) {  // cache pages of word wi's selection pages
+    int c = __popc(u) * msub;
+    if (wi == (last >> 5) && ((u >> (last & 31)) & 1u)) c -= msub - cache_pages_in(last, S, n);
+    return c;
+  };
   int cnt = 0;
   for (int wi = w0 + lane; wi < w1; wi += 32) {
     uint32_t u = 0;
     for (int h = 0; h < G; ++h) u |= word(h, wi);
-    cnt += __popc(u);
+    cnt += pages_of(u, wi);
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
@@ -242,7 +250,7 @@ __device__ void block_union(const WordFn& word, int G, int W32, int2* out, int* 
       hw[h] = (h < G && wi < w1) ? word(h, wi) : 0u;
       u |= hw[h];
     }
-    const int c = __popc(u);
+    const int c = pages_of(u, wi);
     int incl = c;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -256,7 +264,9 @@ __device__ void block_union(const WordFn& word, int G, int W32, int2* out, int* 
       uint32_t m = 0;
 #pragma unroll
       for (int h = 0; h < 8; ++h) m |= ((hw[h] >> bit) & 1u) << h;
-      out[pos++] = make_int2(wi * 32 + bit, static_cast<int>(m));
+      const int ps = wi * 32 + bit;
+      const int k = msub == 1 ? 1 : cache_pages_in(ps, S, n);
+      for (int i = 0; i < k; ++i) out[pos++] = make_int2(ps * msub + i, static_cast<int>(m));
     }
     before += __shfl_sync(0xffffffffu, incl, 31);
   }
@@ -316,7 +326,7 @@ __global__ void __launch_bounds__(kSelThreads) topk_kernel(const TopkArgs a) {
   uint32_t* bits = a.bitmaps + static_cast<int64_t>(row) * a.W32;
   auto word_out = [&](int w, uint32_t v) { bits[w] = v; };
   // a shorter sequence: its own pages only, and possibly fewer than kk kept
-  const int Pb = static_cast<int>(ceil_div(seq_len_of(a.lens, row / a.Hq, a.N), kPage));
+  const int Pb = static_cast<int>(ceil_div(seq_len_of(a.lens, row / a.Hq, a.N), a.S));
   const int kkb = min(a.kk, Pb);
   uint32_t prefix, mask;
   int need;
@@ -336,8 +346,9 @@ __global__ void __launch_bounds__(kSelThreads) union_kernel(const UnionArgs a) {
   const int b = unit / a.Hkv, kvh = unit % a.Hkv;
   const uint32_t* bm = a.bitmaps + (static_cast<int64_t>(b) * a.Hq + kvh * a.G) * a.W32;
   auto word = [&](int h, int w) { return __ldcg(bm + static_cast<int64_t>(h) * a.W32 + w); };
-  block_union(word, a.G, a.W32, a.union_list + static_cast<int64_t>(unit) * a.union_stride,
-              a.union_count + unit, sc);
+  block_union(word, a.G, a.W32, a.S, seq_len_of(a.lens, b, a.N),
+              a.union_list + static_cast<int64_t>(unit) * a.union_stride, a.union_count + unit,
+              sc);
 }
 
 // ------------------------------------------------------- one CTA per unit
@@ -400,8 +411,9 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int unit = blockIdx.x;
   const int b = unit / a.Hkv, kvh = unit % a.Hkv;
-  // pages of this sequence (all P without per-sequence lengths)
-  const int Pb = static_cast<int>(ceil_div(seq_len_of(a.lens, b, a.N), kPage));
+  // selection pages of this sequence (all P without per-sequence lengths)
+  const int Nb = seq_len_of(a.lens, b, a.N);
+  const int Pb = static_cast<int>(ceil_div(Nb, a.S));
   const int n_boxes = static_cast<int>(ceil_div(Pb, kUnitBoxPages));
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -577,7 +589,9 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
     return;
   }
   // Union of the heads' bitmaps, ascending, with a bit per head: warp w ORs
-  // words w * wpw .. (one per lane), the per-warp counts place them.
+  // words w * wpw .. (one per lane), the per-warp counts place them.  Each
+  // selection page becomes its S / 16 cache pages (fewer for the sequence's
+  // last).
   {
     const int wpw = static_cast<int>(ceil_div(W, kUnionWarps));
     const int wi = warp * wpw + lane;
@@ -589,7 +603,11 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
       hw[h] = (own && h < a.G) ? s_bm[(a.group ? 0 : h) * kSelBitmapWords + wi] : 0u;
       u |= hw[h];
     }
-    const int c = __popc(u);
+    const int msub = a.S / kPage;  // cache pages per selection page
+    const int last = Pb - 1;
+    int c = __popc(u) * msub;
+    if (own && wi == (last >> 5) && ((u >> (last & 31)) & 1u))
+      c -= msub - cache_pages_in(last, a.S, Nb);
     int incl = c;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -607,6 +625,10 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
     }
     int2* out = a.union_list + static_cast<int64_t>(unit) * a.union_stride;
     int at = before + incl - c;
+    auto put = [&](int ps, uint32_t m) {  // selection page ps -> its cache pages
+      const int n = msub == 1 ? 1 : cache_pages_in(ps, a.S, Nb);
+      for (int i = 0; i < n; ++i) out[at++] = make_int2(ps * msub + i, static_cast<int>(m));
+    };
     if (a.G <= 4) {
       while (u) {
         const int bit = __ffs(u) - 1;
@@ -614,7 +636,7 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
         uint32_t m = 0;
 #pragma unroll
         for (int h = 0; h < 4; ++h) m |= ((hw[h] >> bit) & 1u) << h;
-        out[at++] = make_int2(wi * 32 + bit, static_cast<int>(m));
+        put(wi * 32 + bit, m);
       }
     } else {
       while (u) {
@@ -623,7 +645,7 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
         uint32_t m = 0;
 #pragma unroll
         for (int h = 0; h < 8; ++h) m |= ((hw[h] >> bit) & 1u) << h;
-        out[at++] = make_int2(wi * 32 + bit, static_cast<int>(m));
+        put(wi * 32 + bit, m);
       }
     }
     if (threadIdx.x == 0) a.union_count[unit] = count;

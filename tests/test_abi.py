@@ -62,7 +62,11 @@ def test_workspace_bytes_layout(L):
     assert sel > full
     assert L.dkv_workspace_bytes(ctypes.byref(_params(head_dim=96)), 0) == 0
     assert L.dkv_workspace_bytes(ctypes.byref(_params(num_q_heads=7)), 0) == 0
-    assert L.dkv_workspace_bytes(ctypes.byref(_params(page_size=32)), 0) == 0
+    assert L.dkv_workspace_bytes(ctypes.byref(_params(page_size=8)), 0) == 0
+    assert L.dkv_workspace_bytes(ctypes.byref(_params(page_size=48)), 0) == 0
+    # selection pages of 32 or 64 tokens: the exact path is unchanged
+    assert L.dkv_workspace_bytes(ctypes.byref(_params(page_size=32)), 0) == full
+    assert L.dkv_workspace_bytes(ctypes.byref(_params(page_size=64)), 8) > 0
     assert L.dkv_workspace_bytes(None, 0) == 0
 
 
