@@ -162,14 +162,17 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def union_tokens(sel: torch.Tensor, w: Workload) -> int:
-    """Valid tokens of the unique pages gathered per (batch, kv head)."""
+def union_tokens(sel: torch.Tensor, w: Workload, S: int = 0) -> int:
+    """Valid tokens of the unique pages (of S tokens, default the workload's)
+    gathered per (batch, kv head)."""
+    S = S or w.S
+    P = (w.N + S - 1) // S
     B, Hq, kk = sel.shape
-    mask = torch.zeros(B, w.Hkv, w.P, dtype=torch.bool, device=sel.device)
+    mask = torch.zeros(B, w.Hkv, P, dtype=torch.bool, device=sel.device)
     grp = sel.view(B, w.Hkv, w.G * kk).long()
     mask.scatter_(2, grp, True)
-    toks = torch.full((w.P,), w.S, dtype=torch.int64, device=sel.device)
-    toks[-1] = w.N - (w.P - 1) * w.S
+    toks = torch.full((P,), S, dtype=torch.int64, device=sel.device)
+    toks[-1] = w.N - (P - 1) * S
     return int((mask.long() * toks).sum().item())
 
 
@@ -393,6 +396,53 @@ def paged_leg(q, K, V, w, dev, stream, reps=10):
         torch.equal(outs["full"], outs["full_paged"]) and
         torch.equal(outs["select"], outs["select_paged"]))
     del PK, PV
+    return res
+
+
+def page_size_leg(q, K, V, w, dev, stream, reps=10):
+    """Selection page sizes S = 16, 32, 64 ("TinyServe" page-size variants) on
+    the bench workload at the same token budget (K = budget / S pages):
+    metadata build and select, 10 back-to-back calls each."""
+    import decode_attention_paged_kv_gb300 as dkv
+    from decode_attention_paged_kv_gb300 import accounting as acc
+
+    budget = w.top_k * w.S
+    peak, _ = peaks()
+    res = {"workload": w.name, "token_budget": budget, "timing": f"{reps} back-to-back calls"}
+    for S in (16, 32, 64):
+        kk = budget // S
+        P = (w.N + S - 1) // S
+        ws = torch.zeros(dkv.workspace_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, kk, page_size=S),
+                         dtype=torch.uint8, device=dev)
+        out = torch.empty(w.B, w.Hq, w.d, dtype=torch.float32, device=dev)
+        sel = torch.empty(w.B, w.Hq, min(kk, P), dtype=torch.int32, device=dev)
+        meta = dkv.kv_meta_build(K, page_size=S)
+        calls = {"kv_meta_build": lambda: dkv.kv_meta_build(K, page_size=S),
+                 "decode_attn_select": lambda: dkv.decode_attn_select(
+                     q, K, V, meta, kk, out=out, selected=sel, workspace=ws, page_size=S)}
+        r = {"top_k_pages": kk}
+        for name, fn in calls.items():
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / reps
+            if name == "kv_meta_build":
+                nbytes = acc.meta_bytes(w.B, w.Hkv, w.d, w.N, S)
+            else:
+                nbytes = acc.select_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, union_tokens(sel, w, S), S)
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            r[name] = {"ms": round(ms, 5), "alg_bytes": nbytes, "GB/s": round(gbs, 1),
+                       "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+                       "frac_of_measured_hbm": round(gbs / peak, 4)}
+        r["gathered_tokens"] = union_tokens(sel, w, S)
+        res[f"S{S}"] = r
+        del meta, ws
     return res
 
 
@@ -649,6 +699,7 @@ def main():
         res["e2e"] = e2e_leg(q, K, V, w, dev, stream, args.steps)
         res["group_select"] = group_select_leg(q, K, V, w, dev, stream)
         res["paged"] = paged_leg(q, K, V, w, dev, stream)
+        res["page_sizes"] = page_size_leg(q, K, V, w, dev, stream)
         res["cpu_baseline"] = cpu_baseline_leg(q, K, V, w)
         del q, K, V
         torch.cuda.empty_cache()

@@ -26,7 +26,7 @@ namespace {
 constexpr int kMetaThreads = 256;
 
 template <bool Q4>
-__global__ void __launch_bounds__(kMetaThreads) meta_kernel(const MetaArgs a) {
+__global__ void __launch_bounds__(kMetaThreads, 2) meta_kernel(const MetaArgs a) {
   griddep_launch_dependents();
   griddep_wait();
   const int vpr = a.d / 8;  // 16-byte vectors per row
@@ -47,6 +47,7 @@ __global__ void __launch_bounds__(kMetaThreads) meta_kernel(const MetaArgs a) {
     uint32_t kmax[4] = {0u, 0u, 0u, 0u};
     if constexpr (!Q4) {
       // the metadata page's 16-token cache pages, one at a time
+#pragma unroll 1
       for (int c0 = 0; c0 < nt; c0 += kPage) {
         const int cp = (t0 + c0) / kPage;  // cache page
         const int ntc = min(kPage, nt - c0);
