@@ -29,9 +29,10 @@ import torch
 from . import build as _build_mod
 
 __all__ = [
-    "Q4Cache", "DkvError", "lib", "kv_meta_build", "decode_attn_full", "decode_attn_select",
-    "kv_quant4", "kv_dequant4", "workspace_bytes", "read_device_status", "status_string",
-    "PAGE_SIZE",
+    "Q4Cache", "PagedCache", "DkvError", "lib", "kv_meta_build", "decode_attn_full",
+    "decode_attn_select", "decode_attn_topk_tokens", "kv_quant4", "kv_dequant4",
+    "workspace_bytes", "workspace_bytes_tokens", "read_device_status", "status_string",
+    "PAGE_SIZE", "DKV_FLAG_GROUP_SELECT",
 ]
 
 PAGE_SIZE = 16
@@ -117,6 +118,10 @@ def lib() -> ctypes.CDLL:
             L.dkv_decode_attn_full.argtypes = [P, vp, KVp, KVp, vp, i32, vp, sz, vp]
             L.dkv_decode_attn_select.argtypes = [P, vp, KVp, KVp, vp, vp, i32, vp, i32, vp, vp,
                                                  sz, vp]
+            L.dkv_decode_attn_topk_tokens.argtypes = [P, vp, KVp, KVp, i32, vp, i32, vp, vp,
+                                                      sz, vp]
+            L.dkv_workspace_bytes_tokens.argtypes = [P, i32]
+            L.dkv_workspace_bytes_tokens.restype = sz
             L.dkv_kv_quant4.argtypes = [i64, i32, vp, vp, vp, vp, vp]
             L.dkv_kv_dequant4.argtypes = [i64, i32, vp, vp, vp, vp, vp]
             L.dkv_read_device_status.argtypes = [vp, vp]
@@ -124,6 +129,7 @@ def lib() -> ctypes.CDLL:
             L.dkv_status_string.argtypes = [i32]
             L.dkv_status_string.restype = ctypes.c_char_p
             for name in ("dkv_kv_meta_build", "dkv_decode_attn_full", "dkv_decode_attn_select",
+                         "dkv_decode_attn_topk_tokens",
                          "dkv_kv_quant4", "dkv_kv_dequant4", "dkv_read_device_status",
                          "dkv_attn_ctas_per_sm"):
                 getattr(L, name).restype = ctypes.c_int
@@ -318,6 +324,45 @@ def decode_attn_select(q, K, V, meta, top_k: int, scale: Optional[float] = None,
                                         sel_ptr, ws.data_ptr(), nbytes, _stream(q)),
            "dkv_decode_attn_select")
     return (out, selected) if return_selected else out
+
+
+def decode_attn_topk_tokens(q, K, V, top_k: int, scale: Optional[float] = None,
+                            out_dtype: torch.dtype = torch.float32,
+                            out: Optional[torch.Tensor] = None, return_selected: bool = False,
+                            selected: Optional[torch.Tensor] = None,
+                            workspace: Optional[torch.Tensor] = None):
+    """Token-level sparse decode attention: per q-head, the top_k tokens by the
+    exact score q . k and attention over them only (K contiguous [B, Hkv, N, d])."""
+    ks, B, H, N, d = _kv_struct(K)
+    vs, B2, H2, N2, d2 = _kv_struct(V)
+    if (B, H, N, d) != (B2, H2, N2, d2):
+        raise ValueError("K and V shapes differ")
+    if out is None:
+        out = torch.empty(B, q.shape[1], d, dtype=out_dtype, device=q.device)
+    kk = min(int(top_k), N)
+    if return_selected and selected is None:
+        selected = torch.empty(B, q.shape[1], kk, dtype=torch.int32, device=q.device)
+    p = _params(q, B, H, N, d, out, scale)
+    nbytes = lib().dkv_workspace_bytes_tokens(ctypes.byref(p), int(top_k))
+    ws = _workspace(nbytes, q.device, workspace)
+    sel_ptr = selected.data_ptr() if selected is not None else None
+    _check(lib().dkv_decode_attn_topk_tokens(ctypes.byref(p), q.data_ptr(), ctypes.byref(ks),
+                                             ctypes.byref(vs), int(top_k), out.data_ptr(),
+                                             _dtype_code(out.dtype), sel_ptr, ws.data_ptr(),
+                                             nbytes, _stream(q)),
+           "dkv_decode_attn_topk_tokens")
+    return (out, selected) if return_selected else out
+
+
+def workspace_bytes_tokens(B: int, Hq: int, Hkv: int, d: int, N: int, top_k: int) -> int:
+    """Workspace bytes dkv_decode_attn_topk_tokens needs."""
+    p = _Params()
+    p.batch, p.num_q_heads, p.num_kv_heads, p.head_dim, p.seq_len = B, Hq, Hkv, d, N
+    p.page_size, p.scale = PAGE_SIZE, 1.0
+    n = lib().dkv_workspace_bytes_tokens(ctypes.byref(p), int(top_k))
+    if n == 0:
+        raise DkvError(2, "dkv_workspace_bytes_tokens")
+    return int(n)
 
 
 def kv_quant4(x: torch.Tensor) -> Q4Cache:

@@ -563,6 +563,111 @@ dkv_status dkv_kv_dequant4(int64_t rows, int32_t d, const void* codes, const voi
       dkv::launch_dequant4(rows, d, codes, gmin, gmax, x, static_cast<cudaStream_t>(stream)));
 }
 
+// Token-level top-K workspace: header | scores [rows, N] fp32 | selected
+// [rows, kk] int32 | the top-K's bitmaps [rows, ceil(N / 32)] u32.
+static size_t token_layout(const dkv_params* p, int top_k, size_t* scores, size_t* sel,
+                           size_t* bits) {
+  const int64_t rows = static_cast<int64_t>(p->batch) * p->num_q_heads;
+  const int64_t N = p->seq_len;
+  const int64_t kk = top_k < N ? top_k : N;
+  size_t off = DKV_WORKSPACE_HEADER_BYTES;
+  *scores = off;
+  off = align_up(off + sizeof(float) * rows * N);
+  *sel = off;
+  off = align_up(off + sizeof(int32_t) * rows * kk);
+  *bits = off;
+  off = align_up(off + sizeof(uint32_t) * rows * ceil_div(N, 32));
+  return off;
+}
+
+size_t dkv_workspace_bytes_tokens(const dkv_params* p, int32_t top_k) {
+  if (check_params(p) != DKV_OK || top_k < 1) return 0;
+  size_t a, b, c;
+  return token_layout(p, top_k, &a, &b, &c);
+}
+
+dkv_status dkv_decode_attn_topk_tokens(const dkv_params* p, const void* q, const dkv_kv* K,
+                                       const dkv_kv* V, int32_t top_k, void* out,
+                                       int32_t out_dtype, int32_t* selected, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+  dkv_status st = check_params(p);
+  if (st != DKV_OK) return st;
+  if (top_k < 1) return DKV_ERR_SHAPE;
+  if ((st = check_query_out(p, q, out)) != DKV_OK) return st;
+  if ((st = check_kv(p, K)) != DKV_OK) return st;
+  if ((st = check_kv(p, V)) != DKV_OK) return st;
+  if (K->format != DKV_KV_DENSE || V->format != DKV_KV_DENSE || K->dtype != V->dtype)
+    return DKV_ERR_DTYPE;
+  const int d = p->head_dim;
+  const int64_t N = p->seq_len;
+  // the score pass reads K as one contiguous row per token
+  if (K->stride_h != N * d || K->stride_b != static_cast<int64_t>(p->num_kv_heads) * N * d)
+    return DKV_ERR_UNSUPPORTED;
+  if (p->seq_lens != nullptr) return DKV_ERR_UNSUPPORTED;
+  if (out_dtype != DKV_FP32 && out_dtype != DKV_BF16 && out_dtype != DKV_FP16)
+    return DKV_ERR_DTYPE;
+  if (selected != nullptr && (reinterpret_cast<uintptr_t>(selected) & 3u)) return DKV_ERR_ALIGN;
+  size_t o_scores, o_sel, o_bits;
+  const size_t need = token_layout(p, top_k, &o_scores, &o_sel, &o_bits);
+  if (workspace == nullptr) return DKV_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return DKV_ERR_ALIGN;
+  if (workspace_bytes < need) return DKV_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool f16 = K->dtype == DKV_FP16;
+  const int G = p->num_q_heads / p->num_kv_heads;
+  const int rows = p->batch * p->num_q_heads;
+  const int kk = static_cast<int>(top_k < N ? top_k : N);
+  float* scores = reinterpret_cast<float*>(ws + o_scores);
+  int32_t* sel = selected != nullptr ? selected : reinterpret_cast<int32_t*>(ws + o_sel);
+
+  // exact scores: the bound score over single-token pages (m = M = k)
+  dkv::ScoreArgs sa{};
+  sa.q = q;
+  sa.q_sb = p->q_stride_b;
+  sa.q_sh = p->q_stride_h;
+  sa.meta_min = K->data;
+  sa.meta_max = K->data;
+  sa.B = p->batch;
+  sa.Hq = p->num_q_heads;
+  sa.Hkv = p->num_kv_heads;
+  sa.G = G;
+  sa.P = static_cast<int>(N);
+  sa.scores = scores;
+  if ((st = cuda_status(dkv::launch_score(d, f16, sa, s))) != DKV_OK) return st;
+  // the top-K tokens, ties to the lower index, ascending
+  dkv::TopkArgs ta{};
+  ta.scores = scores;
+  ta.rows = rows;
+  ta.P = static_cast<int>(N);
+  ta.kk = kk;
+  ta.Hq = p->num_q_heads;
+  ta.group = 1;
+  ta.N = static_cast<int>(N);
+  ta.S = 1;
+  ta.selected = sel;
+  ta.bitmaps = reinterpret_cast<uint32_t*>(ws + o_bits);
+  ta.W32 = static_cast<int>(ceil_div(N, 32));
+  if ((st = cuda_status(dkv::launch_topk(ta, s))) != DKV_OK) return st;
+  dkv::TokenAttnArgs aa{};
+  aa.scores = scores;
+  aa.selected = sel;
+  aa.kk = kk;
+  aa.N = static_cast<int>(N);
+  aa.Hq = p->num_q_heads;
+  aa.G = G;
+  aa.v = V->data;
+  aa.v_sb = V->stride_b;
+  aa.v_sh = V->stride_h;
+  aa.v_st = d;
+  aa.scale_log2 = p->scale * 1.4426950408889634f;
+  aa.out = out;
+  aa.out_dtype = out_code(out_dtype);
+  aa.o_sb = p->o_stride_b;
+  aa.o_sh = p->o_stride_h;
+  return cuda_status(dkv::launch_token_attn(d, f16, aa, rows, s));
+}
+
 dkv_status dkv_read_device_status(void* workspace, void* stream) {
   if (workspace == nullptr) return DKV_ERR_NULL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -172,6 +172,19 @@ struct UnitSelectArgs {
   uint64_t wait_limit_ns;
 };
 
+// Attention over each (b, q-head)'s top-K tokens (token-level sparse attention).
+struct TokenAttnArgs {
+  const float* scores;         // [B * Hq, N] exact q . k_t
+  const int32_t* selected;     // [B * Hq, kk] ascending token indices
+  int kk, N, Hq, G;
+  const void* v;               // V [B, Hkv, N, d]
+  int64_t v_sb, v_sh, v_st;    // elements
+  float scale_log2;            // softmax scale * log2(e)
+  void* out;
+  int out_dtype;               // 0 bf16, 1 fp16, 2 fp32
+  int64_t o_sb, o_sh;
+};
+
 struct MetaArgs {
   const void* data;            // dense K or Q4 codes
   const void* gmin;
@@ -213,6 +226,7 @@ cudaError_t launch_attn_q4(int d, bool sparse, const AttnArgs& a, int num_sms, c
 // Resident attention CTAs per SM for one instantiation (1 .. kAttnCtasPerSm).
 cudaError_t attn_ctas_per_sm(int d, bool f16, bool sparse, bool q4, int* out);
 cudaError_t launch_merge(int d, const MergeArgs& m, int rows, cudaStream_t s);
+cudaError_t launch_token_attn(int d, bool f16, const TokenAttnArgs& a, int rows, cudaStream_t s);
 cudaError_t launch_score(int d, bool f16, const ScoreArgs& a, cudaStream_t s);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
 cudaError_t launch_union(const UnionArgs& a, int units, cudaStream_t s);

@@ -188,6 +188,23 @@ dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_
                                   int32_t out_dtype, int32_t* selected, void* workspace,
                                   size_t workspace_bytes, void* stream);
 
+/* Token-level sparse decode attention ("FlexGen: High-Throughput Generative
+   Inference of Large Language Models with a Single GPU" (解读), its sparse
+   attention: each query keeps the top 10% of the K cache's indices and loads
+   only that subset of V).  For each (b, q-head): the exact scores q . k_t of
+   all N tokens, the top_k highest (ties to the lower token index; top_k
+   clamped to N), softmax over those tokens' scaled scores, and the weighted
+   sum of their V rows.  K and V dense bf16 / fp16 (q in the same dtype); K
+   contiguous [B, Hkv, N, d] (the score pass reads it as one row per token);
+   no per-sequence lengths.  `selected` (nullable) receives the tokens
+   [B, Hq, min(top_k, N)], ascending.  The workspace needs
+   dkv_workspace_bytes_tokens(p, top_k) bytes; page_size is not used. */
+dkv_status dkv_decode_attn_topk_tokens(const dkv_params* p, const void* q, const dkv_kv* K,
+                                       const dkv_kv* V, int32_t top_k, void* out,
+                                       int32_t out_dtype, int32_t* selected, void* workspace,
+                                       size_t workspace_bytes, void* stream);
+size_t dkv_workspace_bytes_tokens(const dkv_params* p, int32_t top_k);
+
 /* 4-bit group-of-64 quantisation of `rows` fp16 rows of d channels (d % 64 == 0):
      mn, mx = group min / max;  step = fp16(fp32(fp32(mx - mn) / 15))
      code   = step == 0 ? 0 : clamp(rint(fp32(fp32(x - mn) / step)), 0, 15)

@@ -176,3 +176,31 @@ def test_paged_cache_validation(L):
     dense.stride_b, dense.stride_h = 2 * 1000 * 128, 1000 * 128
     assert f(ctypes.byref(p), q, ctypes.byref(k), ctypes.byref(dense), out, 2, ws, 1 << 20,
              None) == 4
+
+
+def test_token_topk_validation(L):
+    import decode_attention_paged_kv_gb300 as dkv
+    p = _params()
+    ws = ctypes.c_void_p(1 << 20)
+    q = out = ctypes.c_void_p(1 << 16)
+    kv = dkv._KV()
+    kv.format, kv.dtype, kv.data = 0, 0, 4096
+    kv.stride_b, kv.stride_h = 2 * 1000 * 128, 1000 * 128  # contiguous [2, 2, 1000, 128]
+    t = L.dkv_decode_attn_topk_tokens
+    args = lambda k, v, top_k=100, size=1 << 30, pp=p: (
+        ctypes.byref(pp), q, ctypes.byref(k), ctypes.byref(v), top_k, out, 2, None, ws, size, None)
+    need = L.dkv_workspace_bytes_tokens(ctypes.byref(p), 100)
+    assert need >= 256 + 16 * 1000 * 4 + 16 * 100 * 4
+    assert L.dkv_workspace_bytes_tokens(ctypes.byref(p), 0) == 0
+    assert t(*args(kv, kv, top_k=0)) == 2
+    assert t(*args(kv, kv, size=need - 1)) == 6
+    strided = dkv._KV()
+    strided.format, strided.dtype, strided.data = 0, 0, 4096
+    strided.stride_b, strided.stride_h = 2 * 1024 * 128, 1024 * 128  # not contiguous in N
+    assert t(*args(strided, kv)) == 5
+    q4 = dkv._KV()
+    q4.format, q4.dtype, q4.data, q4.gmin, q4.gmax = 1, 1, 4096, 4096, 4096
+    assert t(*args(q4, q4)) == 4
+    lens = (ctypes.c_int32 * 2)(1000, 500)
+    pl = _params(seq_lens=ctypes.addressof(lens))
+    assert t(*args(kv, kv, pp=pl)) == 5
