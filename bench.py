@@ -446,6 +446,39 @@ def page_size_leg(q, K, V, w, dev, stream, reps=10):
     return res
 
 
+def token_leg(q, K, V, w, dev, stream, reps=10):
+    """Token-level sparse attention on the bench workload, keeping the top 10%
+    of the tokens per q-head (10 back-to-back calls)."""
+    import decode_attention_paged_kv_gb300 as dkv
+    from decode_attention_paged_kv_gb300 import accounting as acc
+
+    ktok = w.N // 10
+    ws = torch.zeros(dkv.workspace_bytes_tokens(w.B, w.Hq, w.Hkv, w.d, w.N, ktok),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty(w.B, w.Hq, w.d, dtype=torch.float32, device=dev)
+
+    def call():
+        dkv.decode_attn_topk_tokens(q, K, V, ktok, out=out, workspace=ws)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    nbytes = acc.token_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, ktok)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak, _ = peaks()
+    return {"workload": w.name, "top_k_tokens": ktok, "ms": round(ms, 5), "alg_bytes": nbytes,
+            "GB/s": round(gbs, 1), "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+            "frac_of_measured_hbm": round(gbs / peak, 4),
+            "queries_per_s": round(w.B / (ms * 1e-3), 1), "timing": f"{reps} back-to-back calls"}
+
+
 def headwise_leg(dev, stream):
     """1M-token context, 8 kv heads: exact attention all heads at once and one
     kv head at a time (HeadInfer), bitwise-equal outputs."""
@@ -538,6 +571,18 @@ def workload_leg(name, dev, stream, reps=10):
     calls += [("kv_meta_build", meta, acc.meta_bytes(w.B, w.Hkv, w.d, w.N, w.S, q4=w.q4)),
               ("decode_attn_full", full, acc.full_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, q4=w.q4)),
               ("decode_attn_select", select, None)]
+    if not w.q4:
+        # token-level sparse attention keeping the top 10% of the tokens per head
+        ktok = max(1, w.N // 10)
+        ws_tok = torch.zeros(dkv.workspace_bytes_tokens(w.B, w.Hq, w.Hkv, w.d, w.N, ktok),
+                             dtype=torch.uint8, device=dev)
+        out_tok = torch.empty_like(out_full)
+
+        def tokens():
+            dkv.decode_attn_topk_tokens(q, K, V, ktok, out=out_tok, workspace=ws_tok)
+
+        calls.append(("decode_attn_topk_tokens (10%)", tokens,
+                      acc.token_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, ktok)))
     for _ in range(3):
         for _, fn, _ in calls:
             fn()
@@ -700,6 +745,7 @@ def main():
         res["group_select"] = group_select_leg(q, K, V, w, dev, stream)
         res["paged"] = paged_leg(q, K, V, w, dev, stream)
         res["page_sizes"] = page_size_leg(q, K, V, w, dev, stream)
+        res["topk_tokens"] = token_leg(q, K, V, w, dev, stream)
         res["cpu_baseline"] = cpu_baseline_leg(q, K, V, w)
         del q, K, V
         torch.cuda.empty_cache()

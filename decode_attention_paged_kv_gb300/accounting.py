@@ -59,3 +59,10 @@ def quant4_bytes(rows, d) -> int:
 def memory_fraction(S: int, K: int, L: int, rho: float = 1.0) -> float:
     """TinyServe's sparse-over-full memory fraction 1/S + rho K S / L."""
     return 1.0 / S + rho * K * S / L
+
+
+def token_bytes(B, Hq, Hkv, d, N, kk, elt=2, out_elt=4) -> int:
+    """Token-level top-K attention: q + all of K (every token is scored) + the
+    V rows of each q-head's kk selected tokens + out.  The score workspace is
+    overhead, as for the page-sparse path."""
+    return B * Hq * d * elt + B * Hkv * N * d * elt + B * Hq * kk * d * elt + B * Hq * d * out_elt

@@ -634,6 +634,7 @@ dkv_status dkv_decode_attn_topk_tokens(const dkv_params* p, const void* q, const
   sa.G = G;
   sa.P = static_cast<int>(N);
   sa.scores = scores;
+  sa.exact = 1;
   if ((st = cuda_status(dkv::launch_score(d, f16, sa, s))) != DKV_OK) return st;
   // the top-K tokens, ties to the lower index, ascending
   dkv::TopkArgs ta{};

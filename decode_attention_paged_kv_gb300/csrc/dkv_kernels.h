@@ -126,6 +126,7 @@ struct ScoreArgs {
   const void* meta_max;
   int B, Hq, Hkv, G, P;
   float* scores;               // [B, Hq, P]
+  int exact;                   // 1: meta_max holds single keys (m = M): score q . k once
 };
 
 struct TopkArgs {

@@ -37,14 +37,28 @@ namespace {
 
 constexpr int kScoreWarps = 4;
 constexpr int kScorePagesPerCta = 16 * kScoreWarps;
-constexpr int kSelThreads = 256;  // top-K and union CTAs
+constexpr int kSelThreads = 1024;  // top-K and union CTAs
 constexpr int kSelWarps = kSelThreads / 32;
+static_assert(kSelWarps <= 32, "one warp partial a lane");
+
+// Per-warp partials part[0 .. kSelWarps) summed by every warp, one partial a
+// lane: over all warps, or over the warps before the calling one.
+__device__ __forceinline__ int warps_total(const uint32_t* part) {
+  const int lane = threadIdx.x & 31;
+  return __reduce_add_sync(0xffffffffu, lane < kSelWarps ? static_cast<int>(part[lane]) : 0);
+}
+__device__ __forceinline__ int warps_before(const uint32_t* part) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  return __reduce_add_sync(0xffffffffu, lane < warp ? static_cast<int>(part[lane]) : 0);
+}
 constexpr size_t kTopkSmemKeyBytes = 160 * 1024;  // stage rows of up to 40960 pages
 
 // B operand of the score MMA for lane (g, t4): [q+ | q-] of query head g of the
 // group (zero for g >= G).  The contraction index runs over the concatenation
 // [M | m]; the lane owns 16-byte chunks c = t4 + 4 s of it, two k-steps each.
-template <int D>
+// EXACT: plain q over the d channels (rows of single keys, m = M = k: the
+// bound is the dot product itself, computed once).
+template <int D, bool EXACT = false>
 __device__ __forceinline__ void load_q_pm(const void* q, int64_t q_sb, int64_t q_sh, int b,
                                           int kvh, int G, int lane,
                                           uint32_t (&bq)[D / 16][4]) {
@@ -52,38 +66,52 @@ __device__ __forceinline__ void load_q_pm(const void* q, int64_t q_sb, int64_t q
   const bool hv = g < G;
   const uint16_t* qrow = static_cast<const uint16_t*>(q) + b * q_sb +
                          static_cast<int64_t>(kvh * G + (hv ? g : 0)) * q_sh;
+  if constexpr (EXACT) {
 #pragma unroll
-  for (int s = 0; s < D / 16; ++s) {
-    const int c = t4 + 4 * s;
-    const bool neg_part = c >= D / 8;
-    const int ch = 8 * (neg_part ? c - D / 8 : c);
-    const uint4 w = hv ? *reinterpret_cast<const uint4*>(qrow + ch) : make_uint4(0, 0, 0, 0);
-    bq[s][0] = keep_sign(w.x, neg_part);
-    bq[s][1] = keep_sign(w.y, neg_part);
-    bq[s][2] = keep_sign(w.z, neg_part);
-    bq[s][3] = keep_sign(w.w, neg_part);
+    for (int s = 0; s < D / 32; ++s) {
+      const uint4 w = hv ? *reinterpret_cast<const uint4*>(qrow + 8 * (t4 + 4 * s))
+                         : make_uint4(0, 0, 0, 0);
+      bq[s][0] = w.x;
+      bq[s][1] = w.y;
+      bq[s][2] = w.z;
+      bq[s][3] = w.w;
+    }
+  } else {
+#pragma unroll
+    for (int s = 0; s < D / 16; ++s) {
+      const int c = t4 + 4 * s;
+      const bool neg_part = c >= D / 8;
+      const int ch = 8 * (neg_part ? c - D / 8 : c);
+      const uint4 w = hv ? *reinterpret_cast<const uint4*>(qrow + ch) : make_uint4(0, 0, 0, 0);
+      bq[s][0] = keep_sign(w.x, neg_part);
+      bq[s][1] = keep_sign(w.y, neg_part);
+      bq[s][2] = keep_sign(w.z, neg_part);
+      bq[s][3] = keep_sign(w.w, neg_part);
+    }
   }
 }
 
 // Bound scores of pages page0 .. page0+15 (< P) of one (batch, kv head) for the
 // group's query heads: acc = [page g][head 2t4], [g][2t4+1], [g+8][2t4],
 // [g+8][2t4+1].  mmax / mmin point at the unit's [P, d] metadata.
-template <int D, bool F16>
+template <int D, bool F16, bool EXACT = false>
 __device__ __forceinline__ void score_tile(const uint32_t (&bq)[D / 16][4], const uint16_t* mmax,
                                            const uint16_t* mmin, int page0, int P, int lane,
                                            float (&acc)[4]) {
   const int g = lane >> 2, t4 = lane & 3;
+  constexpr int NS = EXACT ? D / 32 : D / 16;  // 16-byte chunks a lane contracts
   // Every load is issued before the first MMA (rows past P read a valid page
-  // and are zeroed afterwards), so a lane has 2 d / 8 16-byte loads in flight.
+  // and are zeroed afterwards), so a lane has 2 NS 16-byte loads in flight.
   uint4 ra[2][D / 16];
 #pragma unroll
   for (int hr = 0; hr < 2; ++hr) {
     const int page = min(page0 + g + 8 * hr, P - 1);
 #pragma unroll
-    for (int s = 0; s < D / 16; ++s) {
+    for (int s = 0; s < NS; ++s) {
       const int c = t4 + 4 * s;
-      const uint16_t* src = (c < D / 8) ? mmax + static_cast<int64_t>(page) * D + 8 * c
-                                        : mmin + static_cast<int64_t>(page) * D + 8 * (c - D / 8);
+      const uint16_t* src = (EXACT || c < D / 8)
+                                ? mmax + static_cast<int64_t>(page) * D + 8 * c
+                                : mmin + static_cast<int64_t>(page) * D + 8 * (c - D / 8);
       ra[hr][s] = __ldg(reinterpret_cast<const uint4*>(src));
     }
   }
@@ -91,121 +119,535 @@ __device__ __forceinline__ void score_tile(const uint32_t (&bq)[D / 16][4], cons
   for (int hr = 0; hr < 2; ++hr) {
     if (page0 + g + 8 * hr >= P) {
 #pragma unroll
-      for (int s = 0; s < D / 16; ++s) ra[hr][s] = make_uint4(0, 0, 0, 0);
+      for (int s = 0; s < NS; ++s) ra[hr][s] = make_uint4(0, 0, 0, 0);
     }
   }
   acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
 #pragma unroll
-  for (int s = 0; s < D / 16; ++s) {
+  for (int s = 0; s < NS; ++s) {
     mma16816<F16>(acc, ra[0][s].x, ra[1][s].x, ra[0][s].y, ra[1][s].y, bq[s][0], bq[s][1]);
     mma16816<F16>(acc, ra[0][s].z, ra[1][s].z, ra[0][s].w, ra[1][s].w, bq[s][2], bq[s][3]);
   }
 }
 
+constexpr int kSelCompCap = 4096;  // bucket keys the block top-K compacts
 struct SelScratch {
   uint32_t hist[256];
-  long long warp_tot[kSelWarps];
-  uint32_t digit, above;
+  uint32_t warp_gt[kSelWarps];         // per-warp counts (emit: keys > prefix,
+  uint32_t warp_eq[kSelWarps];         // == prefix; union: pages)
+  uint32_t comp[kSelCompCap];
 };
 
-// Radix selection (block of kSelThreads) of the kk largest of P keys.  On
-// return: keys with (key & mask) > prefix are selected, and of the keys with
+// Stores v at p (global) or addr (shared) when c holds: one predicated store,
+// so a warp whose lanes differ on c takes no branch.
+__device__ __forceinline__ void st_global_if(void* p, uint32_t v, bool c) {
+  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q st.global.u32 [%0], %1;\n\t}"
+               :
+               : "l"(p), "r"(v), "r"(static_cast<uint32_t>(c))
+               : "memory");
+}
+__device__ __forceinline__ void st_shared_if(uint32_t addr, uint32_t v, bool c) {
+  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q st.shared.u32 [%0], %1;\n\t}"
+               :
+               : "r"(addr), "r"(v), "r"(static_cast<uint32_t>(c))
+               : "memory");
+}
+
+// Selection (block of kSelThreads) of the kk largest of P keys: the K-th
+// largest key found bit by bit below the keys' common prefix (radix selection
+// with 1-bit digits, as the per-head warp top-K), every pass one count over the
+// block, stopping as soon as exactly kk keys are >= the candidate.  On return:
+// keys with (key & mask) > prefix are selected, and of the keys with
 // (key & mask) == prefix the first `need` in index order.
 template <typename KeyFn>
 __device__ void block_radix_select(const KeyFn& key, int P, int kk, SelScratch& sc,
                                    uint32_t& prefix, uint32_t& mask, int& need) {
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int P_round = (P + kSelThreads - 1) / kSelThreads * kSelThreads;
-  prefix = 0;
-  mask = 0;
-  need = kk;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    sc.hist[tid] = 0;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t* wcnt = sc.hist;            // per-warp counts
+  uint32_t* wmax = sc.hist + kSelWarps;
+  uint32_t* wmin = sc.hist + 2 * kSelWarps;
+  // the keys' largest and smallest: the bits they all share are skipped
+  uint32_t mx = 0u, mn = ~0u;
+  for (int j = tid; j < P; j += kSelThreads) {
+    const uint32_t k = key(j);
+    mx = max(mx, k);
+    mn = min(mn, k);
+  }
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  if (lane == 0) {
+    wmax[warp] = mx;
+    wmin[warp] = mn;
+  }
+  __syncthreads();
+  const uint32_t kmax = __reduce_max_sync(0xffffffffu, lane < kSelWarps ? wmax[lane] : 0u);
+  const uint32_t kmin = __reduce_min_sync(0xffffffffu, lane < kSelWarps ? wmin[lane] : ~0u);
+  __syncthreads();
+  // keys >= x over the block (four partial sums a thread, then warps in order)
+  auto block_sum = [&](int mine) {
+    const int wsum = __reduce_add_sync(0xffffffffu, mine);
+    if (lane == 0) wcnt[warp] = static_cast<uint32_t>(wsum);
     __syncthreads();
-    for (int j = tid; j < P_round; j += kSelThreads) {
-      const uint32_t k = (j < P) ? key(j) : 0u;
-      const bool in = (j < P) && (k & mask) == prefix;
-      const uint32_t digit = (k >> shift) & 0xffu;
-      const uint32_t act = __ballot_sync(0xffffffffu, in);
-      if (in) {  // one shared atomic per distinct digit per warp
-        const uint32_t peers = __match_any_sync(act, digit);
-        if (lane == __ffs(peers) - 1)
-          atomicAdd(&sc.hist[digit], static_cast<uint32_t>(__popc(peers)));
-      }
+    const int tot = warps_total(wcnt);
+    __syncthreads();
+    return tot;
+  };
+  auto count_ge = [&](uint32_t x) {
+    int c0 = 0, c1 = 0, c2 = 0, c3 = 0;
+    int j = tid;
+    for (; j + 3 * kSelThreads < P; j += 4 * kSelThreads) {
+      c0 -= minus_borrow(key(j), x);
+      c1 -= minus_borrow(key(j + kSelThreads), x);
+      c2 -= minus_borrow(key(j + 2 * kSelThreads), x);
+      c3 -= minus_borrow(key(j + 3 * kSelThreads), x);
     }
-    __syncthreads();
-    if (tid < 32) {
-      // lane L owns digits 255-8L .. 248-8L (descending).
-      uint32_t c[8], sum = 0;
+    for (; j < P; j += kSelThreads) c0 -= minus_borrow(key(j), x);
+    const int below = (c0 + c1) + (c2 + c3);
+    return block_sum(max(static_cast<int>(ceil_div(P - tid, kSelThreads)), 0) - below);
+  };
+  // Once the keys that agree with the bits fixed so far (the bucket) are few,
+  // they are copied to sc.comp; counts are then `base` (keys above the bucket)
+  // plus the bucket's keys >= x.
+  int ncomp = -1, base = 0;
+  auto count_comp = [&](uint32_t x) {
+    int c = 0;
+    for (int j = tid; j < ncomp; j += kSelThreads) c -= minus_borrow(sc.comp[j], x);
+    return base + block_sum(max(static_cast<int>(ceil_div(ncomp - tid, kSelThreads)), 0) - c);
+  };
+  uint32_t T;
+  int ge = -1;
+  if (kmax == kmin) {
+    T = kmax;  // all equal: a tie at T
+  } else {
+    const int top = 31 - __clz(kmax ^ kmin);
+    T = top == 31 ? 0u : (kmax >> (top + 1)) << (top + 1);
+    int geT = P, above = 0;  // keys >= T; keys above the bucket
+    for (int bit = top; bit >= 0; --bit) {
+      if (ncomp < 0 && geT - above <= kSelCompCap) {
+        // the bucket: keys whose bits above `bit` equal T's; each thread
+        // counts its own, a block scan places them, then each writes its own
+        const int sh = bit + 1;
+        auto in_bucket = [&](uint32_t k) { return sh == 32 || (k >> sh) == (T >> sh); };
+        int mine = 0;
+        for (int j = tid; j < P; j += kSelThreads) mine += in_bucket(key(j)) ? 1 : 0;
+        int incl = mine;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        c[u] = sc.hist[255 - 8 * tid - u];
-        sum += c[u];
-      }
-      uint32_t incl = sum;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, off);
-        if (tid >= off) incl += t;
-      }
-      uint32_t above = incl - sum;  // keys with a larger digit
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (above < static_cast<uint32_t>(need) && above + c[u] >= static_cast<uint32_t>(need)) {
-          sc.digit = 255 - 8 * tid - u;
-          sc.above = above;
+        for (int off = 1; off < 32; off <<= 1) {
+          const int t = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += t;
         }
-        above += c[u];
+        if (lane == 31) wcnt[warp] = static_cast<uint32_t>(incl);
+        __syncthreads();
+        int at = incl - mine + warps_before(wcnt);
+        ncomp = warps_total(wcnt);
+        for (int j = tid; j < P; j += kSelThreads) {
+          const uint32_t k = key(j);
+          if (in_bucket(k)) sc.comp[at++] = k;
+        }
+        base = above;
+        __syncthreads();
+      }
+      const uint32_t cand = T | (1u << bit);
+      const int c = ncomp >= 0 ? count_comp(cand) : count_ge(cand);
+      if (c >= kk) {
+        T = cand;
+        ge = geT = c;
+        if (c == kk) break;
+      } else {
+        above = c;
       }
     }
-    __syncthreads();
-    const uint32_t digit = sc.digit;
-    need -= static_cast<int>(sc.above);
-    prefix |= digit << shift;
-    mask |= 0xffu << shift;
-    const bool all_taken = sc.hist[digit] == static_cast<uint32_t>(need);
-    __syncthreads();
-    if (all_taken) break;
+  }
+  mask = ~0u;
+  if (ge == kk) {
+    // exactly kk keys are >= T (T >= 1 here): all of them
+    prefix = T - 1u;
+    need = 0;
+  } else {
+    // a tie at the kk-th key T: the keys above T, then the first equal ones
+    const int gt = T == ~0u ? 0 : (ncomp >= 0 ? count_comp(T + 1u) : count_ge(T + 1u));
+    prefix = T;
+    need = kk - gt;
   }
 }
 
-// Writes the selection in ascending page order to sel_row[0 .. kk) and its
-// bitmap word by word (word_out(w, bits)).  Warp w walks a contiguous range of
-// pages 32 at a time; one block scan of the per-warp counts places it.
-template <typename KeyFn, typename WordOut>
-__device__ void block_emit(const KeyFn& key, int P, uint32_t prefix, uint32_t mask, int need,
-                           int32_t* sel_row, const WordOut& word_out, SelScratch& sc) {
+// Warp w of block_emit takes pages [w span, (w + 1) span).
+__device__ __forceinline__ int emit_span(int P) {
+  return (P + 32 * kSelWarps - 1) / (32 * kSelWarps) * 32;
+}
+
+constexpr int kSampleMinP = 4096;
+
+// The sample ranks of the two splitters for kk of P keys: hi at rank r_hi
+// (none when r_hi < 1), lo at rank r_lo; false when r_lo passes the sample.
+__device__ __forceinline__ bool sample_ranks(int kk, int P, int& r_hi, int& r_lo) {
+  const float pk = static_cast<float>(kk) / static_cast<float>(P);
+  const float rho = 1024.f * pk, margin = 3.f * sqrtf(1024.f * pk * (1.f - pk)) + 8.f;
+  r_hi = static_cast<int>(floorf(rho - margin));
+  r_lo = static_cast<int>(ceilf(rho + margin));
+  return r_lo <= 1024;
+}
+
+// One warp: the splitter of rank r among 1024 sampled keys (sample i = 32 m +
+// lane is key i * stride + lane % stride, stride = P / 1024), to *out; ~0 when
+// r < 1 (no upper splitter).  The keys are those of the score rows r, r + rs,
+// ... (group of them summed in order, as the staged keys), fetched sixteen a
+// lane at a time through stash[0 .. 1024) (shared memory).
+__device__ void sample_splitter(const float* r, int64_t rs, int group, int P, int rank,
+                                uint32_t* stash, uint32_t* out) {
+  const int lane = threadIdx.x & 31;
+  const int stride = P >> 10;
+  const int off = lane % stride;
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    float v[16];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) v[m] = __ldcg(r + (32 * (16 * b + m) + lane) * stride + off);
+    for (int h = 1; h < group; ++h) {
+      const float* rh = r + h * rs;
+#pragma unroll
+      for (int m = 0; m < 16; ++m)
+        v[m] = __fadd_rn(v[m], __ldcg(rh + (32 * (16 * b + m) + lane) * stride + off));
+    }
+#pragma unroll
+    for (int m = 0; m < 16; ++m) stash[32 * (16 * b + m) + lane] = score_key(v[m]);
+  }
+  __syncwarp();
+  uint32_t smp[32];
+#pragma unroll
+  for (int m = 0; m < 32; ++m) smp[m] = stash[32 * m + lane];
+  uint32_t smax = 0u, smin = ~0u;
+#pragma unroll
+  for (int m = 0; m < 32; ++m) {
+    smax = max(smax, smp[m]);
+    smin = min(smin, smp[m]);
+  }
+  smax = __reduce_max_sync(0xffffffffu, smax);
+  smin = __reduce_min_sync(0xffffffffu, smin);
+  uint32_t t = ~0u;
+  if (rank >= 1) {
+    if (smax == smin) {
+      t = smax;
+    } else {
+      const int top = 31 - __clz(smax ^ smin);
+      const uint32_t t0 = top == 31 ? 0u : (smax >> (top + 1)) << (top + 1);
+      int ge;
+      t = warp_threshold(smp, rank, rank + 2, ge, t0, top);
+    }
+  }
+  if (lane == 0) *out = t;
+}
+
+// Where the two splitters sit in SelScratch::hist (hi, then lo).
+constexpr int kSplitOffset = 2 * kSelWarps;
+
+// Warps that search the sample bracket's bucket (a named barrier among them).
+constexpr int kSearchWarps = 8;
+__device__ __forceinline__ void search_sync() {
+  asm volatile("bar.sync 3, %0;" ::"r"(kSearchWarps * 32) : "memory");
+}
+
+// Block top-K of P >= kSampleMinP keys staged in shared memory (`keys`, zero
+// from P up to a multiple of 4) by a sample bracket.  1024 keys, one from each
+// of 1024 equal windows, give two splitters lo < hi between which the kk-th
+// largest key most likely lies: the sample ranks of that key's expected
+// place, kk * 1024 / P, minus and plus three binomial standard deviations and
+// 8 (sample_splitter, run by two warps while the others stage the keys, leaves
+// them in sc.hist + kSplitOffset).  One pass over the
+// keys counts A = #(>= hi) and the bucket [lo, hi); when A < kk <= A +
+// #bucket and the bucket fits kSelCompCap, a second pass copies the bucket out
+// and the bit search runs on the bucket alone (counts are A plus the bucket's
+// keys >= x).  Otherwise it returns false, having written nothing, and the
+// full search runs.  The splitters only decide which keys are compacted, so
+// the selection is the same exact one either way.  Output as
+// block_radix_select, plus block_emit's per-warp counts in sc.warp_gt and
+// sc.warp_eq (the passes walk the keys in block_emit's warp ranges).
+__device__ bool block_sample_select(const uint32_t* keys, int P, int kk, SelScratch& sc,
+                                    uint32_t& prefix, uint32_t& mask, int& need) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t* wcnt = sc.hist;               // per-warp bucket counts
+  uint32_t* wabove = sc.hist + kSelWarps;  // per-warp counts of keys >= hi
+  const uint32_t* split = sc.hist + kSplitOffset;
+  const uint32_t hi = split[0], lo = max(split[1], 1u);
+  // pass 1: keys >= hi and keys in [lo, hi) (zero padding is below both);
+  // warp w takes the keys block_emit gives it, four at a time
+  const uint4* k4 = reinterpret_cast<const uint4*>(keys);
+  const int span = emit_span(P);
+  const int q0 = (warp * span) >> 2, q1 = (min(P, warp * span + span) + 3) >> 2;
+  int below_hi = 0, inb = 0, seen = 0;
+  auto tally = [&](uint32_t k) {
+    const int bh = minus_borrow(k, hi), bl = minus_borrow(k, lo);
+    below_hi -= bh;
+    inb += bl - bh;
+  };
+  for (int j = q0 + lane; j < q1; j += 32) {
+    const uint4 v = k4[j];
+    tally(v.x);
+    tally(v.y);
+    tally(v.z);
+    tally(v.w);
+    seen += 4;
+  }
+  int incl = inb;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += t;
+  }
+  const int wa = __reduce_add_sync(0xffffffffu, seen - below_hi);
+  if (lane == 31) wcnt[warp] = static_cast<uint32_t>(incl);
+  if (lane == 0) wabove[warp] = static_cast<uint32_t>(wa);
+  __syncthreads();
+  int at = incl - inb + warps_before(wcnt);
+  const int nb = warps_total(wcnt), A = warps_total(wabove);
+  const int my_above = static_cast<int>(wabove[warp]);
+  __syncthreads();
+  if (!(A < kk && kk <= A + nb && nb <= kSelCompCap)) return false;
+  const int my0 = at, my1 = at + inb;  // this thread's bucket keys in sc.comp
+  // pass 2: the bucket to sc.comp (in any order)
+  const uint32_t comp = smem_u32(sc.comp);
+  auto put = [&](uint32_t k) {
+    const bool in = k >= lo && k < hi;
+    st_shared_if(comp + 4u * static_cast<uint32_t>(at), k, in);
+    at += in ? 1 : 0;
+  };
+  for (int j = q0 + lane; j < q1; j += 32) {
+    const uint4 v = k4[j];
+    put(v.x);
+    put(v.y);
+    put(v.z);
+    put(v.w);
+  }
+  __syncthreads();
+  // Warps 0 .. kSearchWarps - 1 find T on the bucket, held in registers (zero
+  // past its end: zero is below every x counted); the other warps wait.
+  // Counts of keys >= x, for lo <= x <= hi, are A plus the bucket's keys >= x
+  // (for x > hi that gives A, an overcount still < kk, so every decision
+  // holds; below lo it gives A + #bucket, a lower bound, which only accepts).
+  uint32_t* res = sc.hist + 4 * kSelWarps;
+  if (warp < kSearchWarps) {
+    constexpr int kBk = kSelCompCap / (32 * kSearchWarps);
+    uint32_t bk[kBk];
+#pragma unroll
+    for (int i = 0; i < kBk; ++i) {
+      const int c = tid + i * 32 * kSearchWarps;
+      bk[i] = c < nb ? sc.comp[c] : 0u;
+    }
+    uint32_t* wc1 = sc.hist;
+    uint32_t* wc2 = sc.hist + kSearchWarps;
+    uint32_t* wc3 = sc.hist + 2 * kSearchWarps;
+    auto part_sum = [&](const uint32_t* part) {
+      return __reduce_add_sync(0xffffffffu, lane < kSearchWarps ? static_cast<int>(part[lane]) : 0);
+    };
+    auto count3 = [&](uint32_t x1, uint32_t x2, uint32_t x3, int& n1, int& n2, int& n3) {
+      int b1 = 0, b2 = 0, b3 = 0;
+#pragma unroll
+      for (int i = 0; i < kBk; ++i) {
+        b1 += minus_borrow(bk[i], x1);
+        b2 += minus_borrow(bk[i], x2);
+        b3 += minus_borrow(bk[i], x3);
+      }
+      b1 = __reduce_add_sync(0xffffffffu, kBk + b1);
+      b2 = __reduce_add_sync(0xffffffffu, kBk + b2);
+      b3 = __reduce_add_sync(0xffffffffu, kBk + b3);
+      if (lane == 0) {
+        wc1[warp] = static_cast<uint32_t>(b1);
+        wc2[warp] = static_cast<uint32_t>(b2);
+        wc3[warp] = static_cast<uint32_t>(b3);
+      }
+      search_sync();
+      n1 = A + part_sum(wc1);
+      n2 = A + part_sum(wc2);
+      n3 = A + part_sum(wc3);
+      search_sync();
+    };
+    // the bucket's keys agree with lo and hi - 1 above their first differing
+    // bit; below it T is found two bits a round (the largest 2-bit digit whose
+    // count reaches kk), stopping once exactly kk keys are >= T
+    const uint32_t hm1 = hi - 1u;
+    uint32_t T = lo;
+    int ge = -1;
+    if (lo != hm1) {
+      const int top = 31 - __clz(lo ^ hm1);
+      T = top == 31 ? 0u : (lo >> (top + 1)) << (top + 1);
+      for (int bit = top; bit >= 0; bit -= 2) {
+        const int sh = bit >= 1 ? bit - 1 : 0;
+        const uint32_t c1 = T | (1u << sh);
+        const uint32_t c2 = bit >= 1 ? T | (2u << sh) : c1;
+        const uint32_t c3 = bit >= 1 ? T | (3u << sh) : c1;
+        int n1, n2, n3;
+        count3(c1, c2, c3, n1, n2, n3);
+        uint32_t cand = 0u;
+        int c = -1;
+        if (n3 >= kk) {
+          cand = c3;
+          c = n3;
+        } else if (n2 >= kk) {
+          cand = c2;
+          c = n2;
+        } else if (n1 >= kk) {
+          cand = c1;
+          c = n1;
+        }
+        if (c >= 0) {
+          T = cand;
+          ge = c;
+          if (c == kk && cand >= lo) break;
+        }
+      }
+    }
+    if (ge == kk) {
+      if (tid == 0) {
+        res[0] = T - 1u;
+        res[1] = 0u;
+      }
+    } else {
+      int n1, n2, n3;
+      count3(T + 1u, T + 1u, T + 1u, n1, n2, n3);  // T < hi, so T + 1 <= hi
+      if (tid == 0) {
+        res[0] = T;
+        res[1] = static_cast<uint32_t>(kk - n1);
+      }
+    }
+  }
+  __syncthreads();
+  mask = ~0u;
+  prefix = res[0];
+  need = static_cast<int>(res[1]);
+  // block_emit's per-warp counts: keys > prefix are the warp's keys >= hi and
+  // its bucket keys > prefix (prefix >= lo - 1); keys == prefix matter only
+  // when need > 0, where prefix = T >= lo and they all lie in the bucket
+  int gt = 0, eq = 0;
+  for (int i = my0; i < my1; ++i) {
+    const uint32_t k = sc.comp[i];
+    gt += k > prefix ? 1 : 0;
+    eq += k == prefix ? 1 : 0;
+  }
+  gt = __reduce_add_sync(0xffffffffu, gt) + my_above;
+  eq = __reduce_add_sync(0xffffffffu, eq);
+  if (lane == 0) {
+    sc.warp_gt[warp] = static_cast<uint32_t>(gt);
+    sc.warp_eq[warp] = static_cast<uint32_t>(eq);
+  }
+  __syncthreads();
+  return true;
+}
+
+// block_emit's first pass: per warp, the keys > prefix and == prefix, to
+// sc.warp_gt and sc.warp_eq.
+template <typename KeyFn>
+__device__ void block_emit_counts(const KeyFn& key, int P, uint32_t prefix, uint32_t mask,
+                                  SelScratch& sc) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int span = (P + 32 * kSelWarps - 1) / (32 * kSelWarps) * 32;
+  const int span = emit_span(P);
   const int j0 = warp * span, j1 = min(P, j0 + span);
   int gt = 0, eq = 0;
-  for (int base = j0; base < j1; base += 32) {
-    const int j = base + lane;
-    const uint32_t k = (j < j1) ? (key(j) & mask) : 0u;
-    gt += __popc(__ballot_sync(0xffffffffu, j < j1 && k > prefix));
-    eq += __popc(__ballot_sync(0xffffffffu, j < j1 && k == prefix));
+  for (int base = j0; base < j1; base += 256) {
+    uint32_t k[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int j = base + 32 * u + lane;
+      k[u] = j < j1 ? key(j) & mask : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int j = base + 32 * u + lane;
+      gt += (j < j1 && k[u] > prefix) ? 1 : 0;
+      eq += (j < j1 && k[u] == prefix) ? 1 : 0;
+    }
   }
-  if (lane == 0) sc.warp_tot[warp] = (static_cast<long long>(gt) << 32) | eq;
+  gt = __reduce_add_sync(0xffffffffu, gt);
+  eq = __reduce_add_sync(0xffffffffu, eq);
+  if (lane == 0) {
+    sc.warp_gt[warp] = static_cast<uint32_t>(gt);
+    sc.warp_eq[warp] = static_cast<uint32_t>(eq);
+  }
   __syncthreads();
-  long long before = 0;
-  for (int w = 0; w < warp; ++w) before += sc.warp_tot[w];
-  int gt_before = static_cast<int>(before >> 32);
-  int eq_before = static_cast<int>(before & 0xffffffffll);
+}
+
+// Writes the selection in ascending page order to sel_row[0 .. kk) and its
+// bitmap to bits[0 .. ceil(P / 32)), given the per-warp counts in
+// sc.warp_gt / sc.warp_eq.  Warp w walks its range 256 keys at a time; the
+// counts of the warps before it place it.  skeys: the keys staged in shared
+// memory (zero-padded to a multiple of 4), or nullptr to read them by key().
+// Without a partial tie (no key equal to the prefix is left out) a page is
+// selected by its own key alone.
+template <typename KeyFn>
+__device__ void block_emit(const KeyFn& key, const uint32_t* skeys, int P, uint32_t prefix,
+                           uint32_t mask, int need, int32_t* sel_row, uint32_t* bits,
+                           SelScratch& sc) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int span = emit_span(P);
+  const int j0 = warp * span, j1 = min(P, j0 + span);
+  int gt_before = warps_before(sc.warp_gt);
+  int eq_before = warps_before(sc.warp_eq);
   const uint32_t lt = (1u << lane) - 1u;
-  for (int base = j0; base < j1; base += 32) {
-    const int j = base + lane;
-    const uint32_t k = (j < j1) ? (key(j) & mask) : 0u;
-    const bool is_gt = j < j1 && k > prefix, is_eq = j < j1 && k == prefix;
-    const uint32_t gtm = __ballot_sync(0xffffffffu, is_gt);
-    const uint32_t eqm = __ballot_sync(0xffffffffu, is_eq);
-    const int eq_rank = eq_before + __popc(eqm & lt);
-    const bool sel = is_gt || (is_eq && eq_rank < need);
-    const uint32_t selm = __ballot_sync(0xffffffffu, sel);
-    if (sel) sel_row[gt_before + __popc(gtm & lt) + min(eq_rank, need)] = j;
-    if (lane == 0) word_out(base >> 5, selm);
-    gt_before += __popc(gtm);
-    eq_before += __popc(eqm);
+  if (need == 0 || need == warps_total(sc.warp_eq)) {
+    // every key > prefix, and the keys == prefix all or none (need == 0 only
+    // with prefix = T - 1 for a T >= 1, so prefix + 1 does not wrap)
+    int at = gt_before + (need == 0 ? 0 : eq_before);
+    const uint32_t cut = need == 0 ? prefix + 1u : prefix;  // selected: key & mask >= cut
+    // lane l takes the 8 keys base + 8 l .. base + 8 l + 7: one count, one
+    // warp scan and one bitmap byte a lane per 256 keys
+    const int pad = 4 * static_cast<int>(ceil_div(P, 4));  // staged keys (zero-padded)
+    for (int base = j0; base < j1; base += 256) {
+      const int jb = base + 8 * lane;
+      uint32_t k[8];
+      if (skeys != nullptr) {
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        const uint4 a4 = jb + 4 <= pad ? *reinterpret_cast<const uint4*>(skeys + jb) : z;
+        const uint4 b4 = jb + 8 <= pad ? *reinterpret_cast<const uint4*>(skeys + jb + 4) : z;
+        k[0] = a4.x;
+        k[1] = a4.y;
+        k[2] = a4.z;
+        k[3] = a4.w;
+        k[4] = b4.x;
+        k[5] = b4.y;
+        k[6] = b4.z;
+        k[7] = b4.w;
+      } else {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) k[u] = jb + u < j1 ? key(jb + u) : 0u;
+      }
+      uint32_t m8 = 0u;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) m8 |= (jb + u < j1 && (k[u] & mask) >= cut) ? 1u << u : 0u;
+      const int c = __popc(m8);
+      int incl = c;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += t;
+      }
+      // bitmap word i of the 8: the bytes of lanes 4 i .. 4 i + 3
+      uint32_t w = m8 << (8 * (lane & 3));
+      w |= __shfl_xor_sync(0xffffffffu, w, 1);
+      w |= __shfl_xor_sync(0xffffffffu, w, 2);
+      st_global_if(bits + (base >> 5) + (lane >> 2), w, (lane & 3) == 0 && base + 8 * lane < j1);
+      int pos = at + incl - c;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const bool sel = (m8 >> u) & 1u;
+        st_global_if(sel_row + pos, static_cast<uint32_t>(jb + u), sel);
+        pos += sel ? 1 : 0;
+      }
+      at += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  } else {
+    for (int base = j0; base < j1; base += 32) {
+      const int j = base + lane;
+      const uint32_t k = (j < j1) ? (key(j) & mask) : 0u;
+      const bool is_gt = j < j1 && k > prefix, is_eq = j < j1 && k == prefix;
+      const uint32_t gtm = __ballot_sync(0xffffffffu, is_gt);
+      const uint32_t eqm = __ballot_sync(0xffffffffu, is_eq);
+      const int eq_rank = eq_before + __popc(eqm & lt);
+      const bool sel = is_gt || (is_eq && eq_rank < need);
+      const uint32_t selm = __ballot_sync(0xffffffffu, sel);
+      if (sel) sel_row[gt_before + __popc(gtm & lt) + min(eq_rank, need)] = j;
+      if (lane == 0) bits[base >> 5] = selm;
+      gt_before += __popc(gtm);
+      eq_before += __popc(eqm);
+    }
   }
   __syncthreads();  // the scratch may be reused
 }
@@ -234,13 +676,10 @@ __device__ void block_union(const WordFn& word, int G, int W32, int S, int n, in
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
-  if (lane == 0) sc.warp_tot[warp] = cnt;
+  if (lane == 0) sc.warp_gt[warp] = static_cast<uint32_t>(cnt);
   __syncthreads();
-  int before = 0, total = 0;
-  for (int w = 0; w < kSelWarps; ++w) {
-    before += (w < warp) ? static_cast<int>(sc.warp_tot[w]) : 0;
-    total += static_cast<int>(sc.warp_tot[w]);
-  }
+  int before = warps_before(sc.warp_gt);
+  const int total = warps_total(sc.warp_gt);
   for (int base = w0; base < w1; base += 32) {
     const int wi = base + lane;
     uint32_t hw[8];
@@ -275,7 +714,7 @@ __device__ void block_union(const WordFn& word, int G, int W32, int S, int n, in
 }
 
 // ---------------------------------------------------------------- kernels
-template <int D, bool F16>
+template <int D, bool F16, bool EXACT>
 __global__ void __launch_bounds__(kScoreWarps * 32) score_kernel(const ScoreArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t4 = lane & 3;
@@ -285,10 +724,10 @@ __global__ void __launch_bounds__(kScoreWarps * 32) score_kernel(const ScoreArgs
   griddep_wait();
   if (page0 >= a.P) return;
   uint32_t bq[D / 16][4];
-  load_q_pm<D>(a.q, a.q_sb, a.q_sh, b, kvh, a.G, lane, bq);
+  load_q_pm<D, EXACT>(a.q, a.q_sb, a.q_sh, b, kvh, a.G, lane, bq);
   const int64_t mbase = (static_cast<int64_t>(b) * a.Hkv + kvh) * a.P * D;
   float acc[4];
-  score_tile<D, F16>(bq, static_cast<const uint16_t*>(a.meta_max) + mbase,
+  score_tile<D, F16, EXACT>(bq, static_cast<const uint16_t*>(a.meta_max) + mbase,
                      static_cast<const uint16_t*>(a.meta_min) + mbase, page0, a.P, lane, acc);
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
@@ -315,24 +754,60 @@ __global__ void __launch_bounds__(kSelThreads) topk_kernel(const TopkArgs a) {
     for (int h = 1; h < a.group; ++h) s = __fadd_rn(s, __ldcg(r + static_cast<int64_t>(h) * a.P + j));
     return s;
   };
-  if constexpr (SMEM) {
-    for (int j = threadIdx.x; j < a.P; j += kSelThreads) s_keys[j] = score_key(score(j));
-    __syncthreads();
-  }
+  // a shorter sequence: its own pages only, and possibly fewer than kk kept
+  const int Pb = static_cast<int>(ceil_div(seq_len_of(a.lens, row / a.Hq, a.N), a.S));
+  const int kkb = min(a.kk, Pb);
   auto key = [&](int j) {
     if constexpr (SMEM) return s_keys[j];
     return score_key(score(j));
   };
-  uint32_t* bits = a.bitmaps + static_cast<int64_t>(row) * a.W32;
-  auto word_out = [&](int w, uint32_t v) { bits[w] = v; };
-  // a shorter sequence: its own pages only, and possibly fewer than kk kept
-  const int Pb = static_cast<int>(ceil_div(seq_len_of(a.lens, row / a.Hq, a.N), a.S));
-  const int kkb = min(a.kk, Pb);
   uint32_t prefix, mask;
   int need;
-  block_radix_select(key, Pb, kkb, sc, prefix, mask, need);
+  bool found = false;
+  if constexpr (SMEM) {
+    // Keys 0 .. Pb - 1 to shared memory, zero from Pb up to a multiple of 4
+    // (the sample bracket's vector passes).  With the sample bracket, warps 0
+    // and 1 pick its splitters from the score row meanwhile.
+    int r_hi = 0, r_lo = 0;
+    const bool sampled = Pb >= kSampleMinP && sample_ranks(kkb, Pb, r_hi, r_lo);
+    const int t0 = sampled ? 64 : 0, nt = kSelThreads - t0;
+    const int tid = static_cast<int>(threadIdx.x);
+    if (tid < t0) {
+      sample_splitter(r, a.P, a.group, Pb, tid < 32 ? r_hi : r_lo, sc.comp + 1024 * (tid >> 5),
+                      sc.hist + kSplitOffset + (tid >> 5));
+    } else if (a.group == 1 && (a.P & 3) == 0) {
+      // one score row: 16-byte loads, eight in flight a thread
+      const float4* r4 = reinterpret_cast<const float4*>(r);
+      const int n4 = a.P / 4;
+#pragma unroll 8
+      for (int j = tid - t0; j < n4; j += nt) {
+        const float4 v = __ldcg(r4 + j);
+        uint4 k = make_uint4(score_key(v.x), score_key(v.y), score_key(v.z), score_key(v.w));
+        if (4 * j + 3 >= Pb) {
+          k.x = 4 * j < Pb ? k.x : 0u;
+          k.y = 4 * j + 1 < Pb ? k.y : 0u;
+          k.z = 4 * j + 2 < Pb ? k.z : 0u;
+          k.w = 0u;
+        }
+        *reinterpret_cast<uint4*>(s_keys + 4 * j) = k;
+      }
+    } else {
+#pragma unroll 8
+      for (int j = tid - t0; j < a.P; j += nt) s_keys[j] = j < Pb ? score_key(score(j)) : 0u;
+      // past P (up to a multiple of 4): no thread stages there
+      if (tid - t0 < 3 && a.P + tid - t0 < 4 * static_cast<int>(ceil_div(Pb, 4)))
+        s_keys[a.P + tid - t0] = 0u;
+    }
+    __syncthreads();
+    if (sampled) found = block_sample_select(s_keys, Pb, kkb, sc, prefix, mask, need);
+  }
+  uint32_t* bits = a.bitmaps + static_cast<int64_t>(row) * a.W32;
+  if (!found) block_radix_select(key, Pb, kkb, sc, prefix, mask, need);
   int32_t* sel_row = a.selected + static_cast<int64_t>(row) * a.kk;
-  block_emit(key, Pb, prefix, mask, need, sel_row, word_out, sc);
+  if (!found) block_emit_counts(key, Pb, prefix, mask, sc);
+  const uint32_t* skeys = nullptr;
+  if constexpr (SMEM) skeys = s_keys;
+  block_emit(key, skeys, Pb, prefix, mask, need, sel_row, bits, sc);
   for (int w = static_cast<int>(ceil_div(Pb, 32)) + threadIdx.x; w < a.W32; w += kSelThreads)
     bits[w] = 0u;
   for (int i = kkb + threadIdx.x; i < a.kk; i += kSelThreads) sel_row[i] = -1;
@@ -657,16 +1132,23 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
 cudaError_t launch_score(int d, bool f16, const ScoreArgs& a, cudaStream_t s) {
   dim3 grid(static_cast<unsigned>(ceil_div(a.P, kScorePagesPerCta)), a.Hkv, a.B);
   dim3 block(kScoreWarps * 32);
-  if (d == 128) {
-    return f16 ? launch_pdl(score_kernel<128, true>, grid, block, 0, s, a)
-               : launch_pdl(score_kernel<128, false>, grid, block, 0, s, a);
+  if (a.exact) {
+    if (d == 128)
+      return f16 ? launch_pdl(score_kernel<128, true, true>, grid, block, 0, s, a)
+                 : launch_pdl(score_kernel<128, false, true>, grid, block, 0, s, a);
+    return f16 ? launch_pdl(score_kernel<64, true, true>, grid, block, 0, s, a)
+               : launch_pdl(score_kernel<64, false, true>, grid, block, 0, s, a);
   }
-  return f16 ? launch_pdl(score_kernel<64, true>, grid, block, 0, s, a)
-             : launch_pdl(score_kernel<64, false>, grid, block, 0, s, a);
+  if (d == 128) {
+    return f16 ? launch_pdl(score_kernel<128, true, false>, grid, block, 0, s, a)
+               : launch_pdl(score_kernel<128, false, false>, grid, block, 0, s, a);
+  }
+  return f16 ? launch_pdl(score_kernel<64, true, false>, grid, block, 0, s, a)
+             : launch_pdl(score_kernel<64, false, false>, grid, block, 0, s, a);
 }
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
-  const size_t key_bytes = sizeof(uint32_t) * static_cast<size_t>(a.P);
+  const size_t key_bytes = 16 * static_cast<size_t>(ceil_div(a.P, 4));  // zero-padded to 4
   if (key_bytes <= kTopkSmemKeyBytes) {
     cudaError_t e = cudaFuncSetAttribute(topk_kernel<true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,

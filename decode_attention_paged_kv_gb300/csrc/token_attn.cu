@@ -11,7 +11,7 @@
 //   out = (sum p_t v_t) / (sum p_t) over the selected tokens.
 // Warp w takes the w-th contiguous slice of the ascending token list, so its
 // V rows come in ascending order; lane l owns channels [c l, c (l + 1)),
-// c = d / 32, so a warp reads whole 2d-byte V rows.  Eight tokens' loads are
+// c = d / 32, so a warp reads whole 2d-byte V rows.  Sixteen tokens' loads are
 // in flight per warp.  The warps' sums are combined in warp order:
 // deterministic.  Bytes per row: kk V rows (d * 2 each) + kk indices and
 // scores + out.
@@ -25,7 +25,7 @@ namespace dkv {
 namespace {
 
 constexpr int kTokWarps = 8;
-constexpr int kTokUnroll = 8;
+constexpr int kTokUnroll = 16;
 
 template <int D, bool F16>
 __device__ __forceinline__ void load_v(const uint16_t* v, float (&x)[D / 32]) {

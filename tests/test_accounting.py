@@ -38,3 +38,11 @@ def test_full_bytes_workloads():
 def test_quant4_bytes():
     # 2 bytes in per value; 4 bits + 4 bytes of bounds per 64 values out
     assert acc.quant4_bytes(10, 128) == 10 * 256 + 10 * (64 + 8)
+
+
+def test_token_bytes():
+    # keeping every token with one head per group reads what the exact path reads
+    assert acc.token_bytes(2, 8, 8, 128, 1000, 1000) == acc.full_bytes(2, 8, 8, 128, 1000)
+    # GQA: K once per kv head, V rows once per q head
+    assert (acc.token_bytes(1, 32, 8, 128, 32768, 3276) ==
+            32 * 128 * 2 + 8 * 32768 * 128 * 2 + 32 * 3276 * 128 * 2 + 32 * 128 * 4)

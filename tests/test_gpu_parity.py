@@ -52,6 +52,8 @@ CASES = [
     Workload("unit-select-gqa8", B=2, Hq=16, Hkv=2, d=128, N=20000, top_k=50, kind="hot"),
     Workload("unit-select-mha-fp16", B=3, Hq=3, Hkv=3, d=64, N=16400, top_k=200, dtype="fp16"),
     Workload("unit-select-ties", B=2, Hq=8, Hkv=2, d=64, N=16384, top_k=77, kind="coarse"),
+    # exact score ties in the separate selection kernels (500 pages)
+    Workload("kernels-ties", B=2, Hq=8, Hkv=2, d=64, N=8000, top_k=77, kind="coarse"),
     # more work items than persistent CTAs (2 per SM): every CTA streams
     # several items back to back, exact and sparse
     Workload("multi-item-gqa", B=16, Hq=16, Hkv=8, d=128, N=8192, top_k=48, kind="hot"),

@@ -62,3 +62,24 @@ def test_token_topk_all_tokens_equals_full(dev, dkv):
     out = dkv.decode_attn_topk_tokens(q, K, V, w.N + 7)
     full = dkv.decode_attn_full(q, K, V)
     assert max_abs(out, full.double().cpu().numpy()) <= 1e-5
+
+
+def test_token_topk_exact_ties_take_lower_tokens(dev, dkv):
+    """K repeats with period 8, so the scores fall into 8 exactly tied classes
+    (identical rows give identical scores on both sides): the top-K is the
+    best classes whole and the lowest-index tokens of the class at the K-th
+    place, the same set as the oracle's."""
+    w = Workload("tok-ties", B=1, Hq=4, Hkv=1, d=128, N=6000, top_k=1000)
+    q, K, V = make_inputs(w, seed=85)
+    K = K[:, :, :8].repeat(1, 1, w.N // 8, 1).contiguous()
+    out, sel = dkv.decode_attn_topk_tokens(q.to(dev), K.to(dev), V.to(dev), w.top_k,
+                                           return_selected=True)
+    sel = sel.cpu().numpy()
+    qb, Kb, Vb = bits(q), bits(K), bits(V)
+    km, kx = oracle.meta(Kb, 1, 0)
+    r = oracle.scores(qb, km, kx, 0).reshape(-1, w.N)
+    for i in range(r.shape[0]):
+        order = sorted(range(w.N), key=lambda j: (-r[i, j], j))
+        assert sel[0, i].tolist() == sorted(order[:w.top_k]), f"head {i}"
+    ref = oracle.attention(qb, Kb, Vb, 1, 1.0 / math.sqrt(w.d), 0, sel=sel)
+    assert max_abs(out, ref) <= ATOL
