@@ -55,7 +55,16 @@ def parse_args():
                     help="override the workload's batch (small cases for ncu captures)")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the e2e, CPU-baseline, 1M-token head-wise and other-workload legs")
-    return ap.parse_args()
+    ap.add_argument("--legs", default="all",
+                    help="comma list of extra legs to run (e2e, group, paged, pagesize, tokens, "
+                         "cpu, headwise, others) or 'all'; for small profiling runs")
+    args = ap.parse_args()
+    legs = {"e2e", "group", "paged", "pagesize", "tokens", "cpu", "headwise", "others"}
+    args.legs = set() if args.no_extra else (legs if args.legs == "all" else set(args.legs.split(",")))
+    unknown = args.legs - legs
+    if unknown:
+        ap.error(f"unknown legs: {sorted(unknown)}")
+    return args
 
 
 # ------------------------------------------------------------------ helpers
@@ -740,18 +749,27 @@ def main():
         torch.cuda.set_device(local)
         torch.distributed.init_process_group("nccl")
     res, (q, K, V, w, widx, dev, stream) = run_dkv(args, rank, world, local)
-    if not args.no_extra and rank == 0:
-        res["e2e"] = e2e_leg(q, K, V, w, dev, stream, args.steps)
-        res["group_select"] = group_select_leg(q, K, V, w, dev, stream)
-        res["paged"] = paged_leg(q, K, V, w, dev, stream)
-        res["page_sizes"] = page_size_leg(q, K, V, w, dev, stream)
-        res["topk_tokens"] = token_leg(q, K, V, w, dev, stream)
-        res["cpu_baseline"] = cpu_baseline_leg(q, K, V, w)
+    if args.legs and rank == 0:
+        L = args.legs
+        if "e2e" in L:
+            res["e2e"] = e2e_leg(q, K, V, w, dev, stream, args.steps)
+        if "group" in L:
+            res["group_select"] = group_select_leg(q, K, V, w, dev, stream)
+        if "paged" in L:
+            res["paged"] = paged_leg(q, K, V, w, dev, stream)
+        if "pagesize" in L:
+            res["page_sizes"] = page_size_leg(q, K, V, w, dev, stream)
+        if "tokens" in L:
+            res["topk_tokens"] = token_leg(q, K, V, w, dev, stream)
+        if "cpu" in L:
+            res["cpu_baseline"] = cpu_baseline_leg(q, K, V, w)
         del q, K, V
         torch.cuda.empty_cache()
-        res["headwise_1m"] = headwise_leg(dev, stream)
-        res["other_workloads"] = [workload_leg(n, dev, stream)
-                                  for n in (WORKLOADS[1].name, WORKLOADS[4].name)]
+        if "headwise" in L:
+            res["headwise_1m"] = headwise_leg(dev, stream)
+        if "others" in L:
+            res["other_workloads"] = [workload_leg(n, dev, stream)
+                                      for n in (WORKLOADS[1].name, WORKLOADS[4].name)]
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:
