@@ -26,7 +26,7 @@ namespace {
 constexpr int kMetaThreads = 256;
 
 template <bool Q4>
-__global__ void __launch_bounds__(kMetaThreads, 2) meta_kernel(const MetaArgs a) {
+__global__ void __launch_bounds__(kMetaThreads, Q4 ? 4 : 2) meta_kernel(const MetaArgs a) {
   griddep_launch_dependents();
   griddep_wait();
   const int vpr = a.d / 8;  // 16-byte vectors per row

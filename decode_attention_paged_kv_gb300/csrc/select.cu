@@ -37,15 +37,19 @@ namespace {
 
 constexpr int kScoreWarps = 4;
 constexpr int kScorePagesPerCta = 16 * kScoreWarps;
-constexpr int kSelThreads = 1024;  // top-K and union CTAs
-constexpr int kSelWarps = kSelThreads / 32;
-static_assert(kSelWarps <= 32, "one warp partial a lane");
+// Top-K and union CTAs: up to kSelMaxThreads threads (the block functions
+// read the block's size at run time; shared scratch is laid out for the most).
+constexpr int kSelMaxThreads = 1024;
+constexpr int kSelMaxWarps = kSelMaxThreads / 32;
+static_assert(kSelMaxWarps <= 32, "one warp partial a lane");
+__device__ __forceinline__ int sel_threads() { return static_cast<int>(blockDim.x); }
+__device__ __forceinline__ int sel_warps() { return static_cast<int>(blockDim.x) >> 5; }
 
-// Per-warp partials part[0 .. kSelWarps) summed by every warp, one partial a
+// Per-warp partials part[0 .. warps) summed by every warp, one partial a
 // lane: over all warps, or over the warps before the calling one.
 __device__ __forceinline__ int warps_total(const uint32_t* part) {
   const int lane = threadIdx.x & 31;
-  return __reduce_add_sync(0xffffffffu, lane < kSelWarps ? static_cast<int>(part[lane]) : 0);
+  return __reduce_add_sync(0xffffffffu, lane < sel_warps() ? static_cast<int>(part[lane]) : 0);
 }
 __device__ __forceinline__ int warps_before(const uint32_t* part) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -133,8 +137,8 @@ __device__ __forceinline__ void score_tile(const uint32_t (&bq)[D / 16][4], cons
 constexpr int kSelCompCap = 4096;  // bucket keys the block top-K compacts
 struct SelScratch {
   uint32_t hist[256];
-  uint32_t warp_gt[kSelWarps];         // per-warp counts (emit: keys > prefix,
-  uint32_t warp_eq[kSelWarps];         // == prefix; union: pages)
+  uint32_t warp_gt[kSelMaxWarps];      // per-warp counts (emit: keys > prefix,
+  uint32_t warp_eq[kSelMaxWarps];      // == prefix; union: pages)
   uint32_t comp[kSelCompCap];
 };
 
@@ -153,7 +157,7 @@ __device__ __forceinline__ void st_shared_if(uint32_t addr, uint32_t v, bool c) 
                : "memory");
 }
 
-// Selection (block of kSelThreads) of the kk largest of P keys: the K-th
+// Selection (by the whole block) of the kk largest of P keys: the K-th
 // largest key found bit by bit below the keys' common prefix (radix selection
 // with 1-bit digits, as the per-head warp top-K), every pass one count over the
 // block, stopping as soon as exactly kk keys are >= the candidate.  On return:
@@ -164,11 +168,12 @@ __device__ void block_radix_select(const KeyFn& key, int P, int kk, SelScratch& 
                                    uint32_t& prefix, uint32_t& mask, int& need) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t* wcnt = sc.hist;            // per-warp counts
-  uint32_t* wmax = sc.hist + kSelWarps;
-  uint32_t* wmin = sc.hist + 2 * kSelWarps;
+  uint32_t* wmax = sc.hist + kSelMaxWarps;
+  uint32_t* wmin = sc.hist + 2 * kSelMaxWarps;
+  const int nt = sel_threads(), nw = sel_warps();
   // the keys' largest and smallest: the bits they all share are skipped
   uint32_t mx = 0u, mn = ~0u;
-  for (int j = tid; j < P; j += kSelThreads) {
+  for (int j = tid; j < P; j += nt) {
     const uint32_t k = key(j);
     mx = max(mx, k);
     mn = min(mn, k);
@@ -180,8 +185,8 @@ __device__ void block_radix_select(const KeyFn& key, int P, int kk, SelScratch& 
     wmin[warp] = mn;
   }
   __syncthreads();
-  const uint32_t kmax = __reduce_max_sync(0xffffffffu, lane < kSelWarps ? wmax[lane] : 0u);
-  const uint32_t kmin = __reduce_min_sync(0xffffffffu, lane < kSelWarps ? wmin[lane] : ~0u);
+  const uint32_t kmax = __reduce_max_sync(0xffffffffu, lane < nw ? wmax[lane] : 0u);
+  const uint32_t kmin = __reduce_min_sync(0xffffffffu, lane < nw ? wmin[lane] : ~0u);
   __syncthreads();
   // keys >= x over the block (four partial sums a thread, then warps in order)
   auto block_sum = [&](int mine) {
@@ -195,15 +200,15 @@ __device__ void block_radix_select(const KeyFn& key, int P, int kk, SelScratch& 
   auto count_ge = [&](uint32_t x) {
     int c0 = 0, c1 = 0, c2 = 0, c3 = 0;
     int j = tid;
-    for (; j + 3 * kSelThreads < P; j += 4 * kSelThreads) {
+    for (; j + 3 * nt < P; j += 4 * nt) {
       c0 -= minus_borrow(key(j), x);
-      c1 -= minus_borrow(key(j + kSelThreads), x);
-      c2 -= minus_borrow(key(j + 2 * kSelThreads), x);
-      c3 -= minus_borrow(key(j + 3 * kSelThreads), x);
+      c1 -= minus_borrow(key(j + nt), x);
+      c2 -= minus_borrow(key(j + 2 * nt), x);
+      c3 -= minus_borrow(key(j + 3 * nt), x);
     }
-    for (; j < P; j += kSelThreads) c0 -= minus_borrow(key(j), x);
+    for (; j < P; j += nt) c0 -= minus_borrow(key(j), x);
     const int below = (c0 + c1) + (c2 + c3);
-    return block_sum(max(static_cast<int>(ceil_div(P - tid, kSelThreads)), 0) - below);
+    return block_sum(max(static_cast<int>(ceil_div(P - tid, nt)), 0) - below);
   };
   // Once the keys that agree with the bits fixed so far (the bucket) are few,
   // they are copied to sc.comp; counts are then `base` (keys above the bucket)
@@ -211,8 +216,8 @@ __device__ void block_radix_select(const KeyFn& key, int P, int kk, SelScratch& 
   int ncomp = -1, base = 0;
   auto count_comp = [&](uint32_t x) {
     int c = 0;
-    for (int j = tid; j < ncomp; j += kSelThreads) c -= minus_borrow(sc.comp[j], x);
-    return base + block_sum(max(static_cast<int>(ceil_div(ncomp - tid, kSelThreads)), 0) - c);
+    for (int j = tid; j < ncomp; j += nt) c -= minus_borrow(sc.comp[j], x);
+    return base + block_sum(max(static_cast<int>(ceil_div(ncomp - tid, nt)), 0) - c);
   };
   uint32_t T;
   int ge = -1;
@@ -229,7 +234,7 @@ __device__ void block_radix_select(const KeyFn& key, int P, int kk, SelScratch& 
         const int sh = bit + 1;
         auto in_bucket = [&](uint32_t k) { return sh == 32 || (k >> sh) == (T >> sh); };
         int mine = 0;
-        for (int j = tid; j < P; j += kSelThreads) mine += in_bucket(key(j)) ? 1 : 0;
+        for (int j = tid; j < P; j += nt) mine += in_bucket(key(j)) ? 1 : 0;
         int incl = mine;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -240,7 +245,7 @@ __device__ void block_radix_select(const KeyFn& key, int P, int kk, SelScratch& 
         __syncthreads();
         int at = incl - mine + warps_before(wcnt);
         ncomp = warps_total(wcnt);
-        for (int j = tid; j < P; j += kSelThreads) {
+        for (int j = tid; j < P; j += nt) {
           const uint32_t k = key(j);
           if (in_bucket(k)) sc.comp[at++] = k;
         }
@@ -273,7 +278,7 @@ __device__ void block_radix_select(const KeyFn& key, int P, int kk, SelScratch& 
 
 // Warp w of block_emit takes pages [w span, (w + 1) span).
 __device__ __forceinline__ int emit_span(int P) {
-  return (P + 32 * kSelWarps - 1) / (32 * kSelWarps) * 32;
+  return (P + 32 * sel_warps() - 1) / (32 * sel_warps()) * 32;
 }
 
 constexpr int kSampleMinP = 4096;
@@ -339,7 +344,7 @@ __device__ void sample_splitter(const float* r, int64_t rs, int group, int P, in
 }
 
 // Where the two splitters sit in SelScratch::hist (hi, then lo).
-constexpr int kSplitOffset = 2 * kSelWarps;
+constexpr int kSplitOffset = 2 * kSelMaxWarps;
 
 // Warps that search the sample bracket's bucket (a named barrier among them).
 constexpr int kSearchWarps = 8;
@@ -366,7 +371,7 @@ __device__ bool block_sample_select(const uint32_t* keys, int P, int kk, SelScra
                                     uint32_t& prefix, uint32_t& mask, int& need) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t* wcnt = sc.hist;               // per-warp bucket counts
-  uint32_t* wabove = sc.hist + kSelWarps;  // per-warp counts of keys >= hi
+  uint32_t* wabove = sc.hist + kSelMaxWarps;  // per-warp counts of keys >= hi
   const uint32_t* split = sc.hist + kSplitOffset;
   const uint32_t hi = split[0], lo = max(split[1], 1u);
   // pass 1: keys >= hi and keys in [lo, hi) (zero padding is below both);
@@ -424,7 +429,7 @@ __device__ bool block_sample_select(const uint32_t* keys, int P, int kk, SelScra
   // Counts of keys >= x, for lo <= x <= hi, are A plus the bucket's keys >= x
   // (for x > hi that gives A, an overcount still < kk, so every decision
   // holds; below lo it gives A + #bucket, a lower bound, which only accepts).
-  uint32_t* res = sc.hist + 4 * kSelWarps;
+  uint32_t* res = sc.hist + 4 * kSelMaxWarps;
   if (warp < kSearchWarps) {
     constexpr int kBk = kSelCompCap / (32 * kSearchWarps);
     uint32_t bk[kBk];
@@ -660,7 +665,7 @@ template <typename WordFn>
 __device__ void block_union(const WordFn& word, int G, int W32, int S, int n, int2* out,
                             int* count_out, SelScratch& sc) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int span = (W32 + 32 * kSelWarps - 1) / (32 * kSelWarps) * 32;  // words per warp
+  const int span = (W32 + 32 * sel_warps() - 1) / (32 * sel_warps()) * 32;  // words per warp
   const int w0 = warp * span, w1 = min(W32, w0 + span);
   const int msub = S / kPage, last = static_cast<int>(ceil_div(n, S)) - 1;
   auto pages_of = [&](uint32_t u, int wi) {  // cache pages of word wi's selection pages
@@ -739,7 +744,7 @@ __global__ void __launch_bounds__(kScoreWarps * 32) score_kernel(const ScoreArgs
 }
 
 template <bool SMEM>
-__global__ void __launch_bounds__(kSelThreads) topk_kernel(const TopkArgs a) {
+__global__ void __launch_bounds__(kSelMaxThreads) topk_kernel(const TopkArgs a) {
   extern __shared__ uint32_t s_keys[];
   __shared__ SelScratch sc;
   const int row = blockIdx.x;
@@ -770,7 +775,7 @@ __global__ void __launch_bounds__(kSelThreads) topk_kernel(const TopkArgs a) {
     // and 1 pick its splitters from the score row meanwhile.
     int r_hi = 0, r_lo = 0;
     const bool sampled = Pb >= kSampleMinP && sample_ranks(kkb, Pb, r_hi, r_lo);
-    const int t0 = sampled ? 64 : 0, nt = kSelThreads - t0;
+    const int t0 = sampled ? 64 : 0, nt = sel_threads() - t0;
     const int tid = static_cast<int>(threadIdx.x);
     if (tid < t0) {
       sample_splitter(r, a.P, a.group, Pb, tid < 32 ? r_hi : r_lo, sc.comp + 1024 * (tid >> 5),
@@ -808,12 +813,54 @@ __global__ void __launch_bounds__(kSelThreads) topk_kernel(const TopkArgs a) {
   const uint32_t* skeys = nullptr;
   if constexpr (SMEM) skeys = s_keys;
   block_emit(key, skeys, Pb, prefix, mask, need, sel_row, bits, sc);
-  for (int w = static_cast<int>(ceil_div(Pb, 32)) + threadIdx.x; w < a.W32; w += kSelThreads)
+  for (int w = static_cast<int>(ceil_div(Pb, 32)) + threadIdx.x; w < a.W32; w += sel_threads())
     bits[w] = 0u;
-  for (int i = kkb + threadIdx.x; i < a.kk; i += kSelThreads) sel_row[i] = -1;
+  for (int i = kkb + threadIdx.x; i < a.kk; i += sel_threads()) sel_row[i] = -1;
 }
 
-__global__ void __launch_bounds__(kSelThreads) union_kernel(const UnionArgs a) {
+// One warp per (b, h) row of at most kUnitMaxP keys: the row's scores (summed
+// over the group's rows, head by head in order, as topk_kernel) become keys in
+// the warp's shared-memory slot, the warp top-K of the per-unit kernel selects
+// (keys in registers), and the warp writes the ascending row and the bitmap.
+constexpr int kTopkWarpRows = 8;
+__global__ void __launch_bounds__(kTopkWarpRows * 32) topk_warp_kernel(const TopkArgs a) {
+  extern __shared__ uint32_t s_slots[];
+  griddep_launch_dependents();
+  griddep_wait();  // the scores come from the previous kernel
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kTopkWarpRows + warp;
+  if (row >= a.rows) return;
+  const int Pr = static_cast<int>(ceil_div(a.P, 32)) * 32;
+  uint32_t* keys = s_slots + warp * (Pr + kSelBitmapWords);
+  uint32_t* bm = keys + Pr;
+  const int r0 = row - (row % a.Hq) % a.group;
+  const float* r = a.scores + static_cast<int64_t>(r0) * a.P;
+  const int Pb = static_cast<int>(ceil_div(seq_len_of(a.lens, row / a.Hq, a.N), a.S));
+  const int kkb = min(a.kk, Pb);
+  uint32_t mx = 0u, mn = ~0u;
+#pragma unroll 8
+  for (int j = lane; j < Pb; j += 32) {
+    float x = __ldcg(r + j);
+    for (int h = 1; h < a.group; ++h) x = __fadd_rn(x, __ldcg(r + static_cast<int64_t>(h) * a.P + j));
+    const uint32_t k = score_key(x);
+    keys[j] = k;
+    mx = max(mx, k);
+    mn = min(mn, k);
+  }
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  __syncwarp();
+  warp_topk_head([keys](int j) { return keys[j]; }, Pb, kkb, bm, mx, mn);
+  __syncwarp();
+  const int W = static_cast<int>(ceil_div(Pb, 32));
+  uint32_t* bits = a.bitmaps + static_cast<int64_t>(row) * a.W32;
+  int32_t* sel_row = a.selected + static_cast<int64_t>(row) * a.kk;
+  warp_emit_row(bm, W, sel_row, bits);
+  for (int w = W + lane; w < a.W32; w += 32) bits[w] = 0u;
+  for (int i = kkb + lane; i < a.kk; i += 32) sel_row[i] = -1;
+}
+
+__global__ void __launch_bounds__(kSelMaxThreads) union_kernel(const UnionArgs a) {
   __shared__ SelScratch sc;
   griddep_launch_dependents();
   griddep_wait();  // the bitmaps come from the previous kernel
@@ -1148,15 +1195,27 @@ cudaError_t launch_score(int d, bool f16, const ScoreArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
+  if (a.P <= kUnitMaxP) {  // a warp a row, keys in registers
+    const size_t smem = sizeof(uint32_t) * kTopkWarpRows *
+                        (static_cast<size_t>(ceil_div(a.P, 32)) * 32 + kSelBitmapWords);
+    cudaError_t e = cudaFuncSetAttribute(topk_warp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    return launch_pdl(topk_warp_kernel, dim3(static_cast<unsigned>(ceil_div(a.rows, kTopkWarpRows))),
+                      dim3(kTopkWarpRows * 32), smem, s, a);
+  }
   const size_t key_bytes = 16 * static_cast<size_t>(ceil_div(a.P, 4));  // zero-padded to 4
   if (key_bytes <= kTopkSmemKeyBytes) {
     cudaError_t e = cudaFuncSetAttribute(topk_kernel<true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kTopkSmemKeyBytes));
     if (e != cudaSuccess) return e;
-    return launch_pdl(topk_kernel<true>, dim3(a.rows), dim3(kSelThreads), key_bytes, s, a);
+    // rows long enough for the sample bracket get 1024 threads; shorter rows
+    // 256 (their passes are short, and fewer warps meet at each barrier)
+    const int threads = a.P >= kSampleMinP ? kSelMaxThreads : 256;
+    return launch_pdl(topk_kernel<true>, dim3(a.rows), dim3(threads), key_bytes, s, a);
   }
-  return launch_pdl(topk_kernel<false>, dim3(a.rows), dim3(kSelThreads), 0, s, a);
+  return launch_pdl(topk_kernel<false>, dim3(a.rows), dim3(kSelMaxThreads), 0, s, a);
 }
 
 size_t unit_select_smem(int d, int G, int P) {
@@ -1178,7 +1237,7 @@ cudaError_t launch_unit_select(int d, bool f16, const UnitSelectArgs& a, const C
 }
 
 cudaError_t launch_union(const UnionArgs& a, int units, cudaStream_t s) {
-  return launch_pdl(union_kernel, dim3(units), dim3(kSelThreads), 0, s, a);
+  return launch_pdl(union_kernel, dim3(units), dim3(256), 0, s, a);
 }
 
 }  // namespace dkv
