@@ -626,9 +626,12 @@ def workload_leg(name, dev, stream, reps=10):
     return res
 
 
-def e2e_leg(q, K, V, w, dev, stream, steps):
+def e2e_leg(q, K, V, w, dev, stream, steps, chunks=8):
     """The same step through the public API with host inputs: every step copies
-    q, K, V from pinned host memory and reads the outputs back."""
+    q, K, V from pinned host memory and reads the outputs back.  The batch goes
+    in `chunks` parts: a copy stream brings part c + 1 over while the compute
+    stream runs part c (meta + exact + sparse on its sequences) and copies its
+    outputs back, so only the last part's compute is not hidden by the copy."""
     import decode_attention_paged_kv_gb300 as dkv
 
     hq = q.cpu().pin_memory()
@@ -645,18 +648,31 @@ def e2e_leg(q, K, V, w, dev, stream, steps):
                          dtype=torch.uint8, device=dev)
     of, osl = torch.empty(w.B, w.Hq, w.d, device=dev), torch.empty(w.B, w.Hq, w.d, device=dev)
     sel = torch.empty(w.B, w.Hq, kk, dtype=torch.int32, device=dev)
+    copy_stream = torch.cuda.Stream(device=dev)
+    bounds = [(w.B * c) // chunks for c in range(chunks + 1)]
+    parts = [(b0, b1) for b0, b1 in zip(bounds[:-1], bounds[1:]) if b1 > b0]
 
     def step():
-        dq.copy_(hq, non_blocking=True)
-        dK.copy_(hK, non_blocking=True)
-        dV.copy_(hV, non_blocking=True)
-        meta = dkv.kv_meta_build(dK)
-        dkv.decode_attn_full(dq, dK, dV, out=of, workspace=ws_full)
-        dkv.decode_attn_select(dq, dK, dV, meta, w.top_k, out=osl, selected=sel,
-                               workspace=ws_sel)
-        ho.copy_(of, non_blocking=True)
-        hs.copy_(osl, non_blocking=True)
-        hsel.copy_(sel, non_blocking=True)
+        copy_stream.wait_stream(stream)  # the previous step is done with the buffers
+        ready = []
+        with torch.cuda.stream(copy_stream):
+            for b0, b1 in parts:
+                dq[b0:b1].copy_(hq[b0:b1], non_blocking=True)
+                dK[b0:b1].copy_(hK[b0:b1], non_blocking=True)
+                dV[b0:b1].copy_(hV[b0:b1], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(copy_stream)
+                ready.append(ev)
+        for (b0, b1), ev in zip(parts, ready):
+            stream.wait_event(ev)
+            qc, Kc, Vc = dq[b0:b1], dK[b0:b1], dV[b0:b1]
+            meta = dkv.kv_meta_build(Kc)
+            dkv.decode_attn_full(qc, Kc, Vc, out=of[b0:b1], workspace=ws_full)
+            dkv.decode_attn_select(qc, Kc, Vc, meta, w.top_k, out=osl[b0:b1], selected=sel[b0:b1],
+                                   workspace=ws_sel)
+            ho[b0:b1].copy_(of[b0:b1], non_blocking=True)
+            hs[b0:b1].copy_(osl[b0:b1], non_blocking=True)
+            hsel[b0:b1].copy_(sel[b0:b1], non_blocking=True)
 
     for _ in range(2):
         step()
@@ -672,7 +688,8 @@ def e2e_leg(q, K, V, w, dev, stream, steps):
     h2d = (hq.numel() * 2 + hK.numel() * 2 + hV.numel() * 2)
     d2h = ho.numel() * 4 + hs.numel() * 4 + hsel.numel() * 4
     return {"value": round(w.B / (ms * 1e-3), 1), "unit": "queries/s", "ms_per_step": round(ms, 4),
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "pipeline": f"{len(parts)} batch parts, copy of part c + 1 under compute of part c"}
 
 
 # ------------------------------------------------------------------ CPU oracle
