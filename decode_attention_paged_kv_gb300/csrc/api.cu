@@ -41,6 +41,7 @@ struct WsLayout {
   size_t bitmaps = 0;    // sparse: [B, Hq, W32] u32 (fallback selection only)
   size_t union_list = 0; // sparse: [B * Hkv, union_stride] (page, head mask)
   size_t union_count = 0;  // sparse: [B * Hkv] int32
+  size_t unit_ready = 0;   // sparse: [B * Hkv] u32 (per-unit selection only)
   size_t total = 0;
   int n_chunks = 0, pages_per_chunk = 0, kk = 0, W32 = 0, union_stride = 0;
   int64_t n_items = 0;
@@ -87,6 +88,8 @@ WsLayout layout_for(const dkv_params& p, int top_k) {
     off = align_up(off + 8 * static_cast<size_t>(units) * L.union_stride);
     L.union_count = off;
     off = align_up(off + sizeof(int32_t) * units);
+    L.unit_ready = off;
+    off = align_up(off + sizeof(uint32_t) * units);
   }
   L.part_ml = off;
   off = align_up(off + sizeof(float) * 2 * rows * L.n_chunks);
@@ -479,6 +482,9 @@ dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_
     ua.S = p->page_size;
     ua.status = a.status;
     ua.wait_limit_ns = a.wait_limit_ns;
+    // the attention takes each unit's items once its union is written
+    ua.unit_ready = reinterpret_cast<uint32_t*>(ws + L.unit_ready);
+    a.unit_ready = ua.unit_ready;
     CUtensorMap mmx, mmn;
     if (!encode_meta_map(&mmx, p, meta_max, f16, 64) || !encode_meta_map(&mmn, p, meta_min, f16, 64))
       return DKV_ERR_CUDA;

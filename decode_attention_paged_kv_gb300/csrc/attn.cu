@@ -390,7 +390,12 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
     prefetch_tensormap(&mv);
   }
   griddep_launch_dependents();
-  griddep_wait();  // q, K, V, bitmaps and the work counter come from earlier kernels
+  // q, K, V, the selection and the work counter come from earlier kernels.
+  // With per-unit ready flags the sparse path instead waits for each unit's
+  // selection as it takes the unit's items (the selection kernel lets this
+  // grid start only once every earlier kernel has finished).
+  const bool unit_flags = SPARSE && a.unit_ready != nullptr;
+  if (!unit_flags) griddep_wait();
   __syncthreads();
 
   if (warp == kConsumerWarps) {
@@ -432,11 +437,23 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
         b = unit / a.Hkv;
         first = chunk * a.pages_per_chunk;
         if constexpr (SPARSE) {
-          const int count = a.union_count[unit];
+          if (unit_flags) {
+            int rdy = 1;
+            if (lane == 0) rdy = flag_wait_bounded(a.unit_ready + unit, a.wait_limit_ns, abort_flag);
+            if (!__shfl_sync(0xffffffffu, rdy, 0)) {
+              if (lane == 0 && *abort_flag == 0) {
+                set_status(a.status, kStatusTimeout);
+                *abort_flag = 1;
+              }
+              item = -1;  // stop: publish the end of work
+              break;
+            }
+          }
+          const int count = __ldcg(a.union_count + unit);
           n = max(0, min(count - first, a.pages_per_chunk));
           if (n == 0) continue;
           const int2* src = a.union_list + static_cast<int64_t>(unit) * a.union_stride + first;
-          for (int j = lane; j < n; j += 32) list[j] = src[j];
+          for (int j = lane; j < n; j += 32) list[j] = __ldcg(src + j);
           __syncwarp();
         } else {
           // (with per-sequence lengths, chunks past the sequence are skipped)
@@ -599,6 +616,9 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
         atomicExch(a.exit_counter, 0u);
       }
     }
+    // The grid ends only after the selection grid has (so the kernels after
+    // this one, which wait for this grid alone, see every selection output).
+    if (unit_flags) griddep_wait();
     return;
   }
 

@@ -90,6 +90,33 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// A flag one kernel publishes for another running alongside it: a release
+// store after the data it guards, an acquire load before reading that data.
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Wait until *flag is non-zero.  Gives up (returns false) like
+// mbar_wait_bounded: after `limit_ns`, at once when limit_ns == 0, or when
+// *abort becomes non-zero.
+__device__ __forceinline__ bool flag_wait_bounded(const uint32_t* flag, uint64_t limit_ns,
+                                                  const volatile int* abort_flag) {
+  if (limit_ns == 0) return false;
+  if (ld_acquire_gpu(flag) != 0u) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    __nanosleep(100);
+    if (ld_acquire_gpu(flag) != 0u) return true;
+    if (abort_flag != nullptr && *abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
 // ---------------------------------------------------------------- TMA
 // Tiled tensor copy global -> shared, 5-D coordinates, completion counted in
 // bytes on `bar`.

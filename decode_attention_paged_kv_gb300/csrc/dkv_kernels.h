@@ -92,6 +92,10 @@ struct AttnArgs {
   const int2* union_list;      // [B * Hkv, union_stride]
   const int* union_count;      // [B * Hkv]
   int union_stride;
+  // Per (batch, kv head): non-zero once the selection kernel has written that
+  // unit's union.  When set, the kernel starts alongside the selection grid
+  // and waits unit by unit; nullptr: it waits for the whole previous grid.
+  const uint32_t* unit_ready;  // [B * Hkv] or nullptr
   Q4View k4, v4;               // 4-bit caches (the dense path uses the tensor maps)
   // paged caches: page j of batch entry b is pool block bt[b * bts + j] (the
   // tensor maps then view the pool); nullptr for a [B, Hkv, N, d] cache
@@ -164,6 +168,7 @@ struct UnitSelectArgs {
   int2* union_list;            // [B * Hkv, union_stride]
   int* union_count;            // [B * Hkv]
   int union_stride;
+  uint32_t* unit_ready;        // [B * Hkv] or nullptr: set once a unit's union is written
   int group;                   // 1: one selection per kv head group (summed scores)
   const int32_t* lens;         // per-sequence lengths [B] or nullptr; N = the longest
   int N;

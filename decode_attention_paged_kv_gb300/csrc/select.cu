@@ -950,9 +950,16 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
     prefetch_tensormap(&mmx);
     prefetch_tensormap(&mmn);
   }
-  griddep_launch_dependents();
   griddep_wait();
+  // The attention grid may start as soon as every CTA here has passed this
+  // point, and then reads this unit's ready flag: clear it first (the
+  // previous call's attention has finished with it once the wait returns).
+  if (threadIdx.x == 0 && a.unit_ready != nullptr) {
+    a.unit_ready[unit] = 0u;
+    __threadfence();
+  }
   __syncthreads();
+  griddep_launch_dependents();
 
   if (warp == kUnitConsumers) {
     // ------------------------------------------------------------ producer
@@ -1064,7 +1071,13 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
   }
   unit_consumers_sync();
   if (*abort_flag) {
-    if (threadIdx.x == 0) a.union_count[unit] = 0;  // gather nothing for this unit
+    if (threadIdx.x == 0) {
+      a.union_count[unit] = 0;  // gather nothing for this unit
+      if (a.unit_ready != nullptr) {
+        __threadfence();
+        st_release_gpu(a.unit_ready + unit, 1u);
+      }
+    }
     return;
   }
 
@@ -1170,7 +1183,19 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
         put(wi * 32 + bit, m);
       }
     }
-    if (threadIdx.x == 0) a.union_count[unit] = count;
+    if (a.unit_ready != nullptr) {
+      // publish the unit: every writer's list entries, then the count, then
+      // the flag the attention kernel waits on
+      __threadfence();
+      union_sync();
+      if (threadIdx.x == 0) {
+        a.union_count[unit] = count;
+        __threadfence();
+        st_release_gpu(a.unit_ready + unit, 1u);
+      }
+    } else if (threadIdx.x == 0) {
+      a.union_count[unit] = count;
+    }
   }
 }
 
