@@ -185,6 +185,19 @@ def union_tokens(sel: torch.Tensor, w: Workload, S: int = 0) -> int:
     return int((mask.long() * toks).sum().item())
 
 
+def cache_tokens(sel: torch.Tensor, w: Workload, S: int) -> int:
+    """Valid tokens of the unique 16-token cache pages that hold the selected
+    pages of S < 16 tokens, per (batch, kv head)."""
+    P16 = (w.N + 15) // 16
+    B, Hq, kk = sel.shape
+    mask = torch.zeros(B, w.Hkv, P16, dtype=torch.bool, device=sel.device)
+    grp = (sel.view(B, w.Hkv, w.G * kk).long() * S) // 16
+    mask.scatter_(2, grp, True)
+    toks = torch.full((P16,), 16, dtype=torch.int64, device=sel.device)
+    toks[-1] = w.N - (P16 - 1) * 16
+    return int((mask.long() * toks).sum().item())
+
+
 # ------------------------------------------------------------------ GPU arm
 def run_dkv(args, rank, world, local):
     import decode_attention_paged_kv_gb300 as dkv
@@ -409,16 +422,18 @@ def paged_leg(q, K, V, w, dev, stream, reps=10):
 
 
 def page_size_leg(q, K, V, w, dev, stream, reps=10):
-    """Selection page sizes S = 16, 32, 64 ("TinyServe" page-size variants) on
-    the bench workload at the same token budget (K = budget / S pages):
-    metadata build and select, 10 back-to-back calls each."""
+    """Selection page sizes S = 4, 8, 16, 32, 64 ("TinyServe" page-size
+    variants) on the bench workload at the same token budget (K = budget / S
+    pages): metadata build and select, 10 back-to-back calls each.  Pages of 4
+    or 8 tokens are read as the 16-token cache pages holding them
+    (cache_tokens_read); the roofline counts the selected pages' tokens."""
     import decode_attention_paged_kv_gb300 as dkv
     from decode_attention_paged_kv_gb300 import accounting as acc
 
     budget = w.top_k * w.S
     peak, _ = peaks()
     res = {"workload": w.name, "token_budget": budget, "timing": f"{reps} back-to-back calls"}
-    for S in (16, 32, 64):
+    for S in (4, 8, 16, 32, 64):
         kk = budget // S
         P = (w.N + S - 1) // S
         ws = torch.zeros(dkv.workspace_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, kk, page_size=S),
@@ -450,6 +465,8 @@ def page_size_leg(q, K, V, w, dev, stream, reps=10):
                        "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
                        "frac_of_measured_hbm": round(gbs / peak, 4)}
         r["gathered_tokens"] = union_tokens(sel, w, S)
+        if S < 16:
+            r["cache_tokens_read"] = cache_tokens(sel, w, S)
         res[f"S{S}"] = r
         del meta, ws
     return res

@@ -64,7 +64,10 @@ WsLayout layout_for(const dkv_params& p, int top_k) {
     L.W32 = static_cast<int>(ceil_div(P, 32));
     // the union list holds cache pages: a selection page is S / 16 of them
     const int64_t union_sel = (static_cast<int64_t>(G) * L.kk < P) ? G * L.kk : P;
-    const int64_t union_max = std::min(union_sel * (p.page_size / dkv::kPage), P16);
+    // (pages below 16 tokens: each selected page lies in one cache page)
+    const int64_t union_max =
+        std::min(p.page_size < dkv::kPage ? union_sel : union_sel * (p.page_size / dkv::kPage),
+                 P16);
     L.union_stride = static_cast<int>(union_max);
     L.pages_per_chunk = dkv::select_pages_per_chunk(union_max, d);
     if (L.pages_per_chunk > dkv::kMaxSelectList) L.ok = false;
@@ -118,9 +121,10 @@ dkv_status check_params(const dkv_params* p) {
     return DKV_ERR_SHAPE;
   if (p->num_q_heads % p->num_kv_heads != 0) return DKV_ERR_SHAPE;
   if (p->head_dim != 64 && p->head_dim != 128) return DKV_ERR_UNSUPPORTED;
-  // metadata / selection pages of 16, 32 or 64 tokens (the cache's pages are 16)
-  if (p->page_size != dkv::kPage && p->page_size != 2 * dkv::kPage &&
-      p->page_size != 4 * dkv::kPage)
+  // metadata / selection pages of 4, 8, 16, 32 or 64 tokens (the cache's pages
+  // are 16: a smaller selection page is a quarter or half of one)
+  if (p->page_size != 4 && p->page_size != 8 && p->page_size != dkv::kPage &&
+      p->page_size != 2 * dkv::kPage && p->page_size != 4 * dkv::kPage)
     return DKV_ERR_UNSUPPORTED;
   if (p->num_q_heads / p->num_kv_heads > 8) return DKV_ERR_UNSUPPORTED;
   if (p->batch > 65535 || p->num_kv_heads > 65535) return DKV_ERR_SHAPE;  // grid limits
@@ -450,11 +454,12 @@ dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_
 
   dkv::AttnArgs a = attn_args(p, q, L, ws);
   if (!cache_views(p, K, V, &mk, &mv, &a)) return DKV_ERR_CUDA;
+  a.sub_log2 = p->page_size == 4 ? 2 : (p->page_size == 8 ? 1 : 0);
   a.union_list = ulist;
   a.union_count = ucount;
   a.union_stride = L.union_stride;
 
-  if (P >= kUnitSelectMinP && P <= dkv::kUnitMaxP &&
+  if (p->page_size >= dkv::kPage && P >= kUnitSelectMinP && P <= dkv::kUnitMaxP &&
       dkv::unit_select_smem(p->head_dim, G, P) <= static_cast<size_t>(kUnitSelectSmemLimit)) {
     // Long contexts: one CTA per (batch, kv head) scores its pages, selects
     // each head's top-K and builds the union list.  (Shorter ones have too

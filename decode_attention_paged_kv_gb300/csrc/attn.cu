@@ -717,13 +717,22 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
       }
 
       // Online softmax (log2 domain) for head g over its 4 tokens of this page.
-      const bool head_on = head_ok && ((hmask >> g) & 1u);
+      // Token t of the page counts for head g if bit (g << sub_log2) +
+      // (t >> (4 - sub_log2)) of the mask is set: the head selected its
+      // sub-page, or the whole page when sub_log2 = 0.  This lane's tokens
+      // 2 t4, 2 t4 + 1 share one sub-page, and 8 + 2 t4, 9 + 2 t4 the one
+      // sub_log2 bits above it.
+      const int sl = SPARSE ? a.sub_log2 : 0;
+      const uint32_t hbits =
+          head_ok ? (hmask >> ((g << sl) + (sl == 2 ? (t4 >> 1) : 0))) : 0u;
+      const bool on_lo = hbits & 1u, on_hi = (hbits >> sl) & 1u;
       float sv[4];
       float pmax = -INFINITY;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int tok = page * kPage + 8 * (e >> 1) + 2 * t4 + (e & 1);
-        sv[e] = (head_on && tok < Nb) ? sc[e >> 1][e & 1] * a.scale_log2 : -INFINITY;
+        const bool on = e < 2 ? on_lo : on_hi;
+        sv[e] = (on && tok < Nb) ? sc[e >> 1][e & 1] * a.scale_log2 : -INFINITY;
         pmax = fmaxf(pmax, sv[e]);
       }
       pmax = fmaxf(pmax, __shfl_xor_sync(0xffffffffu, pmax, 1));

@@ -92,6 +92,11 @@ struct AttnArgs {
   const int2* union_list;      // [B * Hkv, union_stride]
   const int* union_count;      // [B * Hkv]
   int union_stride;
+  // Selection pages of 16 >> sub_log2 tokens (sub_log2 = 1, 2: 8 or 4 tokens,
+  // 2 or 4 to a cache page): a union entry's mask then holds 1 << sub_log2
+  // bits per query head, one per sub-page (bit (h << sub_log2) + sub-page);
+  // 0 otherwise (one bit per head).
+  int sub_log2;
   // Per (batch, kv head): non-zero once the selection kernel has written that
   // unit's union.  When set, the kernel starts alongside the selection grid
   // and waits unit by unit; nullptr: it waits for the whole previous grid.

@@ -52,9 +52,11 @@ __global__ void __launch_bounds__(kMetaThreads, Q4 ? 4 : 2) meta_kernel(const Me
         const int cp = (t0 + c0) / kPage;  // cache page
         const int ntc = min(kPage, nt - c0);
         // a paged cache: the cache page's pool block (clamped), token 0 of it
+        // (a page of 4 or 8 tokens starts inside its block)
         const int64_t base = a.bt != nullptr
                                  ? static_cast<int64_t>(min(max(a.bt[b * a.bts + cp], 0),
-                                                            a.nblocks - 1)) * a.sb
+                                                            a.nblocks - 1)) * a.sb +
+                                       static_cast<int64_t>((t0 + c0) % kPage) * a.d
                                  : b * a.sb + static_cast<int64_t>(t0 + c0) * a.d;
         const uint16_t* src = static_cast<const uint16_t*>(a.data) + base + h * a.sh + 8 * v;
         uint4 x[kPage];

@@ -657,10 +657,19 @@ __device__ void block_emit(const KeyFn& key, const uint32_t* skeys, int P, uint3
   __syncthreads();  // the scratch may be reused
 }
 
+// Selection pages of S = 16 / sub tokens (sub = 2 or 4): the bits of word u
+// that start a cache page with at least one selected sub-page.
+__device__ __forceinline__ uint32_t subpage_groups(uint32_t u, int sub) {
+  return sub == 2 ? (u | (u >> 1)) & 0x55555555u
+                  : (u | (u >> 1) | (u >> 2) | (u >> 3)) & 0x11111111u;
+}
+
 // The union of G heads' selection bitmaps (word(h, w)) over selection pages of
 // S tokens, ascending, with a bit per head, each selection page written as its
 // cache pages (S / 16 of them, fewer for the last page of a sequence of n
-// tokens): out[0 .. count) = (cache page, mask); *count_out = count.
+// tokens): out[0 .. count) = (cache page, mask); *count_out = count.  Pages of
+// S = 4 or 8 tokens: each cache page holding a selected one is written once,
+// its mask holding 16 / S bits per head (bit h * 16 / S + sub-page).
 template <typename WordFn>
 __device__ void block_union(const WordFn& word, int G, int W32, int S, int n, int2* out,
                             int* count_out, SelScratch& sc) {
@@ -668,7 +677,9 @@ __device__ void block_union(const WordFn& word, int G, int W32, int S, int n, in
   const int span = (W32 + 32 * sel_warps() - 1) / (32 * sel_warps()) * 32;  // words per warp
   const int w0 = warp * span, w1 = min(W32, w0 + span);
   const int msub = S / kPage, last = static_cast<int>(ceil_div(n, S)) - 1;
+  const int sub = S < kPage ? kPage / S : 1;  // selection pages per cache page
   auto pages_of = [&](uint32_t u, int wi) {  // cache pages of word wi's selection pages
+    if (sub > 1) return __popc(subpage_groups(u, sub));
     int c = __popc(u) * msub;
     if (wi == (last >> 5) && ((u >> (last & 31)) & 1u)) c -= msub - cache_pages_in(last, S, n);
     return c;
@@ -702,15 +713,28 @@ __device__ void block_union(const WordFn& word, int G, int W32, int S, int n, in
       if (lane >= off) incl += t;
     }
     int pos = before + incl - c;
-    while (u) {
-      const int bit = __ffs(u) - 1;
-      u &= u - 1;
-      uint32_t m = 0;
+    if (sub > 1) {
+      uint32_t gm = subpage_groups(u, sub);
+      const uint32_t sub_mask = (1u << sub) - 1u;
+      while (gm) {
+        const int bit = __ffs(gm) - 1;  // first sub-page of a cache page
+        gm &= gm - 1;
+        uint32_t m = 0;
 #pragma unroll
-      for (int h = 0; h < 8; ++h) m |= ((hw[h] >> bit) & 1u) << h;
-      const int ps = wi * 32 + bit;
-      const int k = msub == 1 ? 1 : cache_pages_in(ps, S, n);
-      for (int i = 0; i < k; ++i) out[pos++] = make_int2(ps * msub + i, static_cast<int>(m));
+        for (int h = 0; h < 8; ++h) m |= ((hw[h] >> bit) & sub_mask) << (h * sub);
+        out[pos++] = make_int2((wi * 32 + bit) / sub, static_cast<int>(m));
+      }
+    } else {
+      while (u) {
+        const int bit = __ffs(u) - 1;
+        u &= u - 1;
+        uint32_t m = 0;
+#pragma unroll
+        for (int h = 0; h < 8; ++h) m |= ((hw[h] >> bit) & 1u) << h;
+        const int ps = wi * 32 + bit;
+        const int k = msub == 1 ? 1 : cache_pages_in(ps, S, n);
+        for (int i = 0; i < k; ++i) out[pos++] = make_int2(ps * msub + i, static_cast<int>(m));
+      }
     }
     before += __shfl_sync(0xffffffffu, incl, 31);
   }

@@ -53,7 +53,7 @@
  *     wait that expired, an in-kernel check) are written to a status word at
  *     the start of the workspace and read back with dkv_read_device_status.
  *     No call aborts the process.
- *   - Supported: d in {64, 128}; S in {16, 32, 64} (the page of the metadata
+ *   - Supported: d in {64, 128}; S in {4, 8, 16, 32, 64} (the page of the metadata
  *     and of selection; the cache itself is read in pages of 16 tokens, and a
  *     paged cache's blocks hold 16 tokens); Hq % Hkv == 0 and Hq / Hkv <= 8;
  *     1 <= N < 2^31; bf16 or fp16 dense caches (q in the same dtype), or the
@@ -126,9 +126,13 @@ typedef struct dkv_params {
   int32_t num_kv_heads;     /* Hkv >= 1, Hq % Hkv == 0, Hq / Hkv <= 8 */
   int32_t head_dim;         /* d in {64, 128} */
   int32_t seq_len;          /* N >= 1 context tokens, all attended */
-  int32_t page_size;        /* S in {16, 32, 64}: tokens per metadata / selection
-                               page ("TinyServe" 结构化内存布局); P = ceil(N / S).
-                               The exact path does not depend on it. */
+  int32_t page_size;        /* S in {4, 8, 16, 32, 64}: tokens per metadata /
+                               selection page ("TinyServe" 结构化内存布局 and its
+                               page-size study); P = ceil(N / S).  Pages of 4
+                               or 8 tokens are gathered as the 16-token cache
+                               page that holds them, with the tokens of
+                               unselected pages masked out.  The exact path
+                               does not depend on it. */
   int64_t q_stride_b, q_stride_h;   /* q, in elements */
   int64_t o_stride_b, o_stride_h;   /* out, in elements */
   float scale;              /* softmax scale, usually 1/sqrt(d) */

@@ -62,11 +62,13 @@ def test_workspace_bytes_layout(L):
     assert sel > full
     assert L.dkv_workspace_bytes(ctypes.byref(_params(head_dim=96)), 0) == 0
     assert L.dkv_workspace_bytes(ctypes.byref(_params(num_q_heads=7)), 0) == 0
-    assert L.dkv_workspace_bytes(ctypes.byref(_params(page_size=8)), 0) == 0
+    assert L.dkv_workspace_bytes(ctypes.byref(_params(page_size=12)), 0) == 0
     assert L.dkv_workspace_bytes(ctypes.byref(_params(page_size=48)), 0) == 0
-    # selection pages of 32 or 64 tokens: the exact path is unchanged
-    assert L.dkv_workspace_bytes(ctypes.byref(_params(page_size=32)), 0) == full
+    # selection pages of 4, 8, 32 or 64 tokens: the exact path is unchanged
+    for S in (4, 8, 32):
+        assert L.dkv_workspace_bytes(ctypes.byref(_params(page_size=S)), 0) == full
     assert L.dkv_workspace_bytes(ctypes.byref(_params(page_size=64)), 8) > 0
+    assert L.dkv_workspace_bytes(ctypes.byref(_params(page_size=4)), 8) > 0
     assert L.dkv_workspace_bytes(None, 0) == 0
 
 

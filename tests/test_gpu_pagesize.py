@@ -1,8 +1,9 @@
-"""Selection pages of S = 32 and 64 tokens ("TinyServe" page-size variants):
-metadata over S tokens, bound scores and top-K over ceil(N / S) pages, and
-attention over the selected pages' tokens, gathered as the cache's 16-token
-pages.  Checked against the oracle at the same S (metadata bit-exact,
-selection within the band, outputs within 2e-3).
+"""Selection pages of S = 4, 8, 32 and 64 tokens ("TinyServe" page-size
+variants): metadata over S tokens, bound scores and top-K over ceil(N / S)
+pages, and attention over the selected pages' tokens, gathered as the cache's
+16-token pages (pages of 4 or 8 tokens as the cache page holding them, the
+other tokens masked per query head).  Checked against the oracle at the same
+S (metadata bit-exact, selection within the band, outputs within 2e-3).
 """
 
 import math
@@ -39,6 +40,15 @@ CASES = [
     (Workload("s64-unit-mha", B=1, Hq=4, Hkv=4, d=64, N=70000, S=64, top_k=30), None, False),
     (Workload("s64-group-lens", B=2, Hq=8, Hkv=2, d=128, N=3001, S=64, top_k=8, kind="hot"),
      [3001, 100], True),
+    # quarter and half cache pages: a cache page holds pages chosen by some
+    # heads and not others, and pages no head chose
+    (Workload("s8-gqa-ragged", B=2, Hq=8, Hkv=2, d=128, N=5001, S=8, top_k=60, kind="hot"),
+     None, False),
+    (Workload("s4-g8-d64", B=1, Hq=8, Hkv=1, d=64, N=3000, S=4, top_k=70), None, False),
+    (Workload("s4-group-lens", B=2, Hq=8, Hkv=2, d=128, N=2050, S=4, top_k=33, kind="hot"),
+     [2050, 37], True),
+    (Workload("s8-mha-lens", B=3, Hq=4, Hkv=4, d=128, N=1500, S=8, top_k=20),
+     [1500, 9, 801], False),
 ]
 
 
@@ -93,3 +103,35 @@ def test_all_pages_at_s64_equals_full(dev, dkv):
     out = dkv.decode_attn_select(q, K, V, meta, P, page_size=64)
     full = dkv.decode_attn_full(q, K, V)
     assert max_abs(out, full.double().cpu().numpy()) <= 1e-5
+
+
+@pytest.mark.parametrize("S", [4, 8])
+def test_small_pages_all_selected_equals_full(S, dev, dkv):
+    # every page kept: each head's mask covers every sub-page of every cache page
+    w = Workload("small-all", B=2, Hq=8, Hkv=2, d=128, N=1003, S=S)
+    q, K, V = (x.to(dev) for x in make_inputs(w, seed=75))
+    meta = dkv.kv_meta_build(K, page_size=S)
+    P = (w.N + S - 1) // S
+    out = dkv.decode_attn_select(q, K, V, meta, P, page_size=S)
+    full = dkv.decode_attn_full(q, K, V)
+    assert max_abs(out, full.double().cpu().numpy()) <= 1e-5
+
+
+def test_small_pages_paged_cache_equals_contiguous(dev, dkv):
+    # pages of 8 tokens start inside a pool block: metadata and outputs of a
+    # shuffled pool equal the contiguous cache's bitwise
+    from test_gpu_paged import to_paged
+    w = Workload("s8-paged", B=2, Hq=8, Hkv=2, d=128, N=3000, S=8, top_k=40, kind="hot")
+    q, K, V = make_inputs(w, seed=77)
+    P16 = (w.N + 15) // 16
+    pk, bt = to_paged(K, P16, seed=3)
+    pv, _ = to_paged(V, P16, seed=3)
+    qd, Kd, Vd, btd = q.to(dev), K.to(dev), V.to(dev), bt.to(dev)
+    PK = dkv.PagedCache(pk.to(dev), btd, w.N)
+    PV = dkv.PagedCache(pv.to(dev), btd, w.N)
+    mc, mp = dkv.kv_meta_build(Kd, page_size=8), dkv.kv_meta_build(PK, page_size=8)
+    assert torch.equal(mc[0], mp[0]) and torch.equal(mc[1], mp[1])
+    oc, sc = dkv.decode_attn_select(qd, Kd, Vd, mc, w.top_k, return_selected=True, page_size=8)
+    op, sp = dkv.decode_attn_select(qd, PK, PV, mp, w.top_k, return_selected=True, page_size=8)
+    assert torch.equal(sc, sp)
+    assert torch.equal(oc, op)
