@@ -68,6 +68,8 @@ def _load():
             lib.oracle_topk.argtypes = [i32, i32, i32, P, P]
             lib.oracle_attention.argtypes = [i32, i32, i32, i32, i32, i32, i32,
                                              P, P, P, dbl, P, i32, P]
+            lib.oracle_meta8.argtypes = [i64, i32, i32, P, P, P, P, P, P]
+            lib.oracle_scores8.argtypes = [i32, i32, i32, i32, i32, i32, P, P, P, P, P, P]
             lib.oracle_quant4.argtypes = [i64, i32, P, P, P, P]
             lib.oracle_dequant4.argtypes = [i64, i32, P, P, P, P]
             _lib = lib
@@ -151,6 +153,38 @@ def group_scores(q: np.ndarray, meta_min: np.ndarray, meta_max: np.ndarray, is_f
     B, Hq, P = r.shape
     Hkv = meta_min.shape[1]
     return r.reshape(B, Hkv, Hq // Hkv, P).sum(axis=2)
+
+
+def meta8(meta_min: np.ndarray, meta_max: np.ndarray, is_fp16: int):
+    """8-bit page metadata from (m_j, M_j): (code_min, code_max) uint8
+    [B, Hkv, P, d] and (lo, step) float32 [B, Hkv, P], with
+    dec(c) = fma(c, step, lo) rounded outward: dec(code_min) <= m and
+    dec(code_max) >= M channel by channel (definition in dkv_oracle.cpp)."""
+    meta_min = _c(meta_min, np.uint16)
+    meta_max = _c(meta_max, np.uint16)
+    B, Hkv, P, d = meta_min.shape
+    cmin = np.empty((B, Hkv, P, d), np.uint8)
+    cmax = np.empty((B, Hkv, P, d), np.uint8)
+    lo = np.empty((B, Hkv, P), np.float32)
+    step = np.empty((B, Hkv, P), np.float32)
+    _load().oracle_meta8(B * Hkv * P, d, int(is_fp16), _ptr(meta_min), _ptr(meta_max),
+                         _ptr(cmin), _ptr(cmax), _ptr(lo), _ptr(step))
+    return cmin, cmax, lo, step
+
+
+def scores8(q: np.ndarray, cmin: np.ndarray, cmax: np.ndarray, lo: np.ndarray,
+            step: np.ndarray, is_fp16: int):
+    """Bound scores over 8-bit metadata in float64, [B, Hq, P]: r with the
+    decoded dec(code_max) / dec(code_min) in place of M / m."""
+    q = _c(q, np.uint16)
+    cmin, cmax = _c(cmin, np.uint8), _c(cmax, np.uint8)
+    lo, step = _c(lo, np.float32), _c(step, np.float32)
+    B, Hq, d = q.shape
+    _, Hkv, P, _ = cmin.shape
+    out = np.empty((B, Hq, P), np.float64)
+    _load().oracle_scores8(B, Hq, Hkv, P, d, int(is_fp16), _ptr(q), _ptr(cmin), _ptr(cmax),
+                           _ptr(lo), _ptr(step), _ptr(out))
+    return out
 
 
 def topk(r: np.ndarray, K: int) -> np.ndarray:

@@ -29,6 +29,7 @@
 //   q      [B, Hq, d]            16-bit float bits (bf16 or fp16)
 //   K, V   [B, Hkv, N, d]        16-bit float bits
 //   meta   [B, Hkv, P, d]        16-bit float bits, P = ceil(N / S)
+//   meta8  codes [B, Hkv, P, d] u8 (min and max); lo, step [B, Hkv, P] fp32
 //   codes  [rows, d/2]           u8, channel 2i in the low nibble of byte i
 //   gmin, gmax [rows, d/64]      fp16 bits
 //   scores [B, Hq, P]            double
@@ -200,6 +201,89 @@ void oracle_scores(int B, int Hq, int Hkv, int P, int d, int is_fp16, const uint
         } else {
           s += qi * value16(mn[static_cast<int64_t>(j) * d + i], is_fp16);
         }
+      }
+      scores[bh * P + j] = s;
+    }
+  });
+}
+
+// ---------------------------------------------------------------------------
+// 8-bit page metadata: a smaller phi that keeps r an upper bound
+// [TS 相关性函数实例化; the metadata scan is the "lightweight" per-step term of
+// the page's cost model].  The pages keep (m_j, M_j) at the keys' precision and
+// print no compressed form; this one is the plainest that keeps the bound.  Per
+// page j (one batch entry and kv head):
+//   lo = min_i m_{j,i},  hi = max_i M_{j,i}        (a zero is stored as +0)
+//   dec(c) = fma(c, step, lo)                      one fp32 rounding
+//   step   = fp32(fp32(hi - lo) / 255), raised one ulp at a time until
+//            dec(255) >= hi                        (0 when hi == lo)
+//   cm_i   = the largest c in [0, 255] with dec(c) <= m_{j,i}
+//   cM_i   = the smallest c in [0, 255] with dec(c) >= M_{j,i}
+// dec is non-decreasing in c and dec(0) = lo, so both codes exist, and
+// dec(cm_i) <= m_{j,i} <= k_i <= M_{j,i} <= dec(cM_i) for every key of the page:
+// the score with dec(cm), dec(cM) in place of m, M bounds max_k q.k again.
+// Metadata is finite (hi - lo finite).
+// ---------------------------------------------------------------------------
+float dec8(int c, float step, float lo) { return std::fmaf(static_cast<float>(c), step, lo); }
+
+void oracle_meta8(int64_t pages, int d, int is_fp16, const uint16_t* meta_min,
+                  const uint16_t* meta_max, uint8_t* code_min, uint8_t* code_max, float* lo_out,
+                  float* step_out) {
+  parallel_for(pages, [&](int64_t pg) {
+    const uint16_t* mn = meta_min + pg * d;
+    const uint16_t* mx = meta_max + pg * d;
+    float lo = static_cast<float>(value16(mn[0], is_fp16));
+    float hi = static_cast<float>(value16(mx[0], is_fp16));
+    for (int i = 1; i < d; ++i) {
+      lo = std::min(lo, static_cast<float>(value16(mn[i], is_fp16)));
+      hi = std::max(hi, static_cast<float>(value16(mx[i], is_fp16)));
+    }
+    if (lo == 0.0f) lo = 0.0f;  // +0
+    if (hi == 0.0f) hi = 0.0f;
+    float step = 0.0f;
+    if (hi > lo) {
+      const float range = hi - lo;  // one fp32 rounding
+      step = range / 255.0f;        // one fp32 rounding
+      while (dec8(255, step, lo) < hi) step = std::nextafterf(step, INFINITY);
+    }
+    lo_out[pg] = lo;
+    step_out[pg] = step;
+    for (int i = 0; i < d; ++i) {
+      const float m = static_cast<float>(value16(mn[i], is_fp16));
+      const float M = static_cast<float>(value16(mx[i], is_fp16));
+      int cm = 0, cM = 0;
+      if (step > 0.0f) {
+        // a first guess from the division, then the definitions decide
+        const float em = (m - lo) / step, eM = (M - lo) / step;
+        cm = em >= 255.0f ? 255 : (em >= 0.0f ? static_cast<int>(em) : 0);
+        cM = eM >= 255.0f ? 255 : (eM >= 0.0f ? static_cast<int>(std::ceil(eM)) : 0);
+        while (cm < 255 && dec8(cm + 1, step, lo) <= m) ++cm;
+        while (cm > 0 && dec8(cm, step, lo) > m) --cm;
+        while (cM > 0 && dec8(cM - 1, step, lo) >= M) --cM;
+        while (cM < 255 && dec8(cM, step, lo) < M) ++cM;
+      }
+      code_min[pg * d + i] = static_cast<uint8_t>(cm);
+      code_max[pg * d + i] = static_cast<uint8_t>(cM);
+    }
+  });
+}
+
+// The bound score over 8-bit metadata, in float64 over the decoded values:
+//   r8(q, j) = sum_i ( q_i >= 0 ? q_i * dec(cM_{j,i}) : q_i * dec(cm_{j,i}) )
+void oracle_scores8(int B, int Hq, int Hkv, int P, int d, int is_fp16, const uint16_t* q,
+                    const uint8_t* code_min, const uint8_t* code_max, const float* lo,
+                    const float* step, double* scores) {
+  const int G = Hq / Hkv;
+  parallel_for(static_cast<int64_t>(B) * Hq, [&](int64_t bh) {
+    const int64_t b = bh / Hq, h = bh % Hq, kvh = h / G;
+    const uint16_t* qv = q + bh * d;
+    for (int j = 0; j < P; ++j) {
+      const int64_t pg = (b * Hkv + kvh) * P + j;
+      double s = 0.0;
+      for (int i = 0; i < d; ++i) {
+        const double qi = value16(qv[i], is_fp16);
+        const uint8_t c = qi >= 0.0 ? code_max[pg * d + i] : code_min[pg * d + i];
+        s += qi * static_cast<double>(dec8(c, step[pg], lo[pg]));
       }
       scores[bh * P + j] = s;
     }
