@@ -57,9 +57,9 @@ def parse_args():
                     help="skip the e2e, CPU-baseline, 1M-token head-wise and other-workload legs")
     ap.add_argument("--legs", default="all",
                     help="comma list of extra legs to run (e2e, group, paged, pagesize, tokens, "
-                         "cpu, headwise, others) or 'all'; for small profiling runs")
+                         "meta8, cpu, headwise, others) or 'all'; for small profiling runs")
     args = ap.parse_args()
-    legs = {"e2e", "group", "paged", "pagesize", "tokens", "cpu", "headwise", "others"}
+    legs = {"e2e", "group", "paged", "pagesize", "tokens", "meta8", "cpu", "headwise", "others"}
     args.legs = set() if args.no_extra else (legs if args.legs == "all" else set(args.legs.split(",")))
     unknown = args.legs - legs
     if unknown:
@@ -356,6 +356,63 @@ def group_select_leg(q, K, V, w, dev, stream, reps=10):
             "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4), "gathered_pages": gathered // w.S,
             "queries_per_s": round(w.B / (ms * 1e-3), 1),
             "timing": f"{reps} back-to-back calls"}
+
+
+def _time_calls(fn, stream, reps):
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def meta8_leg(q, K, V, w, dev, stream, reps=10):
+    """8-bit page metadata on the bench workload: its build from the 16-bit
+    metadata, and decode_attn_select scoring it (10 back-to-back calls each);
+    how many (batch, q-head) rows keep the 16-bit metadata's page set."""
+    import decode_attention_paged_kv_gb300 as dkv
+    from decode_attention_paged_kv_gb300 import accounting as acc
+
+    meta = dkv.kv_meta_build(K)
+    m8 = dkv.kv_meta8_build(meta)
+    kk = min(w.top_k, w.P)
+    ws = torch.zeros(dkv.workspace_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, w.top_k),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty(w.B, w.Hq, w.d, dtype=torch.float32, device=dev)
+    sel = torch.empty(w.B, w.Hq, kk, dtype=torch.int32, device=dev)
+    peak, _ = peaks()
+    res = {"workload": w.name, "timing": f"{reps} back-to-back calls"}
+    ms = _time_calls(lambda: dkv.kv_meta8_build(meta), stream, reps)
+    nbytes = acc.meta8_bytes(w.B, w.Hkv, w.d, w.N, w.S)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    res["kv_meta8_build"] = {"ms": round(ms, 5), "alg_bytes": nbytes, "GB/s": round(gbs, 1),
+                             "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+                             "frac_of_measured_hbm": round(gbs / peak, 4)}
+    ms = _time_calls(lambda: dkv.decode_attn_select(q, K, V, m8, w.top_k, out=out, selected=sel,
+                                                    workspace=ws), stream, reps)
+    gathered = union_tokens(sel, w)
+    nbytes = acc.select8_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, gathered, w.S)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    res["decode_attn_select"] = {"ms": round(ms, 5), "alg_bytes": nbytes, "GB/s": round(gbs, 1),
+                                 "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+                                 "frac_of_measured_hbm": round(gbs / peak, 4),
+                                 "gathered_pages": gathered // w.S,
+                                 "queries_per_s": round(w.B / (ms * 1e-3), 1)}
+    sel16 = dkv.decode_attn_select(q, K, V, meta, w.top_k, return_selected=True)[1]
+    same = (torch.sort(sel16, -1)[0] == torch.sort(sel, -1)[0]).all(-1)
+    res["rows_with_16bit_page_set"] = round(float(same.float().mean().item()), 4)
+    a, b = sel16.view(-1, kk).long(), sel.view(-1, kk).long()
+    hit = torch.zeros(w.B * w.Hq, w.P, dtype=torch.bool, device=dev)
+    hit.scatter_(1, a, True)
+    overlap = hit.gather(1, b).float().mean()
+    res["page_overlap_with_16bit"] = round(float(overlap.item()), 4)
+    del m8, meta, ws
+    return res
 
 
 def paged_leg(q, K, V, w, dev, stream, reps=10):
@@ -795,6 +852,8 @@ def main():
             res["page_sizes"] = page_size_leg(q, K, V, w, dev, stream)
         if "tokens" in L:
             res["topk_tokens"] = token_leg(q, K, V, w, dev, stream)
+        if "meta8" in L:
+            res["meta8"] = meta8_leg(q, K, V, w, dev, stream)
         if "cpu" in L:
             res["cpu_baseline"] = cpu_baseline_leg(q, K, V, w)
         del q, K, V

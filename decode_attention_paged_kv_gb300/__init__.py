@@ -29,7 +29,8 @@ import torch
 from . import build as _build_mod
 
 __all__ = [
-    "Q4Cache", "PagedCache", "DkvError", "lib", "kv_meta_build", "decode_attn_full",
+    "Q4Cache", "PagedCache", "Meta8", "DkvError", "lib", "kv_meta_build", "kv_meta8_build",
+    "decode_attn_full",
     "decode_attn_select", "decode_attn_topk_tokens", "kv_quant4", "kv_dequant4",
     "workspace_bytes", "workspace_bytes_tokens", "read_device_status", "status_string",
     "PAGE_SIZE", "DKV_FLAG_GROUP_SELECT",
@@ -61,6 +62,17 @@ class Q4Cache(NamedTuple):
     codes: torch.Tensor
     gmin: torch.Tensor
     gmax: torch.Tensor
+
+
+class Meta8(NamedTuple):
+    """8-bit page metadata (kv_meta8_build): per page a grid
+    dec(c) = fmaf(c, step, lo), and per channel the codes of m rounded down
+    and of M rounded up on it.  code_min / code_max uint8 [B, Hkv, P, d];
+    lo / step float32 [B, Hkv, P]."""
+    code_min: torch.Tensor
+    code_max: torch.Tensor
+    lo: torch.Tensor
+    step: torch.Tensor
 
 
 class PagedCache(NamedTuple):
@@ -120,6 +132,9 @@ def lib() -> ctypes.CDLL:
                                                  sz, vp]
             L.dkv_decode_attn_topk_tokens.argtypes = [P, vp, KVp, KVp, i32, vp, i32, vp, vp,
                                                       sz, vp]
+            L.dkv_kv_meta8_build.argtypes = [P, vp, vp, i32, vp, vp, vp, vp, vp]
+            L.dkv_decode_attn_select_meta8.argtypes = [P, vp, KVp, KVp, vp, vp, vp, vp, i32,
+                                                       vp, i32, vp, vp, sz, vp]
             L.dkv_workspace_bytes_tokens.argtypes = [P, i32]
             L.dkv_workspace_bytes_tokens.restype = sz
             L.dkv_kv_quant4.argtypes = [i64, i32, vp, vp, vp, vp, vp]
@@ -129,7 +144,8 @@ def lib() -> ctypes.CDLL:
             L.dkv_status_string.argtypes = [i32]
             L.dkv_status_string.restype = ctypes.c_char_p
             for name in ("dkv_kv_meta_build", "dkv_decode_attn_full", "dkv_decode_attn_select",
-                         "dkv_decode_attn_topk_tokens",
+                         "dkv_decode_attn_topk_tokens", "dkv_kv_meta8_build",
+                         "dkv_decode_attn_select_meta8",
                          "dkv_kv_quant4", "dkv_kv_dequant4", "dkv_read_device_status",
                          "dkv_attn_ctas_per_sm"):
                 getattr(L, name).restype = ctypes.c_int
@@ -266,6 +282,30 @@ def kv_meta_build(K, page_size: int = PAGE_SIZE, seq_lens: Optional[torch.Tensor
     return mn, mx
 
 
+def kv_meta8_build(meta, page_size: int = PAGE_SIZE,
+                   seq_lens: Optional[torch.Tensor] = None) -> Meta8:
+    """8-bit page metadata from (meta_min, meta_max) [B, Hkv, P, d] (bf16 or
+    fp16, as kv_meta_build returns it)."""
+    mn, mx = meta
+    if mn.dtype not in (torch.bfloat16, torch.float16) or mx.dtype != mn.dtype:
+        raise ValueError("meta must be bf16 or fp16")
+    if not mn.is_contiguous() or not mx.is_contiguous() or mn.shape != mx.shape:
+        raise ValueError("meta must be two contiguous [B, Hkv, P, d] tensors")
+    B, H, P, d = mn.shape
+    m8 = Meta8(torch.empty(B, H, P, d, dtype=torch.uint8, device=mn.device),
+               torch.empty(B, H, P, d, dtype=torch.uint8, device=mn.device),
+               torch.empty(B, H, P, dtype=torch.float32, device=mn.device),
+               torch.empty(B, H, P, dtype=torch.float32, device=mn.device))
+    # N only sets P here: the largest N with ceil(N / S) = P
+    p = _params(None, B, H, P * page_size, d, None, None, seq_lens=seq_lens)
+    p.page_size = page_size
+    _check(lib().dkv_kv_meta8_build(ctypes.byref(p), mn.data_ptr(), mx.data_ptr(),
+                                    _dtype_code(mn.dtype), m8.code_min.data_ptr(),
+                                    m8.code_max.data_ptr(), m8.lo.data_ptr(),
+                                    m8.step.data_ptr(), _stream(mn)), "dkv_kv_meta8_build")
+    return m8
+
+
 def decode_attn_full(q, K, V, scale: Optional[float] = None,
                      out_dtype: torch.dtype = torch.float32,
                      out: Optional[torch.Tensor] = None,
@@ -297,17 +337,24 @@ def decode_attn_select(q, K, V, meta, top_k: int, scale: Optional[float] = None,
                        page_size: int = PAGE_SIZE):
     """Query-aware page-sparse decode attention over the top_k pages per q-head
     (group_select: one selection per kv head group, by the summed bound scores;
-    page_size: tokens per metadata / selection page, as meta was built with)."""
+    page_size: tokens per metadata / selection page, as meta was built with;
+    meta: (meta_min, meta_max), or a Meta8 from kv_meta8_build)."""
     if group_select:
         flags |= DKV_FLAG_GROUP_SELECT
     ks, B, H, N, d = _kv_struct(K)
     vs, B2, H2, N2, d2 = _kv_struct(V)
     if (B, H, N, d) != (B2, H2, N2, d2):
         raise ValueError("K and V shapes differ")
-    mn, mx = meta
     P = (N + page_size - 1) // page_size
-    if tuple(mn.shape) != (B, H, P, d) or not mn.is_contiguous() or not mx.is_contiguous():
-        raise ValueError("meta must be contiguous [B, Hkv, P, d]")
+    m8 = meta if isinstance(meta, Meta8) else None
+    if m8 is not None:
+        if (tuple(m8.code_min.shape) != (B, H, P, d) or tuple(m8.lo.shape) != (B, H, P)
+                or not all(t.is_contiguous() for t in m8)):
+            raise ValueError("Meta8 must hold contiguous [B, Hkv, P, d] codes, [B, Hkv, P] grid")
+    else:
+        mn, mx = meta
+        if tuple(mn.shape) != (B, H, P, d) or not mn.is_contiguous() or not mx.is_contiguous():
+            raise ValueError("meta must be contiguous [B, Hkv, P, d]")
     if out is None:
         out = torch.empty(B, q.shape[1], d, dtype=out_dtype, device=q.device)
     kk = min(int(top_k), P)
@@ -318,11 +365,18 @@ def decode_attn_select(q, K, V, meta, top_k: int, scale: Optional[float] = None,
     nbytes = lib().dkv_workspace_bytes(ctypes.byref(p), int(top_k))
     ws = _workspace(nbytes, q.device, workspace)
     sel_ptr = selected.data_ptr() if selected is not None else None
-    _check(lib().dkv_decode_attn_select(ctypes.byref(p), q.data_ptr(), ctypes.byref(ks),
-                                        ctypes.byref(vs), mn.data_ptr(), mx.data_ptr(),
-                                        int(top_k), out.data_ptr(), _dtype_code(out.dtype),
-                                        sel_ptr, ws.data_ptr(), nbytes, _stream(q)),
-           "dkv_decode_attn_select")
+    if m8 is not None:
+        _check(lib().dkv_decode_attn_select_meta8(
+            ctypes.byref(p), q.data_ptr(), ctypes.byref(ks), ctypes.byref(vs),
+            m8.code_min.data_ptr(), m8.code_max.data_ptr(), m8.lo.data_ptr(),
+            m8.step.data_ptr(), int(top_k), out.data_ptr(), _dtype_code(out.dtype), sel_ptr,
+            ws.data_ptr(), nbytes, _stream(q)), "dkv_decode_attn_select_meta8")
+    else:
+        _check(lib().dkv_decode_attn_select(ctypes.byref(p), q.data_ptr(), ctypes.byref(ks),
+                                            ctypes.byref(vs), mn.data_ptr(), mx.data_ptr(),
+                                            int(top_k), out.data_ptr(), _dtype_code(out.dtype),
+                                            sel_ptr, ws.data_ptr(), nbytes, _stream(q)),
+               "dkv_decode_attn_select")
     return (out, selected) if return_selected else out
 
 

@@ -51,6 +51,22 @@ def select_bytes(B, Hq, Hkv, d, N, gathered_tokens, S=16, elt=2, out_elt=4, q4=F
     return q + meta + 2 * gathered_tokens * per_tok + out
 
 
+def meta8_bytes(B, Hkv, d, N, S=16, elt=2) -> int:
+    """16-bit page metadata read; 8-bit codes and the per-page grid written."""
+    P = (N + S - 1) // S
+    return 2 * B * Hkv * P * d * elt + 2 * B * Hkv * P * d + 2 * B * Hkv * P * 4
+
+
+def select8_bytes(B, Hq, Hkv, d, N, gathered_tokens, S=16, elt=2, out_elt=4) -> int:
+    """q + 8-bit metadata of every page (two code bytes per channel, lo and
+    step) + K and V of the gathered tokens + out."""
+    P = (N + S - 1) // S
+    q = B * Hq * d * elt
+    out = B * Hq * d * out_elt
+    meta = 2 * B * Hkv * P * d + 2 * B * Hkv * P * 4
+    return q + meta + 2 * gathered_tokens * d * elt + out
+
+
 def quant4_bytes(rows, d) -> int:
     """fp16 rows read + 4-bit codes and group min / max written."""
     return rows * d * 2 + rows * (d // 2 + 2 * (d // 64) * 2)

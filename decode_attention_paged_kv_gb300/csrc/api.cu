@@ -425,11 +425,20 @@ dkv_status dkv_decode_attn_full(const dkv_params* p, const void* q, const dkv_kv
   return run_attention(p, a, false, K->dtype == DKV_FP16, mk, mv, out, out_dtype, s);
 }
 
-dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_kv* K,
-                                  const dkv_kv* V, const void* meta_min,
-                                  const void* meta_max, int32_t top_k, void* out,
-                                  int32_t out_dtype, int32_t* selected, void* workspace,
-                                  size_t workspace_bytes, void* stream) {
+// 8-bit page metadata (device pointers), for the select path that scores it.
+struct Meta8Ptrs {
+  const uint8_t* code_min;
+  const uint8_t* code_max;
+  const float* lo;
+  const float* step;
+};
+
+// The page-sparse call over 16-bit metadata (m8 == nullptr) or 8-bit metadata.
+static dkv_status select_impl(const dkv_params* p, const void* q, const dkv_kv* K,
+                              const dkv_kv* V, const void* meta_min, const void* meta_max,
+                              const Meta8Ptrs* m8, int32_t top_k, void* out, int32_t out_dtype,
+                              int32_t* selected, void* workspace, size_t workspace_bytes,
+                              void* stream) {
   dkv_status st = check_params(p);
   if (st != DKV_OK) return st;
   if (top_k < 1) return DKV_ERR_SHAPE;
@@ -437,8 +446,17 @@ dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_
   if ((st = attn_common(p, q, K, V, out, out_dtype, workspace, workspace_bytes, top_k, L)) !=
       DKV_OK)
     return st;
-  if (meta_min == nullptr || meta_max == nullptr) return DKV_ERR_NULL;
-  if (!aligned16(meta_min) || !aligned16(meta_max)) return DKV_ERR_ALIGN;
+  if (m8 == nullptr) {
+    if (meta_min == nullptr || meta_max == nullptr) return DKV_ERR_NULL;
+    if (!aligned16(meta_min) || !aligned16(meta_max)) return DKV_ERR_ALIGN;
+  } else {
+    if (m8->code_min == nullptr || m8->code_max == nullptr || m8->lo == nullptr ||
+        m8->step == nullptr)
+      return DKV_ERR_NULL;
+    if (!aligned16(m8->code_min) || !aligned16(m8->code_max) ||
+        (reinterpret_cast<uintptr_t>(m8->lo) & 3u) || (reinterpret_cast<uintptr_t>(m8->step) & 3u))
+      return DKV_ERR_ALIGN;
+  }
   if (selected != nullptr && (reinterpret_cast<uintptr_t>(selected) & 3u)) return DKV_ERR_ALIGN;
   CUtensorMap mk, mv;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -459,7 +477,8 @@ dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_
   a.union_count = ucount;
   a.union_stride = L.union_stride;
 
-  if (p->page_size >= dkv::kPage && P >= kUnitSelectMinP && P <= dkv::kUnitMaxP &&
+  if (m8 == nullptr && p->page_size >= dkv::kPage && P >= kUnitSelectMinP &&
+      P <= dkv::kUnitMaxP &&
       dkv::unit_select_smem(p->head_dim, G, P) <= static_cast<size_t>(kUnitSelectSmemLimit)) {
     // Long contexts: one CTA per (batch, kv head) scores its pages, selects
     // each head's top-K and builds the union list.  (Shorter ones have too
@@ -513,7 +532,25 @@ dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_
     sa.G = G;
     sa.P = P;
     sa.scores = reinterpret_cast<float*>(ws + L.scores);
-    if ((st = cuda_status(dkv::launch_score(p->head_dim, f16, sa, s))) != DKV_OK) return st;
+    if (m8 == nullptr) {
+      if ((st = cuda_status(dkv::launch_score(p->head_dim, f16, sa, s))) != DKV_OK) return st;
+    } else {
+      dkv::Score8Args s8{};
+      s8.q = q;
+      s8.q_sb = p->q_stride_b;
+      s8.q_sh = p->q_stride_h;
+      s8.code_min = m8->code_min;
+      s8.code_max = m8->code_max;
+      s8.lo = m8->lo;
+      s8.step = m8->step;
+      s8.B = p->batch;
+      s8.Hq = p->num_q_heads;
+      s8.Hkv = p->num_kv_heads;
+      s8.G = G;
+      s8.P = P;
+      s8.scores = sa.scores;
+      if ((st = cuda_status(dkv::launch_score8(p->head_dim, f16, s8, s))) != DKV_OK) return st;
+    }
     dkv::TopkArgs ta{};
     ta.scores = sa.scores;
     ta.rows = p->batch * p->num_q_heads;
@@ -546,6 +583,58 @@ dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_
   }
 
   return run_attention(p, a, true, f16, mk, mv, out, out_dtype, s);
+}
+
+dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_kv* K,
+                                  const dkv_kv* V, const void* meta_min,
+                                  const void* meta_max, int32_t top_k, void* out,
+                                  int32_t out_dtype, int32_t* selected, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  return select_impl(p, q, K, V, meta_min, meta_max, nullptr, top_k, out, out_dtype, selected,
+                     workspace, workspace_bytes, stream);
+}
+
+dkv_status dkv_decode_attn_select_meta8(const dkv_params* p, const void* q, const dkv_kv* K,
+                                        const dkv_kv* V, const void* code_min,
+                                        const void* code_max, const void* lo, const void* step,
+                                        int32_t top_k, void* out, int32_t out_dtype,
+                                        int32_t* selected, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+  const Meta8Ptrs m8{static_cast<const uint8_t*>(code_min), static_cast<const uint8_t*>(code_max),
+                     static_cast<const float*>(lo), static_cast<const float*>(step)};
+  return select_impl(p, q, K, V, nullptr, nullptr, &m8, top_k, out, out_dtype, selected,
+                     workspace, workspace_bytes, stream);
+}
+
+dkv_status dkv_kv_meta8_build(const dkv_params* p, const void* meta_min, const void* meta_max,
+                              int32_t meta_dtype, void* code_min, void* code_max, void* lo,
+                              void* step, void* stream) {
+  dkv_status st = check_params(p);
+  if (st != DKV_OK) return st;
+  if (meta_dtype != DKV_BF16 && meta_dtype != DKV_FP16) return DKV_ERR_DTYPE;
+  if (meta_min == nullptr || meta_max == nullptr || code_min == nullptr || code_max == nullptr ||
+      lo == nullptr || step == nullptr)
+    return DKV_ERR_NULL;
+  if (!aligned16(meta_min) || !aligned16(meta_max) || !aligned16(code_min) ||
+      !aligned16(code_max) || (reinterpret_cast<uintptr_t>(lo) & 3u) ||
+      (reinterpret_cast<uintptr_t>(step) & 3u))
+    return DKV_ERR_ALIGN;
+  dkv::Meta8Args a{};
+  a.meta_min = static_cast<const uint16_t*>(meta_min);
+  a.meta_max = static_cast<const uint16_t*>(meta_max);
+  a.code_min = static_cast<uint8_t*>(code_min);
+  a.code_max = static_cast<uint8_t*>(code_max);
+  a.lo = static_cast<float*>(lo);
+  a.step = static_cast<float*>(step);
+  a.B = p->batch;
+  a.Hkv = p->num_kv_heads;
+  a.P = static_cast<int>(ceil_div(p->seq_len, p->page_size));
+  a.d = p->head_dim;
+  a.S = p->page_size;
+  a.N = p->seq_len;
+  a.lens = p->seq_lens;
+  return cuda_status(
+      dkv::launch_meta8(meta_dtype == DKV_FP16, a, static_cast<cudaStream_t>(stream)));
 }
 
 dkv_status dkv_kv_quant4(int64_t rows, int32_t d, const void* x, void* codes, void* gmin,

@@ -138,6 +138,31 @@ struct ScoreArgs {
   int exact;                   // 1: meta_max holds single keys (m = M): score q . k once
 };
 
+// 8-bit page metadata: per page a grid dec(c) = fma(c, step, lo) and, per
+// channel, the codes of m rounded down and of M rounded up on it.
+struct Meta8Args {
+  const uint16_t* meta_min;    // [B, Hkv, P, d] bf16 / fp16 bits
+  const uint16_t* meta_max;
+  uint8_t* code_min;           // [B, Hkv, P, d]
+  uint8_t* code_max;
+  float* lo;                   // [B, Hkv, P]
+  float* step;
+  int B, Hkv, P, d, S, N;
+  const int32_t* lens;         // per-sequence lengths [B] or nullptr
+};
+
+// Bound scores over 8-bit metadata into [B, Hq, P] (same layout as ScoreArgs).
+struct Score8Args {
+  const void* q;
+  int64_t q_sb, q_sh;
+  const uint8_t* code_min;
+  const uint8_t* code_max;
+  const float* lo;
+  const float* step;
+  int B, Hq, Hkv, G, P;
+  float* scores;
+};
+
 struct TopkArgs {
   const float* scores;         // [rows, P]
   int rows, P, kk;
@@ -239,6 +264,8 @@ cudaError_t attn_ctas_per_sm(int d, bool f16, bool sparse, bool q4, int* out);
 cudaError_t launch_merge(int d, const MergeArgs& m, int rows, cudaStream_t s);
 cudaError_t launch_token_attn(int d, bool f16, const TokenAttnArgs& a, int rows, cudaStream_t s);
 cudaError_t launch_score(int d, bool f16, const ScoreArgs& a, cudaStream_t s);
+cudaError_t launch_score8(int d, bool f16, const Score8Args& a, cudaStream_t s);
+cudaError_t launch_meta8(bool f16, const Meta8Args& a, cudaStream_t s);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
 cudaError_t launch_union(const UnionArgs& a, int units, cudaStream_t s);
 // Shared memory of unit_select_kernel for G heads of P pages (P <= kUnitMaxP).

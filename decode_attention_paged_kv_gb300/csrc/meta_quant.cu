@@ -201,6 +201,106 @@ __global__ void __launch_bounds__(256) dequant4_kernel(int64_t groups, const uin
   }
 }
 
+// ---------------------------------------------------------------- 8-bit
+// 8-bit page metadata: the bound of "TinyServe" (相关性函数实例化) needs only
+// m_j <= k <= M_j channel by channel, so the metadata can be stored on a
+// per-page grid dec(c) = fma(c, step, lo) with m rounded down and M rounded up
+// (one byte each instead of two):
+//   lo = min_i m_i, hi = max_i M_i (a zero as +0);
+//   step = fp32(fp32(hi - lo) / 255), raised one ulp at a time until
+//          dec(255) >= hi (0 when hi == lo);
+//   code_min_i = the largest c with dec(c) <= m_i,
+//   code_max_i = the smallest c with dec(c) >= M_i.
+// The codes are defined by those extremes, so the first guess (a product
+// with the step's reciprocal) only sets where the exact search starts.  One warp per page; lane l owns
+// channels D / 32 * l ...; pages past a shorter sequence are not written.
+__device__ __forceinline__ float value16f(uint32_t h, bool f16) {
+  return f16 ? __half2float(__ushort_as_half(static_cast<unsigned short>(h)))
+             : __uint_as_float(h << 16);
+}
+__device__ __forceinline__ float dec8(int c, float step, float lo) {
+  return __fmaf_rn(static_cast<float>(c), step, lo);
+}
+
+template <int D, bool F16>
+__global__ void __launch_bounds__(kMetaThreads) meta8_kernel(const Meta8Args a) {
+  griddep_launch_dependents();
+  griddep_wait();
+  constexpr int CPL = D / 32;  // channels per lane
+  const int lane = threadIdx.x & 31;
+  const int64_t total = static_cast<int64_t>(a.B) * a.Hkv * a.P;
+  const int64_t wstride = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t pg = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+       pg < total; pg += wstride) {
+    const int j = static_cast<int>(pg % a.P);
+    const int b = static_cast<int>(pg / (static_cast<int64_t>(a.Hkv) * a.P));
+    if (static_cast<int64_t>(j) * a.S >= seq_len_of(a.lens, b, a.N)) continue;
+    const int64_t off = pg * D + CPL * lane;
+    uint32_t wm[CPL / 2], wM[CPL / 2];
+    if constexpr (CPL == 4) {
+      const uint2 x = *reinterpret_cast<const uint2*>(a.meta_min + off);
+      const uint2 y = *reinterpret_cast<const uint2*>(a.meta_max + off);
+      wm[0] = x.x; wm[1] = x.y; wM[0] = y.x; wM[1] = y.y;
+    } else {
+      wm[0] = *reinterpret_cast<const uint32_t*>(a.meta_min + off);
+      wM[0] = *reinterpret_cast<const uint32_t*>(a.meta_max + off);
+    }
+    float m[CPL], M[CPL];
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      m[i] = value16f((wm[i / 2] >> (16 * (i & 1))) & 0xffffu, F16);
+      M[i] = value16f((wM[i / 2] >> (16 * (i & 1))) & 0xffffu, F16);
+    }
+    float lo = m[0], hi = M[0];
+#pragma unroll
+    for (int i = 1; i < CPL; ++i) {
+      lo = fminf(lo, m[i]);
+      hi = fmaxf(hi, M[i]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if (lo == 0.f) lo = 0.f;  // +0
+    if (hi == 0.f) hi = 0.f;
+    float step = 0.f;
+    if (hi > lo) {
+      step = __fdiv_rn(__fsub_rn(hi, lo), 255.f);
+      while (dec8(255, step, lo) < hi) step = __int_as_float(__float_as_int(step) + 1);
+    }
+    uint32_t cmw = 0, cMw = 0;
+    const float inv = step > 0.f ? __frcp_rn(step) : 0.f;  // for the first guesses only
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      int cm = 0, cM = 0;
+      if (step > 0.f) {
+        const float em = __fmul_rn(__fsub_rn(m[i], lo), inv);
+        const float eM = __fmul_rn(__fsub_rn(M[i], lo), inv);
+        cm = em >= 255.f ? 255 : (em >= 0.f ? static_cast<int>(em) : 0);
+        cM = eM >= 255.f ? 255 : (eM >= 0.f ? static_cast<int>(ceilf(eM)) : 0);
+        while (cm < 255 && dec8(cm + 1, step, lo) <= m[i]) ++cm;
+        while (cm > 0 && dec8(cm, step, lo) > m[i]) --cm;
+        while (cM > 0 && dec8(cM - 1, step, lo) >= M[i]) --cM;
+        while (cM < 255 && dec8(cM, step, lo) < M[i]) ++cM;
+      }
+      cmw |= static_cast<uint32_t>(cm) << (8 * i);
+      cMw |= static_cast<uint32_t>(cM) << (8 * i);
+    }
+    if constexpr (CPL == 4) {
+      *reinterpret_cast<uint32_t*>(a.code_min + off) = cmw;
+      *reinterpret_cast<uint32_t*>(a.code_max + off) = cMw;
+    } else {
+      *reinterpret_cast<uint16_t*>(a.code_min + off) = static_cast<uint16_t>(cmw);
+      *reinterpret_cast<uint16_t*>(a.code_max + off) = static_cast<uint16_t>(cMw);
+    }
+    if (lane == 0) {
+      a.lo[pg] = lo;
+      a.step[pg] = step;
+    }
+  }
+}
+
 int grid_for(int64_t threads, int block) {
   const int64_t blocks = ceil_div(threads, block);
   return static_cast<int>(blocks < 152 * 64 ? blocks : 152 * 64);
@@ -214,6 +314,16 @@ cudaError_t launch_meta(bool q4, bool f16, const MetaArgs& a, cudaStream_t s) {
   const dim3 grid(grid_for(work, kMetaThreads)), block(kMetaThreads);
   return q4 ? launch_pdl(meta_kernel<true>, grid, block, 0, s, a)
             : launch_pdl(meta_kernel<false>, grid, block, 0, s, a);
+}
+
+cudaError_t launch_meta8(bool f16, const Meta8Args& a, cudaStream_t s) {
+  const int64_t warps = static_cast<int64_t>(a.B) * a.Hkv * a.P;
+  const dim3 grid(grid_for(warps * 32, kMetaThreads)), block(kMetaThreads);
+  if (a.d == 128)
+    return f16 ? launch_pdl(meta8_kernel<128, true>, grid, block, 0, s, a)
+               : launch_pdl(meta8_kernel<128, false>, grid, block, 0, s, a);
+  return f16 ? launch_pdl(meta8_kernel<64, true>, grid, block, 0, s, a)
+             : launch_pdl(meta8_kernel<64, false>, grid, block, 0, s, a);
 }
 
 cudaError_t launch_quant4(int64_t rows, int d, const void* x, void* codes, void* gmin,

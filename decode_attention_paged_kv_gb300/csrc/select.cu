@@ -767,6 +767,116 @@ __global__ void __launch_bounds__(kScoreWarps * 32) score_kernel(const ScoreArgs
   }
 }
 
+// Bound scores over 8-bit metadata ("TinyServe" 相关性函数实例化 with the
+// outward-rounded grid of the 8-bit format): with dec(c) = lo + c * step,
+//   r = sum_i q_i dec(c_i) = lo * sum_i q_i + step * (q+ . code_max + q- . code_min).
+// The codes (0..255) are exact in bf16 and fp16, so both dot products run on
+// tensor cores: query heads on the M side (rows 0-7), eight pages a tile on
+// the N side.  Inside k-step ks, lane (g, t4) holds k positions 2 t4, 2 t4 + 1,
+// 2 t4 + 8, 2 t4 + 9; they carry channels D/4 * t4 + 4 ks + 0..3, for q and
+// codes alike (the order of a dot product's terms does not change it), so a
+// lane reads its D/4 code bytes of a page as contiguous 16-byte vectors.
+constexpr int kScore8Warps = 4;
+constexpr int kScore8TilesPerWarp = 4;
+constexpr int kScore8PagesPerCta = 8 * kScore8TilesPerWarp * kScore8Warps;
+
+template <bool F16>
+__device__ __forceinline__ uint32_t codes_pair(uint32_t w, int first) {
+  // two code bytes as exact 16-bit floats (2^23 + c in fp32, minus 2^23)
+  const float c0 = __uint_as_float(0x4B000000u | ((w >> (8 * first)) & 0xffu)) - 8388608.f;
+  const float c1 = __uint_as_float(0x4B000000u | ((w >> (8 * first + 8)) & 0xffu)) - 8388608.f;
+  if constexpr (F16) {
+    const __half2 h = __floats2half2_rn(c0, c1);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  } else {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(c0, c1);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+}
+
+template <int D, bool F16>
+__global__ void __launch_bounds__(kScore8Warps * 32) score8_kernel(const Score8Args a) {
+  constexpr int KS = D / 16, CPL = D / 4;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int b = blockIdx.z, kvh = blockIdx.y;
+  griddep_launch_dependents();
+  griddep_wait();
+  const int page0 = (blockIdx.x * kScore8Warps + warp) * kScore8TilesPerWarp * 8;
+  if (page0 >= a.P) return;
+  const bool head_ok = g < a.G;
+  // A fragments of q+ and q- for head g, and the lane's part of sum_i q_i
+  uint32_t qp[KS][2], qm[KS][2];
+  float qsum = 0.f;
+  {
+    const uint16_t* qrow = static_cast<const uint16_t*>(a.q) + b * a.q_sb +
+                           static_cast<int64_t>(kvh * a.G + (head_ok ? g : 0)) * a.q_sh +
+                           CPL * t4;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint2 w = make_uint2(0u, 0u);
+      if (head_ok) {
+        w.x = *reinterpret_cast<const uint32_t*>(qrow + 4 * ks);
+        w.y = *reinterpret_cast<const uint32_t*>(qrow + 4 * ks + 2);
+      }
+      qp[ks][0] = keep_sign(w.x, false);
+      qm[ks][0] = keep_sign(w.x, true);
+      qp[ks][1] = keep_sign(w.y, false);
+      qm[ks][1] = keep_sign(w.y, true);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t h = (((e < 2) ? w.x : w.y) >> (16 * (e & 1))) & 0xffffu;
+        qsum += F16 ? __half2float(__ushort_as_half(static_cast<unsigned short>(h)))
+                    : __uint_as_float(h << 16);
+      }
+    }
+    qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+    qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
+  }
+  const int64_t pbase = (static_cast<int64_t>(b) * a.Hkv + kvh) * a.P;
+#pragma unroll 1
+  for (int t = 0; t < kScore8TilesPerWarp; ++t) {
+    const int tile0 = page0 + 8 * t;
+    if (tile0 >= a.P) break;
+    const int pn = tile0 + g;  // this lane's page on the N side
+    uint4 vmx[CPL / 16], vmn[CPL / 16];
+#pragma unroll
+    for (int v = 0; v < CPL / 16; ++v) {
+      if (pn < a.P) {
+        const int64_t off = (pbase + pn) * D + CPL * t4 + 16 * v;
+        vmx[v] = __ldcs(reinterpret_cast<const uint4*>(a.code_max + off));
+        vmn[v] = __ldcs(reinterpret_cast<const uint4*>(a.code_min + off));
+      } else {
+        vmx[v] = make_uint4(0u, 0u, 0u, 0u);
+        vmn[v] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      // k-step ks: code bytes 4 ks .. 4 ks + 3 of the lane's run
+      const uint4& X = vmx[ks / 4];
+      const uint4& Y = vmn[ks / 4];
+      const uint32_t wx = (ks & 3) == 0 ? X.x : (ks & 3) == 1 ? X.y : (ks & 3) == 2 ? X.z : X.w;
+      const uint32_t wy = (ks & 3) == 0 ? Y.x : (ks & 3) == 1 ? Y.y : (ks & 3) == 2 ? Y.z : Y.w;
+      mma16816<F16>(sc, qp[ks][0], 0u, qp[ks][1], 0u, codes_pair<F16>(wx, 0),
+                    codes_pair<F16>(wx, 2));
+      mma16816<F16>(sc, qm[ks][0], 0u, qm[ks][1], 0u, codes_pair<F16>(wy, 0),
+                    codes_pair<F16>(wy, 2));
+    }
+    // head g, pages tile0 + 2 t4 + e
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int page = tile0 + 2 * t4 + e;
+      if (head_ok && page < a.P) {
+        const float lo = a.lo[pbase + page], st = a.step[pbase + page];
+        a.scores[(static_cast<int64_t>(b) * a.Hq + kvh * a.G + g) * a.P + page] =
+            __fmaf_rn(st, sc[e], lo * qsum);
+      }
+    }
+  }
+}
+
 template <bool SMEM>
 __global__ void __launch_bounds__(kSelMaxThreads) topk_kernel(const TopkArgs a) {
   extern __shared__ uint32_t s_keys[];
@@ -1241,6 +1351,16 @@ cudaError_t launch_score(int d, bool f16, const ScoreArgs& a, cudaStream_t s) {
   }
   return f16 ? launch_pdl(score_kernel<64, true, false>, grid, block, 0, s, a)
              : launch_pdl(score_kernel<64, false, false>, grid, block, 0, s, a);
+}
+
+cudaError_t launch_score8(int d, bool f16, const Score8Args& a, cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>(ceil_div(a.P, kScore8PagesPerCta)), a.Hkv, a.B);
+  const dim3 block(kScore8Warps * 32);
+  if (d == 128)
+    return f16 ? launch_pdl(score8_kernel<128, true>, grid, block, 0, s, a)
+               : launch_pdl(score8_kernel<128, false>, grid, block, 0, s, a);
+  return f16 ? launch_pdl(score8_kernel<64, true>, grid, block, 0, s, a)
+             : launch_pdl(score8_kernel<64, false>, grid, block, 0, s, a);
 }
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {

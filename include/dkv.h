@@ -19,6 +19,10 @@
  *                           TinyServe, 相关性函数实例化, 问题公式化定义 and
  *                           Algorithm 1 (Fused Query-Aware Sparse Attention
  *                           Kernel), steps 1-4.
+ *   dkv_kv_meta8_build /    the same metadata in one byte per channel: a
+ *   dkv_decode_attn_select_ per-page grid with m rounded down and M rounded up,
+ *   meta8                   so r stays an upper bound (TinyServe,
+ *                           相关性函数实例化; the byte form is not on the pages).
  *   dkv_kv_quant4 /         4-bit KV format: groups of 64 channels along the head
  *   dkv_kv_dequant4         dimension, per-group min / max, 4-bit codes,
  *                           dequantised to fp16 before use.
@@ -191,6 +195,37 @@ dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_
                                   const void* meta_max, int32_t top_k, void* out,
                                   int32_t out_dtype, int32_t* selected, void* workspace,
                                   size_t workspace_bytes, void* stream);
+
+/* 8-bit page metadata from (meta_min, meta_max) [B, Hkv, P, d] of dtype
+   meta_dtype (DKV_BF16 | DKV_FP16).  TinyServe's bound (相关性函数实例化) needs
+   only m_j <= k <= M_j channel by channel; this stores that interval on a
+   per-page grid at one byte per channel instead of two.  No page defines this
+   form; it is the plainest that keeps r an upper bound.  Per page:
+     lo = min_i m_i, hi = max_i M_i (a zero stored as +0), written to lo [B, Hkv, P]
+     step = fp32(fp32(hi - lo) / 255), raised one ulp at a time until
+            dec(255) >= hi, where dec(c) = fmaf(c, step, lo); 0 when hi == lo;
+            written to step [B, Hkv, P] (fp32)
+     code_min [B, Hkv, P, d] u8 = the largest c with dec(c) <= m_i
+     code_max [B, Hkv, P, d] u8 = the smallest c with dec(c) >= M_i.
+   Uses p->batch, num_kv_heads, head_dim, seq_len, page_size and seq_lens
+   (pages past a shorter sequence are not written).  Metadata must be finite.
+   code_min / code_max / meta 16-byte aligned, lo / step 4-byte aligned. */
+dkv_status dkv_kv_meta8_build(const dkv_params* p, const void* meta_min, const void* meta_max,
+                              int32_t meta_dtype, void* code_min, void* code_max, void* lo,
+                              void* step, void* stream);
+
+/* dkv_decode_attn_select over 8-bit metadata (dkv_kv_meta8_build): the bound
+   score of page j is r = sum_i q_i * dec(q_i >= 0 ? code_max_i : code_min_i),
+   an upper bound of max q.k over the page's keys, then top-K, union and
+   attention exactly as in dkv_decode_attn_select.  Same workspace
+   (dkv_workspace_bytes(p, top_k)), flags, page sizes, cache formats and
+   per-sequence lengths. */
+dkv_status dkv_decode_attn_select_meta8(const dkv_params* p, const void* q, const dkv_kv* K,
+                                        const dkv_kv* V, const void* code_min,
+                                        const void* code_max, const void* lo, const void* step,
+                                        int32_t top_k, void* out, int32_t out_dtype,
+                                        int32_t* selected, void* workspace,
+                                        size_t workspace_bytes, void* stream);
 
 /* Token-level sparse decode attention ("FlexGen: High-Throughput Generative
    Inference of Large Language Models with a Single GPU" (解读), its sparse

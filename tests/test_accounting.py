@@ -46,3 +46,14 @@ def test_token_bytes():
     # GQA: K once per kv head, V rows once per q head
     assert (acc.token_bytes(1, 32, 8, 128, 32768, 3276) ==
             32 * 128 * 2 + 8 * 32768 * 128 * 2 + 32 * 3276 * 128 * 2 + 32 * 128 * 4)
+
+
+def test_meta8_byte_counts():
+    # 32K GQA shape: 16-bit metadata 128 MiB read, codes 64 MiB + grid 1 MiB written
+    B, Hkv, d, N = 16, 8, 128, 32768
+    P = N // 16
+    assert acc.meta8_bytes(B, Hkv, d, N) == 2 * B * Hkv * P * d * 2 + 2 * B * Hkv * P * d + 8 * B * Hkv * P
+    full16 = acc.select_bytes(B, 32, Hkv, d, N, 1000)
+    full8 = acc.select8_bytes(B, 32, Hkv, d, N, 1000)
+    # the 8-bit metadata scan is half the 16-bit one plus 8 bytes a page
+    assert full16 - full8 == 2 * B * Hkv * P * d - 8 * B * Hkv * P
