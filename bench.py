@@ -651,9 +651,21 @@ def workload_leg(name, dev, stream, reps=10):
         dkv.decode_attn_select(q, state["K"], state["V"], state["meta"], w.top_k, out=out_sel,
                                selected=sel, workspace=ws_sel)
 
+    # the same selection over 8-bit metadata (built from the 16-bit one)
+    out_sel8, sel8 = torch.empty_like(out_sel), torch.empty_like(sel)
+
+    def meta8():
+        state["meta8"] = dkv.kv_meta8_build(state["meta"])
+
+    def select8():
+        dkv.decode_attn_select(q, state["K"], state["V"], state["meta8"], w.top_k,
+                               out=out_sel8, selected=sel8, workspace=ws_sel)
+
     calls += [("kv_meta_build", meta, acc.meta_bytes(w.B, w.Hkv, w.d, w.N, w.S, q4=w.q4)),
               ("decode_attn_full", full, acc.full_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, q4=w.q4)),
-              ("decode_attn_select", select, None)]
+              ("decode_attn_select", select, None),
+              ("kv_meta8_build", meta8, acc.meta8_bytes(w.B, w.Hkv, w.d, w.N, w.S)),
+              ("decode_attn_select (8-bit metadata)", select8, "select8")]
     if not w.q4:
         # token-level sparse attention keeping the top 10% of the tokens per head
         ktok = max(1, w.N // 10)
@@ -690,6 +702,9 @@ def workload_leg(name, dev, stream, reps=10):
     for c, _, nbytes in calls:
         if nbytes is None:
             nbytes = acc.select_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, gathered, w.S, q4=w.q4)
+        elif nbytes == "select8":
+            nbytes = acc.select8_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, union_tokens(sel8, w), w.S,
+                                       q4=w.q4)
         gbs = nbytes / (times[c] * 1e-3) / 1e9
         res[c] = {"ms": round(times[c], 5), "alg_bytes": nbytes, "GB/s": round(gbs, 1),
                   "frac_of_measured_hbm": round(gbs / peak, 4),

@@ -57,14 +57,16 @@ def meta8_bytes(B, Hkv, d, N, S=16, elt=2) -> int:
     return 2 * B * Hkv * P * d * elt + 2 * B * Hkv * P * d + 2 * B * Hkv * P * 4
 
 
-def select8_bytes(B, Hq, Hkv, d, N, gathered_tokens, S=16, elt=2, out_elt=4) -> int:
+def select8_bytes(B, Hq, Hkv, d, N, gathered_tokens, S=16, elt=2, out_elt=4,
+                  q4=False) -> int:
     """q + 8-bit metadata of every page (two code bytes per channel, lo and
     step) + K and V of the gathered tokens + out."""
     P = (N + S - 1) // S
     q = B * Hq * d * elt
     out = B * Hq * d * out_elt
     meta = 2 * B * Hkv * P * d + 2 * B * Hkv * P * 4
-    return q + meta + 2 * gathered_tokens * d * elt + out
+    per_tok = (d // 2 + 2 * (d // 64) * 2) if q4 else d * elt
+    return q + meta + 2 * gathered_tokens * per_tok + out
 
 
 def quant4_bytes(rows, d) -> int:
