@@ -619,6 +619,9 @@ dkv_status dkv_kv_meta8_build(const dkv_params* p, const void* meta_min, const v
       !aligned16(code_max) || (reinterpret_cast<uintptr_t>(lo) & 3u) ||
       (reinterpret_cast<uintptr_t>(step) & 3u))
     return DKV_ERR_ALIGN;
+  const int64_t pages =
+      static_cast<int64_t>(p->batch) * p->num_kv_heads * ceil_div(p->seq_len, p->page_size);
+  if (pages >= (static_cast<int64_t>(1) << 31)) return DKV_ERR_UNSUPPORTED;
   dkv::Meta8Args a{};
   a.meta_min = static_cast<const uint16_t*>(meta_min);
   a.meta_max = static_cast<const uint16_t*>(meta_max);

@@ -228,14 +228,15 @@ __global__ void __launch_bounds__(kMetaThreads) meta8_kernel(const Meta8Args a) 
   griddep_wait();
   constexpr int CPL = D / 32;  // channels per lane
   const int lane = threadIdx.x & 31;
-  const int64_t total = static_cast<int64_t>(a.B) * a.Hkv * a.P;
-  const int64_t wstride = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-  for (int64_t pg = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-       pg < total; pg += wstride) {
-    const int j = static_cast<int>(pg % a.P);
-    const int b = static_cast<int>(pg / (static_cast<int64_t>(a.Hkv) * a.P));
+  // (page counts below 2^31, checked by the host: 32-bit index arithmetic)
+  const uint32_t total = static_cast<uint32_t>(a.B) * a.Hkv * a.P;
+  const uint32_t per_b = static_cast<uint32_t>(a.Hkv) * a.P;
+  const uint32_t wstride = gridDim.x * (blockDim.x >> 5);
+  for (uint32_t pg = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; pg < total; pg += wstride) {
+    const int j = static_cast<int>(pg % static_cast<uint32_t>(a.P));
+    const int b = static_cast<int>(pg / per_b);
     if (static_cast<int64_t>(j) * a.S >= seq_len_of(a.lens, b, a.N)) continue;
-    const int64_t off = pg * D + CPL * lane;
+    const int64_t off = static_cast<int64_t>(pg) * D + CPL * lane;
     uint32_t wm[CPL / 2], wM[CPL / 2];
     if constexpr (CPL == 4) {
       const uint2 x = *reinterpret_cast<const uint2*>(a.meta_min + off);

@@ -782,9 +782,10 @@ constexpr int kScore8PagesPerCta = 8 * kScore8TilesPerWarp * kScore8Warps;
 
 template <bool F16>
 __device__ __forceinline__ uint32_t codes_pair(uint32_t w, int first) {
-  // two code bytes as exact 16-bit floats (2^23 + c in fp32, minus 2^23)
-  const float c0 = __uint_as_float(0x4B000000u | ((w >> (8 * first)) & 0xffu)) - 8388608.f;
-  const float c1 = __uint_as_float(0x4B000000u | ((w >> (8 * first + 8)) & 0xffu)) - 8388608.f;
+  // two code bytes as exact 16-bit floats: each byte placed under the exponent
+  // of 2^23 (one byte permute gives the fp32 2^23 + c), minus 2^23
+  const float c0 = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7650u | first)) - 8388608.f;
+  const float c1 = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7650u | (first + 1))) - 8388608.f;
   if constexpr (F16) {
     const __half2 h = __floats2half2_rn(c0, c1);
     return *reinterpret_cast<const uint32_t*>(&h);
