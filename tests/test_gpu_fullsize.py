@@ -3,7 +3,8 @@ benchmark times (inputs drawn on the GPU with the benchmark's seeds, the same
 calls and default workspaces), checked on sampled (batch, kv head) units that
 the oracle computes one by one: metadata and 4-bit codes bit-exact, selections
 within the 1e-5 band, outputs within 2e-3.  The 1M-token workload also checks
-that one kv head per call gives bitwise the all-heads output.
+that one kv head per call gives bitwise the all-heads output, and the 32K
+GQA workload is checked once more over 8-bit page metadata.
 """
 
 import math
@@ -109,3 +110,34 @@ def test_q4_workload_full_size(dev):
             assert np.array_equal(bits(x4.gmax[b:b + 1, h:h + 1].cpu()), gmax)
             planes.append(oracle.dequant4(codes, gmin, gmax))
         _check_unit(w, b, h, q, planes[0], planes[1], 1, out_full, meta, out_sel, sel)
+
+
+def test_meta8_select_full_size(dev):
+    # the 32K-token GQA workload with 8-bit page metadata, as the benchmark's
+    # meta8 leg runs it: codes, lo and step bit-exact on sampled units, the
+    # selection within the band of the oracle's 8-bit scores, outputs vs the
+    # oracle over the GPU's pages
+    import decode_attention_paged_kv_gb300 as dkv
+    w = WORKLOADS[2]
+    q, K, V = make_inputs(w, seed=44, device=dev)
+    m8 = dkv.kv_meta8_build(dkv.kv_meta_build(K))
+    out, sel = dkv.decode_attn_select(q, K, V, m8, w.top_k, return_selected=True)
+    torch.cuda.synchronize()
+    scale = 1.0 / math.sqrt(w.d)
+    for b, h in _units(w, 4):
+        Kb = bits(K[b:b + 1, h:h + 1].cpu())
+        Vb = bits(V[b:b + 1, h:h + 1].cpu())
+        qs = bits(_head_slice(q, b, h, w.G).cpu())
+        mn, mx = oracle.meta(Kb, w.S, 0)
+        cmin, cmax, lo, step = oracle.meta8(mn, mx, 0)
+        assert np.array_equal(m8.code_min[b:b + 1, h:h + 1].cpu().numpy(), cmin)
+        assert np.array_equal(m8.code_max[b:b + 1, h:h + 1].cpu().numpy(), cmax)
+        assert np.array_equal(m8.lo[b:b + 1, h:h + 1].cpu().numpy().view(np.uint32),
+                              lo.view(np.uint32))
+        assert np.array_equal(m8.step[b:b + 1, h:h + 1].cpu().numpy().view(np.uint32),
+                              step.view(np.uint32))
+        r = oracle.scores8(qs, cmin, cmax, lo, step, 0)
+        s = _head_slice(sel, b, h, w.G).cpu().numpy()
+        check_selection(s.reshape(w.G, -1), r.reshape(w.G, -1), w.top_k)
+        ref = oracle.attention(qs, Kb, Vb, w.S, scale, 0, sel=s)
+        assert max_abs(_head_slice(out, b, h, w.G), ref) <= ATOL, (b, h)
