@@ -68,6 +68,25 @@ def parse_args():
 
 
 # ------------------------------------------------------------------ helpers
+def rank_seed(widx: int, rank: int) -> int:
+    """Each rank draws its own batch (weak scaling: no rank repeats another's work)."""
+    return 42 + widx + 1000 * rank
+
+
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time: the job is done when every rank is."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_queries_per_s(world: int, batch: int, ms_step: float) -> float:
+    """Queries of all ranks (each its own batch) per second of the slowest rank."""
+    return world * batch / (ms_step * 1e-3)
+
+
 def dist_info():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -213,7 +232,7 @@ def run_dkv(args, rank, world, local):
         w = w.replace(B=args.batch)
     if w.q4:
         raise SystemExit("the 4-bit workload is a parity case; the bench times the dense path")
-    q, K, V = make_inputs(w, seed=42 + widx + 1000 * rank, device=dev)
+    q, K, V = make_inputs(w, seed=rank_seed(widx, rank), device=dev)
     stream = torch.cuda.current_stream(dev)
 
     ws_full = torch.zeros(dkv.workspace_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, 0), dtype=torch.uint8,
@@ -264,11 +283,7 @@ def run_dkv(args, rank, world, local):
         t1.record(stream)
         torch.cuda.synchronize()
     barrier()
-    ms_total = t0.elapsed_time(t1)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(t0.elapsed_time(t1), world, dev)
     ms_step = ms_total / args.steps
     per_call = {c: statistics.mean(a.elapsed_time(b) for a, b in ev[c]) for c in calls}
 
@@ -300,7 +315,7 @@ def run_dkv(args, rank, world, local):
                 "frac": round(dom_gbs / peak, 4),
                 "frac_of_8tbs": round(dom_gbs / NOMINAL_HBM_GBS, 4),
                 "traffic": ncu_traffic(dom)}
-    value = world * w.B / (ms_step * 1e-3)
+    value = job_queries_per_s(world, w.B, ms_step)
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "queries/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms_step, 5),
