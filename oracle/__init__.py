@@ -72,6 +72,9 @@ def _load():
             lib.oracle_scores8.argtypes = [i32, i32, i32, i32, i32, i32, P, P, P, P, P, P]
             lib.oracle_quant4.argtypes = [i64, i32, P, P, P, P]
             lib.oracle_dequant4.argtypes = [i64, i32, P, P, P, P]
+            lib.oracle_q4_step.argtypes = [ctypes.c_uint16, ctypes.c_uint16,
+                                           ctypes.POINTER(ctypes.c_int)]
+            lib.oracle_q4_step.restype = dbl
             _lib = lib
     return _lib
 
@@ -245,3 +248,14 @@ def dequant4(codes: np.ndarray, gmin: np.ndarray, gmax: np.ndarray) -> np.ndarra
     x = np.empty(codes.shape[:-1] + (d,), np.uint16)
     _load().oracle_dequant4(rows, d, _ptr(codes), _ptr(gmin), _ptr(gmax), _ptr(x))
     return x
+
+
+def q4_step(mn: int, mx: int):
+    """The 4-bit format's step for a group with fp16 min / max bits (mn, mx).
+
+    Returns (step as a float, tiny) where tiny is True for groups whose range is
+    below 451 * 2^-24 (the step then lies on a finer grid than fp16 offers).
+    """
+    tiny = ctypes.c_int(0)
+    s = _load().oracle_q4_step(int(mn), int(mx), ctypes.byref(tiny))
+    return float(s), bool(tiny.value)

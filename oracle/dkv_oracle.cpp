@@ -368,28 +368,94 @@ void oracle_attention(int B, int Hq, int Hkv, int N, int d, int S, int is_fp16,
 // 4-bit KV format  [FG 4-bit 近似方法]
 // The page fixes: groups of 64 elements along the hidden dimension of each
 // (token, head) row, per-group min and max, 4-bit integer codes, values
-// dequantised back to FP16 before use.  It leaves the rounding open; the
-// reading adopted here, and shared by the GPU kernels through the format, is:
-//   mn, mx   = min / max of the group's fp16 values (total order, -0 < +0)
-//   step     = fp16_rn( fp32( fp32(mx - mn) / 15 ) )          (15 steps, 16 levels)
-//   code_i   = 0 if step == 0, else
-//              clamp( rint_even( fp32( fp32(x_i - mn) / step ) ), 0, 15 )
-//   x^_i     = fp16_rn( code_i * step + mn )     (exact, rounded once to fp16),
-//              replaced by mx where it exceeds mx (the rounded step can carry
-//              the top codes past the group max, near the fp16 limit even to
-//              infinity; the reconstruction stays inside [mn, mx])
-// fp32(.) is one IEEE binary32 round-to-nearest-even operation.  Codes are
-// packed two per byte, channel 2i in the low nibble.
+// dequantised back to FP16 before use.  It leaves the step and the rounding
+// open.  The reading adopted here, and shared by the GPU kernels through the
+// format, puts 16 levels at mn + c * s, c = 0 .. 15, with the step s rounded
+// DOWN from (mx - mn) / 15, so no level passes the group max:
+//   mn, mx  = min / max of the group's fp16 values (total order, -0 < +0)
+//   range   = fp32_down(mx - mn)
+//   normal groups (range >= 451 * 2^-24):
+//     s = fp16_down( fp32_down( range / 15 ) )
+//   tiny groups (range < 451 * 2^-24, where an fp16 step is too coarse):
+//     e = floor(log2(max(|mn|, |mx|))), g = 2^(e - 22),
+//     s = floor(range / (15 g)) * g                (0 when range == 0)
+//   code_i = 0 if s == 0, else the c in [0, 15] nearest to (x_i - mn) / s in
+//            exact arithmetic (ties to the even c; above 15 -> 15)
+//   x^_i   = fp16_rn( mn + code_i * s )  -- the exact value, rounded once
+// fp32_down / fp16_down: the largest binary32 / binary16 value <= the exact
+// result.  Why this bounds the error by (mx - mn)/30 + half an fp16 ulp of x^
+// for every finite group: s <= (mx - mn)/15, so every x in [mn, mn + 15 s] is
+// within s/2 of a level; and s >= (29/30)(mx - mn)/15 (normal groups: two
+// downward roundings of 2^-23 or less each and one fp16 rounding of 2^-10
+// relative, or of less than 2^-24 absolute with range >= 451 * 2^-24; tiny
+// groups: g <= (mx - mn)/450), so x in (mn + 15 s, mx] is within
+// mx - mn - 15 s <= (mx - mn)/30 of the top level.  The level mn + c s is
+// exact in double here, so x^ is one rounding of it.  Codes are packed two per
+// byte, channel 2i in the low nibble.
 // ---------------------------------------------------------------------------
 namespace {
-float group_step(uint16_t mn, uint16_t mx) {
-  const float fmn = static_cast<float>(fp16_value(mn));
-  const float fmx = static_cast<float>(fp16_value(mx));
-  const float range = fmx - fmn;       // one fp32 rounding
-  const float third = range / 15.0f;   // one fp32 rounding
-  return static_cast<float>(fp16_value(fp16_round(static_cast<double>(third))));
+// The largest binary32 value <= v (v an exactly known real held in a double).
+float f32_down(double v) {
+  float f = static_cast<float>(v);  // round to nearest
+  if (static_cast<double>(f) > v) f = std::nextafterf(f, -INFINITY);
+  return f;
+}
+
+// The largest binary16 value <= v, for 0 <= v < 65520, as a double.
+double f16_down(double v) {
+  if (v <= 0.0) return 0.0;
+  int e2;
+  std::frexp(v, &e2);
+  int ex = e2 - 1;  // v in [2^ex, 2^(ex+1))
+  if (ex < -14) ex = -14;
+  const double quantum = std::ldexp(1.0, ex - 10);
+  return std::floor(v / quantum) * quantum;  // v / quantum is exact (power of two)
+}
+
+// fp32_down(r / 15) for a binary32 r >= 0: the largest binary32 q with
+// 15 q <= r (15 q and r are exact in double).
+float div15_down(float r) {
+  float q = static_cast<float>(static_cast<double>(r) / 15.0);
+  while (15.0 * static_cast<double>(q) > static_cast<double>(r)) q = std::nextafterf(q, 0.0f);
+  while (15.0 * static_cast<double>(std::nextafterf(q, INFINITY)) <= static_cast<double>(r))
+    q = std::nextafterf(q, INFINITY);
+  return q;
+}
+
+// The group's step s (exact, as a double) from its stored min / max.
+double group_step(uint16_t mn, uint16_t mx, int* tiny) {
+  const double fmn = fp16_value(mn), fmx = fp16_value(mx);
+  const float range = f32_down(fmx - fmn);  // fmx - fmn is exact in double
+  if (static_cast<double>(range) >= 451.0 * std::ldexp(1.0, -24)) {
+    if (tiny) *tiny = 0;
+    return f16_down(static_cast<double>(div15_down(range)));
+  }
+  if (tiny) *tiny = 1;
+  const double a = std::max(std::fabs(fmn), std::fabs(fmx));
+  if (range == 0.0f || a == 0.0) return 0.0;
+  int e2;
+  std::frexp(a, &e2);  // a = m 2^e2, m in [0.5, 1): floor(log2 a) = e2 - 1
+  const double g = std::ldexp(1.0, e2 - 1 - 22);
+  const double r = static_cast<double>(range) / g;  // an integer below 2^24: exact
+  return std::floor(r / 15.0) * g;
+}
+
+// The code of x: the nearest level index, ties to even, clamped to [0, 15].
+int nearest_code(double x, double mn, double s) {
+  if (s == 0.0) return 0;
+  const double diff = x - mn;  // exact: both fp16
+  int c = static_cast<int>(std::floor(diff / s));
+  while ((c + 1) * s <= diff) ++c;  // c s is exact: c < 2^5, s has < 25 bits
+  while (c > 0 && c * s > diff) --c;
+  const double r = 2.0 * diff - (2.0 * c + 1.0) * s;  // exact
+  if (r > 0.0 || (r == 0.0 && (c & 1))) ++c;
+  return std::min(c, 15);
 }
 }  // namespace
+
+// The step and regime of the group (mn, mx), exposed so the tests can pin the
+// step's bracket (29/30)(mx - mn)/15 <= s <= (mx - mn)/15 directly.
+double oracle_q4_step(uint16_t mn, uint16_t mx, int* tiny) { return group_step(mn, mx, tiny); }
 
 void oracle_quant4(int64_t rows, int d, const uint16_t* x, uint8_t* codes, uint16_t* gmin,
                    uint16_t* gmax) {
@@ -406,21 +472,12 @@ void oracle_quant4(int64_t rows, int d, const uint16_t* x, uint8_t* codes, uint1
       }
       gmin[r * ng + g] = lo;
       gmax[r * ng + g] = hi;
-      const float step = group_step(lo, hi);
-      const float fmn = static_cast<float>(fp16_value(lo));
+      const double step = group_step(lo, hi, nullptr);
+      const double fmn = fp16_value(lo);
       for (int i = 0; i < 64; i += 2) {
-        int c[2] = {0, 0};
-        for (int e = 0; e < 2; ++e) {
-          if (step != 0.0f) {
-            const float xv = static_cast<float>(fp16_value(xr[g * 64 + i + e]));
-            const float diff = xv - fmn;   // one fp32 rounding
-            const float u = diff / step;   // one fp32 rounding
-            float rc = std::nearbyint(u);  // ties to even
-            rc = std::min(15.0f, std::max(0.0f, rc));
-            c[e] = static_cast<int>(rc);
-          }
-        }
-        cr[(g * 64 + i) / 2] = static_cast<uint8_t>(c[0] | (c[1] << 4));
+        const int c0 = nearest_code(fp16_value(xr[g * 64 + i]), fmn, step);
+        const int c1 = nearest_code(fp16_value(xr[g * 64 + i + 1]), fmn, step);
+        cr[(g * 64 + i) / 2] = static_cast<uint8_t>(c0 | (c1 << 4));
       }
     }
   });
@@ -432,16 +489,14 @@ void oracle_dequant4(int64_t rows, int d, const uint8_t* codes, const uint16_t* 
   parallel_for(rows, [&](int64_t r) {
     for (int g = 0; g < ng; ++g) {
       const uint16_t lo = gmin[r * ng + g], hi = gmax[r * ng + g];
-      const double step = static_cast<double>(group_step(lo, hi));
+      const double step = group_step(lo, hi, nullptr);
       const double mn = fp16_value(lo);
-      const double mx = fp16_value(hi);
       for (int i = 0; i < 64; ++i) {
         const int ch = g * 64 + i;
         const uint8_t byte = codes[r * (d / 2) + ch / 2];
         const int c = (ch & 1) ? (byte >> 4) : (byte & 0xf);
-        // c * step + mn is exact in double (fp16-scale operands); round once.
-        const uint16_t v = fp16_round(static_cast<double>(c) * step + mn);
-        x[r * d + ch] = (fp16_value(v) > mx) ? hi : v;
+        // mn + c * step is exact in double (fewer than 43 significant bits); round once.
+        x[r * d + ch] = fp16_round(mn + static_cast<double>(c) * step);
       }
     }
   });

@@ -56,12 +56,14 @@ def case_sparse_small():
 
 def case_quant4():
     rng = np.random.default_rng(99)
-    x = rng.standard_normal((6, 128)) * np.array([[0.01], [1], [3], [100], [1e-5], [1]])
+    # scales from fp16 subnormals (the tiny-range step grid) to 100
+    x = rng.standard_normal((7, 128)) * np.array(
+        [[0.01], [1], [3], [100], [1e-5], [1], [3e-7]])
     x[5] = 7.0
     xb = np.asarray(x, np.float64).astype(np.float16).view(np.uint16)
     codes, gmin, gmax = oracle.quant4(xb)
     xh = oracle.dequant4(codes, gmin, gmax)
-    return {"x": xb.ravel().tolist(), "rows": 6, "d": 128,
+    return {"x": xb.ravel().tolist(), "rows": 7, "d": 128,
             "codes": codes.ravel().tolist(), "gmin": gmin.ravel().tolist(),
             "gmax": gmax.ravel().tolist(), "xhat": xh.ravel().tolist()}
 
