@@ -145,7 +145,8 @@ __device__ __forceinline__ void q4_copy_run(const AttnArgs& a, int b, int kvh, i
 // into stage slot `slot`.  The valid tokens' group bounds are loaded with plain
 // loads (released by the caller's barrier arrival, which counts the codes'
 // 2 * nt * d/2 bytes) and the missing tokens' bounds zeroed, so whatever codes
-// their rows hold dequantise to 0; then only the valid tokens' codes are
+// their rows hold dequantise to 0 (a zero-width group: step 0; the page takes
+// the consumers' tiny-group path); then only the valid tokens' codes are
 // copied, so nothing is read past the cache.
 template <typename C, int D>
 __device__ __forceinline__ void q4_ragged_bounds(const AttnArgs& a, int b, int kvh, int page,
@@ -185,14 +186,17 @@ __device__ __forceinline__ void q4_ragged_codes(const AttnArgs& a, int b, int kv
 //     D/8 n + cn.
 // A nibble masked into the mantissa of 1024 (bits 0-3) or 64 (bits 4-7) gives
 // bias + code exactly; subtracting the bias leaves the code, then
-// x = fp16(code * step + mn) by one fp16 FMA, replaced by mx where it exceeds
-// mx -- the dequantisation of the 4-bit format, bit for bit.
+// x = fp16(code * step + mn) by one fp16 FMA -- the dequantisation of the
+// 4-bit format, bit for bit.  A page with a tiny group anywhere in the warp
+// (range below 451 * 2^-24: its step is an fp32 value) takes a slower path
+// that dequantises every pair from its group's min and max.
 template <int D>
 struct Q4Page {
   uint32_t kc[2][D / 32];  // K codes, tokens g and g + 8
   uint32_t vc[4][D / 64];  // V codes, tokens 2 t4, 2 t4 + 1, 2 t4 + 8, 2 t4 + 9
-  __half kmn[2], kmx[2];   // K group bounds, tokens g and g + 8
-  uint32_t vmn[2], vmx[2]; // V group bounds, half pairs for tokens (2 t4, 2 t4 + 1) and + 8
+  __half kmn[2], kx[2];    // K group min and step (group max on a tiny page), tokens g, g + 8
+  uint32_t vmn[2], vx[2];  // V: the same as half pairs, tokens (2 t4, 2 t4 + 1) and + 8
+  bool tiny;               // warp-uniform: the page has a tiny group
 };
 
 template <typename C, int D>
@@ -218,7 +222,7 @@ __device__ __forceinline__ void q4_load(const uint8_t* st, int slot, int g, int 
       r.kc[h][1] = w.y;
     }
     r.kmn[h] = gb[t * ng + gk];
-    r.kmx[h] = gb[kBound + t * ng + gk];
+    r.kx[h] = gb[kBound + t * ng + gk];
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -242,10 +246,31 @@ __device__ __forceinline__ void q4_load(const uint8_t* st, int slot, int g, int 
       const uint2 lo = *reinterpret_cast<const uint2*>(vmn);
       const uint2 hi = *reinterpret_cast<const uint2*>(vmx);
       r.vmn[h] = __byte_perm(lo.x, lo.y, gv ? 0x7632 : 0x5410);
-      r.vmx[h] = __byte_perm(hi.x, hi.y, gv ? 0x7632 : 0x5410);
+      r.vx[h] = __byte_perm(hi.x, hi.y, gv ? 0x7632 : 0x5410);
     } else {
       r.vmn[h] = *reinterpret_cast<const uint32_t*>(vmn);
-      r.vmx[h] = *reinterpret_cast<const uint32_t*>(vmx);
+      r.vx[h] = *reinterpret_cast<const uint32_t*>(vmx);
+    }
+  }
+  // Group bounds -> steps (fp16 steps of normal groups; a tiny group keeps its max).
+  float kr[2], vr[4];
+  bool tiny = false;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    kr[h] = q4_range(r.kmn[h], r.kx[h]);
+    const __half2 mn = *reinterpret_cast<const __half2*>(&r.vmn[h]);
+    const __half2 mx = *reinterpret_cast<const __half2*>(&r.vx[h]);
+    vr[2 * h] = q4_range(__low2half(mn), __low2half(mx));
+    vr[2 * h + 1] = q4_range(__high2half(mn), __high2half(mx));
+    tiny |= fminf(kr[h], fminf(vr[2 * h], vr[2 * h + 1])) < kQ4TinyRange;
+  }
+  r.tiny = __any_sync(0xffffffffu, tiny);
+  if (!r.tiny) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      r.kx[h] = q4_step16(kr[h]);
+      const __half2 st = __halves2half2(q4_step16(vr[2 * h]), q4_step16(vr[2 * h + 1]));
+      r.vx[h] = *reinterpret_cast<const uint32_t*>(&st);
     }
   }
 }
@@ -256,11 +281,30 @@ __device__ __forceinline__ __half2 q4_codes(uint32_t w, uint32_t mask, uint32_t 
   return __hsub2(*reinterpret_cast<const __half2*>(&x), *reinterpret_cast<const __half2*>(&bias));
 }
 
-__device__ __forceinline__ uint32_t q4_value(__half2 code, __half2 step, __half2 mn, __half2 mx) {
+// A pair of codes of normal groups: fp16(code * step + mn), one rounding.
+__device__ __forceinline__ uint32_t q4_value(__half2 code, __half2 step, __half2 mn) {
   const __half2 x = __hfma2(code, step, mn);
-  const uint32_t over = __hgt2_mask(x, mx);
-  return (over & *reinterpret_cast<const uint32_t*>(&mx)) |
-         (~over & *reinterpret_cast<const uint32_t*>(&x));
+  return *reinterpret_cast<const uint32_t*>(&x);
+}
+
+// A pair of codes whose halves belong to the groups (mn.lo, mx.lo) and
+// (mn.hi, mx.hi), normal or tiny.
+__device__ __forceinline__ uint32_t q4_value_any(__half2 code, __half2 mn, __half2 mx) {
+  uint32_t out = 0;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const __half m = i ? __high2half(mn) : __low2half(mn);
+    const __half M = i ? __high2half(mx) : __low2half(mx);
+    const __half c = i ? __high2half(code) : __low2half(code);
+    const float range = q4_range(m, M);
+    const __half x =
+        range >= kQ4TinyRange
+            ? __hfma(c, q4_step16(range), m)
+            : q4_level32(static_cast<uint32_t>(__half2float(c)), q4_step32(range, m, M),
+                         __half2float(m));
+    out |= static_cast<uint32_t>(__half_as_ushort(x)) << (16 * i);
+  }
+  return out;
 }
 
 constexpr uint32_t kNib0 = 0x000f000fu, kNib1 = 0x00f000f0u;
@@ -285,60 +329,68 @@ __device__ __forceinline__ void q4_query(const uint16_t* qrow, bool head_ok, int
 }
 
 // S = Q K^T for a 4-bit page (sc[h]: tokens 8 h + 2 t4 + e, as the 16-bit path).
-template <int D>
-__device__ __forceinline__ void q4_scores(const Q4Page<D>& r, const uint32_t (&qa)[D / 16][2],
-                                          float (&sc)[2][4]) {
+template <int D, bool TINY>
+__device__ __forceinline__ void q4_scores_t(const Q4Page<D>& r, const uint32_t (&qa)[D / 16][2],
+                                            float (&sc)[2][4]) {
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    const __half step = q4_step(r.kmn[h], r.kmx[h]);
-    const __half2 st2 = __half2half2(step), mn2 = __half2half2(r.kmn[h]),
-                  mx2 = __half2half2(r.kmx[h]);
+    const __half2 x2 = __half2half2(r.kx[h]), mn2 = __half2half2(r.kmn[h]);
 #pragma unroll
     for (int j = 0; j < D / 32; ++j) {
       const uint32_t w = r.kc[h][j], w8 = w >> 8;
-      const uint32_t b0 = q4_value(q4_codes(w, kNib0, kBias1024), st2, mn2, mx2);
-      const uint32_t b1 = q4_value(q4_codes(w, kNib1, kBias64), st2, mn2, mx2);
-      const uint32_t b2 = q4_value(q4_codes(w8, kNib0, kBias1024), st2, mn2, mx2);
-      const uint32_t b3 = q4_value(q4_codes(w8, kNib1, kBias64), st2, mn2, mx2);
-      mma16816<true>(sc[h], qa[2 * j][0], 0u, qa[2 * j][1], 0u, b0, b1);
-      mma16816<true>(sc[h], qa[2 * j + 1][0], 0u, qa[2 * j + 1][1], 0u, b2, b3);
+      uint32_t b[4];
+      const __half2 c[4] = {q4_codes(w, kNib0, kBias1024), q4_codes(w, kNib1, kBias64),
+                            q4_codes(w8, kNib0, kBias1024), q4_codes(w8, kNib1, kBias64)};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) b[i] = TINY ? q4_value_any(c[i], mn2, x2) : q4_value(c[i], x2, mn2);
+      mma16816<true>(sc[h], qa[2 * j][0], 0u, qa[2 * j][1], 0u, b[0], b[1]);
+      mma16816<true>(sc[h], qa[2 * j + 1][0], 0u, qa[2 * j + 1][1], 0u, b[2], b[3]);
     }
   }
 }
+template <int D>
+__device__ __forceinline__ void q4_scores(const Q4Page<D>& r, const uint32_t (&qa)[D / 16][2],
+                                          float (&sc)[2][4]) {
+  if (r.tiny)
+    q4_scores_t<D, true>(r, qa, sc);
+  else
+    q4_scores_t<D, false>(r, qa, sc);
+}
 
 // O += P V for a 4-bit page (a0-a3: the P fragments).
-template <int D>
-__device__ __forceinline__ void q4_pv(const Q4Page<D>& r, uint32_t a0, uint32_t a1, uint32_t a2,
-                                      uint32_t a3, float (&acc)[D / 8][4]) {
-  __half2 st2[2];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const __half2 mn = *reinterpret_cast<const __half2*>(&r.vmn[h]);
-    const __half2 mx = *reinterpret_cast<const __half2*>(&r.vmx[h]);
-    st2[h] = __halves2half2(q4_step(__low2half(mn), __low2half(mx)),
-                            q4_step(__high2half(mn), __high2half(mx)));
-  }
+template <int D, bool TINY>
+__device__ __forceinline__ void q4_pv_t(const Q4Page<D>& r, uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, float (&acc)[D / 8][4]) {
 #pragma unroll
   for (int j = 0; j < D / 64; ++j) {
     uint32_t bv[2][8];  // [token pair][nibble]: B fragments of tiles 8 j + nibble
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const __half2 mn = *reinterpret_cast<const __half2*>(&r.vmn[h]);
-      const __half2 mx = *reinterpret_cast<const __half2*>(&r.vmx[h]);
+      const __half2 x2 = *reinterpret_cast<const __half2*>(&r.vx[h]);
       const uint32_t wa = r.vc[2 * h][j], wb = r.vc[2 * h + 1][j];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         // Nibbles 4 hh .. 4 hh + 3 of both tokens, token 2 t4 (+ 8 h) in the low half.
         const uint32_t u = __byte_perm(wa, wb, hh ? 0x7632 : 0x5410), u8 = u >> 8;
-        bv[h][4 * hh + 0] = q4_value(q4_codes(u, kNib0, kBias1024), st2[h], mn, mx);
-        bv[h][4 * hh + 1] = q4_value(q4_codes(u, kNib1, kBias64), st2[h], mn, mx);
-        bv[h][4 * hh + 2] = q4_value(q4_codes(u8, kNib0, kBias1024), st2[h], mn, mx);
-        bv[h][4 * hh + 3] = q4_value(q4_codes(u8, kNib1, kBias64), st2[h], mn, mx);
+        const __half2 c[4] = {q4_codes(u, kNib0, kBias1024), q4_codes(u, kNib1, kBias64),
+                              q4_codes(u8, kNib0, kBias1024), q4_codes(u8, kNib1, kBias64)};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          bv[h][4 * hh + i] = TINY ? q4_value_any(c[i], mn, x2) : q4_value(c[i], x2, mn);
       }
     }
 #pragma unroll
     for (int n = 0; n < 8; ++n) mma16816<true>(acc[8 * j + n], a0, a1, a2, a3, bv[0][n], bv[1][n]);
   }
+}
+template <int D>
+__device__ __forceinline__ void q4_pv(const Q4Page<D>& r, uint32_t a0, uint32_t a1, uint32_t a2,
+                                      uint32_t a3, float (&acc)[D / 8][4]) {
+  if (r.tiny)
+    q4_pv_t<D, true>(r, a0, a1, a2, a3, acc);
+  else
+    q4_pv_t<D, false>(r, a0, a1, a2, a3, acc);
 }
 
 __device__ __forceinline__ void store_out(void* out, int out_dtype, int64_t off, float v) {

@@ -249,37 +249,106 @@ __device__ __forceinline__ uint32_t from_key2(uint32_t k) {
 }
 
 // ---------------------------------------------------------------- 4-bit format
-// step = fp16(fp32(fp32(mx - mn) / 15)), from the group's stored min / max.
-__device__ __forceinline__ __half q4_step(__half mn, __half mx) {
-  const float range = __fsub_rn(__half2float(mx), __half2float(mn));
-  // fl(range / 15) by the FMA method for division by a constant: q = fl(range
-  // * fl(1/15)), corrected once with the exact remainder.  Equal to the IEEE
-  // quotient for every binary32 in [0, 2^18), which holds every fp16 range
-  // (checked exhaustively on the host).
+// A group's 16 levels are mn + c * s, c = 0 .. 15, with the step s rounded
+// down from (mx - mn) / 15 so that no level passes the group max, and the
+// dequantised value is the level rounded once to fp16:
+//   range = fp32_down(mx - mn)
+//   normal groups (range >= 451 * 2^-24): s = fp16_down(fp32_down(range / 15)),
+//     and x = fp16(c * s + mn) is one fused fp16 multiply-add;
+//   tiny groups: s = floor(range / (15 g)) * g, g = 2^(floor(log2 max(|mn|,
+//     |mx|)) - 22), an fp32 value; every value of such a group lies below 2^-5
+//     and mn + c * s is a multiple of g, so it is exact in fp32 and
+//     x = fp16(fp32 fma(c, s, mn)).
+// (fp32_down / fp16_down: the largest binary32 / binary16 at or below.)  With
+// codes chosen as the nearest level, |x - x_in| <= (mx - mn)/30 plus half an
+// fp16 ulp of x for every finite group.
+constexpr float kQ4TinyRange = 451.0f * 0x1p-24f;
+
+__device__ __forceinline__ float q4_range(__half mn, __half mx) {
+  return __fsub_rd(__half2float(mx), __half2float(mn));
+}
+
+// fp16_down(fp32_down(range / 15)) for a normal group's range.  fl(range / 15)
+// by the FMA method for division by a constant (q = fl(range * fl(1/15)),
+// corrected once with the exact remainder), then one ulp down when the exact
+// remainder range - 15 q is negative; both steps are checked for every
+// binary32 below 2^18 on the host.
+__device__ __forceinline__ __half q4_step16(float range) {
   constexpr float kInv15 = 1.0f / 15.0f;
-  const float q = __fmul_rn(range, kInv15);
-  const float r = __fmaf_rn(-q, 15.0f, range);
-  return __float2half_rn(__fmaf_rn(r, kInv15, q));
+  const float q0 = __fmul_rn(range, kInv15);
+  const float r0 = __fmaf_rn(-q0, 15.0f, range);
+  const float q = __fmaf_rn(r0, kInv15, q0);  // the IEEE quotient
+  const float r = __fmaf_rn(-q, 15.0f, range);  // exact
+  const float qd = r < 0.f ? __int_as_float(__float_as_int(q) - 1) : q;
+  return __float2half_rd(qd);
+}
+
+// The fp32 step of a tiny group (range < kQ4TinyRange).
+__device__ __forceinline__ float q4_step32(float range, __half mn, __half mx) {
+  if (range == 0.f) return 0.f;
+  const float a = fmaxf(fabsf(__half2float(mn)), fabsf(__half2float(mx)));
+  const int ea = (__float_as_int(a) >> 23) - 127;  // floor(log2 a), a a normal binary32
+  const float up = __int_as_float((127 + 22 - ea) << 23);  // 1 / g
+  const float g = __int_as_float((127 - 22 + ea) << 23);
+  const uint32_t r = static_cast<uint32_t>(__fmul_rn(range, up));  // exact, below 2^24
+  return __fmul_rn(static_cast<float>(r / 15u), g);  // exact
+}
+
+// The step of any group as an fp32 value (a normal group's fp16 step widened).
+__device__ __forceinline__ float q4_step_f32(__half mn, __half mx) {
+  const float range = q4_range(mn, mx);
+  return range >= kQ4TinyRange ? __half2float(q4_step16(range)) : q4_step32(range, mn, mx);
+}
+
+// The code of x: the c in [0, 15] nearest to (x - mn) / s, ties to the even
+// c.  q = fl(fl(x - mn) * fl(1/s)) is within 2^-18 of (x - mn) / s while it is
+// below 16 (three roundings of 2^-24 relative); so rint(q) is the code unless
+// q lies within 2^-16 of a half-integer, and only then is the choice made
+// exactly: 2 (x - mn) against (2 floor(q) + 1) s in double (both exact).
+__device__ __forceinline__ uint32_t q4_code(float x, float mn, float s, float inv) {
+  const float q = __fmul_rn(__fsub_rn(x, mn), inv);
+  float c = rintf(q);
+  if (fabsf(fabsf(q - c) - 0.5f) < 0x1p-16f) {
+    const double lo = floor(static_cast<double>(q));
+    const double r = 2.0 * (static_cast<double>(x) - static_cast<double>(mn)) -
+                     (2.0 * lo + 1.0) * static_cast<double>(s);
+    c = static_cast<float>(r > 0.0 || (r == 0.0 && fmod(lo, 2.0) != 0.0) ? lo + 1.0 : lo);
+  }
+  return static_cast<uint32_t>(fminf(15.f, fmaxf(0.f, c)));
+}
+
+// One code of a tiny group: fp16(fp32 fma(c, s, mn)), exact before the rounding.
+__device__ __forceinline__ __half q4_level32(uint32_t code, float s, float mn) {
+  return __float2half_rn(__fmaf_rn(static_cast<float>(code), s, mn));
 }
 
 // Dequantise the 8 codes of one 32-bit word (byte i: channel 2i low nibble,
-// 2i+1 high nibble): x = fp16(code * step + mn), one rounding (fp16 FMA),
-// replaced by mx where it exceeds mx.  Output: 4 packed half pairs, channels in
-// order.
-__device__ __forceinline__ void q4_dequant8(uint32_t c4, __half2 mn2, __half2 step2,
-                                            __half2 mx2, uint32_t (&out)[4]) {
-  const __half2 k1024 = __half2half2(__ushort_as_half(0x6400));  // 1024.0
+// 2i+1 high nibble) of the group (mn, mx).  Output: 4 packed half pairs,
+// channels in order.  Normal groups: a nibble masked into the mantissa of
+// 1024 is 1024 + code exactly; subtracting 1024 leaves the code, then one
+// HFMA2 per pair.
+__device__ __forceinline__ void q4_dequant8(uint32_t c4, __half mn, __half mx, uint32_t (&out)[4]) {
+  const float range = q4_range(mn, mx);
+  if (range >= kQ4TinyRange) {
+    const __half2 step2 = __half2half2(q4_step16(range)), mn2 = __half2half2(mn);
+    const __half2 k1024 = __half2half2(__ushort_as_half(0x6400));  // 1024.0
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t byte = (c4 >> (8 * i)) & 0xffu;
-    // 1024 + code as an exact fp16 in each half, then subtract 1024 exactly.
-    const uint32_t bits = (byte & 0x0fu) | ((byte & 0xf0u) << 12) | 0x64006400u;
-    const __half2 biased = *reinterpret_cast<const __half2*>(&bits);
-    const __half2 code = __hsub2(biased, k1024);
-    const __half2 x = __hfma2(code, step2, mn2);
-    const uint32_t over = __hgt2_mask(x, mx2);  // 0xffff per half where x > mx
-    out[i] = (over & *reinterpret_cast<const uint32_t*>(&mx2)) |
-             (~over & *reinterpret_cast<const uint32_t*>(&x));
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t byte = (c4 >> (8 * i)) & 0xffu;
+      const uint32_t bits = (byte & 0x0fu) | ((byte & 0xf0u) << 12) | 0x64006400u;
+      const __half2 code = __hsub2(*reinterpret_cast<const __half2*>(&bits), k1024);
+      const __half2 x = __hfma2(code, step2, mn2);
+      out[i] = *reinterpret_cast<const uint32_t*>(&x);
+    }
+  } else {
+    const float s = q4_step32(range, mn, mx), m = __half2float(mn);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t byte = (c4 >> (8 * i)) & 0xffu;
+      const __half lo = q4_level32(byte & 0x0fu, s, m), hi = q4_level32(byte >> 4, s, m);
+      out[i] = static_cast<uint32_t>(__half_as_ushort(lo)) |
+               (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
+    }
   }
 }
 

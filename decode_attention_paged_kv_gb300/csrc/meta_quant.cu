@@ -12,10 +12,10 @@
 //
 // 4-bit format ("FlexGen: High-Throughput Generative Inference of Large
 // Language Models with a Single GPU" 解读, 4-bit 近似方法): groups of 64
-// channels of one (token, head) row; per-group min / max in fp16; 15 equal
-// steps between them; codes rounded to nearest even in fp32 IEEE operations;
-// values dequantised back to fp16 with one fused fp16 multiply-add, saturated
-// at the group max.
+// channels of one (token, head) row; per-group min / max in fp16; 16 levels
+// mn + c * s with the step s rounded down from (max - min) / 15 (an fp16 step,
+// or an fp32 one for groups narrower than 451 * 2^-24); codes are the nearest
+// level; values are dequantised back to fp16 by rounding the exact level once.
 
 #include "dkv_device.cuh"
 #include "dkv_kernels.h"
@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(kMetaThreads, Q4 ? 4 : 2) meta_kernel(const Me
         const __half mn = gmn[static_cast<int64_t>(t) * ng];
         const __half mx = gmx[static_cast<int64_t>(t) * ng];
         uint32_t w[4];
-        q4_dequant8(c4, __half2half2(mn), __half2half2(q4_step(mn, mx)), __half2half2(mx), w);
+        q4_dequant8(c4, mn, mx, w);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const uint32_t k = to_key2(w[u]);
@@ -150,28 +150,16 @@ __global__ void __launch_bounds__(256) quant4_kernel(int64_t groups, const __hal
     if (!valid) continue;
     const __half mn = __ushort_as_half(static_cast<unsigned short>(from_key2(kmin) & 0xffffu));
     const __half mx = __ushort_as_half(static_cast<unsigned short>(from_key2(kmax) & 0xffffu));
-    const __half step = q4_step(mn, mx);
-    const float fstep = __half2float(step);
+    const float fstep = q4_step_f32(mn, mx);
     const float fmn = __half2float(mn);
     uint32_t packed = 0;
     if (fstep != 0.f) {
-      // code = min(15, rint(fl(d / step))), d = fl(x - mn) >= 0.  The
-      // product q = fl(d * fl(1 / step)) is within 2^-22 relative of
-      // fl(d / step) (three roundings of 2^-24 each), i.e. within 2^-18 while
-      // q < 16; from 16 up both clamp to 15.  So rint(q) is the code unless q
-      // lies within 2^-16 of a half-integer, and only then is the IEEE
-      // quotient computed.
       const float inv = __frcp_rn(fstep);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const uint32_t hv = (w[e >> 1] >> (16 * (e & 1))) & 0xffffu;
         const float xf = __half2float(__ushort_as_half(static_cast<unsigned short>(hv)));
-        const float dq = __fsub_rn(xf, fmn);
-        const float q = __fmul_rn(dq, inv);
-        float c = rintf(q);
-        if (fabsf(fabsf(q - c) - 0.5f) < 0x1p-16f) c = rintf(__fdiv_rn(dq, fstep));
-        c = fminf(15.f, fmaxf(0.f, c));
-        packed |= static_cast<uint32_t>(c) << (4 * e);
+        packed |= q4_code(xf, fmn, fstep, inv) << (4 * e);
       }
     }
     *reinterpret_cast<uint32_t*>(codes + grp * 32 + sub * 4) = packed;
@@ -196,7 +184,7 @@ __global__ void __launch_bounds__(256) dequant4_kernel(int64_t groups, const uin
     const __half mn = gmin[grp], mx = gmax[grp];
     const uint32_t c4 = __ldcs(reinterpret_cast<const uint32_t*>(codes + grp * 32 + sub * 4));
     uint32_t w[4];
-    q4_dequant8(c4, __half2half2(mn), __half2half2(q4_step(mn, mx)), __half2half2(mx), w);
+    q4_dequant8(c4, mn, mx, w);
     *reinterpret_cast<uint4*>(x + grp * 64 + sub * 8) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }

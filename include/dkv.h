@@ -244,16 +244,24 @@ dkv_status dkv_decode_attn_topk_tokens(const dkv_params* p, const void* q, const
                                        size_t workspace_bytes, void* stream);
 size_t dkv_workspace_bytes_tokens(const dkv_params* p, int32_t top_k);
 
-/* 4-bit group-of-64 quantisation of `rows` fp16 rows of d channels (d % 64 == 0):
-     mn, mx = group min / max;  step = fp16(fp32(fp32(mx - mn) / 15))
-     code   = step == 0 ? 0 : clamp(rint(fp32(fp32(x - mn) / step)), 0, 15)
-   codes [rows, d/2] (channel 2i in the low nibble), gmin / gmax [rows, d/64]. */
+/* 4-bit group-of-64 quantisation of `rows` fp16 rows of d channels (d % 64 == 0).
+   Per group of 64 channels: mn, mx = group min / max (written to gmin / gmax);
+   16 levels mn + c * s, c = 0 .. 15, with the step s rounded down from
+   (mx - mn) / 15 so that no level passes mx:
+     range = fp32_down(mx - mn)
+     range >= 451 * 2^-24:  s = fp16_down(fp32_down(range / 15))
+     range <  451 * 2^-24:  s = floor(range / (15 g)) * g,
+                            g = 2^(floor(log2 max(|mn|, |mx|)) - 22)
+     code = 0 if s == 0, else the c nearest to (x - mn) / s (ties to even c)
+   (fp32_down / fp16_down: the largest binary32 / binary16 at or below).
+   Dequantised values are within (mx - mn)/30 plus half an fp16 ulp of the
+   input, for every finite group.  codes [rows, d/2] (channel 2i in the low
+   nibble), gmin / gmax [rows, d/64]. */
 dkv_status dkv_kv_quant4(int64_t rows, int32_t d, const void* x, void* codes, void* gmin,
                          void* gmax, void* stream);
 
-/* Inverse: x = fp16(code * step + mn), rounded once (a fused fp16 multiply-add),
-   replaced by mx where it exceeds mx, so x always lies in [mn, mx].  Inputs are
-   finite fp16 values. */
+/* Inverse: x = fp16(mn + code * s), the exact level rounded once to fp16
+   (always inside [mn, mx]).  Inputs are finite fp16 values. */
 dkv_status dkv_kv_dequant4(int64_t rows, int32_t d, const void* codes, const void* gmin,
                            const void* gmax, void* x, void* stream);
 

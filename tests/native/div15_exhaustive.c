@@ -3,7 +3,10 @@
  * "Correctly rounded multiplication by arbitrary precision constants"):
  *   c = RN(1/15); q = RN(x * c); r = RN(fma(-q, 15, x)); q' = RN(fma(r, c, q))
  * against the IEEE quotient RN(x / 15), for every binary32 x in [0, 2^18)
- * (the range of fl(max - min) for two finite fp16 values is [0, 131008]).
+ * (the range of fl(max - min) for two finite fp16 values is [0, 131008]);
+ * and the quotient rounded down from it, q' or the binary32 just below q' as
+ * the exact remainder fma(-q', 15, x) is >= 0 or < 0, against the largest
+ * binary32 q with 15 q <= x (15 q is exact in double).
  * Optional arguments: the first and one-past-last bit patterns to check (so
  * the range can be split over processes).  Exit status 0 when every x agrees;
  * prints the first mismatch otherwise. */
@@ -28,6 +31,13 @@ int main(int argc, char** argv) {
     const float want = x / 15.0f;
     if (memcmp(&q2, &want, 4) != 0) {
       printf("mismatch at x=%a: got %a want %a\n", x, q2, want);
+      return 1;
+    }
+    const float r2 = fmaf(-q2, 15.0f, x);
+    const float down = r2 < 0.0f ? nextafterf(q2, 0.0f) : q2;
+    if (15.0 * (double)down > (double)x ||
+        15.0 * (double)nextafterf(down, INFINITY) <= (double)x) {
+      printf("rounded-down mismatch at x=%a: got %a\n", x, down);
       return 1;
     }
     ++n;

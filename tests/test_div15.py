@@ -1,9 +1,11 @@
-"""The 4-bit format's step is fp16(fl(fl(max - min) / 15)).  The kernels form
-fl(x / 15) as q = fl(x * c), c = fl(1/15), corrected once with fused
-multiply-adds (q + fl(x - 15 q) * c, the FMA method for division by a
-constant).  This checks, for every binary32 x in [0, 2^18) -- which holds
-fl(max - min) of any two finite fp16 values -- that the result is the IEEE
-quotient, on the host with C's fmaf (split over processes)."""
+"""The 4-bit format's step of a normal group is fp16_down(fp32_down(x / 15)),
+x = fp32_down(max - min).  The kernels form fl(x / 15) as q = fl(x * c),
+c = fl(1/15), corrected once with fused multiply-adds (q + fl(x - 15 q) * c,
+the FMA method for division by a constant), then round it down with the sign
+of the exact remainder x - 15 q.  This checks, for every binary32 x in
+[0, 2^18) -- which holds the range of any two finite fp16 values -- that the
+corrected quotient is the IEEE quotient and the rounded-down one the largest
+binary32 q with 15 q <= x, on the host with C's fmaf (split over processes)."""
 
 import os
 import subprocess

@@ -237,6 +237,19 @@ def test_quant4_dequant4_bit_exact(dev, dkv):
     x[5, 64:] = np.concatenate([[-3.0, 12.0], np.arange(62) * 0.5 - 3.0])
     x[6] = rng.integers(0, 16, d) * 2.0 ** -24  # a subnormal grid
     x[7] = rng.standard_normal(d) * 2.0 ** -20
+    # narrow groups (range below 451 * 2^-24: the fp32 step grid), from the
+    # subnormals up to where fp16 spacing passes the threshold, and around it
+    u = 2.0 ** -24
+    r = 8
+    for base in [0.0, 2.0 ** -14, 2.0 ** -13 - 100 * u, 2.0 ** -10, -2.0 ** -7, 2.0 ** -6]:
+        for k in [1, 2, 7, 14, 15, 16, 29, 31, 100, 255, 300, 449, 450, 451, 452, 600, 2000]:
+            for sign in (1.0, -1.0):
+                x[r] = sign * (base + rng.integers(0, k + 1, d) * u)
+                r += 1
+    for k in range(1, 200):  # straddling zero
+        x[r] = (rng.integers(0, k + 1, d) - k // 2) * u
+        r += 1
+    assert r < rows
     xb = np.asarray(x, np.float64).astype(np.float16).view(np.uint16)
     xt = torch.from_numpy(xb.view(np.int16)).view(torch.float16)
     q4 = dkv.kv_quant4(xt.to(dev))
@@ -289,6 +302,40 @@ def test_q4_attention_matches_oracle(w, dev, dkv):
     out_s, sel = dkv.decode_attn_select(qd, K4, V4, meta, w.top_k, return_selected=True)
     sel = sel.cpu().numpy()
     omn, omx = oracle.meta(kh, w.S, 1)
+    r = oracle.scores(bits(q), omn, omx, 1)
+    check_selection(sel.reshape(-1, sel.shape[-1]), r.reshape(-1, r.shape[-1]), w.top_k)
+    ref_s = oracle.attention(bits(q), kh, vh, w.S, scale, 1, sel=sel)
+    assert max_abs(out_s, ref_s) <= ATOL
+
+
+def test_q4_attention_with_narrow_groups(dev, dkv):
+    # Tokens whose groups are narrower than 451 * 2^-24 dequantise through the
+    # fp32 step (the kernels' slower per-page path); the rest of each page stays
+    # on the fp16 step.  The ragged last page (zeroed bounds) takes it too.
+    w = Workload("q4-narrow", B=2, Hq=8, Hkv=4, d=128, N=520, top_k=12, dtype="fp16")
+    q, K, V = make_inputs(w, seed=303)
+    g = torch.Generator().manual_seed(9)
+    for T in (K, V):
+        rows = torch.randint(0, w.N, (w.B, w.Hkv, 60), generator=g)
+        for b in range(w.B):
+            for h in range(w.Hkv):
+                scale = torch.exp2(-torch.randint(14, 26, (60, 1), generator=g).float())
+                T[b, h, rows[b, h]] = (torch.randn(60, w.d, generator=g) * scale).to(T.dtype)
+    scale = 1.0 / math.sqrt(w.d)
+    K4, V4 = dkv.kv_quant4(K.to(dev)), dkv.kv_quant4(V.to(dev))
+    codes, gmin, gmax = oracle.quant4(bits(K))
+    assert np.array_equal(K4.codes.cpu().numpy(), codes)
+    kh = oracle.dequant4(codes, gmin, gmax)
+    vh = oracle.dequant4(*oracle.quant4(bits(V)))
+    assert np.array_equal(bits(dkv.kv_dequant4(K4).cpu()), kh)
+    qd = q.to(dev)
+    out = dkv.decode_attn_full(qd, K4, V4)
+    assert max_abs(out, oracle.attention(bits(q), kh, vh, w.S, scale, 1)) <= ATOL
+    meta = dkv.kv_meta_build(K4)
+    omn, omx = oracle.meta(kh, w.S, 1)
+    assert np.array_equal(bits(meta[0].cpu()), omn) and np.array_equal(bits(meta[1].cpu()), omx)
+    out_s, sel = dkv.decode_attn_select(qd, K4, V4, meta, w.top_k, return_selected=True)
+    sel = sel.cpu().numpy()
     r = oracle.scores(bits(q), omn, omx, 1)
     check_selection(sel.reshape(-1, sel.shape[-1]), r.reshape(-1, r.shape[-1]), w.top_k)
     ref_s = oracle.attention(bits(q), kh, vh, w.S, scale, 1, sel=sel)
