@@ -56,10 +56,11 @@ def parse_args():
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the e2e, CPU-baseline, 1M-token head-wise and other-workload legs")
     ap.add_argument("--legs", default="all",
-                    help="comma list of extra legs to run (e2e, group, paged, pagesize, tokens, "
-                         "meta8, cpu, headwise, others) or 'all'; for small profiling runs")
+                    help="comma list of extra legs to run (e2e, group, paged, pagesize, ratios, "
+                         "tokens, meta8, cpu, headwise, others) or 'all'; for small profiling runs")
     args = ap.parse_args()
-    legs = {"e2e", "group", "paged", "pagesize", "tokens", "meta8", "cpu", "headwise", "others"}
+    legs = {"e2e", "group", "paged", "pagesize", "ratios", "tokens", "meta8", "cpu", "headwise",
+            "others"}
     args.legs = set() if args.no_extra else (legs if args.legs == "all" else set(args.legs.split(",")))
     unknown = args.legs - legs
     if unknown:
@@ -291,6 +292,33 @@ def run_dkv(args, rank, world, local):
     if status != 0:
         raise SystemExit(f"device status {status} during the timed region")
 
+    # The same three calls again, each after an L2 flush (outside its event
+    # pair): the select call then reads the metadata the build just wrote from
+    # HBM, not from L2.
+    flush = L2Flush(dev)
+    cold = {c: [] for c in calls}
+    for _ in range(max(10, args.steps)):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        flush()
+        e[0].record(stream)
+        meta = dkv.kv_meta_build(K)
+        e[1].record(stream)
+        flush()
+        e[2].record(stream)
+        dkv.decode_attn_full(q, K, V, out=out_full, workspace=ws_full)
+        e[3].record(stream)
+        flush()
+        e[4].record(stream)
+        dkv.decode_attn_select(q, K, V, meta, w.top_k, out=out_sel, selected=sel,
+                               workspace=ws_sel)
+        e[5].record(stream)
+        for i, c in enumerate(calls):
+            cold[c].append((e[2 * i], e[2 * i + 1]))
+    torch.cuda.synchronize()
+    per_call_cold = {c: statistics.median(a.elapsed_time(b) for a, b in cold[c]) for c in calls}
+    if max(dkv.read_device_status(ws_full), dkv.read_device_status(ws_sel)) != 0:
+        raise SystemExit("device status error in the cold-L2 pass")
+
     bytes_call = {
         "kv_meta_build": acc.meta_bytes(w.B, w.Hkv, w.d, w.N, w.S),
         "decode_attn_full": acc.full_bytes(w.B, w.Hq, w.Hkv, w.d, w.N),
@@ -304,6 +332,7 @@ def run_dkv(args, rank, world, local):
         kernels[c] = {"ms": round(per_call[c], 5), "alg_bytes": bytes_call[c],
                       "GB/s": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak, 4),
                       "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4)}
+    kernels_cold = {c: call_stats(per_call_cold[c], bytes_call[c], peak) for c in calls}
     kernels["decode_attn_select"]["gathered_pages"] = gathered // w.S
     kernels["decode_attn_full"]["queries_per_s"] = round(w.B / (per_call["decode_attn_full"] * 1e-3), 1)
     kernels["decode_attn_select"]["queries_per_s"] = round(
@@ -314,7 +343,13 @@ def run_dkv(args, rank, world, local):
                 "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                 "frac": round(dom_gbs / peak, 4),
                 "frac_of_8tbs": round(dom_gbs / NOMINAL_HBM_GBS, 4),
-                "traffic": ncu_traffic(dom)}
+                "traffic": ncu_traffic(dom),
+                # every call of the step, in the timed region (warm) and each
+                # after an L2 flush (cold): ms and fraction of 8 TB/s
+                "calls": {c: {"ms": kernels[c]["ms"], "frac_of_8tbs": kernels[c]["frac_of_8tbs"],
+                              "ms_cold": kernels_cold[c]["ms"],
+                              "frac_of_8tbs_cold": kernels_cold[c]["frac_of_8tbs"]}
+                          for c in calls}}
     value = job_queries_per_s(world, w.B, ms_step)
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "queries/s", "n_gpus": world,
@@ -324,17 +359,21 @@ def run_dkv(args, rank, world, local):
         "config": {"workload": w.name, "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv,
                    "head_dim": w.d, "context": w.N, "page_size": w.S, "top_k_pages": w.top_k,
                    "step": "kv_meta_build + decode_attn_full + decode_attn_select",
-                   "l2": "inputs larger than L2 (2 GiB K+V streamed every step)",
+                   "l2": "inputs larger than L2 (2 GiB K+V streamed every step); per-call "
+                         "figures also taken each after a write of twice the L2 (kernels_cold)",
                    "parallelism": f"replicas x{world} (each rank its own batch)"},
         "effective_GB_per_s": round(step_bytes / (ms_step * 1e-3) / 1e9, 1),
-        "kernels": kernels, "roofline": roofline,
+        "kernels": kernels, "kernels_cold": kernels_cold,
+        "kernels_timing": {"kernels": "inside the timed region (back-to-back steps)",
+                           "kernels_cold": COLD},
+        "roofline": roofline,
         "gpu_launches": args.steps * (1 + 2 + 4),
         "clocks": clk.summary(),
     }
-    return res, (q, K, V, w, widx, dev, stream)
+    return res, (q, K, V, w, widx, dev, stream, flush)
 
 
-def group_select_leg(q, K, V, w, dev, stream, reps=10):
+def group_select_leg(q, K, V, w, dev, stream, flush, reps=10):
     """decode_attn_select with one selection per kv head group (summed bound
     scores) on the bench workload; the same byte count rule (metadata plus the
     unique pages gathered per (batch, kv head))."""
@@ -352,43 +391,61 @@ def group_select_leg(q, K, V, w, dev, stream, reps=10):
         dkv.decode_attn_select(q, K, V, meta, w.top_k, out=out, selected=sel, workspace=ws,
                                group_select=True)
 
-    for _ in range(3):
-        call()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(reps):
-        call()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / reps
+    ms = time_cold(call, stream, flush, reps)
     gathered = union_tokens(sel, w)
     nbytes = acc.select_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, gathered, w.S)
-    gbs = nbytes / (ms * 1e-3) / 1e9
     peak, _ = peaks()
-    return {"workload": w.name, "ms": round(ms, 5), "alg_bytes": nbytes, "GB/s": round(gbs, 1),
-            "frac_of_measured_hbm": round(gbs / peak, 4),
-            "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4), "gathered_pages": gathered // w.S,
-            "queries_per_s": round(w.B / (ms * 1e-3), 1),
-            "timing": f"{reps} back-to-back calls"}
+    res = {"workload": w.name, **call_stats(ms, nbytes, peak), "gathered_pages": gathered // w.S,
+           "queries_per_s": round(w.B / (ms * 1e-3), 1), "timing": COLD}
+    return res
 
 
-def _time_calls(fn, stream, reps):
+class L2Flush:
+    """Writes a buffer of twice the L2 size: the next call then finds none of
+    its inputs (metadata included) in L2."""
+
+    def __init__(self, dev):
+        props = torch.cuda.get_device_properties(dev)
+        l2 = int(getattr(props, "L2_cache_size", 0) or (129 << 20))
+        self.bytes = 2 * l2
+        self.buf = torch.empty(self.bytes // 4, dtype=torch.int32, device=dev)
+        self.n = 0
+
+    def __call__(self):
+        self.n += 1
+        self.buf.fill_(self.n)
+
+
+def time_cold(fn, stream, flush, reps):
+    """Median device time of `fn` over `reps` calls, each after an L2 flush
+    (outside its event pair), after 3 warm-up calls."""
     for _ in range(3):
         fn()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    pairs = []
     for _ in range(reps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
         fn()
-    e1.record(stream)
+        b.record(stream)
+        pairs.append((a, b))
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / reps
+    return statistics.median(a.elapsed_time(b) for a, b in pairs)
 
 
-def meta8_leg(q, K, V, w, dev, stream, reps=10):
+def call_stats(ms, nbytes, peak):
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"ms": round(ms, 5), "alg_bytes": nbytes, "GB/s": round(gbs, 1),
+            "frac_of_measured_hbm": round(gbs / peak, 4),
+            "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4)}
+
+
+COLD = "cold L2: median of 10 calls, each after a write of twice the L2 size"
+
+
+def meta8_leg(q, K, V, w, dev, stream, flush, reps=10):
     """8-bit page metadata on the bench workload: its build from the 16-bit
-    metadata, and decode_attn_select scoring it (10 back-to-back calls each);
+    metadata, and decode_attn_select scoring it (cold L2);
     how many (batch, q-head) rows keep the 16-bit metadata's page set."""
     import decode_attention_paged_kv_gb300 as dkv
     from decode_attention_paged_kv_gb300 import accounting as acc
@@ -401,15 +458,15 @@ def meta8_leg(q, K, V, w, dev, stream, reps=10):
     out = torch.empty(w.B, w.Hq, w.d, dtype=torch.float32, device=dev)
     sel = torch.empty(w.B, w.Hq, kk, dtype=torch.int32, device=dev)
     peak, _ = peaks()
-    res = {"workload": w.name, "timing": f"{reps} back-to-back calls"}
-    ms = _time_calls(lambda: dkv.kv_meta8_build(meta), stream, reps)
+    res = {"workload": w.name, "timing": COLD}
+    ms = time_cold(lambda: dkv.kv_meta8_build(meta), stream, flush, reps)
     nbytes = acc.meta8_bytes(w.B, w.Hkv, w.d, w.N, w.S)
     gbs = nbytes / (ms * 1e-3) / 1e9
     res["kv_meta8_build"] = {"ms": round(ms, 5), "alg_bytes": nbytes, "GB/s": round(gbs, 1),
                              "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
                              "frac_of_measured_hbm": round(gbs / peak, 4)}
-    ms = _time_calls(lambda: dkv.decode_attn_select(q, K, V, m8, w.top_k, out=out, selected=sel,
-                                                    workspace=ws), stream, reps)
+    ms = time_cold(lambda: dkv.decode_attn_select(q, K, V, m8, w.top_k, out=out, selected=sel,
+                                                  workspace=ws), stream, flush, reps)
     gathered = union_tokens(sel, w)
     nbytes = acc.select8_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, gathered, w.S)
     gbs = nbytes / (ms * 1e-3) / 1e9
@@ -430,10 +487,10 @@ def meta8_leg(q, K, V, w, dev, stream, reps=10):
     return res
 
 
-def paged_leg(q, K, V, w, dev, stream, reps=10):
+def paged_leg(q, K, V, w, dev, stream, flush, reps=10):
     """The bench workload held as a pool of 16-token blocks in shuffled order
     with a block table: exact and sparse attention timed like the contiguous
-    cache (10 back-to-back calls each), outputs compared bit for bit."""
+    cache (cold L2), outputs compared bit for bit."""
     import decode_attention_paged_kv_gb300 as dkv
     from decode_attention_paged_kv_gb300 import accounting as acc
 
@@ -466,18 +523,9 @@ def paged_leg(q, K, V, w, dev, stream, reps=10):
                                                        workspace=ws),
     }
     peak, _ = peaks()
-    res = {"workload": w.name, "pool_blocks": nb, "timing": f"{reps} back-to-back calls"}
+    res = {"workload": w.name, "pool_blocks": nb, "timing": COLD}
     for name, fn in calls.items():
-        for _ in range(3):
-            fn()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(reps):
-            fn()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / reps
+        ms = time_cold(fn, stream, flush, reps)
         if name.startswith("full"):
             nbytes = acc.full_bytes(w.B, w.Hq, w.Hkv, w.d, w.N)
         else:
@@ -493,10 +541,10 @@ def paged_leg(q, K, V, w, dev, stream, reps=10):
     return res
 
 
-def page_size_leg(q, K, V, w, dev, stream, reps=10):
+def page_size_leg(q, K, V, w, dev, stream, flush, reps=10):
     """Selection page sizes S = 4, 8, 16, 32, 64 ("TinyServe" page-size
     variants) on the bench workload at the same token budget (K = budget / S
-    pages): metadata build and select, 10 back-to-back calls each.  Pages of 4
+    pages): metadata build and select, cold L2.  Pages of 4
     or 8 tokens are read as the 16-token cache pages holding them
     (cache_tokens_read); the roofline counts the selected pages' tokens."""
     import decode_attention_paged_kv_gb300 as dkv
@@ -504,7 +552,7 @@ def page_size_leg(q, K, V, w, dev, stream, reps=10):
 
     budget = w.top_k * w.S
     peak, _ = peaks()
-    res = {"workload": w.name, "token_budget": budget, "timing": f"{reps} back-to-back calls"}
+    res = {"workload": w.name, "token_budget": budget, "timing": COLD}
     for S in (4, 8, 16, 32, 64):
         kk = budget // S
         P = (w.N + S - 1) // S
@@ -518,16 +566,7 @@ def page_size_leg(q, K, V, w, dev, stream, reps=10):
                      q, K, V, meta, kk, out=out, selected=sel, workspace=ws, page_size=S)}
         r = {"top_k_pages": kk}
         for name, fn in calls.items():
-            for _ in range(3):
-                fn()
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(reps):
-                fn()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            ms = e0.elapsed_time(e1) / reps
+            ms = time_cold(fn, stream, flush, reps)
             if name == "kv_meta_build":
                 nbytes = acc.meta_bytes(w.B, w.Hkv, w.d, w.N, S)
             else:
@@ -544,9 +583,48 @@ def page_size_leg(q, K, V, w, dev, stream, reps=10):
     return res
 
 
-def token_leg(q, K, V, w, dev, stream, reps=10):
+def ratio_leg(name, q, K, V, dev, stream, flush, reps=10):
+    """Selection ratio K / P in {0.1, 0.2, 0.3, 0.5} at S = 16 ("TinyServe"
+    hyper-parameter search: page sizes and selection ratios): select per call
+    (cold L2), its algorithmic bytes against the exact call's, and the model
+    fraction 1/S + K S / L of the pages' normalised comparison."""
+    import decode_attention_paged_kv_gb300 as dkv
+    from decode_attention_paged_kv_gb300 import accounting as acc
+    from workloads import make_inputs
+
+    w = by_name(name)
+    if q is None:
+        widx = [x.name for x in WORKLOADS].index(w.name)
+        q, K, V = make_inputs(w, seed=42 + widx, device=dev)
+    meta = dkv.kv_meta_build(K)
+    full_b = acc.full_bytes(w.B, w.Hq, w.Hkv, w.d, w.N)
+    peak, _ = peaks()
+    res = {"workload": w.name, "page_size": w.S, "pages": w.P, "timing": COLD}
+    for ratio in (0.1, 0.2, 0.3, 0.5):
+        kk = max(1, round(ratio * w.P))
+        ws = torch.zeros(dkv.workspace_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, kk), dtype=torch.uint8,
+                         device=dev)
+        out = torch.empty(w.B, w.Hq, w.d, dtype=torch.float32, device=dev)
+        sel = torch.empty(w.B, w.Hq, kk, dtype=torch.int32, device=dev)
+        ms = time_cold(lambda: dkv.decode_attn_select(q, K, V, meta, kk, out=out, selected=sel,
+                                                      workspace=ws), stream, flush, reps)
+        if dkv.read_device_status(ws) != 0:
+            raise SystemExit(f"device status error in the ratio leg ({name}, {ratio})")
+        gathered = union_tokens(sel, w)
+        nbytes = acc.select_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, gathered, w.S)
+        r = {"top_k_pages": kk, **call_stats(ms, nbytes, peak),
+             "union_pages_per_unit": round(gathered / w.S / (w.B * w.Hkv), 1),
+             "bytes_vs_exact": round(nbytes / full_b, 4),
+             "model_1_over_S_plus_KS_over_L": round(1 / w.S + kk * w.S / w.N, 4),
+             "queries_per_s": round(w.B / (ms * 1e-3), 1)}
+        res[f"r{ratio}"] = r
+        del ws
+    return res
+
+
+def token_leg(q, K, V, w, dev, stream, flush, reps=10):
     """Token-level sparse attention on the bench workload, keeping the top 10%
-    of the tokens per q-head (10 back-to-back calls)."""
+    of the tokens per q-head (cold L2)."""
     import decode_attention_paged_kv_gb300 as dkv
     from decode_attention_paged_kv_gb300 import accounting as acc
 
@@ -558,28 +636,20 @@ def token_leg(q, K, V, w, dev, stream, reps=10):
     def call():
         dkv.decode_attn_topk_tokens(q, K, V, ktok, out=out, workspace=ws)
 
-    for _ in range(3):
-        call()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(reps):
-        call()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / reps
+    ms = time_cold(call, stream, flush, reps)
     nbytes = acc.token_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, ktok)
     gbs = nbytes / (ms * 1e-3) / 1e9
     peak, _ = peaks()
     return {"workload": w.name, "top_k_tokens": ktok, "ms": round(ms, 5), "alg_bytes": nbytes,
             "GB/s": round(gbs, 1), "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
             "frac_of_measured_hbm": round(gbs / peak, 4),
-            "queries_per_s": round(w.B / (ms * 1e-3), 1), "timing": f"{reps} back-to-back calls"}
+            "queries_per_s": round(w.B / (ms * 1e-3), 1), "timing": COLD}
 
 
 def headwise_leg(dev, stream):
     """1M-token context, 8 kv heads: exact attention all heads at once and one
-    kv head at a time (HeadInfer), bitwise-equal outputs."""
+    kv head at a time (HeadInfer), bitwise-equal outputs.  The 4 GiB working
+    set is over 4x the L2, so calls are timed back to back."""
     import decode_attention_paged_kv_gb300 as dkv
     from decode_attention_paged_kv_gb300 import accounting as acc
     from workloads import make_inputs
@@ -627,7 +697,7 @@ def headwise_leg(dev, stream):
     return res
 
 
-def workload_leg(name, dev, stream, reps=10):
+def workload_leg(name, dev, stream, flush, reps=10):
     """Per-call device times and GB/s on another workload: the 1.3B-MHA shape
     (dense bf16) or the OPT-30B shape in the 4-bit format (quantise K and V,
     then metadata, exact and page-sparse attention over the 4-bit cache)."""
@@ -698,22 +768,13 @@ def workload_leg(name, dev, stream, reps=10):
             fn()
     torch.cuda.synchronize()
     gathered = union_tokens(sel, w)
-    # Each call timed over `reps` back-to-back launches (inputs exceed L2), so
-    # host-side launch latency overlaps the device work as in a decode loop.
-    times = {}
-    for c, fn, _ in calls:
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(reps):
-            fn()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        times[c] = e0.elapsed_time(e1) / reps
+    # Each call on a cold L2 (its inputs, metadata included, come from HBM).
+    times = {c: time_cold(fn, stream, flush, reps) for c, fn, _ in calls}
     if max(dkv.read_device_status(ws_full), dkv.read_device_status(ws_sel)) != 0:
         raise SystemExit(f"device status error on {w.name}")
     peak, _ = peaks()
     res = {"workload": w.name, "dtype": w.dtype, "kv_format": "q4g64" if w.q4 else "dense",
-           "top_k_pages": w.top_k, "gathered_pages": gathered // w.S}
+           "top_k_pages": w.top_k, "gathered_pages": gathered // w.S, "timing": COLD}
     for c, _, nbytes in calls:
         if nbytes is None:
             nbytes = acc.select_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, gathered, w.S, q4=w.q4)
@@ -869,21 +930,25 @@ def main():
     if world > 1:
         torch.cuda.set_device(local)
         torch.distributed.init_process_group("nccl")
-    res, (q, K, V, w, widx, dev, stream) = run_dkv(args, rank, world, local)
+    res, (q, K, V, w, widx, dev, stream, flush) = run_dkv(args, rank, world, local)
     if args.legs and rank == 0:
         L = args.legs
         if "e2e" in L:
             res["e2e"] = e2e_leg(q, K, V, w, dev, stream, args.steps)
         if "group" in L:
-            res["group_select"] = group_select_leg(q, K, V, w, dev, stream)
+            res["group_select"] = group_select_leg(q, K, V, w, dev, stream, flush)
         if "paged" in L:
-            res["paged"] = paged_leg(q, K, V, w, dev, stream)
+            res["paged"] = paged_leg(q, K, V, w, dev, stream, flush)
         if "pagesize" in L:
-            res["page_sizes"] = page_size_leg(q, K, V, w, dev, stream)
+            res["page_sizes"] = page_size_leg(q, K, V, w, dev, stream, flush)
+        if "ratios" in L:
+            res["select_ratios"] = [ratio_leg(w.name, q, K, V, dev, stream, flush),
+                                    ratio_leg(WORKLOADS[1].name, None, None, None, dev, stream,
+                                              flush)]
         if "tokens" in L:
-            res["topk_tokens"] = token_leg(q, K, V, w, dev, stream)
+            res["topk_tokens"] = token_leg(q, K, V, w, dev, stream, flush)
         if "meta8" in L:
-            res["meta8"] = meta8_leg(q, K, V, w, dev, stream)
+            res["meta8"] = meta8_leg(q, K, V, w, dev, stream, flush)
         if "cpu" in L:
             res["cpu_baseline"] = cpu_baseline_leg(q, K, V, w)
         del q, K, V
@@ -891,9 +956,11 @@ def main():
         if "headwise" in L:
             res["headwise_1m"] = headwise_leg(dev, stream)
         if "others" in L:
-            res["other_workloads"] = [workload_leg(n, dev, stream)
+            res["other_workloads"] = [workload_leg(n, dev, stream, flush)
                                       for n in (WORKLOADS[1].name, WORKLOADS[4].name)]
     if rank == 0:
+        # the per-call summary last, where a tail of the line shows it
+        res["per_call"] = res["roofline"]["calls"]
         print(json.dumps(res), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

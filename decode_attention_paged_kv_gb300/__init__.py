@@ -41,6 +41,7 @@ PAGE_SIZE = 16
 # enums of include/dkv.h
 DKV_OK = 0
 DKV_ERR_DEVICE_TIMEOUT = 8
+DKV_ERR_DEVICE_CHECK = 9
 DKV_BF16, DKV_FP16, DKV_FP32 = 0, 1, 2
 DKV_KV_DENSE, DKV_KV_Q4G64, DKV_KV_PAGED = 0, 1, 2
 DKV_FLAG_FORCE_TIMEOUT = 0x1

@@ -514,10 +514,14 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
           if (n == 0) continue;
         }
         if (a.bt != nullptr) {
-          // paged cache: the pool block of each of the item's pages (clamped)
+          // paged cache: the pool block of each of the item's pages.  An
+          // entry outside [0, num_blocks) is clamped into it, so no copy
+          // leaves the pool, and reported as a failed check.
           for (int j = lane; j < n; j += 32) {
             const int page = SPARSE ? list[j].x : first + j;
-            blocks[j] = min(max(a.bt[b * a.bts + page], 0), a.nblocks - 1);
+            const int blk = a.bt[b * a.bts + page];
+            if (blk < 0 || blk >= a.nblocks) set_status(a.status, kStatusCheck);
+            blocks[j] = min(max(blk, 0), a.nblocks - 1);
           }
           __syncwarp();
         }

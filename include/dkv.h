@@ -100,7 +100,11 @@ typedef enum dkv_kv_format {
                        h * stride_h (elements), token stride d.  block_table
                        [B, P] int32 (row stride block_table_stride) maps page j
                        of batch entry b to its block; entries outside
-                       [0, num_blocks) are clamped into it.  A sequence's ragged
+                       [0, num_blocks) are clamped into it (nothing outside
+                       the pool is read) and the attention calls then record
+                       DKV_ERR_DEVICE_CHECK in the workspace status word
+                       (dkv_kv_meta_build, which has no workspace, only
+                       clamps).  A sequence's ragged
                        last page may hold anything past N: it is never used.
                        K and V of one call share the table.  ("TinyServe"
                        结构化内存布局: the cache as pages of S tokens.) */
@@ -275,11 +279,14 @@ dkv_status dkv_kv_dequant4(int64_t rows, int32_t d, const void* codes, const voi
    - Returns DKV_ERR_WORKSPACE when the problem needs more scratch than that
      (dkv_workspace_bytes(p, 0) > DKV_NOALLOC_SCRATCH_BYTES).
    - The first call on a device looks up the array's address (with that device
-     current); make that first call before any stream capture.
+     current); make that first call before any stream capture.  The address is
+     kept per device and context: a call under another context (after a device
+     reset, or with a context of the caller's own current) looks it up again.
    - Every call shares the array: calls that may overlap on the GPU race and
      must be serialised by the caller.
-   - Device-side errors (an expired bounded wait) are cleared by the next call
-     and cannot be read back. */
+   - A device-side error (an expired bounded wait) cannot be read back with
+     dkv_read_device_status; instead every element of that call's `out` is
+     set to NaN.  The next call starts clean. */
 #define DKV_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 dkv_status dkv_decode_attn_full_noalloc(const dkv_params* p, const void* q, const dkv_kv* K,
                                         const dkv_kv* V, void* out, int32_t out_dtype,

@@ -97,3 +97,39 @@ def test_paged_matches_oracle(dev, dkv):
     check_selection(sel.reshape(-1, sel.shape[-1]), r.reshape(-1, r.shape[-1]), w.top_k)
     ref = oracle.attention(bits(q), bits(K), bits(V), w.S, scale, 0, sel=sel)
     assert max_abs(out, ref) <= ATOL
+
+
+@pytest.mark.parametrize("bad", [-5, 10 ** 6])
+def test_out_of_range_block_entry_is_reported(bad, dev, dkv):
+    # A block-table entry outside [0, num_blocks) is clamped into the pool
+    # before any copy is issued (nothing outside the pool is read) and
+    # reported as DKV_ERR_DEVICE_CHECK in the workspace status word; the
+    # sequences whose tables are valid are unaffected.
+    w = Workload("paged-bad", B=2, Hq=8, Hkv=2, d=128, N=700, top_k=44)  # 44 pages: all
+    q, K, V = make_inputs(w, seed=57)
+    pk, bt = to_paged(K, w.P, seed=3)
+    pv, _ = to_paged(V, w.P, seed=3)
+    btd = bt.to(dev)  # K and V share one table
+    PK = dkv.PagedCache(pk.to(dev), btd, w.N)
+    PV = dkv.PagedCache(pv.to(dev), btd, w.N)
+    qd = q.to(dev)
+    scale = 1.0 / math.sqrt(w.d)
+    ref = oracle.attention(bits(q), bits(K), bits(V), w.S, scale, 0)
+    ws = torch.zeros(dkv.workspace_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, w.top_k), dtype=torch.uint8,
+                     device=dev)
+    meta = dkv.kv_meta_build(PK)
+    dkv.decode_attn_full(qd, PK, PV, workspace=ws)
+    assert dkv.read_device_status(ws) == dkv.DKV_OK  # a valid table
+    bt_bad = bt.clone()
+    bt_bad[1, 5] = bad
+    btb = bt_bad.to(dev)
+    PKb = dkv.PagedCache(PK.pool, btb, w.N)
+    PVb = dkv.PagedCache(PV.pool, btb, w.N)
+    out = dkv.decode_attn_full(qd, PKb, PVb, workspace=ws)
+    assert dkv.read_device_status(ws) == dkv.DKV_ERR_DEVICE_CHECK
+    assert max_abs(out[:1], ref[:1]) <= ATOL
+    out_s = dkv.decode_attn_select(qd, PKb, PVb, meta, w.top_k, workspace=ws)
+    assert dkv.read_device_status(ws) == dkv.DKV_ERR_DEVICE_CHECK
+    assert max_abs(out_s[:1], ref[:1]) <= ATOL
+    dkv.decode_attn_select(qd, PK, PV, meta, w.top_k, workspace=ws)
+    assert dkv.read_device_status(ws) == dkv.DKV_OK

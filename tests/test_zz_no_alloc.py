@@ -5,28 +5,34 @@ kernels as dkv_decode_attn_full with a fixed scratch array inside the library
 instead of a caller workspace.
 
 Called here through the C ABI directly, twice in a row on different shapes
-(the second call finds the first one's scratch contents), and compared with
-the workspace entry point within the parity tolerance.  This file is collected
-last so that a stop at the first failure has run every other test first; it
-also passes on its own in a fresh process.
+(the second call finds the first one's scratch contents).  Both entry points
+run the same kernels with the same fixed chunking, so the results must be
+bitwise equal; each is also checked against the CPU oracle within the parity
+tolerance.  A call whose bounded waits are forced to expire must show it as
+NaN in its output, and the call after it must be correct again.  This file is
+collected last so that a stop at the first failure has run every other test
+first; it also passes on its own in a fresh process.
 """
 
 import ctypes
 import math
 
+import numpy as np
 import pytest
 import torch
 
+import oracle
 from gpu_helpers import ATOL, max_abs, require_cuda
-from workloads import Workload, make_inputs
+from workloads import Workload, bits, make_inputs
 
 pytestmark = pytest.mark.gpu
 
 
-def _call_noalloc(dkv, q, K, V, out):
+def _call_noalloc(dkv, q, K, V, out, flags=0):
     ks, B, H, N, d = dkv._kv_struct(K)
     vs = dkv._kv_struct(V)[0]
     p = dkv._params(q, B, H, N, d, out, 1.0 / math.sqrt(d))
+    p.flags = flags
     fn = dkv.lib().dkv_decode_attn_full_noalloc
     fn.argtypes = [ctypes.POINTER(dkv._Params), ctypes.c_void_p, ctypes.POINTER(dkv._KV),
                    ctypes.POINTER(dkv._KV), ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]
@@ -41,12 +47,34 @@ def test_noalloc_matches_workspace_entry_point_twice():
     shapes = [Workload("na1", B=4, Hq=32, Hkv=8, d=128, N=20000, kind="hot"),
               Workload("na2", B=3, Hq=8, Hkv=8, d=64, N=3001, kind="offset")]
     for i, w in enumerate(shapes):
-        q, K, V = (t.to(dev) for t in make_inputs(w, seed=100 + i))
+        qc, Kc, Vc = make_inputs(w, seed=100 + i)
+        q, K, V = qc.to(dev), Kc.to(dev), Vc.to(dev)
         ref = dkv.decode_attn_full(q, K, V)
         out = torch.full_like(ref, float("nan"))
         assert _call_noalloc(dkv, q, K, V, out) == dkv.DKV_OK
         torch.cuda.synchronize()
-        assert max_abs(out, ref) <= ATOL
+        assert torch.equal(out, ref)
+        want = oracle.attention(bits(qc), bits(Kc), bits(Vc), w.S, 1.0 / math.sqrt(w.d),
+                                0 if w.dtype == "bf16" else 1)
+        assert max_abs(out, want) <= ATOL
+
+
+def test_noalloc_device_error_shows_as_nan_then_recovers():
+    dev = require_cuda()
+    import decode_attention_paged_kv_gb300 as dkv
+    w = Workload("na3", B=2, Hq=8, Hkv=2, d=128, N=4000)
+    q, K, V = (t.to(dev) for t in make_inputs(w, seed=7))
+    out = torch.zeros(w.B, w.Hq, w.d, device=dev)
+    # every bounded wait gives up at once (no hang): the call still returns
+    # DKV_OK, its output is all NaN
+    assert _call_noalloc(dkv, q, K, V, out, flags=dkv.DKV_FLAG_FORCE_TIMEOUT) == dkv.DKV_OK
+    torch.cuda.synchronize()
+    assert torch.isnan(out).all()
+    ref = dkv.decode_attn_full(q, K, V)
+    out2 = torch.full_like(ref, float("nan"))
+    assert _call_noalloc(dkv, q, K, V, out2) == dkv.DKV_OK
+    torch.cuda.synchronize()
+    assert torch.equal(out2, ref)
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
