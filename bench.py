@@ -57,10 +57,11 @@ def parse_args():
                     help="skip the e2e, CPU-baseline, 1M-token head-wise and other-workload legs")
     ap.add_argument("--legs", default="all",
                     help="comma list of extra legs to run (e2e, group, paged, pagesize, ratios, "
-                         "tokens, meta8, cpu, headwise, others) or 'all'; for small profiling runs")
+                         "reuse, tokens, meta8, cpu, headwise, others) or 'all'; for small "
+                         "profiling runs")
     args = ap.parse_args()
-    legs = {"e2e", "group", "paged", "pagesize", "ratios", "tokens", "meta8", "cpu", "headwise",
-            "others"}
+    legs = {"e2e", "group", "paged", "pagesize", "ratios", "reuse", "tokens", "meta8", "cpu",
+            "headwise", "others"}
     args.legs = set() if args.no_extra else (legs if args.legs == "all" else set(args.legs.split(",")))
     unknown = args.legs - legs
     if unknown:
@@ -622,6 +623,83 @@ def ratio_leg(name, q, K, V, dev, stream, flush, reps=10):
     return res
 
 
+def reuse_leg(q, K, V, w, dev, stream, steps=16, sigma=0.15):
+    """Cross-step page reuse ("TinyServe" 内存效率量化模型构建: a step moves the
+    metadata plus rho K new pages; 系统实现意义: hot pages stay resident): a
+    decode loop of `steps` steps on the bench workload, each appending one
+    token (metadata of its page rebuilt) and selecting with a query that
+    drifts by sigma N(0, 1) per step.  Run twice, through the hot-page call
+    (pages gathered at the previous step kept in L2) and through the plain
+    select; per step time, rho and bytes."""
+    import decode_attention_paged_kv_gb300 as dkv
+    from decode_attention_paged_kv_gb300 import accounting as acc
+
+    g = torch.Generator(device=dev).manual_seed(77)
+    qs, cur = [], q.float()
+    for _ in range(steps):
+        qs.append(cur.to(q.dtype))
+        cur = cur + sigma * torch.randn(cur.shape, generator=g, device=dev)
+    N0 = w.N - steps
+    kk = min(w.top_k, w.P)
+    ws = torch.zeros(dkv.workspace_bytes(w.B, w.Hq, w.Hkv, w.d, w.N, w.top_k), dtype=torch.uint8,
+                     device=dev)
+    out = torch.empty(w.B, w.Hq, w.d, dtype=torch.float32, device=dev)
+    sels = [torch.empty(w.B, w.Hq, kk, dtype=torch.int32, device=dev) for _ in range(steps)]
+    lens = [torch.full((w.B,), N0 + t + 1, dtype=torch.int32, device=dev) for t in range(steps)]
+    peak, _ = peaks()
+    res = {"workload": w.name, "steps": steps, "query_drift_sigma": sigma,
+           "timing": "each loop after an L2 flush; per step = loop time / steps"}
+    flush = L2Flush(dev)
+    for mode in ("hot", "plain"):
+        meta = dkv.kv_meta_build(K, seq_lens=lens[0])
+        hot = dkv.hot_state(w.B, w.Hkv, w.N, dev) if mode == "hot" else None
+
+        def loop():
+            for t in range(steps):
+                if t > 0:
+                    dkv.kv_meta_append(K, meta, seq_lens=lens[t])
+                dkv.decode_attn_select(qs[t], K, V, meta, w.top_k, out=out, selected=sels[t],
+                                       workspace=ws, seq_lens=lens[t], hot=hot, step=t + 1)
+
+        loop()  # warm-up (and the selections the counters are checked against)
+        if hot is not None:
+            hot.zero_()
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        loop()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        if dkv.read_device_status(ws) != 0:
+            raise SystemExit("device status error in the reuse leg")
+        r = {"ms_per_step": round(ms, 5), "queries_per_s": round(w.B / (ms * 1e-3), 1)}
+        if hot is not None:
+            loads, hits = dkv.hot_stats(hot)
+            first = union_tokens(sels[0], w) // w.S
+            r["pages_gathered"] = loads
+            r["pages_held_from_previous_step"] = hits
+            # rho over steps 2.. (step 1 has no previous step)
+            r["rho"] = round(1.0 - hits / max(1, loads - first), 4)
+        res[mode] = r
+        del meta, hot
+    # bytes per step (steps 2..): metadata + the pages gathered (algorithmic),
+    # and the pages new to the step (the rho K S term of the pages' model)
+    loads, hits = res["hot"]["pages_gathered"], res["hot"]["pages_held_from_previous_step"]
+    first = union_tokens(sels[0], w) // w.S
+    per_step_pages = (loads - first) / (steps - 1)
+    page_bytes = 2 * 16 * w.d * 2
+    meta_b = acc.meta_bytes(w.B, w.Hkv, w.d, w.N, w.S) - w.B * w.Hkv * w.N * w.d * 2
+    res["bytes_per_step"] = {
+        "metadata": int(meta_b), "gathered_pages": int(per_step_pages * page_bytes),
+        "new_pages_rho_K_S": int((per_step_pages - hits / (steps - 1)) * page_bytes)}
+    gbs = (meta_b + per_step_pages * page_bytes) / (res["plain"]["ms_per_step"] * 1e-3) / 1e9
+    res["plain"]["GB/s_algorithmic"] = round(gbs, 1)
+    res["plain"]["frac_of_8tbs"] = round(gbs / NOMINAL_HBM_GBS, 4)
+    res["hot_vs_plain_time"] = round(res["hot"]["ms_per_step"] / res["plain"]["ms_per_step"], 4)
+    return res
+
+
 def token_leg(q, K, V, w, dev, stream, flush, reps=10):
     """Token-level sparse attention on the bench workload, keeping the top 10%
     of the tokens per q-head (cold L2)."""
@@ -945,6 +1023,8 @@ def main():
             res["select_ratios"] = [ratio_leg(w.name, q, K, V, dev, stream, flush),
                                     ratio_leg(WORKLOADS[1].name, None, None, None, dev, stream,
                                               flush)]
+        if "reuse" in L:
+            res["reuse"] = reuse_leg(q, K, V, w, dev, stream)
         if "tokens" in L:
             res["topk_tokens"] = token_leg(q, K, V, w, dev, stream, flush)
         if "meta8" in L:

@@ -30,7 +30,7 @@ from . import build as _build_mod
 
 __all__ = [
     "Q4Cache", "PagedCache", "Meta8", "DkvError", "lib", "kv_meta_build", "kv_meta8_build",
-    "decode_attn_full",
+    "kv_meta_append", "hot_state", "hot_stats", "decode_attn_full",
     "decode_attn_select", "decode_attn_topk_tokens", "kv_quant4", "kv_dequant4",
     "workspace_bytes", "workspace_bytes_tokens", "read_device_status", "status_string",
     "PAGE_SIZE", "DKV_FLAG_GROUP_SELECT",
@@ -138,6 +138,11 @@ def lib() -> ctypes.CDLL:
                                                        vp, i32, vp, vp, sz, vp]
             L.dkv_workspace_bytes_tokens.argtypes = [P, i32]
             L.dkv_workspace_bytes_tokens.restype = sz
+            L.dkv_kv_meta_append.argtypes = [P, KVp, vp, vp, vp]
+            L.dkv_hot_state_bytes.argtypes = [P]
+            L.dkv_hot_state_bytes.restype = sz
+            L.dkv_decode_attn_select_hot.argtypes = [P, vp, KVp, KVp, vp, vp, i32, vp, i32, vp,
+                                                     vp, sz, i32, vp, sz, vp]
             L.dkv_kv_quant4.argtypes = [i64, i32, vp, vp, vp, vp, vp]
             L.dkv_kv_dequant4.argtypes = [i64, i32, vp, vp, vp, vp, vp]
             L.dkv_read_device_status.argtypes = [vp, vp]
@@ -146,7 +151,8 @@ def lib() -> ctypes.CDLL:
             L.dkv_status_string.restype = ctypes.c_char_p
             for name in ("dkv_kv_meta_build", "dkv_decode_attn_full", "dkv_decode_attn_select",
                          "dkv_decode_attn_topk_tokens", "dkv_kv_meta8_build",
-                         "dkv_decode_attn_select_meta8",
+                         "dkv_decode_attn_select_meta8", "dkv_kv_meta_append",
+                         "dkv_decode_attn_select_hot",
                          "dkv_kv_quant4", "dkv_kv_dequant4", "dkv_read_device_status",
                          "dkv_attn_ctas_per_sm"):
                 getattr(L, name).restype = ctypes.c_int
@@ -283,6 +289,40 @@ def kv_meta_build(K, page_size: int = PAGE_SIZE, seq_lens: Optional[torch.Tensor
     return mn, mx
 
 
+def kv_meta_append(K, meta, page_size: int = PAGE_SIZE,
+                   seq_lens: Optional[torch.Tensor] = None):
+    """After a decode step appended tokens: rebuild, in place, only the page
+    of `meta` (from kv_meta_build) holding each sequence's last token (N_b - 1,
+    N_b from seq_lens, else the cache length)."""
+    ks, B, H, N, d = _kv_struct(K)
+    mn, mx = meta
+    P = (N + page_size - 1) // page_size
+    if tuple(mn.shape) != (B, H, P, d) or not mn.is_contiguous() or not mx.is_contiguous():
+        raise ValueError("meta must be contiguous [B, Hkv, P, d]")
+    p = _params(None, B, H, N, d, None, None, seq_lens=seq_lens)
+    p.page_size = page_size
+    _check(lib().dkv_kv_meta_append(ctypes.byref(p), ctypes.byref(ks), mn.data_ptr(),
+                                    mx.data_ptr(), _stream(mn)), "dkv_kv_meta_append")
+    return mn, mx
+
+
+def hot_state(B: int, Hkv: int, N: int, device) -> torch.Tensor:
+    """A zeroed cross-step reuse state for decode_attn_select(hot=..., step=...)
+    on caches of B sequences, Hkv kv heads and N tokens."""
+    p = _params(None, B, Hkv, N, 64, None, None)
+    n = int(lib().dkv_hot_state_bytes(ctypes.byref(p)))
+    if n == 0:
+        raise ValueError("invalid shape for a reuse state")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def hot_stats(state: torch.Tensor) -> tuple[int, int]:
+    """(cache pages gathered, of them gathered at the previous step too), summed
+    over the calls since the state was zeroed."""
+    h = state[:16].cpu().view(torch.int64)
+    return int(h[0]), int(h[1])
+
+
 def kv_meta8_build(meta, page_size: int = PAGE_SIZE,
                    seq_lens: Optional[torch.Tensor] = None) -> Meta8:
     """8-bit page metadata from (meta_min, meta_max) [B, Hkv, P, d] (bf16 or
@@ -335,11 +375,14 @@ def decode_attn_select(q, K, V, meta, top_k: int, scale: Optional[float] = None,
                        selected: Optional[torch.Tensor] = None,
                        workspace: Optional[torch.Tensor] = None, flags: int = 0,
                        group_select: bool = False, seq_lens: Optional[torch.Tensor] = None,
-                       page_size: int = PAGE_SIZE):
+                       page_size: int = PAGE_SIZE, hot: Optional[torch.Tensor] = None,
+                       step: int = 0):
     """Query-aware page-sparse decode attention over the top_k pages per q-head
     (group_select: one selection per kv head group, by the summed bound scores;
     page_size: tokens per metadata / selection page, as meta was built with;
-    meta: (meta_min, meta_max), or a Meta8 from kv_meta8_build)."""
+    meta: (meta_min, meta_max), or a Meta8 from kv_meta8_build; hot, step: one
+    step (1, 2, ...) of a decode loop keeping hot pages in L2, with a state
+    from hot_state())."""
     if group_select:
         flags |= DKV_FLAG_GROUP_SELECT
     ks, B, H, N, d = _kv_struct(K)
@@ -372,6 +415,14 @@ def decode_attn_select(q, K, V, meta, top_k: int, scale: Optional[float] = None,
             m8.code_min.data_ptr(), m8.code_max.data_ptr(), m8.lo.data_ptr(),
             m8.step.data_ptr(), int(top_k), out.data_ptr(), _dtype_code(out.dtype), sel_ptr,
             ws.data_ptr(), nbytes, _stream(q)), "dkv_decode_attn_select_meta8")
+    elif hot is not None:
+        if m8 is not None:
+            raise ValueError("cross-step reuse takes 16-bit metadata")
+        _check(lib().dkv_decode_attn_select_hot(
+            ctypes.byref(p), q.data_ptr(), ctypes.byref(ks), ctypes.byref(vs), mn.data_ptr(),
+            mx.data_ptr(), int(top_k), out.data_ptr(), _dtype_code(out.dtype), sel_ptr,
+            hot.data_ptr(), hot.numel(), int(step), ws.data_ptr(), nbytes, _stream(q)),
+            "dkv_decode_attn_select_hot")
     else:
         _check(lib().dkv_decode_attn_select(ctypes.byref(p), q.data_ptr(), ctypes.byref(ks),
                                             ctypes.byref(vs), mn.data_ptr(), mx.data_ptr(),

@@ -263,8 +263,8 @@ size_t dkv_workspace_bytes(const dkv_params* p, int32_t top_k) {
   return L.ok ? L.total : 0;
 }
 
-dkv_status dkv_kv_meta_build(const dkv_params* p, const dkv_kv* K, void* meta_min,
-                             void* meta_max, void* stream) {
+static dkv_status meta_impl(const dkv_params* p, const dkv_kv* K, void* meta_min,
+                            void* meta_max, bool last_only, void* stream) {
   dkv_status st = check_params(p);
   if (st != DKV_OK) return st;
   if ((st = check_kv(p, K)) != DKV_OK) return st;
@@ -287,6 +287,7 @@ dkv_status dkv_kv_meta_build(const dkv_params* p, const dkv_kv* K, void* meta_mi
   a.meta_min = meta_min;
   a.meta_max = meta_max;
   a.lens = p->seq_lens;
+  a.last_only = last_only ? 1 : 0;
   if (K->format == DKV_KV_PAGED) {
     a.bt = K->block_table;
     a.bts = K->block_table_stride;
@@ -294,6 +295,16 @@ dkv_status dkv_kv_meta_build(const dkv_params* p, const dkv_kv* K, void* meta_mi
   }
   return cuda_status(dkv::launch_meta(K->format == DKV_KV_Q4G64, K->dtype == DKV_FP16, a,
                                       static_cast<cudaStream_t>(stream)));
+}
+
+dkv_status dkv_kv_meta_build(const dkv_params* p, const dkv_kv* K, void* meta_min,
+                             void* meta_max, void* stream) {
+  return meta_impl(p, K, meta_min, meta_max, false, stream);
+}
+
+dkv_status dkv_kv_meta_append(const dkv_params* p, const dkv_kv* K, void* meta_min,
+                              void* meta_max, void* stream) {
+  return meta_impl(p, K, meta_min, meta_max, true, stream);
 }
 
 static dkv_status attn_common(const dkv_params* p, const void* q, const dkv_kv* K,
@@ -433,12 +444,31 @@ struct Meta8Ptrs {
   const float* step;
 };
 
-// The page-sparse call over 16-bit metadata (m8 == nullptr) or 8-bit metadata.
+// Cross-step reuse state of dkv_decode_attn_select_hot: a 256-byte header
+// (u64 pages gathered, u64 of them gathered at the previous step) and the
+// per-page stamps [B, Hkv, ceil(N / 16)] u32.
+struct HotArgs {
+  void* state;
+  size_t bytes;
+  int32_t step;
+};
+
+static size_t hot_stamp_pages(const dkv_params& p) {
+  return static_cast<size_t>(ceil_div(p.seq_len, dkv::kPage));
+}
+
+static size_t hot_bytes(const dkv_params& p) {
+  return kAlign + align_up(sizeof(uint32_t) * static_cast<size_t>(p.batch) * p.num_kv_heads *
+                           hot_stamp_pages(p));
+}
+
+// The page-sparse call over 16-bit metadata (m8 == nullptr) or 8-bit metadata,
+// with cross-step reuse when hot != nullptr.
 static dkv_status select_impl(const dkv_params* p, const void* q, const dkv_kv* K,
                               const dkv_kv* V, const void* meta_min, const void* meta_max,
                               const Meta8Ptrs* m8, int32_t top_k, void* out, int32_t out_dtype,
                               int32_t* selected, void* workspace, size_t workspace_bytes,
-                              void* stream) {
+                              void* stream, const HotArgs* hot = nullptr) {
   dkv_status st = check_params(p);
   if (st != DKV_OK) return st;
   if (top_k < 1) return DKV_ERR_SHAPE;
@@ -446,6 +476,13 @@ static dkv_status select_impl(const dkv_params* p, const void* q, const dkv_kv* 
   if ((st = attn_common(p, q, K, V, out, out_dtype, workspace, workspace_bytes, top_k, L)) !=
       DKV_OK)
     return st;
+  if (hot != nullptr) {
+    if (K->format == DKV_KV_Q4G64) return DKV_ERR_UNSUPPORTED;
+    if (hot->state == nullptr) return DKV_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(hot->state) & 15u) return DKV_ERR_ALIGN;
+    if (hot->bytes < hot_bytes(*p)) return DKV_ERR_WORKSPACE;
+    if (hot->step < 1) return DKV_ERR_SHAPE;
+  }
   if (m8 == nullptr) {
     if (meta_min == nullptr || meta_max == nullptr) return DKV_ERR_NULL;
     if (!aligned16(meta_min) || !aligned16(meta_max)) return DKV_ERR_ALIGN;
@@ -473,6 +510,25 @@ static dkv_status select_impl(const dkv_params* p, const void* q, const dkv_kv* 
   dkv::AttnArgs a = attn_args(p, q, L, ws);
   if (!cache_views(p, K, V, &mk, &mv, &a)) return DKV_ERR_CUDA;
   a.sub_log2 = p->page_size == 4 ? 2 : (p->page_size == 8 ? 1 : 0);
+  if (hot != nullptr) {
+    uint8_t* hs = static_cast<uint8_t*>(hot->state);
+    a.hot_stats = reinterpret_cast<unsigned long long*>(hs);
+    a.hot_stamp = reinterpret_cast<uint32_t*>(hs + kAlign);
+    a.hot_pages = static_cast<int>(hot_stamp_pages(*p));
+    a.hot_step = static_cast<uint32_t>(hot->step);
+    // Keep as many units' pages as half the L2 holds, at the union's upper
+    // bound: G * kk selection pages, each S / 16 cache pages (or one), per unit.
+    int dev = 0, l2 = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
+      return DKV_ERR_CUDA;
+    const int64_t sel_pages = static_cast<int64_t>(G) * L.kk *
+                              (p->page_size > dkv::kPage ? p->page_size / dkv::kPage : 1);
+    const int64_t pages = std::min<int64_t>(sel_pages, hot_stamp_pages(*p));
+    const int64_t unit_bytes = pages * 2 * dkv::kPage * p->head_dim * 2;
+    a.hot_keep_units = static_cast<int>(std::min<int64_t>(
+        static_cast<int64_t>(p->batch) * p->num_kv_heads, (l2 / 2) / std::max<int64_t>(unit_bytes, 1)));
+  }
   a.union_list = ulist;
   a.union_count = ucount;
   a.union_stride = L.union_stride;
@@ -583,6 +639,22 @@ static dkv_status select_impl(const dkv_params* p, const void* q, const dkv_kv* 
   }
 
   return run_attention(p, a, true, f16, mk, mv, out, out_dtype, s);
+}
+
+size_t dkv_hot_state_bytes(const dkv_params* p) {
+  if (check_params(p) != DKV_OK) return 0;
+  return hot_bytes(*p);
+}
+
+dkv_status dkv_decode_attn_select_hot(const dkv_params* p, const void* q, const dkv_kv* K,
+                                      const dkv_kv* V, const void* meta_min,
+                                      const void* meta_max, int32_t top_k, void* out,
+                                      int32_t out_dtype, int32_t* selected, void* hot_state,
+                                      size_t hot_state_bytes, int32_t step, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+  const HotArgs hot{hot_state, hot_state_bytes, step};
+  return select_impl(p, q, K, V, meta_min, meta_max, nullptr, top_k, out, out_dtype, selected,
+                     workspace, workspace_bytes, stream, &hot);
 }
 
 dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_kv* K,

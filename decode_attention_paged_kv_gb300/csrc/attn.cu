@@ -465,6 +465,9 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
     constexpr int kIssueLanes = 8;
     constexpr int kQ4Parts = 6, kQ4IssueLanes = kQ4Parts * kConsumerWarps;
     const uint64_t pol = l2_evict_first_policy();
+    const uint64_t pol_keep = l2_evict_last_policy();
+    const bool hot = SPARSE && !Q4 && a.hot_stamp != nullptr;
+    unsigned long long hot_loads = 0, hot_hits = 0;  // lane 0's running totals
     // consumer warp this lane feeds
     const int my_w = Q4 ? (lane < kQ4IssueLanes ? lane / kQ4Parts : 0) : (lane & 3);
     const int part = lane % kQ4Parts;  // 4-bit: which of the page's copies
@@ -476,6 +479,7 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
       // Next work item with pages (sparse chunks past a unit's union are
       // skipped here and never published).
       int item = 0, n = 0, b = 0, kvh = 0, first = 0;
+      bool keep = false;  // reuse: the item's pages stay in L2 for the next step
       while (true) {
         if (lane == 0) item = static_cast<int>(atomicAdd(a.work_counter, 1u));
         item = __shfl_sync(0xffffffffu, item, 0);
@@ -506,6 +510,22 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
           if (n == 0) continue;
           const int2* src = a.union_list + static_cast<int64_t>(unit) * a.union_stride + first;
           for (int j = lane; j < n; j += 32) list[j] = __ldcg(src + j);
+          if (hot) {
+            // Cross-step reuse: each page of a unit's union is in exactly one
+            // item, so its stamp has one writer per call.
+            uint32_t* stamp = a.hot_stamp + static_cast<int64_t>(unit) * a.hot_pages;
+            int hits = 0;
+            for (int j = lane; j < n; j += 32) {
+              const int page = __ldcg(src + j).x;
+              const uint32_t last = stamp[page];
+              stamp[page] = a.hot_step;
+              hits += last != 0u && last + 1u == a.hot_step;
+            }
+            hits = __reduce_add_sync(0xffffffffu, hits);
+            hot_loads += n;
+            hot_hits += hits;
+            keep = unit < a.hot_keep_units;
+          }
           __syncwarp();
         } else {
           // (with per-sequence lengths, chunks past the sequence are skipped)
@@ -625,8 +645,9 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
               // {channel, token in block, half, kv head, block} of a pool
               const int y = a.bt != nullptr ? 0 : page * kPage;
               const int z = a.bt != nullptr ? blocks[j] : b;
-              tma_load_5d_hint(dst, &mk, full0 + 8 * s, 0, y, 0, kvh, z, pol);
-              tma_load_5d_hint(dst + C::kPageBytes, &mv, full0 + 8 * s, 0, y, 0, kvh, z, pol);
+              const uint64_t pl = keep ? pol_keep : pol;
+              tma_load_5d_hint(dst, &mk, full0 + 8 * s, 0, y, 0, kvh, z, pl);
+              tma_load_5d_hint(dst + C::kPageBytes, &mv, full0 + 8 * s, 0, y, 0, kvh, z, pl);
             }
           }
           if (!__all_sync(0xffffffffu, lok)) break;
@@ -662,6 +683,10 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
       }
     }
     __syncwarp();
+    if (hot && lane == 0 && hot_loads > 0) {
+      atomicAdd(a.hot_stats, hot_loads);
+      atomicAdd(a.hot_stats + 1, hot_hits);
+    }
     if (lane == 0) {
       // This CTA fetches no more work.  The last CTA to get here resets the
       // counters for the next call (every earlier fetch is ordered before its

@@ -110,6 +110,18 @@ struct AttnArgs {
   const int32_t* lens;         // per-sequence lengths [B] or nullptr (all N)
   uint32_t* status;
   uint64_t wait_limit_ns;
+  // Cross-step page reuse (sparse path, 16-bit caches; nullptr when unused):
+  // per (batch, kv head) and cache page, the step that last gathered the page
+  // (0: never), and counters of pages gathered and of those gathered at
+  // hot_step - 1 too.  The pages of units (b * Hkv + kv head) below
+  // hot_keep_units -- as many as half the L2 holds -- are loaded with an L2
+  // evict-last policy, so the next step finds the ones it selects again;
+  // every other page streams through with evict-first.
+  uint32_t* hot_stamp;         // [B * Hkv, hot_pages]
+  int hot_pages;               // cache pages per (batch, kv head)
+  uint32_t hot_step;           // this call's step, >= 1
+  int hot_keep_units;
+  unsigned long long* hot_stats;  // [0] pages gathered, [1] of them gathered at hot_step - 1
 };
 
 struct MergeArgs {
@@ -234,6 +246,7 @@ struct MetaArgs {
   int nblocks;
   const int32_t* lens;         // per-sequence lengths [B] or nullptr (all N)
   int S;                       // tokens per metadata page (16, 32 or 64); P = ceil(N / S)
+  int last_only;               // 1: only the page holding each sequence's last token
 };
 
 // Launch `kern` with programmatic stream serialisation, so it may begin while

@@ -30,17 +30,20 @@ __global__ void __launch_bounds__(kMetaThreads, Q4 ? 4 : 2) meta_kernel(const Me
   griddep_launch_dependents();
   griddep_wait();
   const int vpr = a.d / 8;  // 16-byte vectors per row
-  const int64_t total = static_cast<int64_t>(a.B) * a.Hkv * a.P * vpr;
+  // every page, or (last_only) one page per (batch, kv head)
+  const int pages = a.last_only ? 1 : a.P;
+  const int64_t total = static_cast<int64_t>(a.B) * a.Hkv * pages * vpr;
   for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
        idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int v = static_cast<int>(idx % vpr);
-    const int64_t pg = idx / vpr;  // (b * Hkv + h) * P + page
-    const int page = static_cast<int>(pg % a.P);
-    const int64_t bh = pg / a.P;
+    const int64_t bh = idx / vpr / pages;
     const int h = static_cast<int>(bh % a.Hkv);
     const int b = static_cast<int>(bh / a.Hkv);
-    const int t0 = page * a.S;  // a metadata page of S tokens
     const int Nb = seq_len_of(a.lens, b, a.N);
+    // the page holding the sequence's newest token, or page idx / vpr % P
+    const int page = a.last_only ? (Nb - 1) / a.S : static_cast<int>(idx / vpr % a.P);
+    const int64_t pg = bh * a.P + page;  // (b * Hkv + h) * P + page
+    const int t0 = page * a.S;  // a metadata page of S tokens
     if (t0 >= Nb) continue;  // past a shorter sequence: not written
     const int nt = min(a.S, Nb - t0);
     uint32_t kmin[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
@@ -299,7 +302,8 @@ int grid_for(int64_t threads, int block) {
 
 cudaError_t launch_meta(bool q4, bool f16, const MetaArgs& a, cudaStream_t s) {
   (void)f16;  // min / max on order-preserving keys: identical code for bf16 and fp16
-  const int64_t work = static_cast<int64_t>(a.B) * a.Hkv * a.P * (a.d / 8);
+  const int64_t work =
+      static_cast<int64_t>(a.B) * a.Hkv * (a.last_only ? 1 : a.P) * (a.d / 8);
   const dim3 grid(grid_for(work, kMetaThreads)), block(kMetaThreads);
   return q4 ? launch_pdl(meta_kernel<true>, grid, block, 0, s, a)
             : launch_pdl(meta_kernel<false>, grid, block, 0, s, a);

@@ -181,6 +181,17 @@ size_t dkv_workspace_bytes(const dkv_params* p, int32_t top_k);
 dkv_status dkv_kv_meta_build(const dkv_params* p, const dkv_kv* K, void* meta_min,
                              void* meta_max, void* stream);
 
+/* Page metadata after a decode step appended tokens: rebuilds, for every
+   (batch entry b, kv head), only the page holding the sequence's last token
+   N_b - 1 (N_b from seq_lens, else seq_len), the one page an appended token
+   changes; every other page's (m_j, M_j) is left as it is.  Same arguments
+   and layout as dkv_kv_meta_build, whose result it reproduces bit for bit
+   when the other pages are already built.  ("TinyServe: Query-Aware Cache
+   Selection for Efficient LLM Serving", 结构化内存布局 and 系统实现意义: the
+   page metadata is kept alongside the cache as it grows.) */
+dkv_status dkv_kv_meta_append(const dkv_params* p, const dkv_kv* K, void* meta_min,
+                              void* meta_max, void* stream);
+
 /* Exact decode attention.  out [B, Hq, d] in out_dtype (DKV_FP32 | DKV_BF16 |
    DKV_FP16).  Splits the sequence into fixed chunks whose length depends only
    on d, so evaluating one kv head at a time (a view with Hkv = 1) gives results
@@ -199,6 +210,38 @@ dkv_status dkv_decode_attn_select(const dkv_params* p, const void* q, const dkv_
                                   const void* meta_max, int32_t top_k, void* out,
                                   int32_t out_dtype, int32_t* selected, void* workspace,
                                   size_t workspace_bytes, void* stream);
+
+/* dkv_decode_attn_select as one step of a decode loop that keeps hot pages
+   resident across steps ("TinyServe: Query-Aware Cache Selection for
+   Efficient LLM Serving", 内存效率量化模型构建 / 单步解码内存移动公式: a
+   step moves the metadata of all pages plus only the rho K pages not already
+   held; 系统实现意义: hot pages stay resident).  The cache is HBM-resident,
+   so "resident" here means the L2: the pages of the first (batch entry, kv
+   head) units, as many as half the L2 holds at the selection's largest
+   union, are loaded with an L2 evict-last policy and stay there for the
+   next step, which finds those it selects again; every other page streams
+   through with evict-first.  Results are exactly those
+   of dkv_decode_attn_select on the same arguments; only the cache policy and
+   the counters below differ.
+   - hot_state: caller-owned DEVICE buffer of dkv_hot_state_bytes(p) bytes
+     (16-byte aligned), zero-filled once before the first step of a decode
+     sequence and then passed, unchanged, to every step of it.  It holds a
+     256-byte header -- u64 at offset 0: cache pages gathered so far, u64 at
+     offset 8: how many of them the step before had gathered too, both
+     summed over calls (rho of a run = 1 - [8] / [0]; the caller may zero
+     them between reads) -- and one u32 stamp per (batch entry, kv head,
+     16-token cache page): the last step that gathered it.
+   - step: 1 for the first step, +1 for each step after (a page counts as
+     held when its stamp is step - 1).
+   - 16-bit caches only (DKV_KV_DENSE or DKV_KV_PAGED; DKV_ERR_UNSUPPORTED for
+     DKV_KV_Q4G64).  One hot_state serves one call at a time. */
+size_t dkv_hot_state_bytes(const dkv_params* p);
+dkv_status dkv_decode_attn_select_hot(const dkv_params* p, const void* q, const dkv_kv* K,
+                                      const dkv_kv* V, const void* meta_min,
+                                      const void* meta_max, int32_t top_k, void* out,
+                                      int32_t out_dtype, int32_t* selected, void* hot_state,
+                                      size_t hot_state_bytes, int32_t step, void* workspace,
+                                      size_t workspace_bytes, void* stream);
 
 /* 8-bit page metadata from (meta_min, meta_max) [B, Hkv, P, d] of dtype
    meta_dtype (DKV_BF16 | DKV_FP16).  TinyServe's bound (相关性函数实例化) needs

@@ -72,6 +72,16 @@ def test_workspace_bytes_layout(L):
     assert L.dkv_workspace_bytes(None, 0) == 0
 
 
+def test_hot_state_bytes(L):
+    # a 256-byte header (two u64 counters) and one u32 stamp per 16-token cache
+    # page of every (batch entry, kv head), rounded up to 256 bytes
+    p = _params()
+    pages = -(-p.seq_len // 16)
+    want = 256 + -(-(4 * p.batch * p.num_kv_heads * pages) // 256) * 256
+    assert L.dkv_hot_state_bytes(ctypes.byref(p)) == want
+    assert L.dkv_hot_state_bytes(ctypes.byref(_params(head_dim=96))) == 0
+
+
 def test_host_validation_before_launch(L):
     import decode_attention_paged_kv_gb300 as dkv
     kv = dkv._KV()
