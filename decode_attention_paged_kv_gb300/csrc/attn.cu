@@ -57,8 +57,12 @@ struct ItemDesc {
 };
 
 // QUAD: four pages a stage (the dense 4-bit path, whose pages are consecutive).
-template <int D, bool Q4, bool QUAD>
+// MHA: the 4-bit single-head layout, three CTAs per SM (fewer stages each --
+// two consecutive pages a stage in the dense path -- and a merge area of one
+// row).
+template <int D, bool Q4, bool QUAD, bool MHA = false>
 struct AttnCfg {
+  static constexpr int kCtasPerSm = MHA ? 3 : kAttnCtasPerSm;
   static constexpr int kPageBytes = kPage * D * 2;          // one 16-bit page tile
   static constexpr int kCodeBytes = kPage * D / 2;          // 4-bit: one tensor's page of codes
   static constexpr int kGroupBytes = kPage * (D / 64) * 2;  // 4-bit: one page of gmin (or gmax)
@@ -66,28 +70,29 @@ struct AttnCfg {
   // dense path (consecutive pages of the cache move with one copy per part):
   //   K codes [q][page] | V codes [q][page] | K min | K max | V min | V max,
   // each bound array [q][page], q = kPagesPerStage.
-  static constexpr int kPagesPerStage = QUAD ? 4 : 1;
+  static constexpr int kPagesPerStage = QUAD ? (MHA ? 2 : 4) : 1;
   static constexpr int kQ4PageBytes = 2 * kCodeBytes + 4 * kGroupBytes;
   static constexpr int kQ4VCodeOffset = kPagesPerStage * kCodeBytes;
   static constexpr int kQ4BoundsOffset = 2 * kPagesPerStage * kCodeBytes;
   static constexpr int kStageBytes =
       Q4 ? (kPagesPerStage * kQ4PageBytes + 127) / 128 * 128 : 2 * kPageBytes;
   // 4-bit pages are a quarter the size: more of them in flight.
-  static constexpr int kStages = Q4 ? (D == 128 ? 32 : 48) / kPagesPerStage : attn_stages(D);
+  static constexpr int kStages =
+      Q4 ? (MHA ? (D == 128 ? 24 : 32) : (D == 128 ? 32 : 48)) / kPagesPerStage : attn_stages(D);
   static constexpr int kSub = kStages / kConsumerWarps;             // stages per consumer warp
   static constexpr int kBarOffset = (kStages * kStageBytes + 15) / 16 * 16;
   static constexpr int kStageMetaOffset = kBarOffset + (2 * kStages + 4) * 8;
   static constexpr int kDescOffset = kStageMetaOffset + kStages * kPagesPerStage * 8;
   static constexpr int kMergeOffset = kDescOffset + 2 * 16;
   static constexpr int kMergeRow = D + 2;                           // o[D], max, sum
-  static constexpr int kMergeBytes = (kConsumerWarps - 1) * 8 * kMergeRow * 4;
+  static constexpr int kMergeBytes = (kConsumerWarps - 1) * (MHA ? 1 : 8) * kMergeRow * 4;
   static constexpr int kListOffset = kMergeOffset + kMergeBytes;
   static constexpr int kBlockOffset = kListOffset + 8 * kMaxSelectList;  // paged: pool blocks
   static constexpr int kMiscOffset = kBlockOffset + 4 * kMaxSelectList;
   static constexpr int kSmemBytes = 1024 + kMiscOffset + 16;
   static_assert(Q4 || kPageBytes % 1024 == 0, "TMA stages must stay 1024-byte aligned");
   static_assert(kStages % kConsumerWarps == 0, "one sub-ring per consumer warp");
-  static_assert((kSmemBytes + 1024) * kAttnCtasPerSm <= 228 * 1024, "two CTAs per SM");
+  static_assert((kSmemBytes + 1024) * kCtasPerSm <= 228 * 1024, "the CTAs fit an SM");
 };
 
 // Shared address of channels [c, c+8) of token t in a page tile written by the
@@ -187,20 +192,24 @@ __device__ __forceinline__ void q4_ragged_codes(const AttnArgs& a, int b, int kv
 // A nibble masked into the mantissa of 1024 (bits 0-3) or 64 (bits 4-7) gives
 // bias + code exactly; subtracting the bias leaves the code, then
 // x = fp16(code * step + mn) by one fp16 FMA -- the dequantisation of the
-// 4-bit format, bit for bit.  A page with a tiny group anywhere in the warp
-// (range below 451 * 2^-24: its step is an fp32 value) takes a slower path
-// that dequantises every pair from its group's min and max.
+// 4-bit format, bit for bit.  The steps come from the stage, where the owning
+// warp computed each group's once (q4_stage_steps).  A stage with a tiny group
+// (range below 451 * 2^-24: its step is an fp32 value) keeps its maxes and
+// takes a slower path that dequantises every pair from its group's min and
+// max.
 template <int D>
 struct Q4Page {
   uint32_t kc[2][D / 32];  // K codes, tokens g and g + 8
   uint32_t vc[4][D / 64];  // V codes, tokens 2 t4, 2 t4 + 1, 2 t4 + 8, 2 t4 + 9
-  __half kmn[2], kx[2];    // K group min and step (group max on a tiny page), tokens g, g + 8
+  __half kmn[2], kx[2];    // K group min and step (group max on a tiny stage), tokens g, g + 8
   uint32_t vmn[2], vx[2];  // V: the same as half pairs, tokens (2 t4, 2 t4 + 1) and + 8
-  bool tiny;               // warp-uniform: the page has a tiny group
+  bool tiny;               // warp-uniform: the page's stage has a tiny group
 };
 
 template <typename C, int D>
-__device__ __forceinline__ void q4_load(const uint8_t* st, int slot, int g, int t4, Q4Page<D>& r) {
+__device__ __forceinline__ void q4_load(const uint8_t* st, int slot, int g, int t4, bool tiny,
+                                        Q4Page<D>& r) {
+  r.tiny = tiny;
   constexpr int ng = D / 64;
   constexpr int kBound = C::kPagesPerStage * kPage * ng;  // halves from one bound array to the next
   const __half* gb =
@@ -252,27 +261,51 @@ __device__ __forceinline__ void q4_load(const uint8_t* st, int slot, int g, int 
       r.vx[h] = *reinterpret_cast<const uint32_t*>(vmx);
     }
   }
-  // Group bounds -> steps (fp16 steps of normal groups; a tiny group keeps its max).
-  float kr[2], vr[4];
+}
+
+// A landed 4-bit stage of `cnt` pages: the owning warp replaces every group's
+// max by its fp16 step, each group once, unless a group of the stage is tiny
+// (then the maxes stay and the stage's pages take the tiny-group path).
+// Returns that warp-uniform flag.  The generic-proxy writes are fenced before
+// the stage is handed back to the producer's bulk copies (q4_stage_release).
+template <typename C, int D>
+__device__ __forceinline__ bool q4_stage_steps(uint8_t* st, int cnt, int lane) {
+  constexpr int ng = D / 64;
+  constexpr int kBound = C::kPagesPerStage * kPage * ng;  // halves per bound array
+  constexpr int kPer = (kBound + 31) / 32;                // groups per lane per tensor
+  __half* gb = reinterpret_cast<__half*>(st + C::kQ4BoundsOffset);
+  const int n = cnt * kPage * ng;  // groups per tensor in this stage
+  __half step[2][kPer];
   bool tiny = false;
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    kr[h] = q4_range(r.kmn[h], r.kx[h]);
-    const __half2 mn = *reinterpret_cast<const __half2*>(&r.vmn[h]);
-    const __half2 mx = *reinterpret_cast<const __half2*>(&r.vx[h]);
-    vr[2 * h] = q4_range(__low2half(mn), __low2half(mx));
-    vr[2 * h + 1] = q4_range(__high2half(mn), __high2half(mx));
-    tiny |= fminf(kr[h], fminf(vr[2 * h], vr[2 * h + 1])) < kQ4TinyRange;
-  }
-  r.tiny = __any_sync(0xffffffffu, tiny);
-  if (!r.tiny) {
+  for (int v = 0; v < 2; ++v) {  // K, V
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      r.kx[h] = q4_step16(kr[h]);
-      const __half2 st = __halves2half2(q4_step16(vr[2 * h]), q4_step16(vr[2 * h + 1]));
-      r.vx[h] = *reinterpret_cast<const uint32_t*>(&st);
+    for (int i = 0; i < kPer; ++i) {
+      const int e = lane + 32 * i;
+      step[v][i] = __ushort_as_half(0);
+      if (e < n) {
+        const float range = q4_range(gb[2 * v * kBound + e], gb[(2 * v + 1) * kBound + e]);
+        tiny |= range < kQ4TinyRange;
+        step[v][i] = q4_step16(fmaxf(range, kQ4TinyRange));
+      }
     }
   }
+  tiny = __any_sync(0xffffffffu, tiny);
+  if (!tiny) {
+#pragma unroll
+    for (int v = 0; v < 2; ++v)
+#pragma unroll
+      for (int i = 0; i < kPer; ++i)
+        if (lane + 32 * i < n) gb[(2 * v + 1) * kBound + lane + 32 * i] = step[v][i];
+  }
+  __syncwarp();
+  return tiny;
+}
+
+// Before a stage the consumers wrote to goes back to the producer's bulk
+// copies: order those generic-proxy writes before the async proxy's.
+__device__ __forceinline__ void q4_stage_release() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // (bits & mask) | bias, minus the bias: the masked nibbles as exact fp16 codes.
@@ -393,6 +426,85 @@ __device__ __forceinline__ void q4_pv(const Q4Page<D>& r, uint32_t a0, uint32_t 
     q4_pv_t<D, false>(r, a0, a1, a2, a3, acc);
 }
 
+// One query head per kv head (G = 1): the head-group MMA layout above would
+// fill 1 of its 16 A rows.  Instead the page's tokens take the M side of
+// S = K q (A = the K fragments the lane already builds, B = the query
+// fragments, column 0) and its channels the M side of O^T = V^T P (A = the V
+// fragments, B = the softmax weights as two columns, hi and lo): 16 MMAs a
+// page instead of 32, and 32 accumulators instead of 64.  Scores land in
+// lanes t4 = 0 (d[0]: token g, d[2]: token g + 8); output tile 4 j + m of
+// lane (g, 0) holds channels D/8 g + 8 j + 2 m (d[0] + d[1]) and + 1
+// (d[2] + d[3]).  (Layouts checked by a CPU emulation of the fragments.)
+template <int D, bool TINY>
+__device__ __forceinline__ void q4_scores_mha_t(const Q4Page<D>& r,
+                                                const uint32_t (&qa)[D / 16][2], float (&sc)[4]) {
+  __half2 x2[2], mn2[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    x2[h] = __half2half2(r.kx[h]);
+    mn2[h] = __half2half2(r.kmn[h]);
+  }
+#pragma unroll
+  for (int j = 0; j < D / 32; ++j) {
+    uint32_t v[2][4];  // [token g, g + 8][nibble pairs (0,4) (1,5) (2,6) (3,7)]
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t w = r.kc[h][j], w8 = w >> 8;
+      const __half2 c[4] = {q4_codes(w, kNib0, kBias1024), q4_codes(w, kNib1, kBias64),
+                            q4_codes(w8, kNib0, kBias1024), q4_codes(w8, kNib1, kBias64)};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        v[h][i] = TINY ? q4_value_any(c[i], mn2[h], x2[h]) : q4_value(c[i], x2[h], mn2[h]);
+    }
+    mma16816<true>(sc, v[0][0], v[1][0], v[0][1], v[1][1], qa[2 * j][0], qa[2 * j][1]);
+    mma16816<true>(sc, v[0][2], v[1][2], v[0][3], v[1][3], qa[2 * j + 1][0], qa[2 * j + 1][1]);
+  }
+}
+template <int D>
+__device__ __forceinline__ void q4_scores_mha(const Q4Page<D>& r, const uint32_t (&qa)[D / 16][2],
+                                              float (&sc)[4]) {
+  if (r.tiny)
+    q4_scores_mha_t<D, true>(r, qa, sc);
+  else
+    q4_scores_mha_t<D, false>(r, qa, sc);
+}
+
+template <int D, bool TINY>
+__device__ __forceinline__ void q4_pv_mha_t(const Q4Page<D>& r, uint32_t b0, uint32_t b1,
+                                            float (&acc)[D / 16][4]) {
+#pragma unroll
+  for (int j = 0; j < D / 64; ++j) {
+    uint32_t bv[2][8];  // [token pair][nibble]: channel D/8 g + 8 j + nibble
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const __half2 mn = *reinterpret_cast<const __half2*>(&r.vmn[h]);
+      const __half2 x2 = *reinterpret_cast<const __half2*>(&r.vx[h]);
+      const uint32_t wa = r.vc[2 * h][j], wb = r.vc[2 * h + 1][j];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint32_t u = __byte_perm(wa, wb, hh ? 0x7632 : 0x5410), u8 = u >> 8;
+        const __half2 c[4] = {q4_codes(u, kNib0, kBias1024), q4_codes(u, kNib1, kBias64),
+                              q4_codes(u8, kNib0, kBias1024), q4_codes(u8, kNib1, kBias64)};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          bv[h][4 * hh + i] = TINY ? q4_value_any(c[i], mn, x2) : q4_value(c[i], x2, mn);
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+      mma16816<true>(acc[4 * j + m], bv[0][2 * m], bv[0][2 * m + 1], bv[1][2 * m],
+                     bv[1][2 * m + 1], b0, b1);
+  }
+}
+template <int D>
+__device__ __forceinline__ void q4_pv_mha(const Q4Page<D>& r, uint32_t b0, uint32_t b1,
+                                          float (&acc)[D / 16][4]) {
+  if (r.tiny)
+    q4_pv_mha_t<D, true>(r, b0, b1, acc);
+  else
+    q4_pv_mha_t<D, false>(r, b0, b1, acc);
+}
+
 __device__ __forceinline__ void store_out(void* out, int out_dtype, int64_t off, float v) {
   if (out_dtype == 2) {
     static_cast<float*>(out)[off] = v;
@@ -403,12 +515,14 @@ __device__ __forceinline__ void store_out(void* out, int out_dtype, int64_t off,
   }
 }
 
-template <int D, bool F16, bool SPARSE, bool Q4>
-__global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
+// MHA: the 4-bit path's single-head layout (q4_scores_mha), for G = 1.
+template <int D, bool F16, bool SPARSE, bool Q4, bool MHA = false>
+__global__ void __launch_bounds__(kAttnThreads, MHA ? 3 : (D == 64 ? kAttnCtasPerSm : 0))
     attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mk,
                 const __grid_constant__ CUtensorMap mv) {
-  using C = AttnCfg<D, Q4, Q4 && !SPARSE>;
+  using C = AttnCfg<D, Q4, Q4 && !SPARSE, MHA>;
   static_assert(!Q4 || F16, "a 4-bit cache is dequantised to fp16");
+  static_assert(!MHA || Q4, "the single-head layout is the 4-bit path's");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -748,9 +862,10 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
       }
     }
     float m_run = -INFINITY, l_run = 0.f;
-    float acc[D / 8][4];
+    constexpr int kAccTiles = MHA ? D / 16 : D / 8;
+    float acc[kAccTiles][4];
 #pragma unroll
-    for (int cn = 0; cn < D / 8; ++cn) acc[cn][0] = acc[cn][1] = acc[cn][2] = acc[cn][3] = 0.f;
+    for (int cn = 0; cn < kAccTiles; ++cn) acc[cn][0] = acc[cn][1] = acc[cn][2] = acc[cn][3] = 0.f;
 
     bool aborted = false;
     // Stage q of the item goes to warp q % 4; it holds pages kQ q .. of the item.
@@ -769,6 +884,8 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
         break;
       }
       const int cnt = min(kQ, n_pages - sq * kQ);
+      bool stage_tiny = false;
+      if constexpr (Q4) stage_tiny = q4_stage_steps<C, D>(smem + s * C::kStageBytes, cnt, lane);
       for (int t = 0; t < cnt; ++t) {
       const int2 meta = stage_meta[s * kQ + t];
       const int page = meta.x;
@@ -781,12 +898,16 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
       if constexpr (Q4) {
         // Everything the warp needs from the page goes to registers; after
         // the stage's last page, the stage is free.
-        q4_load<C, D>(smem + s * C::kStageBytes, t, g, t4, q4);
+        q4_load<C, D>(smem + s * C::kStageBytes, t, g, t4, stage_tiny, q4);
         if (t == cnt - 1) {
+          q4_stage_release();
           __syncwarp();
           if (lane == 0) mbar_arrive(empty0 + 8 * s);
         }
-        q4_scores<D>(q4, qa, sc);
+        if constexpr (MHA)
+          q4_scores_mha<D>(q4, qa, sc[0]);
+        else
+          q4_scores<D>(q4, qa, sc);
       } else {
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
@@ -797,6 +918,50 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
         }
       }
 
+      if constexpr (MHA) {
+        // One head: lanes t4 = 0 hold the page's scores, tokens g (sc[0][0])
+        // and g + 8 (sc[0][2]).  Token t counts if bit t >> (4 - sub_log2)
+        // of the mask is set (head 0's sub-page; bit 0 for whole pages).
+        const int sl = SPARSE ? a.sub_log2 : 0;
+        const int tk0 = page * kPage + g, tk1 = tk0 + 8;
+        const bool on0 = (hmask >> (sl ? (g >> (4 - sl)) : 0)) & 1u;
+        const bool on1 = (hmask >> (sl ? ((g + 8) >> (4 - sl)) : 0)) & 1u;
+        const float s0 = (t4 == 0 && on0 && tk0 < Nb) ? sc[0][0] * a.scale_log2 : -INFINITY;
+        const float s1 = (t4 == 0 && on1 && tk1 < Nb) ? sc[0][2] * a.scale_log2 : -INFINITY;
+        float pmax = fmaxf(s0, s1);
+        pmax = fmaxf(pmax, __shfl_xor_sync(0xffffffffu, pmax, 4));
+        pmax = fmaxf(pmax, __shfl_xor_sync(0xffffffffu, pmax, 8));
+        pmax = fmaxf(pmax, __shfl_xor_sync(0xffffffffu, pmax, 16));
+        pmax = __shfl_sync(0xffffffffu, pmax, 0);  // warp-uniform
+        const float m_new = fmaxf(m_run, pmax);
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = exp2f(m_run - m_use);
+        const float p0 = exp2f(s0 - m_use), p1 = exp2f(s1 - m_use);
+        l_run = l_run * alpha + (p0 + p1);
+        if (m_new != m_run) {
+#pragma unroll
+          for (int cn = 0; cn < kAccTiles; ++cn) {
+            acc[cn][0] *= alpha;
+            acc[cn][1] *= alpha;
+            acc[cn][2] *= alpha;
+            acc[cn][3] *= alpha;
+          }
+        }
+        m_run = m_new;
+        // B of O^T += V^T P: the weights of tokens 2 t4, 2 t4 + 1 (b0) and
+        // 2 t4 + 8, 2 t4 + 9 (b1), their fp16 hi parts in column 0 (lanes
+        // g = 0) and lo parts in column 1 (g = 1).
+        const float x0 = __shfl_sync(0xffffffffu, p0, 8 * t4);
+        const float x1 = __shfl_sync(0xffffffffu, p0, 8 * t4 + 4);
+        const float y0 = __shfl_sync(0xffffffffu, p1, 8 * t4);
+        const float y1 = __shfl_sync(0xffffffffu, p1, 8 * t4 + 4);
+        uint32_t hx, lx, hy, ly;
+        split_pair<true>(x0, x1, hx, lx);
+        split_pair<true>(y0, y1, hy, ly);
+        const uint32_t b0 = g == 0 ? hx : (g == 1 ? lx : 0u);
+        const uint32_t b1 = g == 0 ? hy : (g == 1 ? ly : 0u);
+        q4_pv_mha<D>(q4, b0, b1, acc);
+      } else {
       // Online softmax (log2 domain) for head g over its 4 tokens of this page.
       // Token t of the page counts for head g if bit (g << sub_log2) +
       // (t >> (4 - sub_log2)) of the mask is set: the head selected its
@@ -873,8 +1038,66 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
         if (lane == 0) mbar_arrive(empty0 + 8 * s);
       }
       }
+      }
     }
 
+    if constexpr (MHA) {
+      // One head: the weight sums of lanes (g, 0) add up over g; lane (g, 0)
+      // holds output channels D/8 g + 8 j + 2 m and + 1 of tile 4 j + m.
+      l_run += __shfl_xor_sync(0xffffffffu, l_run, 4);
+      l_run += __shfl_xor_sync(0xffffffffu, l_run, 8);
+      l_run += __shfl_xor_sync(0xffffffffu, l_run, 16);
+      auto channel = [g](int tile) { return (D / 8) * g + 8 * (tile >> 2) + 2 * (tile & 3); };
+      if (consumers_any(aborted)) return;
+      if (warp > 0) {
+        float* r = mrg + (warp - 1) * C::kMergeRow;
+        if (lane == 0) {
+          r[D] = m_run;
+          r[D + 1] = l_run;
+        }
+        if (t4 == 0) {
+#pragma unroll
+          for (int cn = 0; cn < kAccTiles; ++cn) {
+            r[channel(cn)] = acc[cn][0] + acc[cn][1];
+            r[channel(cn) + 1] = acc[cn][2] + acc[cn][3];
+          }
+        }
+      }
+      consumers_sync();
+      if (warp == 0) {
+        float M = m_run;
+#pragma unroll
+        for (int w = 1; w < kConsumerWarps; ++w) M = fmaxf(M, mrg[(w - 1) * C::kMergeRow + D]);
+        float f[kConsumerWarps];
+        f[0] = (m_run == -INFINITY) ? 0.f : exp2f(m_run - M);
+        float L = f[0] * l_run;
+#pragma unroll
+        for (int w = 1; w < kConsumerWarps; ++w) {
+          const float* r = mrg + (w - 1) * C::kMergeRow;
+          f[w] = (r[D] == -INFINITY) ? 0.f : exp2f(r[D] - M);
+          L += f[w] * r[D + 1];
+        }
+        const int64_t pi = (static_cast<int64_t>(b) * a.Hq + kvh * a.G) * a.n_chunks + chunk;
+        float* po = a.part_o + pi * D;
+        if (t4 == 0) {
+#pragma unroll
+          for (int cn = 0; cn < kAccTiles; ++cn) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int c = channel(cn) + e;
+              float O = f[0] * (acc[cn][2 * e] + acc[cn][2 * e + 1]);
+#pragma unroll
+              for (int w = 1; w < kConsumerWarps; ++w) O += f[w] * mrg[(w - 1) * C::kMergeRow + c];
+              po[c] = O;
+            }
+          }
+        }
+        if (lane == 0) {
+          a.part_ml[2 * pi] = M;
+          a.part_ml[2 * pi + 1] = L;
+        }
+      }
+    } else {
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
 
@@ -926,6 +1149,7 @@ __global__ void __launch_bounds__(kAttnThreads, D == 64 ? kAttnCtasPerSm : 0)
         a.part_ml[2 * pi] = M;
         a.part_ml[2 * pi + 1] = L;
       }
+    }
     }
     consumers_sync();  // merge area free again; the descriptor slot was read by all
     if (threadIdx.x == 0) mbar_arrive(dempty0 + 8 * slot);
@@ -1054,15 +1278,15 @@ __global__ void __launch_bounds__(kSmallMergeThreads) merge_small_kernel(const M
 
 // Resident CTAs per SM of one attention instantiation (its registers and shared
 // memory as compiled), at most kAttnCtasPerSm; computed once.
-template <int D, bool F16, bool SPARSE, bool Q4>
+template <int D, bool F16, bool SPARSE, bool Q4, bool MHA = false>
 cudaError_t attn_ctas_per_sm_t(int* out) {
-  using C = AttnCfg<D, Q4, Q4 && !SPARSE>;
+  using C = AttnCfg<D, Q4, Q4 && !SPARSE, MHA>;
   static int cached = 0;  // benign race: every thread computes the same value
   if (cached > 0) {
     *out = cached;
     return cudaSuccess;
   }
-  auto kern = attn_kernel<D, F16, SPARSE, Q4>;
+  auto kern = attn_kernel<D, F16, SPARSE, Q4, MHA>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -1070,21 +1294,21 @@ cudaError_t attn_ctas_per_sm_t(int* out) {
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kAttnThreads, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   if (n < 1) return cudaErrorInvalidConfiguration;
-  cached = n < kAttnCtasPerSm ? n : kAttnCtasPerSm;
+  cached = n < C::kCtasPerSm ? n : C::kCtasPerSm;
   *out = cached;
   return cudaSuccess;
 }
 
-template <int D, bool F16, bool SPARSE, bool Q4>
+template <int D, bool F16, bool SPARSE, bool Q4, bool MHA = false>
 cudaError_t launch_attn_t(const AttnArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
                           int num_sms, cudaStream_t s) {
-  using C = AttnCfg<D, Q4, Q4 && !SPARSE>;
+  using C = AttnCfg<D, Q4, Q4 && !SPARSE, MHA>;
   int per_sm = 0;
-  cudaError_t e = attn_ctas_per_sm_t<D, F16, SPARSE, Q4>(&per_sm);
+  cudaError_t e = attn_ctas_per_sm_t<D, F16, SPARSE, Q4, MHA>(&per_sm);
   if (e != cudaSuccess) return e;
   const int64_t want = static_cast<int64_t>(num_sms) * per_sm;
   const int grid = static_cast<int>(a.n_items < want ? a.n_items : want);
-  return launch_pdl(attn_kernel<D, F16, SPARSE, Q4>, dim3(grid), dim3(kAttnThreads),
+  return launch_pdl(attn_kernel<D, F16, SPARSE, Q4, MHA>, dim3(grid), dim3(kAttnThreads),
                     C::kSmemBytes, s, a, mk, mv);
 }
 
@@ -1107,6 +1331,13 @@ cudaError_t launch_attn(int d, bool f16, bool sparse, const AttnArgs& a, const C
 cudaError_t launch_attn_q4(int d, bool sparse, const AttnArgs& a, int num_sms, cudaStream_t s) {
   CUtensorMap unused;  // the 4-bit path moves pages with 1-D bulk copies
   memset(&unused, 0, sizeof unused);
+  if (a.G == 1) {  // one query head per kv head: the single-head layout
+    if (d == 128)
+      return sparse ? launch_attn_t<128, true, true, true, true>(a, unused, unused, num_sms, s)
+                    : launch_attn_t<128, true, false, true, true>(a, unused, unused, num_sms, s);
+    return sparse ? launch_attn_t<64, true, true, true, true>(a, unused, unused, num_sms, s)
+                  : launch_attn_t<64, true, false, true, true>(a, unused, unused, num_sms, s);
+  }
   if (d == 128)
     return sparse ? launch_attn_t<128, true, true, true>(a, unused, unused, num_sms, s)
                   : launch_attn_t<128, true, false, true>(a, unused, unused, num_sms, s);
