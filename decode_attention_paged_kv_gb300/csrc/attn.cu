@@ -58,8 +58,8 @@ struct ItemDesc {
 
 // QUAD: four pages a stage (the dense 4-bit path, whose pages are consecutive).
 // MHA: the 4-bit single-head layout, three CTAs per SM (fewer stages each --
-// two consecutive pages a stage in the dense path -- and a merge area of one
-// row).
+// two consecutive pages a stage in the dense path -- and a merge area of
+// one row).
 template <int D, bool Q4, bool QUAD, bool MHA = false>
 struct AttnCfg {
   static constexpr int kCtasPerSm = MHA ? 3 : kAttnCtasPerSm;
@@ -78,7 +78,7 @@ struct AttnCfg {
       Q4 ? (kPagesPerStage * kQ4PageBytes + 127) / 128 * 128 : 2 * kPageBytes;
   // 4-bit pages are a quarter the size: more of them in flight.
   static constexpr int kStages =
-      Q4 ? (MHA ? (D == 128 ? 24 : 32) : (D == 128 ? 32 : 48)) / kPagesPerStage : attn_stages(D);
+      Q4 ? (MHA ? (D == 128 ? 24 : 48) : (D == 128 ? 32 : 48)) / kPagesPerStage : attn_stages(D);
   static constexpr int kSub = kStages / kConsumerWarps;             // stages per consumer warp
   static constexpr int kBarOffset = (kStages * kStageBytes + 15) / 16 * 16;
   static constexpr int kStageMetaOffset = kBarOffset + (2 * kStages + 4) * 8;
@@ -524,8 +524,7 @@ __global__ void __launch_bounds__(kAttnThreads, MHA ? 3 : (D == 64 ? kAttnCtasPe
   static_assert(!Q4 || F16, "a 4-bit cache is dequantised to fp16");
   static_assert(!MHA || Q4, "the single-head layout is the 4-bit path's");
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t full0 = sbase + C::kBarOffset;
   const uint32_t empty0 = full0 + 8 * C::kStages;

@@ -1055,8 +1055,7 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
                        const __grid_constant__ CUtensorMap mmn) {
   using C = UnitCfg<D>;
   extern __shared__ uint8_t usm_raw[];
-  uint8_t* usm = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(usm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* usm = usm_raw + ((1024u - (smem_u32(usm_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(usm);
   const uint32_t full0 = sbase + C::kBarOffset, empty0 = full0 + 8 * C::kStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(usm + C::kBarOffset + 16 * C::kStages);
