@@ -89,18 +89,62 @@ __global__ void __launch_bounds__(kMetaThreads, Q4 ? 4 : 2) meta_kernel(const Me
                           static_cast<int64_t>(t0) * ng + grp;
       const __half* gmx = static_cast<const __half*>(a.gmax) + b * a.gsb + h * a.gsh +
                           static_cast<int64_t>(t0) * ng + grp;
-#pragma unroll 4
-      for (int t = 0; t < nt; ++t) {
-        const uint32_t c4 = __ldcs(reinterpret_cast<const uint32_t*>(src + static_cast<int64_t>(t) * (a.d / 2)));
-        const __half mn = gmn[static_cast<int64_t>(t) * ng];
-        const __half mx = gmx[static_cast<int64_t>(t) * ng];
-        uint32_t w[4];
-        q4_dequant8(c4, mn, mx, w);
+      // The 8 lanes of one (page, group) -- aligned lanes, v % 8 == lane % 8 --
+      // share the group steps: per chunk of 8 tokens, lane u computes token
+      // u's step and the others take it by shuffle.  A chunk with a tiny
+      // group takes the per-token path.
+      const int sub = threadIdx.x & 7;
+      const unsigned gmask = 0xffu << (threadIdx.x & 24);
+      const __half2 k1024 = __half2half2(__ushort_as_half(0x6400));
+#pragma unroll 1
+      for (int c0 = 0; c0 < nt; c0 += 8) {
+        uint32_t own = 0;  // (mn, step) of token c0 + sub, as a half pair
+        bool tiny = false;
+        if (c0 + sub < nt) {
+          const __half mn = gmn[static_cast<int64_t>(c0 + sub) * ng];
+          const __half mx = gmx[static_cast<int64_t>(c0 + sub) * ng];
+          const float range = q4_range(mn, mx);
+          tiny = range < kQ4TinyRange;
+          own = static_cast<uint32_t>(__half_as_ushort(mn)) |
+                (static_cast<uint32_t>(__half_as_ushort(q4_step16(fmaxf(range, kQ4TinyRange))))
+                 << 16);
+        }
+        if (!__any_sync(gmask, tiny)) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t k = to_key2(w[u]);
-          kmin[u] = __vminu2(kmin[u], k);
-          kmax[u] = __vmaxu2(kmax[u], k);
+          for (int u = 0; u < 8; ++u) {
+            if (c0 + u < nt) {  // the same for the group's 8 lanes
+              const uint32_t ms = __shfl_sync(gmask, own, u, 8);
+              const uint32_t c4 = __ldcs(reinterpret_cast<const uint32_t*>(
+                  src + static_cast<int64_t>(c0 + u) * (a.d / 2)));
+              const __half2 mn2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(ms)));
+              const __half2 st2 =
+                  __half2half2(__ushort_as_half(static_cast<unsigned short>(ms >> 16)));
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const uint32_t byte = (c4 >> (8 * i)) & 0xffu;
+                const uint32_t bits = (byte & 0x0fu) | ((byte & 0xf0u) << 12) | 0x64006400u;
+                const __half2 x = __hfma2(__hsub2(*reinterpret_cast<const __half2*>(&bits), k1024),
+                                          st2, mn2);
+                const uint32_t k = to_key2(*reinterpret_cast<const uint32_t*>(&x));
+                kmin[i] = __vminu2(kmin[i], k);
+                kmax[i] = __vmaxu2(kmax[i], k);
+              }
+            }
+          }
+        } else {
+          for (int t = c0; t < min(nt, c0 + 8); ++t) {
+            const uint32_t c4 = __ldcs(
+                reinterpret_cast<const uint32_t*>(src + static_cast<int64_t>(t) * (a.d / 2)));
+            uint32_t w[4];
+            q4_dequant8(c4, gmn[static_cast<int64_t>(t) * ng], gmx[static_cast<int64_t>(t) * ng],
+                        w);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const uint32_t k = to_key2(w[u]);
+              kmin[u] = __vminu2(kmin[u], k);
+              kmax[u] = __vmaxu2(kmax[u], k);
+            }
+          }
         }
       }
     }
