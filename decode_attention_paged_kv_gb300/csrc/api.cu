@@ -23,7 +23,7 @@ static_assert(DKV_WORKSPACE_HEADER_BYTES == kAlign, "status word and counters");
 // Shared memory the per-unit selection kernel may take (one CTA per SM), and
 // the shortest context (pages) it is used for.
 constexpr size_t kUnitSelectSmemLimit = 227 * 1024;
-constexpr int kUnitSelectMinP = 1024;
+constexpr int kUnitSelectMinP = 256;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -562,6 +562,7 @@ static dkv_status select_impl(const dkv_params* p, const void* q, const dkv_kv* 
     ua.S = p->page_size;
     ua.status = a.status;
     ua.wait_limit_ns = a.wait_limit_ns;
+    ua.num_sms = current_sm_count();
     // the attention takes each unit's items once its union is written
     ua.unit_ready = reinterpret_cast<uint32_t*>(ws + L.unit_ready);
     a.unit_ready = ua.unit_ready;

@@ -199,7 +199,8 @@ struct UnionArgs {
   int S;                       // tokens per selection page (16, 32 or 64)
 };
 
-// One CTA per (batch, kv head): bound scores, per-head top-K and union.
+// Per (batch, kv head) unit: bound scores, per-head top-K and union; a
+// persistent grid of at most num_sms CTAs takes the units in turn.
 struct UnitSelectArgs {
   const void* q;
   int64_t q_sb, q_sh;
@@ -218,6 +219,7 @@ struct UnitSelectArgs {
                                // list holds 16-token cache pages
   uint32_t* status;
   uint64_t wait_limit_ns;
+  int num_sms;                 // multiprocessors of the device (grid bound)
 };
 
 // Attention over each (b, q-head)'s top-K tokens (token-level sparse attention).

@@ -1008,9 +1008,9 @@ __global__ void __launch_bounds__(kSelMaxThreads) union_kernel(const UnionArgs a
               sc);
 }
 
-// ------------------------------------------------------- one CTA per unit
-// unit_select_kernel: the bound scores, per-head top-K and union of one
-// (batch, kv head) in one CTA.  Warp 8 streams the unit's metadata with TMA
+// ------------------------------------------------------- units of a CTA
+// unit_select_kernel: the bound scores, per-head top-K and union of each
+// (batch, kv head) unit, one unit at a time per CTA of a persistent grid.  Warp 8 streams the unit's metadata with TMA
 // tensor copies, 64 pages of [M] and [m] per stage (128-byte swizzle); a stage
 // goes to consumer warps 0-3 or 4-7 (alternately), each of which scores one
 // 16-page tile of it on tensor cores: S[head][page] = q+ . M + q- . m, as in
@@ -1065,12 +1065,14 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
   // group score's (one selection per group)
   uint32_t* s_kext = s_bm + static_cast<size_t>(a.G) * kSelBitmapWords;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int unit = blockIdx.x;
-  const int b = unit / a.Hkv, kvh = unit % a.Hkv;
-  // selection pages of this sequence (all P without per-sequence lengths)
-  const int Nb = seq_len_of(a.lens, b, a.N);
-  const int Pb = static_cast<int>(ceil_div(Nb, a.S));
-  const int n_boxes = static_cast<int>(ceil_div(Pb, kUnitBoxPages));
+  const int n_units = a.B * a.Hkv;
+  // This CTA's units: blockIdx.x, blockIdx.x + gridDim.x, ...  The producer
+  // warp streams their metadata back to back (box gi of the CTA, counted over
+  // all its units, goes to stage gi % kStages), so the next unit's boxes are
+  // in flight while the consumers select and build the current one's union.
+  auto unit_pages = [&](int u) {  // selection pages of unit u's sequence
+    return static_cast<int>(ceil_div(seq_len_of(a.lens, u / a.Hkv, a.N), a.S));
+  };
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(full0 + 8 * s, 1);
@@ -1079,17 +1081,16 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (threadIdx.x < 18) s_kext[threadIdx.x] = (threadIdx.x < 8 || threadIdx.x == 16) ? 0u : ~0u;
   if (warp == kUnitConsumers && lane == 0) {
     prefetch_tensormap(&mmx);
     prefetch_tensormap(&mmn);
   }
   griddep_wait();
   // The attention grid may start as soon as every CTA here has passed this
-  // point, and then reads this unit's ready flag: clear it first (the
-  // previous call's attention has finished with it once the wait returns).
+  // point, and then reads the units' ready flags: clear this CTA's first (the
+  // previous call's attention has finished with them once the wait returns).
   if (threadIdx.x == 0 && a.unit_ready != nullptr) {
-    a.unit_ready[unit] = 0u;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) a.unit_ready[u] = 0u;
     __threadfence();
   }
   __syncthreads();
@@ -1099,29 +1100,34 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
-      int issued = 0;
-      for (int i = 0; i < n_boxes; ++i) {
-        const int s = i % C::kStages;
-        if (i >= C::kStages &&
-            !mbar_wait_bounded(empty0 + 8 * s, ((i / C::kStages) - 1) & 1, a.wait_limit_ns,
-                               abort_flag)) {
-          if (*abort_flag == 0) {
-            set_status(a.status, kStatusTimeout);
-            *abort_flag = 1;
+      int gi = 0;  // boxes issued by this CTA
+      bool failed = false;
+      for (int u = blockIdx.x; u < n_units && !failed; u += gridDim.x) {
+        const int ub = u / a.Hkv, ukvh = u % a.Hkv;
+        const int nb = static_cast<int>(ceil_div(unit_pages(u), kUnitBoxPages));
+        for (int i = 0; i < nb; ++i, ++gi) {
+          const int s = gi % C::kStages;
+          if (gi >= C::kStages &&
+              !mbar_wait_bounded(empty0 + 8 * s, ((gi / C::kStages) - 1) & 1, a.wait_limit_ns,
+                                 abort_flag)) {
+            if (*abort_flag == 0) {
+              set_status(a.status, kStatusTimeout);
+              *abort_flag = 1;
+            }
+            failed = true;
+            break;
           }
-          break;
+          const uint32_t dst = sbase + s * C::kStageBytes;
+          mbar_arrive_expect_tx(full0 + 8 * s, C::kStageBytes);
+          tma_load_5d_hint(dst, &mmx, full0 + 8 * s, 0, i * kUnitBoxPages, 0, ukvh, ub, pol);
+          tma_load_5d_hint(dst + C::kBoxBytes, &mmn, full0 + 8 * s, 0, i * kUnitBoxPages, 0,
+                           ukvh, ub, pol);
         }
-        const uint32_t dst = sbase + s * C::kStageBytes;
-        mbar_arrive_expect_tx(full0 + 8 * s, C::kStageBytes);
-        tma_load_5d_hint(dst, &mmx, full0 + 8 * s, 0, i * kUnitBoxPages, 0, kvh, b, pol);
-        tma_load_5d_hint(dst + C::kBoxBytes, &mmn, full0 + 8 * s, 0, i * kUnitBoxPages, 0, kvh, b,
-                         pol);
-        issued = i + 1;
       }
       // The last copies issued have landed before this warp leaves (so no copy
       // is still writing when the consumers stop early); each wait is bounded.
       const uint64_t deadline = globaltimer_ns() + 200000000ull;
-      for (int j = max(0, issued - C::kStages); j < issued; ++j) {
+      for (int j = max(0, gi - C::kStages); j < gi; ++j) {
         const uint64_t now = globaltimer_ns();
         if (now >= deadline) break;
         mbar_wait_bounded(full0 + 8 * (j % C::kStages), (j / C::kStages) & 1, deadline - now,
@@ -1131,10 +1137,20 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
     return;
   }
 
-  // -------------------------------------------------------------- scoring
   const int g = lane >> 2, t4 = lane & 3;
   const bool head_ok = g < a.G;
   const int mtx = lane >> 3, mrow = lane & 7;
+  const int half = warp >> 2, tile = warp & 3;  // boxes of parity `half`, tile `tile` of each
+  int gbase = 0;  // boxes of this CTA's earlier units
+  for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
+  const int b = unit / a.Hkv, kvh = unit % a.Hkv;
+  const int Nb = seq_len_of(a.lens, b, a.N);
+  const int Pb = unit_pages(unit);
+  const int n_boxes = static_cast<int>(ceil_div(Pb, kUnitBoxPages));
+  if (threadIdx.x < 18) s_kext[threadIdx.x] = (threadIdx.x < 8 || threadIdx.x == 16) ? 0u : ~0u;
+  unit_consumers_sync();
+
+  // -------------------------------------------------------------- scoring
   uint32_t qp[D / 16][2], qm[D / 16][2];  // A fragments of q+ and q- (rows = heads)
   {
     const uint16_t* qrow = static_cast<const uint16_t*>(a.q) + b * a.q_sb +
@@ -1151,12 +1167,12 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
       qm[ks][1] = keep_sign(w1, true);
     }
   }
-  const int half = warp >> 2, tile = warp & 3;  // boxes of parity `half`, tile `tile` of each
   bool ok = true;
   uint32_t kmx = 0u, kmn = ~0u;  // extremes of head g's keys this lane wrote
   for (int i = half; i < n_boxes; i += 2) {
-    const int s = i % C::kStages;
-    ok = mbar_wait_bounded(full0 + 8 * s, (i / C::kStages) & 1, a.wait_limit_ns, abort_flag);
+    const int gi = gbase + i;
+    const int s = gi % C::kStages;
+    ok = mbar_wait_bounded(full0 + 8 * s, (gi / C::kStages) & 1, a.wait_limit_ns, abort_flag);
     if (!__all_sync(0xffffffffu, ok)) {
       ok = false;
       break;
@@ -1189,6 +1205,7 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
       }
     }
   }
+  gbase += n_boxes;
   // each head's largest and smallest key, for the selection's common prefix
   kmx = max(kmx, __shfl_xor_sync(0xffffffffu, kmx, 1));
   kmx = max(kmx, __shfl_xor_sync(0xffffffffu, kmx, 2));
@@ -1206,10 +1223,13 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
   unit_consumers_sync();
   if (*abort_flag) {
     if (threadIdx.x == 0) {
-      a.union_count[unit] = 0;  // gather nothing for this unit
-      if (a.unit_ready != nullptr) {
-        __threadfence();
-        st_release_gpu(a.unit_ready + unit, 1u);
+      // gather nothing for this unit or this CTA's later ones
+      for (int u = unit; u < n_units; u += gridDim.x) {
+        a.union_count[u] = 0;
+        if (a.unit_ready != nullptr) {
+          __threadfence();
+          st_release_gpu(a.unit_ready + u, 1u);
+        }
       }
     }
     return;
@@ -1255,13 +1275,11 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
                     nullptr);
       for (int i = kkb + lane; i < a.kk; i += 32) a.selected[row * a.kk + i] = -1;
     }
-    return;
-  }
+  } else {
   // Union of the heads' bitmaps, ascending, with a bit per head: warp w ORs
   // words w * wpw .. (one per lane), the per-warp counts place them.  Each
   // selection page becomes its S / 16 cache pages (fewer for the sequence's
   // last).
-  {
     const int wpw = static_cast<int>(ceil_div(W, kUnionWarps));
     const int wi = warp * wpw + lane;
     const bool own = lane < wpw && wi < W;
@@ -1331,6 +1349,8 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
       a.union_count[unit] = count;
     }
   }
+  unit_consumers_sync();  // keys, bitmaps and extremes are free for the next unit
+  }
 }
 
 }  // namespace
@@ -1396,7 +1416,12 @@ size_t unit_select_smem(int d, int G, int P) {
 cudaError_t launch_unit_select(int d, bool f16, const UnitSelectArgs& a, const CUtensorMap& mmx,
                                const CUtensorMap& mmn, cudaStream_t s) {
   const size_t smem = unit_select_smem(d, a.G, a.P);
-  const dim3 grid(a.B * a.Hkv), block(kUnitThreads);
+  // One CTA per SM at most (a CTA takes most of an SM's shared memory), each
+  // taking units blockIdx.x, + gridDim.x, ...: with fewer CTAs the metadata
+  // scan streams from too few SMs (measured: 64, 80, 96, 112 CTAs for 128
+  // units were slower than 128).
+  const int units = a.B * a.Hkv;
+  const dim3 grid(units < a.num_sms ? units : a.num_sms), block(kUnitThreads);
   auto kern = d == 128 ? (f16 ? unit_select_kernel<128, true> : unit_select_kernel<128, false>)
                        : (f16 ? unit_select_kernel<64, true> : unit_select_kernel<64, false>);
   cudaError_t e =
