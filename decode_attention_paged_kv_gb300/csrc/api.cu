@@ -247,6 +247,27 @@ bool encode_meta_map(CUtensorMap* map, const dkv_params* p, const void* meta, bo
   return r == CUDA_SUCCESS;
 }
 
+// Map over 8-bit metadata codes [B, Hkv, P, d] (u8) for the per-unit selection
+// kernel: {d bytes, P pages, 1, Hkv, B}, box {d, box_pages, 1, 1, 1}, with a
+// d-byte swizzle (128 or 64 bytes).
+bool encode_code_map(CUtensorMap* map, const dkv_params* p, const void* codes, int box_pages) {
+  if (!get_encode()) return false;
+  const uint64_t d = static_cast<uint64_t>(p->head_dim);
+  const uint64_t P = static_cast<uint64_t>(ceil_div(p->seq_len, p->page_size));
+  const cuuint64_t dims[5] = {d, P, 1, static_cast<cuuint64_t>(p->num_kv_heads),
+                              static_cast<cuuint64_t>(p->batch)};
+  const cuuint64_t st[4] = {d, P * d, P * d, P * d * static_cast<cuuint64_t>(p->num_kv_heads)};
+  const cuuint32_t box[5] = {static_cast<cuuint32_t>(d), static_cast<cuuint32_t>(box_pages), 1, 1,
+                             1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(codes),
+                              dims, st, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int out_code(int32_t out_dtype) {
   return out_dtype == DKV_FP32 ? 2 : (out_dtype == DKV_FP16 ? 1 : 0);
 }
@@ -533,19 +554,25 @@ static dkv_status select_impl(const dkv_params* p, const void* q, const dkv_kv* 
   a.union_count = ucount;
   a.union_stride = L.union_stride;
 
-  if (m8 == nullptr && p->page_size >= dkv::kPage && P >= kUnitSelectMinP &&
-      P <= dkv::kUnitMaxP &&
-      dkv::unit_select_smem(p->head_dim, G, P) <= static_cast<size_t>(kUnitSelectSmemLimit)) {
-    // Long contexts: one CTA per (batch, kv head) scores its pages, selects
-    // each head's top-K and builds the union list.  (Shorter ones have too
-    // little metadata per CTA to hide the selection's latency; the three
-    // kernels below spread the same work wider.)
+  if (p->page_size >= dkv::kPage && P >= kUnitSelectMinP && P <= dkv::kUnitMaxP &&
+      dkv::unit_select_smem(p->head_dim, m8 != nullptr, G, P) <=
+          static_cast<size_t>(kUnitSelectSmemLimit)) {
+    // Contexts of 256 pages and more: a persistent grid of selection CTAs
+    // takes the (batch, kv head) units in turn; each unit's metadata (16-bit,
+    // or 8-bit codes) is scored, each head's top-K selected and the union
+    // list built in one CTA.  (Shorter contexts have too little metadata per
+    // CTA to hide the selection's latency; the three kernels below spread the
+    // same work wider.)
     dkv::UnitSelectArgs ua{};
     ua.q = q;
     ua.q_sb = p->q_stride_b;
     ua.q_sh = p->q_stride_h;
     ua.meta_min = meta_min;
     ua.meta_max = meta_max;
+    if (m8 != nullptr) {
+      ua.lo = m8->lo;
+      ua.step = m8->step;
+    }
     ua.B = p->batch;
     ua.Hq = p->num_q_heads;
     ua.Hkv = p->num_kv_heads;
@@ -567,9 +594,13 @@ static dkv_status select_impl(const dkv_params* p, const void* q, const dkv_kv* 
     ua.unit_ready = reinterpret_cast<uint32_t*>(ws + L.unit_ready);
     a.unit_ready = ua.unit_ready;
     CUtensorMap mmx, mmn;
-    if (!encode_meta_map(&mmx, p, meta_max, f16, 64) || !encode_meta_map(&mmn, p, meta_min, f16, 64))
-      return DKV_ERR_CUDA;
-    if ((st = cuda_status(dkv::launch_unit_select(p->head_dim, f16, ua, mmx, mmn, s))) != DKV_OK)
+    const bool maps_ok =
+        m8 != nullptr
+            ? encode_code_map(&mmx, p, m8->code_max, 64) && encode_code_map(&mmn, p, m8->code_min, 64)
+            : encode_meta_map(&mmx, p, meta_max, f16, 64) && encode_meta_map(&mmn, p, meta_min, f16, 64);
+    if (!maps_ok) return DKV_ERR_CUDA;
+    if ((st = cuda_status(dkv::launch_unit_select(p->head_dim, f16, m8 != nullptr, ua, mmx, mmn,
+                                                  s))) != DKV_OK)
       return st;
     return run_attention(p, a, true, f16, mk, mv, out, out_dtype, s);
   }

@@ -206,6 +206,10 @@ struct UnitSelectArgs {
   int64_t q_sb, q_sh;
   const void* meta_min;        // [B, Hkv, P, d]
   const void* meta_max;
+  // 8-bit metadata (the M8 kernel; the codes come through the tensor maps):
+  // r = lo * sum_i q_i + step * (q+ . code_max + q- . code_min), lo / step [B, Hkv, P]
+  const float* lo;
+  const float* step;
   int B, Hq, Hkv, G, P, kk;
   int32_t* selected;           // [B, Hq, kk]
   int2* union_list;            // [B * Hkv, union_stride]
@@ -284,10 +288,11 @@ cudaError_t launch_meta8(bool f16, const Meta8Args& a, cudaStream_t s);
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
 cudaError_t launch_union(const UnionArgs& a, int units, cudaStream_t s);
 // Shared memory of unit_select_kernel for G heads of P pages (P <= kUnitMaxP).
-size_t unit_select_smem(int d, int G, int P);
-// mmx / mmn: maps over meta_max / meta_min, box {64, 64 pages, d/64, 1, 1}.
-cudaError_t launch_unit_select(int d, bool f16, const UnitSelectArgs& a, const CUtensorMap& mmx,
-                               const CUtensorMap& mmn, cudaStream_t s);
+size_t unit_select_smem(int d, bool m8, int G, int P);
+// mmx / mmn: maps over meta_max / meta_min, box {64, 64 pages, d/64, 1, 1}; with
+// m8, over code_max / code_min, box {d bytes, 64 pages, 1, 1, 1}.
+cudaError_t launch_unit_select(int d, bool f16, bool m8, const UnitSelectArgs& a,
+                               const CUtensorMap& mmx, const CUtensorMap& mmn, cudaStream_t s);
 
 cudaError_t launch_meta(bool q4, bool f16, const MetaArgs& a, cudaStream_t s);
 cudaError_t launch_quant4(int64_t rows, int d, const void* x, void* codes, void* gmin,

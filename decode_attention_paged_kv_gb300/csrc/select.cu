@@ -780,6 +780,16 @@ constexpr int kScore8Warps = 4;
 constexpr int kScore8TilesPerWarp = 4;
 constexpr int kScore8PagesPerCta = 8 * kScore8TilesPerWarp * kScore8Warps;
 
+// Two code bytes (bytes `first`, first + 1 of w) as an exact fp16 pair: each
+// byte under the high byte 0x64 of 1024 (one byte permute) is 1024 + c;
+// subtracting 1024 leaves c.
+__device__ __forceinline__ uint32_t codes_h2(uint32_t w, int first) {
+  const uint32_t bits = __byte_perm(w, 0x64646464u, first == 0 ? 0x4140u : 0x4342u);
+  const __half2 c = __hsub2(*reinterpret_cast<const __half2*>(&bits),
+                            __half2half2(__ushort_as_half(0x6400)));
+  return *reinterpret_cast<const uint32_t*>(&c);
+}
+
 template <bool F16>
 __device__ __forceinline__ uint32_t codes_pair(uint32_t w, int first) {
   // two code bytes as exact 16-bit floats: each byte placed under the exponent
@@ -1022,9 +1032,10 @@ constexpr int kUnitConsumers = 8;
 constexpr int kUnitThreads = (kUnitConsumers + 1) * 32;
 constexpr int kUnitBoxPages = 64;
 
-template <int D>
+template <int D, bool M8 = false>
 struct UnitCfg {
-  static constexpr int kBoxBytes = kUnitBoxPages * D * 2;  // one of [M] / [m]
+  // one of [M] / [m] (16-bit), or of the code bytes [cM] / [cm] (8-bit)
+  static constexpr int kBoxBytes = kUnitBoxPages * D * (M8 ? 1 : 2);
   static constexpr int kStageBytes = 2 * kBoxBytes;
   static constexpr int kStages = (128 * 1024) / kStageBytes;  // 128 KiB in flight
   static constexpr int kBarOffset = kStages * kStageBytes;
@@ -1039,6 +1050,16 @@ __device__ __forceinline__ uint32_t box_addr(uint32_t base, int t, int c) {
   return base + static_cast<uint32_t>(row * 128 + chunk * 16);
 }
 
+// Shared address of the 16 code bytes (channels) [16 c, 16 c + 16) of page row
+// t of an 8-bit box {D bytes, 64 pages} written with D-byte swizzle (D = 128:
+// 128-byte swizzle, the chunk XORed with t % 8; D = 64: 64-byte swizzle, the
+// chunk XORed with (t / 2) % 4).
+template <int D>
+__device__ __forceinline__ uint32_t box8_addr(uint32_t base, int t, int c) {
+  const int chunk = D == 128 ? (c ^ (t & 7)) : (c ^ ((t >> 1) & 3));
+  return base + static_cast<uint32_t>(t * D + chunk * 16);
+}
+
 __device__ __forceinline__ void unit_consumers_sync() {
   asm volatile("bar.sync 1, %0;" ::"r"(kUnitConsumers * 32) : "memory");
 }
@@ -1049,11 +1070,13 @@ __device__ __forceinline__ void union_sync() {
   asm volatile("bar.sync 2, %0;" ::"r"(kUnionWarps * 32) : "memory");
 }
 
-template <int D, bool F16>
+// M8: the scores come from 8-bit metadata (codes in the boxes, lo / step per
+// page from global memory).
+template <int D, bool F16, bool M8>
 __global__ void __launch_bounds__(kUnitThreads, 1)
     unit_select_kernel(const UnitSelectArgs a, const __grid_constant__ CUtensorMap mmx,
                        const __grid_constant__ CUtensorMap mmn) {
-  using C = UnitCfg<D>;
+  using C = UnitCfg<D, M8>;
   extern __shared__ uint8_t usm_raw[];
   uint8_t* usm = usm_raw + ((1024u - (smem_u32(usm_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(usm);
@@ -1152,7 +1175,61 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
 
   // -------------------------------------------------------------- scoring
   uint32_t qp[D / 16][2], qm[D / 16][2];  // A fragments of q+ and q- (rows = heads)
-  {
+  float qsum = 0.f;  // 8-bit metadata: sum_i q_i of head g
+  float qscale = 1.f;  // 8-bit metadata: the scores' factor 2^k (q was scaled by 2^-k)
+  if constexpr (M8) {
+    // 8-bit metadata: fp16 MMAs.  The codes widen to fp16 exactly (1024 + c,
+    // minus 1024); q is scaled by 2^-k per head, k such that its largest
+    // component lands in [2^14, 2^15), which fp16 holds exactly for every
+    // bf16 component within 2^31 of that largest one (the rest, below 2^-17
+    // after scaling, round to the fp16 grid of 2^-24).  Channels of k-step
+    // ks: 16 ks + 4 t4 + 0..3, the bytes an ldmatrix row fragment of the code
+    // box gives the lane.
+    const uint16_t* qrow = static_cast<const uint16_t*>(a.q) + b * a.q_sb +
+                           static_cast<int64_t>(kvh * a.G + (head_ok ? g : 0)) * a.q_sh;
+    float qmax = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const uint2 w = head_ok ? *reinterpret_cast<const uint2*>(qrow + 16 * ks + 4 * t4)
+                              : make_uint2(0u, 0u);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t h = (((e < 2) ? w.x : w.y) >> (16 * (e & 1))) & 0xffffu;
+        const float x = F16 ? __half2float(__ushort_as_half(static_cast<unsigned short>(h)))
+                            : __uint_as_float(h << 16);
+        qsum += x;
+        qmax = fmaxf(qmax, fabsf(x));
+      }
+    }
+    qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+    qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
+    qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 1));
+    qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 2));
+    const int k = (F16 || qmax == 0.f) ? 0 : ((__float_as_int(qmax) >> 23) & 0xff) - 127 - 14;
+    const float down = __int_as_float((127 - k) << 23);  // 2^-k
+    qscale = __int_as_float((127 + k) << 23);            // 2^k
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const uint2 w = head_ok ? *reinterpret_cast<const uint2*>(qrow + 16 * ks + 4 * t4)
+                              : make_uint2(0u, 0u);
+      uint32_t h2[2];
+#pragma unroll
+      for (int v = 0; v < 2; ++v) {
+        const uint32_t ww = v ? w.y : w.x;
+        if constexpr (F16) {
+          h2[v] = ww;
+        } else {
+          const __half2 hh = __floats2half2_rn(__uint_as_float(ww << 16) * down,
+                                               __uint_as_float(ww & 0xffff0000u) * down);
+          h2[v] = *reinterpret_cast<const uint32_t*>(&hh);
+        }
+      }
+      qp[ks][0] = keep_sign(h2[0], false);
+      qm[ks][0] = keep_sign(h2[0], true);
+      qp[ks][1] = keep_sign(h2[1], false);
+      qm[ks][1] = keep_sign(h2[1], true);
+    }
+  } else {
     const uint16_t* qrow = static_cast<const uint16_t*>(a.q) + b * a.q_sb +
                            static_cast<int64_t>(kvh * a.G + (head_ok ? g : 0)) * a.q_sh;
 #pragma unroll
@@ -1169,7 +1246,32 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
   }
   bool ok = true;
   uint32_t kmx = 0u, kmn = ~0u;  // extremes of head g's keys this lane wrote
+  // 8-bit metadata: lo and step of the lane's four pages of a box, loaded one
+  // of this warp's boxes ahead (box i + 2), so their latency hides behind the
+  // box wait instead of following each tile's MMAs.
+  float lo_n[4] = {0.f, 0.f, 0.f, 0.f}, st_n[4] = {0.f, 0.f, 0.f, 0.f};
+  auto load_lo_step = [&](int box) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int p = box * kUnitBoxPages + 16 * tile + 8 * (e >> 1) + 2 * t4 + (e & 1);
+      const int64_t pi = static_cast<int64_t>(unit) * a.P + p;
+      lo_n[e] = (head_ok && p < Pb) ? __ldg(a.lo + pi) : 0.f;
+      st_n[e] = (head_ok && p < Pb) ? __ldg(a.step + pi) : 0.f;
+    }
+  };
+  if constexpr (M8) {
+    if (half < n_boxes) load_lo_step(half);
+  }
   for (int i = half; i < n_boxes; i += 2) {
+    float lo_c[4], st_c[4];
+    if constexpr (M8) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        lo_c[e] = lo_n[e];
+        st_c[e] = st_n[e];
+      }
+      if (i + 2 < n_boxes) load_lo_step(i + 2);
+    }
     const int gi = gbase + i;
     const int s = gi % C::kStages;
     ok = mbar_wait_bounded(full0 + 8 * s, (gi / C::kStages) & 1, a.wait_limit_ns, abort_flag);
@@ -1179,16 +1281,41 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
     }
     const uint32_t mb = sbase + s * C::kStageBytes, nb = mb + C::kBoxBytes;
     float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    if constexpr (M8) {
+      // Matrices of one ldmatrix.x4: pages 16 tile + 0..7 / + 8..15 (n tiles
+      // 0 / 1) of code chunks ks and ks + 1; lane (g, t4) gets the four code
+      // bytes 4 t4 .. 4 t4 + 3 of its page g of each.
+      const int row = 16 * tile + 8 * ((lane >> 3) & 1) + (lane & 7);
 #pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      uint32_t r0, r1, r2, r3;
-      const int row = 16 * tile + 8 * (mtx >> 1) + mrow, ch = 16 * ks + 8 * (mtx & 1);
-      ldsm_x4(box_addr(mb, row, ch), r0, r1, r2, r3);
-      mma16816<F16>(sc[0], qp[ks][0], 0u, qp[ks][1], 0u, r0, r1);
-      mma16816<F16>(sc[1], qp[ks][0], 0u, qp[ks][1], 0u, r2, r3);
-      ldsm_x4(box_addr(nb, row, ch), r0, r1, r2, r3);
-      mma16816<F16>(sc[0], qm[ks][0], 0u, qm[ks][1], 0u, r0, r1);
-      mma16816<F16>(sc[1], qm[ks][0], 0u, qm[ks][1], 0u, r2, r3);
+      for (int ks = 0; ks < D / 16; ks += 2) {
+        uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
+        ldsm_x4(box8_addr<D>(mb, row, ks + (lane >> 4)), x0, x1, x2, x3);
+        ldsm_x4(box8_addr<D>(nb, row, ks + (lane >> 4)), y0, y1, y2, y3);
+        mma16816<true>(sc[0], qp[ks][0], 0u, qp[ks][1], 0u, codes_h2(x0, 0), codes_h2(x0, 2));
+        mma16816<true>(sc[1], qp[ks][0], 0u, qp[ks][1], 0u, codes_h2(x1, 0), codes_h2(x1, 2));
+        mma16816<true>(sc[0], qm[ks][0], 0u, qm[ks][1], 0u, codes_h2(y0, 0), codes_h2(y0, 2));
+        mma16816<true>(sc[1], qm[ks][0], 0u, qm[ks][1], 0u, codes_h2(y1, 0), codes_h2(y1, 2));
+        mma16816<true>(sc[0], qp[ks + 1][0], 0u, qp[ks + 1][1], 0u, codes_h2(x2, 0),
+                       codes_h2(x2, 2));
+        mma16816<true>(sc[1], qp[ks + 1][0], 0u, qp[ks + 1][1], 0u, codes_h2(x3, 0),
+                       codes_h2(x3, 2));
+        mma16816<true>(sc[0], qm[ks + 1][0], 0u, qm[ks + 1][1], 0u, codes_h2(y2, 0),
+                       codes_h2(y2, 2));
+        mma16816<true>(sc[1], qm[ks + 1][0], 0u, qm[ks + 1][1], 0u, codes_h2(y3, 0),
+                       codes_h2(y3, 2));
+      }
+    } else {
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t r0, r1, r2, r3;
+        const int row = 16 * tile + 8 * (mtx >> 1) + mrow, ch = 16 * ks + 8 * (mtx & 1);
+        ldsm_x4(box_addr(mb, row, ch), r0, r1, r2, r3);
+        mma16816<F16>(sc[0], qp[ks][0], 0u, qp[ks][1], 0u, r0, r1);
+        mma16816<F16>(sc[1], qp[ks][0], 0u, qp[ks][1], 0u, r2, r3);
+        ldsm_x4(box_addr(nb, row, ch), r0, r1, r2, r3);
+        mma16816<F16>(sc[0], qm[ks][0], 0u, qm[ks][1], 0u, r0, r1);
+        mma16816<F16>(sc[1], qm[ks][0], 0u, qm[ks][1], 0u, r2, r3);
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * s);
@@ -1197,7 +1324,9 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
       for (int e = 0; e < 4; ++e) {
         const int p = i * kUnitBoxPages + 16 * tile + 8 * (e >> 1) + 2 * t4 + (e & 1);
         if (p < Pb) {
-          const uint32_t key = score_key(sc[e >> 1][e & 1]);
+          float sv = sc[e >> 1][e & 1];
+          if constexpr (M8) sv = __fmaf_rn(st_c[e], sv * qscale, lo_c[e] * qsum);
+          const uint32_t key = score_key(sv);
           s_keys[g * a.P + p] = key;
           kmx = max(kmx, key);
           kmn = min(kmn, key);
@@ -1407,23 +1536,30 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
   return launch_pdl(topk_kernel<false>, dim3(a.rows), dim3(kSelMaxThreads), 0, s, a);
 }
 
-size_t unit_select_smem(int d, int G, int P) {
-  const size_t keys_off = d == 128 ? UnitCfg<128>::kKeysOffset : UnitCfg<64>::kKeysOffset;
+size_t unit_select_smem(int d, bool m8, int G, int P) {
+  const size_t keys_off =
+      d == 128 ? (m8 ? UnitCfg<128, true>::kKeysOffset : UnitCfg<128>::kKeysOffset)
+               : (m8 ? UnitCfg<64, true>::kKeysOffset : UnitCfg<64>::kKeysOffset);
   return 1024 + keys_off + static_cast<size_t>(G) * P * 4 +
          static_cast<size_t>(G) * kSelBitmapWords * 4 + 32 * 4;
 }
 
-cudaError_t launch_unit_select(int d, bool f16, const UnitSelectArgs& a, const CUtensorMap& mmx,
-                               const CUtensorMap& mmn, cudaStream_t s) {
-  const size_t smem = unit_select_smem(d, a.G, a.P);
+cudaError_t launch_unit_select(int d, bool f16, bool m8, const UnitSelectArgs& a,
+                               const CUtensorMap& mmx, const CUtensorMap& mmn, cudaStream_t s) {
+  const size_t smem = unit_select_smem(d, m8, a.G, a.P);
   // One CTA per SM at most (a CTA takes most of an SM's shared memory), each
   // taking units blockIdx.x, + gridDim.x, ...: with fewer CTAs the metadata
   // scan streams from too few SMs (measured: 64, 80, 96, 112 CTAs for 128
   // units were slower than 128).
   const int units = a.B * a.Hkv;
   const dim3 grid(units < a.num_sms ? units : a.num_sms), block(kUnitThreads);
-  auto kern = d == 128 ? (f16 ? unit_select_kernel<128, true> : unit_select_kernel<128, false>)
-                       : (f16 ? unit_select_kernel<64, true> : unit_select_kernel<64, false>);
+  auto kern =
+      m8 ? (d == 128
+                ? (f16 ? unit_select_kernel<128, true, true> : unit_select_kernel<128, false, true>)
+                : (f16 ? unit_select_kernel<64, true, true> : unit_select_kernel<64, false, true>))
+         : (d == 128
+                ? (f16 ? unit_select_kernel<128, true, false> : unit_select_kernel<128, false, false>)
+                : (f16 ? unit_select_kernel<64, true, false> : unit_select_kernel<64, false, false>));
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;

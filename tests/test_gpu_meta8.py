@@ -39,6 +39,11 @@ def _u16(t):
 CASES = [
     # (workload, per-sequence lengths, group selection)
     (Workload("m8-gqa-hot", B=2, Hq=8, Hkv=2, d=128, N=20000, top_k=64, kind="hot"), None, False),
+    # 375 pages at d = 64: the per-unit kernel over 8-bit codes (64-byte rows)
+    (Workload("m8-unit-d64", B=2, Hq=4, Hkv=4, d=64, N=6000, top_k=24, kind="offset"), None,
+     False),
+    (Workload("m8-unit-d64-fp16", B=2, Hq=8, Hkv=2, d=64, N=5000, top_k=20, dtype="fp16"), None,
+     False),
     (Workload("m8-mha-d64-fp16", B=3, Hq=4, Hkv=4, d=64, N=3001, top_k=12, dtype="fp16"),
      None, False),
     (Workload("m8-offset-s32-group", B=2, Hq=8, Hkv=2, d=128, N=9000, S=32, top_k=20,
