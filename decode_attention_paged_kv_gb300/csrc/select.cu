@@ -1174,6 +1174,22 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
   unit_consumers_sync();
 
   // -------------------------------------------------------------- scoring
+  // 8-bit metadata: lo and step of the lane's four pages of a box, loaded one
+  // of this warp's boxes ahead (box i + 2), so their latency hides behind the
+  // box wait instead of following each tile's MMAs.
+  float lo_n[4] = {0.f, 0.f, 0.f, 0.f}, st_n[4] = {0.f, 0.f, 0.f, 0.f};
+  auto load_lo_step = [&](int box) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int p = box * kUnitBoxPages + 16 * tile + 8 * (e >> 1) + 2 * t4 + (e & 1);
+      const int64_t pi = static_cast<int64_t>(unit) * a.P + p;
+      lo_n[e] = (head_ok && p < Pb) ? __ldg(a.lo + pi) : 0.f;
+      st_n[e] = (head_ok && p < Pb) ? __ldg(a.step + pi) : 0.f;
+    }
+  };
+  if constexpr (M8) {
+    if (half < n_boxes) load_lo_step(half);  // (its latency overlaps the query loads)
+  }
   uint32_t qp[D / 16][2], qm[D / 16][2];  // A fragments of q+ and q- (rows = heads)
   float qsum = 0.f;  // 8-bit metadata: sum_i q_i of head g
   float qscale = 1.f;  // 8-bit metadata: the scores' factor 2^k (q was scaled by 2^-k)
@@ -1246,22 +1262,6 @@ __global__ void __launch_bounds__(kUnitThreads, 1)
   }
   bool ok = true;
   uint32_t kmx = 0u, kmn = ~0u;  // extremes of head g's keys this lane wrote
-  // 8-bit metadata: lo and step of the lane's four pages of a box, loaded one
-  // of this warp's boxes ahead (box i + 2), so their latency hides behind the
-  // box wait instead of following each tile's MMAs.
-  float lo_n[4] = {0.f, 0.f, 0.f, 0.f}, st_n[4] = {0.f, 0.f, 0.f, 0.f};
-  auto load_lo_step = [&](int box) {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int p = box * kUnitBoxPages + 16 * tile + 8 * (e >> 1) + 2 * t4 + (e & 1);
-      const int64_t pi = static_cast<int64_t>(unit) * a.P + p;
-      lo_n[e] = (head_ok && p < Pb) ? __ldg(a.lo + pi) : 0.f;
-      st_n[e] = (head_ok && p < Pb) ? __ldg(a.step + pi) : 0.f;
-    }
-  };
-  if constexpr (M8) {
-    if (half < n_boxes) load_lo_step(half);
-  }
   for (int i = half; i < n_boxes; i += 2) {
     float lo_c[4], st_c[4];
     if constexpr (M8) {
