@@ -247,8 +247,8 @@ __global__ void __launch_bounds__(256) dequant4_kernel(int64_t groups, const uin
 //   code_min_i = the largest c with dec(c) <= m_i,
 //   code_max_i = the smallest c with dec(c) >= M_i.
 // The codes are defined by those extremes, so the first guess (a product
-// with the step's reciprocal) only sets where the exact search starts.  One warp per page; lane l owns
-// channels D / 32 * l ...; pages past a shorter sequence are not written.
+// with the step's reciprocal) only sets where the exact search starts.  Pages
+// past a shorter sequence are not written.
 __device__ __forceinline__ float value16f(uint32_t h, bool f16) {
   return f16 ? __half2float(__ushort_as_half(static_cast<unsigned short>(h)))
              : __uint_as_float(h << 16);
@@ -257,29 +257,37 @@ __device__ __forceinline__ float dec8(int c, float step, float lo) {
   return __fmaf_rn(static_cast<float>(c), step, lo);
 }
 
+// One page per 8 lanes (four pages a warp); lane u of a page owns channels
+// D/8 u .. D/8 u + D/8 - 1 (two or four 16-byte loads of m and M).  The
+// page's lo / hi by three shuffles within the 8 lanes; the step by the
+// definition (an IEEE division, then one-ulp raises); each code from a first
+// guess (a product with the step's reciprocal) and bounded walks to the
+// defining extreme, which take at most one step in practice: a 16-bit page's
+// range is at least one 16-bit ulp of its values, so the step is at least 16
+// fp32 ulps of any dec(c) and the guess is within one of the code.
 template <int D, bool F16>
 __global__ void __launch_bounds__(kMetaThreads) meta8_kernel(const Meta8Args a) {
   griddep_launch_dependents();
   griddep_wait();
-  constexpr int CPL = D / 32;  // channels per lane
-  const int lane = threadIdx.x & 31;
+  constexpr int CPL = D / 8;  // channels per lane
+  const int lane = threadIdx.x & 31, u = lane & 7;
+  const unsigned gmask = 0xffu << (lane & 24);
   // (page counts below 2^31, checked by the host: 32-bit index arithmetic)
   const uint32_t total = static_cast<uint32_t>(a.B) * a.Hkv * a.P;
   const uint32_t per_b = static_cast<uint32_t>(a.Hkv) * a.P;
-  const uint32_t wstride = gridDim.x * (blockDim.x >> 5);
-  for (uint32_t pg = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; pg < total; pg += wstride) {
+  const uint32_t gstride = gridDim.x * (blockDim.x >> 3);
+  for (uint32_t pg = (blockIdx.x * blockDim.x + threadIdx.x) >> 3; pg < total; pg += gstride) {
     const int j = static_cast<int>(pg % static_cast<uint32_t>(a.P));
     const int b = static_cast<int>(pg / per_b);
-    if (static_cast<int64_t>(j) * a.S >= seq_len_of(a.lens, b, a.N)) continue;
-    const int64_t off = static_cast<int64_t>(pg) * D + CPL * lane;
+    if (static_cast<int64_t>(j) * a.S >= seq_len_of(a.lens, b, a.N)) continue;  // the 8 lanes alike
+    const int64_t off = static_cast<int64_t>(pg) * D + CPL * u;
     uint32_t wm[CPL / 2], wM[CPL / 2];
-    if constexpr (CPL == 4) {
-      const uint2 x = *reinterpret_cast<const uint2*>(a.meta_min + off);
-      const uint2 y = *reinterpret_cast<const uint2*>(a.meta_max + off);
-      wm[0] = x.x; wm[1] = x.y; wM[0] = y.x; wM[1] = y.y;
-    } else {
-      wm[0] = *reinterpret_cast<const uint32_t*>(a.meta_min + off);
-      wM[0] = *reinterpret_cast<const uint32_t*>(a.meta_max + off);
+#pragma unroll
+    for (int v = 0; v < CPL / 8; ++v) {
+      const uint4 x = __ldcs(reinterpret_cast<const uint4*>(a.meta_min + off) + v);
+      const uint4 y = __ldcs(reinterpret_cast<const uint4*>(a.meta_max + off) + v);
+      wm[4 * v] = x.x; wm[4 * v + 1] = x.y; wm[4 * v + 2] = x.z; wm[4 * v + 3] = x.w;
+      wM[4 * v] = y.x; wM[4 * v + 1] = y.y; wM[4 * v + 2] = y.z; wM[4 * v + 3] = y.w;
     }
     float m[CPL], M[CPL];
 #pragma unroll
@@ -294,9 +302,9 @@ __global__ void __launch_bounds__(kMetaThreads) meta8_kernel(const Meta8Args a) 
       hi = fmaxf(hi, M[i]);
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-      hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    for (int o = 4; o > 0; o >>= 1) {
+      lo = fminf(lo, __shfl_xor_sync(gmask, lo, o));
+      hi = fmaxf(hi, __shfl_xor_sync(gmask, hi, o));
     }
     if (lo == 0.f) lo = 0.f;  // +0
     if (hi == 0.f) hi = 0.f;
@@ -305,32 +313,44 @@ __global__ void __launch_bounds__(kMetaThreads) meta8_kernel(const Meta8Args a) 
       step = __fdiv_rn(__fsub_rn(hi, lo), 255.f);
       while (dec8(255, step, lo) < hi) step = __int_as_float(__float_as_int(step) + 1);
     }
-    uint32_t cmw = 0, cMw = 0;
-    const float inv = step > 0.f ? __frcp_rn(step) : 0.f;  // for the first guesses only
+    uint32_t cmw[CPL / 4], cMw[CPL / 4];
 #pragma unroll
-    for (int i = 0; i < CPL; ++i) {
-      int cm = 0, cM = 0;
-      if (step > 0.f) {
+    for (int i = 0; i < CPL / 4; ++i) cmw[i] = cMw[i] = 0u;
+    if (step > 0.f) {
+      const float inv = __frcp_rn(step);  // for the first guesses only
+#pragma unroll
+      for (int i = 0; i < CPL; ++i) {
         const float em = __fmul_rn(__fsub_rn(m[i], lo), inv);
         const float eM = __fmul_rn(__fsub_rn(M[i], lo), inv);
-        cm = em >= 255.f ? 255 : (em >= 0.f ? static_cast<int>(em) : 0);
-        cM = eM >= 255.f ? 255 : (eM >= 0.f ? static_cast<int>(ceilf(eM)) : 0);
-        while (cm < 255 && dec8(cm + 1, step, lo) <= m[i]) ++cm;
-        while (cm > 0 && dec8(cm, step, lo) > m[i]) --cm;
-        while (cM > 0 && dec8(cM - 1, step, lo) >= M[i]) --cM;
-        while (cM < 255 && dec8(cM, step, lo) < M[i]) ++cM;
+        const float fm = fminf(fmaxf(floorf(em), 0.f), 255.f);
+        const float fM = fminf(fmaxf(ceilf(eM), 0.f), 255.f);
+        int cm = static_cast<int>(fm), cM = static_cast<int>(fM);
+        // the largest c with dec(c) <= m, the smallest with dec(c) >= M: the
+        // guesses checked at once; a miss walks there
+        const bool m_ok = (cm == 0 || __fmaf_rn(fm, step, lo) <= m[i]) &&
+                          (cm == 255 || __fmaf_rn(fm + 1.f, step, lo) > m[i]);
+        const bool M_ok = (cM == 255 || __fmaf_rn(fM, step, lo) >= M[i]) &&
+                          (cM == 0 || __fmaf_rn(fM - 1.f, step, lo) < M[i]);
+        if (!m_ok) {
+          for (int t = 0; t < 256 && cm < 255 && dec8(cm + 1, step, lo) <= m[i]; ++t) ++cm;
+          for (int t = 0; t < 256 && cm > 0 && dec8(cm, step, lo) > m[i]; ++t) --cm;
+        }
+        if (!M_ok) {
+          for (int t = 0; t < 256 && cM > 0 && dec8(cM - 1, step, lo) >= M[i]; ++t) --cM;
+          for (int t = 0; t < 256 && cM < 255 && dec8(cM, step, lo) < M[i]; ++t) ++cM;
+        }
+        cmw[i / 4] |= static_cast<uint32_t>(cm) << (8 * (i & 3));
+        cMw[i / 4] |= static_cast<uint32_t>(cM) << (8 * (i & 3));
       }
-      cmw |= static_cast<uint32_t>(cm) << (8 * i);
-      cMw |= static_cast<uint32_t>(cM) << (8 * i);
     }
-    if constexpr (CPL == 4) {
-      *reinterpret_cast<uint32_t*>(a.code_min + off) = cmw;
-      *reinterpret_cast<uint32_t*>(a.code_max + off) = cMw;
+    if constexpr (CPL == 16) {
+      *reinterpret_cast<uint4*>(a.code_min + off) = make_uint4(cmw[0], cmw[1], cmw[2], cmw[3]);
+      *reinterpret_cast<uint4*>(a.code_max + off) = make_uint4(cMw[0], cMw[1], cMw[2], cMw[3]);
     } else {
-      *reinterpret_cast<uint16_t*>(a.code_min + off) = static_cast<uint16_t>(cmw);
-      *reinterpret_cast<uint16_t*>(a.code_max + off) = static_cast<uint16_t>(cMw);
+      *reinterpret_cast<uint2*>(a.code_min + off) = make_uint2(cmw[0], cmw[1]);
+      *reinterpret_cast<uint2*>(a.code_max + off) = make_uint2(cMw[0], cMw[1]);
     }
-    if (lane == 0) {
+    if (u == 0) {
       a.lo[pg] = lo;
       a.step[pg] = step;
     }
@@ -354,8 +374,8 @@ cudaError_t launch_meta(bool q4, bool f16, const MetaArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_meta8(bool f16, const Meta8Args& a, cudaStream_t s) {
-  const int64_t warps = static_cast<int64_t>(a.B) * a.Hkv * a.P;
-  const dim3 grid(grid_for(warps * 32, kMetaThreads)), block(kMetaThreads);
+  const int64_t pages = static_cast<int64_t>(a.B) * a.Hkv * a.P;  // 8 threads a page
+  const dim3 grid(grid_for(pages * 8, kMetaThreads)), block(kMetaThreads);
   if (a.d == 128)
     return f16 ? launch_pdl(meta8_kernel<128, true>, grid, block, 0, s, a)
                : launch_pdl(meta8_kernel<128, false>, grid, block, 0, s, a);
