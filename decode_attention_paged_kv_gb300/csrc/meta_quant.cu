@@ -256,15 +256,30 @@ __device__ __forceinline__ float value16f(uint32_t h, bool f16) {
 __device__ __forceinline__ float dec8(int c, float step, float lo) {
   return __fmaf_rn(static_cast<float>(c), step, lo);
 }
+constexpr float kTwo23 = 8388608.0f;  // 2^23: x + 2^23 holds an integer x in its low bits
+// the low bytes of four words, in order, as one word
+__device__ __forceinline__ uint32_t low_bytes4(const uint32_t (&c)[4]) {
+  return __byte_perm(__byte_perm(c[0], c[1], 0x0040u), __byte_perm(c[2], c[3], 0x0040u),
+                     0x5410u);
+}
 
 // One page per 8 lanes (four pages a warp); lane u of a page owns channels
 // D/8 u .. D/8 u + D/8 - 1 (two or four 16-byte loads of m and M).  The
 // page's lo / hi by three shuffles within the 8 lanes; the step by the
-// definition (an IEEE division, then one-ulp raises); each code from a first
-// guess (a product with the step's reciprocal) and bounded walks to the
-// defining extreme, which take at most one step in practice: a 16-bit page's
-// range is at least one 16-bit ulp of its values, so the step is at least 16
-// fp32 ulps of any dec(c) and the guess is within one of the code.
+// definition (an IEEE division, then one-ulp raises).  Each code without a
+// search: with t = (m - lo) / step exactly and em = fl(fl(m - lo) fl(1/step)),
+// |em - t| <= 256 * 3 * 2^-24; and a 16-bit page's range is at least one
+// 16-bit ulp of its values (2^13 fp32 ulps for fp16, 2^16 for bf16), so the
+// step is at least 16 fp32 ulps of any value in it and the largest c with
+// dec(c) <= m is floor(t) or floor(t) + 1.  Hence code_min is within one of
+// fm = floor(em), and
+//   code_min = fm - 1 + [dec(fm) <= m] + [dec(fm + 1) <= m];
+// likewise code_max = gM + 1 - [dec(gM) >= M] - [dec(gM - 1) >= M] with
+// gM = ceil(eM).  floor / ceil as 2^23 + em rounded down / up, whose low byte
+// is the code (the sum stays within 2^23 .. 2^23 + 256).  This needs 1 / step
+// finite and normal: steps below 2^-100 (bf16 pages below about 2^-92
+// throughout) and infinite ones (a bf16 range above the largest float) take
+// bounded walks from a clamped guess instead.
 template <int D, bool F16>
 __global__ void __launch_bounds__(kMetaThreads) meta8_kernel(const Meta8Args a) {
   griddep_launch_dependents();
@@ -316,29 +331,41 @@ __global__ void __launch_bounds__(kMetaThreads) meta8_kernel(const Meta8Args a) 
     uint32_t cmw[CPL / 4], cMw[CPL / 4];
 #pragma unroll
     for (int i = 0; i < CPL / 4; ++i) cmw[i] = cMw[i] = 0u;
-    if (step > 0.f) {
-      const float inv = __frcp_rn(step);  // for the first guesses only
+    if (step >= 0x1p-100f && step < INFINITY) {
+      // the guess and the two comparisons that settle the code
+      const float inv = __frcp_rn(step);
+#pragma unroll
+      for (int w = 0; w < CPL / 4; ++w) {
+        uint32_t cm[4], cM[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = 4 * w + e;
+          const float tm = __fadd_rd(__fmul_rn(__fsub_rn(m[i], lo), inv), kTwo23);
+          const float fm = __fsub_rn(tm, kTwo23);  // floor of the guess
+          cm[e] = __float_as_uint(tm) - 1u + (__fmaf_rn(fm, step, lo) <= m[i]) +
+                  (__fmaf_rn(__fadd_rn(fm, 1.f), step, lo) <= m[i]);
+          const float tM = __fadd_ru(__fmul_rn(__fsub_rn(M[i], lo), inv), kTwo23);
+          const float gM = __fsub_rn(tM, kTwo23);  // ceiling of the guess
+          cM[e] = __float_as_uint(tM) + 1u - (__fmaf_rn(gM, step, lo) >= M[i]) -
+                  (__fmaf_rn(__fsub_rn(gM, 1.f), step, lo) >= M[i]);
+        }
+        cmw[w] = low_bytes4(cm);
+        cMw[w] = low_bytes4(cM);
+      }
+    } else if (step > 0.f) {
+      // a step below 2^-100 (1 / step may overflow) or an infinite one: the
+      // clamped guess and bounded walks to the defining extremes
+      const float inv = __frcp_rn(step);
 #pragma unroll
       for (int i = 0; i < CPL; ++i) {
         const float em = __fmul_rn(__fsub_rn(m[i], lo), inv);
         const float eM = __fmul_rn(__fsub_rn(M[i], lo), inv);
-        const float fm = fminf(fmaxf(floorf(em), 0.f), 255.f);
-        const float fM = fminf(fmaxf(ceilf(eM), 0.f), 255.f);
-        int cm = static_cast<int>(fm), cM = static_cast<int>(fM);
-        // the largest c with dec(c) <= m, the smallest with dec(c) >= M: the
-        // guesses checked at once; a miss walks there
-        const bool m_ok = (cm == 0 || __fmaf_rn(fm, step, lo) <= m[i]) &&
-                          (cm == 255 || __fmaf_rn(fm + 1.f, step, lo) > m[i]);
-        const bool M_ok = (cM == 255 || __fmaf_rn(fM, step, lo) >= M[i]) &&
-                          (cM == 0 || __fmaf_rn(fM - 1.f, step, lo) < M[i]);
-        if (!m_ok) {
-          for (int t = 0; t < 256 && cm < 255 && dec8(cm + 1, step, lo) <= m[i]; ++t) ++cm;
-          for (int t = 0; t < 256 && cm > 0 && dec8(cm, step, lo) > m[i]; ++t) --cm;
-        }
-        if (!M_ok) {
-          for (int t = 0; t < 256 && cM > 0 && dec8(cM - 1, step, lo) >= M[i]; ++t) --cM;
-          for (int t = 0; t < 256 && cM < 255 && dec8(cM, step, lo) < M[i]; ++t) ++cM;
-        }
+        int cm = static_cast<int>(fminf(fmaxf(floorf(em), 0.f), 255.f));
+        int cM = static_cast<int>(fminf(fmaxf(ceilf(eM), 0.f), 255.f));
+        for (int t = 0; t < 256 && cm < 255 && dec8(cm + 1, step, lo) <= m[i]; ++t) ++cm;
+        for (int t = 0; t < 256 && cm > 0 && dec8(cm, step, lo) > m[i]; ++t) --cm;
+        for (int t = 0; t < 256 && cM > 0 && dec8(cM - 1, step, lo) >= M[i]; ++t) --cM;
+        for (int t = 0; t < 256 && cM < 255 && dec8(cM, step, lo) < M[i]; ++t) ++cM;
         cmw[i / 4] |= static_cast<uint32_t>(cm) << (8 * (i & 3));
         cMw[i / 4] |= static_cast<uint32_t>(cM) << (8 * (i & 3));
       }

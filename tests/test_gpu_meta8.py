@@ -127,3 +127,100 @@ def test_meta8_paged_cache_equals_contiguous(dev, dkv):
     oc, sc = dkv.decode_attn_select(qd, Kd, Vd, mc, w.top_k, return_selected=True)
     op, sp = dkv.decode_attn_select(qd, PK, PV, mp, w.top_k, return_selected=True)
     assert torch.equal(sc, sp) and torch.equal(oc, op)
+
+
+def _finite_values(f16):
+    """Every finite 16-bit value once (one zero), ascending, as float64."""
+    u = np.arange(65536, dtype=np.uint32)
+    with np.errstate(invalid="ignore"):
+        if f16:
+            v = u.astype(np.uint16).view(np.float16).astype(np.float64)
+        else:
+            v = (u << 16).view(np.float32).astype(np.float64)
+    return np.unique(v[np.isfinite(v)])
+
+
+def _to16(x, f16):
+    """float64 values that are 16-bit values -> their bit patterns."""
+    if f16:
+        return x.astype(np.float16).view(np.uint16)
+    return (x.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def _edge_pages(f16, d, seed):
+    """Metadata pages (m, M) [1, 1, P, d] at the edges of the 8-bit code rule:
+    pages of two 16-bit values up to 16 apart with every value between; every
+    exact grid point lo + c step that is a 16-bit value, as m and as M; values
+    at and beside the 16-bit values nearest to grid points of wide pages;
+    constant pages; the format's extremes; for bf16 also pages whose step is
+    below 2^-100 or infinite."""
+    rng = np.random.default_rng(seed)
+    vals = _finite_values(f16)
+    n = len(vals)
+    pages = []  # (lo index, hi index, extra values)
+    for _ in range(48):  # tight, half of them straddling a power of two
+        if len(pages) % 2:
+            e = rng.integers(-12 if f16 else -100, 15 if f16 else 100)
+            a = int(np.searchsorted(vals, 2.0 ** e)) - int(rng.integers(1, 9))
+        else:
+            a = int(rng.integers(0, n - 17))
+        w = int(rng.integers(1, 17))
+        pages.append((a, a + w, vals[a:a + w + 1]))
+    for _ in range(48):  # wide
+        a = int(rng.integers(0, n - 4097))
+        pages.append((a, a + int(rng.integers(64, 4096)), None))
+    top = n - 1
+    pages.append((0, top, None))  # -max .. max (bf16: an infinite range)
+    pages.append((top // 2 - 3, top // 2 + 3, vals[top // 2 - 3:top // 2 + 4]))  # around 0
+    pages.append((top - 1, top, vals[top - 1:]))
+    pages.append((5, 5, None))  # constant
+    if not f16:  # steps below 2^-100
+        a = int(np.searchsorted(vals, 2.0 ** -120))
+        pages.append((a, a + 40, vals[a:a + 41]))
+        a = int(np.searchsorted(vals, -(2.0 ** -110)))
+        pages.append((a, a + 300, None))
+    P = len(pages)
+    mn = np.empty((P, d), np.float64)
+    mx = np.empty((P, d), np.float64)
+    for j, (a, b, extra) in enumerate(pages):
+        cand = extra if extra is not None else vals[a:b + 1][rng.integers(0, b - a + 1, 4 * d)]
+        x = rng.choice(cand, size=(2, d))
+        mn[j], mx[j] = np.minimum(x[0], x[1]), np.maximum(x[0], x[1])
+        mn[j, 0], mx[j, 1] = vals[a], vals[b]
+    # the grid of each page, from the oracle: exact grid points, and the
+    # 16-bit values at and beside the nearest ones, replace channels 2..
+    shape = (1, 1, P, d)
+    _, _, lo, step = oracle.meta8(_to16(mn, f16).reshape(shape), _to16(mx, f16).reshape(shape),
+                                  int(f16))
+    lo, step = lo.reshape(P).astype(np.float64), step.reshape(P).astype(np.float64)
+    for j, (a, b, extra) in enumerate(pages):
+        if extra is not None or not (0 < step[j] < np.inf):
+            continue
+        g = lo[j] + np.arange(256) * step[j]
+        idx = np.clip(np.searchsorted(vals, g), a, b)
+        exact = vals[idx] == g
+        picks = list(vals[idx[exact]])
+        for k in (-1, 0, 1):
+            picks += list(vals[np.clip(idx + k, a, b)][rng.integers(0, 256, 16)])
+        picks = np.array(picks[:2 * (d - 2)])
+        half = len(picks) // 2
+        mn[j, 2:2 + half] = np.minimum(picks[:half], mx[j, 2:2 + half])
+        mx[j, 2:2 + half] = np.maximum(picks[half:2 * half], mn[j, 2:2 + half])
+    return _to16(mn, f16).reshape(shape), _to16(mx, f16).reshape(shape)
+
+
+@pytest.mark.parametrize("f16", [0, 1], ids=["bf16", "fp16"])
+@pytest.mark.parametrize("d", [128, 64])
+def test_meta8_codes_on_edge_pages(f16, d, dev, dkv):
+    mn, mx = _edge_pages(f16, d, seed=91 + d + f16)
+    want = oracle.meta8(mn, mx, f16)
+    dt = torch.float16 if f16 else torch.bfloat16
+    md = torch.from_numpy(mn.view(np.int16)).view(dt).to(dev)
+    Md = torch.from_numpy(mx.view(np.int16)).view(dt).to(dev)
+    m8 = dkv.kv_meta8_build((md, Md), page_size=16)
+    got = (m8.code_min.cpu().numpy(), m8.code_max.cpu().numpy(),
+           m8.lo.cpu().numpy().view(np.uint32), m8.step.cpu().numpy().view(np.uint32))
+    for name, g, w in zip(("code_min", "code_max", "lo", "step"), got,
+                          (want[0], want[1], want[2].view(np.uint32), want[3].view(np.uint32))):
+        bad = np.argwhere(g != w)
+        assert bad.size == 0, f"{name}: {len(bad)} differ, first at {bad[0]}"
