@@ -257,6 +257,42 @@ __device__ __forceinline__ float dec8(int c, float step, float lo) {
   return __fmaf_rn(static_cast<float>(c), step, lo);
 }
 constexpr float kTwo23 = 8388608.0f;  // 2^23: x + 2^23 holds an integer x in its low bits
+
+// Two fp32 values in one 64-bit register pair, and the packed fp32 pair
+// arithmetic of sm_100 and later (each lane rounded as the scalar operation
+// with the same rounding mode; subnormals kept).
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add_down(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rm.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add_up(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rp.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint32_t lo32(uint64_t v) { return static_cast<uint32_t>(v); }
+__device__ __forceinline__ uint32_t hi32(uint64_t v) { return static_cast<uint32_t>(v >> 32); }
 // the low bytes of four words, in order, as one word
 __device__ __forceinline__ uint32_t low_bytes4(const uint32_t (&c)[4]) {
   return __byte_perm(__byte_perm(c[0], c[1], 0x0040u), __byte_perm(c[2], c[3], 0x0040u),
@@ -332,22 +368,32 @@ __global__ void __launch_bounds__(kMetaThreads) meta8_kernel(const Meta8Args a) 
 #pragma unroll
     for (int i = 0; i < CPL / 4; ++i) cmw[i] = cMw[i] = 0u;
     if (step >= 0x1p-100f && step < INFINITY) {
-      // the guess and the two comparisons that settle the code
+      // the guess and the two comparisons that settle the code, two channels
+      // per packed operation; a comparison as the sign of a difference
+      // (fl(x - y) is negative exactly when x < y, +0 when equal)
       const float inv = __frcp_rn(step);
+      const uint64_t LO = f2(lo, lo), INV = f2(inv, inv), STEP = f2(step, step);
+      const uint64_t K = f2(kTwo23, kTwo23), KM1 = f2(kTwo23 - 1.f, kTwo23 - 1.f);
+      const uint64_t KP1 = f2(kTwo23 + 1.f, kTwo23 + 1.f);
 #pragma unroll
       for (int w = 0; w < CPL / 4; ++w) {
         uint32_t cm[4], cM[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int e = 0; e < 4; e += 2) {
           const int i = 4 * w + e;
-          const float tm = __fadd_rd(__fmul_rn(__fsub_rn(m[i], lo), inv), kTwo23);
-          const float fm = __fsub_rn(tm, kTwo23);  // floor of the guess
-          cm[e] = __float_as_uint(tm) - 1u + (__fmaf_rn(fm, step, lo) <= m[i]) +
-                  (__fmaf_rn(__fadd_rn(fm, 1.f), step, lo) <= m[i]);
-          const float tM = __fadd_ru(__fmul_rn(__fsub_rn(M[i], lo), inv), kTwo23);
-          const float gM = __fsub_rn(tM, kTwo23);  // ceiling of the guess
-          cM[e] = __float_as_uint(tM) + 1u - (__fmaf_rn(gM, step, lo) >= M[i]) -
-                  (__fmaf_rn(__fsub_rn(gM, 1.f), step, lo) >= M[i]);
+          const uint64_t mm = f2(m[i], m[i + 1]), MM = f2(M[i], M[i + 1]);
+          // code_min = floor + 1 - [m < dec(floor)] - [m < dec(floor + 1)]
+          const uint64_t tm = f2_add_down(f2_mul(f2_sub(mm, LO), INV), K);
+          const uint64_t dm0 = f2_sub(mm, f2_fma(f2_sub(tm, K), STEP, LO));
+          const uint64_t dm1 = f2_sub(mm, f2_fma(f2_sub(tm, KM1), STEP, LO));
+          cm[e] = lo32(tm) + 1u - (lo32(dm0) >> 31) - (lo32(dm1) >> 31);
+          cm[e + 1] = hi32(tm) + 1u - (hi32(dm0) >> 31) - (hi32(dm1) >> 31);
+          // code_max = ceil - 1 + [dec(ceil) < M] + [dec(ceil - 1) < M]
+          const uint64_t tM = f2_add_up(f2_mul(f2_sub(MM, LO), INV), K);
+          const uint64_t dM0 = f2_sub(f2_fma(f2_sub(tM, K), STEP, LO), MM);
+          const uint64_t dM1 = f2_sub(f2_fma(f2_sub(tM, KP1), STEP, LO), MM);
+          cM[e] = lo32(tM) - 1u + (lo32(dM0) >> 31) + (lo32(dM1) >> 31);
+          cM[e + 1] = hi32(tM) - 1u + (hi32(dM0) >> 31) + (hi32(dM1) >> 31);
         }
         cmw[w] = low_bytes4(cm);
         cMw[w] = low_bytes4(cM);

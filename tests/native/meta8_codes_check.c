@@ -9,7 +9,9 @@
  *   inv = fl(1 / step),  em = fl(fl(m - lo) * inv),  eM = fl(fl(M - lo) * inv),
  *   fm = floor(em),      gM = ceil(eM)          (as 2^23 + x rounded down / up),
  *   code_min = fm - 1 + [dec(fm) <= m] + [dec(fm + 1) <= m],
- *   code_max = gM + 1 - [dec(gM) >= M] - [dec(gM - 1) >= M].
+ *   code_max = gM + 1 - [dec(gM) >= M] - [dec(gM - 1) >= M],
+ * each comparison taken, as the kernel takes it, from the sign bit of a
+ * difference (fl(x - y) < 0 exactly when x < y).
  * It holds when the defining code is within one of the guess; that follows
  * from |em - t| <= 256 * 3 * 2^-24 (t the exact (m - lo) / step) and from a
  * 16-bit page's step being at least 16 fp32 ulps of any value in the page
@@ -95,21 +97,23 @@ static int def_max(float M, float step, float lo) {
 
 static const float kMagic = 8388608.0f; /* 2^23 */
 
+/* a comparison as the sign of a difference: fl(x - y) is negative exactly
+ * when x < y (and +0 when they are equal) */
+static uint32_t neg(float d) { return bits_of(d) >> 31; }
+
 static int rule_min(float m, float step, float lo, float inv) {
   const float em = (m - lo) * inv;
-  const float tm = add_dir(em, kMagic, 0);
-  const float fm = tm - kMagic;
-  const int64_t c = (int64_t)bits_of(tm) - 1 + (fmaf(fm, step, lo) <= m) +
-                    (fmaf(fm + 1.0f, step, lo) <= m);
+  const float tm = add_dir(em, kMagic, 0); /* 2^23 + floor(em) */
+  const int64_t c = (int64_t)bits_of(tm) + 1 - neg(m - fmaf(tm - kMagic, step, lo)) -
+                    neg(m - fmaf(tm - (kMagic - 1.0f), step, lo));
   return (int)(c - (int64_t)bits_of(kMagic));
 }
 
 static int rule_max(float M, float step, float lo, float inv) {
   const float eM = (M - lo) * inv;
-  const float tM = add_dir(eM, kMagic, 1);
-  const float gM = tM - kMagic;
-  const int64_t c = (int64_t)bits_of(tM) + 1 - (fmaf(gM, step, lo) >= M) -
-                    (fmaf(gM - 1.0f, step, lo) >= M);
+  const float tM = add_dir(eM, kMagic, 1); /* 2^23 + ceil(eM) */
+  const int64_t c = (int64_t)bits_of(tM) - 1 + neg(fmaf(tM - kMagic, step, lo) - M) +
+                    neg(fmaf(tM - (kMagic + 1.0f), step, lo) - M);
   return (int)(c - (int64_t)bits_of(kMagic));
 }
 
