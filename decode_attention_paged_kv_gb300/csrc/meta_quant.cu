@@ -253,10 +253,41 @@ __device__ __forceinline__ float value16f(uint32_t h, bool f16) {
   return f16 ? __half2float(__ushort_as_half(static_cast<unsigned short>(h)))
              : __uint_as_float(h << 16);
 }
+template <bool F16>
+__device__ __forceinline__ uint32_t min16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  if constexpr (F16) {
+    const __half2 v = __hmin2(*reinterpret_cast<const __half2*>(&a),
+                              *reinterpret_cast<const __half2*>(&b));
+    r = *reinterpret_cast<const uint32_t*>(&v);
+  } else {
+    const __nv_bfloat162 v = __hmin2(*reinterpret_cast<const __nv_bfloat162*>(&a),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&b));
+    r = *reinterpret_cast<const uint32_t*>(&v);
+  }
+  return r;
+}
+template <bool F16>
+__device__ __forceinline__ uint32_t max16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  if constexpr (F16) {
+    const __half2 v = __hmax2(*reinterpret_cast<const __half2*>(&a),
+                              *reinterpret_cast<const __half2*>(&b));
+    r = *reinterpret_cast<const uint32_t*>(&v);
+  } else {
+    const __nv_bfloat162 v = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&a),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&b));
+    r = *reinterpret_cast<const uint32_t*>(&v);
+  }
+  return r;
+}
 __device__ __forceinline__ float dec8(int c, float step, float lo) {
   return __fmaf_rn(static_cast<float>(c), step, lo);
 }
-constexpr float kTwo23 = 8388608.0f;  // 2^23: x + 2^23 holds an integer x in its low bits
+// 3 2^22: for 0 <= x < 2^22, x + K - 1 lies where floats are spaced by one,
+// so its rounding down / up is K - 1 + floor(x) / ceil(x), held in the low
+// bits (the float bits of K + j are those of K plus j)
+constexpr float kMagic = 12582912.0f;
 
 // Two fp32 values in one 64-bit register pair, and the packed fp32 pair
 // arithmetic of sm_100 and later (each lane rounded as the scalar operation
@@ -269,6 +300,13 @@ __device__ __forceinline__ uint64_t f2(float a, float b) {
 __device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
   uint64_t r;
   asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// rounded down: an exact zero difference is -0 (IEEE 754, rounding toward
+// negative), so the sign bit of a - b is set exactly when a <= b
+__device__ __forceinline__ uint64_t f2_sub_down(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rm.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
 __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
@@ -311,8 +349,8 @@ __device__ __forceinline__ uint32_t low_bytes4(const uint32_t (&c)[4]) {
 // fm = floor(em), and
 //   code_min = fm - 1 + [dec(fm) <= m] + [dec(fm + 1) <= m];
 // likewise code_max = gM + 1 - [dec(gM) >= M] - [dec(gM - 1) >= M] with
-// gM = ceil(eM).  floor / ceil as 2^23 + em rounded down / up, whose low byte
-// is the code (the sum stays within 2^23 .. 2^23 + 256).  This needs 1 / step
+// gM = ceil(eM).  floor / ceil as em + 3 2^22 - 1 rounded down / up, whose
+// low byte plus the two comparison bits is the code.  This needs 1 / step
 // finite and normal: steps below 2^-100 (bf16 pages below about 2^-92
 // throughout) and infinite ones (a bf16 range above the largest float) take
 // bounded walks from a clamped guess instead.
@@ -346,12 +384,14 @@ __global__ void __launch_bounds__(kMetaThreads) meta8_kernel(const Meta8Args a) 
       m[i] = value16f((wm[i / 2] >> (16 * (i & 1))) & 0xffffu, F16);
       M[i] = value16f((wM[i / 2] >> (16 * (i & 1))) & 0xffffu, F16);
     }
-    float lo = m[0], hi = M[0];
+    uint32_t wlo = wm[0], whi = wM[0];  // two 16-bit lanes at a time
 #pragma unroll
-    for (int i = 1; i < CPL; ++i) {
-      lo = fminf(lo, m[i]);
-      hi = fmaxf(hi, M[i]);
+    for (int i = 1; i < CPL / 2; ++i) {
+      wlo = min16x2<F16>(wlo, wm[i]);
+      whi = max16x2<F16>(whi, wM[i]);
     }
+    float lo = fminf(value16f(wlo & 0xffffu, F16), value16f(wlo >> 16, F16));
+    float hi = fmaxf(value16f(whi & 0xffffu, F16), value16f(whi >> 16, F16));
 #pragma unroll
     for (int o = 4; o > 0; o >>= 1) {
       lo = fminf(lo, __shfl_xor_sync(gmask, lo, o));
@@ -369,12 +409,11 @@ __global__ void __launch_bounds__(kMetaThreads) meta8_kernel(const Meta8Args a) 
     for (int i = 0; i < CPL / 4; ++i) cmw[i] = cMw[i] = 0u;
     if (step >= 0x1p-100f && step < INFINITY) {
       // the guess and the two comparisons that settle the code, two channels
-      // per packed operation; a comparison as the sign of a difference
-      // (fl(x - y) is negative exactly when x < y, +0 when equal)
+      // per packed operation, each comparison the sign bit of a difference
       const float inv = __frcp_rn(step);
       const uint64_t LO = f2(lo, lo), INV = f2(inv, inv), STEP = f2(step, step);
-      const uint64_t K = f2(kTwo23, kTwo23), KM1 = f2(kTwo23 - 1.f, kTwo23 - 1.f);
-      const uint64_t KP1 = f2(kTwo23 + 1.f, kTwo23 + 1.f);
+      const uint64_t K1 = f2(kMagic - 1.f, kMagic - 1.f), K2 = f2(kMagic - 2.f, kMagic - 2.f);
+      const uint64_t K0 = f2(kMagic, kMagic);
 #pragma unroll
       for (int w = 0; w < CPL / 4; ++w) {
         uint32_t cm[4], cM[4];
@@ -382,18 +421,18 @@ __global__ void __launch_bounds__(kMetaThreads) meta8_kernel(const Meta8Args a) 
         for (int e = 0; e < 4; e += 2) {
           const int i = 4 * w + e;
           const uint64_t mm = f2(m[i], m[i + 1]), MM = f2(M[i], M[i + 1]);
-          // code_min = floor + 1 - [m < dec(floor)] - [m < dec(floor + 1)]
-          const uint64_t tm = f2_add_down(f2_mul(f2_sub(mm, LO), INV), K);
-          const uint64_t dm0 = f2_sub(mm, f2_fma(f2_sub(tm, K), STEP, LO));
-          const uint64_t dm1 = f2_sub(mm, f2_fma(f2_sub(tm, KM1), STEP, LO));
-          cm[e] = lo32(tm) + 1u - (lo32(dm0) >> 31) - (lo32(dm1) >> 31);
-          cm[e + 1] = hi32(tm) + 1u - (hi32(dm0) >> 31) - (hi32(dm1) >> 31);
-          // code_max = ceil - 1 + [dec(ceil) < M] + [dec(ceil - 1) < M]
-          const uint64_t tM = f2_add_up(f2_mul(f2_sub(MM, LO), INV), K);
-          const uint64_t dM0 = f2_sub(f2_fma(f2_sub(tM, K), STEP, LO), MM);
-          const uint64_t dM1 = f2_sub(f2_fma(f2_sub(tM, KP1), STEP, LO), MM);
-          cM[e] = lo32(tM) - 1u + (lo32(dM0) >> 31) + (lo32(dM1) >> 31);
-          cM[e + 1] = hi32(tM) - 1u + (hi32(dM0) >> 31) + (hi32(dM1) >> 31);
+          // code_min = (floor - 1) + [dec(floor) <= m] + [dec(floor + 1) <= m]
+          const uint64_t tm = f2_add_down(f2_mul(f2_sub(mm, LO), INV), K1);  // K - 1 + floor
+          const uint64_t sm0 = f2_sub_down(f2_fma(f2_sub(tm, K1), STEP, LO), mm);
+          const uint64_t sm1 = f2_sub_down(f2_fma(f2_sub(tm, K2), STEP, LO), mm);
+          cm[e] = lo32(tm) + (lo32(sm0) >> 31) + (lo32(sm1) >> 31);
+          cm[e + 1] = hi32(tm) + (hi32(sm0) >> 31) + (hi32(sm1) >> 31);
+          // code_max = (ceil - 1) + [dec(ceil) < M] + [dec(ceil - 1) < M]
+          const uint64_t tM = f2_add_up(f2_mul(f2_sub(MM, LO), INV), K1);  // K - 1 + ceil
+          const uint64_t sM0 = f2_sub(f2_fma(f2_sub(tM, K1), STEP, LO), MM);
+          const uint64_t sM1 = f2_sub(f2_fma(f2_sub(tM, K0), STEP, LO), MM);
+          cM[e] = lo32(tM) + (lo32(sM0) >> 31) + (lo32(sM1) >> 31);
+          cM[e + 1] = hi32(tM) + (hi32(sM0) >> 31) + (hi32(sM1) >> 31);
         }
         cmw[w] = low_bytes4(cm);
         cMw[w] = low_bytes4(cM);

@@ -7,11 +7,11 @@
  *   code_max(M) = the smallest c with dec(c) >= M,
  * found here by trying all 256 codes.  The rule checked against them:
  *   inv = fl(1 / step),  em = fl(fl(m - lo) * inv),  eM = fl(fl(M - lo) * inv),
- *   fm = floor(em),      gM = ceil(eM)          (as 2^23 + x rounded down / up),
+ *   fm = floor(em),      gM = ceil(eM)   (as x + 3 2^22 - 1 rounded down / up),
  *   code_min = fm - 1 + [dec(fm) <= m] + [dec(fm + 1) <= m],
- *   code_max = gM + 1 - [dec(gM) >= M] - [dec(gM - 1) >= M],
+ *   code_max = gM - 1 + [dec(gM) < M] + [dec(gM - 1) < M],
  * each comparison taken, as the kernel takes it, from the sign bit of a
- * difference (fl(x - y) < 0 exactly when x < y).
+ * difference (rounded down for the <= comparisons).
  * It holds when the defining code is within one of the guess; that follows
  * from |em - t| <= 256 * 3 * 2^-24 (t the exact (m - lo) / step) and from a
  * 16-bit page's step being at least 16 fp32 ulps of any value in the page
@@ -36,6 +36,7 @@
  * maxw; for random: count, seed.
  * Exit status 0 and "ok <checked> <pages outside the rule>" when every code
  * agrees; the first mismatch otherwise. */
+#include <fenv.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -69,7 +70,7 @@ static float dec8(int c, float step, float lo) { return fmaf((float)c, step, lo)
 
 static float add_dir(float a, float b, int up) {
   const float s = a + b;
-  const double exact = (double)a + (double)b; /* exact: |a| < 2^9, b = 2^23 */
+  const double exact = (double)a + (double)b; /* exact: |a| < 2^9, b < 2^24 */
   if (!up && (double)s > exact) return nextafterf(s, -INFINITY);
   if (up && (double)s < exact) return nextafterf(s, INFINITY);
   return s;
@@ -95,25 +96,35 @@ static int def_max(float M, float step, float lo) {
   return -1;
 }
 
-static const float kMagic = 8388608.0f; /* 2^23 */
+/* 3 2^22: x + K - 1 (0 <= x < 2^22) lies where floats are spaced by one, so
+ * its rounding down / up is K - 1 + floor(x) / ceil(x), and the float bits of
+ * K + j are those of K plus j */
+static const float kMagic = 12582912.0f;
 
-/* a comparison as the sign of a difference: fl(x - y) is negative exactly
- * when x < y (and +0 when they are equal) */
-static uint32_t neg(float d) { return bits_of(d) >> 31; }
+/* the sign bit of a difference: fl(x - y) is negative exactly when x < y (+0
+ * when equal); rounded down, an exact zero is -0, so the sign bit of
+ * fl_down(x - y) is set exactly when x <= y */
+static uint32_t sign_of(float d) { return bits_of(d) >> 31; }
+static float sub_down(float a, float b) {
+  fesetround(FE_DOWNWARD);
+  volatile float r = a - b;
+  fesetround(FE_TONEAREST);
+  return r;
+}
 
 static int rule_min(float m, float step, float lo, float inv) {
   const float em = (m - lo) * inv;
-  const float tm = add_dir(em, kMagic, 0); /* 2^23 + floor(em) */
-  const int64_t c = (int64_t)bits_of(tm) + 1 - neg(m - fmaf(tm - kMagic, step, lo)) -
-                    neg(m - fmaf(tm - (kMagic - 1.0f), step, lo));
+  const float tm = add_dir(em, kMagic - 1.0f, 0); /* K - 1 + floor(em) */
+  const int64_t c = (int64_t)bits_of(tm) + sign_of(sub_down(fmaf(tm - (kMagic - 1.0f), step, lo), m)) +
+                    sign_of(sub_down(fmaf(tm - (kMagic - 2.0f), step, lo), m));
   return (int)(c - (int64_t)bits_of(kMagic));
 }
 
 static int rule_max(float M, float step, float lo, float inv) {
   const float eM = (M - lo) * inv;
-  const float tM = add_dir(eM, kMagic, 1); /* 2^23 + ceil(eM) */
-  const int64_t c = (int64_t)bits_of(tM) - 1 + neg(fmaf(tM - kMagic, step, lo) - M) +
-                    neg(fmaf(tM - (kMagic + 1.0f), step, lo) - M);
+  const float tM = add_dir(eM, kMagic - 1.0f, 1); /* K - 1 + ceil(eM) */
+  const int64_t c = (int64_t)bits_of(tM) + sign_of(fmaf(tM - (kMagic - 1.0f), step, lo) - M) +
+                    sign_of(fmaf(tM - kMagic, step, lo) - M);
   return (int)(c - (int64_t)bits_of(kMagic));
 }
 

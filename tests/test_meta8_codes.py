@@ -2,11 +2,13 @@
 guesses fm = floor(fl(fl(m - lo) * fl(1 / step))) and gM = ceil(same for M) it
 takes
     code_min = fm - 1 + [dec(fm) <= m] + [dec(fm + 1) <= m],
-    code_max = gM + 1 - [dec(gM) >= M] - [dec(gM - 1) >= M],
+    code_max = gM - 1 + [dec(gM) < M] + [dec(gM - 1) < M],
 which is the definition (the largest c with dec(c) <= m, the smallest with
 dec(c) >= M, dec(c) = fma(c, step, lo)) whenever the defining code is within
 one of the guess -- true for a 16-bit page with a step in [2^-100, inf), whose
-step is at least 16 fp32 ulps of every value in it.  This checks the rule
+step is at least 16 fp32 ulps of every value in it.  Each comparison is the
+sign bit of a difference (rounded down for <=, where an exact zero is -0).
+This checks the rule
 against the definition (all 256 codes tried) on the host with C's fmaf, over
 every page of two 16-bit values up to 16 apart with every value between,
 whole random pages, every exact grid hit of random pages (where the rounded
@@ -21,7 +23,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 
 def test_branch_free_codes_equal_definition(tmp_path):
     exe = str(tmp_path / "meta8_codes")
-    r = subprocess.run(["gcc", "-O2", "-ffp-contract=off", "-o", exe,
+    r = subprocess.run(["gcc", "-O2", "-ffp-contract=off", "-frounding-math", "-o", exe,
                         os.path.join(HERE, "native", "meta8_codes_check.c"), "-lm"],
                        capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
