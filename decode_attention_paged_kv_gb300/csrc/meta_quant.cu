@@ -25,8 +25,7 @@ namespace {
 
 constexpr int kMetaThreads = 256;
 
-template <bool Q4>
-__global__ void __launch_bounds__(kMetaThreads, Q4 ? 4 : 2) meta_kernel(const MetaArgs a) {
+__global__ void __launch_bounds__(kMetaThreads, 2) meta_kernel(const MetaArgs a) {
   griddep_launch_dependents();
   griddep_wait();
   const int vpr = a.d / 8;  // 16-byte vectors per row
@@ -48,102 +47,33 @@ __global__ void __launch_bounds__(kMetaThreads, Q4 ? 4 : 2) meta_kernel(const Me
     const int nt = min(a.S, Nb - t0);
     uint32_t kmin[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
     uint32_t kmax[4] = {0u, 0u, 0u, 0u};
-    if constexpr (!Q4) {
-      // the metadata page's 16-token cache pages, one at a time
+    // the metadata page's 16-token cache pages, one at a time
 #pragma unroll 1
-      for (int c0 = 0; c0 < nt; c0 += kPage) {
-        const int cp = (t0 + c0) / kPage;  // cache page
-        const int ntc = min(kPage, nt - c0);
-        // a paged cache: the cache page's pool block (clamped), token 0 of it
-        // (a page of 4 or 8 tokens starts inside its block)
-        const int64_t base = a.bt != nullptr
-                                 ? static_cast<int64_t>(min(max(a.bt[b * a.bts + cp], 0),
-                                                            a.nblocks - 1)) * a.sb +
-                                       static_cast<int64_t>((t0 + c0) % kPage) * a.d
-                                 : b * a.sb + static_cast<int64_t>(t0 + c0) * a.d;
-        const uint16_t* src = static_cast<const uint16_t*>(a.data) + base + h * a.sh + 8 * v;
-        uint4 x[kPage];
+    for (int c0 = 0; c0 < nt; c0 += kPage) {
+      const int cp = (t0 + c0) / kPage;  // cache page
+      const int ntc = min(kPage, nt - c0);
+      // a paged cache: the cache page's pool block (clamped), token 0 of it
+      // (a page of 4 or 8 tokens starts inside its block)
+      const int64_t base = a.bt != nullptr
+                               ? static_cast<int64_t>(min(max(a.bt[b * a.bts + cp], 0),
+                                                          a.nblocks - 1)) * a.sb +
+                                     static_cast<int64_t>((t0 + c0) % kPage) * a.d
+                               : b * a.sb + static_cast<int64_t>(t0 + c0) * a.d;
+      const uint16_t* src = static_cast<const uint16_t*>(a.data) + base + h * a.sh + 8 * v;
+      uint4 x[kPage];
 #pragma unroll
-        for (int t = 0; t < kPage; ++t)
-          if (t < ntc)
-            x[t] = __ldcs(reinterpret_cast<const uint4*>(src + static_cast<int64_t>(t) * a.d));
+      for (int t = 0; t < kPage; ++t)
+        if (t < ntc)
+          x[t] = __ldcs(reinterpret_cast<const uint4*>(src + static_cast<int64_t>(t) * a.d));
 #pragma unroll
-        for (int t = 0; t < kPage; ++t) {
-          if (t < ntc) {
-            const uint32_t w[4] = {x[t].x, x[t].y, x[t].z, x[t].w};
+      for (int t = 0; t < kPage; ++t) {
+        if (t < ntc) {
+          const uint32_t w[4] = {x[t].x, x[t].y, x[t].z, x[t].w};
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const uint32_t k = to_key2(w[u]);
-              kmin[u] = __vminu2(kmin[u], k);
-              kmax[u] = __vmaxu2(kmax[u], k);
-            }
-          }
-        }
-      }
-    } else {
-      const uint8_t* src = static_cast<const uint8_t*>(a.data) + b * a.sb + h * a.sh +
-                           static_cast<int64_t>(t0) * (a.d / 2) + 4 * v;
-      const int grp = v / 8;
-      const int ng = a.d / 64;
-      const __half* gmn = static_cast<const __half*>(a.gmin) + b * a.gsb + h * a.gsh +
-                          static_cast<int64_t>(t0) * ng + grp;
-      const __half* gmx = static_cast<const __half*>(a.gmax) + b * a.gsb + h * a.gsh +
-                          static_cast<int64_t>(t0) * ng + grp;
-      // The 8 lanes of one (page, group) -- aligned lanes, v % 8 == lane % 8 --
-      // share the group steps: per chunk of 8 tokens, lane u computes token
-      // u's step and the others take it by shuffle.  A chunk with a tiny
-      // group takes the per-token path.
-      const int sub = threadIdx.x & 7;
-      const unsigned gmask = 0xffu << (threadIdx.x & 24);
-      const __half2 k1024 = __half2half2(__ushort_as_half(0x6400));
-#pragma unroll 1
-      for (int c0 = 0; c0 < nt; c0 += 8) {
-        uint32_t own = 0;  // (mn, step) of token c0 + sub, as a half pair
-        bool tiny = false;
-        if (c0 + sub < nt) {
-          const __half mn = gmn[static_cast<int64_t>(c0 + sub) * ng];
-          const __half mx = gmx[static_cast<int64_t>(c0 + sub) * ng];
-          const float range = q4_range(mn, mx);
-          tiny = range < kQ4TinyRange;
-          own = static_cast<uint32_t>(__half_as_ushort(mn)) |
-                (static_cast<uint32_t>(__half_as_ushort(q4_step16(fmaxf(range, kQ4TinyRange))))
-                 << 16);
-        }
-        if (!__any_sync(gmask, tiny)) {
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            if (c0 + u < nt) {  // the same for the group's 8 lanes
-              const uint32_t ms = __shfl_sync(gmask, own, u, 8);
-              const uint32_t c4 = __ldcs(reinterpret_cast<const uint32_t*>(
-                  src + static_cast<int64_t>(c0 + u) * (a.d / 2)));
-              const __half2 mn2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(ms)));
-              const __half2 st2 =
-                  __half2half2(__ushort_as_half(static_cast<unsigned short>(ms >> 16)));
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const uint32_t byte = (c4 >> (8 * i)) & 0xffu;
-                const uint32_t bits = (byte & 0x0fu) | ((byte & 0xf0u) << 12) | 0x64006400u;
-                const __half2 x = __hfma2(__hsub2(*reinterpret_cast<const __half2*>(&bits), k1024),
-                                          st2, mn2);
-                const uint32_t k = to_key2(*reinterpret_cast<const uint32_t*>(&x));
-                kmin[i] = __vminu2(kmin[i], k);
-                kmax[i] = __vmaxu2(kmax[i], k);
-              }
-            }
-          }
-        } else {
-          for (int t = c0; t < min(nt, c0 + 8); ++t) {
-            const uint32_t c4 = __ldcs(
-                reinterpret_cast<const uint32_t*>(src + static_cast<int64_t>(t) * (a.d / 2)));
-            uint32_t w[4];
-            q4_dequant8(c4, gmn[static_cast<int64_t>(t) * ng], gmx[static_cast<int64_t>(t) * ng],
-                        w);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const uint32_t k = to_key2(w[u]);
-              kmin[u] = __vminu2(kmin[u], k);
-              kmax[u] = __vmaxu2(kmax[u], k);
-            }
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t k = to_key2(w[u]);
+            kmin[u] = __vminu2(kmin[u], k);
+            kmax[u] = __vmaxu2(kmax[u], k);
           }
         }
       }
@@ -160,6 +90,182 @@ __global__ void __launch_bounds__(kMetaThreads, Q4 ? 4 : 2) meta_kernel(const Me
     const int64_t o = pg * a.d + 8 * v;
     *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.meta_min) + o) = omin;
     *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.meta_max) + o) = omax;
+  }
+}
+
+// A 4-bit cache: D/16 lanes per page, lane u owning channels 16u .. 16u + 15
+// (two code words of a token row, one 8-byte load).  One row of blocks per
+// (batch, kv head) (grid y), a warp over 32/(D/16) consecutive pages of it, so
+// every lane of a warp runs the same chunks of 8 tokens (those of the warp's
+// first page; a shorter page's extra tokens are skipped) and full-warp
+// shuffles and votes are safe.  The four lanes of a group share its steps: per
+// chunk each computes two and the others take them by shuffle.  A normal
+// group's levels fl16(c * step + mn) are multiples of 2^-24, so they are never
+// -0 and fp16 min / max (two lanes at a time) is exact on them; the nibble
+// pairs (c, c + 4) of a code word are dequantised together and the order
+// restored once per page.  When a chunk of the warp holds a narrow group (the
+// fp32 step), its pages are taken again from their first token, token by
+// token, on order-preserving keys (-0 below +0).
+template <int D>
+__device__ __forceinline__ void q4_minmax_token(uint2 cw, uint32_t ms, uint32_t (&hmin)[8],
+                                                uint32_t (&hmax)[8]) {
+  const __half2 k1024 = __half2half2(__ushort_as_half(0x6400));
+  const __half2 mn2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(ms)));
+  const __half2 st2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(ms >> 16)));
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const uint32_t w = j ? cw.y : cw.x;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t bits = ((w >> (4 * i)) & 0x000f000fu) | 0x64006400u;
+      const __half2 x =
+          __hfma2(__hsub2(*reinterpret_cast<const __half2*>(&bits), k1024), st2, mn2);
+      __half2 lo2 = *reinterpret_cast<const __half2*>(&hmin[4 * j + i]);
+      __half2 hi2 = *reinterpret_cast<const __half2*>(&hmax[4 * j + i]);
+      lo2 = __hmin2(lo2, x);
+      hi2 = __hmax2(hi2, x);
+      hmin[4 * j + i] = *reinterpret_cast<const uint32_t*>(&lo2);
+      hmax[4 * j + i] = *reinterpret_cast<const uint32_t*>(&hi2);
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kMetaThreads, 3) meta_q4_kernel(const MetaArgs a) {
+  griddep_launch_dependents();
+  griddep_wait();
+  constexpr int LPP = D / 16;  // lanes per page
+  constexpr int NG = D / 64;   // groups per token row
+  constexpr unsigned kFull = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  const int u = lane % LPP, g = u >> 2;
+  const int lin = blockIdx.x * blockDim.x + threadIdx.x;
+  const int wpage = (lin - lane) / LPP;  // the warp's first page slot
+  for (int bh = blockIdx.y; bh < a.B * a.Hkv; bh += gridDim.y) {
+    const int h = bh % a.Hkv, b = bh / a.Hkv;
+    const int Nb = seq_len_of(a.lens, b, a.N);
+    // page slot -> page: every page, or (last_only) slot 0 is the newest token's page
+    const int slot = lin / LPP;
+    const int last = (Nb - 1) / a.S;
+    const bool live = a.last_only ? slot == 0 : slot < a.P;
+    const int page = a.last_only ? last : slot;
+    const int nt = live ? max(0, min(a.S, Nb - page * a.S)) : 0;
+    // tokens of the warp's first and last pages (pages are consecutive)
+    const int wfirst = a.last_only ? (wpage == 0 ? last : a.P) : wpage;
+    const int wlast = a.last_only ? wfirst : wpage + 32 / LPP - 1;
+    const int nt_first = wfirst < a.P ? max(0, min(a.S, Nb - wfirst * a.S)) : 0;
+    const int nt_last = wlast < a.P ? max(0, min(a.S, Nb - wlast * a.S)) : 0;
+    const int t0 = page * a.S;
+    const uint8_t* src = static_cast<const uint8_t*>(a.data) + b * a.sb + h * a.sh +
+                         static_cast<int64_t>(t0) * (D / 2) + 8 * u;
+    const int64_t goff = b * a.gsb + h * a.gsh + static_cast<int64_t>(t0) * NG + g;
+    const __half* gmn = static_cast<const __half*>(a.gmin) + goff;
+    const __half* gmx = static_cast<const __half*>(a.gmax) + goff;
+    uint32_t omin[8], omax[8];
+    bool narrow_page = false;
+    {
+      uint32_t hmin[8], hmax[8];  // fp16 pairs (c, c + 4) of each code word
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        hmin[i] = 0x7c007c00u;  // +inf
+        hmax[i] = 0xfc00fc00u;  // -inf
+      }
+#pragma unroll 1
+      for (int c0 = 0; c0 < nt_first; c0 += 8) {
+        const bool full = c0 + 8 <= nt_last;  // every page of the warp: a whole chunk
+        uint2 cw[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (full || c0 + k < nt)
+            cw[k] = __ldcs(reinterpret_cast<const uint2*>(src + static_cast<int64_t>(c0 + k) *
+                                                                    (D / 2)));
+        uint32_t own[2];  // (mn, step) of tokens c0 + 2 (u & 3) + e, as a half pair
+        bool narrow = false;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int t = c0 + 2 * (u & 3) + e;
+          own[e] = 0u;
+          if (t < nt) {
+            const __half mn = gmn[static_cast<int64_t>(t) * NG];
+            const __half mx = gmx[static_cast<int64_t>(t) * NG];
+            const float range = q4_range(mn, mx);
+            narrow |= range < kQ4TinyRange;
+            own[e] = static_cast<uint32_t>(__half_as_ushort(mn)) |
+                     (static_cast<uint32_t>(
+                          __half_as_ushort(q4_step16(fmaxf(range, kQ4TinyRange))))
+                      << 16);
+          }
+        }
+        if (__any_sync(kFull, narrow)) {
+          narrow_page = true;
+          break;
+        }
+        uint32_t ms[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) ms[k] = __shfl_sync(kFull, own[k & 1], k >> 1, 4);
+        if (full) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) q4_minmax_token<D>(cw[k], ms[k], hmin, hmax);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            if (c0 + k < nt) q4_minmax_token<D>(cw[k], ms[k], hmin, hmax);
+        }
+      }
+      // pairs (c0, c4) (c1, c5) (c2, c6) (c3, c7) -> (c0, c1) (c2, c3) (c4, c5) (c6, c7)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const uint32_t* pn = hmin + 4 * j;
+        const uint32_t* px = hmax + 4 * j;
+        omin[4 * j] = __byte_perm(pn[0], pn[1], 0x5410u);
+        omin[4 * j + 1] = __byte_perm(pn[2], pn[3], 0x5410u);
+        omin[4 * j + 2] = __byte_perm(pn[0], pn[1], 0x7632u);
+        omin[4 * j + 3] = __byte_perm(pn[2], pn[3], 0x7632u);
+        omax[4 * j] = __byte_perm(px[0], px[1], 0x5410u);
+        omax[4 * j + 1] = __byte_perm(px[2], px[3], 0x5410u);
+        omax[4 * j + 2] = __byte_perm(px[0], px[1], 0x7632u);
+        omax[4 * j + 3] = __byte_perm(px[2], px[3], 0x7632u);
+      }
+    }
+    if (nt == 0) continue;  // no page here (after the warp's shuffles and votes)
+    if (narrow_page) {
+      // the whole page again, token by token, on order-preserving keys
+      uint32_t kmin[8], kmax[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        kmin[i] = 0xffffffffu;
+        kmax[i] = 0u;
+      }
+      for (int t = 0; t < nt; ++t) {
+        const uint2 c =
+            __ldcs(reinterpret_cast<const uint2*>(src + static_cast<int64_t>(t) * (D / 2)));
+        const __half mn = gmn[static_cast<int64_t>(t) * NG];
+        const __half mx = gmx[static_cast<int64_t>(t) * NG];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          uint32_t w[4];
+          q4_dequant8(j ? c.y : c.x, mn, mx, w);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t k = to_key2(w[i]);
+            kmin[4 * j + i] = __vminu2(kmin[4 * j + i], k);
+            kmax[4 * j + i] = __vmaxu2(kmax[4 * j + i], k);
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        omin[i] = from_key2(kmin[i]);
+        omax[i] = from_key2(kmax[i]);
+      }
+    }
+    const int64_t pg = static_cast<int64_t>(bh) * a.P + page;
+    uint4* dmin = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.meta_min) + pg * D + 16 * u);
+    uint4* dmax = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.meta_max) + pg * D + 16 * u);
+    dmin[0] = make_uint4(omin[0], omin[1], omin[2], omin[3]);
+    dmin[1] = make_uint4(omin[4], omin[5], omin[6], omin[7]);
+    dmax[0] = make_uint4(omax[0], omax[1], omax[2], omax[3]);
+    dmax[1] = make_uint4(omax[4], omax[5], omax[6], omax[7]);
   }
 }
 
@@ -481,8 +587,14 @@ cudaError_t launch_meta(bool q4, bool f16, const MetaArgs& a, cudaStream_t s) {
   const int64_t work =
       static_cast<int64_t>(a.B) * a.Hkv * (a.last_only ? 1 : a.P) * (a.d / 8);
   const dim3 grid(grid_for(work, kMetaThreads)), block(kMetaThreads);
-  return q4 ? launch_pdl(meta_kernel<true>, grid, block, 0, s, a)
-            : launch_pdl(meta_kernel<false>, grid, block, 0, s, a);
+  if (!q4) return launch_pdl(meta_kernel, grid, block, 0, s, a);
+  // one row of blocks per (batch, kv head): the row's pages, d/16 lanes each
+  const int64_t row = static_cast<int64_t>(a.last_only ? 1 : a.P) * (a.d / 16);
+  const int64_t rows = static_cast<int64_t>(a.B) * a.Hkv;
+  const dim3 grid4(static_cast<unsigned>(ceil_div(row, kMetaThreads)),
+                   static_cast<unsigned>(rows < 65535 ? rows : 65535));
+  return a.d == 128 ? launch_pdl(meta_q4_kernel<128>, grid4, block, 0, s, a)
+                    : launch_pdl(meta_q4_kernel<64>, grid4, block, 0, s, a);
 }
 
 cudaError_t launch_meta8(bool f16, const Meta8Args& a, cudaStream_t s) {

@@ -273,6 +273,47 @@ def test_q4_meta_bit_exact(dev, dkv):
     assert np.array_equal(bits(mx.cpu()), omx)
 
 
+@pytest.mark.parametrize("S", [4, 8, 16, 32, 64])
+@pytest.mark.parametrize("d", [64, 128])
+def test_q4_meta_page_sizes_lengths_and_append(S, d, dev, dkv):
+    # Metadata of a 4-bit cache for every page size, sequences of different
+    # lengths (ragged last pages, one shorter than a page) and rows of narrow
+    # groups (the fp32 step, some straddling zero) in two of the sequences, so
+    # that pages take both the fp16 min / max and the key path; then each
+    # sequence's last page rebuilt alone (kv_meta_append) over a spoiled copy.
+    w = Workload(f"q4m-s{S}", B=3, Hq=2, Hkv=2, d=d, N=1000, dtype="fp16")
+    _, K, _ = make_inputs(w, seed=97 + S + d)
+    g = torch.Generator().manual_seed(S + d)
+    u = 2.0 ** -24
+    for b in (0, 2):
+        for h in range(w.Hkv):
+            rows = torch.randint(0, w.N, (12,), generator=g)
+            span = torch.randint(1, 400, (12, 1), generator=g).float()
+            base = torch.randint(-300, 300, (12, 1), generator=g).float()
+            K[b, h, rows] = ((base + torch.floor(torch.rand(12, w.d, generator=g) * span)) * u).to(K.dtype)
+    lens = [1000, 3, 517]
+    L = torch.tensor(lens, dtype=torch.int32, device=dev)
+    q4 = dkv.kv_quant4(K.to(dev).contiguous())
+    meta = dkv.kv_meta_build(q4, page_size=S, seq_lens=L)
+    kh = oracle.dequant4(*oracle.quant4(bits(K)))
+    want = []
+    for b, n in enumerate(lens):
+        P = (n + S - 1) // S
+        omn, omx = oracle.meta(kh[b:b + 1, :, :n], S, 1)
+        assert np.array_equal(bits(meta[0][b:b + 1, :, :P].cpu()), omn), f"min, sequence {b}"
+        assert np.array_equal(bits(meta[1][b:b + 1, :, :P].cpu()), omx), f"max, sequence {b}"
+        want.append((P, omn, omx))
+    spoiled = tuple(m.clone() for m in meta)
+    for b, n in enumerate(lens):
+        last = (n - 1) // S
+        for m in spoiled:
+            m[b, :, last] = 7.0
+    dkv.kv_meta_append(q4, spoiled, page_size=S, seq_lens=L)
+    for b, (P, omn, omx) in enumerate(want):
+        assert np.array_equal(bits(spoiled[0][b:b + 1, :, :P].cpu()), omn), f"append min {b}"
+        assert np.array_equal(bits(spoiled[1][b:b + 1, :, :P].cpu()), omx), f"append max {b}"
+
+
 # 4-bit caches: contiguous group bounds need N * d / 64 to be a multiple of 8
 # (16-byte head strides); every case still ends in a ragged page.
 Q4_CASES = [
