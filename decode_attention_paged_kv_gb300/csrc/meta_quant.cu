@@ -106,27 +106,37 @@ __global__ void __launch_bounds__(kMetaThreads, 2) meta_kernel(const MetaArgs a)
 // restored once per page.  When a chunk of the warp holds a narrow group (the
 // fp32 step), its pages are taken again from their first token, token by
 // token, on order-preserving keys (-0 below +0).
-template <int D>
+// One token's 16 channels into the running fp16 min / max.  Nibble pairs
+// (c, c + 4) of a code word become exact fp16 codes by the exponent trick:
+// bits 0-3 under 1024.0 (ulp 1) and bits 4-7 under 64.0 (ulp 1/16) give
+// 1024 + c and 64 + c, so one shift of the word by 8 and four masks reach all
+// four pairs; then c = that - 1024 (or - 64) and fl16(c step + mn), one fused
+// rounding as the format defines.  All on packed registers.
+__device__ __forceinline__ uint32_t h2_level(uint32_t bits, uint32_t bias, uint32_t st2,
+                                            uint32_t mn2) {
+  uint32_t c, x;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(c) : "r"(bits), "r"(bias));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(x) : "r"(c), "r"(st2), "r"(mn2));
+  return x;
+}
+__device__ __forceinline__ void h2_minmax(uint32_t& lo, uint32_t& hi, uint32_t x) {
+  asm("min.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(x));
+  asm("max.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(x));
+}
 __device__ __forceinline__ void q4_minmax_token(uint2 cw, uint32_t ms, uint32_t (&hmin)[8],
                                                 uint32_t (&hmax)[8]) {
-  const __half2 k1024 = __half2half2(__ushort_as_half(0x6400));
-  const __half2 mn2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(ms)));
-  const __half2 st2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(ms >> 16)));
+  const uint32_t mn2 = __byte_perm(ms, 0u, 0x1010u), st2 = __byte_perm(ms, 0u, 0x3232u);
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
-    const uint32_t w = j ? cw.y : cw.x;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t bits = ((w >> (4 * i)) & 0x000f000fu) | 0x64006400u;
-      const __half2 x =
-          __hfma2(__hsub2(*reinterpret_cast<const __half2*>(&bits), k1024), st2, mn2);
-      __half2 lo2 = *reinterpret_cast<const __half2*>(&hmin[4 * j + i]);
-      __half2 hi2 = *reinterpret_cast<const __half2*>(&hmax[4 * j + i]);
-      lo2 = __hmin2(lo2, x);
-      hi2 = __hmax2(hi2, x);
-      hmin[4 * j + i] = *reinterpret_cast<const uint32_t*>(&lo2);
-      hmax[4 * j + i] = *reinterpret_cast<const uint32_t*>(&hi2);
-    }
+    const uint32_t w = j ? cw.y : cw.x, w8 = w >> 8;
+    h2_minmax(hmin[4 * j], hmax[4 * j],
+              h2_level((w & 0x000f000fu) | 0x64006400u, 0x64006400u, st2, mn2));
+    h2_minmax(hmin[4 * j + 1], hmax[4 * j + 1],
+              h2_level((w & 0x00f000f0u) | 0x54005400u, 0x54005400u, st2, mn2));
+    h2_minmax(hmin[4 * j + 2], hmax[4 * j + 2],
+              h2_level((w8 & 0x000f000fu) | 0x64006400u, 0x64006400u, st2, mn2));
+    h2_minmax(hmin[4 * j + 3], hmax[4 * j + 3],
+              h2_level((w8 & 0x00f000f0u) | 0x54005400u, 0x54005400u, st2, mn2));
   }
 }
 
@@ -205,11 +215,11 @@ __global__ void __launch_bounds__(kMetaThreads, 3) meta_q4_kernel(const MetaArgs
         for (int k = 0; k < 8; ++k) ms[k] = __shfl_sync(kFull, own[k & 1], k >> 1, 4);
         if (full) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) q4_minmax_token<D>(cw[k], ms[k], hmin, hmax);
+          for (int k = 0; k < 8; ++k) q4_minmax_token(cw[k], ms[k], hmin, hmax);
         } else {
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            if (c0 + k < nt) q4_minmax_token<D>(cw[k], ms[k], hmin, hmax);
+            if (c0 + k < nt) q4_minmax_token(cw[k], ms[k], hmin, hmax);
         }
       }
       // pairs (c0, c4) (c1, c5) (c2, c6) (c3, c7) -> (c0, c1) (c2, c3) (c4, c5) (c6, c7)
