@@ -477,15 +477,14 @@ __global__ void __launch_bounds__(kMetaThreads) meta8_kernel(const Meta8Args a) 
   constexpr int CPL = D / 8;  // channels per lane
   const int lane = threadIdx.x & 31, u = lane & 7;
   const unsigned gmask = 0xffu << (lane & 24);
-  // (page counts below 2^31, checked by the host: 32-bit index arithmetic)
-  const uint32_t total = static_cast<uint32_t>(a.B) * a.Hkv * a.P;
-  const uint32_t per_b = static_cast<uint32_t>(a.Hkv) * a.P;
-  const uint32_t gstride = gridDim.x * (blockDim.x >> 3);
-  for (uint32_t pg = (blockIdx.x * blockDim.x + threadIdx.x) >> 3; pg < total; pg += gstride) {
-    const int j = static_cast<int>(pg % static_cast<uint32_t>(a.P));
-    const int b = static_cast<int>(pg / per_b);
-    if (static_cast<int64_t>(j) * a.S >= seq_len_of(a.lens, b, a.N)) continue;  // the 8 lanes alike
-    const int64_t off = static_cast<int64_t>(pg) * D + CPL * u;
+  // one row of blocks per (batch, kv head) (grid y), 8 lanes a page along it
+  const int j = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 3);
+  for (int bh = blockIdx.y; bh < a.B * a.Hkv; bh += gridDim.y) {
+    const int b = bh / a.Hkv;
+    if (j >= a.P || static_cast<int64_t>(j) * a.S >= seq_len_of(a.lens, b, a.N))
+      continue;  // the 8 lanes alike
+    const int64_t pg = static_cast<int64_t>(bh) * a.P + j;
+    const int64_t off = pg * D + CPL * u;
     uint32_t wm[CPL / 2], wM[CPL / 2];
 #pragma unroll
     for (int v = 0; v < CPL / 8; ++v) {
@@ -608,8 +607,11 @@ cudaError_t launch_meta(bool q4, bool f16, const MetaArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_meta8(bool f16, const Meta8Args& a, cudaStream_t s) {
-  const int64_t pages = static_cast<int64_t>(a.B) * a.Hkv * a.P;  // 8 threads a page
-  const dim3 grid(grid_for(pages * 8, kMetaThreads)), block(kMetaThreads);
+  // one row of blocks per (batch, kv head): its pages, 8 threads each
+  const int64_t rows = static_cast<int64_t>(a.B) * a.Hkv;
+  const dim3 grid(static_cast<unsigned>(ceil_div(static_cast<int64_t>(a.P) * 8, kMetaThreads)),
+                  static_cast<unsigned>(rows < 65535 ? rows : 65535));
+  const dim3 block(kMetaThreads);
   if (a.d == 128)
     return f16 ? launch_pdl(meta8_kernel<128, true>, grid, block, 0, s, a)
                : launch_pdl(meta8_kernel<128, false>, grid, block, 0, s, a);

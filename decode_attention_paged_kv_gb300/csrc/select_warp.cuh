@@ -73,18 +73,20 @@ __device__ uint32_t warp_threshold(const uint32_t (&k)[NK], int lo, int hi, int&
 }
 
 // Top-kk of one head's P keys (key_at(j): the order-preserving key of page j;
-// 1 <= kk <= P <= kUnitMaxP) by one warp: writes the selection bitmap words
-// bm[0 .. ceil(P / 32)).  kmax / kmin: the largest and smallest of the keys.
-template <class KeyAt>
-__device__ void warp_topk_head(const KeyAt& key_at, int P, int kk, uint32_t* bm, uint32_t kmax,
-                               uint32_t kmin) {
+// 1 <= kk <= P <= 32 NK) by one warp, NK key slots a lane: writes the
+// selection bitmap words bm[0 .. ceil(P / 32)).  kmax / kmin: the largest and
+// smallest of the keys.
+template <int NK, class KeyAt>
+__device__ void warp_topk_head_n(const KeyAt& key_at, int P, int kk, uint32_t* bm, uint32_t kmax,
+                                 uint32_t kmin) {
+  static_assert(NK % 8 == 0 && NK <= kSelKeys, "eight ballots at a time");
   const int lane = threadIdx.x & 31;
   const uint32_t lt = (1u << lane) - 1u;
   const int nr = static_cast<int>(ceil_div(P, 32));         // key rows
   const int nv = static_cast<int>(ceil_div(P - lane, 32));  // this lane's valid rows
-  uint32_t key[kSelKeys];
+  uint32_t key[NK];
 #pragma unroll
-  for (int i = 0; i < kSelKeys; ++i) key[i] = i < nv ? key_at(32 * i + lane) : 0u;
+  for (int i = 0; i < NK; ++i) key[i] = i < nv ? key_at(32 * i + lane) : 0u;
   // The kk-th largest key T, bit by bit below the common prefix (keys past P
   // read as 0 and stay below every candidate when the prefix is not 0).
   int ge = -1;
@@ -99,7 +101,7 @@ __device__ void warp_topk_head(const KeyAt& key_at, int P, int kk, uint32_t* bm,
   if (ge == kk) {
     // No tie at T: the selection is every key >= T (eight ballots at a time).
 #pragma unroll
-    for (int g = 0; g < kSelKeys / 8; ++g) {
+    for (int g = 0; g < NK / 8; ++g) {
       if (8 * g < nr) {
         uint32_t m8[8];
 #pragma unroll
@@ -119,12 +121,12 @@ __device__ void warp_topk_head(const KeyAt& key_at, int P, int kk, uint32_t* bm,
   T = warp_threshold(key, kk, kk, ge);
   int gt = 0;
 #pragma unroll
-  for (int i = 0; i < kSelKeys; ++i)
+  for (int i = 0; i < NK; ++i)
     if (i < nr) gt += __popc(__ballot_sync(0xffffffffu, i < nv && key[i] > T));
   const int need = kk - gt;  // keys equal to T to take, lowest pages first
   int eq_before = 0;
 #pragma unroll
-  for (int i = 0; i < kSelKeys; ++i) {
+  for (int i = 0; i < NK; ++i) {
     if (i < nr) {
       const bool is_gt = i < nv && key[i] > T, is_eq = i < nv && key[i] == T;
       const uint32_t eqm = __ballot_sync(0xffffffffu, is_eq);
@@ -134,6 +136,19 @@ __device__ void warp_topk_head(const KeyAt& key_at, int P, int kk, uint32_t* bm,
       eq_before += __popc(eqm);
     }
   }
+}
+
+// The same with as few key slots a lane as P needs (every count touches every
+// slot, so short heads run on 16 or 32).
+template <class KeyAt>
+__device__ void warp_topk_head(const KeyAt& key_at, int P, int kk, uint32_t* bm, uint32_t kmax,
+                               uint32_t kmin) {
+  if (P <= 16 * 32)
+    warp_topk_head_n<16>(key_at, P, kk, bm, kmax, kmin);
+  else if (P <= 32 * 32)
+    warp_topk_head_n<32>(key_at, P, kk, bm, kmax, kmin);
+  else
+    warp_topk_head_n<kSelKeys>(key_at, P, kk, bm, kmax, kmin);
 }
 
 // Ascending page rows from a head's selection bitmap (words [0, W)); the words
