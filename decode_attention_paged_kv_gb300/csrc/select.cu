@@ -1032,12 +1032,14 @@ constexpr int kUnitConsumers = 8;
 constexpr int kUnitThreads = (kUnitConsumers + 1) * 32;
 constexpr int kUnitBoxPages = 64;
 
-template <int D, bool M8 = false>
+// TWO: two CTAs a streaming multiprocessor (for more units than SMs), each with
+// half the ring, so the SM keeps the same bytes in flight.
+template <int D, bool M8 = false, bool TWO = false>
 struct UnitCfg {
   // one of [M] / [m] (16-bit), or of the code bytes [cM] / [cm] (8-bit)
   static constexpr int kBoxBytes = kUnitBoxPages * D * (M8 ? 1 : 2);
   static constexpr int kStageBytes = 2 * kBoxBytes;
-  static constexpr int kStages = (128 * 1024) / kStageBytes;  // 128 KiB in flight
+  static constexpr int kStages = ((TWO ? 64 : 128) * 1024) / kStageBytes;  // bytes in flight
   static constexpr int kBarOffset = kStages * kStageBytes;
   static constexpr int kKeysOffset = kBarOffset + 2 * kStages * 8 + 16;  // + abort flag
 };
@@ -1072,11 +1074,11 @@ __device__ __forceinline__ void union_sync() {
 
 // M8: the scores come from 8-bit metadata (codes in the boxes, lo / step per
 // page from global memory).
-template <int D, bool F16, bool M8>
-__global__ void __launch_bounds__(kUnitThreads, 1)
+template <int D, bool F16, bool M8, bool TWO = false>
+__global__ void __launch_bounds__(kUnitThreads, TWO ? 2 : 1)
     unit_select_kernel(const UnitSelectArgs a, const __grid_constant__ CUtensorMap mmx,
                        const __grid_constant__ CUtensorMap mmn) {
-  using C = UnitCfg<D, M8>;
+  using C = UnitCfg<D, M8, TWO>;
   extern __shared__ uint8_t usm_raw[];
   uint8_t* usm = usm_raw + ((1024u - (smem_u32(usm_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(usm);
@@ -1536,34 +1538,59 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s) {
   return launch_pdl(topk_kernel<false>, dim3(a.rows), dim3(kSelMaxThreads), 0, s, a);
 }
 
-size_t unit_select_smem(int d, bool m8, int G, int P) {
-  const size_t keys_off =
-      d == 128 ? (m8 ? UnitCfg<128, true>::kKeysOffset : UnitCfg<128>::kKeysOffset)
-               : (m8 ? UnitCfg<64, true>::kKeysOffset : UnitCfg<64>::kKeysOffset);
-  return 1024 + keys_off + static_cast<size_t>(G) * P * 4 +
+namespace {
+template <int D, bool M8, bool TWO>
+size_t unit_smem_t(int G, int P) {
+  return 1024 + UnitCfg<D, M8, TWO>::kKeysOffset + static_cast<size_t>(G) * P * 4 +
          static_cast<size_t>(G) * kSelBitmapWords * 4 + 32 * 4;
+}
+// Shared memory a CTA may take when two share a multiprocessor.
+constexpr size_t kUnitTwoSmemLimit = 112 * 1024;
+
+template <int D, bool F16, bool M8, bool TWO>
+cudaError_t launch_unit_t(const UnitSelectArgs& a, const CUtensorMap& mmx, const CUtensorMap& mmn,
+                          int grid, cudaStream_t s) {
+  const size_t smem = unit_smem_t<D, M8, TWO>(a.G, a.P);
+  auto kern = unit_select_kernel<D, F16, M8, TWO>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  return launch_pdl(kern, dim3(grid), dim3(kUnitThreads), smem, s, a, mmx, mmn);
+}
+}  // namespace
+
+size_t unit_select_smem(int d, bool m8, int G, int P) {
+  return d == 128 ? (m8 ? unit_smem_t<128, true, false>(G, P) : unit_smem_t<128, false, false>(G, P))
+                  : (m8 ? unit_smem_t<64, true, false>(G, P) : unit_smem_t<64, false, false>(G, P));
 }
 
 cudaError_t launch_unit_select(int d, bool f16, bool m8, const UnitSelectArgs& a,
                                const CUtensorMap& mmx, const CUtensorMap& mmn, cudaStream_t s) {
-  const size_t smem = unit_select_smem(d, m8, a.G, a.P);
   // One CTA per SM at most (a CTA takes most of an SM's shared memory), each
   // taking units blockIdx.x, + gridDim.x, ...: with fewer CTAs the metadata
   // scan streams from too few SMs (measured: 64, 80, 96, 112 CTAs for 128
-  // units were slower than 128).
+  // units were slower than 128).  With more units than SMs at d = 64, two
+  // CTAs of half the ring share each SM, so every unit starts at once.
   const int units = a.B * a.Hkv;
-  const dim3 grid(units < a.num_sms ? units : a.num_sms), block(kUnitThreads);
-  auto kern =
-      m8 ? (d == 128
-                ? (f16 ? unit_select_kernel<128, true, true> : unit_select_kernel<128, false, true>)
-                : (f16 ? unit_select_kernel<64, true, true> : unit_select_kernel<64, false, true>))
-         : (d == 128
-                ? (f16 ? unit_select_kernel<128, true, false> : unit_select_kernel<128, false, false>)
-                : (f16 ? unit_select_kernel<64, true, false> : unit_select_kernel<64, false, false>));
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  return launch_pdl(kern, grid, block, smem, s, a, mmx, mmn);
+  if (d == 64 && units > a.num_sms &&
+      (m8 ? unit_smem_t<64, true, true>(a.G, a.P) : unit_smem_t<64, false, true>(a.G, a.P)) <=
+          kUnitTwoSmemLimit) {
+    const int grid = units < 2 * a.num_sms ? units : 2 * a.num_sms;
+    return m8 ? (f16 ? launch_unit_t<64, true, true, true>(a, mmx, mmn, grid, s)
+                     : launch_unit_t<64, false, true, true>(a, mmx, mmn, grid, s))
+              : (f16 ? launch_unit_t<64, true, false, true>(a, mmx, mmn, grid, s)
+                     : launch_unit_t<64, false, false, true>(a, mmx, mmn, grid, s));
+  }
+  const int grid = units < a.num_sms ? units : a.num_sms;
+  if (d == 128)
+    return m8 ? (f16 ? launch_unit_t<128, true, true, false>(a, mmx, mmn, grid, s)
+                     : launch_unit_t<128, false, true, false>(a, mmx, mmn, grid, s))
+              : (f16 ? launch_unit_t<128, true, false, false>(a, mmx, mmn, grid, s)
+                     : launch_unit_t<128, false, false, false>(a, mmx, mmn, grid, s));
+  return m8 ? (f16 ? launch_unit_t<64, true, true, false>(a, mmx, mmn, grid, s)
+                   : launch_unit_t<64, false, true, false>(a, mmx, mmn, grid, s))
+            : (f16 ? launch_unit_t<64, true, false, false>(a, mmx, mmn, grid, s)
+                   : launch_unit_t<64, false, false, false>(a, mmx, mmn, grid, s));
 }
 
 cudaError_t launch_union(const UnionArgs& a, int units, cudaStream_t s) {

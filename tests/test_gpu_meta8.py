@@ -46,6 +46,9 @@ CASES = [
      False),
     (Workload("m8-mha-d64-fp16", B=3, Hq=4, Hkv=4, d=64, N=3001, top_k=12, dtype="fp16"),
      None, False),
+    # 192 units at d = 64: more units than multiprocessors, two selection CTAs a one
+    (Workload("m8-many-units-d64", B=8, Hq=24, Hkv=24, d=64, N=4200, top_k=20, kind="offset"),
+     None, False),
     (Workload("m8-offset-s32-group", B=2, Hq=8, Hkv=2, d=128, N=9000, S=32, top_k=20,
               kind="offset"), None, True),
     (Workload("m8-lens-s8", B=3, Hq=8, Hkv=2, d=128, N=2500, S=8, top_k=40, kind="hot"),
