@@ -352,8 +352,9 @@ __device__ __forceinline__ void search_sync() {
   asm volatile("bar.sync 3, %0;" ::"r"(kSearchWarps * 32) : "memory");
 }
 
-// Block top-K of P >= kSampleMinP keys staged in shared memory (`keys`, zero
-// from P up to a multiple of 4) by a sample bracket.  1024 keys, one from each
+// Block top-K of P >= kSampleMinP keys (load4(q): keys 4 q .. 4 q + 3, zero
+// from P up to a multiple of 4; staged in shared memory or read from the
+// score row) by a sample bracket.  1024 keys, one from each
 // of 1024 equal windows, give two splitters lo < hi between which the kk-th
 // largest key most likely lies: the sample ranks of that key's expected
 // place, kk * 1024 / P, minus and plus three binomial standard deviations and
@@ -367,7 +368,8 @@ __device__ __forceinline__ void search_sync() {
 // the selection is the same exact one either way.  Output as
 // block_radix_select, plus block_emit's per-warp counts in sc.warp_gt and
 // sc.warp_eq (the passes walk the keys in block_emit's warp ranges).
-__device__ bool block_sample_select(const uint32_t* keys, int P, int kk, SelScratch& sc,
+template <typename Load4>
+__device__ bool block_sample_select(const Load4& load4, int P, int kk, SelScratch& sc,
                                     uint32_t& prefix, uint32_t& mask, int& need) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t* wcnt = sc.hist;               // per-warp bucket counts
@@ -376,7 +378,6 @@ __device__ bool block_sample_select(const uint32_t* keys, int P, int kk, SelScra
   const uint32_t hi = split[0], lo = max(split[1], 1u);
   // pass 1: keys >= hi and keys in [lo, hi) (zero padding is below both);
   // warp w takes the keys block_emit gives it, four at a time
-  const uint4* k4 = reinterpret_cast<const uint4*>(keys);
   const int span = emit_span(P);
   const int q0 = (warp * span) >> 2, q1 = (min(P, warp * span + span) + 3) >> 2;
   int below_hi = 0, inb = 0, seen = 0;
@@ -386,7 +387,7 @@ __device__ bool block_sample_select(const uint32_t* keys, int P, int kk, SelScra
     inb += bl - bh;
   };
   for (int j = q0 + lane; j < q1; j += 32) {
-    const uint4 v = k4[j];
+    const uint4 v = load4(j);
     tally(v.x);
     tally(v.y);
     tally(v.z);
@@ -417,7 +418,7 @@ __device__ bool block_sample_select(const uint32_t* keys, int P, int kk, SelScra
     at += in ? 1 : 0;
   };
   for (int j = q0 + lane; j < q1; j += 32) {
-    const uint4 v = k4[j];
+    const uint4 v = load4(j);
     put(v.x);
     put(v.y);
     put(v.z);
@@ -573,12 +574,12 @@ __device__ void block_emit_counts(const KeyFn& key, int P, uint32_t prefix, uint
 // Writes the selection in ascending page order to sel_row[0 .. kk) and its
 // bitmap to bits[0 .. ceil(P / 32)), given the per-warp counts in
 // sc.warp_gt / sc.warp_eq.  Warp w walks its range 256 keys at a time; the
-// counts of the warps before it place it.  skeys: the keys staged in shared
-// memory (zero-padded to a multiple of 4), or nullptr to read them by key().
-// Without a partial tie (no key equal to the prefix is left out) a page is
-// selected by its own key alone.
-template <typename KeyFn>
-__device__ void block_emit(const KeyFn& key, const uint32_t* skeys, int P, uint32_t prefix,
+// counts of the warps before it place it.  load4(q): keys 4 q .. 4 q + 3 (zero
+// from P up to a multiple of 4), called for q < ceil(P / 4) only.  Without a
+// partial tie (no key equal to the prefix is left out) a page is selected by
+// its own key alone.
+template <typename KeyFn, typename Load4>
+__device__ void block_emit(const KeyFn& key, const Load4& load4, int P, uint32_t prefix,
                            uint32_t mask, int need, int32_t* sel_row, uint32_t* bits,
                            SelScratch& sc) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -594,26 +595,21 @@ __device__ void block_emit(const KeyFn& key, const uint32_t* skeys, int P, uint3
     const uint32_t cut = need == 0 ? prefix + 1u : prefix;  // selected: key & mask >= cut
     // lane l takes the 8 keys base + 8 l .. base + 8 l + 7: one count, one
     // warp scan and one bitmap byte a lane per 256 keys
-    const int pad = 4 * static_cast<int>(ceil_div(P, 4));  // staged keys (zero-padded)
+    const int pad = 4 * static_cast<int>(ceil_div(P, 4));  // keys with zero padding
     for (int base = j0; base < j1; base += 256) {
-      const int jb = base + 8 * lane;
+      const int jb = base + 8 * lane;  // a multiple of 8
       uint32_t k[8];
-      if (skeys != nullptr) {
-        const uint4 z = make_uint4(0, 0, 0, 0);
-        const uint4 a4 = jb + 4 <= pad ? *reinterpret_cast<const uint4*>(skeys + jb) : z;
-        const uint4 b4 = jb + 8 <= pad ? *reinterpret_cast<const uint4*>(skeys + jb + 4) : z;
-        k[0] = a4.x;
-        k[1] = a4.y;
-        k[2] = a4.z;
-        k[3] = a4.w;
-        k[4] = b4.x;
-        k[5] = b4.y;
-        k[6] = b4.z;
-        k[7] = b4.w;
-      } else {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) k[u] = jb + u < j1 ? key(jb + u) : 0u;
-      }
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      const uint4 a4 = jb + 4 <= pad ? load4(jb >> 2) : z;
+      const uint4 b4 = jb + 8 <= pad ? load4((jb >> 2) + 1) : z;
+      k[0] = a4.x;
+      k[1] = a4.y;
+      k[2] = a4.z;
+      k[3] = a4.w;
+      k[4] = b4.x;
+      k[5] = b4.y;
+      k[6] = b4.z;
+      k[7] = b4.w;
       uint32_t m8 = 0u;
 #pragma unroll
       for (int u = 0; u < 8; ++u) m8 |= (jb + u < j1 && (k[u] & mask) >= cut) ? 1u << u : 0u;
@@ -911,6 +907,23 @@ __global__ void __launch_bounds__(kSelMaxThreads) topk_kernel(const TopkArgs a) 
     if constexpr (SMEM) return s_keys[j];
     return score_key(score(j));
   };
+  // keys 4 q .. 4 q + 3, zero from Pb on: staged, or from the score row (one
+  // 16-byte load when the row is one head's and 16-byte aligned)
+  const bool vec_row = a.group == 1 && (a.P & 3) == 0;
+  auto load4 = [&](int q) -> uint4 {
+    if constexpr (SMEM) return *reinterpret_cast<const uint4*>(s_keys + 4 * q);
+    uint4 k;
+    if (vec_row && 4 * q + 3 < Pb) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(r) + q);
+      k = make_uint4(score_key(v.x), score_key(v.y), score_key(v.z), score_key(v.w));
+    } else {
+      k.x = 4 * q < Pb ? key(4 * q) : 0u;
+      k.y = 4 * q + 1 < Pb ? key(4 * q + 1) : 0u;
+      k.z = 4 * q + 2 < Pb ? key(4 * q + 2) : 0u;
+      k.w = 4 * q + 3 < Pb ? key(4 * q + 3) : 0u;
+    }
+    return k;
+  };
   uint32_t prefix, mask;
   int need;
   bool found = false;
@@ -949,15 +962,25 @@ __global__ void __launch_bounds__(kSelMaxThreads) topk_kernel(const TopkArgs a) 
         s_keys[a.P + tid - t0] = 0u;
     }
     __syncthreads();
-    if (sampled) found = block_sample_select(s_keys, Pb, kkb, sc, prefix, mask, need);
+    if (sampled) found = block_sample_select(load4, Pb, kkb, sc, prefix, mask, need);
+  } else {
+    // rows longer than the staging area: keys read from the score row (in L2
+    // after the score kernel) in every pass, with the same sample bracket
+    int r_hi = 0, r_lo = 0;
+    if (Pb >= kSampleMinP && sample_ranks(kkb, Pb, r_hi, r_lo)) {
+      const int tid = static_cast<int>(threadIdx.x);
+      if (tid < 64)
+        sample_splitter(r, a.P, a.group, Pb, tid < 32 ? r_hi : r_lo, sc.comp + 1024 * (tid >> 5),
+                        sc.hist + kSplitOffset + (tid >> 5));
+      __syncthreads();
+      found = block_sample_select(load4, Pb, kkb, sc, prefix, mask, need);
+    }
   }
   uint32_t* bits = a.bitmaps + static_cast<int64_t>(row) * a.W32;
   if (!found) block_radix_select(key, Pb, kkb, sc, prefix, mask, need);
   int32_t* sel_row = a.selected + static_cast<int64_t>(row) * a.kk;
   if (!found) block_emit_counts(key, Pb, prefix, mask, sc);
-  const uint32_t* skeys = nullptr;
-  if constexpr (SMEM) skeys = s_keys;
-  block_emit(key, skeys, Pb, prefix, mask, need, sel_row, bits, sc);
+  block_emit(key, load4, Pb, prefix, mask, need, sel_row, bits, sc);
   for (int w = static_cast<int>(ceil_div(Pb, 32)) + threadIdx.x; w < a.W32; w += sel_threads())
     bits[w] = 0u;
   for (int i = kkb + threadIdx.x; i < a.kk; i += sel_threads()) sel_row[i] = -1;

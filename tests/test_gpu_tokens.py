@@ -33,6 +33,8 @@ CASES = [
     Workload("tok-mha-d64-fp16", B=2, Hq=4, Hkv=4, d=64, N=3001, top_k=300, dtype="fp16"),
     # 45000 keys per row: more than the top-K keeps in shared memory
     Workload("tok-long", B=1, Hq=4, Hkv=1, d=128, N=45000, top_k=4500, kind="offset"),
+    # 192 rows of 5000 keys: the top-K reads its keys from the score rows
+    Workload("tok-many-rows", B=4, Hq=48, Hkv=8, d=64, N=5000, top_k=500),
 ]
 
 
@@ -64,12 +66,15 @@ def test_token_topk_all_tokens_equals_full(dev, dkv):
     assert max_abs(out, full.double().cpu().numpy()) <= 1e-5
 
 
-def test_token_topk_exact_ties_take_lower_tokens(dev, dkv):
+@pytest.mark.parametrize("shape", [(1, 4, 1), (4, 48, 8)], ids=["4-rows", "192-rows"])
+def test_token_topk_exact_ties_take_lower_tokens(shape, dev, dkv):
     """K repeats with period 8, so the scores fall into 8 exactly tied classes
     (identical rows give identical scores on both sides): the top-K is the
     best classes whole and the lowest-index tokens of the class at the K-th
-    place, the same set as the oracle's."""
-    w = Workload("tok-ties", B=1, Hq=4, Hkv=1, d=128, N=6000, top_k=1000)
+    place, the same set as the oracle's (rows staged in shared memory, and
+    rows read from the score rows)."""
+    B, Hq, Hkv = shape
+    w = Workload("tok-ties", B=B, Hq=Hq, Hkv=Hkv, d=128, N=6000, top_k=1000)
     q, K, V = make_inputs(w, seed=85)
     K = K[:, :, :8].repeat(1, 1, w.N // 8, 1).contiguous()
     out, sel = dkv.decode_attn_topk_tokens(q.to(dev), K.to(dev), V.to(dev), w.top_k,
@@ -78,8 +83,9 @@ def test_token_topk_exact_ties_take_lower_tokens(dev, dkv):
     qb, Kb, Vb = bits(q), bits(K), bits(V)
     km, kx = oracle.meta(Kb, 1, 0)
     r = oracle.scores(qb, km, kx, 0).reshape(-1, w.N)
+    rows = sel.reshape(-1, sel.shape[-1])
     for i in range(r.shape[0]):
         order = sorted(range(w.N), key=lambda j: (-r[i, j], j))
-        assert sel[0, i].tolist() == sorted(order[:w.top_k]), f"head {i}"
+        assert rows[i].tolist() == sorted(order[:w.top_k]), f"row {i}"
     ref = oracle.attention(qb, Kb, Vb, 1, 1.0 / math.sqrt(w.d), 0, sel=sel)
     assert max_abs(out, ref) <= ATOL
