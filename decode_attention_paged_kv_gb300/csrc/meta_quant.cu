@@ -25,6 +25,55 @@ namespace {
 
 constexpr int kMetaThreads = 256;
 
+// Two fp32 values in one 64-bit register pair, and the packed fp32 pair
+// arithmetic of sm_100 and later (each lane rounded as the scalar operation
+// with the same rounding mode; subnormals kept).
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// rounded down: an exact zero difference is -0 (IEEE 754, rounding toward
+// negative), so the sign bit of a - b is set exactly when a <= b
+__device__ __forceinline__ uint64_t f2_sub_down(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rm.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add_down(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rm.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add_up(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rp.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint32_t lo32(uint64_t v) { return static_cast<uint32_t>(v); }
+__device__ __forceinline__ uint32_t hi32(uint64_t v) { return static_cast<uint32_t>(v >> 32); }
+
+
 __global__ void __launch_bounds__(kMetaThreads, 2) meta_kernel(const MetaArgs a) {
   griddep_launch_dependents();
   griddep_wait();
@@ -279,57 +328,106 @@ __global__ void __launch_bounds__(kMetaThreads, 3) meta_q4_kernel(const MetaArgs
   }
 }
 
-// 8 threads per group of 64 channels, 8 channels (16 bytes) per thread.  The
-// loop advances whole blocks, so the 8 lanes of a group always shuffle together.
+// One predicated 16-bit store (no branch when the lanes differ on c).
+__device__ __forceinline__ void st_global_u16_if(void* p, unsigned short v, bool c) {
+  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q st.global.u16 [%0], %1;\n\t}"
+               :
+               : "l"(p), "h"(v), "r"(static_cast<uint32_t>(c))
+               : "memory");
+}
+
+constexpr float kRint23 = 8388608.0f;      // 2^23: x + 2^23 holds rint(x) in its low bits
+constexpr uint32_t kRint23Bits = 0x4b000000u;  // the float bits of 2^23
+
+// One thread's 16 channels of group t / 4 (every lane of the warp calls it:
+// the group's min / max go round its 4 lanes).
+__device__ __forceinline__ void quant4_part(const uint4 (&xv)[2], int64_t t, bool valid,
+                                            uint8_t* codes, __half* gmin, __half* gmax) {
+  const int64_t grp = t >> 2;
+  const int quarter = static_cast<int>(t & 3);
+  const uint32_t w[8] = {xv[0].x, xv[0].y, xv[0].z, xv[0].w, xv[1].x, xv[1].y, xv[1].z, xv[1].w};
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const uint32_t k = to_key2(w[u]);
+    kmin = __vminu2(kmin, k);
+    kmax = __vmaxu2(kmax, k);
+  }
+  // fold the two halfwords, then the 4 lanes of the group
+  kmin = min(kmin & 0xffffu, kmin >> 16);
+  kmax = max(kmax & 0xffffu, kmax >> 16);
+#pragma unroll
+  for (int off = 1; off < 4; off <<= 1) {
+    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, off));
+    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, off));
+  }
+  if (!valid) return;
+  const __half mn = __ushort_as_half(static_cast<unsigned short>(from_key2(kmin) & 0xffffu));
+  const __half mx = __ushort_as_half(static_cast<unsigned short>(from_key2(kmax) & 0xffffu));
+  const float fstep = q4_step_f32(mn, mx);
+  const float fmn = __half2float(mn);
+  // q4_code's decisions two values at a time: the same q, rint(q) as 2^23 + q
+  // rounded to nearest (ties to even, 0 <= q < 17), the same test for q near
+  // a half-integer (|q - rint(q)| <= 1/2, so | |d| - 1/2 | < 2^-16 is
+  // |d| > 1/2 - 2^-16); each such value takes q4_code's exact decision.  A
+  // zero step (every value equal to mn) gives q = 0 through a zero
+  // reciprocal: codes 0.
+  const float inv = fstep != 0.f ? __frcp_rn(fstep) : 0.f;
+  const uint64_t MN = f2(fmn, fmn), INV = f2(inv, inv);
+  const uint64_t K23 = f2(kRint23, kRint23);
+  uint32_t packed[2] = {0u, 0u};
+  uint32_t near = 0u;  // bit e: value e's quotient is near a half-integer
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const float2 xf = __half22float2(*reinterpret_cast<const __half2*>(&w[u]));
+    const uint64_t q = f2_mul(f2_sub(f2(xf.x, xf.y), MN), INV);
+    const uint64_t tq = f2_add(q, K23);               // 2^23 + rint(q)
+    const uint64_t dq = f2_sub(q, f2_sub(tq, K23));   // q - rint(q), exact
+    near |= (fabsf(__uint_as_float(lo32(dq))) > 0.5f - 0x1p-16f ? 1u : 0u) << (2 * u);
+    near |= (fabsf(__uint_as_float(hi32(dq))) > 0.5f - 0x1p-16f ? 2u : 0u) << (2 * u);
+    const uint32_t c0 = min(lo32(tq) - kRint23Bits, 15u), c1 = min(hi32(tq) - kRint23Bits, 15u);
+    packed[u >> 2] |= (c0 | (c1 << 4)) << (8 * (u & 3));
+  }
+  // those values (a few in ten thousand) take q4_code's exact decision
+  while (near != 0u) {
+    const int e = __ffs(near) - 1;
+    near &= near - 1u;
+    const uint32_t hv = (w[e >> 1] >> (16 * (e & 1))) & 0xffffu;
+    const float xf = __half2float(__ushort_as_half(static_cast<unsigned short>(hv)));
+    const int sh = 4 * (e & 7);
+    packed[e >> 3] = (packed[e >> 3] & ~(0xfu << sh)) | (q4_code(xf, fmn, fstep, inv) << sh);
+  }
+  *reinterpret_cast<uint2*>(codes + grp * 32 + quarter * 8) = make_uint2(packed[0], packed[1]);
+  st_global_u16_if(gmin + grp, __half_as_ushort(mn), quarter == 0);
+  st_global_u16_if(gmax + grp, __half_as_ushort(mx), quarter == 0);
+}
+
+// 4 threads per group of 64 channels, 16 channels (32 bytes) per thread; two
+// iterations' loads go out before either is used.  The loop advances whole
+// blocks, so the 4 lanes of a group always shuffle together.
 __global__ void __launch_bounds__(256) quant4_kernel(int64_t groups, const __half* x,
                                                      uint8_t* codes, __half* gmin, __half* gmax) {
   griddep_launch_dependents();
   griddep_wait();
-  const int64_t total = groups * 8;
+  const int64_t total = groups * 4;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.x; t0 < total; t0 += stride) {
-    const int64_t t = t0 + threadIdx.x;
-    const int64_t grp = t >> 3;
-    const int sub = static_cast<int>(t & 7);
-    const bool valid = grp < groups;
-    uint4 xv = make_uint4(0, 0, 0, 0);
-    if (valid) xv = __ldcs(reinterpret_cast<const uint4*>(x + grp * 64 + sub * 8));
-    const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
-    uint32_t kmin = 0xffffffffu, kmax = 0u;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const uint32_t k = to_key2(w[u]);
-      kmin = __vminu2(kmin, k);
-      kmax = __vmaxu2(kmax, k);
+  for (int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.x; t0 < total; t0 += 2 * stride) {
+    const int64_t ta = t0 + threadIdx.x, tb = ta + stride;
+    const bool va = (ta >> 2) < groups, vb = (tb >> 2) < groups;
+    uint4 xa[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    uint4 xb[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    const uint4* pa = reinterpret_cast<const uint4*>(x + (ta >> 2) * 64 + (ta & 3) * 16);
+    const uint4* pb = reinterpret_cast<const uint4*>(x + (tb >> 2) * 64 + (tb & 3) * 16);
+    if (va) {
+      xa[0] = __ldcs(pa);
+      xa[1] = __ldcs(pa + 1);
     }
-    // fold the two halfwords, then the 8 lanes of the group
-    kmin = min(kmin & 0xffffu, kmin >> 16);
-    kmax = max(kmax & 0xffffu, kmax >> 16);
-#pragma unroll
-    for (int off = 1; off < 8; off <<= 1) {
-      kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, off));
-      kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, off));
+    if (vb) {
+      xb[0] = __ldcs(pb);
+      xb[1] = __ldcs(pb + 1);
     }
-    if (!valid) continue;
-    const __half mn = __ushort_as_half(static_cast<unsigned short>(from_key2(kmin) & 0xffffu));
-    const __half mx = __ushort_as_half(static_cast<unsigned short>(from_key2(kmax) & 0xffffu));
-    const float fstep = q4_step_f32(mn, mx);
-    const float fmn = __half2float(mn);
-    uint32_t packed = 0;
-    if (fstep != 0.f) {
-      const float inv = __frcp_rn(fstep);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const uint32_t hv = (w[e >> 1] >> (16 * (e & 1))) & 0xffffu;
-        const float xf = __half2float(__ushort_as_half(static_cast<unsigned short>(hv)));
-        packed |= q4_code(xf, fmn, fstep, inv) << (4 * e);
-      }
-    }
-    *reinterpret_cast<uint32_t*>(codes + grp * 32 + sub * 4) = packed;
-    if (sub == 0) {
-      gmin[grp] = mn;
-      gmax[grp] = mx;
-    }
+    quant4_part(xa, ta, va, codes, gmin, gmax);
+    quant4_part(xb, tb, vb, codes, gmin, gmax);
   }
 }
 
@@ -405,48 +503,6 @@ __device__ __forceinline__ float dec8(int c, float step, float lo) {
 // bits (the float bits of K + j are those of K plus j)
 constexpr float kMagic = 12582912.0f;
 
-// Two fp32 values in one 64-bit register pair, and the packed fp32 pair
-// arithmetic of sm_100 and later (each lane rounded as the scalar operation
-// with the same rounding mode; subnormals kept).
-__device__ __forceinline__ uint64_t f2(float a, float b) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-// rounded down: an exact zero difference is -0 (IEEE 754, rounding toward
-// negative), so the sign bit of a - b is set exactly when a <= b
-__device__ __forceinline__ uint64_t f2_sub_down(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("sub.rm.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2_add_down(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rm.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2_add_up(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rp.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-__device__ __forceinline__ uint32_t lo32(uint64_t v) { return static_cast<uint32_t>(v); }
-__device__ __forceinline__ uint32_t hi32(uint64_t v) { return static_cast<uint32_t>(v >> 32); }
 // the low bytes of four words, in order, as one word
 __device__ __forceinline__ uint32_t low_bytes4(const uint32_t (&c)[4]) {
   return __byte_perm(__byte_perm(c[0], c[1], 0x0040u), __byte_perm(c[2], c[3], 0x0040u),
@@ -622,7 +678,7 @@ cudaError_t launch_meta8(bool f16, const Meta8Args& a, cudaStream_t s) {
 cudaError_t launch_quant4(int64_t rows, int d, const void* x, void* codes, void* gmin,
                           void* gmax, cudaStream_t s) {
   const int64_t groups = rows * (d / 64);
-  return launch_pdl(quant4_kernel, dim3(grid_for(groups * 8, 256)), dim3(256), 0, s, groups,
+  return launch_pdl(quant4_kernel, dim3(grid_for(groups * 4, 256)), dim3(256), 0, s, groups,
                     static_cast<const __half*>(x), static_cast<uint8_t*>(codes),
                     static_cast<__half*>(gmin), static_cast<__half*>(gmax));
 }
