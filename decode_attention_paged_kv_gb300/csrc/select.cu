@@ -139,6 +139,7 @@ struct SelScratch {
   uint32_t hist[256];
   uint32_t warp_gt[kSelMaxWarps];      // per-warp counts (emit: keys > prefix,
   uint32_t warp_eq[kSelMaxWarps];      // == prefix; union: pages)
+  uint32_t res[4];                     // the bucket search's verdicts
   uint32_t comp[kSelCompCap];
 };
 
@@ -346,12 +347,6 @@ __device__ void sample_splitter(const float* r, int64_t rs, int group, int P, in
 // Where the two splitters sit in SelScratch::hist (hi, then lo).
 constexpr int kSplitOffset = 2 * kSelMaxWarps;
 
-// Warps that search the sample bracket's bucket (a named barrier among them).
-constexpr int kSearchWarps = 8;
-__device__ __forceinline__ void search_sync() {
-  asm volatile("bar.sync 3, %0;" ::"r"(kSearchWarps * 32) : "memory");
-}
-
 // Block top-K of P >= kSampleMinP keys (load4(q): keys 4 q .. 4 q + 3, zero
 // from P up to a multiple of 4; staged in shared memory or read from the
 // score row) by a sample bracket.  1024 keys, one from each
@@ -425,101 +420,76 @@ __device__ bool block_sample_select(const Load4& load4, int P, int kk, SelScratc
     put(v.w);
   }
   __syncthreads();
-  // Warps 0 .. kSearchWarps - 1 find T on the bucket, held in registers (zero
-  // past its end: zero is below every x counted); the other warps wait.
-  // Counts of keys >= x, for lo <= x <= hi, are A plus the bucket's keys >= x
-  // (for x > hi that gives A, an overcount still < kk, so every decision
-  // holds; below lo it gives A + #bucket, a lower bound, which only accepts).
-  uint32_t* res = sc.hist + 4 * kSelMaxWarps;
-  if (warp < kSearchWarps) {
-    constexpr int kBk = kSelCompCap / (32 * kSearchWarps);
-    uint32_t bk[kBk];
-#pragma unroll
-    for (int i = 0; i < kBk; ++i) {
-      const int c = tid + i * 32 * kSearchWarps;
-      bk[i] = c < nb ? sc.comp[c] : 0u;
-    }
-    uint32_t* wc1 = sc.hist;
-    uint32_t* wc2 = sc.hist + kSearchWarps;
-    uint32_t* wc3 = sc.hist + 2 * kSearchWarps;
-    auto part_sum = [&](const uint32_t* part) {
-      return __reduce_add_sync(0xffffffffu, lane < kSearchWarps ? static_cast<int>(part[lane]) : 0);
-    };
-    auto count3 = [&](uint32_t x1, uint32_t x2, uint32_t x3, int& n1, int& n2, int& n3) {
-      int b1 = 0, b2 = 0, b3 = 0;
-#pragma unroll
-      for (int i = 0; i < kBk; ++i) {
-        b1 += minus_borrow(bk[i], x1);
-        b2 += minus_borrow(bk[i], x2);
-        b3 += minus_borrow(bk[i], x3);
-      }
-      b1 = __reduce_add_sync(0xffffffffu, kBk + b1);
-      b2 = __reduce_add_sync(0xffffffffu, kBk + b2);
-      b3 = __reduce_add_sync(0xffffffffu, kBk + b3);
-      if (lane == 0) {
-        wc1[warp] = static_cast<uint32_t>(b1);
-        wc2[warp] = static_cast<uint32_t>(b2);
-        wc3[warp] = static_cast<uint32_t>(b3);
-      }
-      search_sync();
-      n1 = A + part_sum(wc1);
-      n2 = A + part_sum(wc2);
-      n3 = A + part_sum(wc3);
-      search_sync();
-    };
-    // the bucket's keys agree with lo and hi - 1 above their first differing
-    // bit; below it T is found two bits a round (the largest 2-bit digit whose
-    // count reaches kk), stopping once exactly kk keys are >= T
-    const uint32_t hm1 = hi - 1u;
-    uint32_t T = lo;
-    int ge = -1;
-    if (lo != hm1) {
-      const int top = 31 - __clz(lo ^ hm1);
-      T = top == 31 ? 0u : (lo >> (top + 1)) << (top + 1);
-      for (int bit = top; bit >= 0; bit -= 2) {
-        const int sh = bit >= 1 ? bit - 1 : 0;
-        const uint32_t c1 = T | (1u << sh);
-        const uint32_t c2 = bit >= 1 ? T | (2u << sh) : c1;
-        const uint32_t c3 = bit >= 1 ? T | (3u << sh) : c1;
-        int n1, n2, n3;
-        count3(c1, c2, c3, n1, n2, n3);
-        uint32_t cand = 0u;
-        int c = -1;
-        if (n3 >= kk) {
-          cand = c3;
-          c = n3;
-        } else if (n2 >= kk) {
-          cand = c2;
-          c = n2;
-        } else if (n1 >= kk) {
-          cand = c1;
-          c = n1;
-        }
-        if (c >= 0) {
-          T = cand;
-          ge = c;
-          if (c == kk && cand >= lo) break;
-        }
-      }
-    }
-    if (ge == kk) {
-      if (tid == 0) {
-        res[0] = T - 1u;
-        res[1] = 0u;
-      }
-    } else {
-      int n1, n2, n3;
-      count3(T + 1u, T + 1u, T + 1u, n1, n2, n3);  // T < hi, so T + 1 <= hi
-      if (tid == 0) {
-        res[0] = T;
-        res[1] = static_cast<uint32_t>(kk - n1);
-      }
-    }
-  }
+  // The (kk - A)-th largest bucket key T by radix selection over the bucket,
+  // 8 bits a pass below the bits all bucket keys share (those of lo and
+  // hi - 1), by the whole block: a shared histogram of the next digit of the
+  // keys that agree with T so far, then warp 0 finds the digit holding the
+  // rank (and zeroes the histogram for the next pass).  After the last pass r
+  // is T's rank among the keys equal to it and cnt their number.
+  uint32_t* hist = sc.hist;
+  for (int i = tid; i < 256; i += sel_threads()) hist[i] = 0u;
+  const uint32_t hm1 = hi - 1u;
+  const int top = lo == hm1 ? -1 : 31 - __clz(lo ^ hm1);  // highest bit that may differ
+  uint32_t fixed = top < 0 ? ~0u : (top >= 31 ? 0u : ~((2u << top) - 1u));  // bits settled
+  uint32_t T = lo & fixed;
+  int r = kk - A, cnt = nb;
   __syncthreads();
+  for (int hb = top; hb >= 0; hb -= 8) {
+    const int lb = hb >= 7 ? hb - 7 : 0;
+    const uint32_t dmask = (2u << (hb - lb)) - 1u;
+    for (int j = tid; j < nb; j += sel_threads()) {
+      const uint32_t k = sc.comp[j];
+      if ((k & fixed) == T) atomicAdd(hist + ((k >> lb) & dmask), 1u);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l holds digits 8 l .. 8 l + 7; the digit d where the count of
+      // digits >= d first reaches r, counting from the top
+      uint32_t h[8];
+      int tot = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        h[e] = hist[8 * lane + e];
+        hist[8 * lane + e] = 0u;
+        tot += static_cast<int>(h[e]);
+      }
+      int incl = tot;  // digits of this lane and the lanes above
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int t = __shfl_down_sync(0xffffffffu, incl, off);
+        if (lane + off < 32) incl += t;
+      }
+      const int above = incl - tot;
+      if (above < r && r <= incl) {  // exactly one lane
+        int run = above, d = 0;
+        uint32_t hd = 0u;
+        bool found = false;
+#pragma unroll
+        for (int e = 7; e >= 0; --e) {
+          if (!found && run + static_cast<int>(h[e]) >= r) {
+            found = true;
+            d = e;
+            hd = h[e];
+          } else if (!found) {
+            run += static_cast<int>(h[e]);
+          }
+        }
+        sc.res[0] = static_cast<uint32_t>(8 * lane + d);
+        sc.res[1] = static_cast<uint32_t>(r - run);
+        sc.res[2] = hd;
+      }
+    }
+    __syncthreads();
+    T |= sc.res[0] << lb;
+    r = static_cast<int>(sc.res[1]);
+    cnt = static_cast<int>(sc.res[2]);
+    fixed |= dmask << lb;
+  }
+  // keys > T, and of the cnt keys equal to T the first r: all of them when
+  // r == cnt (then the selection is every key >= T, T >= lo >= 1)
   mask = ~0u;
-  prefix = res[0];
-  need = static_cast<int>(res[1]);
+  prefix = r == cnt ? T - 1u : T;
+  need = r == cnt ? 0 : r;
   // block_emit's per-warp counts: keys > prefix are the warp's keys >= hi and
   // its bucket keys > prefix (prefix >= lo - 1); keys == prefix matter only
   // when need > 0, where prefix = T >= lo and they all lie in the bucket
