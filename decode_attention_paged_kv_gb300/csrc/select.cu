@@ -1387,7 +1387,8 @@ __global__ void __launch_bounds__(kUnitThreads, TWO ? 2 : 1)
   for (int h = warp; h < n_sel; h += kUnitConsumers) {
     uint32_t* bm = s_bm + h * kSelBitmapWords;
     const uint32_t* keys = s_keys + h * a.P;
-    warp_topk_head([keys](int j) { return keys[j]; }, Pb, kkb, bm,
+    // (the short-head copies only where d = 64 contexts run short)
+    warp_topk_head<D == 64>([keys](int j) { return keys[j]; }, Pb, kkb, bm,
                    s_kext[a.group ? 16 : h], s_kext[a.group ? 17 : 8 + h]);
   }
   unit_consumers_sync();

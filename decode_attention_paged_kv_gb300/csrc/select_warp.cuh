@@ -139,16 +139,22 @@ __device__ void warp_topk_head_n(const KeyAt& key_at, int P, int kk, uint32_t* b
 }
 
 // The same with as few key slots a lane as P needs (every count touches every
-// slot, so short heads run on 16 or 32).
-template <class KeyAt>
+// slot, so short heads run on 16 or 32).  SHORT = false keeps one copy (64
+// slots), for kernels whose heads are long and whose code size matters.
+template <bool SHORT = true, class KeyAt>
 __device__ void warp_topk_head(const KeyAt& key_at, int P, int kk, uint32_t* bm, uint32_t kmax,
                                uint32_t kmin) {
-  if (P <= 16 * 32)
-    warp_topk_head_n<16>(key_at, P, kk, bm, kmax, kmin);
-  else if (P <= 32 * 32)
-    warp_topk_head_n<32>(key_at, P, kk, bm, kmax, kmin);
-  else
-    warp_topk_head_n<kSelKeys>(key_at, P, kk, bm, kmax, kmin);
+  if constexpr (SHORT) {
+    if (P <= 16 * 32) {
+      warp_topk_head_n<16>(key_at, P, kk, bm, kmax, kmin);
+      return;
+    }
+    if (P <= 32 * 32) {
+      warp_topk_head_n<32>(key_at, P, kk, bm, kmax, kmin);
+      return;
+    }
+  }
+  warp_topk_head_n<kSelKeys>(key_at, P, kk, bm, kmax, kmin);
 }
 
 // Ascending page rows from a head's selection bitmap (words [0, W)); the words
