@@ -527,7 +527,7 @@ __device__ __forceinline__ uint32_t low_bytes4(const uint32_t (&c)[4]) {
 // throughout) and infinite ones (a bf16 range above the largest float) take
 // bounded walks from a clamped guess instead.
 template <int D, bool F16>
-__global__ void __launch_bounds__(kMetaThreads) meta8_kernel(const Meta8Args a) {
+__global__ void __launch_bounds__(kMetaThreads, D == 128 ? 5 : 0) meta8_kernel(const Meta8Args a) {
   griddep_launch_dependents();
   griddep_wait();
   constexpr int CPL = D / 8;  // channels per lane
