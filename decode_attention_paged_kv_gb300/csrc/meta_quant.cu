@@ -190,7 +190,7 @@ __device__ __forceinline__ void q4_minmax_token(uint2 cw, uint32_t ms, uint32_t 
 }
 
 template <int D>
-__global__ void __launch_bounds__(kMetaThreads, 3) meta_q4_kernel(const MetaArgs a) {
+__global__ void __launch_bounds__(kMetaThreads, 4) meta_q4_kernel(const MetaArgs a) {
   griddep_launch_dependents();
   griddep_wait();
   constexpr int LPP = D / 16;  // lanes per page
