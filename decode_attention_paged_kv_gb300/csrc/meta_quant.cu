@@ -142,6 +142,65 @@ __global__ void __launch_bounds__(kMetaThreads, 2) meta_kernel(const MetaArgs a)
   }
 }
 
+// Pages of S = 16 / SUBS tokens (8 or 4) over a 16-bit cache: one thread owns 8
+// channels of a whole 16-token cache page (its 16 rows in flight, as for
+// S = 16) and writes the page's SUBS metadata pages, each from its own S rows
+// -- rather than a thread per S-token page with S rows in flight.
+template <int SUBS>
+__global__ void __launch_bounds__(kMetaThreads, 2) meta_sub_kernel(const MetaArgs a) {
+  griddep_launch_dependents();
+  griddep_wait();
+  constexpr int S = kPage / SUBS;
+  const int vpr = a.d / 8;  // 16-byte vectors per row
+  const int P16 = static_cast<int>(ceil_div(a.N, kPage));
+  const int64_t total = static_cast<int64_t>(a.B) * a.Hkv * P16 * vpr;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int v = static_cast<int>(idx % vpr);
+    const int cp = static_cast<int>(idx / vpr % P16);  // cache page
+    const int64_t bh = idx / vpr / P16;
+    const int h = static_cast<int>(bh % a.Hkv);
+    const int b = static_cast<int>(bh / a.Hkv);
+    const int Nb = seq_len_of(a.lens, b, a.N);
+    const int t0 = cp * kPage;
+    if (t0 >= Nb) continue;  // past a shorter sequence: not written
+    const int nt = min(kPage, Nb - t0);
+    // a paged cache: the cache page's pool block (clamped)
+    const int64_t base = a.bt != nullptr
+                             ? static_cast<int64_t>(min(max(a.bt[b * a.bts + cp], 0),
+                                                        a.nblocks - 1)) * a.sb
+                             : b * a.sb + static_cast<int64_t>(t0) * a.d;
+    const uint16_t* src = static_cast<const uint16_t*>(a.data) + base + h * a.sh + 8 * v;
+    uint4 x[kPage];
+#pragma unroll
+    for (int t = 0; t < kPage; ++t)
+      if (t < nt) x[t] = __ldcs(reinterpret_cast<const uint4*>(src + static_cast<int64_t>(t) * a.d));
+#pragma unroll
+    for (int sp = 0; sp < SUBS; ++sp) {
+      if (sp * S >= nt) break;  // past the sequence: not written
+      uint32_t kmin[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+      uint32_t kmax[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int t = sp * S; t < sp * S + S; ++t) {
+        if (t < nt) {
+          const uint32_t w[4] = {x[t].x, x[t].y, x[t].z, x[t].w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t k = to_key2(w[u]);
+            kmin[u] = __vminu2(kmin[u], k);
+            kmax[u] = __vmaxu2(kmax[u], k);
+          }
+        }
+      }
+      const int64_t o = (bh * a.P + static_cast<int64_t>(cp) * SUBS + sp) * a.d + 8 * v;
+      *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.meta_min) + o) =
+          make_uint4(from_key2(kmin[0]), from_key2(kmin[1]), from_key2(kmin[2]), from_key2(kmin[3]));
+      *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.meta_max) + o) =
+          make_uint4(from_key2(kmax[0]), from_key2(kmax[1]), from_key2(kmax[2]), from_key2(kmax[3]));
+    }
+  }
+}
+
 // A 4-bit cache: D/16 lanes per page, lane u owning channels 16u .. 16u + 15
 // (two code words of a token row, one 8-byte load).  One row of blocks per
 // (batch, kv head) (grid y), a warp over 32/(D/16) consecutive pages of it, so
@@ -652,6 +711,14 @@ cudaError_t launch_meta(bool q4, bool f16, const MetaArgs& a, cudaStream_t s) {
   const int64_t work =
       static_cast<int64_t>(a.B) * a.Hkv * (a.last_only ? 1 : a.P) * (a.d / 8);
   const dim3 grid(grid_for(work, kMetaThreads)), block(kMetaThreads);
+  if (!q4 && !a.last_only && (a.S == 4 || a.S == 8)) {
+    // a thread per 16-token cache page and 8 channels
+    const int64_t sub_work =
+        static_cast<int64_t>(a.B) * a.Hkv * ceil_div(a.N, kPage) * (a.d / 8);
+    const dim3 sgrid(grid_for(sub_work, kMetaThreads));
+    return a.S == 8 ? launch_pdl(meta_sub_kernel<2>, sgrid, block, 0, s, a)
+                    : launch_pdl(meta_sub_kernel<4>, sgrid, block, 0, s, a);
+  }
   if (!q4) return launch_pdl(meta_kernel, grid, block, 0, s, a);
   // one row of blocks per (batch, kv head): the row's pages, d/16 lanes each
   const int64_t row = static_cast<int64_t>(a.last_only ? 1 : a.P) * (a.d / 16);
