@@ -158,6 +158,9 @@ dkv_status check_kv(const dkv_params* p, const dkv_kv* kv) {
     if (kv->block_table == nullptr) return DKV_ERR_NULL;
     if (reinterpret_cast<uintptr_t>(kv->block_table) & 3u) return DKV_ERR_ALIGN;
     if (kv->num_blocks < 1 || kv->block_table_stride < 0) return DKV_ERR_SHAPE;
+    // the [B, P] table's rows may not overlap (P = ceil(N / 16) cache pages)
+    if (p->batch > 1 && kv->block_table_stride < ceil_div(p->seq_len, dkv::kPage))
+      return DKV_ERR_SHAPE;
     return DKV_OK;
   }
   if (kv->format == DKV_KV_Q4G64) {

@@ -98,7 +98,8 @@ typedef enum dkv_kv_format {
   DKV_KV_PAGED = 2  /* a pool of pages (blocks) of S = 16 tokens, `dtype` bf16 or
                        fp16: block n of kv head h starts at data + n * stride_b +
                        h * stride_h (elements), token stride d.  block_table
-                       [B, P] int32 (row stride block_table_stride) maps page j
+                       [B, P] int32 (row stride block_table_stride, at least
+                       P = ceil(N / 16) when B > 1) maps page j
                        of batch entry b to its block; entries outside
                        [0, num_blocks) are clamped into it (nothing outside
                        the pool is read) and the attention calls then record

@@ -178,6 +178,8 @@ def test_paged_cache_validation(L):
     assert mb(ctypes.byref(p), ctypes.byref(paged(num_blocks=0)), q, q, None) == 2
     assert mb(ctypes.byref(p), ctypes.byref(paged(stride_h=16 * 128 + 4)), q, q, None) == 3
     assert mb(ctypes.byref(p), ctypes.byref(paged(dtype=2)), q, q, None) == 4
+    # rows of the [B, P] block table may not overlap (P = 63 cache pages here)
+    assert mb(ctypes.byref(p), ctypes.byref(paged(block_table_stride=62)), q, q, None) == 2
     # K and V must share one block table
     assert f(ctypes.byref(p), q, ctypes.byref(k), ctypes.byref(paged(block_table_stride=64)), out,
              2, ws, 1 << 20, None) == 2
