@@ -1,14 +1,16 @@
 // meta_quant.cu -- page metadata build and the 4-bit KV format.
 //
 // Page metadata ("TinyServe: Query-Aware Cache Selection for Efficient LLM
-// Serving", 结构化内存布局 / 相关性函数实例化): for every page of S = 16 tokens,
-// m_j and M_j are the channel-wise min / max of the page's keys.  One thread
-// owns 8 channels of one page: it streams the page's (up to) 16 rows as 16-byte
-// vectors -- a warp covers whole contiguous 256-byte key rows -- and reduces on
-// order-preserving 16-bit keys with per-halfword integer min / max, so the
-// result is exactly one of the stored values (-0 below +0).  A 4-bit cache is
-// dequantised in registers first; its metadata describes the fp16 keys that
-// attention actually uses.
+// Serving", 结构化内存布局 / 相关性函数实例化): for every page of S tokens, m_j
+// and M_j are the channel-wise min / max of the page's keys.  One thread owns
+// 8 channels of one page (of a 16-token cache page for S = 4 and 8): it
+// streams the rows as 16-byte vectors -- a warp covers whole contiguous
+// 256-byte key rows -- and reduces on order-preserving 16-bit keys with
+// per-halfword integer min / max, so the result is exactly one of the stored
+// values (-0 below +0).  A 4-bit cache is dequantised in registers first (its
+// own kernel, meta_q4_kernel); its metadata describes the fp16 keys that
+// attention actually uses.  The 8-bit metadata of the same pages (a byte grid
+// per page, rounded outward) is built from the 16-bit one (meta8_kernel).
 //
 // 4-bit format ("FlexGen: High-Throughput Generative Inference of Large
 // Language Models with a Single GPU" 解读, 4-bit 近似方法): groups of 64
