@@ -14,17 +14,21 @@
 //
 // Top-K (问题公式化定义: S_t = TopK_j r, |S_t| = K; Algorithm 1 step 2, "radix
 // select"): radix selection of the K largest scores of one (b, h) on
-// order-preserving 32-bit keys (8-bit digits, most significant first), then
-// the selected pages in ascending order; among equal scores the lower page
-// index is taken first.
+// order-preserving 32-bit keys, most significant bits first -- one bit at a
+// time by a warp over keys in registers (select_warp.cuh) or by a block; for
+// long rows a sample bracket first narrows the K-th key to a bucket of a few
+// thousand keys, searched with 8-bit digits -- then the selected pages in
+// ascending order; among equal scores the lower page index is taken first.
 //
 // Union: the pages any query head of a group selected, ascending, each with a
 // bit per head that chose it -- the list the sparse attention gathers (each
 // page once for the whole group).
 //
-// Three kernels, chained with programmatic dependent launch: score_kernel
-// (scores to global memory), topk_kernel (one CTA per (b, h): selection and
-// its bitmap) and union_kernel (one CTA per (batch, kv head)).
+// Contexts of 256 to 2048 pages: unit_select_kernel does all three for a
+// (batch, kv head) in one CTA.  Otherwise three kernels, chained with
+// programmatic dependent launch: score_kernel (scores to global memory),
+// topk_kernel (one CTA per (b, h): selection and its bitmap) and
+// union_kernel (one CTA per (batch, kv head)).
 
 #include <math.h>
 
