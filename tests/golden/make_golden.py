@@ -1,7 +1,8 @@
 """Write the golden fixtures in this folder.  Calls only the oracle.
 
 The pages print no worked numeric example of the kernel, so these fixtures are
-regression pins of the oracle itself: small inputs (stored verbatim as bit
+regression pins of the oracle itself (page metadata, bound scores, top-K and
+attention; the 4-bit format; the 8-bit metadata and its scores): small inputs (stored verbatim as bit
 patterns, drawn from numpy's PCG64 so they are platform independent) together
 with the oracle's outputs.  ``tests/test_golden.py`` recomputes them on
 whatever machine runs the suite (x86 here, Arm on the GPU host) and requires the
@@ -68,8 +69,45 @@ def case_quant4():
             "gmax": gmax.ravel().tolist(), "xhat": xh.ravel().tolist()}
 
 
+def case_meta8_small():
+    rng = np.random.default_rng(808)
+    out = {}
+    for f16 in (0, 1):
+        Hkv, P, d, Hq = 2, 7, 64, 4
+        if f16:
+            a = rng.standard_normal((1, Hkv, P, d)) * 2.0
+            b = a + np.abs(rng.standard_normal((1, Hkv, P, d)))
+            conv = lambda x: np.asarray(x, np.float64).astype(np.float16).view(np.uint16)  # noqa
+        else:
+            a = rng.standard_normal((1, Hkv, P, d)) * 3.0
+            b = a + np.abs(rng.standard_normal((1, Hkv, P, d)))
+            conv = _bf16_bits
+        mn, mx = conv(a), conv(b)
+        # page 0 of head 0 constant; page 1 two neighbouring values around a
+        # power of two (the smallest step against the ulp); page 2 straddling zero
+        mn[0, 0, 0], mx[0, 0, 0] = conv(np.full(d, 1.25)), conv(np.full(d, 1.25))
+        lo2, hi2 = (2.0 - 2.0 ** -10, 2.0) if f16 else (2.0 - 2.0 ** -7, 2.0)
+        mn[0, 0, 1], mx[0, 0, 1] = conv(np.full(d, lo2)), conv(np.full(d, hi2))
+        mn[0, 0, 2] = conv(-np.abs(rng.standard_normal(d)))
+        mx[0, 0, 2] = conv(np.abs(rng.standard_normal(d)))
+        cm, cM, lo, step = oracle.meta8(mn, mx, f16)
+        q = conv(rng.standard_normal((1, Hq, d)))
+        r8 = oracle.scores8(q, cm, cM, lo, step, f16)
+        out["fp16" if f16 else "bf16"] = {
+            "shape": dict(Hkv=Hkv, P=P, d=d, Hq=Hq),
+            "meta_min": mn.ravel().tolist(), "meta_max": mx.ravel().tolist(),
+            "code_min": cm.ravel().tolist(), "code_max": cM.ravel().tolist(),
+            "lo": [float.hex(float(v)) for v in lo.ravel()],
+            "step": [float.hex(float(v)) for v in step.ravel()],
+            "q": q.ravel().tolist(),
+            "scores8": [float.hex(float(v)) for v in r8.ravel()],
+        }
+    return out
+
+
 def main():
-    for name, fn in [("sparse_small", case_sparse_small), ("quant4", case_quant4)]:
+    for name, fn in [("sparse_small", case_sparse_small), ("quant4", case_quant4),
+                     ("meta8_small", case_meta8_small)]:
         with open(os.path.join(HERE, f"{name}.json"), "w") as f:
             json.dump(fn(), f, separators=(",", ":"))
             f.write("\n")

@@ -56,3 +56,21 @@ def test_quant4_fixture():
     assert gmin.ravel().tolist() == g["gmin"]
     assert gmax.ravel().tolist() == g["gmax"]
     assert oracle.dequant4(codes, gmin, gmax).ravel().tolist() == g["xhat"]
+
+
+def test_meta8_fixture():
+    g = _load("meta8_small.json")
+    for fmt, f16 in (("bf16", 0), ("fp16", 1)):
+        c = g[fmt]
+        s = c["shape"]
+        shape = (1, s["Hkv"], s["P"], s["d"])
+        mn = np.array(c["meta_min"], np.uint16).reshape(shape)
+        mx = np.array(c["meta_max"], np.uint16).reshape(shape)
+        cm, cM, lo, step = oracle.meta8(mn, mx, f16)
+        assert cm.ravel().tolist() == c["code_min"], fmt
+        assert cM.ravel().tolist() == c["code_max"], fmt
+        assert np.array_equal(lo.ravel().astype(np.float64), _hexarr(c["lo"])), fmt
+        assert np.array_equal(step.ravel().astype(np.float64), _hexarr(c["step"])), fmt
+        q = np.array(c["q"], np.uint16).reshape(1, s["Hq"], s["d"])
+        r8 = oracle.scores8(q, cm, cM, lo, step, f16)
+        assert np.array_equal(r8.ravel(), _hexarr(c["scores8"])), fmt
