@@ -2,7 +2,8 @@
 
 The pages print no worked numeric example of the kernel, so these fixtures are
 regression pins of the oracle itself (page metadata, bound scores, top-K and
-attention; the 4-bit format; the 8-bit metadata and its scores): small inputs (stored verbatim as bit
+attention; metadata at page sizes 4, 8 and 32 with group scores; the 4-bit
+format; the 8-bit metadata and its scores): small inputs (stored verbatim as bit
 patterns, drawn from numpy's PCG64 so they are platform independent) together
 with the oracle's outputs.  ``tests/test_golden.py`` recomputes them on
 whatever machine runs the suite (x86 here, Arm on the GPU host) and requires the
@@ -105,9 +106,24 @@ def case_meta8_small():
     return out
 
 
+def case_pages_small():
+    rng = np.random.default_rng(4096)
+    B, Hq, Hkv, d, N = 1, 4, 2, 32, 77   # ragged at every page size below
+    q = _bf16_bits(rng.standard_normal((B, Hq, d)))
+    Kc = _bf16_bits(rng.standard_normal((B, Hkv, N, d)))
+    out = {"shape": dict(B=B, Hq=Hq, Hkv=Hkv, d=d, N=N), "q": q.ravel().tolist(),
+           "K": Kc.ravel().tolist()}
+    for S in (4, 8, 32):
+        mn, mx = oracle.meta(Kc, S, 0)
+        g = oracle.group_scores(q, mn, mx, 0)
+        out[f"S{S}"] = {"meta_min": mn.ravel().tolist(), "meta_max": mx.ravel().tolist(),
+                        "group_scores": [float.hex(float(v)) for v in g.ravel()]}
+    return out
+
+
 def main():
     for name, fn in [("sparse_small", case_sparse_small), ("quant4", case_quant4),
-                     ("meta8_small", case_meta8_small)]:
+                     ("meta8_small", case_meta8_small), ("pages_small", case_pages_small)]:
         with open(os.path.join(HERE, f"{name}.json"), "w") as f:
             json.dump(fn(), f, separators=(",", ":"))
             f.write("\n")

@@ -74,3 +74,18 @@ def test_meta8_fixture():
         q = np.array(c["q"], np.uint16).reshape(1, s["Hq"], s["d"])
         r8 = oracle.scores8(q, cm, cM, lo, step, f16)
         assert np.array_equal(r8.ravel(), _hexarr(c["scores8"])), fmt
+
+
+def test_pages_fixture():
+    g = _load("pages_small.json")
+    s = g["shape"]
+    q = np.array(g["q"], np.uint16).reshape(s["B"], s["Hq"], s["d"])
+    Kc = np.array(g["K"], np.uint16).reshape(s["B"], s["Hkv"], s["N"], s["d"])
+    for S in (4, 8, 32):
+        c = g[f"S{S}"]
+        mn, mx = oracle.meta(Kc, S, 0)
+        assert mn.ravel().tolist() == c["meta_min"], S
+        assert mx.ravel().tolist() == c["meta_max"], S
+        assert mn.shape[2] == (s["N"] + S - 1) // S
+        gs = oracle.group_scores(q, mn, mx, 0)
+        assert np.array_equal(gs.ravel(), _hexarr(c["group_scores"])), S
