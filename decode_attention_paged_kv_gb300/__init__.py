@@ -391,6 +391,8 @@ def decode_attn_select(q, K, V, meta, top_k: int, scale: Optional[float] = None,
         raise ValueError("K and V shapes differ")
     P = (N + page_size - 1) // page_size
     m8 = meta if isinstance(meta, Meta8) else None
+    if m8 is not None and hot is not None:
+        raise ValueError("cross-step reuse takes 16-bit metadata")
     if m8 is not None:
         if (tuple(m8.code_min.shape) != (B, H, P, d) or tuple(m8.lo.shape) != (B, H, P)
                 or not all(t.is_contiguous() for t in m8)):
@@ -416,8 +418,6 @@ def decode_attn_select(q, K, V, meta, top_k: int, scale: Optional[float] = None,
             m8.step.data_ptr(), int(top_k), out.data_ptr(), _dtype_code(out.dtype), sel_ptr,
             ws.data_ptr(), nbytes, _stream(q)), "dkv_decode_attn_select_meta8")
     elif hot is not None:
-        if m8 is not None:
-            raise ValueError("cross-step reuse takes 16-bit metadata")
         _check(lib().dkv_decode_attn_select_hot(
             ctypes.byref(p), q.data_ptr(), ctypes.byref(ks), ctypes.byref(vs), mn.data_ptr(),
             mx.data_ptr(), int(top_k), out.data_ptr(), _dtype_code(out.dtype), sel_ptr,

@@ -146,3 +146,5 @@ def test_hot_state_rejects_bad_use(dev, dkv):
     with pytest.raises(dkv.DkvError) as e:
         dkv.decode_attn_select(q, K, V, meta, w.top_k, hot=hot[:64], step=1)  # too small
     assert e.value.status == 6
+    with pytest.raises(ValueError, match="16-bit metadata"):
+        dkv.decode_attn_select(q, K, V, dkv.kv_meta8_build(meta), w.top_k, hot=hot, step=1)

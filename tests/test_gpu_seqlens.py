@@ -119,3 +119,42 @@ def test_seq_lens_all_full_equals_no_lens(dev, dkv):
     o1, s1 = dkv.decode_attn_select(q, K, V, meta, w.top_k, return_selected=True)
     o2, s2 = dkv.decode_attn_select(q, K, V, meta, w.top_k, return_selected=True, seq_lens=L)
     assert torch.equal(s1, s2) and torch.equal(o1, o2)
+
+
+def test_seq_lens_outside_the_cache_are_clamped(dev, dkv):
+    """A length below 1 attends one token and one above seq_len attends all of
+    them (the documented clamp into [1, seq_len]): every call gives bitwise the
+    results of the clamped lengths."""
+    w, _ = CASES[0]
+    raw, clamped = [0, -3, 10 ** 6, 3333], [1, 1, w.N, 3333]
+    q, K, V = make_inputs(w, seed=67)
+    Kn, Vn = _nan_past(K, clamped), _nan_past(V, clamped)
+    qd, Kd, Vd = q.to(dev), Kn.to(dev), Vn.to(dev)
+    Lr = torch.tensor(raw, dtype=torch.int32, device=dev)
+    Lc = torch.tensor(clamped, dtype=torch.int32, device=dev)
+    pages = [(n + w.S - 1) // w.S for n in clamped]
+
+    def written(m):  # metadata rows the lengths write, per sequence
+        return [m[b, :, :pages[b]] for b in range(w.B)]
+
+    def same_rows(a, b):
+        return all(torch.equal(x, y) for x, y in zip(written(a), written(b)))
+
+    mr, mc = dkv.kv_meta_build(Kd, seq_lens=Lr), dkv.kv_meta_build(Kd, seq_lens=Lc)
+    assert same_rows(mr[0], mc[0]) and same_rows(mr[1], mc[1])
+    dkv.kv_meta_append(Kd, mr, seq_lens=Lr)
+    dkv.kv_meta_append(Kd, mc, seq_lens=Lc)
+    assert same_rows(mr[0], mc[0]) and same_rows(mr[1], mc[1])
+    r8, c8 = dkv.kv_meta8_build(mc, seq_lens=Lr), dkv.kv_meta8_build(mc, seq_lens=Lc)
+    for x, y in zip(r8, c8):
+        assert same_rows(x, y)
+    assert torch.equal(dkv.decode_attn_full(qd, Kd, Vd, seq_lens=Lr),
+                       dkv.decode_attn_full(qd, Kd, Vd, seq_lens=Lc))
+    for meta in (mc, c8):
+        for group in (False, True):
+            o1, s1 = dkv.decode_attn_select(qd, Kd, Vd, meta, w.top_k, return_selected=True,
+                                            group_select=group, seq_lens=Lr)
+            o2, s2 = dkv.decode_attn_select(qd, Kd, Vd, meta, w.top_k, return_selected=True,
+                                            group_select=group, seq_lens=Lc)
+            assert torch.equal(s1, s2) and torch.equal(o1, o2)
+            assert torch.isfinite(o1).all()
