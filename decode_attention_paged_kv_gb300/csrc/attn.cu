@@ -927,11 +927,12 @@ __global__ void __launch_bounds__(kAttnThreads, MHA ? 3 : (D == 64 ? kAttnCtasPe
         const bool on1 = (hmask >> (sl ? ((g + 8) >> (4 - sl)) : 0)) & 1u;
         const float s0 = (t4 == 0 && on0 && tk0 < Nb) ? sc[0][0] * a.scale_log2 : -INFINITY;
         const float s1 = (t4 == 0 && on1 && tk1 < Nb) ? sc[0][2] * a.scale_log2 : -INFINITY;
-        float pmax = fmaxf(s0, s1);
-        pmax = fmaxf(pmax, __shfl_xor_sync(0xffffffffu, pmax, 4));
-        pmax = fmaxf(pmax, __shfl_xor_sync(0xffffffffu, pmax, 8));
-        pmax = fmaxf(pmax, __shfl_xor_sync(0xffffffffu, pmax, 16));
-        pmax = __shfl_sync(0xffffffffu, pmax, 0);  // warp-uniform
+        // the page's largest score, warp-uniform, by one integer max over
+        // order-preserving keys (a float's bits, the magnitude bits flipped
+        // when negative; the map is its own inverse)
+        const int kb = __float_as_int(fmaxf(s0, s1));
+        const int km = __reduce_max_sync(0xffffffffu, kb >= 0 ? kb : kb ^ 0x7fffffff);
+        const float pmax = __int_as_float(km >= 0 ? km : km ^ 0x7fffffff);
         const float m_new = fmaxf(m_run, pmax);
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
         const float alpha = exp2f(m_run - m_use);
