@@ -422,10 +422,16 @@ static dkv_status run_attention(const dkv_params* p, const dkv::AttnArgs& a, boo
   const int sms = current_sm_count();
   if (sms <= 0) return DKV_ERR_CUDA;
   const bool q4 = a.k4.codes != nullptr;
+  dkv::AttnArgs ao = a;
+  ao.out = out;
+  ao.out_dtype = out_code(out_dtype);
+  ao.o_sb = p->o_stride_b;
+  ao.o_sh = p->o_stride_h;
   dkv_status st = cuda_status(
-      q4 ? dkv::launch_attn_q4(p->head_dim, sparse, a, sms, s)
-         : dkv::launch_attn(p->head_dim, f16, sparse, a, mk, mv, sms, s));
+      q4 ? dkv::launch_attn_q4(p->head_dim, sparse, ao, sms, s)
+         : dkv::launch_attn(p->head_dim, f16, sparse, ao, mk, mv, sms, s));
   if (st != DKV_OK) return st;
+  if (q4 && sparse && a.n_chunks == 1) return DKV_OK;  // the attention wrote out itself
   dkv::MergeArgs m{};
   m.part_ml = a.part_ml;
   m.part_o = a.part_o;

@@ -31,9 +31,15 @@
 //     their (max, sum, o) to warp 0 through shared memory, which merges them
 //     with its own and writes the item's partial.
 // merge_small_kernel (units of up to 32 chunks) or merge_kernel then combines
-// the chunks of every (b, h) in a fixed order and writes out.  Its structure, like the chunking, depends only on (P, d), and
-// partials do not depend on which CTA computed them, so results are
-// deterministic and one kv head at a time gives bitwise the all-heads result.
+// the chunks of every (b, h) in a fixed order and writes out.  Its structure,
+// like the chunking, depends only on (P, d), and partials do not depend on
+// which CTA computed them, so results are deterministic and one kv head at a
+// time gives bitwise the all-heads result.  The sparse 4-bit path with one
+// chunk per unit (unions of up to 32 pages at d = 128, 64 at d = 64) skips
+// the merge: warp 0 writes O / L itself, the value the merge would write
+// (its weight is 2^0 = 1).  The other instantiations keep the partials only:
+// the extra epilogue costs them more in registers and code than the merge's
+// round trip (4% on the 4-bit exact kernel, 3% on the dense sparse one).
 // The last CTA to stop fetching work resets the work counter.
 // Every mbarrier wait is bounded; on expiry the kernel records a timeout in
 // the status word, stops issuing, drains the copies it issued and exits.
@@ -1078,7 +1084,9 @@ __global__ void __launch_bounds__(kAttnThreads, MHA ? 3 : (D == 64 ? kAttnCtasPe
           L += f[w] * r[D + 1];
         }
         const int64_t pi = (static_cast<int64_t>(b) * a.Hq + kvh * a.G) * a.n_chunks + chunk;
+        const bool whole = Q4 && SPARSE && a.n_chunks == 1;  // out = O / L
         float* po = a.part_o + pi * D;
+        const int64_t oo = b * a.o_sb + kvh * a.G * a.o_sh;
         if (t4 == 0) {
 #pragma unroll
           for (int cn = 0; cn < kAccTiles; ++cn) {
@@ -1088,11 +1096,14 @@ __global__ void __launch_bounds__(kAttnThreads, MHA ? 3 : (D == 64 ? kAttnCtasPe
               float O = f[0] * (acc[cn][2 * e] + acc[cn][2 * e + 1]);
 #pragma unroll
               for (int w = 1; w < kConsumerWarps; ++w) O += f[w] * mrg[(w - 1) * C::kMergeRow + c];
-              po[c] = O;
+              if (whole)
+                store_out(a.out, a.out_dtype, oo + c, O / L);
+              else
+                po[c] = O;
             }
           }
         }
-        if (lane == 0) {
+        if (lane == 0 && !whole) {
           a.part_ml[2 * pi] = M;
           a.part_ml[2 * pi + 1] = L;
         }
@@ -1132,7 +1143,9 @@ __global__ void __launch_bounds__(kAttnThreads, MHA ? 3 : (D == 64 ? kAttnCtasPe
         L += f[w] * r[D + 1];
       }
       const int64_t pi = (static_cast<int64_t>(b) * a.Hq + kvh * a.G + g) * a.n_chunks + chunk;
+      const bool whole = Q4 && SPARSE && a.n_chunks == 1;  // out = O / L
       float* po = a.part_o + pi * D;
+      const int64_t oo = b * a.o_sb + (kvh * a.G + g) * a.o_sh;
 #pragma unroll
       for (int cn = 0; cn < D / 8; ++cn) {
 #pragma unroll
@@ -1142,10 +1155,13 @@ __global__ void __launch_bounds__(kAttnThreads, MHA ? 3 : (D == 64 ? kAttnCtasPe
 #pragma unroll
           for (int w = 1; w < kConsumerWarps; ++w)
             O += f[w] * mrg[((w - 1) * 8 + g) * C::kMergeRow + c];
-          po[c] = O;
+          if (whole)
+            store_out(a.out, a.out_dtype, oo + c, O / L);
+          else
+            po[c] = O;
         }
       }
-      if (t4 == 0) {
+      if (t4 == 0 && !whole) {
         a.part_ml[2 * pi] = M;
         a.part_ml[2 * pi + 1] = L;
       }

@@ -85,6 +85,11 @@ struct AttnArgs {
   int n_items;                 // B * Hkv * n_chunks work items
   float* part_ml;              // [B, Hq, n_chunks, 2]  (max in log2 units, sum)
   float* part_o;               // [B, Hq, n_chunks, d]  unnormalised
+  // sparse 4-bit path with n_chunks == 1: each item is its rows' whole result,
+  // written normalised to out (strides in elements), no partials, no merge
+  void* out;
+  int out_dtype;               // 0 bf16, 1 fp16, 2 fp32
+  int64_t o_sb, o_sh;
   uint32_t* work_counter;      // next work item; zero between calls
   uint32_t* exit_counter;      // CTAs done fetching; zero between calls
   // sparse path: per (batch, kv head) the ascending union of the group's

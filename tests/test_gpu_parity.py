@@ -325,6 +325,22 @@ Q4_CASES = [
 ]
 
 
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("w", [Q4_CASES[0], Q4_CASES[1], Q4_CASES[4]],
+                         ids=["one-chunk-mha", "one-chunk-gqa-d64", "merged-chunks"])
+def test_q4_select_half_outputs_are_the_rounded_fp32_outputs(w, out_dtype, dev, dkv):
+    # A unit whose union fits one work item writes out from the attention
+    # kernel itself; longer unions go through the merge.  Either way a 16-bit
+    # output is the fp32 result rounded to nearest.
+    q, K, V = make_inputs(w, seed=203)
+    K4, V4 = dkv.kv_quant4(K.to(dev)), dkv.kv_quant4(V.to(dev))
+    qd = q.to(dev)
+    meta = dkv.kv_meta_build(K4)
+    o32 = dkv.decode_attn_select(qd, K4, V4, meta, w.top_k)
+    o16 = dkv.decode_attn_select(qd, K4, V4, meta, w.top_k, out_dtype=out_dtype)
+    assert o16.dtype == out_dtype and torch.equal(o16, o32.to(out_dtype))
+
+
 @pytest.mark.parametrize("w", Q4_CASES, ids=lambda w: w.name)
 def test_q4_attention_matches_oracle(w, dev, dkv):
     # Attention over 4-bit caches: the kernels dequantise in registers to the
