@@ -661,7 +661,15 @@ static dkv_status select_impl(const dkv_params* p, const void* q, const dkv_kv* 
     ta.lens = p->seq_lens;
     ta.N = p->seq_len;
     ta.S = p->page_size;
+    // one query head per kv head at 16-token pages: the rows are the unions
+    const bool row_unions = G == 1 && p->page_size == dkv::kPage;
+    if (row_unions) {
+      ta.union_list = ulist;
+      ta.union_count = ucount;
+      ta.union_stride = L.union_stride;
+    }
     if ((st = cuda_status(dkv::launch_topk(ta, s))) != DKV_OK) return st;
+    if (row_unions) return run_attention(p, a, true, f16, mk, mv, out, out_dtype, s);
     dkv::UnionArgs ua{};
     ua.bitmaps = ta.bitmaps;
     ua.Hq = p->num_q_heads;

@@ -191,6 +191,11 @@ struct TopkArgs {
   int32_t* selected;           // [rows, kk]
   uint32_t* bitmaps;           // [rows, W32]
   int W32;
+  // One query head per kv head at 16-token pages: the units' union lists,
+  // written here from the rows (nullptr: the union kernel builds them)
+  int2* union_list;            // [rows, union_stride]
+  int* union_count;            // [rows]
+  int union_stride;
 };
 
 struct UnionArgs {

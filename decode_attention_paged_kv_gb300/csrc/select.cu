@@ -858,6 +858,18 @@ __global__ void __launch_bounds__(kScore8Warps * 32) score8_kernel(const Score8A
   }
 }
 
+// One query head per kv head and 16-token pages: a unit's union is its one
+// row, ascending, each page with mask 1, so the top-K kernel writes it (row
+// b * Hq + h is unit b * Hkv + h) and the union kernel is not launched.  The
+// row's kkb entries are read back from L2 after the barrier that ordered
+// their writes; threads t, t + nt, ... of the row take them.
+__device__ __forceinline__ void write_row_union(const int32_t* sel_row, int kkb, int row,
+                                                const TopkArgs& a, int t, int nt) {
+  int2* ul = a.union_list + static_cast<int64_t>(row) * a.union_stride;
+  for (int i = t; i < kkb; i += nt) ul[i] = make_int2(__ldcg(sel_row + i), 1);
+  if (t == 0) a.union_count[row] = kkb;
+}
+
 template <bool SMEM>
 __global__ void __launch_bounds__(kSelMaxThreads) topk_kernel(const TopkArgs a) {
   extern __shared__ uint32_t s_keys[];
@@ -954,10 +966,12 @@ __global__ void __launch_bounds__(kSelMaxThreads) topk_kernel(const TopkArgs a) 
   if (!found) block_radix_select(key, Pb, kkb, sc, prefix, mask, need);
   int32_t* sel_row = a.selected + static_cast<int64_t>(row) * a.kk;
   if (!found) block_emit_counts(key, Pb, prefix, mask, sc);
-  block_emit(key, load4, Pb, prefix, mask, need, sel_row, bits, sc);
+  block_emit(key, load4, Pb, prefix, mask, need, sel_row, bits, sc);  // ends in a block barrier
   for (int w = static_cast<int>(ceil_div(Pb, 32)) + threadIdx.x; w < a.W32; w += sel_threads())
     bits[w] = 0u;
   for (int i = kkb + threadIdx.x; i < a.kk; i += sel_threads()) sel_row[i] = -1;
+  if (a.union_list != nullptr)
+    write_row_union(sel_row, kkb, row, a, static_cast<int>(threadIdx.x), sel_threads());
 }
 
 // One warp per (b, h) row of at most kUnitMaxP keys: the row's scores (summed
@@ -1000,6 +1014,10 @@ __global__ void __launch_bounds__(kTopkWarpRows * 32) topk_warp_kernel(const Top
   warp_emit_row(bm, W, sel_row, bits);
   for (int w = W + lane; w < a.W32; w += 32) bits[w] = 0u;
   for (int i = kkb + lane; i < a.kk; i += 32) sel_row[i] = -1;
+  if (a.union_list != nullptr) {
+    __syncwarp();  // the row's entries, written by the warp's lanes
+    write_row_union(sel_row, kkb, row, a, lane, 32);
+  }
 }
 
 __global__ void __launch_bounds__(kSelMaxThreads) union_kernel(const UnionArgs a) {

@@ -61,6 +61,10 @@ CASES = [
     # a union of 2400 pages (75 chunks per unit) chosen by the separate
     # selection kernels
     Workload("select-merge-kernel", B=1, Hq=4, Hkv=1, d=128, N=40000, top_k=600, kind="hot"),
+    # one head per kv head past the per-unit kernel's 2048 pages: the block
+    # top-K writes the union lists itself (as the warp top-K does for the
+    # shorter one-head cases above)
+    Workload("block-topk-mha", B=2, Hq=2, Hkv=2, d=64, N=40000, top_k=100, kind="offset"),
 ]
 
 
