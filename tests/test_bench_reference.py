@@ -1,0 +1,30 @@
+"""The bench's reference arm (the oracle on the host cores) keeps the line the
+driver reads: one JSON object with the arm's metric, unit and workload, a
+cpu_baseline describing the run and an e2e entry with no host copies.  It
+needs no GPU, so it runs here on a short sample."""
+
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_reference_arm_prints_one_contract_line():
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1",
+                        "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 1
+    assert d["steps"] == 1 and d["warmup"] == 3
+    assert d["unit"] == "queries/s" and d["higher_is_better"] is True
+    assert d["config"]["workload"] == "llama3-8b-gqa-b16-n32k"
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
+    assert cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
