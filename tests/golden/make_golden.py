@@ -3,7 +3,8 @@
 The pages print no worked numeric example of the kernel, so these fixtures are
 regression pins of the oracle itself (page metadata, bound scores, top-K and
 attention; metadata at page sizes 4, 8 and 32 with group scores; the 4-bit
-format; the 8-bit metadata and its scores): small inputs (stored verbatim as bit
+format; the 8-bit metadata and its scores; token-level top-K with exact ties):
+small inputs (stored verbatim as bit
 patterns, drawn from numpy's PCG64 so they are platform independent) together
 with the oracle's outputs.  ``tests/test_golden.py`` recomputes them on
 whatever machine runs the suite (x86 here, Arm on the GPU host) and requires the
@@ -121,9 +122,36 @@ def case_pages_small():
     return out
 
 
+def case_tokens_small():
+    # token-level top-K: single-token pages (m = M = k, so r = q . k), fp16,
+    # two query heads per kv head; the K rows repeat every 8 tokens, so whole
+    # score classes tie and the K-th place falls inside one (ties to the lower
+    # token index)
+    rng = np.random.default_rng(1717)
+    B, Hq, Hkv, d, N, K = 1, 4, 2, 64, 53, 9
+    f16 = lambda x: np.asarray(x, np.float64).astype(np.float16).view(np.uint16)  # noqa
+    q = f16(rng.standard_normal((B, Hq, d)))
+    base = rng.standard_normal((B, Hkv, 8, d))
+    Kc = f16(np.concatenate([base] * 7, axis=2)[:, :, :N])
+    Vc = f16(rng.standard_normal((B, Hkv, N, d)))
+    mn, mx = oracle.meta(Kc, 1, 1)
+    r = oracle.scores(q, mn, mx, 1)
+    sel = oracle.topk(r, K)
+    scale = 1.0 / math.sqrt(d)
+    out = oracle.attention(q, Kc, Vc, 1, scale, 1, sel=sel)
+    return {
+        "shape": dict(B=B, Hq=Hq, Hkv=Hkv, d=d, N=N, K=K, scale=scale, dtype="fp16"),
+        "q": q.ravel().tolist(), "K": Kc.ravel().tolist(), "V": Vc.ravel().tolist(),
+        "scores": [float.hex(float(v)) for v in r.ravel()],
+        "selected": sel.ravel().tolist(),
+        "out": [float.hex(float(v)) for v in out.ravel()],
+    }
+
+
 def main():
     for name, fn in [("sparse_small", case_sparse_small), ("quant4", case_quant4),
-                     ("meta8_small", case_meta8_small), ("pages_small", case_pages_small)]:
+                     ("meta8_small", case_meta8_small), ("pages_small", case_pages_small),
+                     ("tokens_small", case_tokens_small)]:
         with open(os.path.join(HERE, f"{name}.json"), "w") as f:
             json.dump(fn(), f, separators=(",", ":"))
             f.write("\n")

@@ -89,3 +89,22 @@ def test_pages_fixture():
         assert mn.shape[2] == (s["N"] + S - 1) // S
         gs = oracle.group_scores(q, mn, mx, 0)
         assert np.array_equal(gs.ravel(), _hexarr(c["group_scores"])), S
+
+
+def test_tokens_fixture():
+    # single-token pages: scores q . k, the top K with ties to the lower token
+    # index (the K-th place falls inside a class of equal scores), attention
+    # over the chosen tokens
+    g = _load("tokens_small.json")
+    s = g["shape"]
+    q = np.array(g["q"], np.uint16).reshape(s["B"], s["Hq"], s["d"])
+    Kc = np.array(g["K"], np.uint16).reshape(s["B"], s["Hkv"], s["N"], s["d"])
+    Vc = np.array(g["V"], np.uint16).reshape(s["B"], s["Hkv"], s["N"], s["d"])
+    mn, mx = oracle.meta(Kc, 1, 1)
+    assert np.array_equal(mn, Kc) and np.array_equal(mx, Kc)
+    r = oracle.scores(q, mn, mx, 1)
+    assert np.array_equal(r.ravel(), _hexarr(g["scores"]))
+    sel = oracle.topk(r, s["K"])
+    assert sel.ravel().tolist() == g["selected"]
+    out = oracle.attention(q, Kc, Vc, 1, s["scale"], 1, sel=sel)
+    np.testing.assert_allclose(out.ravel(), _hexarr(g["out"]), rtol=1e-13, atol=0)
