@@ -192,6 +192,25 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def step_launches(w: Workload) -> int:
+    """The library's kernel launches in one step (meta build, exact, select) on
+    workload w, by the library's dispatch rules for these shapes: one metadata
+    kernel; the exact call's attention and merge; the select call's per-unit
+    selection kernel (selection pages of 16 tokens or more, 256 to 2048 of
+    them) or its score, top-K and union kernels (no union kernel with one
+    query head per kv head at 16-token pages: the top-K writes the unions),
+    then its attention and merge (no merge on a 4-bit cache whose unions fit
+    one work item)."""
+    P, P16, G = w.P, -(-w.N // 16), w.Hq // w.Hkv
+    kk = min(w.top_k, P)
+    select = 1 if (w.S >= 16 and 256 <= P <= 2048) else (2 + (0 if G == 1 and w.S == 16 else 1))
+    union_sel = min(G * kk, P)
+    union_max = min(union_sel * (w.S // 16) if w.S > 16 else union_sel, P16)
+    ppc = max(32 if w.d == 128 else 64, -(-union_max // 256))
+    merge = 0 if (w.q4 and -(-union_max // ppc) == 1) else 1
+    return 1 + 2 + select + 1 + merge
+
+
 def union_tokens(sel: torch.Tensor, w: Workload, S: int = 0) -> int:
     """Valid tokens of the unique pages (of S tokens, default the workload's)
     gathered per (batch, kv head)."""
@@ -372,7 +391,7 @@ def run_dkv(args, rank, world, local):
         "kernels_timing": {"kernels": "inside the timed region (back-to-back steps)",
                            "kernels_cold": COLD},
         "roofline": roofline,
-        "gpu_launches": args.steps * (1 + 2 + 4),
+        "gpu_launches": args.steps * step_launches(w),
         "clocks": clk.summary(),
     }
     return res, (q, K, V, w, widx, dev, stream, flush)
